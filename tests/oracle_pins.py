@@ -1,0 +1,346 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each ``pin_*`` takes an :class:`oracle.oracle.Oracle` and raises
+``AssertionError`` when the oracle disagrees with a closed form, a textbook
+special case, an invariance or brute force.  ``test_oracle_pins.py`` runs them
+against the real oracle; ``test_oracle_mutants.py`` runs them against builds of
+the oracle with a planted mistake and checks that every mistake is caught.
+
+The pages ("FlashSinkhorn", Methodologie 1-3; "CUDA-Optimized APML",
+Abstract) print no worked numeric example, so these pins replace one.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+
+import numpy as np
+from scipy.special import logsumexp
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _close(a, b, rtol, atol=0.0, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    lim = atol + rtol * max(np.max(np.abs(b)) if b.size else 0.0, 1e-300)
+    assert err <= lim, f"{what}: max|diff| {err:.3e} > {lim:.3e}"
+
+
+def _gauge(f, g, fr, gr):
+    """Remove the common constant shift (f + c, g - c) before comparing."""
+    c = 0.5 * (np.mean(f - fr) - np.mean(g - gr))
+    return f - c, g + c
+
+
+def pin_closed_form_single_point(orc):
+    """n = m = 1, a = b = 1: after any number of iterations f = |x-y|^2, g = 0,
+    cost = |x-y|^2 and grad = 2(x - y)."""
+    rng = _rng(1)
+    for d in (1, 3, 5):
+        x = rng.normal(size=(1, d))
+        y = rng.normal(size=(1, d))
+        c = float(np.sum((x - y) ** 2))
+        for eps, it in ((0.01, 1), (0.5, 4)):
+            f, g = orc.sinkhorn(x, y, [1.0], [1.0], [eps], [it])
+            _close(f, [c], 1e-12, what="f at n=1")
+            _close(g, [0.0], 0, atol=1e-12 * c, what="g at n=1")
+            out = orc.plan_apply(x, y, [1.0], [1.0], f, g, eps)
+            _close(out["cost"], c, 1e-12, what="cost at n=1")
+            _close(out["grad"], 2 * (x - y), 1e-12, what="grad at n=1")
+
+
+def two_point_plan(C, a, b, eps):
+    """Exact entropic plan of a 2 x 2 problem.
+
+    P = [[p, a1 - p], [b1 - p, a2 - b1 + p]] has the right marginals for any p,
+    and a Sinkhorn plan diag(u) K diag(v) satisfies
+    P11 P22 / (P12 P21) = K11 K22 / (K12 K21) = rho = exp(-(C11 + C22 - C12 - C21)/eps),
+    which is a quadratic in p with one root in the feasible interval.
+    """
+    a1, a2 = a
+    b1, _ = b
+    rho = np.exp(-(C[0, 0] + C[1, 1] - C[0, 1] - C[1, 0]) / eps)
+    A = 1.0 - rho
+    Bq = a2 - b1 + rho * (a1 + b1)
+    Cq = -rho * a1 * b1
+    lo, hi = max(0.0, b1 - a2), min(a1, b1)
+    if abs(A) < 1e-14:
+        roots = [-Cq / Bq]
+    else:
+        disc = np.sqrt(Bq * Bq - 4 * A * Cq)
+        # numerically stable pair of roots
+        q = -0.5 * (Bq + np.copysign(disc, Bq))
+        roots = [q / A, Cq / q]
+    p = [r for r in roots if lo - 1e-15 <= r <= hi + 1e-15]
+    assert len(p) >= 1, "no feasible root"
+    p = p[0]
+    return np.array([[p, a1 - p], [b1 - p, a2 - b1 + p]])
+
+
+def pin_two_point_closed_form(orc):
+    """2 x 2 problems with unequal weights converge to the closed-form plan."""
+    with open(os.path.join(GOLDEN, "two_point.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for case in cases:
+        X = np.array(case["X"])
+        Y = np.array(case["Y"])
+        a = np.array(case["a"])
+        b = np.array(case["b"])
+        eps = case["eps"]
+        f, g = orc.sinkhorn(X, Y, a, b, [eps], [case["iters"]])
+        out = orc.plan_apply(X, Y, a, b, f, g, eps)
+        P = np.array(case["P"])
+        _close(out["rowsum"], P.sum(1), 1e-10, what="2x2 row sums")
+        _close(out["cost"], case["cost"], 1e-10, what="2x2 cost")
+        _close(out["grad"], np.array(case["grad"]), 1e-9, what="2x2 grad")
+
+
+def pin_attention_form(orc):
+    """Propositie 1 ("FlashSinkhorn", Methodologie 1): with Q = sqrt2 X,
+    K = sqrt2 Y, g_hat = g - |y|^2, delta = eps log b, the f-half equals
+    |x_i|^2 - eps * LSE_j[(Q K^T + 1 (g_hat + delta)^T)/eps]; the g-half is the
+    mirror with f_hat = f - |x|^2 and gamma = eps log a.  Evaluated here in the
+    expanded (dot-product) form, against the oracle's direct form."""
+    rng = _rng(2)
+    n, m, d = 37, 29, 4
+    X = rng.normal(size=(n, d))
+    Y = rng.normal(size=(m, d)) + 0.3
+    a = rng.random(n) + 0.1
+    a /= a.sum()
+    b = rng.random(m) + 0.1
+    b /= b.sum()
+    g = rng.normal(size=m)
+    f = rng.normal(size=n)
+    for eps in (0.05, 1.0):
+        Q, K = np.sqrt(2) * X, np.sqrt(2) * Y
+        S = (Q @ K.T + (g - (Y * Y).sum(1) + eps * np.log(b))[None, :]) / eps
+        f_att = (X * X).sum(1) - eps * logsumexp(S, axis=1)
+        _close(orc.f_half(X, Y, b, g, eps), f_att, 1e-11, atol=1e-11, what="attention form, f-half")
+        S2 = (K @ Q.T + (f - (X * X).sum(1) + eps * np.log(a))[None, :]) / eps
+        g_att = (Y * Y).sum(1) - eps * logsumexp(S2, axis=1)
+        _close(orc.g_half(X, Y, a, f, eps), g_att, 1e-11, atol=1e-11, what="attention form, g-half")
+
+
+def _problem(seed, n, m, d, scale=1.0):
+    rng = _rng(seed)
+    X = scale * rng.normal(size=(n, d))
+    Y = scale * rng.normal(size=(m, d)) + 0.2
+    a = rng.random(n) + 0.2
+    a /= a.sum()
+    b = rng.random(m) + 0.2
+    b /= b.sum()
+    return X, Y, a, b
+
+
+def pin_marginals_and_duality(orc):
+    """At convergence the plan has both marginals, and the dual objective
+    <a,f> + <b,g> equals <C,P> + eps KL(P || a x b)."""
+    X, Y, a, b = _problem(3, 23, 17, 2)
+    eps = 0.2
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [1500])
+    out = orc.plan_apply(X, Y, a, b, f, g, eps)
+    assert np.abs(out["rowsum"] - a).sum() < 1e-10, "row marginal not reached"
+    assert np.abs(out["colsum"] - b).sum() < 1e-12, "column marginal not exact after a g-half"
+    dual, primal = orc.objectives(X, Y, a, b, f, g, eps)
+    _close(dual, primal, 1e-9, what="duality")
+
+
+def pin_brute_force_assignment(orc):
+    """Uniform clouds with n = m <= 6: 0 <= <C,P_eps> - OT_0 <= eps log n, with
+    OT_0 the best permutation found by enumeration; at small eps the row argmax
+    of the plan is that permutation."""
+    rng = _rng(4)
+    for n in (3, 5, 6):
+        for trial in range(3):
+            X = rng.random((n, 2))
+            Y = rng.random((n, 2))
+            C = ((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1)
+            costs = sorted((np.mean(C[np.arange(n), list(p)]), p) for p in itertools.permutations(range(n)))
+            ot0, best = costs[0]
+            gap = costs[1][0] - ot0
+            for eps in (0.05, 0.01):
+                f, g = orc.sinkhorn(X, Y, None, None, [eps], [3000])
+                out = orc.plan_apply(X, Y, None, None, f, g, eps)
+                slack = np.abs(out["rowsum"] - 1.0 / n).sum() * C.max()
+                assert out["cost"] >= ot0 - slack - 1e-12, "entropic cost below the exact OT cost"
+                assert out["cost"] <= ot0 + eps * np.log(n) + slack + 1e-12, "entropic cost above OT_0 + eps log n"
+            if gap > 0.02:
+                epss = [0.1, 0.03, 0.01, 0.003, 1e-3]
+                f, g = orc.sinkhorn(X, Y, None, None, epss, [400] * len(epss))
+                eps = epss[-1]
+                a = np.full(n, 1.0 / n)
+                s = (f[:, None] + g[None, :] - C) / eps
+                assert tuple(np.argmax(s, axis=1)) == tuple(best), "argmax of the plan is not the optimal permutation"
+
+
+def pin_sorted_matching_1d(orc):
+    """d = 1, uniform weights: the exact OT cost is the sorted (monotone)
+    matching; the entropic cost lies within eps log n above it."""
+    rng = _rng(5)
+    n = 96
+    x = rng.random(n)
+    y = rng.random(n) * 0.8 + 0.3
+    ot0 = np.mean((np.sort(x) - np.sort(y)) ** 2)
+    for eps in (0.02, 0.005):
+        f, g = orc.sinkhorn(x[:, None], y[:, None], None, None, [eps * 4, eps * 2, eps], [200, 200, 600])
+        out = orc.plan_apply(x[:, None], y[:, None], None, None, f, g, eps)
+        slack = np.abs(out["rowsum"] - 1.0 / n).sum()
+        assert ot0 - slack - 1e-12 <= out["cost"] <= ot0 + eps * np.log(n) + slack + 1e-12, \
+            f"1-D sorted matching bound violated: {out['cost']} vs {ot0}"
+
+
+def pin_large_eps(orc):
+    """eps -> infinity: P -> a x b, so cost -> sum_i a_i|x_i|^2 + sum_j b_j|y_j|^2
+    - 2 xbar_a . ybar_b and grad_i -> 2 a_i (x_i - ybar_b), errors O(Var C / eps)."""
+    X, Y, a, b = _problem(6, 31, 27, 3)
+    eps = 1e6
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [3])
+    out = orc.plan_apply(X, Y, a, b, f, g, eps)
+    xb = a @ X
+    yb = b @ Y
+    c_inf = a @ (X * X).sum(1) + b @ (Y * Y).sum(1) - 2 * xb @ yb
+    _close(out["cost"], c_inf, 1e-4, what="large-eps cost")
+    _close(out["grad"], 2 * a[:, None] * (X - yb[None, :]), 1e-4, what="large-eps grad")
+
+
+def pin_invariances(orc):
+    """Translation leaves f, g, cost unchanged; rotation leaves them unchanged
+    and rotates the gradient; shifting the warm start by (c, -c) shifts the
+    output by (c, -c); swapping the clouds swaps f and g at convergence."""
+    X, Y, a, b = _problem(7, 19, 23, 3)
+    eps, it = 0.1, 30
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [it])
+    ref = orc.plan_apply(X, Y, a, b, f, g, eps)
+    t = np.array([0.7, -1.3, 2.1])
+    f2, g2 = orc.sinkhorn(X + t, Y + t, a, b, [eps], [it])
+    _close(f2, f, 1e-11, atol=1e-11, what="translation f")
+    _close(g2, g, 1e-11, atol=1e-11, what="translation g")
+    _close(orc.plan_apply(X + t, Y + t, a, b, f2, g2, eps)["cost"], ref["cost"], 1e-11, what="translation cost")
+    th = 0.77
+    R = np.array([[np.cos(th), -np.sin(th), 0], [np.sin(th), np.cos(th), 0], [0, 0, 1.0]])
+    f3, g3 = orc.sinkhorn(X @ R.T, Y @ R.T, a, b, [eps], [it])
+    out3 = orc.plan_apply(X @ R.T, Y @ R.T, a, b, f3, g3, eps)
+    _close(out3["cost"], ref["cost"], 1e-11, what="rotation cost")
+    _close(out3["grad"], ref["grad"] @ R.T, 1e-10, what="rotation grad")
+    # shift invariance through the warm start
+    f0, g0 = orc.sinkhorn(X, Y, a, b, [eps], [3])
+    c = 0.37
+    fa, ga = orc.sinkhorn(X, Y, a, b, [eps], [5], f0=f0, g0=g0)
+    fb, gb = orc.sinkhorn(X, Y, a, b, [eps], [5], f0=f0 + c, g0=g0 - c)
+    _close(fb, fa + c, 1e-12, atol=1e-12, what="shift f")
+    _close(gb, ga - c, 1e-12, atol=1e-12, what="shift g")
+    # swap at convergence
+    fc, gc = orc.sinkhorn(X, Y, a, b, [eps], [2000])
+    fs, gs = orc.sinkhorn(Y, X, b, a, [eps], [2000])
+    gs_f, fs_g = _gauge(gs, fs, fc, gc)
+    _close(gs_f, fc, 1e-9, atol=1e-9, what="swap f")
+    _close(fs_g, gc, 1e-9, atol=1e-9, what="swap g")
+
+
+def pin_dual_finite_differences(orc):
+    """At convergence the gradient equals finite differences of the dual
+    objective <a,f> + <b,g> with respect to X (envelope theorem)."""
+    X, Y, a, b = _problem(8, 6, 5, 2, scale=0.6)
+    eps = 0.3
+
+    def obj(Xp):
+        f, g = orc.sinkhorn(Xp, Y, a, b, [eps], [3000])
+        return a @ f + b @ g
+
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [3000])
+    grad = orc.plan_apply(X, Y, a, b, f, g, eps)["grad"]
+    h = 1e-5
+    fd = np.zeros_like(X)
+    for i in range(X.shape[0]):
+        for k in range(X.shape[1]):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[i, k] += h
+            Xm[i, k] -= h
+            fd[i, k] = (obj(Xp) - obj(Xm)) / (2 * h)
+    _close(grad, fd, 1e-6, atol=1e-9, what="finite differences of the dual")
+
+
+def pin_marginal_error_shortcut(orc):
+    """Row marginal error by definition, sum_i |sum_j P_ij - a_i|, equals the
+    shortcut sum_i a_i |exp((f_i - f'_i)/eps) - 1| with f' the next f-half."""
+    X, Y, a, b = _problem(9, 33, 21, 3)
+    eps = 0.15
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [4])
+    fnew = orc.f_half(X, Y, b, g, eps)
+    short = np.sum(a * np.abs(np.exp((f - fnew) / eps) - 1.0))
+    _close(orc.marginal_err(X, Y, a, b, f, g, eps), short, 1e-10, what="marginal error shortcut")
+
+
+def pin_coo_limits(orc):
+    """tau = 0 keeps every pair; tau = 1 keeps exactly the row and column
+    argmax pairs; tau -> 0 takes the support gradient to the dense gradient,
+    with |difference| bounded by 2 (dropped mass) max|x_i - y_j| per row."""
+    X, Y, a, b = _problem(10, 25, 18, 3)
+    eps = 0.05
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [800])
+    full = orc.coo(X, Y, a, b, f, g, eps, 0.0, 3)
+    assert len(full["rows"]) == 25 * 18, "tau = 0 must keep every pair"
+    C = ((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1)
+    s_row = (g[None, :] - C) / eps + np.log(b)[None, :]
+    s_col = (f[:, None] - C) / eps + np.log(a)[:, None]
+    want = set(zip(range(25), np.argmax(s_row, axis=1))) | set(zip(np.argmax(s_col, axis=0), range(18)))
+    one = orc.coo(X, Y, a, b, f, g, eps, 1.0, 3)
+    got = set(zip(one["rows"].tolist(), one["cols"].tolist()))
+    assert got == {(int(i), int(j)) for i, j in want}, "tau = 1 must keep the argmax pairs only"
+    rows_only = orc.coo(X, Y, a, b, f, g, eps, 1.0, 1)
+    assert sorted(rows_only["rows"].tolist()) == list(range(25)), "row test keeps one argmax per row"
+    dense = orc.plan_apply(X, Y, a, b, f, g, eps)
+    gs_full = orc.grad_support(X, Y, full["rows"], full["cols"], full["vals"])
+    # on the full support 2 sum_j P_ij (x_i - y_j) = 2 (r_i x_i - sum_j P_ij y_j),
+    # which is the dense gradient plus 2 (r_i - a_i) x_i
+    want_full = dense["grad"] + 2 * (dense["rowsum"] - a)[:, None] * X
+    _close(gs_full, want_full, 1e-10, atol=1e-14, what="full-support gradient")
+    for tau in (1e-3, 1e-8):
+        sp = orc.coo(X, Y, a, b, f, g, eps, tau, 3)
+        gs = orc.grad_support(X, Y, sp["rows"], sp["cols"], sp["vals"])
+        kept = np.zeros(25)
+        np.add.at(kept, sp["rows"], sp["vals"])
+        dropped = dense["rowsum"] - kept
+        bound = 2 * dropped * np.sqrt(C.max()) + 1e-12
+        assert np.all(np.linalg.norm(gs - gs_full, axis=1) <= bound + 1e-12), "support gradient bound"
+
+
+def pin_anneal_schedule(orc):
+    """eps_k = max(1e-3, 0.9^k): 66 geometric stages from 1.0 down to 0.9^65,
+    then one clamped stage at 1e-3 (67 in all).  The annealed solve equals a
+    replay of its own realised per-stage iteration counts, and reports the
+    marginal error of the returned iterate."""
+    st = orc.anneal_stages(1.0, 0.9, 1e-3)
+    assert len(st) == 67 and st[0] == 1.0 and st[-1] == 1e-3, "annealing stage list"
+    _close(st[:-1], 0.9 ** np.arange(66), 1e-13, what="geometric stages")
+    X, Y, a, b = _problem(11, 21, 16, 3)
+    out = orc.sinkhorn_anneal(X, Y, a, b, 1.0, 0.5, 0.1, 5, 1e-8, 3000)
+    eps_list = orc.anneal_stages(1.0, 0.5, 0.1)[: out["stages_done"]]
+    f, g = orc.sinkhorn(X, Y, a, b, eps_list, out["stage_iters"])
+    assert np.array_equal(f, out["f"]) and np.array_equal(g, out["g"]), "replay differs"
+    assert out["converged"] and out["err"] < 1e-8
+    _close(orc.marginal_err(X, Y, a, b, f, g, eps_list[-1]), out["err"], 1e-12, what="reported err")
+    assert out["iters_done"] == int(np.sum(out["stage_iters"]))
+
+
+ALL_PINS = [
+    pin_closed_form_single_point,
+    pin_two_point_closed_form,
+    pin_attention_form,
+    pin_marginals_and_duality,
+    pin_brute_force_assignment,
+    pin_sorted_matching_1d,
+    pin_large_eps,
+    pin_invariances,
+    pin_dual_finite_differences,
+    pin_marginal_error_shortcut,
+    pin_coo_limits,
+    pin_anneal_schedule,
+]
