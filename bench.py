@@ -1,0 +1,337 @@
+#!/usr/bin/env python
+"""Throughput of the fused log-domain Sinkhorn path on one GB300 (or N, weak scaling).
+
+Workload (per GPU): B=1, n=m=70000, d=64, X ~ N(0, I), Y ~ N(mu, I),
+mu ~ N(0, 0.25 I), a, b = softmax of N(0,1) logits, eps = 0.1, 100 fixed
+iterations, then cost + gradient wrt X.  One step = one pass of the whole
+path over that input: preprocessing, 100 iterations (200 fused half-steps),
+the marginal error of the result, and plan application (cost, gradient).
+
+Metric: Sinkhorn pair-evaluations per second, 2 B n m iterations / step time
+(one pair-evaluation = one score + exp of one (i, j) in one half-step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on this machine's host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import shutil
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sinkhorn_point_cloud_gb300 import datagen  # noqa: E402
+
+WORKLOAD_ID = 4
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+METRIC = "Sinkhorn pair-evaluations/s (n=m=70000, d=64)"
+UNIT = "Gpair-evals/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+# ---- clocks ---------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, index: int, out_path: str | None = None):
+        self.index = index
+        self.proc = None
+        self.path = out_path
+
+    def __enter__(self):
+        if shutil.which("nvidia-smi"):
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        return self
+
+    def __exit__(self, *exc):
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.text, _ = self.proc.communicate()
+            if self.path:
+                with open(self.path, "w") as fh:
+                    fh.write(self.text)
+        return False
+
+    def summary(self):
+        return parse_clocks(getattr(self, "text", ""))
+
+
+def parse_clocks(text: str):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for row in csv.reader(io.StringIO(text)):
+        if len(row) < 9:
+            continue
+        try:
+            sm.append(float(row[1]))
+            mx.append(float(row[2]))
+        except ValueError:
+            continue
+        for nm, v in zip(names, row[5:9]):
+            if v.strip().lower() == "active":
+                reasons.add(nm)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+# ---- distributed helpers ------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- reference arm: the fp64 oracle on host cores -------------------------------
+def oracle_rate(target_s: float, X, Y, b, eps):
+    """Time the oracle's f-half on a sample of rows (all m columns) for about
+    target_s seconds; returns (pair-evals/s, rows, seconds, threads)."""
+    from oracle import oracle as O
+    orc = O.get()
+    m = Y.shape[0]
+    g = np.zeros(m)
+    rows = min(X.shape[0], 2 * orc.num_threads)
+    t0 = time.perf_counter()
+    orc.f_half(X[:rows], Y, b, g, eps)
+    t = max(time.perf_counter() - t0, 1e-3)
+    rows = int(max(orc.num_threads, min(X.shape[0], rows * target_s / t)))
+    t0 = time.perf_counter()
+    orc.f_half(X[:rows], Y, b, g, eps)
+    t = time.perf_counter() - t0
+    return rows * m / t, rows, t, orc.num_threads
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    w = datagen.WORKLOADS[WORKLOAD_ID]
+    X, Y, a, b = datagen.make_batch(WORKLOAD_ID, B=1)
+    rates = []
+    for _ in range(args.warmup):
+        oracle_rate(0.5, X[0], Y[0], b[0], w["eps"])
+    sample = None
+    for _ in range(args.steps):
+        r, rows, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], w["eps"])
+        rates.append(r)
+        sample = f"f-half of {rows} rows x {w['m']} columns (d={w['d']}), {t:.1f} s"
+    value = float(np.median(rates)) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w["name"], "B": 1, "n": w["n"], "m": w["m"], "d": w["d"], "eps": w["eps"],
+                       "iters": w["iters"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- GPU arm -------------------------------------------------------------------
+def run_gpu(args, ws, rank, local):
+    import torch
+    import sinkhorn_point_cloud_gb300 as sot
+    from sinkhorn_point_cloud_gb300 import build
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    w = datagen.WORKLOADS[WORKLOAD_ID]
+    B, n, m, d, eps, iters = 1, w["n"], w["m"], w["d"], w["eps"], w["iters"]
+    if args.n:
+        n = m = args.n
+    if args.iters:
+        iters = args.iters
+    # weak scaling: every rank solves its own problem (seeded by rank)
+    X, Y, a, b = datagen.make_batch(WORKLOAD_ID, B=B, n=n, m=m, clouds=[rank])
+    hX, hY, ha, hb = (torch.from_numpy(v).pin_memory() for v in (X, Y, a, b))
+    Xd, Yd, ad, bd = (v.to(dev) for v in (hX, hY, ha, hb))
+    flags = {"auto": sot.SOT_PREC_AUTO, "fp32": sot.SOT_PREC_FP32, "f16x3": sot.SOT_PREC_F16X3}[args.prec]
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    pairs = 2.0 * B * n * m * iters
+
+    def step(Xs, Ys, As, Bs):
+        f, g, info = sot.sot_potentials_ex(Xs, Ys, As, Bs, eps=eps, iters_per_stage=iters, max_iters=iters,
+                                           flags=flags, stats=True)
+        cost, grad, _ = sot.sot_plan_apply(Xs, Ys, As, Bs, f, g, eps, flags=flags & 3)
+        return cost, grad, info
+
+    for _ in range(args.warmup):
+        step(Xd, Yd, ad, bd)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing, L2 flushed before every step -------------
+    launches0 = sot.sot_kernel_launches()
+    sot.sot_profile_read()
+    sot.sot_profile_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clk_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
+        else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    info = None
+    with ClockSampler(local, clk_path) as cs:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush_buf.zero_()
+            ev[k][0].record(stream)
+            cost, grad, info = step(Xd, Yd, ad, bd)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(ws)
+    sot.sot_profile_enable(False)
+    nl, half_ms = sot.sot_profile_read()
+    launches = sot.sot_kernel_launches() - launches0
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    t_dev = sum(step_ms) / 1e3
+    t_max = max_over_ranks(t_dev, ws, dev)
+    clocks = cs.summary()
+
+    # ---- end to end through the public API with host buffers -------------------
+    h2d = sum(v.numel() * 4 for v in (hX, hY, ha, hb))
+    d2h = (B + B * n * d) * 4
+    hcost = torch.empty(B, dtype=torch.float32).pin_memory()
+    hgrad = torch.empty(B, n, d, dtype=torch.float32).pin_memory()
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for k in range(args.steps):
+        flush_buf.zero_()
+        e0.record(stream)
+        Xs, Ys, As, Bs = (v.to(dev, non_blocking=True) for v in (hX, hY, ha, hb))
+        cost, grad, _ = step(Xs, Ys, As, Bs)
+        hcost.copy_(cost, non_blocking=True)
+        hgrad.copy_(grad, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_max = max_over_ranks(e2e_ms / 1e3, ws, dev)
+
+    if rank != 0:
+        return 0
+    pk, pk_kind = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per_launch_ms = half_ms / max(nl, 1)
+    per_launch_pairs = B * n * m
+    mhz = float(pk.get("sm_max_mhz", 2070.0))
+    if sot.sot_select_path(d, flags) == 2:
+        flops_pair = 3 * 2 * d  # fp16 hi*hi + hi*lo + lo*hi products
+        achieved = flops_pair * per_launch_pairs / (per_launch_ms / 1e3) / 1e12
+        peak = float(pk["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{pk_kind} bf16 dense (fp16 has the same nominal rate)",
+                "kernel": "tcgen05 f16x3 half-step"}
+        dtype = "f16x3"
+    else:
+        flops_pair = 2 * d  # one FMA per coordinate
+        achieved = flops_pair * per_launch_pairs / (per_launch_ms / 1e3) / 1e12
+        peak = 2 * 128 * sms * mhz * 1e6 / 1e12  # FP32 FMA lanes x 2 flops x SMs x max clock
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "peak_source": f"128 FP32 lanes/SM x {sms} SMs x {mhz:.0f} MHz x 2",
+                "kernel": "fp32 FMA half-step"}
+        dtype = "f32"
+    # CPU baseline: the oracle on a bounded sample of the same workload
+    cpu = None
+    if not args.no_cpu_baseline:
+        r, rows, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], eps)
+        cpu = {"value": r / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle",
+               "sample": f"f-half of {rows} rows x {m} columns (d={d}), {t:.1f} s"}
+    value = ws * pairs * args.steps / t_max / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": dtype, "data": "synthetic",
+        "config": {"workload": w["name"], "B": B, "n": n, "m": m, "d": d, "eps": eps, "iters": iters,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "iters_per_s": ws * iters * args.steps / t_max,
+        "half_step": {"launches": nl, "avg_ms": per_launch_ms, "pairs_per_launch": per_launch_pairs},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": ws * pairs * args.steps / e2e_max / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "marginal_err": info["err"][0] if info else None,
+        "wall_s": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--prec", choices=["auto", "fp32", "f16x3"], default="auto")
+    ap.add_argument("--n", type=int, default=0, help="override n = m (testing only)")
+    ap.add_argument("--iters", type=int, default=0, help="override the iteration count (testing only)")
+    ap.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    return run_gpu(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

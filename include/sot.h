@@ -1,0 +1,210 @@
+/*
+ * sot.h -- C ABI of the GB300 (sm_103a) log-domain Sinkhorn library for point
+ * clouds with squared-Euclidean cost.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All array pointers are DEVICE pointers (cudaMalloc'd or torch-allocated
+ *   memory on the current device) unless the parameter name ends in _host.
+ *   The caller owns every array; the library never allocates an output.
+ * - Layout: float32, row-major, contiguous, batch-major:
+ *     X[B][n][d], Y[B][m][d]          point clouds (source rows, target columns)
+ *     a[B][n], b[B][m]                probability weights; NULL = uniform 1/n, 1/m
+ *     f[B][n], g[B][m]                dual potentials (true, unshifted values)
+ *   Weights must be > 0 and finite, each a[k] and b[k] summing to one.
+ * - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call is stream-ordered.  Calls are asynchronous unless documented
+ *   otherwise; scratch memory is taken with cudaMallocAsync / cudaFreeAsync on
+ *   `stream` and released before the call returns its status.
+ * - Every call returns an int status (SOT_OK = 0 or a negative SOT_ERR_*)
+ *   and never throws or aborts.  Arguments are checked on the host before
+ *   anything is launched; on error, output contents are unspecified except
+ *   where stated.  sot_last_error() gives a one-line description of the most
+ *   recent failure on the calling thread.
+ * - Non-finite inputs are not detected by the asynchronous calls (they
+ *   propagate into the outputs); sot_check_inputs() validates synchronously.
+ *
+ * Notation (page "FlashSinkhorn: IO-aware entropic optimal transport on GPU",
+ * Methodologie 1, Propositie 1):
+ *   C_ij = |x_i - y_j|^2,  P_ij = a_i b_j exp((f_i + g_j - C_ij) / eps)
+ *   f-half:  f_i <- -eps LSE_j[(g_j - C_ij)/eps + log b_j]
+ *   g-half:  g_j <- -eps LSE_i[(f_i - C_ij)/eps + log a_i]
+ * One iteration is an f-half followed by a g-half that uses the new f.  The
+ * kernels evaluate each half as a row-wise LSE of the biased dot-product
+ * score (2 x_i.y_j + g_j - |y_j|^2 + eps log b_j)/eps, streaming tiles of the
+ * other cloud; the n x m cost matrix is never stored (same page,
+ * Methodologie 2).
+ */
+#ifndef SOT_H
+#define SOT_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+enum sot_status {
+    SOT_OK = 0,
+    SOT_ERR_INVALID_ARG = -1,  /* bad size, NULL pointer, eps <= 0, ... */
+    SOT_ERR_NONFINITE = -2,    /* sot_check_inputs: NaN/Inf coordinate or weight, or weight <= 0 */
+    SOT_ERR_CAPACITY = -3,     /* sot_plan_coo: capacity < nnz; *nnz_host holds the required count */
+    SOT_ERR_TIMEOUT = -4,      /* a bounded device-side wait gave up */
+    SOT_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
+    SOT_ERR_UNSUPPORTED = -6,  /* the requested precision / size has no kernel on this device */
+    SOT_ERR_NOMEM = -7         /* stream-ordered scratch allocation failed */
+};
+
+/* ---- schedule flags ---------------------------------------------------- */
+enum sot_flags {
+    SOT_PREC_AUTO = 0,          /* d <= 3: fp32 FMA; d % 16 == 0, 16 <= d <= 256: tensor cores (fp16 x3); else fp32 */
+    SOT_PREC_FP32 = 1,          /* fp32 FMA contraction for any d */
+    SOT_PREC_F16X3 = 2,         /* tcgen05 fp16 products hi*hi + hi*lo + lo*hi (fp32-class accuracy) */
+    SOT_PREC_MASK = 3,
+    SOT_WARM_START = 1 << 4,    /* read f, g as the initial potentials instead of f = g = 0 */
+    SOT_STAGE_EARLY_EXIT = 1 << 5 /* apply the stop test in every stage, not only at the final eps */
+};
+
+/*
+ * Annealing schedule.  Stages k = 0, 1, ... use eps_k = max(eps, eps_init * eps_factor^k);
+ * the first k with eps_init * eps_factor^k <= eps is the last stage (clamped
+ * to eps).  eps_init <= eps (or eps_factor outside (0,1)) means one stage at eps.
+ * Every stage runs iters_per_stage iterations, warm-started from the previous one.
+ * Stop test (tol > 0): after an iteration at the final eps (or in any stage
+ * with SOT_STAGE_EARLY_EXIT) the row-marginal error sum_i |sum_j P_ij - a_i|
+ * of the current (f, g) is compared with tol, using the largest error over the
+ * batch; passing ends the stage (the solve, at the final eps).  The final
+ * stage continues past iters_per_stage until the test passes or the total
+ * number of iterations reaches max_iters (max_iters <= 0: no extension).
+ * eps annealing and the stop rule are not fixed by the pages; this is the
+ * reading this library implements.
+ */
+typedef struct {
+    float eps;            /* final (or only) eps, > 0 */
+    float eps_init;       /* first-stage eps (annealing when > eps) */
+    float eps_factor;     /* per-stage factor in (0, 1) */
+    int iters_per_stage;  /* >= 0 */
+    int max_iters;        /* cap on total iterations (<= 0: stages only) */
+    float tol;            /* stop tolerance on the marginal error (<= 0: none) */
+    int flags;            /* sot_flags */
+} sot_schedule;
+
+/* Filled by sot_potentials_ex when non-NULL (the call then synchronises `stream`). */
+typedef struct {
+    int iters_done;        /* total iterations returned */
+    int stages_done;       /* stages entered */
+    int converged;         /* 1 if the stop test passed at the final eps */
+    float final_eps;
+    float* err_host;       /* [B] or NULL: marginal error of the returned iterate (NaN if not evaluated) */
+    int* stage_iters_host; /* [stage_iters_cap] or NULL: iterations realised per stage */
+    int stage_iters_cap;
+} sot_stats;
+
+/* ---- calls --------------------------------------------------------------- */
+
+/*
+ * Fixed schedule: `iters` iterations at `eps` from f = g = 0.  Asynchronous.
+ * Page: "FlashSinkhorn", Methodologie 1 (the update) and 2 (fused streaming).
+ */
+int sot_potentials(const float* X, const float* Y, const float* a, const float* b,
+                   int B, int n, int m, int d, float eps, int iters,
+                   float* f, float* g, void* stream);
+
+/*
+ * General schedule (annealing, stop test, warm start, precision), see
+ * sot_schedule.  Synchronises `stream` when st != NULL, or when the stop test
+ * is active (it reads a device flag every few iterations).
+ */
+int sot_potentials_ex(const float* X, const float* Y, const float* a, const float* b,
+                      int B, int n, int m, int d, const sot_schedule* s,
+                      float* f, float* g, sot_stats* st, void* stream);
+
+/*
+ * Plan application with the given (f, g) at eps, without storing P
+ * ("FlashSinkhorn", Methodologie 3):
+ *   cost[k]     = sum_ij P_ij C_ij                        (may be NULL)
+ *   grad[k][i]  = 2 (a_i x_i - sum_j P_ij y_j)  [B][n][d] (may be NULL)
+ *   rowsum[k][i]= sum_j P_ij                    [B][n]    (may be NULL)
+ * Asynchronous.  flags: SOT_PREC_* (0 = auto).
+ */
+int sot_plan_apply(const float* X, const float* Y, const float* a, const float* b,
+                   int B, int n, int m, int d, const float* f, const float* g, float eps,
+                   float* cost, float* grad, float* rowsum, int flags, void* stream);
+
+/* Convenience forms of sot_plan_apply (precision auto). */
+int sot_cost(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+             const float* f, const float* g, float eps, float* cost, void* stream);
+int sot_grad_x(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+               const float* f, const float* g, float eps, float* grad, void* stream);
+int sot_cost_grad(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                  const float* f, const float* g, float eps, float* cost, float* grad, void* stream);
+
+/*
+ * Thresholded COO plan ("From Theory to Throughput: CUDA-Optimized APML",
+ * Abstract and Innovation: thresholded assignments, bidirectional
+ * symmetrisation, COO storage).  With s_ij = (g_j - C_ij)/eps + log b_j and
+ * s'_ij = (f_i - C_ij)/eps + log a_i, pair (i, j) is kept when
+ *   (dirs & 1) and s_ij  >= max_j' s_ij'  + log(threshold)   [P_ij >= threshold * row max], or
+ *   (dirs & 2) and s'_ij >= max_i' s'_i'j + log(threshold)   [P_ij >= threshold * column max].
+ * threshold in [0, 1]; 0 keeps every pair.  Output, cloud after cloud, row-major
+ * (row ascending, then column ascending) with cloud-local int32 indices:
+ *   rows[nnz], cols[nnz], vals[nnz] = P_ij (fp32), batch_offsets[B+1] (int64, device).
+ * Synchronises `stream` once (to read the count).  *nnz_host (host) always
+ * receives the total count; if it exceeds capacity the call returns
+ * SOT_ERR_CAPACITY and writes no entries.
+ */
+int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b,
+                 int B, int n, int m, int d, const float* f, const float* g, float eps,
+                 float threshold, int dirs, long long capacity,
+                 int* rows, int* cols, float* vals, long long* batch_offsets,
+                 long long* nnz_host, void* stream);
+
+/*
+ * Gradient on a stored support ("CUDA-Optimized APML", Innovation: gradients
+ * preserved on the stored support):
+ *   grad[k][i] = 2 sum_{e in cloud k, rows[e] = i} vals[e] (x_i - y_cols[e])
+ * The COO must be row-sorted within each cloud (as sot_plan_coo writes it);
+ * unsorted or out-of-range entries make the call return SOT_ERR_INVALID_ARG
+ * (checked on the device).  batch_offsets is a device array [B+1] whose last
+ * element is the number of entries.  The call synchronises `stream` once to
+ * read the check's result.
+ */
+int sot_grad_x_coo(const float* X, const float* Y, int B, int n, int m, int d,
+                   const int* rows, const int* cols, const float* vals,
+                   const long long* batch_offsets, float* grad, void* stream);
+
+/*
+ * Synchronous input validation: every coordinate finite, every weight finite
+ * and > 0.  Returns SOT_OK, SOT_ERR_NONFINITE or SOT_ERR_INVALID_ARG.
+ */
+int sot_check_inputs(const float* X, const float* Y, const float* a, const float* b,
+                     int B, int n, int m, int d, void* stream);
+
+/*
+ * Per-kernel timing with CUDA events recorded on the launching stream around
+ * every half-step launch (off by default).  sot_profile_read synchronises the
+ * device events, returns the number of half-step launches since the last
+ * reset and their summed duration in milliseconds, and resets the counters.
+ */
+int sot_profile_enable(int on);
+int sot_profile_read(long long* launches_host, double* total_ms_host);
+
+/*
+ * Which kernel family a solve of dimension d with these flags would use:
+ * 0 = fp32 point kernels (d <= 3), 1 = fp32 dense kernels, 2 = tcgen05
+ * tensor-core kernels; or a negative SOT_ERR_* when none applies.  Host only.
+ */
+int sot_select_path(int d, int flags);
+
+/* Number of CUDA kernels this library has launched since it was loaded
+ * (all devices, all threads).  Diagnostic; no synchronisation. */
+long long sot_kernel_launches(void);
+
+/* Static strings; never NULL. */
+const char* sot_status_string(int status);
+const char* sot_last_error(void);
+int sot_version(void); /* major * 10000 + minor * 100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SOT_H */

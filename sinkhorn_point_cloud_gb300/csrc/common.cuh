@@ -1,0 +1,103 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of libsot.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define SOT_LN2 0.69314718055994530942f
+#define SOT_LOG2E 1.44269504088896340736f
+
+// Hardware base-2 exponential / logarithm (MUFU).  ex2 of -inf is +0; the
+// .ftz forms flush subnormal results to zero.
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Packed two-lane fp32 arithmetic (one instruction, two IEEE results; each
+// lane is rounded exactly as the scalar instruction would round it).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\tmov.b64 rc, {%6,%7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0,%1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0,%1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Block-wide reductions (fixed tree => deterministic).  `red` must hold one
+// float per warp.  Every thread of the block must call them.
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (threadIdx.x < 32) {
+        t = (l < NT / 32) ? red[l] : 0.f;
+        t = warp_sum(t);
+        if (l == 0) red[0] = t;
+    }
+    __syncthreads();
+    return red[0];
+}
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* red) {
+    v = warp_max(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float t = -INFINITY;
+    if (threadIdx.x < 32) {
+        t = (l < NT / 32) ? red[l] : -INFINITY;
+        t = warp_max(t);
+        if (l == 0) red[0] = t;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// Row-state stabiliser handling shared by the half-step kernels.
+// A row's running log2-sum is (m, s): value = m + log2(s).
+// The tile sum is considered unsafe (overflow risk) above this bound.
+#define SOT_TILE_SUM_MAX 1.2676506e30f  /* 2^100 */
+// Below this bound the final sum may have lost precision to flushed terms.
+#define SOT_SUM_MIN 8.2718061e-25f      /* 2^-80 */
+// The warm stabiliser sits this many log2 units below the previous row value.
+#define SOT_STAB_BIAS 32.0f
+
+// Combine two (m, s) partial log2-sums.
+__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
+    if (m2 == -INFINITY || s2 == 0.f) return;
+    if (m == -INFINITY || s == 0.f) { m = m2; s = s2; return; }
+    if (m2 > m) { s = s * ex2f(m - m2) + s2; m = m2; }
+    else        { s = s + s2 * ex2f(m2 - m); }
+}
+
+// Device status bits (OR-ed into a status word).
+#define SOT_DEV_RETRY_ROWS 1  /* some rows took the slow full-row recompute */
+#define SOT_DEV_BAD_COO 2     /* COO input unsorted / out of range */

@@ -1,0 +1,537 @@
+// k_point.cu -- fused Sinkhorn half-steps for point clouds with d <= 3 on
+// FP32 FMA + MUFU ex2 (no tensor cores: a 3-term dot product is no dense
+// contraction).
+//
+// One half-step ("FlashSinkhorn", Methodologie 1-2) for row i of the updated
+// side, in base 2 with kappa = 1/(eps ln 2):
+//     L_i = log2 sum_j 2^( 2 kappa x_i.y_j + c_j ),   c_j = log2 w_j - Lam_j
+// The score tile is formed in registers from a column tile staged in shared
+// memory and never stored; the row-wise log-sum-exp is accumulated on chip
+// (Methodologie 2, "Online LSE"), one row block stays resident while every
+// column tile streams past it (row-stationary traversal).
+//
+// Stabiliser.  Each row keeps a running (m, s) with value m + log2 s.  m
+// starts at the previous row value minus a bias (or -inf on a cold start) so
+// a column costs 3 FFMA + 1 FADD + 1 ex2 + 1 FADD and no per-pair max.  A
+// tile whose sum leaves the safe range takes a slow path that recomputes it
+// against the tile maximum, so the result is the exact LSE for any start.
+// Rows whose final sum underflowed are recomputed with a two-pass LSE.
+//
+// Layout of a column tile in shared memory: column pairs interleaved so that
+// one 16-byte load yields two 2-lane operands of the packed f32x2 FMA:
+//     tile[2p]   = (x_j, x_j', y_j, y_j'),   tile[2p+1] = (z_j, z_j', c_j, c_j')
+#include "common.cuh"
+#include "kernels.h"
+
+namespace sot {
+
+constexpr int PT_T = 128;               // threads per CTA
+constexpr int PT_RPT = 4;               // rows per thread
+constexpr int PT_ROWS = PT_T * PT_RPT;  // rows per CTA
+constexpr int PT_TC = 2 * PT_T;         // columns per shared-memory tile
+
+int point_rows_per_cta() { return PT_ROWS; }
+int point_cols_per_tile() { return PT_TC; }
+
+// Score of two columns for one row: t = ((c + q0*x) + q1*y) + q2*z, fp32 FMAs
+// in this fixed order (the COO kernels evaluate the same chain).
+template <int D>
+__device__ __forceinline__ float2 pair_chain(float2 t, float2 q0, float2 q1, float2 q2, float4 A, float4 Bv) {
+    if (D >= 1) t = ffma2(q0, make_float2(A.x, A.y), t);
+    if (D >= 2) t = ffma2(q1, make_float2(A.z, A.w), t);
+    if (D >= 3) t = ffma2(q2, make_float2(Bv.x, Bv.y), t);
+    return t;
+}
+template <int D>
+__device__ __forceinline__ float scalar_chain(float t, float q0, float q1, float q2, float4 c) {
+    if (D >= 1) t = fmaf(q0, c.x, t);
+    if (D >= 2) t = fmaf(q1, c.y, t);
+    if (D >= 3) t = fmaf(q2, c.z, t);
+    return t;
+}
+
+// Stage columns [base, base + PT_TC) of the chunk ending at c_end.
+__device__ __forceinline__ void load_point_tile(float4* tile, const float4* cp, const float* cst, int base,
+                                                int c_end) {
+    const int j0 = base + 2 * threadIdx.x, j1 = j0 + 1;
+    float4 c0 = make_float4(0.f, 0.f, 0.f, -INFINITY), c1 = c0;
+    if (j0 < c_end) { c0 = cp[j0]; c0.w = c0.w - cst[j0]; }
+    if (j1 < c_end) { c1 = cp[j1]; c1.w = c1.w - cst[j1]; }
+    tile[2 * threadIdx.x] = make_float4(c0.x, c1.x, c0.y, c1.y);
+    tile[2 * threadIdx.x + 1] = make_float4(c0.z, c1.z, c0.w, c1.w);
+}
+
+// Two-pass LSE of one full row by the whole CTA (slow path for rows whose
+// stabilised sum underflowed).  Returns log2 sum_j 2^(score_j).
+template <int D>
+__device__ float point_row_full(const float4* cp, const float* cst, int nc, float q0, float q1, float q2,
+                                float* red) {
+    float mx = -INFINITY;
+    for (int j = threadIdx.x; j < nc; j += PT_T) {
+        float4 c = cp[j];
+        mx = fmaxf(mx, scalar_chain<D>(c.w - cst[j], q0, q1, q2, c));
+    }
+    mx = block_max<PT_T>(mx, red);
+    if (mx == -INFINITY) return -INFINITY;
+    float sm = 0.f;
+    for (int j = threadIdx.x; j < nc; j += PT_T) {
+        float4 c = cp[j];
+        sm += ex2f(scalar_chain<D>(c.w - cst[j], q0, q1, q2, c) - mx);
+    }
+    sm = block_sum<PT_T>(sm, red);
+    return mx + log2f(sm);
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
+    if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
+    __shared__ float4 tile[PT_TC];
+    __shared__ float red[PT_T / 32];
+    __shared__ int s_last;
+    __shared__ int s_nretry;
+    __shared__ int s_retry[PT_ROWS];
+
+    const int b = blockIdx.y;
+    const int rt = blockIdx.x / p.split, ch = blockIdx.x % p.split;
+    const int row0 = rt * PT_ROWS;
+    const int c_begin = ch * p.chunk;
+    const int c_end = min(p.nc, c_begin + p.chunk);
+    const float4* rp = reinterpret_cast<const float4*>(p.rpack) + (size_t)b * p.nr;
+    const float4* cp = reinterpret_cast<const float4*>(p.cpack) + (size_t)b * p.nc;
+    const float* cst = p.cstate + (size_t)b * p.nc;
+    const size_t rbase = (size_t)b * p.nr;
+
+    float2 q0[PT_RPT], q1[PT_RPT], q2[PT_RPT], nm[PT_RPT];
+    float m[PT_RPT], s[PT_RPT];
+#pragma unroll
+    for (int r = 0; r < PT_RPT; ++r) {
+        const int row = row0 + threadIdx.x + r * PT_T;
+        const bool valid = row < p.nr;
+        float4 x = valid ? rp[row] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float a0 = p.two_kappa * x.x, a1 = p.two_kappa * x.y, a2 = p.two_kappa * x.z;
+        q0[r] = make_float2(a0, a0);
+        q1[r] = make_float2(a1, a1);
+        q2[r] = make_float2(a2, a2);
+        if (MODE == MODE_MAX) {
+            m[r] = -INFINITY;
+        } else if (!valid) {
+            m[r] = INFINITY;  // every term becomes 2^-inf = 0; never written
+        } else {
+            m[r] = p.cold ? -INFINITY : p.rstate_in[rbase + row] - SOT_STAB_BIAS;
+        }
+        nm[r] = make_float2(-m[r], -m[r]);
+        s[r] = 0.f;
+    }
+
+    for (int base = c_begin; base < c_end; base += PT_TC) {
+        __syncthreads();
+        load_point_tile(tile, cp, cst, base, c_end);
+        __syncthreads();
+        if (MODE == MODE_MAX) {
+            float2 mx[PT_RPT];
+#pragma unroll
+            for (int r = 0; r < PT_RPT; ++r) mx[r] = make_float2(-INFINITY, -INFINITY);
+#pragma unroll 4
+            for (int pp = 0; pp < PT_TC / 2; ++pp) {
+                const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
+                const float2 cj = make_float2(Bv.z, Bv.w);
+#pragma unroll
+                for (int r = 0; r < PT_RPT; ++r) {
+                    float2 t = pair_chain<D>(cj, q0[r], q1[r], q2[r], A, Bv);
+                    mx[r].x = fmaxf(mx[r].x, t.x);
+                    mx[r].y = fmaxf(mx[r].y, t.y);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < PT_RPT; ++r) m[r] = fmaxf(m[r], fmaxf(mx[r].x, mx[r].y));
+        } else {
+            float2 st[PT_RPT];
+#pragma unroll
+            for (int r = 0; r < PT_RPT; ++r) st[r] = make_float2(0.f, 0.f);
+#pragma unroll 4
+            for (int pp = 0; pp < PT_TC / 2; ++pp) {
+                const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
+                const float2 cj = make_float2(Bv.z, Bv.w);
+#pragma unroll
+                for (int r = 0; r < PT_RPT; ++r) {
+                    float2 t = pair_chain<D>(fadd2(cj, nm[r]), q0[r], q1[r], q2[r], A, Bv);
+                    st[r] = fadd2(st[r], make_float2(ex2f(t.x), ex2f(t.y)));
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < PT_RPT; ++r) {
+                float ts = st[r].x + st[r].y;
+                if (!(ts < SOT_TILE_SUM_MAX)) {
+                    // slow path: re-stabilise this row on the tile maximum
+                    float mt = -INFINITY;
+                    for (int pp = 0; pp < PT_TC / 2; ++pp) {
+                        const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
+                        float2 t = pair_chain<D>(make_float2(Bv.z, Bv.w), q0[r], q1[r], q2[r], A, Bv);
+                        mt = fmaxf(mt, fmaxf(t.x, t.y));
+                    }
+                    const float mn = fmaxf(m[r], mt);
+                    if (mn == -INFINITY) {
+                        ts = 0.f;
+                    } else {
+                        s[r] = (m[r] == -INFINITY) ? 0.f : s[r] * ex2f(m[r] - mn);
+                        m[r] = mn;
+                        nm[r] = make_float2(-mn, -mn);
+                        float2 acc = make_float2(0.f, 0.f);
+                        for (int pp = 0; pp < PT_TC / 2; ++pp) {
+                            const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
+                            float2 t = pair_chain<D>(fadd2(make_float2(Bv.z, Bv.w), nm[r]), q0[r], q1[r],
+                                                     q2[r], A, Bv);
+                            acc = fadd2(acc, make_float2(ex2f(t.x), ex2f(t.y)));
+                        }
+                        ts = acc.x + acc.y;
+                    }
+                }
+                s[r] += ts;
+            }
+        }
+    }
+
+    // ---- combine column chunks -------------------------------------------
+    if (p.split > 1) {
+        const size_t stride = (size_t)p.B * p.nr;
+#pragma unroll
+        for (int r = 0; r < PT_RPT; ++r) {
+            const int row = row0 + threadIdx.x + r * PT_T;
+            if (row < p.nr) {
+                p.part_m[ch * stride + rbase + row] = m[r];
+                if (MODE == MODE_LSE) p.part_s[ch * stride + rbase + row] = s[r];
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned prev = atomicAdd(&p.counters[b * p.rowtiles + rt], 1u);
+            s_last = (prev == (unsigned)(p.split - 1));
+        }
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+#pragma unroll
+        for (int r = 0; r < PT_RPT; ++r) {
+            const int row = row0 + threadIdx.x + r * PT_T;
+            if (row >= p.nr) continue;
+            float M = -INFINITY, S = 0.f;
+            for (int c = 0; c < p.split; ++c) {
+                const float pm = __ldcg(p.part_m + c * stride + rbase + row);
+                if (MODE == MODE_MAX) {
+                    M = fmaxf(M, pm);
+                } else {
+                    lse_combine(M, S, pm, __ldcg(p.part_s + c * stride + rbase + row));
+                }
+            }
+            m[r] = M;
+            s[r] = S;
+        }
+        if (threadIdx.x == 0) p.counters[b * p.rowtiles + rt] = 0u;
+    }
+
+    // ---- finalise rows ----------------------------------------------------
+    if (threadIdx.x == 0) s_nretry = 0;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < PT_RPT; ++r) {
+        const int row = row0 + threadIdx.x + r * PT_T;
+        if (row >= p.nr) continue;
+        if (MODE == MODE_MAX) {
+            p.rstate_out[rbase + row] = m[r];
+        } else if (s[r] >= SOT_SUM_MIN && s[r] < INFINITY && m[r] > -INFINITY) {
+            p.rstate_out[rbase + row] = m[r] + log2f(s[r]);
+        } else {
+            s_retry[atomicAdd(&s_nretry, 1)] = row;
+        }
+    }
+    __syncthreads();
+    if (MODE == MODE_LSE) {
+        const int nretry = s_nretry;
+        for (int k = 0; k < nretry; ++k) {
+            const int row = s_retry[k];
+            const float4 x = rp[row];
+            const float v = point_row_full<D>(cp, cst, p.nc, p.two_kappa * x.x, p.two_kappa * x.y,
+                                              p.two_kappa * x.z, red);
+            if (threadIdx.x == 0) {
+                p.rstate_out[rbase + row] = v;
+                atomicOr(p.status, SOT_DEV_RETRY_ROWS);
+            }
+        }
+        if (p.errpart) {
+            __syncthreads();
+            float e = 0.f;
+            const float wu = 1.f / (float)p.nr;
+#pragma unroll
+            for (int r = 0; r < PT_RPT; ++r) {
+                const int row = row0 + threadIdx.x + r * PT_T;
+                if (row >= p.nr) continue;
+                const float w = p.rweight ? p.rweight[rbase + row] : wu;
+                e += w * fabsf(ex2f(p.rstate_out[rbase + row] - p.rstate_in[rbase + row]) - 1.f);
+            }
+            e = block_sum<PT_T>(e, red);
+            if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rt] = e;
+        }
+    }
+}
+
+cudaError_t launch_point_half(const HalfArgs& p, int mode, cudaStream_t st) {
+    dim3 grid(p.rowtiles * p.split, p.B), block(PT_T);
+#define SOT_PT_CASE(DD)                                                               \
+    case DD:                                                                          \
+        if (mode == MODE_MAX) { count_launches(1); point_half_kernel<DD, MODE_MAX><<<grid, block, 0, st>>>(p); } \
+        else { count_launches(1); point_half_kernel<DD, MODE_LSE><<<grid, block, 0, st>>>(p); } \
+        break;
+    switch (p.d) {
+        SOT_PT_CASE(1)
+        SOT_PT_CASE(2)
+        SOT_PT_CASE(3)
+        default: return cudaErrorInvalidValue;
+    }
+#undef SOT_PT_CASE
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Plan application ("FlashSinkhorn", Methodologie 3): per row, with the given
+// potentials and P_ij / a_i = 2^(kappa nx_i - L_i + kappa ny_j + log2 b_j - Lam_j - kappa C_ij),
+//   r_i = sum_j P_ij,  v_i = sum_j P_ij y_j,  q_i = sum_j P_ij C_ij
+// with C_ij in the direct form |x_i - y_j|^2 (accurate for near-coincident
+// points).  Outputs cost = sum_i q_i (per-CTA partials), grad_i =
+// 2 (a_i x_i - sum_j P_ij y_j) in the caller's coordinates, rowsum r_i.
+constexpr int AP_T = 128;
+constexpr int AP_TC = 256;
+int point_apply_rows_per_cta() { return AP_T; }
+
+template <int D>
+__global__ void __launch_bounds__(AP_T) point_apply_kernel(ApplyArgs p) {
+    __shared__ float4 tile[AP_TC];
+    __shared__ float red[AP_T / 32];
+    const int b = blockIdx.y;
+    const int row = blockIdx.x * AP_T + threadIdx.x;
+    const bool valid = row < p.n;
+    const float4* xp = reinterpret_cast<const float4*>(p.xpack) + (size_t)b * p.n;
+    const float4* yp = reinterpret_cast<const float4*>(p.ypack) + (size_t)b * p.m;
+    const float* ny = p.ny + (size_t)b * p.m;
+    const float* lam = p.Lam + (size_t)b * p.m;
+    const float4 x = valid ? xp[row] : make_float4(0.f, 0.f, 0.f, 0.f);
+    // row part of the exponent, relative to the row weight
+    const float A = valid ? p.kappa * p.nx[(size_t)b * p.n + row] - p.L[(size_t)b * p.n + row] : 0.f;
+    float m = valid ? -SOT_STAB_BIAS : INFINITY;
+    float r = 0.f, v0 = 0.f, v1 = 0.f, v2 = 0.f, q = 0.f;
+    for (int base = 0; base < p.m; base += AP_TC) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < AP_TC; t += AP_T) {
+            const int j = base + t;
+            float4 c = make_float4(0.f, 0.f, 0.f, -INFINITY);
+            if (j < p.m) {
+                c = yp[j];
+                c.w = fmaf(p.kappa, ny[j], c.w - lam[j]);
+            }
+            tile[t] = c;
+        }
+        __syncthreads();
+        const float Am = A - m;
+        float tr = 0.f, t0 = 0.f, t1 = 0.f, t2 = 0.f, tq = 0.f;
+#pragma unroll 4
+        for (int t = 0; t < AP_TC; ++t) {
+            const float4 c = tile[t];
+            const float d0 = x.x - c.x, d1 = x.y - c.y, d2 = x.z - c.z;
+            float C = d0 * d0;
+            if (D >= 2) C = fmaf(d1, d1, C);
+            if (D >= 3) C = fmaf(d2, d2, C);
+            const float w = ex2f(fmaf(-p.kappa, C, Am + c.w));
+            tr += w;
+            t0 = fmaf(w, c.x, t0);
+            if (D >= 2) t1 = fmaf(w, c.y, t1);
+            if (D >= 3) t2 = fmaf(w, c.z, t2);
+            tq = fmaf(w, C, tq);
+        }
+        if (!(tr < SOT_TILE_SUM_MAX)) {
+            float mt = -INFINITY;
+            for (int t = 0; t < AP_TC; ++t) {
+                const float4 c = tile[t];
+                const float d0 = x.x - c.x, d1 = x.y - c.y, d2 = x.z - c.z;
+                float C = d0 * d0;
+                if (D >= 2) C = fmaf(d1, d1, C);
+                if (D >= 3) C = fmaf(d2, d2, C);
+                mt = fmaxf(mt, fmaf(-p.kappa, C, A + c.w));
+            }
+            const float mn = fmaxf(m, mt);
+            const float sc = ex2f(m - mn);
+            r *= sc; v0 *= sc; v1 *= sc; v2 *= sc; q *= sc;
+            m = mn;
+            const float Am2 = A - m;
+            tr = t0 = t1 = t2 = tq = 0.f;
+            for (int t = 0; t < AP_TC; ++t) {
+                const float4 c = tile[t];
+                const float d0 = x.x - c.x, d1 = x.y - c.y, d2 = x.z - c.z;
+                float C = d0 * d0;
+                if (D >= 2) C = fmaf(d1, d1, C);
+                if (D >= 3) C = fmaf(d2, d2, C);
+                const float w = ex2f(fmaf(-p.kappa, C, Am2 + c.w));
+                tr += w;
+                t0 = fmaf(w, c.x, t0);
+                if (D >= 2) t1 = fmaf(w, c.y, t1);
+                if (D >= 3) t2 = fmaf(w, c.z, t2);
+                tq = fmaf(w, C, tq);
+            }
+        }
+        r += tr; v0 += t0; v1 += t1; v2 += t2; q += tq;
+    }
+    float qi = 0.f;
+    if (valid) {
+        const float ai = p.a ? p.a[(size_t)b * p.n + row] : 1.f / (float)p.n;
+        const float fac = ai * ex2f(m);
+        r *= fac; v0 *= fac; v1 *= fac; v2 *= fac; qi = q * fac;
+        if (p.rowsum) p.rowsum[(size_t)b * p.n + row] = r;
+        if (p.grad) {
+            // v_i in caller coordinates: sum_j P_ij (y'_j + t) = v'_i + r_i t
+            const float* sh = p.shift + (size_t)b * D;
+            const float* xo = p.X + ((size_t)b * p.n + row) * D;
+            float* gr = p.grad + ((size_t)b * p.n + row) * D;
+            const float vv[3] = {v0, v1, v2};
+#pragma unroll
+            for (int k = 0; k < D; ++k) gr[k] = 2.f * (ai * xo[k] - fmaf(r, sh[k], vv[k]));
+        }
+    }
+    if (p.cost_part) {
+        qi = block_sum<AP_T>(qi, red);
+        if (threadIdx.x == 0) p.cost_part[b * p.rowtiles + blockIdx.x] = qi;
+    }
+}
+
+cudaError_t launch_point_apply(const ApplyArgs& p, cudaStream_t st) {
+    dim3 grid(p.rowtiles, p.B), block(AP_T);
+    switch (p.d) {
+        case 1: count_launches(1); point_apply_kernel<1><<<grid, block, 0, st>>>(p); break;
+        case 2: count_launches(1); point_apply_kernel<2><<<grid, block, 0, st>>>(p); break;
+        case 3: count_launches(1); point_apply_kernel<3><<<grid, block, 0, st>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Thresholded COO plan ("CUDA-Optimized APML", Abstract / Innovation).
+// Pair (i, j) is kept when
+//   (dirs & 1) and t_ij >= Mr_i + log2 tau   (row-relative), or
+//   (dirs & 2) and u_ji >= Mc_j + log2 tau   (column-relative),
+// with t_ij = 2 kappa x_i.y_j + log2 b_j - Lam_j evaluated by the same FMA
+// chain as the f-half maximum pass and u_ji = 2 kappa y_j.x_i + log2 a_i - L_i
+// by the chain of the g-half pass, so the maxima and the predicate agree bit
+// for bit.  One warp owns CO_RW rows; its lanes take 32 consecutive columns,
+// and a ballot / popc over the predicate gives each kept pair its slot, so a
+// row's entries come out in ascending column order with coalesced stores.
+constexpr int CO_T = 256;
+constexpr int CO_RW = 4;                      // rows per warp
+constexpr int CO_ROWS = (CO_T / 32) * CO_RW;  // rows per CTA
+constexpr int CO_TC = 256;                    // columns per tile
+
+template <int D, bool WRITE>
+__global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
+    __shared__ float4 cy[CO_TC];   // (y, log2 b_j - Lam_j)
+    __shared__ float4 cq[CO_TC];   // (2 kappa y, Mc_j + log2 tau)
+    __shared__ float cby[CO_TC];   // kappa ny_j + log2 b_j - Lam_j  (value exponent)
+    const int b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rowb = blockIdx.x * CO_ROWS + warp * CO_RW;
+    const float4* xp = reinterpret_cast<const float4*>(p.xpack) + (size_t)b * p.n;
+    const float4* yp = reinterpret_cast<const float4*>(p.ypack) + (size_t)b * p.m;
+    const size_t xb = (size_t)b * p.n, yb = (size_t)b * p.m;
+
+    float4 x[CO_RW];
+    float q0[CO_RW], q1[CO_RW], q2[CO_RW], thr_r[CO_RW], e_r[CO_RW], arow[CO_RW];
+    long long pos[CO_RW];
+    int cnt[CO_RW];
+#pragma unroll
+    for (int r = 0; r < CO_RW; ++r) {
+        const int i = rowb + r;
+        const bool ok = i < p.n;
+        x[r] = ok ? xp[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        q0[r] = p.two_kappa * x[r].x;
+        q1[r] = p.two_kappa * x[r].y;
+        q2[r] = p.two_kappa * x[r].z;
+        thr_r[r] = ok ? p.Mr[xb + i] + p.log2tau : INFINITY;
+        e_r[r] = ok ? x[r].w - p.L[xb + i] : 0.f;  // log2 a_i - L_i
+        arow[r] = ok ? p.kappa * p.nx[xb + i] - p.L[xb + i] : 0.f;
+        pos[r] = (WRITE && ok) ? p.rowptr[xb + i] : 0;
+        cnt[r] = 0;
+    }
+    for (int base = 0; base < p.m; base += CO_TC) {
+        __syncthreads();
+        for (int t = threadIdx.x; t < CO_TC; t += CO_T) {
+            const int j = base + t;
+            float4 c = make_float4(0.f, 0.f, 0.f, -INFINITY);
+            float4 c2 = make_float4(0.f, 0.f, 0.f, INFINITY);
+            float vb = -INFINITY;
+            if (j < p.m) {
+                c = yp[j];
+                const float lam = p.Lam[yb + j];
+                c.w = c.w - lam;
+                c2 = make_float4(p.two_kappa * c.x, p.two_kappa * c.y, p.two_kappa * c.z, p.Mc[yb + j] + p.log2tau);
+                vb = fmaf(p.kappa, p.ny[yb + j], c.w);
+            }
+            cy[t] = c;
+            cq[t] = c2;
+            cby[t] = vb;
+        }
+        __syncthreads();
+        for (int cc = 0; cc < CO_TC; cc += 32) {
+            const int t = cc + lane;
+            const int j = base + t;
+            const float4 c = cy[t], c2 = cq[t];
+#pragma unroll
+            for (int r = 0; r < CO_RW; ++r) {
+                bool keep = false;
+                if (p.dirs & 1) keep = scalar_chain<D>(c.w, q0[r], q1[r], q2[r], c) >= thr_r[r];
+                if (p.dirs & 2) {
+                    const float u = scalar_chain<D>(e_r[r], c2.x, c2.y, c2.z, x[r]);
+                    keep = keep || (u >= c2.w);
+                }
+                keep = keep && (j < p.m) && (rowb + r < p.n);
+                const unsigned mask = __ballot_sync(0xffffffffu, keep);
+                if (WRITE) {
+                    const long long o = pos[r] + __popc(mask & ((1u << lane) - 1u));
+                    if (keep && o < p.capacity) {
+                        const float d0 = x[r].x - c.x, d1 = x[r].y - c.y, d2 = x[r].z - c.z;
+                        float C = d0 * d0;
+                        if (D >= 2) C = fmaf(d1, d1, C);
+                        if (D >= 3) C = fmaf(d2, d2, C);
+                        const float ai = p.a ? p.a[xb + rowb + r] : 1.f / (float)p.n;
+                        p.rows[o] = rowb + r;
+                        p.cols[o] = j;
+                        p.vals[o] = ai * ex2f(fmaf(-p.kappa, C, arow[r] + cby[t]));
+                    }
+                    pos[r] += __popc(mask);
+                } else {
+                    cnt[r] += __popc(mask);
+                }
+            }
+        }
+    }
+    if (!WRITE && lane == 0) {
+#pragma unroll
+        for (int r = 0; r < CO_RW; ++r)
+            if (rowb + r < p.n) p.counts[xb + rowb + r] = cnt[r];
+    }
+}
+
+cudaError_t launch_point_coo(const CooArgs& p, int write_pass, cudaStream_t st) {
+    dim3 grid((p.n + CO_ROWS - 1) / CO_ROWS, p.B), block(CO_T);
+#define SOT_CO_CASE(DD)                                                           \
+    case DD:                                                                      \
+        if (write_pass) { count_launches(1); point_coo_kernel<DD, true><<<grid, block, 0, st>>>(p); } \
+        else { count_launches(1); point_coo_kernel<DD, false><<<grid, block, 0, st>>>(p); } \
+        break;
+    switch (p.d) {
+        SOT_CO_CASE(1)
+        SOT_CO_CASE(2)
+        SOT_CO_CASE(3)
+        default: return cudaErrorInvalidValue;
+    }
+#undef SOT_CO_CASE
+    return cudaGetLastError();
+}
+
+}  // namespace sot

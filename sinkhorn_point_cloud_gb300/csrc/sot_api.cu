@@ -1,0 +1,742 @@
+// sot_api.cu -- the C ABI of libsot (declared in include/sot.h): argument
+// checks, stream-ordered scratch, path choice, and the orchestration of the
+// fused half-step kernels into fixed, annealed and stop-tested Sinkhorn
+// solves ("FlashSinkhorn", Methodologie 1-3), plan application and the
+// thresholded COO plan ("CUDA-Optimized APML", Abstract / Innovation).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sot.h"
+#include "tc.h"
+
+using namespace sot;
+
+namespace sot {
+static std::atomic<long long> g_kernel_launches{0};
+void count_launches(int k) { g_kernel_launches.fetch_add(k, std::memory_order_relaxed); }
+long long launches_total() { return g_kernel_launches.load(std::memory_order_relaxed); }
+}  // namespace sot
+
+namespace {
+
+constexpr double SOT_LN2_D = 0.69314718055994530942;
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+#define SOT_CUDA(call)                                                                   \
+    do {                                                                                 \
+        cudaError_t _e = (call);                                                         \
+        if (_e != cudaSuccess)                                                           \
+            return fail(SOT_ERR_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(_e), __FILE__, __LINE__); \
+    } while (0)
+
+// Stream-ordered scratch: every allocation is released on the same stream
+// when the owning call returns.
+struct Scratch {
+    cudaStream_t st;
+    std::vector<void*> ptrs;
+    explicit Scratch(cudaStream_t s) : st(s) {}
+    ~Scratch() {
+        for (void* p : ptrs) cudaFreeAsync(p, st);
+    }
+    template <class T>
+    T* alloc(size_t count) {
+        void* p = nullptr;
+        if (count == 0) count = 1;
+        if (cudaMallocAsync(&p, count * sizeof(T), st) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        ptrs.push_back(p);
+        return static_cast<T*>(p);
+    }
+};
+
+int device_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 148;
+    }
+    return cached[dev];
+}
+
+// ---- per-launch timing (sot_profile_*) ------------------------------------
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_prof_pending;
+std::vector<cudaEvent_t> g_prof_pool;
+long long g_prof_launches = 0;
+double g_prof_ms = 0.0;
+
+cudaEvent_t prof_event() {
+    if (!g_prof_pool.empty()) {
+        cudaEvent_t e = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct ProfScope {
+    cudaEvent_t a = nullptr, b = nullptr;
+    cudaStream_t st;
+    ProfScope(cudaStream_t s, bool want) : st(s) {
+        if (!want) return;
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        if (!g_prof_on) return;
+        a = prof_event();
+        b = prof_event();
+        cudaEventRecord(a, st);
+    }
+    ~ProfScope() {
+        if (!a) return;
+        cudaEventRecord(b, st);
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        g_prof_pending.emplace_back(a, b);
+    }
+};
+
+enum Path { PATH_POINT = 0, PATH_DENSE = 1, PATH_TC = 2 };
+
+int choose_path(int d, int flags, Path* out) {
+    const int prec = flags & SOT_PREC_MASK;
+    if (prec == SOT_PREC_F16X3) {
+        if (!tc_supported(d)) return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d %% 16 == 0, 16 <= d <= %d", tc_max_d());
+        *out = PATH_TC;
+        return SOT_OK;
+    }
+    if (prec != SOT_PREC_AUTO && prec != SOT_PREC_FP32) return fail(SOT_ERR_INVALID_ARG, "unknown precision flag");
+    if (d <= 3) { *out = PATH_POINT; return SOT_OK; }
+    if (prec == SOT_PREC_AUTO && tc_supported(d)) { *out = PATH_TC; return SOT_OK; }
+    if (d > dense_max_d()) return fail(SOT_ERR_UNSUPPORTED, "d = %d exceeds the fp32 path limit %d", d, dense_max_d());
+    *out = PATH_DENSE;
+    return SOT_OK;
+}
+
+int check_sizes(const float* X, const float* Y, int B, int n, int m, int d) {
+    if (B < 0 || n <= 0 || m <= 0 || d <= 0)
+        return fail(SOT_ERR_INVALID_ARG, "sizes must satisfy B >= 0, n, m, d >= 1 (got B=%d n=%d m=%d d=%d)", B, n, m, d);
+    if (B > 65535) return fail(SOT_ERR_INVALID_ARG, "B = %d exceeds 65535", B);
+    if ((long long)B * n * d >= (1LL << 40) || (long long)B * m * d >= (1LL << 40))
+        return fail(SOT_ERR_INVALID_ARG, "problem too large");
+    if ((long long)B * n >= (1LL << 31) || (long long)B * m >= (1LL << 31))
+        return fail(SOT_ERR_INVALID_ARG, "B*n and B*m must be < 2^31");
+    if (B > 0 && (!X || !Y)) return fail(SOT_ERR_INVALID_ARG, "X and Y must not be NULL");
+    return SOT_OK;
+}
+
+// Column split of one half-step: rows in tiles of rpc, columns in tiles of
+// cpt; choose the number of column chunks that keeps the SMs busy (fewest
+// "rounds" of resident CTAs per unit of work).
+void choose_split(int B, int nr, int nc, int rpc, int cpt, int sms, int occ, int* split, int* chunk, int* rowtiles) {
+    *rowtiles = (nr + rpc - 1) / rpc;
+    const long long base = (long long)B * *rowtiles;
+    const long long slots = (long long)sms * (occ > 0 ? occ : 1);
+    const int ntiles = (nc + cpt - 1) / cpt;
+    int smax = ntiles < 64 ? ntiles : 64;
+    double best = 1e300;
+    int bs = 1;
+    for (int s = 1; s <= smax; ++s) {
+        const long long units = base * s;
+        const double rounds = (double)((units + slots - 1) / slots);
+        const double t = rounds / s * (1.0 + 0.01 * (s - 1));
+        if (t < best * 0.999) { best = t; bs = s; }
+    }
+    const int tiles_per_chunk = (ntiles + bs - 1) / bs;
+    *chunk = tiles_per_chunk * cpt;
+    *split = (nc + *chunk - 1) / *chunk;
+}
+
+// Annealing stages: eps_k = max(eps, eps_init * factor^k); the first k with
+// eps_init * factor^k <= eps is the last (clamped) stage.
+std::vector<float> stages_of(const sot_schedule& s) {
+    std::vector<float> v;
+    const double e_min = s.eps;
+    if (!(s.eps_init > s.eps) || !(s.eps_factor > 0.f) || !(s.eps_factor < 1.f)) {
+        v.push_back(s.eps);
+        return v;
+    }
+    double e = s.eps_init;
+    for (;;) {
+        v.push_back((float)(e > e_min ? e : e_min));
+        if (e <= e_min || v.size() > 100000) break;
+        e *= (double)s.eps_factor;
+    }
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+struct Solver {
+    int B, n, m, d;
+    Path path;
+    cudaStream_t st;
+    const float *X, *Y, *a, *b;
+    Scratch S;
+    float *shift = nullptr, *xpack = nullptr, *ypack = nullptr, *lw2x = nullptr, *lw2y = nullptr;
+    float *nx = nullptr, *ny = nullptr;
+    float *L = nullptr, *Lnext = nullptr, *Lam = nullptr;
+    float *part_m = nullptr, *part_s = nullptr, *errpart = nullptr, *err = nullptr;
+    unsigned* counters = nullptr;
+    int* dflags = nullptr;  // [0] status, [1] stop, [2] conv, [3..] per-stage iteration counts
+    int nstage_slots = 0;
+    int sms;
+    int split[2], chunk[2], rowtiles[2];  // [0] f-half (rows X), [1] g-half (rows Y)
+    TcPlan tc;
+
+    Solver(const float* X_, const float* Y_, const float* a_, const float* b_, int B_, int n_, int m_, int d_, Path p,
+           cudaStream_t s)
+        : B(B_), n(n_), m(m_), d(d_), path(p), st(s), X(X_), Y(Y_), a(a_), b(b_), S(s) {
+        sms = device_sms();
+    }
+
+    int prepare(int stage_slots) {
+        nstage_slots = stage_slots;
+        const bool point = (path == PATH_POINT);
+        shift = S.alloc<float>((size_t)B * d);
+        nx = S.alloc<float>((size_t)B * n);
+        ny = S.alloc<float>((size_t)B * m);
+        L = S.alloc<float>((size_t)B * n);
+        Lam = S.alloc<float>((size_t)B * m);
+        dflags = S.alloc<int>(3 + stage_slots);
+        if (point) {
+            xpack = S.alloc<float>((size_t)B * n * 4);
+            ypack = S.alloc<float>((size_t)B * m * 4);
+        } else {
+            xpack = S.alloc<float>((size_t)B * n * d);
+            ypack = S.alloc<float>((size_t)B * m * d);
+            lw2x = S.alloc<float>((size_t)B * n);
+            lw2y = S.alloc<float>((size_t)B * m);
+        }
+        if (!shift || !nx || !ny || !L || !Lam || !dflags || !xpack || !ypack || (!point && (!lw2x || !lw2y)))
+            return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        SOT_CUDA(cudaMemsetAsync(dflags, 0, sizeof(int) * (3 + stage_slots), st));
+        SOT_CUDA(launch_center(X, Y, B, n, m, d, shift, st));
+        SOT_CUDA(launch_pack(X, a, B, n, d, shift, point, xpack, lw2x, nx, st));
+        SOT_CUDA(launch_pack(Y, b, B, m, d, shift, point, ypack, lw2y, ny, st));
+        // split plans for the two halves
+        for (int h = 0; h < 2; ++h) {
+            const int nr = h ? m : n, nc = h ? n : m;
+            if (path == PATH_POINT)
+                choose_split(B, nr, nc, point_rows_per_cta(), point_cols_per_tile(), sms, 4, &split[h], &chunk[h],
+                             &rowtiles[h]);
+            else if (path == PATH_DENSE)
+                choose_split(B, nr, nc, dense_rows_per_cta(), dense_cols_per_tile(), sms, 2, &split[h], &chunk[h],
+                             &rowtiles[h]);
+            else
+                choose_split(B, nr, nc, tc_rows_per_cta(), tc_cols_per_tile(), sms, 1, &split[h], &chunk[h],
+                             &rowtiles[h]);
+        }
+        const int smax = split[0] > split[1] ? split[0] : split[1];
+        const size_t rows_max = (size_t)B * (n > m ? n : m);
+        const int rt_max = rowtiles[0] > rowtiles[1] ? rowtiles[0] : rowtiles[1];
+        if (smax > 1) {
+            part_m = S.alloc<float>(rows_max * smax);
+            part_s = S.alloc<float>(rows_max * smax);
+            if (!part_m || !part_s) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        }
+        counters = S.alloc<unsigned>((size_t)B * rt_max);
+        errpart = S.alloc<float>((size_t)B * rt_max);
+        err = S.alloc<float>((size_t)B);
+        if (!counters || !errpart || !err) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        SOT_CUDA(cudaMemsetAsync(counters, 0, sizeof(unsigned) * B * rt_max, st));
+        if (path == PATH_TC) {
+            unsigned char* buf = S.alloc<unsigned char>(tc_scratch_bytes(B, n, m, d));
+            if (!buf) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+            cudaError_t e = tc_prepare(tc, buf, B, n, m, d, xpack, ypack, st);
+            if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "tensor-core operand preparation failed: %s", cudaGetErrorString(e));
+        }
+        return SOT_OK;
+    }
+
+    int* stop_flag() { return dflags + 1; }
+    int* conv_flag() { return dflags + 2; }
+
+    // One half-step.  h = 0: f-half (rows X, state L); h = 1: g-half (rows Y, state Lam).
+    int half(int h, int mode, float kappa, bool cold, const float* rin, float* rout, float* errp, bool guarded,
+             const float* cstate_override = nullptr) {
+        HalfArgs p;
+        p.B = B;
+        p.nr = h ? m : n;
+        p.nc = h ? n : m;
+        p.d = d;
+        p.rpack = h ? ypack : xpack;
+        p.cpack = h ? xpack : ypack;
+        p.cw2 = h ? lw2x : lw2y;
+        p.cstate = cstate_override ? cstate_override : (h ? L : Lam);
+        p.rstate_in = rin;
+        p.rstate_out = rout;
+        p.rweight = h ? b : a;
+        p.two_kappa = 2.f * kappa;
+        p.cold = cold ? 1 : 0;
+        p.split = split[h];
+        p.chunk = chunk[h];
+        p.rowtiles = rowtiles[h];
+        p.part_m = part_m;
+        p.part_s = part_s;
+        p.counters = counters;
+        p.errpart = errp;
+        p.stop_flag = guarded ? stop_flag() : nullptr;
+        p.status = dflags;
+        cudaError_t e;
+        {
+            ProfScope ps(st, mode == MODE_LSE);
+            if (path == PATH_POINT) e = launch_point_half(p, mode, st);
+            else if (path == PATH_DENSE) e = launch_dense_half(p, mode, st);
+            else e = launch_tc_half(tc, p, h, mode, st);
+        }
+        if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "half-step launch failed: %s", cudaGetErrorString(e));
+        return SOT_OK;
+    }
+
+    int init_states(const float* f, const float* g, float kappa) {
+        SOT_CUDA(launch_state_from_potential(nx, f, kappa, B * n, L, st));
+        SOT_CUDA(launch_state_from_potential(ny, g, kappa, B * m, Lam, st));
+        return SOT_OK;
+    }
+
+    int write_potentials(float* f, float* g, float kappa) {
+        SOT_CUDA(launch_potential_from_state(nx, L, kappa, B * n, f, st));
+        SOT_CUDA(launch_potential_from_state(ny, Lam, kappa, B * m, g, st));
+        return SOT_OK;
+    }
+
+    // Plain iteration: f-half then g-half, both in place.
+    int iterate(float kappa, bool cold, bool guarded) {
+        int rc = half(0, MODE_LSE, kappa, cold, L, L, nullptr, guarded);
+        if (rc) return rc;
+        return half(1, MODE_LSE, kappa, cold, Lam, Lam, nullptr, guarded);
+    }
+
+    // Stop-tested step: the f-half of the next iteration evaluates the
+    // row-marginal error of the current iterate; the decision either stops
+    // (keeping the current iterate) or commits that f-half.
+    int tested_fhalf(float kappa, float tol, int force) {
+        if (!Lnext) {
+            Lnext = S.alloc<float>((size_t)B * n);
+            if (!Lnext) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        }
+        int rc = half(0, MODE_LSE, kappa, false, L, Lnext, errpart, true);
+        if (rc) return rc;
+        SOT_CUDA(launch_decide(errpart, B, rowtiles[0], tol, force, err, stop_flag(), conv_flag(), Lnext, L, B * n, st));
+        return SOT_OK;
+    }
+};
+
+int read_flag(const int* dptr, cudaStream_t st, int* out) {
+    SOT_CUDA(cudaMemcpyAsync(out, dptr, sizeof(int), cudaMemcpyDeviceToHost, st));
+    SOT_CUDA(cudaStreamSynchronize(st));
+    return SOT_OK;
+}
+
+int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float* g0, float* f, float* g,
+                 sot_stats* stt) {
+    const std::vector<float> eps = stages_of(s);
+    const int K = (int)eps.size();
+    int rc = sv.prepare(K);
+    if (rc) return rc;
+    const bool warm = (s.flags & SOT_WARM_START) != 0;
+    const bool early = (s.flags & SOT_STAGE_EARLY_EXIT) != 0;
+    const bool testing = s.tol > 0.f;
+    const int ips = s.iters_per_stage;
+    const long long max_total = s.max_iters > 0 ? s.max_iters : (long long)ips * K;
+    bool cold = !warm;
+    if (warm) {
+        rc = sv.init_states(f0, g0, 1.f / (eps[0] * SOT_LN2_D));
+        if (rc) return rc;
+    }
+    std::vector<int> host_counts(K, -1);  // realised iterations of untested stages
+    long long total = 0;                  // iterations realised so far
+    int stages_done = 0;
+    bool stopped_all = false;
+    bool err_valid = false;
+    for (int k = 0; k < K && !stopped_all; ++k) {
+        if (total >= max_total) break;
+        const float kappa = 1.f / (eps[k] * SOT_LN2_D);
+        if (k > 0) {
+            const float ratio = eps[k - 1] / eps[k];
+            SOT_CUDA(launch_scale(sv.L, ratio, sv.B * sv.n, sv.st));
+            SOT_CUDA(launch_scale(sv.Lam, ratio, sv.B * sv.m, sv.st));
+        }
+        SOT_CUDA(cudaMemsetAsync(sv.stop_flag(), 0, 2 * sizeof(int), sv.st));  // stop + conv
+        stages_done = k + 1;
+        int* counter = sv.dflags + 3 + k;
+        const bool final_stage = (k == K - 1);
+        const bool test = testing && (early || final_stage);
+        if (!test) {
+            long long todo = ips;
+            if (total + todo > max_total) todo = max_total - total;
+            for (long long t = 0; t < todo; ++t) {
+                rc = sv.iterate(kappa, cold, false);
+                if (rc) return rc;
+                cold = false;
+            }
+            total += todo;
+            host_counts[k] = (int)todo;
+            continue;
+        }
+        // tested stage: first iteration plain, then tested iterations
+        const long long stage_cap = final_stage ? (max_total - total) : (long long)ips;
+        if (stage_cap <= 0) break;
+        rc = sv.iterate(kappa, cold, false);
+        if (rc) return rc;
+        cold = false;
+        SOT_CUDA(launch_count_iter(nullptr, counter, sv.st));
+        long long enq = 1;
+        const int chunk = 8;
+        int stopped = 0;
+        while (!stopped) {
+            if (enq >= stage_cap) {
+                if (final_stage) {
+                    // evaluate the error of the returned iterate and stop
+                    rc = sv.tested_fhalf(kappa, s.tol, 1);
+                    if (rc) return rc;
+                    err_valid = true;
+                }
+                break;
+            }
+            for (int c = 0; c < chunk && enq < stage_cap; ++c, ++enq) {
+                rc = sv.tested_fhalf(kappa, s.tol, 0);
+                if (rc) return rc;
+                rc = sv.half(1, MODE_LSE, kappa, false, sv.Lam, sv.Lam, nullptr, true);
+                if (rc) return rc;
+                SOT_CUDA(launch_count_iter(sv.stop_flag(), counter, sv.st));
+            }
+            if (final_stage) {
+                rc = read_flag(sv.stop_flag(), sv.st, &stopped);
+                if (rc) return rc;
+                if (stopped) err_valid = true;
+            }
+        }
+        int realised = 0;
+        rc = read_flag(counter, sv.st, &realised);
+        if (rc) return rc;
+        total += realised;
+        if (final_stage) {
+            int conv = 0;
+            rc = read_flag(sv.conv_flag(), sv.st, &conv);
+            if (rc) return rc;
+            if (stt) stt->converged = conv;
+            stopped_all = true;
+        }
+    }
+    const float kappa_f = 1.f / (eps[stages_done > 0 ? stages_done - 1 : 0] * SOT_LN2_D);
+    if (stt && !err_valid) {
+        // evaluate the marginal error of the returned iterate without changing it
+        SOT_CUDA(cudaMemsetAsync(sv.stop_flag(), 0, 2 * sizeof(int), sv.st));
+        rc = sv.tested_fhalf(kappa_f, -1.f, 1);
+        if (rc) return rc;
+    }
+    rc = sv.write_potentials(f, g, kappa_f);
+    if (rc) return rc;
+    if (stt) {
+        std::vector<int> counts(K > 0 ? K : 1, 0);
+        SOT_CUDA(cudaMemcpyAsync(counts.data(), sv.dflags + 3, sizeof(int) * K, cudaMemcpyDeviceToHost, sv.st));
+        std::vector<float> errs(sv.B > 0 ? sv.B : 1, NAN);
+        SOT_CUDA(cudaMemcpyAsync(errs.data(), sv.err, sizeof(float) * sv.B, cudaMemcpyDeviceToHost, sv.st));
+        SOT_CUDA(cudaStreamSynchronize(sv.st));
+        for (int k = 0; k < K; ++k)
+            if (host_counts[k] >= 0) counts[k] = host_counts[k];
+        long long tot = 0;
+        for (int k = 0; k < stages_done; ++k) tot += counts[k];
+        stt->iters_done = (int)tot;
+        stt->stages_done = stages_done;
+        if (!testing) stt->converged = 0;
+        stt->final_eps = eps[stages_done > 0 ? stages_done - 1 : 0];
+        if (stt->err_host)
+            for (int i = 0; i < sv.B; ++i) stt->err_host[i] = errs[i];
+        if (stt->stage_iters_host)
+            for (int k = 0; k < stt->stage_iters_cap && k < K; ++k)
+                stt->stage_iters_host[k] = k < stages_done ? counts[k] : 0;
+    }
+    return SOT_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+extern "C" {
+
+int sot_version(void) { return 100; }
+
+long long sot_kernel_launches(void) { return launches_total(); }
+
+int sot_select_path(int d, int flags) {
+    g_err[0] = 0;
+    if (d <= 0) return fail(SOT_ERR_INVALID_ARG, "d must be >= 1");
+    Path p;
+    int rc = choose_path(d, flags, &p);
+    return rc ? rc : (int)p;
+}
+
+const char* sot_last_error(void) { return g_err; }
+
+const char* sot_status_string(int status) {
+    switch (status) {
+        case SOT_OK: return "ok";
+        case SOT_ERR_INVALID_ARG: return "invalid argument";
+        case SOT_ERR_NONFINITE: return "non-finite input or non-positive weight";
+        case SOT_ERR_CAPACITY: return "COO capacity too small";
+        case SOT_ERR_TIMEOUT: return "device wait timed out";
+        case SOT_ERR_CUDA: return "CUDA error";
+        case SOT_ERR_UNSUPPORTED: return "unsupported configuration";
+        case SOT_ERR_NOMEM: return "out of device memory";
+        default: return "unknown status";
+    }
+}
+
+int sot_potentials_ex(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                      const sot_schedule* s, float* f, float* g, sot_stats* st, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!s) return fail(SOT_ERR_INVALID_ARG, "schedule must not be NULL");
+    if (!(s->eps > 0.f) || !std::isfinite(s->eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (s->iters_per_stage < 0) return fail(SOT_ERR_INVALID_ARG, "iters_per_stage must be >= 0");
+    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT))
+        return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
+    if (B > 0 && (!f || !g)) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
+    if (st && st->stage_iters_host && st->stage_iters_cap < 0) return fail(SOT_ERR_INVALID_ARG, "stage_iters_cap < 0");
+    if (B == 0) {
+        if (st) { st->iters_done = 0; st->stages_done = 0; st->converged = 0; st->final_eps = s->eps; }
+        return SOT_OK;
+    }
+    Path path;
+    rc = choose_path(d, s->flags, &path);
+    if (rc) return rc;
+    Solver sv(X, Y, a, b, B, n, m, d, path, (cudaStream_t)stream);
+    rc = run_schedule(sv, *s, f, g, f, g, st);
+    if (rc) return rc;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "%s", cudaGetErrorString(e));
+    return SOT_OK;
+}
+
+int sot_potentials(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                   float eps, int iters, float* f, float* g, void* stream) {
+    if (iters < 0) return fail(SOT_ERR_INVALID_ARG, "iters must be >= 0");
+    sot_schedule s;
+    s.eps = eps;
+    s.eps_init = eps;
+    s.eps_factor = 0.5f;
+    s.iters_per_stage = iters;
+    s.max_iters = iters;
+    s.tol = 0.f;
+    s.flags = 0;
+    return sot_potentials_ex(X, Y, a, b, B, n, m, d, &s, f, g, nullptr, stream);
+}
+
+int sot_plan_apply(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                   const float* f, const float* g, float eps, float* cost, float* grad, float* rowsum, int flags,
+                   void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (B > 0 && (!f || !g)) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
+    if (flags & ~SOT_PREC_MASK) return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
+    if (B == 0 || (!cost && !grad && !rowsum)) return SOT_OK;
+    Path path;
+    rc = choose_path(d, flags, &path);
+    if (rc) return rc;
+    if (path == PATH_TC && !tc_apply_supported(d)) path = PATH_DENSE;
+    cudaStream_t cs = (cudaStream_t)stream;
+    Solver sv(X, Y, a, b, B, n, m, d, path, cs);
+    rc = sv.prepare(0);
+    if (rc) return rc;
+    const float kappa = 1.f / (eps * SOT_LN2_D);
+    rc = sv.init_states(f, g, kappa);
+    if (rc) return rc;
+    ApplyArgs p;
+    p.B = B; p.n = n; p.m = m; p.d = d;
+    p.xpack = sv.xpack; p.ypack = sv.ypack; p.lw2x = sv.lw2x; p.lw2y = sv.lw2y;
+    p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam;
+    p.X = X; p.a = a; p.shift = sv.shift; p.kappa = kappa;
+    const int rpc = (sv.path == PATH_POINT) ? point_apply_rows_per_cta()
+                    : (sv.path == PATH_TC) ? tc_apply_rows_per_cta() : dense_apply_rows_per_cta();
+    p.rowtiles = (n + rpc - 1) / rpc;
+    float* cpart = nullptr;
+    if (cost) {
+        cpart = sv.S.alloc<float>((size_t)B * p.rowtiles);
+        if (!cpart) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    }
+    p.cost_part = cpart; p.grad = grad; p.rowsum = rowsum;
+    cudaError_t e;
+    if (sv.path == PATH_POINT) e = launch_point_apply(p, cs);
+    else if (sv.path == PATH_TC) e = launch_tc_apply(sv.tc, p, cs);
+    else e = launch_dense_apply(p, cs);
+    if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "plan-apply launch failed: %s", cudaGetErrorString(e));
+    if (cost) SOT_CUDA(launch_reduce_parts(cpart, B, p.rowtiles, cost, cs));
+    return SOT_OK;
+}
+
+int sot_cost(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+             const float* f, const float* g, float eps, float* cost, void* stream) {
+    if (B > 0 && !cost) return fail(SOT_ERR_INVALID_ARG, "cost must not be NULL");
+    return sot_plan_apply(X, Y, a, b, B, n, m, d, f, g, eps, cost, nullptr, nullptr, 0, stream);
+}
+int sot_grad_x(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+               const float* f, const float* g, float eps, float* grad, void* stream) {
+    if (B > 0 && !grad) return fail(SOT_ERR_INVALID_ARG, "grad must not be NULL");
+    return sot_plan_apply(X, Y, a, b, B, n, m, d, f, g, eps, nullptr, grad, nullptr, 0, stream);
+}
+int sot_cost_grad(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                  const float* f, const float* g, float eps, float* cost, float* grad, void* stream) {
+    if (B > 0 && (!cost || !grad)) return fail(SOT_ERR_INVALID_ARG, "cost and grad must not be NULL");
+    return sot_plan_apply(X, Y, a, b, B, n, m, d, f, g, eps, cost, grad, nullptr, 0, stream);
+}
+
+int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                 const float* f, const float* g, float eps, float threshold, int dirs, long long capacity, int* rows,
+                 int* cols, float* vals, long long* batch_offsets, long long* nnz_host, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!nnz_host) return fail(SOT_ERR_INVALID_ARG, "nnz_host must not be NULL");
+    *nnz_host = 0;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (!(threshold >= 0.f && threshold <= 1.f)) return fail(SOT_ERR_INVALID_ARG, "threshold must lie in [0, 1]");
+    if (dirs < 1 || dirs > 3) return fail(SOT_ERR_INVALID_ARG, "dirs must be 1, 2 or 3");
+    if (capacity < 0) return fail(SOT_ERR_INVALID_ARG, "capacity must be >= 0");
+    if (B > 0 && (!f || !g || !batch_offsets)) return fail(SOT_ERR_INVALID_ARG, "f, g, batch_offsets must not be NULL");
+    if (B == 0) return SOT_OK;
+    if (capacity > 0 && (!rows || !cols || !vals)) return fail(SOT_ERR_INVALID_ARG, "rows, cols, vals must not be NULL");
+    cudaStream_t cs = (cudaStream_t)stream;
+    Solver sv(X, Y, a, b, B, n, m, d, d <= 3 ? PATH_POINT : PATH_DENSE, cs);
+    if (d > dense_max_d()) return fail(SOT_ERR_UNSUPPORTED, "COO extraction supports d <= %d", dense_max_d());
+    rc = sv.prepare(0);
+    if (rc) return rc;
+    const float kappa = 1.f / (eps * SOT_LN2_D);
+    rc = sv.init_states(f, g, kappa);
+    if (rc) return rc;
+    float* Mr = sv.S.alloc<float>((size_t)B * n);
+    float* Mc = sv.S.alloc<float>((size_t)B * m);
+    int* counts = sv.S.alloc<int>((size_t)B * n);
+    long long* rowptr = sv.S.alloc<long long>((size_t)B * n + 1);
+    long long* dnnz = sv.S.alloc<long long>(1);
+    if (!Mr || !Mc || !counts || !rowptr || !dnnz) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    rc = sv.half(0, MODE_MAX, kappa, true, nullptr, Mr, nullptr, false);
+    if (rc) return rc;
+    rc = sv.half(1, MODE_MAX, kappa, true, nullptr, Mc, nullptr, false);
+    if (rc) return rc;
+    CooArgs p;
+    p.B = B; p.n = n; p.m = m; p.d = d;
+    p.xpack = sv.xpack; p.ypack = sv.ypack; p.lw2x = sv.lw2x; p.lw2y = sv.lw2y;
+    p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam; p.Mr = Mr; p.Mc = Mc; p.a = a;
+    p.two_kappa = 2.f * kappa; p.kappa = kappa;
+    p.log2tau = threshold > 0.f ? log2f(threshold) : -INFINITY;
+    p.dirs = dirs;
+    p.counts = counts; p.rowptr = rowptr; p.rows = rows; p.cols = cols; p.vals = vals;
+    p.capacity = capacity;
+    cudaError_t e = (d <= 3) ? launch_point_coo(p, 0, cs) : launch_dense_coo(p, 0, cs);
+    if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "COO count launch failed: %s", cudaGetErrorString(e));
+    SOT_CUDA(launch_scan_counts(counts, B, n, rowptr, batch_offsets, cs));
+    long long nnz = 0;
+    SOT_CUDA(cudaMemcpyAsync(&nnz, rowptr + (size_t)B * n, sizeof(long long), cudaMemcpyDeviceToHost, cs));
+    SOT_CUDA(cudaStreamSynchronize(cs));
+    *nnz_host = nnz;
+    if (nnz > capacity) return fail(SOT_ERR_CAPACITY, "COO needs %lld entries, capacity %lld", nnz, capacity);
+    if (nnz > 0) {
+        e = (d <= 3) ? launch_point_coo(p, 1, cs) : launch_dense_coo(p, 1, cs);
+        if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "COO write launch failed: %s", cudaGetErrorString(e));
+    }
+    return SOT_OK;
+}
+
+int sot_grad_x_coo(const float* X, const float* Y, int B, int n, int m, int d, const int* rows, const int* cols,
+                   const float* vals, const long long* batch_offsets, float* grad, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (B == 0) return SOT_OK;
+    if (!batch_offsets || !grad) return fail(SOT_ERR_INVALID_ARG, "batch_offsets and grad must not be NULL");
+    cudaStream_t cs = (cudaStream_t)stream;
+    Scratch S(cs);
+    int* status = S.alloc<int>(1);
+    if (!status) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    SOT_CUDA(cudaMemsetAsync(status, 0, sizeof(int), cs));
+    SOT_CUDA(launch_grad_coo(X, Y, B, n, m, d, rows, cols, vals, batch_offsets, grad, status, cs));
+    int h = 0;
+    SOT_CUDA(cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, cs));
+    SOT_CUDA(cudaStreamSynchronize(cs));
+    if (h & SOT_DEV_BAD_COO) return fail(SOT_ERR_INVALID_ARG, "COO not row-sorted within a cloud or index out of range");
+    return SOT_OK;
+}
+
+int sot_check_inputs(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                     void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (B == 0) return SOT_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    Scratch S(cs);
+    int* bad = S.alloc<int>(1);
+    if (!bad) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    SOT_CUDA(cudaMemsetAsync(bad, 0, sizeof(int), cs));
+    SOT_CUDA(launch_check_inputs(X, a, (long long)B * n, d, (long long)B * n, bad, cs));
+    SOT_CUDA(launch_check_inputs(Y, b, (long long)B * m, d, (long long)B * m, bad, cs));
+    int h = 0;
+    SOT_CUDA(cudaMemcpyAsync(&h, bad, sizeof(int), cudaMemcpyDeviceToHost, cs));
+    SOT_CUDA(cudaStreamSynchronize(cs));
+    if (h) return fail(SOT_ERR_NONFINITE, "%s", (h & 1) ? "non-finite coordinate" : "weight not finite or <= 0");
+    return SOT_OK;
+}
+
+int sot_profile_enable(int on) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    g_prof_on = on != 0;
+    return SOT_OK;
+}
+
+int sot_profile_read(long long* launches_host, double* total_ms_host) {
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pend;
+    {
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        pend.swap(g_prof_pending);
+    }
+    double ms = 0.0;
+    for (auto& pr : pend) {
+        if (cudaEventSynchronize(pr.second) != cudaSuccess) return fail(SOT_ERR_CUDA, "event synchronisation failed");
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, pr.first, pr.second) != cudaSuccess) return fail(SOT_ERR_CUDA, "event timing failed");
+        ms += t;
+    }
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    for (auto& pr : pend) {
+        g_prof_pool.push_back(pr.first);
+        g_prof_pool.push_back(pr.second);
+    }
+    g_prof_launches += (long long)pend.size();
+    g_prof_ms += ms;
+    if (launches_host) *launches_host = g_prof_launches;
+    if (total_ms_host) *total_ms_host = g_prof_ms;
+    g_prof_launches = 0;
+    g_prof_ms = 0.0;
+    return SOT_OK;
+}
+
+}  // extern "C"

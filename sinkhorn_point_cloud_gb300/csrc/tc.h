@@ -1,0 +1,30 @@
+// tc.h -- interface of the tcgen05 (5th-generation tensor core) Sinkhorn
+// path, k_tc.cu.  Internal to libsot.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace sot {
+
+// Operand images for the tensor-core half-steps, prepared once per call from
+// the centred coordinates.
+struct TcPlan {
+    int B = 0, n = 0, m = 0, d = 0;
+    unsigned char* xop = nullptr;  // row-side operand image of X
+    unsigned char* yop = nullptr;  // row-side operand image of Y
+};
+
+bool tc_supported(int d);
+int tc_max_d();
+int tc_rows_per_cta();
+int tc_cols_per_tile();
+size_t tc_scratch_bytes(int B, int n, int m, int d);
+cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m, int d, const float* xc,
+                       const float* yc, cudaStream_t st);
+cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st);
+bool tc_apply_supported(int d);
+int tc_apply_rows_per_cta();
+cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& p, cudaStream_t st);
+
+}  // namespace sot

@@ -1,0 +1,91 @@
+"""The C ABI library without a GPU: it builds, loads, exports every function
+include/sot.h declares, and its host-side argument checks answer before any
+CUDA call is made."""
+import ctypes as C
+
+import pytest
+
+from sinkhorn_point_cloud_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = binding.declared_functions()
+    assert len(names) >= 14
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sot_version() == 100
+    for code in range(0, -8, -1):
+        s = lib.sot_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.sot_status_string(-99).decode() == "unknown status"
+
+
+NULL = None
+
+
+def test_invalid_sizes_rejected_on_host(lib):
+    p = C.c_void_p(16)  # never dereferenced: the size check fails first
+    assert lib.sot_potentials(p, p, NULL, NULL, 1, 0, 5, 3, 0.1, 10, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert b"n, m, d" in lib.sot_last_error()
+    assert lib.sot_potentials(p, p, NULL, NULL, 1, 5, 0, 3, 0.1, 10, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_potentials(p, p, NULL, NULL, 1, 5, 5, 0, 0.1, 10, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_potentials(p, p, NULL, NULL, -1, 5, 5, 3, 0.1, 10, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_potentials(p, p, NULL, NULL, 1, 5, 5, 3, 0.1, -1, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_potentials(NULL, p, NULL, NULL, 1, 5, 5, 3, 0.1, 10, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+
+
+def test_invalid_eps_and_flags_rejected(lib):
+    p = C.c_void_p(16)
+    for eps in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.sot_potentials(p, p, NULL, NULL, 1, 5, 5, 3, eps, 10, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, 1 << 12)
+    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 3, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 3, NULL, p, p, NULL, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_plan_apply(p, p, NULL, NULL, 1, 5, 5, 3, p, p, 0.0, p, p, NULL, 0, NULL) == binding.SOT_ERR_INVALID_ARG
+
+
+def test_unsupported_precision_rejected(lib):
+    p = C.c_void_p(16)
+    s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, binding.SOT_PREC_F16X3)
+    # d = 3 has no tensor-core path
+    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 3, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
+    s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, 0)
+    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 300, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
+
+
+def test_coo_argument_checks(lib):
+    p = C.c_void_p(16)
+    nnz = C.c_longlong(123)
+    assert lib.sot_plan_coo(p, p, NULL, NULL, 1, 5, 5, 3, p, p, 0.1, 1.5, 3, 10, p, p, p, p, C.byref(nnz), NULL) \
+        == binding.SOT_ERR_INVALID_ARG
+    assert nnz.value == 0
+    assert lib.sot_plan_coo(p, p, NULL, NULL, 1, 5, 5, 3, p, p, 0.1, 1e-8, 0, 10, p, p, p, p, C.byref(nnz), NULL) \
+        == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_plan_coo(p, p, NULL, NULL, 1, 5, 5, 3, p, p, 0.1, 1e-8, 3, -1, p, p, p, p, C.byref(nnz), NULL) \
+        == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_plan_coo(p, p, NULL, NULL, 1, 5, 5, 3, p, p, 0.1, 1e-8, 3, 10, p, p, p, p, NULL, NULL) \
+        == binding.SOT_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert lib.sot_potentials(NULL, NULL, NULL, NULL, 0, 5, 5, 3, 0.1, 10, NULL, NULL, NULL) == binding.SOT_OK
+    nnz = C.c_longlong(7)
+    assert lib.sot_plan_coo(NULL, NULL, NULL, NULL, 0, 5, 5, 3, NULL, NULL, 0.1, 1e-8, 3, 0, NULL, NULL, NULL, NULL,
+                            C.byref(nnz), NULL) == binding.SOT_OK
+    assert nnz.value == 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    X = torch.zeros(1, 4, 3)
+    with pytest.raises(ValueError):
+        binding.sot_potentials(X, X, eps=0.1, iters=1)
