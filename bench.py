@@ -49,6 +49,24 @@ def peaks():
         "fallback"
 
 
+def alu_rates():
+    """Measured per-SM-per-clock rates of MUFU ex2, FFMA lanes and packed f32x2
+    FMA lanes (libsotpeaks probes), or None if the probe library is absent."""
+    import ctypes as C
+    from sinkhorn_point_cloud_gb300 import build
+    if not os.path.exists(build.PEAKS_LIB):
+        return None
+    L = C.CDLL(build.PEAKS_LIB)
+    L.sotpeaks_measure.argtypes = [C.c_int, C.POINTER(C.c_double)]
+    out = {}
+    for kind, name in ((0, "ex2_per_sm_clk"), (1, "ffma_lanes_per_sm_clk"), (2, "ffma2_lanes_per_sm_clk")):
+        v = C.c_double(0)
+        if L.sotpeaks_measure(kind, C.byref(v)) != 0:
+            return None
+        out[name] = round(v.value, 2)
+    return out
+
+
 # ---- clocks ---------------------------------------------------------------
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -269,23 +287,34 @@ def run_gpu(args, ws, rank, local):
     per_launch_ms = half_ms / max(nl, 1)
     per_launch_pairs = B * n * m
     mhz = float(pk.get("sm_max_mhz", 2070.0))
+    rates = alu_rates()
+    secs = per_launch_ms / 1e3
+    mufu = None
+    if rates:
+        mufu_peak = rates["ex2_per_sm_clk"] * sms * mhz * 1e6
+        mufu = {"achieved_ex2_per_s": per_launch_pairs / secs, "peak_ex2_per_s": mufu_peak,
+                "frac": per_launch_pairs / secs / mufu_peak}
     if sot.sot_select_path(d, flags) == 2:
-        flops_pair = 3 * 2 * d  # fp16 hi*hi + hi*lo + lo*hi products
-        achieved = flops_pair * per_launch_pairs / (per_launch_ms / 1e3) / 1e12
-        peak = float(pk["bf16_tflops"])
+        flops_pair = 3 * 2 * d  # fp16 products hi*hi + hi*lo + lo*hi, 2 flops per multiply-add
+        achieved = flops_pair * per_launch_pairs / secs / 1e12
+        peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None,
-                "peak_source": f"{pk_kind} bf16 dense (fp16 has the same nominal rate)",
-                "kernel": "tcgen05 f16x3 half-step"}
+                "peak_source": f"{pk_kind} sustained bf16 dense GEMM (fp16 has the same nominal rate)",
+                "kernel": "tc_half_kernel (tcgen05 kind::f16, 3 products per pair)"}
         dtype = "f16x3"
     else:
         flops_pair = 2 * d  # one FMA per coordinate
-        achieved = flops_pair * per_launch_pairs / (per_launch_ms / 1e3) / 1e12
-        peak = 2 * 128 * sms * mhz * 1e6 / 1e12  # FP32 FMA lanes x 2 flops x SMs x max clock
+        achieved = flops_pair * per_launch_pairs / secs / 1e12
+        lanes = rates["ffma_lanes_per_sm_clk"] if rates else 128.0
+        peak = 2 * lanes * sms * mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "peak_source": f"128 FP32 lanes/SM x {sms} SMs x {mhz:.0f} MHz x 2",
-                "kernel": "fp32 FMA half-step"}
+                "traffic": None,
+                "peak_source": f"{'measured' if rates else 'nominal'} {lanes:.0f} FP32 FMA lanes/SM/clk x {sms} SMs x "
+                               f"{mhz:.0f} MHz x 2", "kernel": "dense_half_kernel (fp32 FMA)"}
         dtype = "f32"
+    roof["mufu"] = mufu
+    roof["alu_rates"] = rates
     # CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if not args.no_cpu_baseline:

@@ -19,6 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsot.so")
+PEAKS_LIB = os.path.join(BUILD, "libsotpeaks.so")
+PEAKS_SRC = "peaks.cu"  # throughput probes for the benchmark; not part of libsot
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}"]
 
@@ -34,15 +36,15 @@ def nvcc_path() -> str:
 
 
 def _inputs():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu"))), \
+    return sorted(f for f in glob.glob(os.path.join(CSRC, "*.cu")) if os.path.basename(f) != PEAKS_SRC), \
         sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) +
                glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(PEAKS_LIB):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(PEAKS_LIB))
     srcs, hdrs = _inputs()
     return any(os.path.getmtime(f) > t for f in srcs + hdrs + [__file__])
 
@@ -66,8 +68,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(r.stdout, r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(compile_one, srcs))
+    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs) + 1, os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(compile_one, srcs + [os.path.join(CSRC, PEAKS_SRC)]))
+    peaks_obj = objs.pop()
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", PEAKS_LIB + ".tmp", peaks_obj], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(PEAKS_LIB + ".tmp", PEAKS_LIB)
     tmp = LIB + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

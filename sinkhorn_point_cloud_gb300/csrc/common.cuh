@@ -101,3 +101,4 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
 // Device status bits (OR-ed into a status word).
 #define SOT_DEV_RETRY_ROWS 1  /* some rows took the slow full-row recompute */
 #define SOT_DEV_BAD_COO 2     /* COO input unsorted / out of range */
+#define SOT_DEV_TIMEOUT 4     /* a bounded device-side wait gave up */

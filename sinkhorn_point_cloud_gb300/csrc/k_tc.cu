@@ -1,21 +1,485 @@
-// k_tc.cu -- tcgen05 tensor-core half-steps (placeholder: no tensor-core
-// kernel is compiled in yet, so tc_supported() is false and every dimension
-// takes the fp32 paths).
+// k_tc.cu -- Sinkhorn half-steps on the 5th-generation tensor cores
+// (tcgen05, kind::f16) for d = 64.
+//
+// The half-step ("FlashSinkhorn", Methodologie 1-2) needs the dot products
+// x_i . y_j of every (row, column) pair: a dense contraction over d = 64, so it
+// runs on the tensor cores.  Single-pass fp16 (or tf32) products carry 11
+// significant bits, which moves the gradient of the n = 70000 problem by
+// ~3e-2 relative; fp32 accuracy comes from splitting every coordinate into
+// an fp16 pair v = hi + lo and summing hi*hi + hi*lo + lo*hi (the lo*lo term
+// is below fp32 rounding), all accumulated in fp32 in TMEM.
+//
+// CTA layout (one CTA per SM; 320 threads):
+//   warp 0      producer: bulk copies (TMA engine) of 128-column operand tiles
+//               into a 4-stage shared-memory ring, plus the column biases
+//               c_j = log2 w_j - Lam_j of each tile;
+//   warp 1      MMA issuer (one thread) and TMEM owner (512 columns);
+//   warps 2-9   two warpgroups, one per 128-row tile: tcgen05.ld of the fp32
+//               accumulator, score = acc * 2 kappa / s^2 + c_j, ex2, row sums.
+// The 256 rows of the CTA stay resident (row-stationary); every column tile
+// is used by both row tiles (12 MMAs of 128 x 128 x 16 each) before its stage
+// is released.  Accumulators are double-buffered per row tile so the MMAs of
+// tile t+1 overlap the exponentials of tile t.
+//
+// Operands live in HBM as images of the exact shared-memory layout (128-byte
+// swizzle, K-major): per 128 points, 16 KB of hi parts then 16 KB of lo parts,
+// so one 1-D bulk copy moves a whole tile.  Coordinates are scaled per cloud by
+// a power of two s (max |s x| in (256, 512]) before the split; the epilogue
+// divides by s^2.
+//
+// Every mbarrier wait is bounded (2 s of wall time, or as soon as another role
+// gave up); a CTA that gives up poisons its rows with NaN, sets the device
+// timeout bit, drains its own bulk copies, frees TMEM and returns.
+#include <cuda_fp16.h>
+
+#include "common.cuh"
 #include "tc.h"
+#include "tc_ptx.cuh"
 
 namespace sot {
 
-bool tc_supported(int) { return false; }
-int tc_max_d() { return 0; }
-int tc_rows_per_cta() { return 128; }
-int tc_cols_per_tile() { return 128; }
-size_t tc_scratch_bytes(int, int, int, int) { return 0; }
-cudaError_t tc_prepare(TcPlan&, unsigned char*, int, int, int, int, const float*, const float*, cudaStream_t) {
-    return cudaErrorNotSupported;
-}
-cudaError_t launch_tc_half(const TcPlan&, const HalfArgs&, int, int, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int TC_D = 64;
+constexpr int TC_M = 128;             // rows per row tile (MMA M)
+constexpr int TC_ROWS = 2 * TC_M;     // rows per CTA
+constexpr int TC_N = 128;             // columns per tile (MMA N)
+constexpr int TC_S = 4;               // pipeline stages
+constexpr int TC_THREADS = 320;
+constexpr uint32_t TILE_BYTES = 16384;          // 128 x 64 fp16, one swizzled K-block
+constexpr uint32_t OP_BYTES = 2 * TILE_BYTES;   // hi + lo
+constexpr uint32_t OFF_A = 0;                           // [2 row tiles][hi, lo]
+constexpr uint32_t OFF_B = OFF_A + 2 * OP_BYTES;        // [TC_S][hi, lo]
+constexpr uint32_t OFF_BIAS = OFF_B + TC_S * OP_BYTES;  // [TC_S][TC_N] float
+constexpr uint32_t OFF_BAR = OFF_BIAS + TC_S * TC_N * 4;
+constexpr uint32_t NBAR = 17;
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last
+constexpr uint32_t OFF_RED = OFF_MISC + 16;             // 16 floats
+constexpr uint32_t OFF_RETRY = OFF_RED + 64;            // TC_ROWS ints
+constexpr uint32_t TC_SMEM = OFF_RETRY + TC_ROWS * 4 + 1024;  // + alignment slack
+constexpr uint64_t TC_WAIT_NS = 2000000000ull;
+
+// barrier indices
+__host__ __device__ constexpr int BAR_FULL(int s) { return s; }
+__host__ __device__ constexpr int BAR_EMPTY(int s) { return TC_S + s; }
+__host__ __device__ constexpr int BAR_ACCFULL(int r, int u) { return 2 * TC_S + 2 * r + u; }
+__host__ __device__ constexpr int BAR_ACCEMPTY(int r, int u) { return 2 * TC_S + 4 + 2 * r + u; }
+__host__ __device__ constexpr int BAR_A() { return 2 * TC_S + 8; }
+static_assert(BAR_A() + 1 == (int)NBAR, "barrier count");
+static_assert(TC_SMEM <= 227 * 1024, "shared memory budget");
+
+bool tc_supported(int d) { return d == TC_D; }
+int tc_max_d() { return TC_D; }
+int tc_rows_per_cta() { return TC_ROWS; }
+int tc_cols_per_tile() { return TC_N; }
 bool tc_apply_supported(int) { return false; }
-int tc_apply_rows_per_cta() { return 128; }
+int tc_apply_rows_per_cta() { return TC_ROWS; }
+
+static inline int tc_tiles(int n) { return 2 * ((n + TC_ROWS - 1) / TC_ROWS); }
+
+size_t tc_scratch_bytes(int B, int n, int m, int d) {
+    (void)d;
+    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 8;
+}
+
+// ---- operand images -----------------------------------------------------------
+__global__ void tc_maxabs_kernel(const float* xc, long long nx, const float* yc, long long ny, unsigned* maxbits) {
+    const int b = blockIdx.y;
+    const float* xb = xc + (size_t)b * nx;
+    const float* yb = yc + (size_t)b * ny;
+    float mx = 0.f;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < nx; e += (long long)gridDim.x * blockDim.x)
+        mx = fmaxf(mx, fabsf(xb[e]));
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < ny; e += (long long)gridDim.x * blockDim.x)
+        mx = fmaxf(mx, fabsf(yb[e]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) atomicMax(maxbits + b, __float_as_uint(mx));
+}
+
+// scale[b] = 2^e with max|s x| in (256, 512]; exact power of two.
+__device__ __forceinline__ float tc_scale_of(unsigned bits) {
+    const float mx = __uint_as_float(bits);
+    if (!(mx > 0.f) || !isfinite(mx)) return 1.f;
+    int e;
+    frexpf(mx, &e);  // mx = f * 2^e, f in [0.5, 1)
+    return ldexpf(1.f, 9 - e);
+}
+
+// One thread per point (row of a 128-row tile): 8 chunks of 8 fp16 for hi and lo.
+__global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigned* maxbits, float* scale,
+                                unsigned char* img) {
+    const int b = blockIdx.y;
+    const int tile = blockIdx.x;
+    const int r = threadIdx.x;
+    const int p = tile * TC_M + r;
+    const float s = tc_scale_of(maxbits[b]);
+    if (tile == 0 && r == 0) scale[b] = s;
+    unsigned char* hi = img + ((size_t)b * tiles + tile) * OP_BYTES;
+    unsigned char* lo = hi + TILE_BYTES;
+    const float* src = pc + ((size_t)b * n + p) * TC_D;
+#pragma unroll
+    for (int c = 0; c < TC_D / 8; ++c) {
+        __align__(16) __half h[8], l[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float v = (p < n) ? src[8 * c + k] * s : 0.f;
+            const __half hv = __float2half_rn(v);
+            h[k] = hv;
+            l[k] = __float2half_rn(v - __half2float(hv));
+        }
+        const uint32_t off = sw128_offset(r, 8 * c);
+        *reinterpret_cast<uint4*>(hi + off) = *reinterpret_cast<const uint4*>(h);
+        *reinterpret_cast<uint4*>(lo + off) = *reinterpret_cast<const uint4*>(l);
+    }
+}
+
+cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m, int d, const float* xc,
+                       const float* yc, cudaStream_t st) {
+    if (d != TC_D) return cudaErrorInvalidValue;
+    plan.B = B; plan.n = n; plan.m = m; plan.d = d;
+    plan.tiles_x = tc_tiles(n);
+    plan.tiles_y = tc_tiles(m);
+    uintptr_t base = ((uintptr_t)scratch + 255) & ~(uintptr_t)255;
+    plan.xop = reinterpret_cast<unsigned char*>(base);
+    plan.yop = plan.xop + (size_t)B * plan.tiles_x * OP_BYTES;
+    unsigned* maxbits = reinterpret_cast<unsigned*>(plan.yop + (size_t)B * plan.tiles_y * OP_BYTES);
+    plan.scale = reinterpret_cast<float*>(maxbits + B);
+    cudaError_t e = cudaMemsetAsync(maxbits, 0, sizeof(unsigned) * B, st);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    tc_maxabs_kernel<<<dim3(64, B), 256, 0, st>>>(xc, (long long)n * d, yc, (long long)m * d, maxbits);
+    count_launches(1);
+    tc_image_kernel<<<dim3(plan.tiles_x, B), TC_M, 0, st>>>(xc, n, plan.tiles_x, maxbits, plan.scale, plan.xop);
+    count_launches(1);
+    tc_image_kernel<<<dim3(plan.tiles_y, B), TC_M, 0, st>>>(yc, m, plan.tiles_y, maxbits, plan.scale, plan.yop);
+    return cudaGetLastError();
+}
+
+// ---- the half-step ----------------------------------------------------------------
+struct TcOps {
+    const unsigned char* aimg;  // row-side image
+    const unsigned char* bimg;  // column-side image
+    const float* scale;
+    int tiles_r, tiles_c;
+};
+
+__device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc,
+                             int row, float tk, float* red) {
+    const float* xr = rows + (size_t)row * TC_D;
+    float mx = -INFINITY;
+    for (int j = threadIdx.x; j < nc; j += TC_THREADS) {
+        const float* y = cols + (size_t)j * TC_D;
+        float acc = 0.f;
+        for (int k = 0; k < TC_D; ++k) acc = fmaf(xr[k], y[k], acc);
+        mx = fmaxf(mx, fmaf(tk, acc, cw[j] - cst[j]));
+    }
+    mx = block_max<TC_THREADS>(mx, red);
+    if (mx == -INFINITY) return -INFINITY;
+    float sm = 0.f;
+    for (int j = threadIdx.x; j < nc; j += TC_THREADS) {
+        const float* y = cols + (size_t)j * TC_D;
+        float acc = 0.f;
+        for (int k = 0; k < TC_D; ++k) acc = fmaf(xr[k], y[k], acc);
+        sm += ex2f(fmaf(tk, acc, cw[j] - cst[j]) - mx);
+    }
+    sm = block_sum<TC_THREADS>(sm, red);
+    return mx + log2f(sm);
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOps ops) {
+    if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    unsigned char* sm = smem_raw + (sbase - raw);
+    float* bias = reinterpret_cast<float*>(sm + OFF_BIAS);
+    int* misc = reinterpret_cast<int*>(sm + OFF_MISC);  // [0] tmem, [1] abort, [2] nretry, [3] last
+    volatile int* abort = misc + 1;
+    float* red = reinterpret_cast<float*>(sm + OFF_RED);
+    int* retry = reinterpret_cast<int*>(sm + OFF_RETRY);
+    auto BAR = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int rb = blockIdx.x / p.split, ch = blockIdx.x % p.split;
+    const int row0 = rb * TC_ROWS;
+    const int c_begin = ch * p.chunk;
+    const int c_end = min(p.nc, c_begin + p.chunk);
+    const int t0 = c_begin / TC_N;
+    const int nt = (c_end - c_begin + TC_N - 1) / TC_N;
+    const float* cw = p.cw2 + (size_t)b * p.nc;
+    const float* cst = p.cstate + (size_t)b * p.nc;
+    const size_t rbase = (size_t)b * p.nr;
+    const float sc = ops.scale[b];
+    const float tk = p.two_kappa / (sc * sc);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_S; ++s) {
+            mbar_init(BAR(BAR_FULL(s)), 32);
+            mbar_init(BAR(BAR_EMPTY(s)), 1 + 8);
+        }
+        for (int r = 0; r < 2; ++r)
+            for (int u = 0; u < 2; ++u) {
+                mbar_init(BAR(BAR_ACCFULL(r, u)), 1);
+                mbar_init(BAR(BAR_ACCEMPTY(r, u)), 4);
+            }
+        mbar_init(BAR(BAR_A()), 1);
+        misc[1] = 0;
+        misc[2] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + OFF_MISC, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)misc[0];
+
+    float m = 0.f, s = 0.f;  // epilogue row state
+    const int ew = warp - 2;
+    const int wg = ew >> 2;      // row tile of this epilogue warp
+    const int q4 = warp & 3;     // TMEM lane quarter this warp may access
+    const int rl = wg * TC_M + q4 * 32 + lane;
+    const int row = row0 + rl;
+    const bool erow = (warp >= 2) && row < p.nr;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        int issued = 0;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(BAR(BAR_A()), 2 * OP_BYTES);
+            bulk_g2s(sbase + OFF_A, ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES, 2 * OP_BYTES,
+                     BAR(BAR_A()));
+        }
+        const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
+        for (int lt = 0; lt < nt; ++lt) {
+            const int st = lt % TC_S;
+            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+            if (!mbar_wait_bounded(BAR(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
+            const int jt = (t0 + lt) * TC_N;
+            for (int c = lane; c < TC_N; c += 32) {
+                const int j = jt + c;
+                bias[st * TC_N + c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(BAR(BAR_FULL(st)), OP_BYTES);
+                bulk_g2s(sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, OP_BYTES,
+                         BAR(BAR_FULL(st)));
+            } else {
+                mbar_arrive(BAR(BAR_FULL(st)));
+            }
+            issued = lt + 1;
+        }
+        // drain: never leave a bulk copy in flight into this CTA's shared memory
+        if (lane == 0) {
+            int dummy = 0;
+            for (int lt = (issued > TC_S ? issued - TC_S : 0); lt < issued; ++lt)
+                mbar_wait_bounded(BAR(BAR_FULL(lt % TC_S)), (uint32_t)(lt / TC_S) & 1u, (volatile int*)&dummy,
+                                  TC_WAIT_NS);
+            mbar_wait_bounded(BAR(BAR_A()), 0u, (volatile int*)&dummy, TC_WAIT_NS);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(BAR(BAR_A()), 0u, abort, TC_WAIT_NS);
+            const uint32_t idesc = f16_idesc(TC_M, TC_N);
+            for (int lt = 0; ok && lt < nt; ++lt) {
+                const int st = lt % TC_S;
+                const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+                const int u = lt & 1;
+                const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
+                if (!mbar_wait_bounded(BAR(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+                for (int r = 0; r < 2 && ok; ++r) {
+                    if (!mbar_wait_bounded(BAR(BAR_ACCEMPTY(r, u)), pu ^ 1u, abort, TC_WAIT_NS)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
+                    const uint32_t ahi = sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
+                    const uint32_t bhi = sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < TC_D / 16; ++k) {
+                        const uint32_t ko = 32u * (uint32_t)k;
+                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
+                        tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    }
+#pragma unroll
+                    for (int k = 0; k < TC_D / 16; ++k) {
+                        const uint32_t ko = 32u * (uint32_t)k;
+                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    }
+                    tc_commit(BAR(BAR_ACCFULL(r, u)));
+                }
+                if (!ok) break;
+                tc_commit(BAR(BAR_EMPTY(st)));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: exponentials and row sums ----------------
+        m = erow ? (p.cold ? -INFINITY : p.rstate_in[rbase + row] - SOT_STAB_BIAS) : INFINITY;
+        s = 0.f;
+        const float2 tk2 = make_float2(tk, tk);
+        for (int lt = 0; lt < nt; ++lt) {
+            const int st = lt % TC_S;
+            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+            const int u = lt & 1;
+            const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
+            if (!mbar_wait_bounded(BAR(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(BAR(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
+            const float* cb = bias + st * TC_N;
+            const float2 nm2 = make_float2(-m, -m);
+            float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll 1
+            for (int q = 0; q < TC_N / 32; ++q) {
+                float v[32];
+                tmem_ld32(tb + 32u * (uint32_t)q, v);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(cb + 32 * q + j);
+                    float2 t = ffma2(make_float2(v[j], v[j + 1]), tk2, make_float2(c4.x, c4.y));
+                    t = fadd2(t, nm2);
+                    acc2 = fadd2(acc2, make_float2(ex2f(t.x), ex2f(t.y)));
+                    t = ffma2(make_float2(v[j + 2], v[j + 3]), tk2, make_float2(c4.z, c4.w));
+                    t = fadd2(t, nm2);
+                    acc2 = fadd2(acc2, make_float2(ex2f(t.x), ex2f(t.y)));
+                }
+            }
+            float ts = acc2.x + acc2.y;
+            const bool ovf = !(ts < SOT_TILE_SUM_MAX);
+            if (__any_sync(0xffffffffu, ovf)) {
+                // warp-uniform slow path: re-stabilise overflowing rows on the tile maximum
+                float mt = -INFINITY;
+#pragma unroll 1
+                for (int q = 0; q < TC_N / 32; ++q) {
+                    float v[32];
+                    tmem_ld32(tb + 32u * (uint32_t)q, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, fmaf(v[j], tk, cb[32 * q + j]));
+                }
+                const float mn = fmaxf(m, mt);
+                if (ovf) {
+                    if (mn == -INFINITY) {
+                        ts = 0.f;
+                    } else {
+                        s = (m == -INFINITY) ? 0.f : s * ex2f(m - mn);
+                        m = mn;
+                    }
+                }
+                float ts2 = 0.f;
+#pragma unroll 1
+                for (int q = 0; q < TC_N / 32; ++q) {
+                    float v[32];
+                    tmem_ld32(tb + 32u * (uint32_t)q, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ts2 += ex2f(fmaf(v[j], tk, cb[32 * q + j]) - m);
+                }
+                if (ovf && mn > -INFINITY) ts = ts2;
+            }
+            s += ts;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(BAR(BAR_ACCEMPTY(wg, u)));
+                mbar_arrive(BAR(BAR_EMPTY(st)));
+            }
+        }
+    }
+
+    // ---------------- all roles done: free TMEM, combine, finalise -------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    const bool aborted = *abort != 0;
+    if (aborted) {
+        m = NAN;
+        s = NAN;
+        if (threadIdx.x == 0) atomicOr(p.status, SOT_DEV_TIMEOUT);
+    }
+    if (p.split > 1) {
+        const size_t stride = (size_t)p.B * p.nr;
+        if (erow) {
+            p.part_m[ch * stride + rbase + row] = m;
+            p.part_s[ch * stride + rbase + row] = s;
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned prev = atomicAdd(&p.counters[b * p.rowtiles + rb], 1u);
+            misc[3] = (prev == (unsigned)(p.split - 1));
+        }
+        __syncthreads();
+        if (!misc[3]) return;
+        __threadfence();
+        if (erow) {
+            float M = -INFINITY, S = 0.f;
+            bool nan = false;
+            for (int c = 0; c < p.split; ++c) {
+                const float pm = __ldcg(p.part_m + c * stride + rbase + row);
+                const float ps = __ldcg(p.part_s + c * stride + rbase + row);
+                if (pm != pm || ps != ps) nan = true;
+                lse_combine(M, S, pm, ps);
+            }
+            m = nan ? NAN : M;
+            s = nan ? NAN : S;
+        }
+        if (threadIdx.x == 0) p.counters[b * p.rowtiles + rb] = 0u;
+    }
+    if (threadIdx.x == 0) misc[2] = 0;
+    __syncthreads();
+    if (erow) {
+        if (m != m || s != s) {
+            p.rstate_out[rbase + row] = NAN;
+        } else if (s >= SOT_SUM_MIN && s < INFINITY && m > -INFINITY) {
+            p.rstate_out[rbase + row] = m + log2f(s);
+        } else {
+            retry[atomicAdd(&misc[2], 1)] = row;
+        }
+    }
+    __syncthreads();
+    const int nretry = misc[2];
+    const float* rows_fp32 = p.rpack + (size_t)b * p.nr * TC_D;
+    const float* cols_fp32 = p.cpack + (size_t)b * p.nc * TC_D;
+    for (int k = 0; k < nretry; ++k) {
+        const int r = retry[k];
+        const float v = tc_row_full(rows_fp32, cols_fp32, cw, cst, p.nc, r, p.two_kappa, red);
+        if (threadIdx.x == 0) {
+            p.rstate_out[rbase + r] = v;
+            atomicOr(p.status, SOT_DEV_RETRY_ROWS);
+        }
+    }
+    if (p.errpart) {
+        __syncthreads();
+        float e = 0.f;
+        if (erow) {
+            const float w = p.rweight ? p.rweight[rbase + row] : 1.f / (float)p.nr;
+            e = w * fabsf(ex2f(p.rstate_out[rbase + row] - p.rstate_in[rbase + row]) - 1.f);
+        }
+        e = block_sum<TC_THREADS>(e, red);
+        if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rb] = e;
+    }
+}
+
+cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st) {
+    if (mode != MODE_LSE || p.d != TC_D) return cudaErrorInvalidValue;
+    TcOps ops;
+    ops.aimg = h ? plan.yop : plan.xop;
+    ops.bimg = h ? plan.xop : plan.yop;
+    ops.scale = plan.scale;
+    ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
+    ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
+    cudaError_t e = cudaFuncSetAttribute(tc_half_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.rowtiles * p.split, p.B), block(TC_THREADS);
+    count_launches(1);
+    tc_half_kernel<<<grid, block, TC_SMEM, st>>>(p, ops);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_tc_apply(const TcPlan&, const ApplyArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 
 }  // namespace sot

@@ -11,8 +11,10 @@ namespace sot {
 // the centred coordinates.
 struct TcPlan {
     int B = 0, n = 0, m = 0, d = 0;
-    unsigned char* xop = nullptr;  // row-side operand image of X
-    unsigned char* yop = nullptr;  // row-side operand image of Y
+    int tiles_x = 0, tiles_y = 0;  // 128-point tiles per cloud in each image (even count)
+    unsigned char* xop = nullptr;  // operand image of X: per tile 16 KB fp16 hi + 16 KB fp16 lo, swizzled
+    unsigned char* yop = nullptr;  // operand image of Y
+    float* scale = nullptr;        // [B] power-of-two coordinate scale used by the images
 };
 
 bool tc_supported(int d);

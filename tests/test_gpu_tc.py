@@ -1,0 +1,92 @@
+"""The tcgen05 tensor-core path (d = 64, fp16 x3 products) vs the fp64 oracle.
+
+Reduced sizes span several 256-row blocks, several 128-column tiles and
+ragged tails; the full n = m = 70000 configuration (the one bench.py times) is
+checked on sampled rows of the first half-step, which the oracle computes
+from X, Y and b alone, and on column marginals after 100 iterations.
+"""
+import numpy as np
+import pytest
+
+from gpu_util import TOL, dev, host, normwise, potentials_error
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sot():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sinkhorn_point_cloud_gb300 as s
+    from sinkhorn_point_cloud_gb300 import build
+    build.build()
+    if s.sot_select_path(64, s.SOT_PREC_F16X3) != 2:
+        pytest.skip("tensor-core path not built")
+    return s
+
+
+@pytest.mark.parametrize("n,m,B", [(1000, 1100, 1), (300, 257, 2), (513, 129, 1)])
+def test_tc_matches_oracle(sot, orc, n, m, B):
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=B, n=n, m=m, d=64)
+    eps, iters = 0.1, 100
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    f, g = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=iters, max_iters=iters,
+                                 flags=sot.SOT_PREC_F16X3)
+    c, gr, _ = sot.sot_plan_apply(Xd, Yd, ad, bd, f, g, eps)
+    f, g, c, gr = host(f), host(g), host(c), host(gr)
+    ef = eg = ec = egr = 0.0
+    for k in range(B):
+        fr, gref = orc.sinkhorn(X[k], Y[k], a[k], b[k], [eps], [iters])
+        out = orc.plan_apply(X[k], Y[k], a[k], b[k], fr, gref, eps)
+        e1, e2 = potentials_error(f[k:k + 1], g[k:k + 1], fr[None], gref[None])
+        ef, eg = max(ef, e1), max(eg, e2)
+        ec = max(ec, abs(c[k] - out["cost"]) / abs(out["cost"]))
+        egr = max(egr, normwise(gr[k], out["grad"]))
+    msg = f"f {ef:.2e} g {eg:.2e} cost {ec:.2e} grad {egr:.2e}"
+    print(msg)
+    assert max(ef, eg, ec, egr) < TOL, msg
+
+
+def test_tc_agrees_with_fp32_path(sot):
+    """Same problem through the fp16 x3 tensor path and the fp32 FMA path."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=3000, m=2600, d=64)
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    ft, gt = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=0.1, iters_per_stage=50, max_iters=50,
+                                   flags=sot.SOT_PREC_F16X3)
+    ff, gf = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=0.1, iters_per_stage=50, max_iters=50,
+                                   flags=sot.SOT_PREC_FP32)
+    ef, eg = potentials_error(host(ft), host(gt), host(ff), host(gf))
+    assert ef < TOL and eg < TOL, (ef, eg)
+
+
+def test_tc_full_size_first_half_step(sot, orc):
+    """n = m = 70000, d = 64: after one iteration f is the first f-half, which
+    the oracle evaluates row by row from X, Y and b (g = 0)."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4)
+    eps = 0.1
+    f, g = sot.sot_potentials(dev(X), dev(Y), dev(a), dev(b), eps=eps, iters=1)
+    fh = host(f)[0]
+    rows = np.random.default_rng(3).choice(X.shape[1], 48, replace=False)
+    fr = orc.f_half(X[0][rows], Y[0], b[0], np.zeros(Y.shape[1]), eps)
+    err = np.max(np.abs(fh[rows] - fr)) / np.max(np.abs(fr))
+    assert err < TOL, err
+
+
+def test_tc_full_size_column_marginals(sot):
+    """After 100 iterations (ending with a g-half) the column sums of the plan
+    equal b exactly; recomputed in float64 for sampled columns."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4)
+    eps = 0.1
+    f, g = sot.sot_potentials(dev(X), dev(Y), dev(a), dev(b), eps=eps, iters=100)
+    fh, gh = host(f)[0], host(g)[0]
+    X64, Y64 = X[0].astype(np.float64), Y[0].astype(np.float64)
+    a64, b64 = a[0].astype(np.float64), b[0].astype(np.float64)
+    for j in np.random.default_rng(5).choice(Y.shape[1], 12, replace=False):
+        C = ((X64 - Y64[j]) ** 2).sum(1)
+        col = np.sum(a64 * b64[j] * np.exp((fh + gh[j] - C) / eps))
+        assert abs(col - b64[j]) / b64[j] < 5e-3, (j, col / b64[j])
