@@ -268,7 +268,7 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
-    for k in range(args.steps):
+    for k in range(0 if args.no_e2e else args.steps):
         flush_buf.zero_()
         e0.record(stream)
         Xs, Ys, As, Bs = (v.to(dev, non_blocking=True) for v in (hX, hY, ha, hb))
@@ -278,7 +278,7 @@ def run_gpu(args, ws, rank, local):
         e1.record(stream)
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
-    e2e_max = max_over_ranks(e2e_ms / 1e3, ws, dev)
+    e2e_max = max_over_ranks(e2e_ms / 1e3, ws, dev) if not args.no_e2e else None
 
     if rank != 0:
         return 0
@@ -333,8 +333,8 @@ def run_gpu(args, ws, rank, local):
         "half_step": {"launches": nl, "avg_ms": per_launch_ms, "pairs_per_launch": per_launch_pairs},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": ws * pairs * args.steps / e2e_max / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e_max is None else {"value": ws * pairs * args.steps / e2e_max / 1e9, "unit": UNIT,
+                                             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
         "marginal_err": info["err"][0] if info else None,
@@ -355,6 +355,7 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=0, help="override the iteration count (testing only)")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
     if args.impl == "reference":

@@ -88,6 +88,11 @@ __global__ void pot_from_state_kernel(const float* nrm, const float* state, floa
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < count) pot[i] = nrm[i] - state[i] / kappa;
 }
+// Cold start (f = g = 0): state = kappa * nrm.
+__global__ void state_cold_kernel(const float* nrm, float kappa, int count, float* state) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < count) state[i] = kappa * nrm[i];
+}
 __global__ void scale_kernel(float* v, float s, int count) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < count) v[i] *= s;
@@ -106,6 +111,10 @@ cudaError_t launch_state_from_potential(const float* nrm, const float* pot, floa
 cudaError_t launch_potential_from_state(const float* nrm, const float* state, float kappa, int count, float* pot,
                                         cudaStream_t st) {
     count_launches(1); pot_from_state_kernel<<<(count + 255) / 256, 256, 0, st>>>(nrm, state, kappa, count, pot);
+    return cudaGetLastError();
+}
+cudaError_t launch_state_cold(const float* nrm, float kappa, int count, float* state, cudaStream_t st) {
+    count_launches(1); state_cold_kernel<<<(count + 255) / 256, 256, 0, st>>>(nrm, kappa, count, state);
     return cudaGetLastError();
 }
 cudaError_t launch_scale(float* v, float s, int count, cudaStream_t st) {

@@ -106,6 +106,7 @@ cudaError_t launch_state_from_potential(const float* nrm, const float* pot, floa
                                         float* state, cudaStream_t st);
 cudaError_t launch_potential_from_state(const float* nrm, const float* state, float kappa, int count,
                                         float* pot, cudaStream_t st);
+cudaError_t launch_state_cold(const float* nrm, float kappa, int count, float* state, cudaStream_t st);
 cudaError_t launch_scale(float* v, float s, int count, cudaStream_t st);
 cudaError_t launch_copy(float* dst, const float* src, int count, const int* stop_flag, cudaStream_t st);
 cudaError_t launch_reduce_parts(const float* part, int B, int parts, float* out, cudaStream_t st);

@@ -364,9 +364,16 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
     const int ips = s.iters_per_stage;
     const long long max_total = s.max_iters > 0 ? s.max_iters : (long long)ips * K;
     bool cold = !warm;
-    if (warm) {
-        rc = sv.init_states(f0, g0, 1.f / (eps[0] * SOT_LN2_D));
-        if (rc) return rc;
+    {
+        const float kappa0 = 1.f / (eps[0] * SOT_LN2_D);
+        if (warm) {
+            rc = sv.init_states(f0, g0, kappa0);
+            if (rc) return rc;
+        } else {
+            // f = g = 0: the column state of the first f-half is Lam = kappa |y|^2
+            SOT_CUDA(launch_state_cold(sv.nx, kappa0, sv.B * sv.n, sv.L, sv.st));
+            SOT_CUDA(launch_state_cold(sv.ny, kappa0, sv.B * sv.m, sv.Lam, sv.st));
+        }
     }
     std::vector<int> host_counts(K, -1);  // realised iterations of untested stages
     long long total = 0;                  // iterations realised so far
