@@ -49,7 +49,8 @@ constexpr uint32_t OP_BYTES = 2 * TILE_BYTES;   // hi + lo
 constexpr uint32_t OFF_A = 0;                           // [2 row tiles][hi, lo]
 constexpr uint32_t OFF_B = OFF_A + 2 * OP_BYTES;        // [TC_S][hi, lo]
 constexpr uint32_t OFF_BIAS = OFF_B + TC_S * OP_BYTES;  // [TC_S][TC_N] float
-constexpr uint32_t OFF_BAR = OFF_BIAS + TC_S * TC_N * 4;
+constexpr uint32_t OFF_NY = OFF_BIAS + TC_S * TC_N * 4;    // [TC_S][TC_N] float (plan application)
+constexpr uint32_t OFF_BAR = OFF_NY + TC_S * TC_N * 4;
 constexpr uint32_t NBAR = 17;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last
 constexpr uint32_t OFF_RED = OFF_MISC + 16;             // 16 floats
@@ -70,7 +71,10 @@ bool tc_supported(int d) { return d == TC_D; }
 int tc_max_d() { return TC_D; }
 int tc_rows_per_cta() { return TC_ROWS; }
 int tc_cols_per_tile() { return TC_N; }
-bool tc_apply_supported(int) { return false; }
+bool tc_apply_supported(int d) { return d == TC_D; }
+// Automatic precision uses the tensor-core plan application only once it has
+// passed its GPU parity tests; SOT_PREC_F16X3 selects it explicitly.
+bool tc_apply_default() { return false; }
 int tc_apply_rows_per_cta() { return TC_ROWS; }
 
 static inline int tc_tiles(int n) { return 2 * ((n + TC_ROWS - 1) / TC_ROWS); }
@@ -153,13 +157,156 @@ cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m
     return cudaGetLastError();
 }
 
-// ---- the half-step ----------------------------------------------------------------
+// ---- shared machinery of the tensor-core kernels ----------------------------------
 struct TcOps {
     const unsigned char* aimg;  // row-side image
     const unsigned char* bimg;  // column-side image
     const float* scale;
     int tiles_r, tiles_c;
 };
+
+struct TcSmem {
+    uint32_t sbase;       // 1024-aligned shared address of the layout
+    unsigned char* sm;    // generic pointer to the same place
+    __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8u * (uint32_t)i; }
+    __device__ float* bias() const { return reinterpret_cast<float*>(sm + OFF_BIAS); }
+    __device__ float* nyb() const { return reinterpret_cast<float*>(sm + OFF_NY); }
+    __device__ int* misc() const { return reinterpret_cast<int*>(sm + OFF_MISC); }  // tmem, abort, nretry, last
+    __device__ volatile int* abort() const { return misc() + 1; }
+    __device__ float* red() const { return reinterpret_cast<float*>(sm + OFF_RED); }
+    __device__ int* retry() const { return reinterpret_cast<int*>(sm + OFF_RETRY); }
+};
+
+__device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr) {
+    TcSmem S;
+    const uint32_t raw = smem_u32(raw_ptr);
+    S.sbase = (raw + 1023u) & ~1023u;
+    S.sm = raw_ptr + (S.sbase - raw);
+    return S;
+}
+
+// Barriers, TMEM allocation (warp 1, 512 columns); returns the TMEM base address.
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_S; ++s) {
+            mbar_init(S.bar(BAR_FULL(s)), 32);
+            mbar_init(S.bar(BAR_EMPTY(s)), 1 + 8);
+        }
+        for (int r = 0; r < 2; ++r)
+            for (int u = 0; u < 2; ++u) {
+                mbar_init(S.bar(BAR_ACCFULL(r, u)), 1);
+                mbar_init(S.bar(BAR_ACCEMPTY(r, u)), 4);
+            }
+        mbar_init(S.bar(BAR_A()), 1);
+        S.misc()[1] = 0;
+        S.misc()[2] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(S.sbase + OFF_MISC, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return (uint32_t)S.misc()[0];
+}
+
+// Producer warp: the CTA's two row tiles once, then the column tiles of the
+// chunk through the TC_S-stage ring, with the tile's column biases (and, for
+// plan application, the column norms) written to shared memory.
+__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, int c_end,
+                            const float* cw, const float* cst, const float* ny) {
+    const int lane = threadIdx.x & 31;
+    volatile int* abort = S.abort();
+    int issued = 0;
+    if (lane == 0) {
+        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * OP_BYTES);
+        bulk_g2s(S.sbase + OFF_A, ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES, 2 * OP_BYTES,
+                 S.bar(BAR_A()));
+    }
+    const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
+    float* bias = S.bias();
+    float* nyb = S.nyb();
+    for (int lt = 0; lt < nt; ++lt) {
+        const int st = lt % TC_S;
+        const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
+        const int jt = (t0 + lt) * TC_N;
+        for (int c = lane; c < TC_N; c += 32) {
+            const int j = jt + c;
+            bias[st * TC_N + c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
+            if (ny) nyb[st * TC_N + c] = (j < c_end) ? ny[j] : 0.f;
+        }
+        if (lane == 0) {
+            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES);
+            bulk_g2s(S.sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, OP_BYTES,
+                     S.bar(BAR_FULL(st)));
+        } else {
+            mbar_arrive(S.bar(BAR_FULL(st)));
+        }
+        issued = lt + 1;
+    }
+    // drain: never leave a bulk copy in flight into this CTA's shared memory
+    if (lane == 0) {
+        int dummy = 0;
+        for (int lt = (issued > TC_S ? issued - TC_S : 0); lt < issued; ++lt)
+            mbar_wait_bounded(S.bar(BAR_FULL(lt % TC_S)), (uint32_t)(lt / TC_S) & 1u, (volatile int*)&dummy,
+                              TC_WAIT_NS);
+        mbar_wait_bounded(S.bar(BAR_A()), 0u, (volatile int*)&dummy, TC_WAIT_NS);
+    }
+    __syncwarp();
+}
+
+// MMA warp (one thread): per column tile and row tile, 12 MMAs of
+// 128 x 128 x 16 -- lo*hi and hi*lo first, then hi*hi -- into the row tile's
+// TMEM buffer (lt & 1); commits signal the epilogue and free the stage.
+__device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
+    if ((threadIdx.x & 31) == 0) {
+        volatile int* abort = S.abort();
+        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, TC_WAIT_NS);
+        const uint32_t idesc = f16_idesc(TC_M, TC_N);
+        for (int lt = 0; ok && lt < nt; ++lt) {
+            const int st = lt % TC_S;
+            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+            const int u = lt & 1;
+            const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            for (int r = 0; r < 2 && ok; ++r) {
+                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, u)), pu ^ 1u, abort, TC_WAIT_NS)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
+                const uint32_t ahi = S.sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
+                const uint32_t bhi = S.sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < TC_D / 16; ++k) {
+                    const uint32_t ko = 32u * (uint32_t)k;
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
+                    tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
+                }
+#pragma unroll
+                for (int k = 0; k < TC_D / 16; ++k) {
+                    const uint32_t ko = 32u * (uint32_t)k;
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, 1u);
+                }
+                tc_commit(S.bar(BAR_ACCFULL(r, u)));
+            }
+            if (!ok) break;
+            tc_commit(S.bar(BAR_EMPTY(st)));
+        }
+    }
+    __syncwarp();
+}
+
+// After an epilogue warp has consumed tile lt: release its TMEM buffer and its stage.
+__device__ __forceinline__ void tc_release(const TcSmem& S, int wg, int lt) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        mbar_arrive(S.bar(BAR_ACCEMPTY(wg, lt & 1)));
+        mbar_arrive(S.bar(BAR_EMPTY(lt % TC_S)));
+    }
+}
 
 __device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc,
                              int row, float tk, float* red) {
@@ -184,18 +331,15 @@ __device__ float tc_row_full(const float* rows, const float* cols, const float* 
     return mx + log2f(sm);
 }
 
+// ---- the half-step ------------------------------------------------------------------
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOps ops) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     extern __shared__ unsigned char smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t sbase = (raw + 1023u) & ~1023u;
-    unsigned char* sm = smem_raw + (sbase - raw);
-    float* bias = reinterpret_cast<float*>(sm + OFF_BIAS);
-    int* misc = reinterpret_cast<int*>(sm + OFF_MISC);  // [0] tmem, [1] abort, [2] nretry, [3] last
-    volatile int* abort = misc + 1;
-    float* red = reinterpret_cast<float*>(sm + OFF_RED);
-    int* retry = reinterpret_cast<int*>(sm + OFF_RETRY);
-    auto BAR = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * (uint32_t)i; };
+    const TcSmem S = tc_smem(smem_raw);
+    int* misc = S.misc();
+    volatile int* abort = S.abort();
+    float* red = S.red();
+    int* retry = S.retry();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
@@ -211,121 +355,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     const float sc = ops.scale[b];
     const float tk = p.two_kappa / (sc * sc);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < TC_S; ++s) {
-            mbar_init(BAR(BAR_FULL(s)), 32);
-            mbar_init(BAR(BAR_EMPTY(s)), 1 + 8);
-        }
-        for (int r = 0; r < 2; ++r)
-            for (int u = 0; u < 2; ++u) {
-                mbar_init(BAR(BAR_ACCFULL(r, u)), 1);
-                mbar_init(BAR(BAR_ACCEMPTY(r, u)), 4);
-            }
-        mbar_init(BAR(BAR_A()), 1);
-        misc[1] = 0;
-        misc[2] = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(sbase + OFF_MISC, 512);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = (uint32_t)misc[0];
+    const uint32_t tmem = tc_setup(S, warp);
 
     float m = 0.f, s = 0.f;  // epilogue row state
-    const int ew = warp - 2;
-    const int wg = ew >> 2;      // row tile of this epilogue warp
-    const int q4 = warp & 3;     // TMEM lane quarter this warp may access
-    const int rl = wg * TC_M + q4 * 32 + lane;
-    const int row = row0 + rl;
+    const int wg = (warp - 2) >> 2;  // row tile of this epilogue warp
+    const int q4 = warp & 3;         // TMEM lane quarter this warp may access
+    const int row = row0 + wg * TC_M + q4 * 32 + lane;
     const bool erow = (warp >= 2) && row < p.nr;
 
     if (warp == 0) {
-        // ---------------- producer ----------------
-        int issued = 0;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(BAR(BAR_A()), 2 * OP_BYTES);
-            bulk_g2s(sbase + OFF_A, ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES, 2 * OP_BYTES,
-                     BAR(BAR_A()));
-        }
-        const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
-        for (int lt = 0; lt < nt; ++lt) {
-            const int st = lt % TC_S;
-            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-            if (!mbar_wait_bounded(BAR(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
-            const int jt = (t0 + lt) * TC_N;
-            for (int c = lane; c < TC_N; c += 32) {
-                const int j = jt + c;
-                bias[st * TC_N + c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(BAR(BAR_FULL(st)), OP_BYTES);
-                bulk_g2s(sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, OP_BYTES,
-                         BAR(BAR_FULL(st)));
-            } else {
-                mbar_arrive(BAR(BAR_FULL(st)));
-            }
-            issued = lt + 1;
-        }
-        // drain: never leave a bulk copy in flight into this CTA's shared memory
-        if (lane == 0) {
-            int dummy = 0;
-            for (int lt = (issued > TC_S ? issued - TC_S : 0); lt < issued; ++lt)
-                mbar_wait_bounded(BAR(BAR_FULL(lt % TC_S)), (uint32_t)(lt / TC_S) & 1u, (volatile int*)&dummy,
-                                  TC_WAIT_NS);
-            mbar_wait_bounded(BAR(BAR_A()), 0u, (volatile int*)&dummy, TC_WAIT_NS);
-        }
-        __syncwarp();
+        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst, nullptr);
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            bool ok = mbar_wait_bounded(BAR(BAR_A()), 0u, abort, TC_WAIT_NS);
-            const uint32_t idesc = f16_idesc(TC_M, TC_N);
-            for (int lt = 0; ok && lt < nt; ++lt) {
-                const int st = lt % TC_S;
-                const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-                const int u = lt & 1;
-                const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-                if (!mbar_wait_bounded(BAR(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
-                for (int r = 0; r < 2 && ok; ++r) {
-                    if (!mbar_wait_bounded(BAR(BAR_ACCEMPTY(r, u)), pu ^ 1u, abort, TC_WAIT_NS)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
-                    const uint32_t ahi = sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
-                    const uint32_t bhi = sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
-#pragma unroll
-                    for (int k = 0; k < TC_D / 16; ++k) {
-                        const uint32_t ko = 32u * (uint32_t)k;
-                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
-                        tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
-                    }
-#pragma unroll
-                    for (int k = 0; k < TC_D / 16; ++k) {
-                        const uint32_t ko = 32u * (uint32_t)k;
-                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, 1u);
-                    }
-                    tc_commit(BAR(BAR_ACCFULL(r, u)));
-                }
-                if (!ok) break;
-                tc_commit(BAR(BAR_EMPTY(st)));
-            }
-        }
-        __syncwarp();
+        tc_mma(S, tmem, nt);
     } else {
         // ---------------- epilogue: exponentials and row sums ----------------
         m = erow ? (p.cold ? -INFINITY : p.rstate_in[rbase + row] - SOT_STAB_BIAS) : INFINITY;
         s = 0.f;
         const float2 tk2 = make_float2(tk, tk);
+        const float* bias = S.bias();
         for (int lt = 0; lt < nt; ++lt) {
             const int st = lt % TC_S;
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(BAR(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
-            if (!mbar_wait_bounded(BAR(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
             const float* cb = bias + st * TC_N;
@@ -378,12 +432,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
                 if (ovf && mn > -INFINITY) ts = ts2;
             }
             s += ts;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(BAR(BAR_ACCEMPTY(wg, u)));
-                mbar_arrive(BAR(BAR_EMPTY(st)));
-            }
+            tc_release(S, wg, lt);
         }
     }
 
@@ -394,8 +443,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-    const bool aborted = *abort != 0;
-    if (aborted) {
+    if (*abort) {
         m = NAN;
         s = NAN;
         if (threadIdx.x == 0) atomicOr(p.status, SOT_DEV_TIMEOUT);
@@ -416,16 +464,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
         if (!misc[3]) return;
         __threadfence();
         if (erow) {
-            float M = -INFINITY, S = 0.f;
+            float M = -INFINITY, Sm = 0.f;
             bool nan = false;
             for (int c = 0; c < p.split; ++c) {
                 const float pm = __ldcg(p.part_m + c * stride + rbase + row);
                 const float ps = __ldcg(p.part_s + c * stride + rbase + row);
                 if (pm != pm || ps != ps) nan = true;
-                lse_combine(M, S, pm, ps);
+                lse_combine(M, Sm, pm, ps);
             }
             m = nan ? NAN : M;
-            s = nan ? NAN : S;
+            s = nan ? NAN : Sm;
         }
         if (threadIdx.x == 0) p.counters[b * p.rowtiles + rb] = 0u;
     }
@@ -480,6 +528,272 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc_apply(const TcPlan&, const ApplyArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+// ---- plan application (cost, gradient, row sums) ------------------------------------
+// Per row i, with the final potentials and P_ij / a_i = 2^(score_ij - L_i):
+//   r_i = sum_j P_ij,  q_i = sum_j P_ij C_ij,  v_i = sum_j P_ij y_j
+// (C_ij = |x_i|^2 + |y_j|^2 - 2 x_i.y_j in centred coordinates).  r_i sums every
+// pair.  q_i and v_i sum the pairs whose term is within 2^-40 of the row's
+// running scale: an omitted term is below 2^-40 of the row mass, so at most
+// m * 2^-40 of it is dropped in all.  Such pairs are a handful per row, and
+// v_i gathers y_j only for them.
+// Pass A of a tile forms the exponentials and the row sum, and marks the
+// 4-column groups that hold a significant pair; pass B revisits only those.
+struct TcApplyExtra {
+    const float* nx;      // [B][n]
+    const float* ny;      // [B][m]
+    const float* X;       // [B][n][64] caller coordinates
+    const float* a;       // [B][n] or NULL (uniform)
+    const float* shift;   // [B][64]
+    float* vpart;         // [split][B*n][64], zero on entry
+    float* part_r;        // [split][B*n]
+    float* part_q;        // [split][B*n]
+    float* cost_part;     // [B][rowtiles] or NULL
+    float* grad;          // [B][n][64] or NULL
+    float* rowsum;        // [B][n] or NULL
+};
+
+constexpr float TC_SIG = -40.f;  // log2 threshold of a significant term
+
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcOps ops, TcApplyExtra x) {
+    extern __shared__ unsigned char smem_raw[];
+    const TcSmem S = tc_smem(smem_raw);
+    int* misc = S.misc();
+    volatile int* abort = S.abort();
+    float* red = S.red();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int rb = blockIdx.x / p.split, ch = blockIdx.x % p.split;
+    const int row0 = rb * TC_ROWS;
+    const int c_begin = ch * p.chunk;
+    const int c_end = min(p.nc, c_begin + p.chunk);
+    const int t0 = c_begin / TC_N;
+    const int nt = (c_end - c_begin + TC_N - 1) / TC_N;
+    const float* cw = p.cw2 + (size_t)b * p.nc;
+    const float* cst = p.cstate + (size_t)b * p.nc;
+    const size_t rbase = (size_t)b * p.nr;
+    const float sc = ops.scale[b];
+    const float tk = p.two_kappa / (sc * sc);
+    const float c2 = -2.f / (sc * sc);  // acc -> -2 x.y
+    const float* ycen = p.cpack + (size_t)b * p.nc * TC_D;
+
+    const uint32_t tmem = tc_setup(S, warp);
+
+    float m = 0.f, r = 0.f, q = 0.f;
+    const int wg = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int row = row0 + wg * TC_M + q4 * 32 + lane;
+    const bool erow = (warp >= 2) && row < p.nr;
+    float* vrow = erow ? x.vpart + (((size_t)ch * p.B * p.nr) + rbase + row) * TC_D : nullptr;
+
+    if (warp == 0) {
+        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst, x.ny + (size_t)b * p.nc);
+    } else if (warp == 1) {
+        tc_mma(S, tmem, nt);
+    } else {
+        m = erow ? p.rstate_in[rbase + row] - SOT_STAB_BIAS : INFINITY;
+        const float nxi = erow ? x.nx[rbase + row] : 0.f;
+        const float2 tk2 = make_float2(tk, tk);
+        for (int lt = 0; lt < nt; ++lt) {
+            const int st = lt % TC_S;
+            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+            const int u = lt & 1;
+            const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
+            const float* cb = S.bias() + st * TC_N;
+            const float* nyb = S.nyb() + st * TC_N;
+            // pass A: row sum, significance marks per 4-column group
+            const float2 nm2 = make_float2(-m, -m);
+            float2 acc2 = make_float2(0.f, 0.f);
+            uint32_t sig = 0u;
+#pragma unroll 1
+            for (int qq = 0; qq < TC_N / 32; ++qq) {
+                float v[32];
+                tmem_ld32(tb + 32u * (uint32_t)qq, v);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(cb + 32 * qq + j);
+                    const float2 e0 = fadd2(ffma2(make_float2(v[j], v[j + 1]), tk2, make_float2(c4.x, c4.y)), nm2);
+                    const float2 e1 =
+                        fadd2(ffma2(make_float2(v[j + 2], v[j + 3]), tk2, make_float2(c4.z, c4.w)), nm2);
+                    acc2 = fadd2(acc2, make_float2(ex2f(e0.x), ex2f(e0.y)));
+                    acc2 = fadd2(acc2, make_float2(ex2f(e1.x), ex2f(e1.y)));
+                    const float emax = fmaxf(fmaxf(e0.x, e0.y), fmaxf(e1.x, e1.y));
+                    sig |= (emax > TC_SIG) ? (1u << (8 * qq + j / 4)) : 0u;
+                }
+            }
+            float ts = acc2.x + acc2.y;
+            const bool ovf = !(ts < SOT_TILE_SUM_MAX);
+            if (__any_sync(0xffffffffu, ovf)) {
+                float mt = -INFINITY;
+#pragma unroll 1
+                for (int qq = 0; qq < TC_N / 32; ++qq) {
+                    float v[32];
+                    tmem_ld32(tb + 32u * (uint32_t)qq, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, fmaf(v[j], tk, cb[32 * qq + j]));
+                }
+                const float mn = fmaxf(m, mt);
+                if (ovf && mn > m) {
+                    const float f = ex2f(m - mn);
+                    r *= f;
+                    q *= f;
+                    for (int k = 0; k < TC_D; ++k) vrow[k] *= f;
+                    m = mn;
+                }
+                float ts2 = 0.f;
+#pragma unroll 1
+                for (int qq = 0; qq < TC_N / 32; ++qq) {
+                    float v[32];
+                    tmem_ld32(tb + 32u * (uint32_t)qq, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ts2 += ex2f(fmaf(v[j], tk, cb[32 * qq + j]) - m);
+                }
+                if (ovf) ts = ts2;
+            }
+            r += ts;
+            // pass B: cost and barycentre terms of the significant pairs
+#pragma unroll 1
+            for (int qq = 0; qq < TC_N / 32; ++qq) {
+                const uint32_t mine = (sig >> (8 * qq)) & 0xFFu;
+                if (!__any_sync(0xffffffffu, mine != 0u)) continue;
+                float v[32];
+                tmem_ld32(tb + 32u * (uint32_t)qq, v);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    if (!(mine & (1u << g))) continue;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int cl = 32 * qq + 4 * g + jj;
+                        const float e = fmaf(v[4 * g + jj], tk, cb[cl]) - m;
+                        if (e > TC_SIG) {
+                            const float w = ex2f(e);
+                            q = fmaf(w, fmaf(v[4 * g + jj], c2, nxi + nyb[cl]), q);
+                            const float* y = ycen + (size_t)((t0 + lt) * TC_N + cl) * TC_D;
+                            for (int k = 0; k < TC_D; k += 4) {
+                                const float4 yv = *reinterpret_cast<const float4*>(y + k);
+                                float4 acc = *reinterpret_cast<float4*>(vrow + k);
+                                acc.x = fmaf(w, yv.x, acc.x);
+                                acc.y = fmaf(w, yv.y, acc.y);
+                                acc.z = fmaf(w, yv.z, acc.z);
+                                acc.w = fmaf(w, yv.w, acc.w);
+                                *reinterpret_cast<float4*>(vrow + k) = acc;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_release(S, wg, lt);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (*abort) {
+        m = NAN;
+        if (threadIdx.x == 0) atomicOr(p.status, SOT_DEV_TIMEOUT);
+    }
+    const size_t stride = (size_t)p.B * p.nr;
+    if (p.split > 1) {
+        if (erow) {
+            p.part_m[ch * stride + rbase + row] = m;
+            x.part_r[ch * stride + rbase + row] = r;
+            x.part_q[ch * stride + rbase + row] = q;
+        }
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned prev = atomicAdd(&p.counters[b * p.rowtiles + rb], 1u);
+            misc[3] = (prev == (unsigned)(p.split - 1));
+        }
+        __syncthreads();
+        if (!misc[3]) return;
+        __threadfence();
+        if (threadIdx.x == 0) p.counters[b * p.rowtiles + rb] = 0u;
+    }
+    float qi = 0.f;
+    if (erow) {
+        // merge the chunks: scale each chunk's sums from its stabiliser to the largest
+        float M = -INFINITY;
+        bool nan = false;
+        for (int c = 0; c < p.split; ++c) {
+            const float mc = (p.split > 1) ? __ldcg(p.part_m + c * stride + rbase + row) : m;
+            if (mc != mc) nan = true;
+            M = fmaxf(M, mc);
+        }
+        float R = 0.f, Q = 0.f;
+        float V[TC_D];
+#pragma unroll
+        for (int k = 0; k < TC_D; ++k) V[k] = 0.f;
+        for (int c = 0; c < p.split; ++c) {
+            const float mc = (p.split > 1) ? __ldcg(p.part_m + c * stride + rbase + row) : m;
+            const float f = (mc == -INFINITY || M == -INFINITY) ? 0.f : ex2f(mc - M);
+            R += f * ((p.split > 1) ? __ldcg(x.part_r + c * stride + rbase + row) : r);
+            Q += f * ((p.split > 1) ? __ldcg(x.part_q + c * stride + rbase + row) : q);
+            const float* vc = x.vpart + ((size_t)c * stride + rbase + row) * TC_D;
+#pragma unroll
+            for (int k = 0; k < TC_D; ++k) V[k] = fmaf(f, __ldcg(vc + k), V[k]);
+        }
+        const float ai = x.a ? x.a[rbase + row] : 1.f / (float)p.nr;
+        const float fac = nan ? NAN : ai * ex2f(M);
+        const float ri = fac * R;
+        qi = fac * Q;
+        if (x.rowsum) x.rowsum[rbase + row] = ri;
+        if (x.grad) {
+            const float* xo = x.X + (rbase + row) * TC_D;
+            const float* sh = x.shift + (size_t)b * TC_D;
+            float* gr = x.grad + (rbase + row) * TC_D;
+#pragma unroll
+            for (int k = 0; k < TC_D; ++k) gr[k] = 2.f * (ai * xo[k] - fmaf(ri, sh[k], fac * V[k]));
+        }
+    }
+    if (x.cost_part) {
+        qi = block_sum<TC_THREADS>(qi, red);
+        if (threadIdx.x == 0) x.cost_part[b * p.rowtiles + rb] = qi;
+    }
+}
+
+size_t tc_apply_scratch_floats(int B, int n, int split) {
+    return (size_t)split * B * n * (TC_D + 2);
+}
+
+cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfArgs& hp, float* scratch,
+                            cudaStream_t st) {
+    if (a.d != TC_D) return cudaErrorInvalidValue;
+    TcOps ops;
+    ops.aimg = plan.xop;
+    ops.bimg = plan.yop;
+    ops.scale = plan.scale;
+    ops.tiles_r = plan.tiles_x;
+    ops.tiles_c = plan.tiles_y;
+    TcApplyExtra x;
+    const size_t rows = (size_t)a.B * a.n;
+    x.nx = a.nx;
+    x.ny = a.ny;
+    x.X = a.X;
+    x.a = a.a;
+    x.shift = a.shift;
+    x.vpart = scratch;
+    x.part_r = scratch + (size_t)hp.split * rows * TC_D;
+    x.part_q = x.part_r + (size_t)hp.split * rows;
+    x.cost_part = a.cost_part;
+    x.grad = a.grad;
+    x.rowsum = a.rowsum;
+    cudaError_t e = cudaMemsetAsync(x.vpart, 0, sizeof(float) * (size_t)hp.split * rows * TC_D, st);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(hp.rowtiles * hp.split, hp.B), block(TC_THREADS);
+    count_launches(1);
+    tc_apply_kernel<<<grid, block, TC_SMEM, st>>>(hp, ops, x);
+    return cudaGetLastError();
+}
 
 }  // namespace sot

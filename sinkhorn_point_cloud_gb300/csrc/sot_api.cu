@@ -275,9 +275,8 @@ struct Solver {
     int* stop_flag() { return dflags + 1; }
     int* conv_flag() { return dflags + 2; }
 
-    // One half-step.  h = 0: f-half (rows X, state L); h = 1: g-half (rows Y, state Lam).
-    int half(int h, int mode, float kappa, bool cold, const float* rin, float* rout, float* errp, bool guarded,
-             const float* cstate_override = nullptr) {
+    // Arguments of one half-step.  h = 0: f-half (rows X, state L); h = 1: g-half (rows Y, state Lam).
+    HalfArgs half_args(int h, float kappa, bool cold, const float* rin, float* rout, float* errp, bool guarded) {
         HalfArgs p;
         p.B = B;
         p.nr = h ? m : n;
@@ -286,7 +285,7 @@ struct Solver {
         p.rpack = h ? ypack : xpack;
         p.cpack = h ? xpack : ypack;
         p.cw2 = h ? lw2x : lw2y;
-        p.cstate = cstate_override ? cstate_override : (h ? L : Lam);
+        p.cstate = h ? L : Lam;
         p.rstate_in = rin;
         p.rstate_out = rout;
         p.rweight = h ? b : a;
@@ -301,6 +300,11 @@ struct Solver {
         p.errpart = errp;
         p.stop_flag = guarded ? stop_flag() : nullptr;
         p.status = dflags;
+        return p;
+    }
+
+    int half(int h, int mode, float kappa, bool cold, const float* rin, float* rout, float* errp, bool guarded) {
+        const HalfArgs p = half_args(h, kappa, cold, rin, rout, errp, guarded);
         cudaError_t e;
         {
             ProfScope ps(st, mode == MODE_LSE);
@@ -569,7 +573,9 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     Path path;
     rc = choose_path(d, flags, &path);
     if (rc) return rc;
-    if (path == PATH_TC && !tc_apply_supported(d)) path = PATH_DENSE;
+    if (path == PATH_TC &&
+        (!tc_apply_supported(d) || ((flags & SOT_PREC_MASK) == SOT_PREC_AUTO && !tc_apply_default())))
+        path = PATH_DENSE;
     cudaStream_t cs = (cudaStream_t)stream;
     Solver sv(X, Y, a, b, B, n, m, d, path, cs);
     rc = sv.prepare(0);
@@ -584,7 +590,7 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     p.X = X; p.a = a; p.shift = sv.shift; p.kappa = kappa;
     const int rpc = (sv.path == PATH_POINT) ? point_apply_rows_per_cta()
                     : (sv.path == PATH_TC) ? tc_apply_rows_per_cta() : dense_apply_rows_per_cta();
-    p.rowtiles = (n + rpc - 1) / rpc;
+    p.rowtiles = (sv.path == PATH_TC) ? sv.rowtiles[0] : (n + rpc - 1) / rpc;
     float* cpart = nullptr;
     if (cost) {
         cpart = sv.S.alloc<float>((size_t)B * p.rowtiles);
@@ -592,9 +598,16 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     }
     p.cost_part = cpart; p.grad = grad; p.rowsum = rowsum;
     cudaError_t e;
-    if (sv.path == PATH_POINT) e = launch_point_apply(p, cs);
-    else if (sv.path == PATH_TC) e = launch_tc_apply(sv.tc, p, cs);
-    else e = launch_dense_apply(p, cs);
+    if (sv.path == PATH_POINT) {
+        e = launch_point_apply(p, cs);
+    } else if (sv.path == PATH_TC) {
+        float* scr = sv.S.alloc<float>(tc_apply_scratch_floats(B, n, sv.split[0]));
+        if (!scr) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        const HalfArgs hp = sv.half_args(0, kappa, false, sv.L, nullptr, nullptr, false);
+        e = launch_tc_apply(sv.tc, p, hp, scr, cs);
+    } else {
+        e = launch_dense_apply(p, cs);
+    }
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "plan-apply launch failed: %s", cudaGetErrorString(e));
     if (cost) SOT_CUDA(launch_reduce_parts(cpart, B, p.rowtiles, cost, cs));
     return SOT_OK;

@@ -26,7 +26,13 @@ cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m
                        const float* yc, cudaStream_t st);
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st);
 bool tc_apply_supported(int d);
+bool tc_apply_default();
 int tc_apply_rows_per_cta();
-cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& p, cudaStream_t st);
+// Plan application on the tensor cores.  `hp` carries the split plan and the
+// f-half operands (rows X, columns Y, column state Lam, row state L); scratch
+// holds tc_apply_scratch_floats() floats.
+size_t tc_apply_scratch_floats(int B, int n, int split);
+cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfArgs& hp, float* scratch,
+                            cudaStream_t st);
 
 }  // namespace sot

@@ -90,3 +90,26 @@ def test_tc_full_size_column_marginals(sot):
         C = ((X64 - Y64[j]) ** 2).sum(1)
         col = np.sum(a64 * b64[j] * np.exp((fh + gh[j] - C) / eps))
         assert abs(col - b64[j]) / b64[j] < 5e-3, (j, col / b64[j])
+
+
+@pytest.mark.parametrize("n,m,B", [(1000, 1100, 1), (300, 257, 2)])
+def test_tc_plan_apply_matches_oracle(sot, orc, n, m, B):
+    """Cost, gradient and row sums from the tensor-core plan application, with
+    the oracle's own potentials (rounded to fp32) as input."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=B, n=n, m=m, d=64)
+    eps = 0.1
+    fs, gs = [], []
+    for k in range(B):
+        fr, gref = orc.sinkhorn(X[k], Y[k], a[k], b[k], [eps], [60])
+        fs.append(fr); gs.append(gref)
+    f32 = np.stack(fs).astype(np.float32)
+    g32 = np.stack(gs).astype(np.float32)
+    c, gr, r = sot.sot_plan_apply(dev(X), dev(Y), dev(a), dev(b), dev(f32), dev(g32), eps, rowsum=True,
+                                  flags=sot.SOT_PREC_F16X3)
+    c, gr, r = host(c), host(gr), host(r)
+    for k in range(B):
+        out = orc.plan_apply(X[k], Y[k], a[k], b[k], f32[k], g32[k], eps)
+        assert abs(c[k] - out["cost"]) / abs(out["cost"]) < TOL
+        assert normwise(gr[k], out["grad"]) < TOL
+        assert normwise(r[k], out["rowsum"]) < TOL
