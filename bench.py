@@ -40,6 +40,12 @@ METRIC = "Sinkhorn pair-evaluations/s (n=m=70000, d=64)"
 UNIT = "Gpair-evals/s"
 
 
+def metric_name(wid: int) -> str:
+    if wid == WORKLOAD_ID:
+        return METRIC
+    return f"Sinkhorn pair-evaluations/s ({datagen.WORKLOADS[wid]['name']})"
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -172,8 +178,8 @@ def oracle_rate(target_s: float, X, Y, b, eps):
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
-    w = datagen.WORKLOADS[WORKLOAD_ID]
-    X, Y, a, b = datagen.make_batch(WORKLOAD_ID, B=1)
+    w = datagen.WORKLOADS[args.workload]
+    X, Y, a, b = datagen.make_batch(args.workload, B=1)
     rates = []
     for _ in range(args.warmup):
         oracle_rate(0.5, X[0], Y[0], b[0], w["eps"])
@@ -183,11 +189,11 @@ def run_reference(args, ws, rank):
         rates.append(r)
         sample = f"f-half of {rows} rows x {w['m']} columns (d={w['d']}), {t:.1f} s"
     value = float(np.median(rates)) / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w["name"], "B": 1, "n": w["n"], "m": w["m"], "d": w["d"], "eps": w["eps"],
-                       "iters": w["iters"]},
+            "config": {"workload": w["name"], "B": w["B"], "n": w["n"], "m": w["m"], "d": w["d"], "eps": w["eps"],
+                       "iters": w.get("iters")},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -206,29 +212,46 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    w = datagen.WORKLOADS[WORKLOAD_ID]
-    B, n, m, d, eps, iters = 1, w["n"], w["m"], w["d"], w["eps"], w["iters"]
+    wid = args.workload
+    w = datagen.WORKLOADS[wid]
+    B, n, m, d, eps = w["B"], w["n"], w["m"], w["d"], w["eps"]
+    iters = w.get("iters", 0)
     if args.n:
         n = m = args.n
     if args.iters:
         iters = args.iters
-    # weak scaling: every rank solves its own problem (seeded by rank)
-    X, Y, a, b = datagen.make_batch(WORKLOAD_ID, B=B, n=n, m=m, clouds=[rank])
-    hX, hY, ha, hb = (torch.from_numpy(v).pin_memory() for v in (X, Y, a, b))
-    Xd, Yd, ad, bd = (v.to(dev) for v in (hX, hY, ha, hb))
+    # weak scaling: every rank solves its own problem(s), seeded by rank
+    X, Y, a, b = datagen.make_batch(wid, B=B, n=n, m=m, clouds=range(rank * B, rank * B + B))
+    weighted = w["kind"] == "gauss"  # the other recipes use uniform weights (NULL in the ABI)
+    host_in = [torch.from_numpy(v).pin_memory() for v in ((X, Y, a, b) if weighted else (X, Y))]
+    dev_in = [v.to(dev) for v in host_in]
     flags = {"auto": sot.SOT_PREC_AUTO, "fp32": sot.SOT_PREC_FP32, "f16x3": sot.SOT_PREC_F16X3}[args.prec]
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    pairs = 2.0 * B * n * m * iters
 
-    def step(Xs, Ys, As, Bs):
+    def step(ins):
+        Xs, Ys = ins[0], ins[1]
+        As, Bs = (ins[2], ins[3]) if weighted else (None, None)
+        if wid == 3:
+            f, g, info = sot.sot_potentials_ex(Xs, Ys, As, Bs, eps=eps, eps_init=w["eps_init"],
+                                               eps_factor=w["eps_factor"], iters_per_stage=w["iters_per_stage"],
+                                               max_iters=w["max_iters"], tol=w["tol"], flags=flags, stats=True)
+            return [f, g], info
         f, g, info = sot.sot_potentials_ex(Xs, Ys, As, Bs, eps=eps, iters_per_stage=iters, max_iters=iters,
                                            flags=flags, stats=True)
+        if wid == 5:
+            coo = sot.sot_plan_coo(Xs, Ys, As, Bs, f, g, eps, threshold=w["tau"], dirs=3)
+            gs = sot.sot_grad_x_coo(Xs, Ys, coo["rows"], coo["cols"], coo["vals"], coo["batch_offsets"])
+            info["nnz"] = coo["nnz"]
+            return [coo["rows"], coo["cols"], coo["vals"], gs], info
         cost, grad, _ = sot.sot_plan_apply(Xs, Ys, As, Bs, f, g, eps, flags=flags & 3)
-        return cost, grad, info
+        return [cost, grad], info
+
+    def step_pairs(info):
+        return 2.0 * B * n * m * info["iters_done"]
 
     for _ in range(args.warmup):
-        step(Xd, Yd, ad, bd)
+        step(dev_in)
     torch.cuda.synchronize()
 
     # ---- device-resident timing, L2 flushed before every step -------------
@@ -241,13 +264,15 @@ def run_gpu(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     info = None
+    pairs_total = 0.0
     with ClockSampler(local, clk_path) as cs:
         t_wall0 = time.perf_counter()
         for k in range(args.steps):
             flush_buf.zero_()
             ev[k][0].record(stream)
-            cost, grad, info = step(Xd, Yd, ad, bd)
+            outs, info = step(dev_in)
             ev[k][1].record(stream)
+            pairs_total += step_pairs(info)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
     barrier(ws)
@@ -260,24 +285,23 @@ def run_gpu(args, ws, rank, local):
     clocks = cs.summary()
 
     # ---- end to end through the public API with host buffers -------------------
-    h2d = sum(v.numel() * 4 for v in (hX, hY, ha, hb))
-    d2h = (B + B * n * d) * 4
-    hcost = torch.empty(B, dtype=torch.float32).pin_memory()
-    hgrad = torch.empty(B, n, d, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in)
+    d2h = 0
     barrier(ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = 0.0
+    e2e_ms, e2e_pairs = 0.0, 0.0
     for k in range(0 if args.no_e2e else args.steps):
         flush_buf.zero_()
         e0.record(stream)
-        Xs, Ys, As, Bs = (v.to(dev, non_blocking=True) for v in (hX, hY, ha, hb))
-        cost, grad, _ = step(Xs, Ys, As, Bs)
-        hcost.copy_(cost, non_blocking=True)
-        hgrad.copy_(grad, non_blocking=True)
+        ins = [v.to(dev, non_blocking=True) for v in host_in]
+        outs, inf2 = step(ins)
+        hosts = [o.to("cpu", non_blocking=True) for o in outs]
         e1.record(stream)
         e1.synchronize()
+        d2h = sum(o.numel() * o.element_size() for o in outs)
         e2e_ms += e0.elapsed_time(e1)
+        e2e_pairs += step_pairs(inf2)
     e2e_max = max_over_ranks(e2e_ms / 1e3, ws, dev) if not args.no_e2e else None
 
     if rank != 0:
@@ -294,7 +318,8 @@ def run_gpu(args, ws, rank, local):
         mufu_peak = rates["ex2_per_sm_clk"] * sms * mhz * 1e6
         mufu = {"achieved_ex2_per_s": per_launch_pairs / secs, "peak_ex2_per_s": mufu_peak,
                 "frac": per_launch_pairs / secs / mufu_peak}
-    if sot.sot_select_path(d, flags) == 2:
+    path = sot.sot_select_path(d, flags)
+    if path == 2:
         flops_pair = 3 * 2 * d  # fp16 products hi*hi + hi*lo + lo*hi, 2 flops per multiply-add
         achieved = flops_pair * per_launch_pairs / secs / 1e12
         peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
@@ -304,14 +329,18 @@ def run_gpu(args, ws, rank, local):
                 "kernel": "tc_half_kernel (tcgen05 kind::f16, 3 products per pair)"}
         dtype = "f16x3"
     else:
-        flops_pair = 2 * d  # one FMA per coordinate
-        achieved = flops_pair * per_launch_pairs / secs / 1e12
         lanes = rates["ffma_lanes_per_sm_clk"] if rates else 128.0
-        peak = 2 * lanes * sms * mhz * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None,
-                "peak_source": f"{'measured' if rates else 'nominal'} {lanes:.0f} FP32 FMA lanes/SM/clk x {sms} SMs x "
-                               f"{mhz:.0f} MHz x 2", "kernel": "dense_half_kernel (fp32 FMA)"}
+        src = f"{'measured' if rates else 'nominal'} {lanes:.0f} FP32 lanes/SM/clk x {sms} SMs x {mhz:.0f} MHz"
+        if path == 1:
+            ops_pair, unit, kern = 2 * d, "TFLOP/s", "dense_half_kernel (fp32 FMA, 2 flops per FMA)"
+            peak = 2 * lanes * sms * mhz * 1e6 / 1e12
+            src += " x 2"
+        else:
+            ops_pair, unit, kern = 5, "Tops/s", "point_half_kernel (3 FFMA + 2 FADD lane-ops per pair)"
+            peak = lanes * sms * mhz * 1e6 / 1e12
+        achieved = ops_pair * per_launch_pairs / secs / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": None, "peak_source": src, "kernel": kern}
         dtype = "f32"
     roof["mufu"] = mufu
     roof["alu_rates"] = rates
@@ -321,23 +350,25 @@ def run_gpu(args, ws, rank, local):
         r, rows, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], eps)
         cpu = {"value": r / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle",
                "sample": f"f-half of {rows} rows x {m} columns (d={d}), {t:.1f} s"}
-    value = ws * pairs * args.steps / t_max / 1e9
+    value = ws * pairs_total / t_max / 1e9
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "metric": metric_name(wid), "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": dtype, "data": "synthetic",
-        "config": {"workload": w["name"], "B": B, "n": n, "m": m, "d": d, "eps": eps, "iters": iters,
+        "config": {"workload": w["name"], "B": B, "n": n, "m": m, "d": d, "eps": eps,
+                   "iters": info["iters_done"], **({"stages": info["stages_done"]} if wid == 3 else {}),
+                   **({"nnz": info.get("nnz")} if wid == 5 else {}),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
-        "iters_per_s": ws * iters * args.steps / t_max,
+        "iters_per_s": ws * sum([info["iters_done"]]) * args.steps / t_max,
         "half_step": {"launches": nl, "avg_ms": per_launch_ms, "pairs_per_launch": per_launch_pairs},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": None if e2e_max is None else {"value": ws * pairs * args.steps / e2e_max / 1e9, "unit": UNIT,
+        "e2e": None if e2e_max is None else {"value": ws * e2e_pairs / e2e_max / 1e9, "unit": UNIT,
                                              "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
-        "marginal_err": info["err"][0] if info else None,
+        "marginal_err": max(info["err"]) if info else None,
         "wall_s": t_wall,
     }
     print(json.dumps(line), flush=True)
@@ -351,6 +382,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--prec", choices=["auto", "fp32", "f16x3"], default="auto")
+    ap.add_argument("--workload", type=int, choices=sorted(datagen.WORKLOADS), default=WORKLOAD_ID,
+                    help="1-5; the default (4: n=m=70000, d=64) is the headline configuration")
     ap.add_argument("--n", type=int, default=0, help="override n = m (testing only)")
     ap.add_argument("--iters", type=int, default=0, help="override the iteration count (testing only)")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
