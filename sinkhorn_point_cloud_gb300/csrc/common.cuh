@@ -40,6 +40,11 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -96,6 +101,32 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
     if (m == -INFINITY || s == 0.f) { m = m2; s = s2; return; }
     if (m2 > m) { s = s * ex2f(m - m2) + s2; m = m2; }
     else        { s = s + s2 * ex2f(m2 - m); }
+}
+
+// Order-preserving float <-> unsigned map (for atomicMin on floats):
+// unsigned order of the keys equals the numeric order of the floats.
+#define SOT_ORD_EMPTY 0xFFFFFFFFu  /* identity of the minimum */
+__device__ __forceinline__ unsigned ord_encode(float v) {
+    const unsigned u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord_decode(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Stabiliser of a row at the start of a half-step.  With a per-cloud bound
+// lo = min over the other side of (state_before - state_after) from the
+// half-step that produced the current column state, the new row value
+// satisfies L_new >= L_old + lo, so starting at m = L_old + lo keeps the row
+// sum >= 1 (no underflow).  Without a bound: previous value minus a bias,
+// or -inf on a cold start.
+__device__ __forceinline__ float stabiliser(int cold, const unsigned* lo_in, int b, float old) {
+    if (cold) return -INFINITY;
+    if (lo_in) {
+        const float lo = ord_decode(lo_in[b]);
+        if (isfinite(lo)) return old + lo;
+    }
+    return old - SOT_STAB_BIAS;
 }
 
 // Device status bits (OR-ed into a status word).

@@ -102,14 +102,17 @@ __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
     const size_t rbase = (size_t)b * p.nr;
     const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
 
+    if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int k = threadIdx.x; k < p.B; k += DN_T) p.lo_reset[k] = SOT_ORD_EMPTY;
     dense_stage(Xs, rows, row0, DN_RT, p.nr, d);
-    float m[4], s[4];
+    float m[4], s[4], old[4];
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
         const int row = row0 + 4 * tr + rr;
+        old[rr] = (MODE == MODE_LSE && row < p.nr && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
         if (MODE == MODE_MAX) m[rr] = -INFINITY;
         else if (row >= p.nr) m[rr] = INFINITY;
-        else m[rr] = p.cold ? -INFINITY : p.rstate_in[rbase + row] - SOT_STAB_BIAS;
+        else m[rr] = stabiliser(p.cold, p.lo_in, b, old[rr]);
         s[rr] = 0.f;
     }
     const float tk = p.two_kappa;
@@ -238,18 +241,29 @@ __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
                 atomicOr(p.status, SOT_DEV_RETRY_ROWS);
             }
         }
-        if (p.errpart) {
+        if (p.errpart || p.lo_out) {
             __syncthreads();
-            float e = 0.f;
+            float e = 0.f, lo = INFINITY;
             const float wu = 1.f / (float)p.nr;
-            for (int r = threadIdx.x; r < DN_RT; r += DN_T) {
-                const int row = row0 + r;
-                if (row >= p.nr) continue;
-                const float w = p.rweight ? p.rweight[rbase + row] : wu;
-                e += w * fabsf(ex2f(p.rstate_out[rbase + row] - p.rstate_in[rbase + row]) - 1.f);
+            if (tc == 0) {
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int row = row0 + 4 * tr + rr;
+                    if (row >= p.nr) continue;
+                    const float nv = p.rstate_out[rbase + row];
+                    const float w = p.rweight ? p.rweight[rbase + row] : wu;
+                    e += w * fabsf(ex2f(nv - old[rr]) - 1.f);
+                    lo = fminf(lo, old[rr] - nv);
+                }
             }
-            e = block_sum<DN_T>(e, red);
-            if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rt] = e;
+            if (p.errpart) {
+                e = block_sum<DN_T>(e, red);
+                if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rt] = e;
+            }
+            if (p.lo_out) {
+                lo = warp_min(lo);
+                if ((threadIdx.x & 31) == 0 && lo < INFINITY) atomicMin(p.lo_out + b, ord_encode(lo));
+            }
         }
     }
 }

@@ -101,8 +101,10 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
     const float* cst = p.cstate + (size_t)b * p.nc;
     const size_t rbase = (size_t)b * p.nr;
 
+    if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int k = threadIdx.x; k < p.B; k += PT_T) p.lo_reset[k] = SOT_ORD_EMPTY;
     float2 q0[PT_RPT], q1[PT_RPT], q2[PT_RPT], nm[PT_RPT];
-    float m[PT_RPT], s[PT_RPT];
+    float m[PT_RPT], s[PT_RPT], old[PT_RPT];
 #pragma unroll
     for (int r = 0; r < PT_RPT; ++r) {
         const int row = row0 + threadIdx.x + r * PT_T;
@@ -112,12 +114,13 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
         q0[r] = make_float2(a0, a0);
         q1[r] = make_float2(a1, a1);
         q2[r] = make_float2(a2, a2);
+        old[r] = (MODE == MODE_LSE && valid && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
         if (MODE == MODE_MAX) {
             m[r] = -INFINITY;
         } else if (!valid) {
             m[r] = INFINITY;  // every term becomes 2^-inf = 0; never written
         } else {
-            m[r] = p.cold ? -INFINITY : p.rstate_in[rbase + row] - SOT_STAB_BIAS;
+            m[r] = stabiliser(p.cold, p.lo_in, b, old[r]);
         }
         nm[r] = make_float2(-m[r], -m[r]);
         s[r] = 0.f;
@@ -258,19 +261,27 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
                 atomicOr(p.status, SOT_DEV_RETRY_ROWS);
             }
         }
-        if (p.errpart) {
+        if (p.errpart || p.lo_out) {
             __syncthreads();
-            float e = 0.f;
+            float e = 0.f, lo = INFINITY;
             const float wu = 1.f / (float)p.nr;
 #pragma unroll
             for (int r = 0; r < PT_RPT; ++r) {
                 const int row = row0 + threadIdx.x + r * PT_T;
                 if (row >= p.nr) continue;
+                const float nv = p.rstate_out[rbase + row];
                 const float w = p.rweight ? p.rweight[rbase + row] : wu;
-                e += w * fabsf(ex2f(p.rstate_out[rbase + row] - p.rstate_in[rbase + row]) - 1.f);
+                e += w * fabsf(ex2f(nv - old[r]) - 1.f);
+                lo = fminf(lo, old[r] - nv);
             }
-            e = block_sum<PT_T>(e, red);
-            if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rt] = e;
+            if (p.errpart) {
+                e = block_sum<PT_T>(e, red);
+                if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rt] = e;
+            }
+            if (p.lo_out) {
+                lo = warp_min(lo);
+                if ((threadIdx.x & 31) == 0 && lo < INFINITY) atomicMin(p.lo_out + b, ord_encode(lo));
+            }
         }
     }
 }

@@ -355,6 +355,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     const float sc = ops.scale[b];
     const float tk = p.two_kappa / (sc * sc);
 
+    if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int k = threadIdx.x; k < p.B; k += TC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
     const uint32_t tmem = tc_setup(S, warp);
 
     float m = 0.f, s = 0.f;  // epilogue row state
@@ -362,6 +364,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     const int q4 = warp & 3;         // TMEM lane quarter this warp may access
     const int row = row0 + wg * TC_M + q4 * 32 + lane;
     const bool erow = (warp >= 2) && row < p.nr;
+    const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
         tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst, nullptr);
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
         tc_mma(S, tmem, nt);
     } else {
         // ---------------- epilogue: exponentials and row sums ----------------
-        m = erow ? (p.cold ? -INFINITY : p.rstate_in[rbase + row] - SOT_STAB_BIAS) : INFINITY;
+        m = erow ? stabiliser(p.cold, p.lo_in, b, old) : INFINITY;
         s = 0.f;
         const float2 tk2 = make_float2(tk, tk);
         const float* bias = S.bias();
@@ -500,15 +503,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             atomicOr(p.status, SOT_DEV_RETRY_ROWS);
         }
     }
-    if (p.errpart) {
+    if (p.errpart || p.lo_out) {
         __syncthreads();
-        float e = 0.f;
+        float e = 0.f, lo = INFINITY;
         if (erow) {
+            const float nv = p.rstate_out[rbase + row];
             const float w = p.rweight ? p.rweight[rbase + row] : 1.f / (float)p.nr;
-            e = w * fabsf(ex2f(p.rstate_out[rbase + row] - p.rstate_in[rbase + row]) - 1.f);
+            e = w * fabsf(ex2f(nv - old) - 1.f);
+            lo = old - nv;
         }
-        e = block_sum<TC_THREADS>(e, red);
-        if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rb] = e;
+        if (p.errpart) {
+            e = block_sum<TC_THREADS>(e, red);
+            if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rb] = e;
+        }
+        if (p.lo_out) {
+            lo = warp_min(lo);
+            if (lane == 0 && lo < INFINITY) atomicMin(p.lo_out + b, ord_encode(lo));
+        }
     }
 }
 

@@ -42,6 +42,9 @@ struct HalfArgs {
     float* errpart;         // [B*rowtiles] row-marginal error partials or NULL
     const int* stop_flag;   // NULL or device flag: nonzero => kernel returns at once
     int* status;            // device status word (SOT_DEV_* bits)
+    const unsigned* lo_in;  // [B] stabiliser bound from the other side (ord-encoded) or NULL
+    unsigned* lo_out;       // [B] receives min over rows of (old - new) (ord-encoded) or NULL
+    unsigned* lo_reset;     // [B] slot reset to SOT_ORD_EMPTY by block (0,0) or NULL
 };
 
 struct ApplyArgs {

@@ -202,6 +202,11 @@ struct Solver {
     float *part_m = nullptr, *part_s = nullptr, *errpart = nullptr, *err = nullptr;
     unsigned* counters = nullptr;
     int* dflags = nullptr;  // [0] status, [1] stop, [2] conv, [3..] per-stage iteration counts
+    // Stabiliser bounds: lo[side][slot][B] = min over that side's rows of
+    // (state before - state after) of its last half-steps (two slots, alternating).
+    unsigned* lo = nullptr;
+    int seq[2] = {0, 0};
+    bool bound_ok = false;  // the other side's last bound is valid for the next half-step
     int nstage_slots = 0;
     int sms;
     int split[2], chunk[2], rowtiles[2];  // [0] f-half (rows X), [1] g-half (rows Y)
@@ -222,6 +227,7 @@ struct Solver {
         L = S.alloc<float>((size_t)B * n);
         Lam = S.alloc<float>((size_t)B * m);
         dflags = S.alloc<int>(3 + stage_slots);
+        lo = S.alloc<unsigned>((size_t)4 * B);
         if (point) {
             xpack = S.alloc<float>((size_t)B * n * 4);
             ypack = S.alloc<float>((size_t)B * m * 4);
@@ -231,9 +237,10 @@ struct Solver {
             lw2x = S.alloc<float>((size_t)B * n);
             lw2y = S.alloc<float>((size_t)B * m);
         }
-        if (!shift || !nx || !ny || !L || !Lam || !dflags || !xpack || !ypack || (!point && (!lw2x || !lw2y)))
+        if (!shift || !nx || !ny || !L || !Lam || !dflags || !lo || !xpack || !ypack || (!point && (!lw2x || !lw2y)))
             return fail(SOT_ERR_NOMEM, "scratch allocation failed");
         SOT_CUDA(cudaMemsetAsync(dflags, 0, sizeof(int) * (3 + stage_slots), st));
+        SOT_CUDA(cudaMemsetAsync(lo, 0xFF, sizeof(unsigned) * 4 * B, st));  // empty minima
         SOT_CUDA(launch_center(X, Y, B, n, m, d, shift, st));
         SOT_CUDA(launch_pack(X, a, B, n, d, shift, point, xpack, lw2x, nx, st));
         SOT_CUDA(launch_pack(Y, b, B, m, d, shift, point, ypack, lw2y, ny, st));
@@ -304,7 +311,17 @@ struct Solver {
     }
 
     int half(int h, int mode, float kappa, bool cold, const float* rin, float* rout, float* errp, bool guarded) {
-        const HalfArgs p = half_args(h, kappa, cold, rin, rout, errp, guarded);
+        HalfArgs p = half_args(h, kappa, cold, rin, rout, errp, guarded);
+        p.lo_in = nullptr;
+        p.lo_out = nullptr;
+        p.lo_reset = nullptr;
+        if (mode == MODE_LSE && lo) {
+            p.lo_out = lo + (size_t)(2 * h + (seq[h] & 1)) * B;
+            p.lo_reset = lo + (size_t)(2 * h + ((seq[h] + 1) & 1)) * B;
+            if (!cold && bound_ok && seq[1 - h] > 0)
+                p.lo_in = lo + (size_t)(2 * (1 - h) + ((seq[1 - h] - 1) & 1)) * B;
+            ++seq[h];
+        }
         cudaError_t e;
         {
             ProfScope ps(st, mode == MODE_LSE);
@@ -328,12 +345,18 @@ struct Solver {
         return SOT_OK;
     }
 
-    // Plain iteration: f-half then g-half, both in place.
+    // Plain iteration: f-half then g-half, both in place.  The first iteration
+    // of a stage runs cold (stabiliser -inf); later ones use the bounds.
     int iterate(float kappa, bool cold, bool guarded) {
         int rc = half(0, MODE_LSE, kappa, cold, L, L, nullptr, guarded);
         if (rc) return rc;
-        return half(1, MODE_LSE, kappa, cold, Lam, Lam, nullptr, guarded);
+        rc = half(1, MODE_LSE, kappa, cold, Lam, Lam, nullptr, guarded);
+        bound_ok = true;
+        return rc;
     }
+
+    // A new eps stage starts: states are rescaled, the last bounds no longer apply.
+    void new_stage() { bound_ok = false; }
 
     // Stop-tested step: the f-half of the next iteration evaluates the
     // row-marginal error of the current iterate; the decision either stops
@@ -343,7 +366,7 @@ struct Solver {
             Lnext = S.alloc<float>((size_t)B * n);
             if (!Lnext) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
         }
-        int rc = half(0, MODE_LSE, kappa, false, L, Lnext, errpart, true);
+        int rc = half(0, MODE_LSE, kappa, !bound_ok, L, Lnext, errpart, true);
         if (rc) return rc;
         SOT_CUDA(launch_decide(errpart, B, rowtiles[0], tol, force, err, stop_flag(), conv_flag(), Lnext, L, B * n, st));
         return SOT_OK;
@@ -393,6 +416,8 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
             SOT_CUDA(launch_scale(sv.Lam, ratio, sv.B * sv.m, sv.st));
         }
         SOT_CUDA(cudaMemsetAsync(sv.stop_flag(), 0, 2 * sizeof(int), sv.st));  // stop + conv
+        sv.new_stage();
+        cold = true;
         stages_done = k + 1;
         int* counter = sv.dflags + 3 + k;
         const bool final_stage = (k == K - 1);
