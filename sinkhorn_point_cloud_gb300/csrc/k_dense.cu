@@ -145,21 +145,28 @@ __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) ts += ex2f(fmaf(tk, acc[rr][cc], cb[cc] - m[rr]));
                 ts = sum16(ts);
-                if (!(ts < SOT_TILE_SUM_MAX)) {
+                // The two half-warps own different rows: the slow path is entered by
+                // the whole warp (its shuffles need every lane) and applied per row.
+                const bool ovf = !(ts < SOT_TILE_SUM_MAX);
+                if (__any_sync(0xffffffffu, ovf)) {
                     float mx = -INFINITY;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) mx = fmaxf(mx, fmaf(tk, acc[rr][cc], cb[cc]));
                     mx = max16(mx);
                     const float mn = fmaxf(m[rr], mx);
-                    if (mn == -INFINITY) {
-                        ts = 0.f;
-                    } else {
-                        s[rr] = (m[rr] == -INFINITY) ? 0.f : s[rr] * ex2f(m[rr] - mn);
-                        m[rr] = mn;
-                        ts = 0.f;
+                    const float mu = (ovf && mn > -INFINITY) ? mn : m[rr];
+                    float ts2 = 0.f;
 #pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) ts += ex2f(fmaf(tk, acc[rr][cc], cb[cc] - mn));
-                        ts = sum16(ts);
+                    for (int cc = 0; cc < 4; ++cc) ts2 += ex2f(fmaf(tk, acc[rr][cc], cb[cc] - mu));
+                    ts2 = sum16(ts2);
+                    if (ovf) {
+                        if (mn == -INFINITY) {
+                            ts = 0.f;
+                        } else {
+                            s[rr] = (m[rr] == -INFINITY) ? 0.f : s[rr] * ex2f(m[rr] - mn);
+                            m[rr] = mn;
+                            ts = ts2;
+                        }
                     }
                 }
                 s[rr] += ts;
@@ -348,16 +355,19 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
             }
             ts = sum16(ts);
             sc[rr] = 1.f;
-            if (!(ts < SOT_TILE_SUM_MAX)) {
+            const bool ovf = !(ts < SOT_TILE_SUM_MAX);
+            if (__any_sync(0xffffffffu, ovf)) {  // warp-wide: the shuffles need every lane
                 float mx = -INFINITY;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) mx = fmaxf(mx, fmaf(tk, acc[rr][cc], cb[cc] - Lr[rr]));
                 mx = max16(mx);
-                const float mn = fmaxf(m[rr], mx);
-                sc[rr] = ex2f(m[rr] - mn);
-                m[rr] = mn;
+                if (ovf) {
+                    const float mn = fmaxf(m[rr], mx);
+                    sc[rr] = ex2f(m[rr] - mn);
+                    m[rr] = mn;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) w[cc] = ex2f(fmaf(tk, acc[rr][cc], cb[cc] - Lr[rr] - mn));
+                    for (int cc = 0; cc < 4; ++cc) w[cc] = ex2f(fmaf(tk, acc[rr][cc], cb[cc] - Lr[rr] - mn));
+                }
             }
             float tq = 0.f, trs = 0.f;
 #pragma unroll
