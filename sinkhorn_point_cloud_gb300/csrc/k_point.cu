@@ -1,25 +1,31 @@
 // k_point.cu -- fused Sinkhorn half-steps for point clouds with d <= 3 on
-// FP32 FMA + MUFU ex2 (no tensor cores: a 3-term dot product is no dense
+// FP32 FMA + MUFU ex2 (no tensor cores: a 3-term distance is no dense
 // contraction).
 //
 // One half-step ("FlashSinkhorn", Methodologie 1-2) for row i of the updated
-// side, in base 2 with kappa = 1/(eps ln 2):
-//     L_i = log2 sum_j 2^( 2 kappa x_i.y_j + c_j ),   c_j = log2 w_j - Lam_j
+// side, in base 2 with kappa = 1/(eps ln 2) and the state L_i = -kappa f_i
+// (Lam_j = -kappa g_j):
+//     L_i = log2 sum_j 2^( c_j - kappa |x_i - y_j|^2 ),   c_j = log2 w_j - Lam_j
+// The squared distance is formed in the direct form from coordinates scaled
+// by sqrt(kappa): in fp32 the expanded form 2 kappa x.y - kappa |y|^2 rounds at
+// the magnitude of kappa |x||y| and, at eps = 1e-2 on unit-sphere clouds, moved
+// the gradient by ~1e-4 relative; the direct form rounds at the magnitude of
+// the (small) distances that matter and stays near 5e-6.
 // The score tile is formed in registers from a column tile staged in shared
 // memory and never stored; the row-wise log-sum-exp is accumulated on chip
 // (Methodologie 2, "Online LSE"), one row block stays resident while every
 // column tile streams past it (row-stationary traversal).
 //
-// Stabiliser.  Each row keeps a running (m, s) with value m + log2 s.  m
-// starts at the previous row value minus a bias (or -inf on a cold start) so
-// a column costs 3 FFMA + 1 FADD + 1 ex2 + 1 FADD and no per-pair max.  A
-// tile whose sum leaves the safe range takes a slow path that recomputes it
+// Stabiliser.  Each row keeps a running (m, s) with value m + log2 s; m starts
+// at a bound that keeps the sum >= 1 (see stabiliser() in common.cuh) or -inf
+// on a cold start, so a column costs 3 FADD + 3 FFMA + 1 FADD + 1 ex2 + 1 FADD
+// and no per-pair max.  A tile whose sum leaves the safe range is recomputed
 // against the tile maximum, so the result is the exact LSE for any start.
-// Rows whose final sum underflowed are recomputed with a two-pass LSE.
 //
 // Layout of a column tile in shared memory: column pairs interleaved so that
-// one 16-byte load yields two 2-lane operands of the packed f32x2 FMA:
-//     tile[2p]   = (x_j, x_j', y_j, y_j'),   tile[2p+1] = (z_j, z_j', c_j, c_j')
+// one 16-byte load yields two 2-lane operands of the packed f32x2 arithmetic:
+//     tile[2p]   = (-v_j.x, -v_j'.x, -v_j.y, -v_j'.y),
+//     tile[2p+1] = (-v_j.z, -v_j'.z, -c_j,   -c_j')      with v = sqrt(kappa) y.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -33,30 +39,43 @@ constexpr int PT_TC = 2 * PT_T;         // columns per shared-memory tile
 int point_rows_per_cta() { return PT_ROWS; }
 int point_cols_per_tile() { return PT_TC; }
 
-// Score of two columns for one row: t = ((c + q0*x) + q1*y) + q2*z, fp32 FMAs
-// in this fixed order (the COO kernels evaluate the same chain).
+// Score relative to a base: acc = base + |u - v|^2 with d = u + (-v), fp32 in
+// this fixed order (the maximum passes and the COO predicate evaluate the same
+// chain, so their decisions agree bit for bit).  The score is t = m - acc when
+// base = m - c.
 template <int D>
-__device__ __forceinline__ float2 pair_chain(float2 t, float2 q0, float2 q1, float2 q2, float4 A, float4 Bv) {
-    if (D >= 1) t = ffma2(q0, make_float2(A.x, A.y), t);
-    if (D >= 2) t = ffma2(q1, make_float2(A.z, A.w), t);
-    if (D >= 3) t = ffma2(q2, make_float2(Bv.x, Bv.y), t);
-    return t;
+__device__ __forceinline__ float2 pair_chain(float2 acc, float2 u0, float2 u1, float2 u2, float4 A, float4 Bv) {
+    if (D >= 1) { const float2 d = fadd2(u0, make_float2(A.x, A.y)); acc = ffma2(d, d, acc); }
+    if (D >= 2) { const float2 d = fadd2(u1, make_float2(A.z, A.w)); acc = ffma2(d, d, acc); }
+    if (D >= 3) { const float2 d = fadd2(u2, make_float2(Bv.x, Bv.y)); acc = ffma2(d, d, acc); }
+    return acc;
 }
+// Scalar form of the same chain for one (row, column): u = scaled row point,
+// nv = negated scaled column point, base = m - c.
 template <int D>
-__device__ __forceinline__ float scalar_chain(float t, float q0, float q1, float q2, float4 c) {
-    if (D >= 1) t = fmaf(q0, c.x, t);
-    if (D >= 2) t = fmaf(q1, c.y, t);
-    if (D >= 3) t = fmaf(q2, c.z, t);
-    return t;
+__device__ __forceinline__ float scalar_chain(float base, float u0, float u1, float u2, float nv0, float nv1,
+                                              float nv2) {
+    float acc = base;
+    if (D >= 1) { const float d = u0 + nv0; acc = fmaf(d, d, acc); }
+    if (D >= 2) { const float d = u1 + nv1; acc = fmaf(d, d, acc); }
+    if (D >= 3) { const float d = u2 + nv2; acc = fmaf(d, d, acc); }
+    return acc;
 }
 
-// Stage columns [base, base + PT_TC) of the chunk ending at c_end.
+// Stage columns [base, base + PT_TC) of the chunk ending at c_end: scaled,
+// negated coordinates and the negated column bias.
 __device__ __forceinline__ void load_point_tile(float4* tile, const float4* cp, const float* cst, int base,
-                                                int c_end) {
+                                                int c_end, float sk) {
     const int j0 = base + 2 * threadIdx.x, j1 = j0 + 1;
-    float4 c0 = make_float4(0.f, 0.f, 0.f, -INFINITY), c1 = c0;
-    if (j0 < c_end) { c0 = cp[j0]; c0.w = c0.w - cst[j0]; }
-    if (j1 < c_end) { c1 = cp[j1]; c1.w = c1.w - cst[j1]; }
+    float4 c0 = make_float4(0.f, 0.f, 0.f, INFINITY), c1 = c0;  // padding: -c = +inf -> score -inf
+    if (j0 < c_end) {
+        const float4 y = cp[j0];
+        c0 = make_float4(-(sk * y.x), -(sk * y.y), -(sk * y.z), -(y.w - cst[j0]));
+    }
+    if (j1 < c_end) {
+        const float4 y = cp[j1];
+        c1 = make_float4(-(sk * y.x), -(sk * y.y), -(sk * y.z), -(y.w - cst[j1]));
+    }
     tile[2 * threadIdx.x] = make_float4(c0.x, c1.x, c0.y, c1.y);
     tile[2 * threadIdx.x + 1] = make_float4(c0.z, c1.z, c0.w, c1.w);
 }
@@ -64,19 +83,19 @@ __device__ __forceinline__ void load_point_tile(float4* tile, const float4* cp, 
 // Two-pass LSE of one full row by the whole CTA (slow path for rows whose
 // stabilised sum underflowed).  Returns log2 sum_j 2^(score_j).
 template <int D>
-__device__ float point_row_full(const float4* cp, const float* cst, int nc, float q0, float q1, float q2,
+__device__ float point_row_full(const float4* cp, const float* cst, int nc, float u0, float u1, float u2, float sk,
                                 float* red) {
     float mx = -INFINITY;
     for (int j = threadIdx.x; j < nc; j += PT_T) {
-        float4 c = cp[j];
-        mx = fmaxf(mx, scalar_chain<D>(c.w - cst[j], q0, q1, q2, c));
+        const float4 c = cp[j];
+        mx = fmaxf(mx, -scalar_chain<D>(-(c.w - cst[j]), u0, u1, u2, -(sk * c.x), -(sk * c.y), -(sk * c.z)));
     }
     mx = block_max<PT_T>(mx, red);
     if (mx == -INFINITY) return -INFINITY;
     float sm = 0.f;
     for (int j = threadIdx.x; j < nc; j += PT_T) {
-        float4 c = cp[j];
-        sm += ex2f(scalar_chain<D>(c.w - cst[j], q0, q1, q2, c) - mx);
+        const float4 c = cp[j];
+        sm += ex2f(-scalar_chain<D>(-(c.w - cst[j]), u0, u1, u2, -(sk * c.x), -(sk * c.y), -(sk * c.z)) - mx);
     }
     sm = block_sum<PT_T>(sm, red);
     return mx + log2f(sm);
@@ -103,6 +122,7 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
 
     if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
         for (int k = threadIdx.x; k < p.B; k += PT_T) p.lo_reset[k] = SOT_ORD_EMPTY;
+    const float sk = sqrtf(0.5f * p.two_kappa);  // sqrt(kappa)
     float2 q0[PT_RPT], q1[PT_RPT], q2[PT_RPT], nm[PT_RPT];
     float m[PT_RPT], s[PT_RPT], old[PT_RPT];
 #pragma unroll
@@ -110,7 +130,7 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
         const int row = row0 + threadIdx.x + r * PT_T;
         const bool valid = row < p.nr;
         float4 x = valid ? rp[row] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float a0 = p.two_kappa * x.x, a1 = p.two_kappa * x.y, a2 = p.two_kappa * x.z;
+        const float a0 = sk * x.x, a1 = sk * x.y, a2 = sk * x.z;  // scaled row point u
         q0[r] = make_float2(a0, a0);
         q1[r] = make_float2(a1, a1);
         q2[r] = make_float2(a2, a2);
@@ -122,13 +142,13 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
         } else {
             m[r] = stabiliser(p.cold, p.lo_in, b, old[r]);
         }
-        nm[r] = make_float2(-m[r], -m[r]);
+        nm[r] = make_float2(m[r], m[r]);  // base of the chain: m - c
         s[r] = 0.f;
     }
 
     for (int base = c_begin; base < c_end; base += PT_TC) {
         __syncthreads();
-        load_point_tile(tile, cp, cst, base, c_end);
+        load_point_tile(tile, cp, cst, base, c_end, sk);
         __syncthreads();
         if (MODE == MODE_MAX) {
             float2 mx[PT_RPT];
@@ -137,12 +157,12 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
 #pragma unroll 4
             for (int pp = 0; pp < PT_TC / 2; ++pp) {
                 const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
-                const float2 cj = make_float2(Bv.z, Bv.w);
+                const float2 ncj = make_float2(Bv.z, Bv.w);
 #pragma unroll
                 for (int r = 0; r < PT_RPT; ++r) {
-                    float2 t = pair_chain<D>(cj, q0[r], q1[r], q2[r], A, Bv);
-                    mx[r].x = fmaxf(mx[r].x, t.x);
-                    mx[r].y = fmaxf(mx[r].y, t.y);
+                    const float2 acc = pair_chain<D>(ncj, q0[r], q1[r], q2[r], A, Bv);  // = |u-v|^2 - c
+                    mx[r].x = fmaxf(mx[r].x, -acc.x);
+                    mx[r].y = fmaxf(mx[r].y, -acc.y);
                 }
             }
 #pragma unroll
@@ -154,11 +174,11 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
 #pragma unroll 4
             for (int pp = 0; pp < PT_TC / 2; ++pp) {
                 const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
-                const float2 cj = make_float2(Bv.z, Bv.w);
+                const float2 ncj = make_float2(Bv.z, Bv.w);
 #pragma unroll
                 for (int r = 0; r < PT_RPT; ++r) {
-                    float2 t = pair_chain<D>(fadd2(cj, nm[r]), q0[r], q1[r], q2[r], A, Bv);
-                    st[r] = fadd2(st[r], make_float2(ex2f(t.x), ex2f(t.y)));
+                    const float2 acc = pair_chain<D>(fadd2(nm[r], ncj), q0[r], q1[r], q2[r], A, Bv);  // m - t
+                    st[r] = fadd2(st[r], make_float2(ex2f(-acc.x), ex2f(-acc.y)));
                 }
             }
 #pragma unroll
@@ -169,8 +189,8 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
                     float mt = -INFINITY;
                     for (int pp = 0; pp < PT_TC / 2; ++pp) {
                         const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
-                        float2 t = pair_chain<D>(make_float2(Bv.z, Bv.w), q0[r], q1[r], q2[r], A, Bv);
-                        mt = fmaxf(mt, fmaxf(t.x, t.y));
+                        const float2 acc = pair_chain<D>(make_float2(Bv.z, Bv.w), q0[r], q1[r], q2[r], A, Bv);
+                        mt = fmaxf(mt, fmaxf(-acc.x, -acc.y));
                     }
                     const float mn = fmaxf(m[r], mt);
                     if (mn == -INFINITY) {
@@ -178,15 +198,15 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
                     } else {
                         s[r] = (m[r] == -INFINITY) ? 0.f : s[r] * ex2f(m[r] - mn);
                         m[r] = mn;
-                        nm[r] = make_float2(-mn, -mn);
-                        float2 acc = make_float2(0.f, 0.f);
+                        nm[r] = make_float2(mn, mn);
+                        float2 sum = make_float2(0.f, 0.f);
                         for (int pp = 0; pp < PT_TC / 2; ++pp) {
                             const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
-                            float2 t = pair_chain<D>(fadd2(make_float2(Bv.z, Bv.w), nm[r]), q0[r], q1[r],
-                                                     q2[r], A, Bv);
-                            acc = fadd2(acc, make_float2(ex2f(t.x), ex2f(t.y)));
+                            const float2 acc = pair_chain<D>(fadd2(nm[r], make_float2(Bv.z, Bv.w)), q0[r], q1[r],
+                                                             q2[r], A, Bv);
+                            sum = fadd2(sum, make_float2(ex2f(-acc.x), ex2f(-acc.y)));
                         }
-                        ts = acc.x + acc.y;
+                        ts = sum.x + sum.y;
                     }
                 }
                 s[r] += ts;
@@ -254,8 +274,7 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
         for (int k = 0; k < nretry; ++k) {
             const int row = s_retry[k];
             const float4 x = rp[row];
-            const float v = point_row_full<D>(cp, cst, p.nc, p.two_kappa * x.x, p.two_kappa * x.y,
-                                              p.two_kappa * x.z, red);
+            const float v = point_row_full<D>(cp, cst, p.nc, sk * x.x, sk * x.y, sk * x.z, sk, red);
             if (threadIdx.x == 0) {
                 p.rstate_out[rbase + row] = v;
                 atomicOr(p.status, SOT_DEV_RETRY_ROWS);
@@ -428,12 +447,14 @@ cudaError_t launch_point_apply(const ApplyArgs& p, cudaStream_t st) {
 // Pair (i, j) is kept when
 //   (dirs & 1) and t_ij >= Mr_i + log2 tau   (row-relative), or
 //   (dirs & 2) and u_ji >= Mc_j + log2 tau   (column-relative),
-// with t_ij = 2 kappa x_i.y_j + log2 b_j - Lam_j evaluated by the same FMA
-// chain as the f-half maximum pass and u_ji = 2 kappa y_j.x_i + log2 a_i - L_i
-// by the chain of the g-half pass, so the maxima and the predicate agree bit
-// for bit.  One warp owns CO_RW rows; its lanes take 32 consecutive columns,
-// and a ballot / popc over the predicate gives each kept pair its slot, so a
-// row's entries come out in ascending column order with coalesced stores.
+// with t_ij = c_j - kappa|x_i - y_j|^2 (c_j = log2 b_j - Lam_j) and
+// u_ji = e_i - kappa|x_i - y_j|^2 (e_i = log2 a_i - L_i), each evaluated by the
+// same fp32 chain as the maximum pass of its half (the scaled difference
+// u - v is exactly the negation of v - u, so both directions see the same
+// squares); the maxima and the predicate therefore agree bit for bit.  One
+// warp owns CO_RW rows; its lanes take 32 consecutive columns, and a ballot /
+// popc over the predicate gives each kept pair its slot, so a row's entries
+// come out in ascending column order with coalesced stores.
 constexpr int CO_T = 256;
 constexpr int CO_RW = 4;                      // rows per warp
 constexpr int CO_ROWS = (CO_T / 32) * CO_RW;  // rows per CTA
@@ -441,18 +462,18 @@ constexpr int CO_TC = 256;                    // columns per tile
 
 template <int D, bool WRITE>
 __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
-    __shared__ float4 cy[CO_TC];   // (y, log2 b_j - Lam_j)
-    __shared__ float4 cq[CO_TC];   // (2 kappa y, Mc_j + log2 tau)
-    __shared__ float cby[CO_TC];   // kappa ny_j + log2 b_j - Lam_j  (value exponent)
+    __shared__ float4 cy[CO_TC];   // (y, -c_j)  with c_j = log2 b_j - Lam_j
+    __shared__ float4 cv[CO_TC];   // (-sqrt(kappa) y, Mc_j + log2 tau)
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rowb = blockIdx.x * CO_ROWS + warp * CO_RW;
     const float4* xp = reinterpret_cast<const float4*>(p.xpack) + (size_t)b * p.n;
     const float4* yp = reinterpret_cast<const float4*>(p.ypack) + (size_t)b * p.m;
     const size_t xb = (size_t)b * p.n, yb = (size_t)b * p.m;
+    const float sk = sqrtf(p.kappa);
 
     float4 x[CO_RW];
-    float q0[CO_RW], q1[CO_RW], q2[CO_RW], thr_r[CO_RW], e_r[CO_RW], arow[CO_RW];
+    float u0[CO_RW], u1[CO_RW], u2[CO_RW], thr_r[CO_RW], ne_r[CO_RW], arow[CO_RW];
     long long pos[CO_RW];
     int cnt[CO_RW];
 #pragma unroll
@@ -460,11 +481,11 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
         const int i = rowb + r;
         const bool ok = i < p.n;
         x[r] = ok ? xp[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        q0[r] = p.two_kappa * x[r].x;
-        q1[r] = p.two_kappa * x[r].y;
-        q2[r] = p.two_kappa * x[r].z;
+        u0[r] = sk * x[r].x;
+        u1[r] = sk * x[r].y;
+        u2[r] = sk * x[r].z;
         thr_r[r] = ok ? p.Mr[xb + i] + p.log2tau : INFINITY;
-        e_r[r] = ok ? x[r].w - p.L[xb + i] : 0.f;  // log2 a_i - L_i
+        ne_r[r] = ok ? -(x[r].w - p.L[xb + i]) : 0.f;  // -(log2 a_i - L_i)
         arow[r] = ok ? p.kappa * p.nx[xb + i] - p.L[xb + i] : 0.f;
         pos[r] = (WRITE && ok) ? p.rowptr[xb + i] : 0;
         cnt[r] = 0;
@@ -473,32 +494,30 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
         __syncthreads();
         for (int t = threadIdx.x; t < CO_TC; t += CO_T) {
             const int j = base + t;
-            float4 c = make_float4(0.f, 0.f, 0.f, -INFINITY);
+            float4 c = make_float4(0.f, 0.f, 0.f, INFINITY);
             float4 c2 = make_float4(0.f, 0.f, 0.f, INFINITY);
-            float vb = -INFINITY;
             if (j < p.m) {
-                c = yp[j];
-                const float lam = p.Lam[yb + j];
-                c.w = c.w - lam;
-                c2 = make_float4(p.two_kappa * c.x, p.two_kappa * c.y, p.two_kappa * c.z, p.Mc[yb + j] + p.log2tau);
-                vb = fmaf(p.kappa, p.ny[yb + j], c.w);
+                const float4 y = yp[j];
+                c = make_float4(y.x, y.y, y.z, -(y.w - p.Lam[yb + j]));
+                c2 = make_float4(-(sk * y.x), -(sk * y.y), -(sk * y.z), p.Mc[yb + j] + p.log2tau);
             }
             cy[t] = c;
-            cq[t] = c2;
-            cby[t] = vb;
+            cv[t] = c2;
         }
         __syncthreads();
         for (int cc = 0; cc < CO_TC; cc += 32) {
             const int t = cc + lane;
             const int j = base + t;
-            const float4 c = cy[t], c2 = cq[t];
+            const float4 c = cy[t], c2 = cv[t];
 #pragma unroll
             for (int r = 0; r < CO_RW; ++r) {
                 bool keep = false;
-                if (p.dirs & 1) keep = scalar_chain<D>(c.w, q0[r], q1[r], q2[r], c) >= thr_r[r];
+                const float trow = -scalar_chain<D>(c.w, u0[r], u1[r], u2[r], c2.x, c2.y, c2.z);
+                if (p.dirs & 1) keep = trow >= thr_r[r];
                 if (p.dirs & 2) {
-                    const float u = scalar_chain<D>(e_r[r], c2.x, c2.y, c2.z, x[r]);
-                    keep = keep || (u >= c2.w);
+                    // column direction: rows Y, columns X; d = v + (-u) = -(u - v) exactly
+                    const float ucol = -scalar_chain<D>(ne_r[r], -c2.x, -c2.y, -c2.z, -u0[r], -u1[r], -u2[r]);
+                    keep = keep || (ucol >= c2.w);
                 }
                 keep = keep && (j < p.m) && (rowb + r < p.n);
                 const unsigned mask = __ballot_sync(0xffffffffu, keep);
@@ -510,9 +529,10 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
                         if (D >= 2) C = fmaf(d1, d1, C);
                         if (D >= 3) C = fmaf(d2, d2, C);
                         const float ai = p.a ? p.a[xb + rowb + r] : 1.f / (float)p.n;
+                        // P_ij = a_i 2^(c_j - kappa C_ij - L_i)
                         p.rows[o] = rowb + r;
                         p.cols[o] = j;
-                        p.vals[o] = ai * ex2f(fmaf(-p.kappa, C, arow[r] + cby[t]));
+                        p.vals[o] = ai * ex2f(fmaf(-p.kappa, C, arow[r] - c.w));
                     }
                     pos[r] += __popc(mask);
                 } else {

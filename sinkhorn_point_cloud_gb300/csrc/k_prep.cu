@@ -41,7 +41,8 @@ cudaError_t launch_center(const float* X, const float* Y, int B, int n, int m, i
 // ---- packing --------------------------------------------------------------
 // point layout (d <= 3): pack[b][i] = float4(x - t, log2 w) with zero padding;
 // dense layout: pack[b][i][k] = x - t and lw2[b][i] = log2 w.
-// nrm[b][i] = |x - t|^2.  w == NULL means uniform weights 1/n.
+// nrm[b][i] = |x - t|^2 for the dense layout (expanded-form scores) and 0 for
+// the point layout (direct-distance scores).  w == NULL means uniform weights 1/n.
 __global__ void pack_kernel(const float* P, const float* w, int n, int d, const float* shift, int point,
                             float* pack, float* lw2, float* nrm) {
     const int b = blockIdx.y;
@@ -59,6 +60,7 @@ __global__ void pack_kernel(const float* P, const float* w, int n, int d, const 
             acc = fmaf(v[k], v[k], acc);
         }
         reinterpret_cast<float4*>(pack)[pi] = make_float4(v[0], v[1], v[2], lw);
+        acc = 0.f;  // the point path scores with direct distances: its state is L = -kappa f
     } else {
         float* dst = pack + pi * d;
         for (int k = 0; k < d; ++k) {

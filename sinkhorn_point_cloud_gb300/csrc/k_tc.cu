@@ -752,8 +752,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
 #pragma unroll
             for (int k = 0; k < TC_D; ++k) V[k] = fmaf(f, __ldcg(vc + k), V[k]);
         }
+        // the exponents were taken against m (= L_i - bias), so P_ij / a_i = 2^(e + m - L_i)
         const float ai = x.a ? x.a[rbase + row] : 1.f / (float)p.nr;
-        const float fac = nan ? NAN : ai * ex2f(M);
+        const float fac = nan ? NAN : ai * ex2f(M - p.rstate_in[rbase + row]);
         const float ri = fac * R;
         qi = fac * Q;
         if (x.rowsum) x.rowsum[rbase + row] = ri;

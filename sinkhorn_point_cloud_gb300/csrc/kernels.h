@@ -7,11 +7,15 @@
 //     and unused coordinates zero;
 //   dense / tensor paths: xc[B][n][d], yc[B][m][d] centred coordinates plus
 //     log2 weights lw2x[B][n], lw2y[B][m];
-//   nx[B][n], ny[B][m]: squared norms of the centred points;
+//   nx[B][n], ny[B][m]: squared norms of the centred points (dense and tensor
+//     paths); zero for the point path;
 //   L[B][n], Lam[B][m]: row / column log2-LSE values.  With kappa = 1/(eps ln 2),
 //     f_i = nx_i - L_i / kappa and g_j = ny_j - Lam_j / kappa.
-// f-half (rows X, columns Y): L_i = log2 sum_j 2^(2 kappa x_i.y_j + lw2y_j - Lam_j)
-// g-half (rows Y, columns X): Lam_j = log2 sum_i 2^(2 kappa y_j.x_i + lw2x_i - L_i)
+// Dense / tensor f-half (expanded form):
+//     L_i = log2 sum_j 2^(2 kappa x_i.y_j + lw2y_j - Lam_j)
+// Point f-half (direct form, nx = ny = 0, so L_i = -kappa f_i):
+//     L_i = log2 sum_j 2^(lw2y_j - Lam_j - kappa |x_i - y_j|^2)
+// The g-halves are the mirror images.
 #pragma once
 #include <cuda_runtime.h>
 

@@ -34,10 +34,14 @@ def gauge_fixed(f, g, fr, gr):
 
 
 def potentials_error(f, g, fr, gr):
-    """Normwise relative errors of f and g after the gauge fix (per cloud, max over clouds)."""
+    """Errors of f and g after the gauge fix (per cloud, max over clouds), each
+    relative to the common scale max(|f_ref|_inf, |g_ref|_inf): the two
+    potentials share one gauge and one scale (f_i + g_j ~ C_ij), and one of
+    them can sit near zero (e.g. a single target point has g = 0)."""
     ef, eg = 0.0, 0.0
     for k in range(f.shape[0]):
         fk, gk = gauge_fixed(f[k], g[k], fr[k], gr[k])
-        ef = max(ef, normwise(fk, fr[k]))
-        eg = max(eg, normwise(gk, gr[k]))
+        scale = max(np.max(np.abs(fr[k])), np.max(np.abs(gr[k])), 1e-300)
+        ef = max(ef, float(np.max(np.abs(fk - fr[k])) / scale))
+        eg = max(eg, float(np.max(np.abs(gk - gr[k])) / scale))
     return ef, eg
