@@ -51,16 +51,21 @@ __device__ __forceinline__ float2 pair_chain(float2 acc, float2 u0, float2 u1, f
     return acc;
 }
 // Scalar form of the same chain for one (row, column): u = scaled row point,
-// nv = negated scaled column point, base = m - c.
+// nv = negated scaled column point, base = m - c.  Written with explicitly
+// rounded intrinsics so the compiler can neither contract nor pair these
+// operations: the maximum pass and both COO passes must produce the same bits.
 template <int D>
 __device__ __forceinline__ float scalar_chain(float base, float u0, float u1, float u2, float nv0, float nv1,
                                               float nv2) {
     float acc = base;
-    if (D >= 1) { const float d = u0 + nv0; acc = fmaf(d, d, acc); }
-    if (D >= 2) { const float d = u1 + nv1; acc = fmaf(d, d, acc); }
-    if (D >= 3) { const float d = u2 + nv2; acc = fmaf(d, d, acc); }
+    if (D >= 1) { const float d = __fadd_rn(u0, nv0); acc = __fmaf_rn(d, d, acc); }
+    if (D >= 2) { const float d = __fadd_rn(u1, nv1); acc = __fmaf_rn(d, d, acc); }
+    if (D >= 3) { const float d = __fadd_rn(u2, nv2); acc = __fmaf_rn(d, d, acc); }
     return acc;
 }
+// Scaled point and negated column bias, computed the same way everywhere.
+__device__ __forceinline__ float scaled(float sk, float v) { return __fmul_rn(sk, v); }
+__device__ __forceinline__ float neg_bias(float w2, float state) { return -__fsub_rn(w2, state); }
 
 // Stage columns [base, base + PT_TC) of the chunk ending at c_end: scaled,
 // negated coordinates and the negated column bias.
@@ -70,11 +75,11 @@ __device__ __forceinline__ void load_point_tile(float4* tile, const float4* cp, 
     float4 c0 = make_float4(0.f, 0.f, 0.f, INFINITY), c1 = c0;  // padding: -c = +inf -> score -inf
     if (j0 < c_end) {
         const float4 y = cp[j0];
-        c0 = make_float4(-(sk * y.x), -(sk * y.y), -(sk * y.z), -(y.w - cst[j0]));
+        c0 = make_float4(-scaled(sk, y.x), -scaled(sk, y.y), -scaled(sk, y.z), neg_bias(y.w, cst[j0]));
     }
     if (j1 < c_end) {
         const float4 y = cp[j1];
-        c1 = make_float4(-(sk * y.x), -(sk * y.y), -(sk * y.z), -(y.w - cst[j1]));
+        c1 = make_float4(-scaled(sk, y.x), -scaled(sk, y.y), -scaled(sk, y.z), neg_bias(y.w, cst[j1]));
     }
     tile[2 * threadIdx.x] = make_float4(c0.x, c1.x, c0.y, c1.y);
     tile[2 * threadIdx.x + 1] = make_float4(c0.z, c1.z, c0.w, c1.w);
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
         const int row = row0 + threadIdx.x + r * PT_T;
         const bool valid = row < p.nr;
         float4 x = valid ? rp[row] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float a0 = sk * x.x, a1 = sk * x.y, a2 = sk * x.z;  // scaled row point u
+        const float a0 = scaled(sk, x.x), a1 = scaled(sk, x.y), a2 = scaled(sk, x.z);  // scaled row point u
         q0[r] = make_float2(a0, a0);
         q1[r] = make_float2(a1, a1);
         q2[r] = make_float2(a2, a2);
@@ -157,12 +162,13 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
 #pragma unroll 4
             for (int pp = 0; pp < PT_TC / 2; ++pp) {
                 const float4 A = tile[2 * pp], Bv = tile[2 * pp + 1];
-                const float2 ncj = make_float2(Bv.z, Bv.w);
 #pragma unroll
                 for (int r = 0; r < PT_RPT; ++r) {
-                    const float2 acc = pair_chain<D>(ncj, q0[r], q1[r], q2[r], A, Bv);  // = |u-v|^2 - c
-                    mx[r].x = fmaxf(mx[r].x, -acc.x);
-                    mx[r].y = fmaxf(mx[r].y, -acc.y);
+                    // scalar chain: the COO predicate re-evaluates exactly these bits
+                    const float a0 = scalar_chain<D>(Bv.z, q0[r].x, q1[r].x, q2[r].x, A.x, A.z, Bv.x);
+                    const float a1 = scalar_chain<D>(Bv.w, q0[r].x, q1[r].x, q2[r].x, A.y, A.w, Bv.y);
+                    mx[r].x = fmaxf(mx[r].x, -a0);
+                    mx[r].y = fmaxf(mx[r].y, -a1);
                 }
             }
 #pragma unroll
@@ -481,11 +487,11 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
         const int i = rowb + r;
         const bool ok = i < p.n;
         x[r] = ok ? xp[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        u0[r] = sk * x[r].x;
-        u1[r] = sk * x[r].y;
-        u2[r] = sk * x[r].z;
-        thr_r[r] = ok ? p.Mr[xb + i] + p.log2tau : INFINITY;
-        ne_r[r] = ok ? -(x[r].w - p.L[xb + i]) : 0.f;  // -(log2 a_i - L_i)
+        u0[r] = scaled(sk, x[r].x);
+        u1[r] = scaled(sk, x[r].y);
+        u2[r] = scaled(sk, x[r].z);
+        thr_r[r] = ok ? __fadd_rn(p.Mr[xb + i], p.log2tau) : INFINITY;
+        ne_r[r] = ok ? neg_bias(x[r].w, p.L[xb + i]) : 0.f;  // -(log2 a_i - L_i)
         arow[r] = ok ? p.kappa * p.nx[xb + i] - p.L[xb + i] : 0.f;
         pos[r] = (WRITE && ok) ? p.rowptr[xb + i] : 0;
         cnt[r] = 0;
@@ -498,8 +504,9 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
             float4 c2 = make_float4(0.f, 0.f, 0.f, INFINITY);
             if (j < p.m) {
                 const float4 y = yp[j];
-                c = make_float4(y.x, y.y, y.z, -(y.w - p.Lam[yb + j]));
-                c2 = make_float4(-(sk * y.x), -(sk * y.y), -(sk * y.z), p.Mc[yb + j] + p.log2tau);
+                c = make_float4(y.x, y.y, y.z, neg_bias(y.w, p.Lam[yb + j]));
+                c2 = make_float4(-scaled(sk, y.x), -scaled(sk, y.y), -scaled(sk, y.z),
+                                 __fadd_rn(p.Mc[yb + j], p.log2tau));
             }
             cy[t] = c;
             cv[t] = c2;

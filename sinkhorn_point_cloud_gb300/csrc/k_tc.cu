@@ -49,8 +49,7 @@ constexpr uint32_t OP_BYTES = 2 * TILE_BYTES;   // hi + lo
 constexpr uint32_t OFF_A = 0;                           // [2 row tiles][hi, lo]
 constexpr uint32_t OFF_B = OFF_A + 2 * OP_BYTES;        // [TC_S][hi, lo]
 constexpr uint32_t OFF_BIAS = OFF_B + TC_S * OP_BYTES;  // [TC_S][TC_N] float
-constexpr uint32_t OFF_NY = OFF_BIAS + TC_S * TC_N * 4;    // [TC_S][TC_N] float (plan application)
-constexpr uint32_t OFF_BAR = OFF_NY + TC_S * TC_N * 4;
+constexpr uint32_t OFF_BAR = OFF_BIAS + TC_S * TC_N * 4;
 constexpr uint32_t NBAR = 17;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last
 constexpr uint32_t OFF_RED = OFF_MISC + 16;             // 16 floats
@@ -72,9 +71,8 @@ int tc_max_d() { return TC_D; }
 int tc_rows_per_cta() { return TC_ROWS; }
 int tc_cols_per_tile() { return TC_N; }
 bool tc_apply_supported(int d) { return d == TC_D; }
-// Automatic precision uses the tensor-core plan application only once it has
-// passed its GPU parity tests; SOT_PREC_F16X3 selects it explicitly.
-bool tc_apply_default() { return false; }
+// Automatic precision at d = 64 uses the tensor-core plan application.
+bool tc_apply_default() { return true; }
 int tc_apply_rows_per_cta() { return TC_ROWS; }
 
 static inline int tc_tiles(int n) { return 2 * ((n + TC_ROWS - 1) / TC_ROWS); }
@@ -170,7 +168,6 @@ struct TcSmem {
     unsigned char* sm;    // generic pointer to the same place
     __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8u * (uint32_t)i; }
     __device__ float* bias() const { return reinterpret_cast<float*>(sm + OFF_BIAS); }
-    __device__ float* nyb() const { return reinterpret_cast<float*>(sm + OFF_NY); }
     __device__ int* misc() const { return reinterpret_cast<int*>(sm + OFF_MISC); }  // tmem, abort, nretry, last
     __device__ volatile int* abort() const { return misc() + 1; }
     __device__ float* red() const { return reinterpret_cast<float*>(sm + OFF_RED); }
@@ -213,10 +210,10 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
 }
 
 // Producer warp: the CTA's two row tiles once, then the column tiles of the
-// chunk through the TC_S-stage ring, with the tile's column biases (and, for
-// plan application, the column norms) written to shared memory.
+// chunk through the TC_S-stage ring, with the tile's column biases written to
+// shared memory.
 __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, int c_end,
-                            const float* cw, const float* cst, const float* ny) {
+                            const float* cw, const float* cst) {
     const int lane = threadIdx.x & 31;
     volatile int* abort = S.abort();
     int issued = 0;
@@ -227,7 +224,6 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     }
     const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
     float* bias = S.bias();
-    float* nyb = S.nyb();
     for (int lt = 0; lt < nt; ++lt) {
         const int st = lt % TC_S;
         const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
@@ -236,7 +232,6 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
         for (int c = lane; c < TC_N; c += 32) {
             const int j = jt + c;
             bias[st * TC_N + c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
-            if (ny) nyb[st * TC_N + c] = (j < c_end) ? ny[j] : 0.f;
         }
         if (lane == 0) {
             mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES);
@@ -367,7 +362,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst, nullptr);
+        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst);
     } else if (warp == 1) {
         tc_mma(S, tmem, nt);
     } else {
@@ -541,18 +536,26 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 
 // ---- plan application (cost, gradient, row sums) ------------------------------------
 // Per row i, with the final potentials and P_ij / a_i = 2^(score_ij - L_i):
-//   r_i = sum_j P_ij,  q_i = sum_j P_ij C_ij,  v_i = sum_j P_ij y_j
-// (C_ij = |x_i|^2 + |y_j|^2 - 2 x_i.y_j in centred coordinates).  r_i sums every
-// pair.  q_i and v_i sum the pairs whose term is within 2^-40 of the row's
-// running scale: an omitted term is below 2^-40 of the row mass, so at most
-// m * 2^-40 of it is dropped in all.  Such pairs are a handful per row, and
-// v_i gathers y_j only for them.
-// Pass A of a tile forms the exponentials and the row sum, and marks the
-// 4-column groups that hold a significant pair; pass B revisits only those.
+//   r_i = sum_j P_ij,  q_i = sum_j P_ij C_ij,  v_i = sum_j P_ij y_j.
+// r_i sums every pair.  q_i and v_i sum the pairs whose term is within 2^-40 of
+// the row's running scale: an omitted term is below 2^-40 of the row mass, so
+// at most m * 2^-40 of it is dropped in all.  Such pairs are a handful per row.
+// Their terms are evaluated exactly (fp64, direct form, from the caller's
+// coordinates and potentials): log2(P_ij / a_i) = log2 b_j + kappa (f_i + g_j - C_ij).
+// In fp32 the expanded-form score rounds at the magnitude 2 kappa |x||y|
+// (~1800 log2 units at d = 64, eps = 0.1), which alone moves the gradient by
+// ~1e-4 relative; the exact evaluation of the significant pairs removes that.
+// Pass A of a tile forms the fp32 exponentials and the row sum, and marks the
+// 4-column groups that hold a significant pair; pass B revisits only those,
+// replaces their fp32 terms in r_i and forms q_i and v_i.
 struct TcApplyExtra {
     const float* nx;      // [B][n]
     const float* ny;      // [B][m]
     const float* X;       // [B][n][64] caller coordinates
+    const float* Y;       // [B][m][64] caller coordinates
+    const float* f;       // [B][n] caller potentials
+    const float* g;       // [B][m]
+    double kappa64;
     const float* a;       // [B][n] or NULL (uniform)
     const float* shift;   // [B][64]
     float* vpart;         // [split][B*n][64], zero on entry
@@ -585,8 +588,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     const size_t rbase = (size_t)b * p.nr;
     const float sc = ops.scale[b];
     const float tk = p.two_kappa / (sc * sc);
-    const float c2 = -2.f / (sc * sc);  // acc -> -2 x.y
-    const float* ycen = p.cpack + (size_t)b * p.nc * TC_D;
 
     const uint32_t tmem = tc_setup(S, warp);
 
@@ -598,12 +599,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     float* vrow = erow ? x.vpart + (((size_t)ch * p.B * p.nr) + rbase + row) * TC_D : nullptr;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst, x.ny + (size_t)b * p.nc);
+        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst);
     } else if (warp == 1) {
         tc_mma(S, tmem, nt);
     } else {
-        m = erow ? p.rstate_in[rbase + row] - SOT_STAB_BIAS : INFINITY;
-        const float nxi = erow ? x.nx[rbase + row] : 0.f;
+        const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
+        m = erow ? lrow - SOT_STAB_BIAS : INFINITY;
+        const double fi = erow ? (double)x.f[rbase + row] : 0.0;
+        const float* xorig = x.X + (rbase + (erow ? row : 0)) * TC_D;
+        const float* yorig = x.Y + (size_t)b * p.nc * TC_D;
+        const float* gpot = x.g + (size_t)b * p.nc;
         const float2 tk2 = make_float2(tk, tk);
         for (int lt = 0; lt < nt; ++lt) {
             const int st = lt % TC_S;
@@ -615,7 +620,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
             const float* cb = S.bias() + st * TC_N;
-            const float* nyb = S.nyb() + st * TC_N;
             // pass A: row sum, significance marks per 4-column group
             const float2 nm2 = make_float2(-m, -m);
             float2 acc2 = make_float2(0.f, 0.f);
@@ -681,11 +685,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                         const int cl = 32 * qq + 4 * g + jj;
                         const float e = fmaf(v[4 * g + jj], tk, cb[cl]) - m;
                         if (e > TC_SIG) {
-                            const float w = ex2f(e);
-                            q = fmaf(w, fmaf(v[4 * g + jj], c2, nxi + nyb[cl]), q);
-                            const float* y = ycen + (size_t)((t0 + lt) * TC_N + cl) * TC_D;
+                            // exact term: log2(P/a_i) = log2 b_j + kappa (f_i + g_j - C_ij), C_ij in fp64
+                            const int j = (t0 + lt) * TC_N + cl;
+                            const float* yo = yorig + (size_t)j * TC_D;
+                            double C64 = 0.0;
                             for (int k = 0; k < TC_D; k += 4) {
-                                const float4 yv = *reinterpret_cast<const float4*>(y + k);
+                                const float4 xv = *reinterpret_cast<const float4*>(xorig + k);
+                                const float4 yv = *reinterpret_cast<const float4*>(yo + k);
+                                const double d0 = (double)xv.x - yv.x, d1 = (double)xv.y - yv.y;
+                                const double d2 = (double)xv.z - yv.z, d3 = (double)xv.w - yv.w;
+                                C64 += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+                            }
+                            const double ell = (double)cw[j] + x.kappa64 * (fi + (double)gpot[j] - C64);
+                            const float w = (float)exp2(ell + (double)(lrow - m));
+                            r += w - ex2f(e);
+                            q = fmaf(w, (float)C64, q);
+                            for (int k = 0; k < TC_D; k += 4) {
+                                const float4 yv = *reinterpret_cast<const float4*>(yo + k);
                                 float4 acc = *reinterpret_cast<float4*>(vrow + k);
                                 acc.x = fmaf(w, yv.x, acc.x);
                                 acc.y = fmaf(w, yv.y, acc.y);
@@ -760,10 +776,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
         if (x.rowsum) x.rowsum[rbase + row] = ri;
         if (x.grad) {
             const float* xo = x.X + (rbase + row) * TC_D;
-            const float* sh = x.shift + (size_t)b * TC_D;
             float* gr = x.grad + (rbase + row) * TC_D;
 #pragma unroll
-            for (int k = 0; k < TC_D; ++k) gr[k] = 2.f * (ai * xo[k] - fmaf(ri, sh[k], fac * V[k]));
+            for (int k = 0; k < TC_D; ++k) gr[k] = 2.f * (ai * xo[k] - fac * V[k]);  // v in caller coordinates
         }
     }
     if (x.cost_part) {
@@ -790,6 +805,10 @@ cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfAr
     x.nx = a.nx;
     x.ny = a.ny;
     x.X = a.X;
+    x.Y = a.Yorig;
+    x.f = a.fpot;
+    x.g = a.gpot;
+    x.kappa64 = a.kappa64;
     x.a = a.a;
     x.shift = a.shift;
     x.vpart = scratch;

@@ -69,6 +69,10 @@ struct ApplyArgs {
     float* cost_part;     // [B*rowtiles] or NULL
     float* grad;          // [B][n][d] or NULL
     float* rowsum;        // [B][n] or NULL
+    const float* Yorig;   // original target coordinates (exact pair terms)
+    const float* fpot;    // caller's potentials (exact pair terms)
+    const float* gpot;
+    double kappa64;       // 1 / (eps ln 2) in double
 };
 
 struct CooArgs {

@@ -613,6 +613,7 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     p.xpack = sv.xpack; p.ypack = sv.ypack; p.lw2x = sv.lw2x; p.lw2y = sv.lw2y;
     p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam;
     p.X = X; p.a = a; p.shift = sv.shift; p.kappa = kappa;
+    p.Yorig = Y; p.fpot = f; p.gpot = g; p.kappa64 = 1.0 / ((double)eps * SOT_LN2_D);
     const int rpc = (sv.path == PATH_POINT) ? point_apply_rows_per_cta()
                     : (sv.path == PATH_TC) ? tc_apply_rows_per_cta() : dense_apply_rows_per_cta();
     p.rowtiles = (sv.path == PATH_TC) ? sv.rowtiles[0] : (n + rpc - 1) / rpc;
