@@ -40,6 +40,37 @@ METRIC = "Sinkhorn pair-evaluations/s (n=m=70000, d=64)"
 UNIT = "Gpair-evals/s"
 
 
+KERNEL_SOURCES = {
+    "tc_half_kernel": ["k_tc.cu", "tc_ptx.cuh", "common.cuh", "tc.h", "kernels.h"],
+    "dense_half_kernel": ["k_dense.cu", "common.cuh", "kernels.h"],
+    "point_half_kernel": ["k_point.cu", "common.cuh", "kernels.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sinkhorn_point_cloud_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.json,
+    or None when no capture exists or the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        entries = json.load(fh)
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload and \
+                e.get("source_hash") == kernel_source_hash(kernel):
+            return e.get("bytes_per_launch")
+    return None
+
+
 def metric_name(wid: int) -> str:
     if wid == WORKLOAD_ID:
         return METRIC
@@ -324,7 +355,7 @@ def run_gpu(args, ws, rank, local):
         achieved = flops_pair * per_launch_pairs / secs / 1e12
         peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak, "traffic": measured_traffic("tc_half_kernel", w["name"]),
                 "peak_source": f"{pk_kind} sustained bf16 dense GEMM (fp16 has the same nominal rate)",
                 "kernel": "tc_half_kernel (tcgen05 kind::f16, 3 products per pair)"}
         dtype = "f16x3"
@@ -339,8 +370,9 @@ def run_gpu(args, ws, rank, local):
             ops_pair, unit, kern = 5, "Tops/s", "point_half_kernel (3 FFMA + 2 FADD lane-ops per pair)"
             peak = lanes * sms * mhz * 1e6 / 1e12
         achieved = ops_pair * per_launch_pairs / secs / 1e12
+        kname = "dense_half_kernel" if path == 1 else "point_half_kernel"
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": None, "peak_source": src, "kernel": kern}
+                "traffic": measured_traffic(kname, w["name"]), "peak_source": src, "kernel": kern}
         dtype = "f32"
     roof["mufu"] = mufu
     roof["alu_rates"] = rates

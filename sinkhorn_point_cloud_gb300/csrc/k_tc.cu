@@ -566,7 +566,7 @@ struct TcApplyExtra {
     float* rowsum;        // [B][n] or NULL
 };
 
-constexpr float TC_SIG = -40.f;  // log2 threshold of a significant term
+constexpr float TC_SIG = -40.f;  // a pair is significant when log2(P_ij / a_i) > TC_SIG
 
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcOps ops, TcApplyExtra x) {
     extern __shared__ unsigned char smem_raw[];
@@ -620,8 +620,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
             const float* cb = S.bias() + st * TC_N;
-            // pass A: row sum, significance marks per 4-column group
+            // pass A: row sum, significance marks per 4-column group.  A pair is
+            // significant when t - L_i > TC_SIG, i.e. e = t - m > TC_SIG + (L_i - m).
             const float2 nm2 = make_float2(-m, -m);
+            const float sig_e = TC_SIG + (lrow - m);
             float2 acc2 = make_float2(0.f, 0.f);
             uint32_t sig = 0u;
 #pragma unroll 1
@@ -637,7 +639,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                     acc2 = fadd2(acc2, make_float2(ex2f(e0.x), ex2f(e0.y)));
                     acc2 = fadd2(acc2, make_float2(ex2f(e1.x), ex2f(e1.y)));
                     const float emax = fmaxf(fmaxf(e0.x, e0.y), fmaxf(e1.x, e1.y));
-                    sig |= (emax > TC_SIG) ? (1u << (8 * qq + j / 4)) : 0u;
+                    sig |= (emax > sig_e) ? (1u << (8 * qq + j / 4)) : 0u;
                 }
             }
             float ts = acc2.x + acc2.y;
@@ -684,7 +686,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                     for (int jj = 0; jj < 4; ++jj) {
                         const int cl = 32 * qq + 4 * g + jj;
                         const float e = fmaf(v[4 * g + jj], tk, cb[cl]) - m;
-                        if (e > TC_SIG) {
+                        if (e > TC_SIG + (lrow - m)) {
                             // exact term: log2(P/a_i) = log2 b_j + kappa (f_i + g_j - C_ij), C_ij in fp64
                             const int j = (t0 + lt) * TC_N + cl;
                             const float* yo = yorig + (size_t)j * TC_D;

@@ -3,10 +3,10 @@
 // clock.  Built as a separate small library (libsotpeaks.so) used only by the
 // benchmark; not part of the solver ABI.
 //
-// Each thread runs 8 independent dependency chains for `iters` rounds; every
-// CTA times itself with clock64 (SM cycles).  All CTAs are resident at once
-// (ctas_per_sm x SMs, within occupancy), so per-SM throughput = operations
-// issued on an SM / cycles that SM spent.
+// One CTA of 1024 threads per SM (grid = SM count, so the block scheduler
+// places exactly one per SM); each thread runs 8 independent dependency chains
+// for `iters` rounds and every CTA times itself with clock64 (SM cycles), so
+// per-SM throughput = the CTA's operations / its cycles.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,7 +15,7 @@
 namespace {
 
 template <int KIND>
-__global__ void __launch_bounds__(256) probe_kernel(int iters, float seed, float* sink, long long* cycles) {
+__global__ void __launch_bounds__(1024) probe_kernel(int iters, float seed, float* sink, long long* cycles) {
     float v[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) v[k] = seed + 0.001f * (threadIdx.x + k);
@@ -52,8 +52,8 @@ int sotpeaks_measure(int kind, double* rate_host) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -5;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int threads = 256, per_sm = 4, iters = 4096;
-    const int blocks = sms * per_sm;
+    const int threads = 1024, iters = 2048;
+    const int blocks = sms;
     float* sink = nullptr;
     long long* cyc = nullptr;
     if (cudaMalloc(&sink, threads * sizeof(float)) != cudaSuccess) return -7;
@@ -74,7 +74,7 @@ int sotpeaks_measure(int kind, double* rate_host) {
     cudaFree(cyc);
     if (e != cudaSuccess) return -5;
     const double ops_per_block = (double)threads * iters * 8 * (kind == 2 ? 2 : 1);
-    *rate_host = ops_per_block * per_sm / mean;
+    *rate_host = ops_per_block / mean;
     return 0;
 }
 
