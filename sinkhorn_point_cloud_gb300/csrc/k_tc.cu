@@ -606,7 +606,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
         const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
         m = erow ? lrow - SOT_STAB_BIAS : INFINITY;
         const double fi = erow ? (double)x.f[rbase + row] : 0.0;
-        const float* xorig = x.X + (rbase + (erow ? row : 0)) * TC_D;
         const float* yorig = x.Y + (size_t)b * p.nc * TC_D;
         const float* gpot = x.g + (size_t)b * p.nc;
         const float2 tk2 = make_float2(tk, tk);
@@ -672,46 +671,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                 if (ovf) ts = ts2;
             }
             r += ts;
-            // pass B: cost and barycentre terms of the significant pairs
+            // pass B: cost and barycentre terms of the significant pairs.  The warp
+            // takes them one at a time: every lane owns 2 of the 64 coordinates,
+            // C_ij is reduced across the warp in fp64, and the row's v_i update is
+            // one coalesced 256-byte write.
+            const float sig_b = TC_SIG + (lrow - m);
 #pragma unroll 1
             for (int qq = 0; qq < TC_N / 32; ++qq) {
-                const uint32_t mine = (sig >> (8 * qq)) & 0xFFu;
-                if (!__any_sync(0xffffffffu, mine != 0u)) continue;
+                if (!__any_sync(0xffffffffu, ((sig >> (8 * qq)) & 0xFFu) != 0u)) continue;
                 float v[32];
                 tmem_ld32(tb + 32u * (uint32_t)qq, v);
+#pragma unroll 1
+                for (int c = 0; c < 32; ++c) {
+                    const int cl = 32 * qq + c;
+                    const float e = fmaf(v[c], tk, cb[cl]) - m;
+                    unsigned todo = __ballot_sync(0xffffffffu, erow && e > sig_b);
+                    if (!todo) continue;
+                    const int j = (t0 + lt) * TC_N + cl;
+                    const float2 yv = *reinterpret_cast<const float2*>(yorig + (size_t)j * TC_D + 2 * lane);
+                    const double gj = (double)gpot[j], lbj = (double)cw[j];
+                    while (todo) {
+                        const int l = __ffs(todo) - 1;
+                        todo &= todo - 1u;
+                        const int rl = __shfl_sync(0xffffffffu, row, l);
+                        const float2 xv = *reinterpret_cast<const float2*>(x.X + (rbase + rl) * TC_D + 2 * lane);
+                        const double d0 = (double)xv.x - yv.x, d1 = (double)xv.y - yv.y;
+                        double C64 = d0 * d0 + d1 * d1;
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    if (!(mine & (1u << g))) continue;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int cl = 32 * qq + 4 * g + jj;
-                        const float e = fmaf(v[4 * g + jj], tk, cb[cl]) - m;
-                        if (e > TC_SIG + (lrow - m)) {
-                            // exact term: log2(P/a_i) = log2 b_j + kappa (f_i + g_j - C_ij), C_ij in fp64
-                            const int j = (t0 + lt) * TC_N + cl;
-                            const float* yo = yorig + (size_t)j * TC_D;
-                            double C64 = 0.0;
-                            for (int k = 0; k < TC_D; k += 4) {
-                                const float4 xv = *reinterpret_cast<const float4*>(xorig + k);
-                                const float4 yv = *reinterpret_cast<const float4*>(yo + k);
-                                const double d0 = (double)xv.x - yv.x, d1 = (double)xv.y - yv.y;
-                                const double d2 = (double)xv.z - yv.z, d3 = (double)xv.w - yv.w;
-                                C64 += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
-                            }
-                            const double ell = (double)cw[j] + x.kappa64 * (fi + (double)gpot[j] - C64);
-                            const float w = (float)exp2(ell + (double)(lrow - m));
+                        for (int o = 16; o > 0; o >>= 1) C64 += __shfl_xor_sync(0xffffffffu, C64, o);
+                        const double fl = __shfl_sync(0xffffffffu, fi, l);
+                        const float off = __shfl_sync(0xffffffffu, lrow - m, l);  // L_l - m_l
+                        // exact term: log2(P/a_l) = log2 b_j + kappa (f_l + g_j - C_lj)
+                        const double ell = lbj + x.kappa64 * (fl + gj - C64);
+                        const float w = (float)exp2(ell + (double)off);
+                        if (lane == l) {
                             r += w - ex2f(e);
                             q = fmaf(w, (float)C64, q);
-                            for (int k = 0; k < TC_D; k += 4) {
-                                const float4 yv = *reinterpret_cast<const float4*>(yo + k);
-                                float4 acc = *reinterpret_cast<float4*>(vrow + k);
-                                acc.x = fmaf(w, yv.x, acc.x);
-                                acc.y = fmaf(w, yv.y, acc.y);
-                                acc.z = fmaf(w, yv.z, acc.z);
-                                acc.w = fmaf(w, yv.w, acc.w);
-                                *reinterpret_cast<float4*>(vrow + k) = acc;
-                            }
                         }
+                        float* vr = x.vpart + (((size_t)ch * p.B * p.nr) + rbase + rl) * TC_D + 2 * lane;
+                        float2 acc = *reinterpret_cast<float2*>(vr);
+                        acc.x = fmaf(w, yv.x, acc.x);
+                        acc.y = fmaf(w, yv.y, acc.y);
+                        *reinterpret_cast<float2*>(vr) = acc;
                     }
                 }
             }
