@@ -189,6 +189,32 @@ int sot_profile_enable(int on);
 int sot_profile_read(long long* launches_host, double* total_ms_host);
 
 /*
+ * sot_potentials without any memory allocation.  No counterpart in the source
+ * pages: this entry serves callers that cannot allocate device memory on the
+ * call path -- for example a process whose device memory is entirely reserved
+ * up front by another framework's caching allocator, or real-time and
+ * latency-critical loops where an allocator call (and the synchronisation or
+ * pool growth it can trigger) is not allowed.
+ *
+ * Same computation and result as sot_potentials (fixed schedule, f = g = 0
+ * start) for point clouds with d <= 3.  Its scratch is one statically sized
+ * device array of SOT_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the
+ * library until the process exits; a problem whose scratch would not fit is
+ * rejected with SOT_ERR_INVALID_ARG (sot_last_error() gives the bytes it would
+ * need) before anything runs, and d > 3 gives SOT_ERR_UNSUPPORTED.  The call
+ * makes no cudaMalloc / cudaFree / cudaMallocAsync call.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call reuses the same array and clears what
+ * must start at zero, so calls that overlap on the GPU (other streams, other
+ * host threads on the same device) race on it: serialise them.
+ */
+#define SOT_NOALLOC_SCRATCH_BYTES (16u << 20)
+int sot_potentials_noalloc(const float* X, const float* Y, const float* a, const float* b,
+                           int B, int n, int m, int d, float eps, int iters,
+                           float* f, float* g, void* stream);
+
+/*
  * Which kernel family a solve of dimension d with these flags would use:
  * 0 = fp32 point kernels (d <= 3), 1 = fp32 dense kernels, 2 = tcgen05
  * tensor-core kernels; or a negative SOT_ERR_* when none applies.  Host only.

@@ -91,6 +91,7 @@ def load(path: str | None = None):
         "sot_version": [],
         "sot_kernel_launches": [],
         "sot_select_path": [i, i],
+        "sot_potentials_noalloc": [P, P, P, P, i, i, i, i, f, i, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -168,6 +169,19 @@ def sot_potentials(X, Y, a=None, b=None, eps=0.1, iters=100, f=None, g=None, str
     rc = load().sot_potentials(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, float(eps), int(iters), _ptr(f),
                                _ptr(g), _stream(stream))
     _check(rc, "sot_potentials")
+    return f, g
+
+
+def sot_potentials_noalloc(X, Y, a=None, b=None, eps=0.1, iters=100, f=None, g=None, stream=None):
+    """sot_potentials for d <= 3 using the library's static scratch (no device
+    allocation inside the call; see include/sot.h).  Pass preallocated f, g to
+    keep this call path free of allocations on the Python side too."""
+    X, Y, B, n, m, d = _shapes(X, Y, a, b)
+    f = torch.empty(B, n, device=X.device, dtype=torch.float32) if f is None else f
+    g = torch.empty(B, m, device=X.device, dtype=torch.float32) if g is None else g
+    rc = load().sot_potentials_noalloc(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, float(eps), int(iters),
+                                       _ptr(f), _ptr(g), _stream(stream))
+    _check(rc, "sot_potentials_noalloc")
     return f, g
 
 

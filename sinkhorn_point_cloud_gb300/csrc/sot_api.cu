@@ -53,7 +53,12 @@ int fail(int code, const char* fmt, ...) {
 struct Scratch {
     cudaStream_t st;
     std::vector<void*> ptrs;
+    // Arena mode (sot_potentials_noalloc): carve 256-byte aligned pieces out of a
+    // caller-provided device area instead of allocating; nothing is freed.
+    unsigned char* arena = nullptr;
+    size_t arena_cap = 0, arena_used = 0;
     explicit Scratch(cudaStream_t s) : st(s) {}
+    Scratch(cudaStream_t s, unsigned char* base, size_t cap) : st(s), arena(base), arena_cap(cap) {}
     ~Scratch() {
         for (void* p : ptrs) cudaFreeAsync(p, st);
     }
@@ -61,6 +66,12 @@ struct Scratch {
     T* alloc(size_t count) {
         void* p = nullptr;
         if (count == 0) count = 1;
+        if (arena) {
+            const size_t off = (arena_used + 255) & ~(size_t)255;
+            if (off + count * sizeof(T) > arena_cap) return nullptr;
+            arena_used = off + count * sizeof(T);
+            return reinterpret_cast<T*>(arena + off);
+        }
         if (cudaMallocAsync(&p, count * sizeof(T), st) != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
@@ -215,6 +226,12 @@ struct Solver {
     Solver(const float* X_, const float* Y_, const float* a_, const float* b_, int B_, int n_, int m_, int d_, Path p,
            cudaStream_t s)
         : B(B_), n(n_), m(m_), d(d_), path(p), st(s), X(X_), Y(Y_), a(a_), b(b_), S(s) {
+        sms = device_sms();
+    }
+    // Scratch carved from a fixed device area (no allocation).
+    Solver(const float* X_, const float* Y_, const float* a_, const float* b_, int B_, int n_, int m_, int d_, Path p,
+           cudaStream_t s, unsigned char* arena, size_t arena_cap)
+        : B(B_), n(n_), m(m_), d(d_), path(p), st(s), X(X_), Y(Y_), a(a_), b(b_), S(s, arena, arena_cap) {
         sms = device_sms();
     }
 
@@ -786,3 +803,95 @@ int sot_profile_read(long long* launches_host, double* total_ms_host) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Potentials without any allocation (sot_potentials_noalloc in sot.h).
+//
+// The scratch of the point-cloud solve lives in one statically sized device
+// array that every GPU loading this library holds until the process exits.
+// Host code must not use the array's name as a device address (on the host it
+// is only a stand-in): the address is obtained once per device with
+// cudaGetSymbolAddress and passed to the kernels.
+static __device__ __align__(256) unsigned char g_sot_noalloc_scratch[SOT_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {nullptr};
+
+// Device address of the static scratch on the current device (looked up on the
+// first call for that device, with that device current).
+int noalloc_scratch(unsigned char** out) {
+    int dev = 0;
+    SOT_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(SOT_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_sot_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(SOT_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s", cudaGetErrorString(e));
+        g_noalloc_addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_addr[dev]);
+    return SOT_OK;
+}
+
+// Bytes the point-path solve carves from the arena (mirrors Solver::prepare
+// for the point layout with no stage slots; 256-byte aligned pieces).
+size_t noalloc_required_bytes(int B, int n, int m, int d) {
+    auto piece = [](size_t bytes) { return ((bytes ? bytes : 1) + 255) & ~(size_t)255; };
+    const size_t Bn = (size_t)B * n, Bm = (size_t)B * m;
+    size_t total = piece(sizeof(float) * B * d) + piece(4 * Bn) + piece(4 * Bm) + piece(4 * Bn) + piece(4 * Bm) +
+                   piece(sizeof(int) * 3) + piece(sizeof(unsigned) * 4 * B) + piece(16 * Bn) + piece(16 * Bm);
+    int split[2], chunk[2], rowtiles[2];
+    const int sms = device_sms();
+    for (int h = 0; h < 2; ++h)
+        choose_split(B, h ? m : n, h ? n : m, point_rows_per_cta(), point_cols_per_tile(), sms, 4, &split[h],
+                     &chunk[h], &rowtiles[h]);
+    const int smax = split[0] > split[1] ? split[0] : split[1];
+    const int rt_max = rowtiles[0] > rowtiles[1] ? rowtiles[0] : rowtiles[1];
+    const size_t rows_max = (size_t)B * (n > m ? n : m);
+    if (smax > 1) total += 2 * piece(4 * rows_max * smax);
+    total += piece(4 * (size_t)B * rt_max) * 2 + piece(4 * (size_t)B);
+    return total;
+}
+
+}  // namespace
+
+extern "C" int sot_potentials_noalloc(const float* X, const float* Y, const float* a, const float* b, int B, int n,
+                                      int m, int d, float eps, int iters, float* f, float* g, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (iters < 0) return fail(SOT_ERR_INVALID_ARG, "iters must be >= 0");
+    if (d > 3) return fail(SOT_ERR_UNSUPPORTED, "sot_potentials_noalloc serves point clouds with d <= 3 (got d = %d)", d);
+    if (B == 0) return SOT_OK;
+    if (!f || !g) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
+    const size_t need = noalloc_required_bytes(B, n, m, d);
+    if (need > (size_t)SOT_NOALLOC_SCRATCH_BYTES)
+        return fail(SOT_ERR_INVALID_ARG,
+                    "B=%d n=%d m=%d needs %zu bytes of scratch; the static area holds %zu bytes "
+                    "(use sot_potentials for larger problems)",
+                    B, n, m, need, (size_t)SOT_NOALLOC_SCRATCH_BYTES);
+    unsigned char* base = nullptr;
+    rc = noalloc_scratch(&base);
+    if (rc) return rc;
+    cudaStream_t cs = (cudaStream_t)stream;
+    Solver sv(X, Y, a, b, B, n, m, d, PATH_POINT, cs, base, (size_t)SOT_NOALLOC_SCRATCH_BYTES);
+    rc = sv.prepare(0);  // zeroes the flags, bounds and merge counters left by the previous call
+    if (rc) return rc;
+    const float kappa = 1.f / (eps * SOT_LN2_D);
+    SOT_CUDA(launch_state_cold(sv.nx, kappa, B * n, sv.L, cs));
+    SOT_CUDA(launch_state_cold(sv.ny, kappa, B * m, sv.Lam, cs));
+    for (int t = 0; t < iters; ++t) {
+        rc = sv.iterate(kappa, t == 0, false);
+        if (rc) return rc;
+    }
+    rc = sv.write_potentials(f, g, kappa);
+    if (rc) return rc;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "%s", cudaGetErrorString(e));
+    return SOT_OK;
+}
