@@ -42,6 +42,7 @@ UNIT = "Gpair-evals/s"
 
 KERNEL_SOURCES = {
     "tc_half_kernel": ["k_tc.cu", "tc_ptx.cuh", "common.cuh", "tc.h", "kernels.h"],
+    "tc_screen_kernel": ["k_tc.cu", "tc_ptx.cuh", "common.cuh", "tc.h", "kernels.h"],
     "dense_half_kernel": ["k_dense.cu", "common.cuh", "kernels.h"],
     "point_half_kernel": ["k_point.cu", "common.cuh", "kernels.h"],
 }
@@ -264,6 +265,8 @@ def run_gpu(args, ws, rank, local):
     host_in = [torch.from_numpy(v).pin_memory() for v in ((X, Y, a, b) if weighted else (X, Y))]
     dev_in = [v.to(dev) for v in host_in]
     flags = {"auto": sot.SOT_PREC_AUTO, "fp32": sot.SOT_PREC_FP32, "f16x3": sot.SOT_PREC_F16X3}[args.prec]
+    if args.no_screen:
+        flags |= sot.SOT_TC_NO_SCREEN
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -315,7 +318,9 @@ def run_gpu(args, ws, rank, local):
         t_wall = time.perf_counter() - t_wall0
     barrier(ws)
     sot.sot_profile_enable(False)
-    nl, half_ms = sot.sot_profile_read()
+    kinds = sot.sot_profile_read_kinds()
+    nl = kinds["full"][0] + kinds["screened"][0]
+    half_ms = kinds["full"][1] + kinds["screened"][1]
     launches = sot.sot_kernel_launches() - launches0
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     t_dev = sum(step_ms) / 1e3
@@ -346,25 +351,33 @@ def run_gpu(args, ws, rank, local):
         return 0
     pk, pk_kind = peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    per_launch_ms = half_ms / max(nl, 1)
+    screened = kinds["screened"][0] > 0
+    # the dominant kernel: the screened half-step when it ran, else the full one
+    nl_dom, ms_dom = kinds["screened"] if screened else kinds["full"]
+    per_launch_ms = ms_dom / max(nl_dom, 1)
     per_launch_pairs = B * n * m
     mhz = float(pk.get("sm_max_mhz", 2070.0))
     rates = alu_rates()
     secs = per_launch_ms / 1e3
     mufu = None
-    if rates:
+    if rates and not screened:  # a screened half-step forms exponentials for the kept pairs only
         mufu_peak = rates["ex2_per_sm_clk"] * sms * mhz * 1e6
         mufu = {"achieved_ex2_per_s": per_launch_pairs / secs, "peak_ex2_per_s": mufu_peak,
                 "frac": per_launch_pairs / secs / mufu_peak}
     path = sot.sot_select_path(d, flags)
     if path == 2:
-        flops_pair = 3 * 2 * d  # fp16 products hi*hi + hi*lo + lo*hi, 2 flops per multiply-add
+        if screened:
+            flops_pair = 2 * d  # one fp16 product hi*hi per pair, 2 flops per multiply-add
+            kname, kern = "tc_screen_kernel", "tc_screen_kernel (tcgen05 kind::f16 hi*hi screen + exact kept pairs)"
+        else:
+            flops_pair = 3 * 2 * d  # fp16 products hi*hi + hi*lo + lo*hi, 2 flops per multiply-add
+            kname, kern = "tc_half_kernel", "tc_half_kernel (tcgen05 kind::f16, 3 products per pair)"
         achieved = flops_pair * per_launch_pairs / secs / 1e12
         peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": measured_traffic("tc_half_kernel", w["name"]),
+                "frac": achieved / peak, "traffic": measured_traffic(kname, w["name"]),
                 "peak_source": f"{pk_kind} sustained bf16 dense GEMM (fp16 has the same nominal rate)",
-                "kernel": "tc_half_kernel (tcgen05 kind::f16, 3 products per pair)"}
+                "kernel": kern}
         dtype = "f16x3"
     else:
         lanes = rates["ffma_lanes_per_sm_clk"] if rates else 128.0
@@ -401,7 +414,10 @@ def run_gpu(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
         "iters_per_s": ws * sum([info["iters_done"]]) * args.steps / t_max,
-        "half_step": {"launches": nl, "avg_ms": per_launch_ms, "pairs_per_launch": per_launch_pairs},
+        "half_step": {"launches": nl, "avg_ms": half_ms / max(nl, 1), "pairs_per_launch": per_launch_pairs,
+                      "full": {"launches": kinds["full"][0], "avg_ms": kinds["full"][1] / max(kinds["full"][0], 1)},
+                      "screened": {"launches": kinds["screened"][0],
+                                   "avg_ms": kinds["screened"][1] / max(kinds["screened"][0], 1)}},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": None if e2e_max is None else {"value": ws * e2e_pairs / e2e_max / 1e9, "unit": UNIT,
@@ -431,6 +447,7 @@ def main(argv=None):
                     help="seconds of oracle work for the cpu_baseline sample of the GPU arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--no-screen", action="store_true", help="tensor path: full half-steps only (comparison runs)")
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
     if args.impl == "reference":

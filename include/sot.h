@@ -61,7 +61,9 @@ enum sot_flags {
     SOT_PREC_F16X3 = 2,         /* tcgen05 fp16 products hi*hi + hi*lo + lo*hi (fp32-class accuracy) */
     SOT_PREC_MASK = 3,
     SOT_WARM_START = 1 << 4,    /* read f, g as the initial potentials instead of f = g = 0 */
-    SOT_STAGE_EARLY_EXIT = 1 << 5 /* apply the stop test in every stage, not only at the final eps */
+    SOT_STAGE_EARLY_EXIT = 1 << 5, /* apply the stop test in every stage, not only at the final eps */
+    SOT_TC_NO_SCREEN = 1 << 6      /* tensor path: evaluate every pair's exponential in every half-step
+                                      (default: warm half-steps screen pairs with hi*hi products first) */
 };
 
 /*
@@ -187,6 +189,13 @@ int sot_check_inputs(const float* X, const float* Y, const float* a, const float
  */
 int sot_profile_enable(int on);
 int sot_profile_read(long long* launches_host, double* total_ms_host);
+/*
+ * The same, split by kind: index 0 counts full half-steps (every pair's
+ * exponential formed), index 1 the screened tensor-core half-steps.  Both
+ * arrays (host, 2 entries each) may be NULL.  Resets the counters like
+ * sot_profile_read.
+ */
+int sot_profile_read_kinds(long long* launches_host, double* ms_host);
 
 /*
  * sot_potentials without any memory allocation.  No counterpart in the source

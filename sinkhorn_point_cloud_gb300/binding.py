@@ -31,6 +31,7 @@ SOT_PREC_FP32 = 1
 SOT_PREC_F16X3 = 2
 SOT_WARM_START = 1 << 4
 SOT_STAGE_EARLY_EXIT = 1 << 5
+SOT_TC_NO_SCREEN = 1 << 6
 
 HEADER = os.path.join(_build.ROOT, "include", "sot.h")
 
@@ -86,6 +87,7 @@ def load(path: str | None = None):
         "sot_check_inputs": [P, P, P, P, i, i, i, i, P],
         "sot_profile_enable": [i],
         "sot_profile_read": [C.POINTER(ll), C.POINTER(C.c_double)],
+        "sot_profile_read_kinds": [C.POINTER(ll), C.POINTER(C.c_double)],
         "sot_status_string": [i],
         "sot_last_error": [],
         "sot_version": [],
@@ -297,3 +299,11 @@ def sot_profile_read():
     ms = C.c_double(0)
     _check(load().sot_profile_read(C.byref(n), C.byref(ms)), "sot_profile_read")
     return int(n.value), float(ms.value)
+
+
+def sot_profile_read_kinds():
+    """{"full": (launches, ms), "screened": (launches, ms)} since the last read."""
+    n = (C.c_longlong * 2)()
+    ms = (C.c_double * 2)()
+    _check(load().sot_profile_read_kinds(n, ms), "sot_profile_read_kinds")
+    return {"full": (int(n[0]), float(ms[0])), "screened": (int(n[1]), float(ms[1]))}

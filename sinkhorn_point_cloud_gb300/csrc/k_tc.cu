@@ -51,8 +51,8 @@ constexpr uint32_t OFF_B = OFF_A + 2 * OP_BYTES;        // [TC_S][hi, lo]
 constexpr uint32_t OFF_BIAS = OFF_B + TC_S * OP_BYTES;  // [TC_S][TC_N] float
 constexpr uint32_t OFF_BAR = OFF_BIAS + TC_S * TC_N * 4;
 constexpr uint32_t NBAR = 17;
-constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last
-constexpr uint32_t OFF_RED = OFF_MISC + 16;             // 16 floats
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last, pool count
+constexpr uint32_t OFF_RED = OFF_MISC + 32;             // 16 floats
 constexpr uint32_t OFF_RETRY = OFF_RED + 64;            // TC_ROWS ints
 constexpr uint32_t TC_SMEM = OFF_RETRY + TC_ROWS * 4 + 1024;  // + alignment slack
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;
@@ -79,7 +79,9 @@ static inline int tc_tiles(int n) { return 2 * ((n + TC_ROWS - 1) / TC_ROWS); }
 
 size_t tc_scratch_bytes(int B, int n, int m, int d) {
     (void)d;
-    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 8;
+    const int tmax = tc_tiles(n) > tc_tiles(m) ? tc_tiles(n) : tc_tiles(m);
+    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 24 + 256 +
+           (size_t)B * tmax * TC_N * sizeof(float);
 }
 
 // ---- operand images -----------------------------------------------------------
@@ -106,8 +108,11 @@ __device__ __forceinline__ float tc_scale_of(unsigned bits) {
 }
 
 // One thread per point (row of a 128-row tile): 8 chunks of 8 fp16 for hi and lo.
+// nrm[b][0] / nrm[b][1] receive (as float bits, atomicMax) the largest norm of a
+// point's hi part and of its exact residual v - hi, in scaled units: the
+// screening margin of the hi * hi product is built from them.
 __global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigned* maxbits, float* scale,
-                                unsigned char* img) {
+                                unsigned char* img, unsigned* nrm, int nrm_stride) {
     const int b = blockIdx.y;
     const int tile = blockIdx.x;
     const int r = threadIdx.x;
@@ -117,6 +122,7 @@ __global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigne
     unsigned char* hi = img + ((size_t)b * tiles + tile) * OP_BYTES;
     unsigned char* lo = hi + TILE_BYTES;
     const float* src = pc + ((size_t)b * n + p) * TC_D;
+    float hh = 0.f, rr = 0.f;
 #pragma unroll
     for (int c = 0; c < TC_D / 8; ++c) {
         __align__(16) __half h[8], l[8];
@@ -124,12 +130,22 @@ __global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigne
         for (int k = 0; k < 8; ++k) {
             const float v = (p < n) ? src[8 * c + k] * s : 0.f;
             const __half hv = __float2half_rn(v);
+            const float res = v - __half2float(hv);  // exact in fp32
             h[k] = hv;
-            l[k] = __float2half_rn(v - __half2float(hv));
+            l[k] = __float2half_rn(res);
+            hh = fmaf(__half2float(hv), __half2float(hv), hh);
+            rr = fmaf(res, res, rr);
         }
         const uint32_t off = sw128_offset(r, 8 * c);
         *reinterpret_cast<uint4*>(hi + off) = *reinterpret_cast<const uint4*>(h);
         *reinterpret_cast<uint4*>(lo + off) = *reinterpret_cast<const uint4*>(l);
+    }
+    if (nrm) {
+        const float hn = warp_max(sqrtf(hh)), rn = warp_max(sqrtf(rr));
+        if ((threadIdx.x & 31) == 0) {
+            atomicMax(nrm + (size_t)b * nrm_stride, __float_as_uint(hn));
+            atomicMax(nrm + (size_t)b * nrm_stride + 1, __float_as_uint(rn));
+        }
     }
 }
 
@@ -144,14 +160,18 @@ cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m
     plan.yop = plan.xop + (size_t)B * plan.tiles_x * OP_BYTES;
     unsigned* maxbits = reinterpret_cast<unsigned*>(plan.yop + (size_t)B * plan.tiles_y * OP_BYTES);
     plan.scale = reinterpret_cast<float*>(maxbits + B);
-    cudaError_t e = cudaMemsetAsync(maxbits, 0, sizeof(unsigned) * B, st);
+    plan.nrm = reinterpret_cast<unsigned*>(plan.scale + B);
+    plan.bias = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(plan.nrm + 4 * B) + 255) & ~(uintptr_t)255);
+    cudaError_t e = cudaMemsetAsync(maxbits, 0, sizeof(unsigned) * B * 6, st);  // maxbits, scale, nrm
     if (e != cudaSuccess) return e;
     count_launches(1);
     tc_maxabs_kernel<<<dim3(64, B), 256, 0, st>>>(xc, (long long)n * d, yc, (long long)m * d, maxbits);
     count_launches(1);
-    tc_image_kernel<<<dim3(plan.tiles_x, B), TC_M, 0, st>>>(xc, n, plan.tiles_x, maxbits, plan.scale, plan.xop);
+    tc_image_kernel<<<dim3(plan.tiles_x, B), TC_M, 0, st>>>(xc, n, plan.tiles_x, maxbits, plan.scale, plan.xop,
+                                                            plan.nrm, 4);
     count_launches(1);
-    tc_image_kernel<<<dim3(plan.tiles_y, B), TC_M, 0, st>>>(yc, m, plan.tiles_y, maxbits, plan.scale, plan.yop);
+    tc_image_kernel<<<dim3(plan.tiles_y, B), TC_M, 0, st>>>(yc, m, plan.tiles_y, maxbits, plan.scale, plan.yop,
+                                                            plan.nrm + 2, 4);
     return cudaGetLastError();
 }
 
@@ -160,15 +180,32 @@ struct TcOps {
     const unsigned char* aimg;  // row-side image
     const unsigned char* bimg;  // column-side image
     const float* scale;
+    const float* bias;          // [B][tiles_c * TC_N] column biases c_j, -inf past the last column
     int tiles_r, tiles_c;
 };
+
+// Column biases of one half-step, c_j = log2 w_j - state_j, padded with -inf
+// to whole tiles: the producer moves a tile's biases with one bulk copy.
+__global__ void tc_bias_kernel(const float* cw, const float* cst, int nc, int nc_pad, float* bias) {
+    const int b = blockIdx.y;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < nc_pad; j += gridDim.x * blockDim.x)
+        bias[(size_t)b * nc_pad + j] = (j < nc) ? cw[(size_t)b * nc + j] - cst[(size_t)b * nc + j] : -INFINITY;
+}
+
+static cudaError_t launch_tc_bias(const TcPlan& plan, const HalfArgs& p, int tiles_c, cudaStream_t st) {
+    const int nc_pad = tiles_c * TC_N;
+    const int blocks = (nc_pad + 255) / 256 < 1024 ? (nc_pad + 255) / 256 : 1024;
+    count_launches(1);
+    tc_bias_kernel<<<dim3(blocks, p.B), 256, 0, st>>>(p.cw2, p.cstate, p.nc, nc_pad, plan.bias);
+    return cudaGetLastError();
+}
 
 struct TcSmem {
     uint32_t sbase;       // 1024-aligned shared address of the layout
     unsigned char* sm;    // generic pointer to the same place
     __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8u * (uint32_t)i; }
     __device__ float* bias() const { return reinterpret_cast<float*>(sm + OFF_BIAS); }
-    __device__ int* misc() const { return reinterpret_cast<int*>(sm + OFF_MISC); }  // tmem, abort, nretry, last
+    __device__ int* misc() const { return reinterpret_cast<int*>(sm + OFF_MISC); }  // tmem, abort, nretry, last, pool
     __device__ volatile int* abort() const { return misc() + 1; }
     __device__ float* red() const { return reinterpret_cast<float*>(sm + OFF_RED); }
     __device__ int* retry() const { return reinterpret_cast<int*>(sm + OFF_RETRY); }
@@ -186,7 +223,7 @@ __device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr) {
 __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_S; ++s) {
-            mbar_init(S.bar(BAR_FULL(s)), 32);
+            mbar_init(S.bar(BAR_FULL(s)), 1);
             mbar_init(S.bar(BAR_EMPTY(s)), 1 + 8);
         }
         for (int r = 0; r < 2; ++r)
@@ -197,6 +234,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
         mbar_init(S.bar(BAR_A()), 1);
         S.misc()[1] = 0;
         S.misc()[2] = 0;
+        S.misc()[4] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -209,36 +247,39 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
     return (uint32_t)S.misc()[0];
 }
 
-// Producer warp: the CTA's two row tiles once, then the column tiles of the
-// chunk through the TC_S-stage ring, with the tile's column biases written to
-// shared memory.
-__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, int c_end,
-                            const float* cw, const float* cst) {
+// Producer warp (lane 0 issues): the CTA's two row tiles once, then the
+// column tiles of the chunk through the TC_S-stage ring, each with its 128
+// column biases, all by bulk copies completing on the stage's barrier.
+// With hi_only, only the fp16 hi halves of the operands are copied (the
+// screening kernel multiplies hi * hi alone).
+__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, bool hi_only = false) {
     const int lane = threadIdx.x & 31;
     volatile int* abort = S.abort();
     int issued = 0;
+    const uint32_t bbytes = hi_only ? TILE_BYTES : OP_BYTES;
     if (lane == 0) {
-        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * OP_BYTES);
-        bulk_g2s(S.sbase + OFF_A, ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES, 2 * OP_BYTES,
-                 S.bar(BAR_A()));
+        const unsigned char* a0 = ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES;
+        if (hi_only) {
+            mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * TILE_BYTES);
+            bulk_g2s(S.sbase + OFF_A, a0, TILE_BYTES, S.bar(BAR_A()));
+            bulk_g2s(S.sbase + OFF_A + OP_BYTES, a0 + OP_BYTES, TILE_BYTES, S.bar(BAR_A()));
+        } else {
+            mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * OP_BYTES);
+            bulk_g2s(S.sbase + OFF_A, a0, 2 * OP_BYTES, S.bar(BAR_A()));
+        }
     }
     const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
-    float* bias = S.bias();
+    const float* gbias = ops.bias + (size_t)b * ops.tiles_c * TC_N;
     for (int lt = 0; lt < nt; ++lt) {
         const int st = lt % TC_S;
         const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
         if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
-        const int jt = (t0 + lt) * TC_N;
-        for (int c = lane; c < TC_N; c += 32) {
-            const int j = jt + c;
-            bias[st * TC_N + c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
-        }
         if (lane == 0) {
-            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES);
-            bulk_g2s(S.sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, OP_BYTES,
+            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), bbytes + TC_N * 4);
+            bulk_g2s(S.sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, bbytes,
                      S.bar(BAR_FULL(st)));
-        } else {
-            mbar_arrive(S.bar(BAR_FULL(st)));
+            bulk_g2s(S.sbase + OFF_BIAS + (uint32_t)st * TC_N * 4, gbias + (size_t)(t0 + lt) * TC_N, TC_N * 4,
+                     S.bar(BAR_FULL(st)));
         }
         issued = lt + 1;
     }
@@ -256,6 +297,8 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
 // MMA warp (one thread): per column tile and row tile, 12 MMAs of
 // 128 x 128 x 16 -- lo*hi and hi*lo first, then hi*hi -- into the row tile's
 // TMEM buffer (lt & 1); commits signal the epilogue and free the stage.
+// HI_ONLY issues the 4 hi*hi MMAs alone.
+template <bool HI_ONLY>
 __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
@@ -273,16 +316,18 @@ __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
                 const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
                 const uint32_t ahi = S.sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
                 const uint32_t bhi = S.sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
+                if (!HI_ONLY) {
 #pragma unroll
-                for (int k = 0; k < TC_D / 16; ++k) {
-                    const uint32_t ko = 32u * (uint32_t)k;
-                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
-                    tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    for (int k = 0; k < TC_D / 16; ++k) {
+                        const uint32_t ko = 32u * (uint32_t)k;
+                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
+                        tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    }
                 }
 #pragma unroll
                 for (int k = 0; k < TC_D / 16; ++k) {
                     const uint32_t ko = 32u * (uint32_t)k;
-                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, (HI_ONLY && k == 0) ? 0u : 1u);
                 }
                 tc_commit(S.bar(BAR_ACCFULL(r, u)));
             }
@@ -303,27 +348,78 @@ __device__ __forceinline__ void tc_release(const TcSmem& S, int wg, int lt) {
     }
 }
 
+// Exact two-pass LSE of one row over all columns, by the whole CTA (the
+// fallback for rows whose fast path could not give the value): fp32 dot
+// products of the centred coordinates, x held in registers, y read as float4.
 __device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc,
                              int row, float tk, float* red) {
-    const float* xr = rows + (size_t)row * TC_D;
+    const float4* xr = reinterpret_cast<const float4*>(rows + (size_t)row * TC_D);
+    float4 xv[TC_D / 4];
+#pragma unroll
+    for (int q = 0; q < TC_D / 4; ++q) xv[q] = xr[q];
+    auto score = [&](int j) {
+        const float4* y = reinterpret_cast<const float4*>(cols + (size_t)j * TC_D);
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < TC_D / 4; ++q) {
+            const float4 v = __ldg(y + q);
+            a0 = fmaf(xv[q].x, v.x, a0);
+            a1 = fmaf(xv[q].y, v.y, a1);
+            a0 = fmaf(xv[q].z, v.z, a0);
+            a1 = fmaf(xv[q].w, v.w, a1);
+        }
+        return fmaf(tk, a0 + a1, cw[j] - cst[j]);
+    };
     float mx = -INFINITY;
-    for (int j = threadIdx.x; j < nc; j += TC_THREADS) {
-        const float* y = cols + (size_t)j * TC_D;
-        float acc = 0.f;
-        for (int k = 0; k < TC_D; ++k) acc = fmaf(xr[k], y[k], acc);
-        mx = fmaxf(mx, fmaf(tk, acc, cw[j] - cst[j]));
-    }
+    for (int j = threadIdx.x; j < nc; j += TC_THREADS) mx = fmaxf(mx, score(j));
     mx = block_max<TC_THREADS>(mx, red);
     if (mx == -INFINITY) return -INFINITY;
     float sm = 0.f;
-    for (int j = threadIdx.x; j < nc; j += TC_THREADS) {
-        const float* y = cols + (size_t)j * TC_D;
-        float acc = 0.f;
-        for (int k = 0; k < TC_D; ++k) acc = fmaf(xr[k], y[k], acc);
-        sm += ex2f(fmaf(tk, acc, cw[j] - cst[j]) - mx);
-    }
+    for (int j = threadIdx.x; j < nc; j += TC_THREADS) sm += ex2f(score(j) - mx);
     sm = block_sum<TC_THREADS>(sm, red);
     return mx + log2f(sm);
+}
+
+// Common end of the half-step kernels, run by the CTA that holds the final
+// row values: rows queued in the retry list get the exact two-pass row LSE
+// (whole CTA), then the marginal-error partial and the bound for the next
+// half-step are formed from the new row values.
+__device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, float old, int b, int rb,
+                        size_t rbase, const float* cw, const float* cst) {
+    int* misc = S.misc();
+    float* red = S.red();
+    const int* retry = S.retry();
+    const int lane = threadIdx.x & 31;
+    __syncthreads();
+    const int nretry = misc[2];
+    const float* rows_fp32 = p.rpack + (size_t)b * p.nr * TC_D;
+    const float* cols_fp32 = p.cpack + (size_t)b * p.nc * TC_D;
+    for (int k = 0; k < nretry; ++k) {
+        const int r = retry[k];
+        const float v = tc_row_full(rows_fp32, cols_fp32, cw, cst, p.nc, r, p.two_kappa, red);
+        if (threadIdx.x == 0) {
+            p.rstate_out[rbase + r] = v;
+            atomicOr(p.status, SOT_DEV_RETRY_ROWS);
+        }
+    }
+    if (p.errpart || p.lo_out) {
+        __syncthreads();
+        float e = 0.f, lo = INFINITY;
+        if (erow) {
+            const float nv = p.rstate_out[rbase + row];
+            const float w = p.rweight ? p.rweight[rbase + row] : 1.f / (float)p.nr;
+            e = w * fabsf(ex2f(nv - old) - 1.f);
+            lo = old - nv;
+        }
+        if (p.errpart) {
+            e = block_sum<TC_THREADS>(e, red);
+            if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rb] = e;
+        }
+        if (p.lo_out) {
+            lo = warp_min(lo);
+            if (lane == 0 && lo < INFINITY) atomicMin(p.lo_out + b, ord_encode(lo));
+        }
+    }
 }
 
 // ---- the half-step ------------------------------------------------------------------
@@ -362,9 +458,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst);
+        tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma(S, tmem, nt);
+        tc_mma<false>(S, tmem, nt);
     } else {
         // ---------------- epilogue: exponentials and row sums ----------------
         m = erow ? stabiliser(p.cold, p.lo_in, b, old) : INFINITY;
@@ -486,36 +582,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             retry[atomicAdd(&misc[2], 1)] = row;
         }
     }
-    __syncthreads();
-    const int nretry = misc[2];
-    const float* rows_fp32 = p.rpack + (size_t)b * p.nr * TC_D;
-    const float* cols_fp32 = p.cpack + (size_t)b * p.nc * TC_D;
-    for (int k = 0; k < nretry; ++k) {
-        const int r = retry[k];
-        const float v = tc_row_full(rows_fp32, cols_fp32, cw, cst, p.nc, r, p.two_kappa, red);
-        if (threadIdx.x == 0) {
-            p.rstate_out[rbase + r] = v;
-            atomicOr(p.status, SOT_DEV_RETRY_ROWS);
-        }
-    }
-    if (p.errpart || p.lo_out) {
-        __syncthreads();
-        float e = 0.f, lo = INFINITY;
-        if (erow) {
-            const float nv = p.rstate_out[rbase + row];
-            const float w = p.rweight ? p.rweight[rbase + row] : 1.f / (float)p.nr;
-            e = w * fabsf(ex2f(nv - old) - 1.f);
-            lo = old - nv;
-        }
-        if (p.errpart) {
-            e = block_sum<TC_THREADS>(e, red);
-            if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rb] = e;
-        }
-        if (p.lo_out) {
-            lo = warp_min(lo);
-            if (lane == 0 && lo < INFINITY) atomicMin(p.lo_out + b, ord_encode(lo));
-        }
-    }
+    tc_tail(p, S, erow, row, old, b, rb, rbase, cw, cst);
 }
 
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st) {
@@ -526,11 +593,339 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
     ops.scale = plan.scale;
     ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
+    ops.bias = plan.bias;
+    {
+        const cudaError_t eb = launch_tc_bias(plan, p, ops.tiles_c, st);
+        if (eb != cudaSuccess) return eb;
+    }
     cudaError_t e = cudaFuncSetAttribute(tc_half_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(p.rowtiles * p.split, p.B), block(TC_THREADS);
     count_launches(1);
     tc_half_kernel<<<grid, block, TC_SMEM, st>>>(p, ops);
+    return cudaGetLastError();
+}
+
+// ---- the screened half-step -----------------------------------------------------------
+// At the scales the half-step is used on, a row's log-sum-exp is carried by a
+// handful of columns: every other term lies more than 2^-40 below the row's
+// sum.  The screened half-step finds those columns with the hi * hi products
+// alone (one third of the tensor work of the full half-step) and evaluates
+// only them exactly:
+//   t~_ij = tk acc_ij + c_j  with acc the fp32 accumulation of hi * hi;
+//   |t~_ij - t_ij| <= Mg, from the norms of the hi parts and the residuals
+//   (Cauchy-Schwarz on x.y - hx.hy = rx.hy + hx.ry + rx.ry, plus fp32
+//   accumulation), where t_ij is the exact score.
+// A lower bound of the row's new value is Lb = max(L_old + lo, runmax - Mg):
+// lo is the largest drop of any column bias since the row's last half-step
+// (gathered by the other side), runmax the largest screened score seen so far.
+// A pair is kept when t~_ij >= Lb - theta - Mg; every pair dropped has
+// t_ij < L_new - theta, so the dropped mass is below nc * 2^-theta of the sum,
+// with theta = 26 + log2(nc): 2^-26 relative.
+// Kept pairs go to the CTA's pool (a shared-memory slot counter).  The CTA
+// that finishes the row block evaluates the pools of all its column chunks
+// flattened over its threads (exact scores: compensated fp32 dot products,
+// fp64 combination), takes per-row maxima with shared-memory atomics and the
+// per-row sums in 2^-48 fixed point (integer adds: the result does not depend
+// on the order).  A row with a pair that did not fit in a pool takes the
+// exact full-row LSE.
+constexpr int TC_POOL = 4096;  // kept pairs per CTA
+int tc_screen_pool_cap() { return TC_POOL; }
+constexpr int TC_XS = TC_D + 4;  // row stride of the fp32 row tile in shared memory (bank spread)
+static_assert(TC_ROWS * TC_XS * 4 + TC_ROWS * 16 + 64 * 4 + 64 <= TC_S * OP_BYTES, "finaliser shared memory");
+
+struct TcScreenK {
+    uint2* pool;
+    int pool_cap;
+    int* pool_cnt;
+    int* lost;
+    int* ovf;
+    const unsigned* nrm_r;  // [B][4] with the row side's (hi, residual) pair first
+    const unsigned* nrm_c;  // column side's pair at the same stride
+};
+
+// Screen one 32-column chunk of a row: scores into v, returns the chunk maximum.
+__device__ __forceinline__ float tc_screen_chunk(const uint32_t (&r)[32], const float* cb, float2 tk2, float (&v)[32]) {
+    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const float4 ca = *reinterpret_cast<const float4*>(cb + j);
+        const float4 cc = *reinterpret_cast<const float4*>(cb + j + 4);
+        const float2 e0 = ffma2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), tk2, make_float2(ca.x, ca.y));
+        const float2 e1 = ffma2(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), tk2, make_float2(ca.z, ca.w));
+        const float2 e2 = ffma2(make_float2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])), tk2, make_float2(cc.x, cc.y));
+        const float2 e3 = ffma2(make_float2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])), tk2, make_float2(cc.z, cc.w));
+        v[j] = e0.x; v[j + 1] = e0.y; v[j + 2] = e1.x; v[j + 3] = e1.y;
+        v[j + 4] = e2.x; v[j + 5] = e2.y; v[j + 6] = e3.x; v[j + 7] = e3.y;
+        m0 = fmax3(m0, e0.x, e0.y);
+        m1 = fmax3(m1, e1.x, e1.y);
+        m2 = fmax3(m2, e2.x, e2.y);
+        m3 = fmax3(m3, e3.x, e3.y);
+    }
+    return fmax3(m0, m1, fmaxf(m2, m3));
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, TcOps ops, TcScreenK sk) {
+    if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
+    extern __shared__ unsigned char smem_raw[];
+    const TcSmem S = tc_smem(smem_raw);
+    int* misc = S.misc();
+    volatile int* abort = S.abort();
+    int* retry = S.retry();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int rb = blockIdx.x / p.split, ch = blockIdx.x % p.split;
+    const int row0 = rb * TC_ROWS;
+    const int c_begin = ch * p.chunk;
+    const int c_end = min(p.nc, c_begin + p.chunk);
+    const int t0 = c_begin / TC_N;
+    const int nt = (c_end - c_begin + TC_N - 1) / TC_N;
+    const float* cw = p.cw2 + (size_t)b * p.nc;
+    const float* cst = p.cstate + (size_t)b * p.nc;
+    const size_t rbase = (size_t)b * p.nr;
+    const float sc = ops.scale[b];
+    const float tk = p.two_kappa / (sc * sc);
+    const size_t cta0 = ((size_t)b * p.rowtiles + rb) * p.split;  // first pool of this row block
+
+    if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int k = threadIdx.x; k < p.B; k += TC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
+    const uint32_t tmem = tc_setup(S, warp);
+
+    const int wg = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int row = row0 + wg * TC_M + q4 * 32 + lane;
+    const bool erow = (warp >= 2) && row < p.nr;
+    const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
+
+    if (warp == 0) {
+        tc_producer(S, ops, b, rb, t0, nt, true);
+    } else if (warp == 1) {
+        tc_mma<true>(S, tmem, nt);
+    } else {
+        // screening margin of this cloud (scaled units -> log2 units)
+        const float hr = __uint_as_float(sk.nrm_r[4 * b]), rr = __uint_as_float(sk.nrm_r[4 * b + 1]);
+        const float hc = __uint_as_float(sk.nrm_c[4 * b]), rc = __uint_as_float(sk.nrm_c[4 * b + 1]);
+        const float Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 0.02f;
+        const float theta = 26.f + log2f((float)p.nc);
+        const float off = theta + Mg + 0.05f + 1.5e-5f * fabsf(old);
+        float Lb = -INFINITY;
+        if (!p.cold && p.lo_in) {
+            const float lo = ord_decode(p.lo_in[b]);
+            if (isfinite(lo)) Lb = old + lo;
+        }
+        float runmax = -INFINITY;
+        uint2* pool = sk.pool + (cta0 + ch) * (size_t)sk.pool_cap;
+        int* pcount = misc + 4;
+        const float2 tk2 = make_float2(tk, tk);
+        const float* bias = S.bias();
+        for (int lt = 0; lt < nt; ++lt) {
+            const int st = lt % TC_S;
+            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+            const int u = lt & 1;
+            const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
+            const float* cb = bias + st * TC_N;
+            const int jt = (t0 + lt) * TC_N;
+            uint32_t ra[32], rbuf[32];
+            tmem_ld32_issue(tb, ra);
+            tmem_wait_ld(ra);
+#pragma unroll
+            for (int q = 0; q < TC_N / 32; ++q) {
+                uint32_t (&cur)[32] = (q & 1) ? rbuf : ra;
+                uint32_t (&nxt)[32] = (q & 1) ? ra : rbuf;
+                if (q + 1 < TC_N / 32) tmem_ld32_issue(tb + 32u * (uint32_t)(q + 1), nxt);
+                float v[32];
+                const float cm = tc_screen_chunk(cur, cb + 32 * q, tk2, v);
+                runmax = fmaxf(runmax, cm);
+                const float T = fmaxf(Lb, runmax - Mg) - off;
+                const bool hit = erow && cm >= T;
+                if (__any_sync(0xffffffffu, hit) && hit) {
+                    unsigned mask = 0u;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mask |= (v[j] >= T && v[j] > -INFINITY) ? (1u << j) : 0u;
+                    const int k = __popc(mask);
+                    if (k > 0) {
+                        int slot = atomicAdd(pcount, k);
+                        if (slot + k <= sk.pool_cap) {
+                            while (mask) {
+                                const int j = __ffs(mask) - 1;
+                                mask &= mask - 1u;
+                                pool[slot++] = make_uint2((unsigned)(jt + 32 * q + j), (unsigned)(row - row0));
+                            }
+                        } else {
+                            sk.lost[rbase + row] = 1;
+                        }
+                    }
+                }
+                if (q + 1 < TC_N / 32) tmem_wait_ld(nxt);
+            }
+            tc_release(S, wg, lt);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (*abort) {
+        if (erow) sk.lost[rbase + row] = 2;  // poisoned
+        if (threadIdx.x == 0) atomicOr(p.status, SOT_DEV_TIMEOUT);
+    }
+    if (threadIdx.x == 0) sk.pool_cnt[cta0 + ch] = min(misc[4], sk.pool_cap);
+    if (p.split > 1) {
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned prev = atomicAdd(&p.counters[b * p.rowtiles + rb], 1u);
+            misc[3] = (prev == (unsigned)(p.split - 1));
+        }
+        __syncthreads();
+        if (!misc[3]) return;
+        __threadfence();
+        if (threadIdx.x == 0) p.counters[b * p.rowtiles + rb] = 0u;
+    }
+
+    // ---------------- finish the row block: exact scores of the kept pairs ----------------
+    float* sx = reinterpret_cast<float*>(S.sm + OFF_B);                     // [TC_ROWS][TC_XS] fp32 rows
+    float* s_ref = sx + TC_ROWS * TC_XS;                                     // [TC_ROWS] reference L_old
+    unsigned* s_max = reinterpret_cast<unsigned*>(s_ref + TC_ROWS);          // [TC_ROWS] ord-encoded max
+    unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(s_max + TC_ROWS);  // [TC_ROWS] fixed point
+    int* s_lost = reinterpret_cast<int*>(s_sum + TC_ROWS);                   // [TC_ROWS]
+    int* s_off = s_lost + TC_ROWS;                                           // [split + 1]
+    {
+        const float4* src = reinterpret_cast<const float4*>(p.rpack + rbase * TC_D);
+        for (int e = threadIdx.x; e < TC_ROWS * (TC_D / 4); e += TC_THREADS) {
+            const int r = e / (TC_D / 4), q = e % (TC_D / 4);
+            const int rg = row0 + r;
+            *reinterpret_cast<float4*>(sx + r * TC_XS + 4 * q) =
+                (rg < p.nr) ? src[(size_t)rg * (TC_D / 4) + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int r = threadIdx.x; r < TC_ROWS; r += TC_THREADS) {
+            const int rg = row0 + r;
+            float ref = 0.f;
+            int lost = 0;
+            if (rg < p.nr) {
+                const float o = p.rstate_in ? p.rstate_in[rbase + rg] : 0.f;
+                ref = isfinite(o) ? o : 0.f;
+                lost = __ldcg(sk.lost + rbase + rg);
+                if (lost) sk.lost[rbase + rg] = 0;
+            }
+            s_ref[r] = ref;
+            s_max[r] = 0u;  // below the encoding of every float
+            s_sum[r] = 0ull;
+            s_lost[r] = lost;
+        }
+        if (threadIdx.x == 0) {
+            int acc = 0;
+            for (int c = 0; c < p.split; ++c) {
+                s_off[c] = acc;
+                acc += __ldcg(sk.pool_cnt + cta0 + c);
+            }
+            s_off[p.split] = acc;
+        }
+    }
+    __syncthreads();
+    const int total = s_off[p.split];
+    const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
+    // pass 1: exact score of every kept pair, relative to the row's reference; row maxima
+    for (int k = threadIdx.x; k < total; k += TC_THREADS) {
+        int c = 0;
+        while (c + 1 < p.split && s_off[c + 1] <= k) ++c;
+        uint2* e = sk.pool + (cta0 + c) * (size_t)sk.pool_cap + (k - s_off[c]);
+        const uint2 it = __ldcg(e);
+        const int j = (int)it.x, rl = (int)it.y;
+        if (s_lost[rl]) continue;
+        const float* xr = sx + rl * TC_XS;
+        const float4* yr = ybase + (size_t)j * (TC_D / 4);
+        float hs[4] = {0.f, 0.f, 0.f, 0.f}, es[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < TC_D / 4; ++q) {
+            const float4 y = __ldg(yr + q);
+            const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q);
+            const float xa[4] = {x.x, x.y, x.z, x.w};
+            const float ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                // error-free product and sum (Dekker / Knuth), errors summed alongside
+                const float pr = __fmul_rn(xa[w], ya[w]);
+                const float pe = __fmaf_rn(xa[w], ya[w], -pr);
+                const float sn = __fadd_rn(hs[w], pr);
+                const float z = __fsub_rn(sn, hs[w]);
+                const float se = __fadd_rn(__fsub_rn(hs[w], __fsub_rn(sn, z)), __fsub_rn(pr, z));
+                hs[w] = sn;
+                es[w] = __fadd_rn(es[w], __fadd_rn(pe, se));
+            }
+        }
+        const double dot = ((double)hs[0] + (double)hs[1]) + ((double)hs[2] + (double)hs[3]) +
+                           (((double)es[0] + (double)es[1]) + ((double)es[2] + (double)es[3]));
+        const double t = (double)p.two_kappa * dot + ((double)cw[j] - (double)cst[j]);
+        const float trel = (float)(t - (double)s_ref[rl]);
+        e->x = __float_as_uint(trel);
+        atomicMax(s_max + rl, ord_encode(trel));
+    }
+    __syncthreads();
+    // pass 2: row sums in 2^-48 fixed point (each term <= 1)
+    for (int k = threadIdx.x; k < total; k += TC_THREADS) {
+        int c = 0;
+        while (c + 1 < p.split && s_off[c + 1] <= k) ++c;
+        const uint2 it = __ldcg(sk.pool + (cta0 + c) * (size_t)sk.pool_cap + (k - s_off[c]));
+        const int rl = (int)it.y;
+        if (s_lost[rl]) continue;
+        const float w = ex2f(__uint_as_float(it.x) - ord_decode(s_max[rl]));
+        atomicAdd(s_sum + rl, (unsigned long long)__float2ull_rn(w * 281474976710656.f));
+    }
+    if (threadIdx.x == 0) misc[2] = 0;
+    __syncthreads();
+    if (erow) {
+        const int rl = row - row0;
+        if (s_lost[rl] == 2) {
+            p.rstate_out[rbase + row] = NAN;
+        } else if (s_lost[rl]) {
+            retry[atomicAdd(&misc[2], 1)] = row;
+            atomicAdd(sk.ovf, 1);
+        } else if (s_sum[rl] == 0ull) {
+            p.rstate_out[rbase + row] = -INFINITY;
+        } else {
+            p.rstate_out[rbase + row] =
+                (float)((double)s_ref[rl] + (double)ord_decode(s_max[rl]) + log2((double)s_sum[rl]) - 48.0);
+        }
+    }
+    tc_tail(p, S, erow, row, old, b, rb, rbase, cw, cst);
+}
+
+cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const TcScreen& sc, cudaStream_t st) {
+    if (p.d != TC_D || !p.lo_in || !sc.pool || !sc.pool_cnt || !sc.lost || sc.pool_cap != TC_POOL)
+        return cudaErrorInvalidValue;
+    TcOps ops;
+    ops.aimg = h ? plan.yop : plan.xop;
+    ops.bimg = h ? plan.xop : plan.yop;
+    ops.scale = plan.scale;
+    ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
+    ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
+    ops.bias = plan.bias;
+    {
+        const cudaError_t eb = launch_tc_bias(plan, p, ops.tiles_c, st);
+        if (eb != cudaSuccess) return eb;
+    }
+    TcScreenK sk;
+    sk.pool = sc.pool;
+    sk.pool_cap = sc.pool_cap;
+    sk.pool_cnt = sc.pool_cnt;
+    sk.lost = sc.lost;
+    sk.ovf = sc.ovf;
+    sk.nrm_r = plan.nrm + (h ? 2 : 0);
+    sk.nrm_c = plan.nrm + (h ? 0 : 2);
+    cudaError_t e = cudaFuncSetAttribute(tc_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.rowtiles * p.split, p.B), block(TC_THREADS);
+    count_launches(1);
+    tc_screen_kernel<<<grid, block, TC_SMEM, st>>>(p, ops, sk);
     return cudaGetLastError();
 }
 
@@ -584,7 +979,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     const int t0 = c_begin / TC_N;
     const int nt = (c_end - c_begin + TC_N - 1) / TC_N;
     const float* cw = p.cw2 + (size_t)b * p.nc;
-    const float* cst = p.cstate + (size_t)b * p.nc;
     const size_t rbase = (size_t)b * p.nr;
     const float sc = ops.scale[b];
     const float tk = p.two_kappa / (sc * sc);
@@ -599,9 +993,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     float* vrow = erow ? x.vpart + (((size_t)ch * p.B * p.nr) + rbase + row) * TC_D : nullptr;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt, c_end, cw, cst);
+        tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma(S, tmem, nt);
+        tc_mma<false>(S, tmem, nt);
     } else {
         const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
         m = erow ? lrow - SOT_STAB_BIAS : INFINITY;
@@ -803,6 +1197,11 @@ cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfAr
     ops.scale = plan.scale;
     ops.tiles_r = plan.tiles_x;
     ops.tiles_c = plan.tiles_y;
+    ops.bias = plan.bias;
+    {
+        const cudaError_t eb = launch_tc_bias(plan, hp, ops.tiles_c, st);
+        if (eb != cudaSuccess) return eb;
+    }
     TcApplyExtra x;
     const size_t rows = (size_t)a.B * a.n;
     x.nx = a.nx;

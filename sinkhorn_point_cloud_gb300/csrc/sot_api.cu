@@ -96,10 +96,12 @@ int device_sms() {
 // ---- per-launch timing (sot_profile_*) ------------------------------------
 std::mutex g_prof_mu;
 bool g_prof_on = false;
-std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_prof_pending;
+struct ProfRec {
+    cudaEvent_t a, b;
+    int kind;  // 0: full half-step, 1: screened half-step
+};
+std::vector<ProfRec> g_prof_pending;
 std::vector<cudaEvent_t> g_prof_pool;
-long long g_prof_launches = 0;
-double g_prof_ms = 0.0;
 
 cudaEvent_t prof_event() {
     if (!g_prof_pool.empty()) {
@@ -115,6 +117,7 @@ cudaEvent_t prof_event() {
 struct ProfScope {
     cudaEvent_t a = nullptr, b = nullptr;
     cudaStream_t st;
+    int kind = 0;
     ProfScope(cudaStream_t s, bool want) : st(s) {
         if (!want) return;
         std::lock_guard<std::mutex> g(g_prof_mu);
@@ -127,7 +130,7 @@ struct ProfScope {
         if (!a) return;
         cudaEventRecord(b, st);
         std::lock_guard<std::mutex> g(g_prof_mu);
-        g_prof_pending.emplace_back(a, b);
+        g_prof_pending.push_back(ProfRec{a, b, kind});
     }
 };
 
@@ -222,6 +225,11 @@ struct Solver {
     int sms;
     int split[2], chunk[2], rowtiles[2];  // [0] f-half (rows X), [1] g-half (rows Y)
     TcPlan tc;
+    // Screened tensor-core half-steps: allowed by the caller, and on for the
+    // current stage until too many rows overflow their candidate lists.
+    TcScreen scr;
+    bool screen_allowed = false;
+    bool screen_on = false;
 
     Solver(const float* X_, const float* Y_, const float* a_, const float* b_, int B_, int n_, int m_, int d_, Path p,
            cudaStream_t s)
@@ -292,6 +300,21 @@ struct Solver {
             if (!buf) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
             cudaError_t e = tc_prepare(tc, buf, B, n, m, d, xpack, ypack, st);
             if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "tensor-core operand preparation failed: %s", cudaGetErrorString(e));
+            if (screen_allowed) {
+                const size_t ctas0 = (size_t)rowtiles[0] * split[0], ctas1 = (size_t)rowtiles[1] * split[1];
+                const size_t ctas = (size_t)B * (ctas0 > ctas1 ? ctas0 : ctas1);
+                scr.pool_cap = tc_screen_pool_cap();
+                scr.pool = S.alloc<uint2>(ctas * scr.pool_cap);
+                scr.pool_cnt = S.alloc<int>(ctas);
+                scr.lost = S.alloc<int>(rows_max);
+                scr.ovf = S.alloc<int>(1);
+                if (!scr.pool || !scr.pool_cnt || !scr.lost || !scr.ovf)
+                    return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+                SOT_CUDA(cudaMemsetAsync(scr.lost, 0, sizeof(int) * rows_max, st));
+                SOT_CUDA(cudaMemsetAsync(scr.ovf, 0, sizeof(int), st));
+            }
+        } else {
+            screen_allowed = false;
         }
         return SOT_OK;
     }
@@ -342,9 +365,16 @@ struct Solver {
         cudaError_t e;
         {
             ProfScope ps(st, mode == MODE_LSE);
-            if (path == PATH_POINT) e = launch_point_half(p, mode, st);
-            else if (path == PATH_DENSE) e = launch_dense_half(p, mode, st);
-            else e = launch_tc_half(tc, p, h, mode, st);
+            if (path == PATH_POINT) {
+                e = launch_point_half(p, mode, st);
+            } else if (path == PATH_DENSE) {
+                e = launch_dense_half(p, mode, st);
+            } else if (mode == MODE_LSE && screen_on && !cold && p.lo_in) {
+                ps.kind = 1;
+                e = launch_tc_screen(tc, p, h, scr, st);
+            } else {
+                e = launch_tc_half(tc, p, h, mode, st);
+            }
         }
         if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "half-step launch failed: %s", cudaGetErrorString(e));
         return SOT_OK;
@@ -373,7 +403,26 @@ struct Solver {
     }
 
     // A new eps stage starts: states are rescaled, the last bounds no longer apply.
-    void new_stage() { bound_ok = false; }
+    void new_stage() {
+        bound_ok = false;
+        screen_on = screen_allowed;
+    }
+
+    // After the first screened iteration of a stage: if more than 1 row in 200
+    // (at least 16) had a kept pair that did not fit in its CTA's pool, the plan
+    // is too dense at this eps for screening to pay, and the stage continues
+    // with full half-steps.
+    // Reads one device counter (a stream synchronisation).
+    int screen_check() {
+        if (!screen_on) return SOT_OK;
+        int h = 0;
+        SOT_CUDA(cudaMemcpyAsync(&h, scr.ovf, sizeof(int), cudaMemcpyDeviceToHost, st));
+        SOT_CUDA(cudaStreamSynchronize(st));
+        SOT_CUDA(cudaMemsetAsync(scr.ovf, 0, sizeof(int), st));
+        const long long lim = (long long)B * (n + m) / 200;
+        if (h > (lim > 16 ? lim : 16)) screen_on = false;
+        return SOT_OK;
+    }
 
     // Stop-tested step: the f-half of the next iteration evaluates the
     // row-marginal error of the current iterate; the decision either stops
@@ -446,6 +495,10 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
                 rc = sv.iterate(kappa, cold, false);
                 if (rc) return rc;
                 cold = false;
+                if (t == 1) {
+                    rc = sv.screen_check();
+                    if (rc) return rc;
+                }
             }
             total += todo;
             host_counts[k] = (int)todo;
@@ -477,6 +530,10 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
                 rc = sv.half(1, MODE_LSE, kappa, false, sv.Lam, sv.Lam, nullptr, true);
                 if (rc) return rc;
                 SOT_CUDA(launch_count_iter(sv.stop_flag(), counter, sv.st));
+                if (enq == 1) {
+                    rc = sv.screen_check();
+                    if (rc) return rc;
+                }
             }
             if (final_stage) {
                 rc = read_flag(sv.stop_flag(), sv.st, &stopped);
@@ -569,7 +626,7 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     if (!s) return fail(SOT_ERR_INVALID_ARG, "schedule must not be NULL");
     if (!(s->eps > 0.f) || !std::isfinite(s->eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (s->iters_per_stage < 0) return fail(SOT_ERR_INVALID_ARG, "iters_per_stage must be >= 0");
-    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT))
+    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT | SOT_TC_NO_SCREEN))
         return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
     if (B > 0 && (!f || !g)) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
     if (st && st->stage_iters_host && st->stage_iters_cap < 0) return fail(SOT_ERR_INVALID_ARG, "stage_iters_cap < 0");
@@ -581,6 +638,7 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     rc = choose_path(d, s->flags, &path);
     if (rc) return rc;
     Solver sv(X, Y, a, b, B, n, m, d, path, (cudaStream_t)stream);
+    sv.screen_allowed = (path == PATH_TC) && !(s->flags & SOT_TC_NO_SCREEN);
     rc = run_schedule(sv, *s, f, g, f, g, st);
     if (rc) return rc;
     cudaError_t e = cudaGetLastError();
@@ -775,30 +833,44 @@ int sot_profile_enable(int on) {
     return SOT_OK;
 }
 
-int sot_profile_read(long long* launches_host, double* total_ms_host) {
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pend;
+int sot_profile_read_kinds(long long* launches_host, double* ms_host) {
+    std::vector<ProfRec> pend;
     {
         std::lock_guard<std::mutex> g(g_prof_mu);
         pend.swap(g_prof_pending);
     }
-    double ms = 0.0;
+    long long cnt[2] = {0, 0};
+    double ms[2] = {0.0, 0.0};
+    int rc = SOT_OK;
     for (auto& pr : pend) {
-        if (cudaEventSynchronize(pr.second) != cudaSuccess) return fail(SOT_ERR_CUDA, "event synchronisation failed");
         float t = 0.f;
-        if (cudaEventElapsedTime(&t, pr.first, pr.second) != cudaSuccess) return fail(SOT_ERR_CUDA, "event timing failed");
-        ms += t;
+        if (rc == SOT_OK && cudaEventSynchronize(pr.b) != cudaSuccess) rc = fail(SOT_ERR_CUDA, "event synchronisation failed");
+        if (rc == SOT_OK && cudaEventElapsedTime(&t, pr.a, pr.b) != cudaSuccess) rc = fail(SOT_ERR_CUDA, "event timing failed");
+        cnt[pr.kind] += 1;
+        ms[pr.kind] += t;
     }
-    std::lock_guard<std::mutex> g(g_prof_mu);
-    for (auto& pr : pend) {
-        g_prof_pool.push_back(pr.first);
-        g_prof_pool.push_back(pr.second);
+    {
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        for (auto& pr : pend) {
+            g_prof_pool.push_back(pr.a);
+            g_prof_pool.push_back(pr.b);
+        }
     }
-    g_prof_launches += (long long)pend.size();
-    g_prof_ms += ms;
-    if (launches_host) *launches_host = g_prof_launches;
-    if (total_ms_host) *total_ms_host = g_prof_ms;
-    g_prof_launches = 0;
-    g_prof_ms = 0.0;
+    if (rc) return rc;
+    for (int k = 0; k < 2; ++k) {
+        if (launches_host) launches_host[k] = cnt[k];
+        if (ms_host) ms_host[k] = ms[k];
+    }
+    return SOT_OK;
+}
+
+int sot_profile_read(long long* launches_host, double* total_ms_host) {
+    long long c[2];
+    double t[2];
+    const int rc = sot_profile_read_kinds(c, t);
+    if (rc) return rc;
+    if (launches_host) *launches_host = c[0] + c[1];
+    if (total_ms_host) *total_ms_host = t[0] + t[1];
     return SOT_OK;
 }
 

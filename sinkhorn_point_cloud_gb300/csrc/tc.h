@@ -15,6 +15,19 @@ struct TcPlan {
     unsigned char* xop = nullptr;  // operand image of X: per tile 16 KB fp16 hi + 16 KB fp16 lo, swizzled
     unsigned char* yop = nullptr;  // operand image of Y
     float* scale = nullptr;        // [B] power-of-two coordinate scale used by the images
+    float* bias = nullptr;         // [B][max tiles * 128] column biases of the current half-step
+    unsigned* nrm = nullptr;       // [B][4] float bits: max |x hi|, max |x - x hi|, max |y hi|, max |y - y hi| (scaled)
+};
+
+// Screening state of the hi * hi half-step.  Every CTA appends the pairs it
+// keeps to its own pool; the CTA that finishes a row block evaluates the
+// pools of all its column chunks.
+struct TcScreen {
+    uint2* pool = nullptr;    // [B * rowtiles_max * split_max][pool_cap] (column, local row)
+    int pool_cap = 0;
+    int* pool_cnt = nullptr;  // [B * rowtiles_max * split_max] entries used by each CTA
+    int* lost = nullptr;      // [B * max(n, m)] rows with a pair that did not fit; zero between launches
+    int* ovf = nullptr;       // running count of lost rows
 };
 
 bool tc_supported(int d);
@@ -25,6 +38,11 @@ size_t tc_scratch_bytes(int B, int n, int m, int d);
 cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m, int d, const float* xc,
                        const float* yc, cudaStream_t st);
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st);
+// Screened half-step (warm half-steps only: needs p.lo_in): hi * hi products
+// screen every pair against a bound of the row's new value; the candidates
+// are evaluated exactly in fp32.  Same inputs and outputs as launch_tc_half.
+cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const TcScreen& sc, cudaStream_t st);
+int tc_screen_pool_cap();
 bool tc_apply_supported(int d);
 bool tc_apply_default();
 int tc_apply_rows_per_cta();

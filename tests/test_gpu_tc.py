@@ -113,3 +113,58 @@ def test_tc_plan_apply_matches_oracle(sot, orc, n, m, B):
         assert abs(c[k] - out["cost"]) / abs(out["cost"]) < TOL
         assert normwise(gr[k], out["grad"]) < TOL
         assert normwise(r[k], out["rowsum"]) < TOL
+
+
+def test_tc_screened_agrees_with_full_half_steps(sot):
+    """Warm half-steps screen pairs with hi*hi products and evaluate the kept
+    ones exactly; the result equals the full half-steps' to well below the
+    parity tolerance, and the screened kernel really ran."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=2, n=3000, m=2600, d=64)
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(True)
+    fs, gs = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=0.1, iters_per_stage=50, max_iters=50,
+                                   flags=sot.SOT_PREC_F16X3)
+    kinds = sot.sot_profile_read_kinds()
+    ff, gf = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=0.1, iters_per_stage=50, max_iters=50,
+                                   flags=sot.SOT_PREC_F16X3 | sot.SOT_TC_NO_SCREEN)
+    kinds_full = sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(False)
+    assert kinds["screened"][0] == 98 and kinds["full"][0] == 2, kinds  # the cold first iteration is full
+    assert kinds_full["screened"][0] == 0 and kinds_full["full"][0] == 100, kinds_full
+    ef, eg = potentials_error(host(fs), host(gs), host(ff), host(gf))
+    assert ef < 2e-5 and eg < 2e-5, (ef, eg)
+
+
+def test_tc_screen_gives_way_on_a_dense_plan(sot, orc):
+    """At a large eps every column of a row is within reach of its sum: the
+    candidate lists overflow, those rows take the exact full-row LSE, and the
+    solver continues with full half-steps.  Results still match the oracle."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=600, m=500, d=64)
+    eps, iters = 200.0, 12
+    sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(True)
+    f, g = sot.sot_potentials_ex(dev(X), dev(Y), dev(a), dev(b), eps=eps, iters_per_stage=iters, max_iters=iters,
+                                 flags=sot.SOT_PREC_F16X3)
+    kinds = sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(False)
+    assert kinds["screened"][0] == 2, kinds  # one screened iteration, then full half-steps
+    fr, gref = orc.sinkhorn(X[0], Y[0], a[0], b[0], [eps], [iters])
+    ef, eg = potentials_error(host(f), host(g), fr[None], gref[None])
+    assert ef < TOL and eg < TOL, (ef, eg)
+
+
+def test_tc_screened_annealed_schedule(sot, orc):
+    """Screening across eps stages (each stage's first iteration is full, the
+    bounds restart): eps 1 -> 0.1 by x0.5, 10 iterations per stage."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=1500, m=1300, d=64)
+    f, g, info = sot.sot_potentials_ex(dev(X), dev(Y), dev(a), dev(b), eps=0.1, eps_init=1.0, eps_factor=0.5,
+                                       iters_per_stage=10, max_iters=0, flags=sot.SOT_PREC_F16X3, stats=True)
+    stages = orc.anneal_stages(1.0, 0.5, 0.1)
+    assert info["stages_done"] == len(stages)
+    fr, gref = orc.sinkhorn(X[0], Y[0], a[0], b[0], stages, [10] * len(stages))
+    ef, eg = potentials_error(host(f), host(g), fr[None], gref[None])
+    assert ef < TOL and eg < TOL, (ef, eg)
