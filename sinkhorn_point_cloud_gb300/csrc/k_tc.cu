@@ -80,8 +80,8 @@ static inline int tc_tiles(int n) { return 2 * ((n + TC_ROWS - 1) / TC_ROWS); }
 size_t tc_scratch_bytes(int B, int n, int m, int d) {
     (void)d;
     const int tmax = tc_tiles(n) > tc_tiles(m) ? tc_tiles(n) : tc_tiles(m);
-    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 24 + 256 +
-           (size_t)B * tmax * TC_N * sizeof(float);
+    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 36 + 256 +
+           (size_t)B * tmax * TC_N * sizeof(float) + 256 + (size_t)B * tmax * TILE_BYTES;
 }
 
 // ---- operand images -----------------------------------------------------------
@@ -161,8 +161,14 @@ cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m
     unsigned* maxbits = reinterpret_cast<unsigned*>(plan.yop + (size_t)B * plan.tiles_y * OP_BYTES);
     plan.scale = reinterpret_cast<float*>(maxbits + B);
     plan.nrm = reinterpret_cast<unsigned*>(plan.scale + B);
-    plan.bias = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(plan.nrm + 4 * B) + 255) & ~(uintptr_t)255);
-    cudaError_t e = cudaMemsetAsync(maxbits, 0, sizeof(unsigned) * B * 6, st);  // maxbits, scale, nrm
+    plan.cmax = plan.nrm + 4 * B;
+    plan.bias = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(plan.cmax + 3 * B) + 255) & ~(uintptr_t)255);
+    {
+        const int tmax = plan.tiles_x > plan.tiles_y ? plan.tiles_x : plan.tiles_y;
+        plan.bimg = reinterpret_cast<unsigned char*>(
+            (reinterpret_cast<uintptr_t>(plan.bias + (size_t)B * tmax * TC_N) + 255) & ~(uintptr_t)255);
+    }
+    cudaError_t e = cudaMemsetAsync(maxbits, 0, sizeof(unsigned) * B * 9, st);  // maxbits, scale, nrm, cmax
     if (e != cudaSuccess) return e;
     count_launches(1);
     tc_maxabs_kernel<<<dim3(64, B), 256, 0, st>>>(xc, (long long)n * d, yc, (long long)m * d, maxbits);
@@ -181,6 +187,7 @@ struct TcOps {
     const unsigned char* bimg;  // column-side image
     const float* scale;
     const float* bias;          // [B][tiles_c * TC_N] column biases c_j, -inf past the last column
+    const unsigned char* bias_img;  // [B][tiles_c] 16 KB tiles: fp16 bias parts (screened half-step)
     int tiles_r, tiles_c;
 };
 
@@ -197,6 +204,97 @@ static cudaError_t launch_tc_bias(const TcPlan& plan, const HalfArgs& p, int til
     const int blocks = (nc_pad + 255) / 256 < 1024 ? (nc_pad + 255) / 256 : 1024;
     count_launches(1);
     tc_bias_kernel<<<dim3(blocks, p.B), 256, 0, st>>>(p.cw2, p.cstate, p.nc, nc_pad, plan.bias);
+    return cudaGetLastError();
+}
+
+// ---- column biases of the screened half-step, added by the tensor cores --------
+// The screened half-step lets the MMA add the column bias c_j to the hi * hi
+// products: one more K = 16 step multiplies a row-side constant block
+// (2^E, 2^(E-11), 2^(E-22), 0, ...) by a column-side block (b1, b2, b3, 0, ...)
+// with c_j / tk = 2^E b1 + 2^(E-11) b2 + 2^(E-22) b3 (three fp16 parts, ~33
+// significant bits; tk = 2 kappa / s^2 turns accumulator units into log2
+// units).  Every product is exact; the accumulator then holds score / tk.
+// E is chosen per cloud from max_j |c_j| so that |b1| < 2^15; a cloud that
+// would need E > 15 cannot be screened (its rows take the exact full LSE).
+
+// E of one cloud from max |c_j| (float bits) and the coordinate scale; both
+// the bias image and the row-side constants use this same computation.
+__device__ __forceinline__ int tc_bias_exp(unsigned cmax_bits, float s, float two_kappa) {
+    const float mb = __uint_as_float(cmax_bits) * (s * s / two_kappa);
+    if (!(mb > 0.f)) return -2;
+    if (!isfinite(mb)) return 99;
+    const int e = ilogbf(mb) - 14;
+    return e < -2 ? -2 : e;
+}
+
+// max_j |c_j| per cloud into cmax[2B + b] (float bits).  Warp maxima go to
+// cmax[b] with atomicMax (non-negative floats order as their bits); the last
+// block of the cloud moves the result and clears the running slots.
+__global__ void tc_cmax_kernel(const float* cw, const float* cst, int nc, unsigned* cmax) {
+    const int b = blockIdx.y, B = gridDim.y;
+    float mx = 0.f;
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < nc; j += gridDim.x * blockDim.x)
+        mx = fmaxf(mx, fabsf(cw[(size_t)b * nc + j] - cst[(size_t)b * nc + j]));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) atomicMax(cmax + b, __float_as_uint(mx));
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomicAdd(cmax + B + b, 1u);
+        if (prev == gridDim.x - 1) {
+            __threadfence();
+            cmax[2 * B + b] = atomicExch(cmax + b, 0u);
+            cmax[B + b] = 0u;
+        }
+    }
+}
+
+// Column side of the bias step: per column j of tile t, the parts (b1, b2, b3)
+// as fp16 K-elements 0..2 of row j % 128 of a 128B-swizzled K-major tile
+// (elements 3..15 zero; the MMA reads K = 0..15 only).  Columns past nc get
+// b1 = -inf, so their scores are -inf.
+__global__ void tc_bias_image_kernel(const float* cw, const float* cst, int nc, int nc_pad, const float* scale,
+                                     float two_kappa, const unsigned* cmax, unsigned char* img) {
+    const int b = blockIdx.y, B = gridDim.y;
+    const float s = scale[b];
+    const float inv_tk = s * s / two_kappa;
+    const int E = tc_bias_exp(cmax[2 * B + b], s, two_kappa);
+    const float sc1 = ldexpf(1.f, E > 15 ? 0 : -E);
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < nc_pad; j += gridDim.x * blockDim.x) {
+        __half h0 = __float2half_rn(0.f), h1 = h0, h2 = h0;
+        if (j < nc) {
+            const float v = (cw[(size_t)b * nc + j] - cst[(size_t)b * nc + j]) * inv_tk * sc1;
+            if (E <= 15 && isfinite(v)) {
+                h0 = __float2half_rn(v);
+                const float r1 = (v - __half2float(h0)) * 2048.f;  // exact: the bits of v below h0
+                h1 = __float2half_rn(r1);
+                const float r2 = (r1 - __half2float(h1)) * 2048.f;
+                h2 = __float2half_rn(r2);
+            } else if (E <= 15) {
+                h0 = __float2half_rn(v);  // a NaN bias stays NaN: the pair is never kept
+            }
+        } else {
+            h0 = __float2half_rn(-INFINITY);
+        }
+        unsigned char* tile = img + ((size_t)b * (nc_pad / TC_N) + j / TC_N) * TILE_BYTES;
+        const int jr = j % TC_N;
+        *reinterpret_cast<uint4*>(tile + sw128_offset(jr, 0)) =
+            make_uint4((unsigned)__half_as_ushort(h0) | ((unsigned)__half_as_ushort(h1) << 16),
+                       (unsigned)__half_as_ushort(h2), 0u, 0u);
+        *reinterpret_cast<uint4*>(tile + sw128_offset(jr, 8)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+static cudaError_t launch_tc_bias_image(const TcPlan& plan, const HalfArgs& p, int tiles_c, cudaStream_t st) {
+    const int nc_pad = tiles_c * TC_N;
+    int blocks = (p.nc + 255) / 256 < 1024 ? (p.nc + 255) / 256 : 1024;
+    if (blocks < 1) blocks = 1;
+    count_launches(1);
+    tc_cmax_kernel<<<dim3(blocks, p.B), 256, 0, st>>>(p.cw2, p.cstate, p.nc, plan.cmax);
+    blocks = (nc_pad + 255) / 256 < 1024 ? (nc_pad + 255) / 256 : 1024;
+    count_launches(1);
+    tc_bias_image_kernel<<<dim3(blocks, p.B), 256, 0, st>>>(p.cw2, p.cstate, p.nc, nc_pad, plan.scale, p.two_kappa,
+                                                            plan.cmax, plan.bimg);
     return cudaGetLastError();
 }
 
@@ -220,11 +318,13 @@ __device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr) {
 }
 
 // Barriers, TMEM allocation (warp 1, 512 columns); returns the TMEM base address.
-__device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
+// `empty_count`: arrivals that free a stage (the MMA commit, plus one per
+// epilogue warp when the epilogue reads the stage's biases).
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t empty_count = 1 + 8) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_S; ++s) {
             mbar_init(S.bar(BAR_FULL(s)), 1);
-            mbar_init(S.bar(BAR_EMPTY(s)), 1 + 8);
+            mbar_init(S.bar(BAR_EMPTY(s)), empty_count);
         }
         for (int r = 0; r < 2; ++r)
             for (int u = 0; u < 2; ++u) {
@@ -248,18 +348,18 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp) {
 }
 
 // Producer warp (lane 0 issues): the CTA's two row tiles once, then the
-// column tiles of the chunk through the TC_S-stage ring, each with its 128
-// column biases, all by bulk copies completing on the stage's barrier.
-// With hi_only, only the fp16 hi halves of the operands are copied (the
-// screening kernel multiplies hi * hi alone).
-__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, bool hi_only = false) {
+// column tiles of the chunk through the TC_S-stage ring, all by bulk copies
+// completing on the stage's barrier.  Full half-step: hi and lo operand halves
+// plus the 128 fp32 column biases of each tile.  Screened half-step
+// (`screened`): the hi halves only, and in each stage's lo slot the tile of the
+// fp16 bias image (the column side of the tensor-core bias step).
+__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, bool screened = false) {
     const int lane = threadIdx.x & 31;
     volatile int* abort = S.abort();
     int issued = 0;
-    const uint32_t bbytes = hi_only ? TILE_BYTES : OP_BYTES;
     if (lane == 0) {
         const unsigned char* a0 = ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES;
-        if (hi_only) {
+        if (screened) {
             mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * TILE_BYTES);
             bulk_g2s(S.sbase + OFF_A, a0, TILE_BYTES, S.bar(BAR_A()));
             bulk_g2s(S.sbase + OFF_A + OP_BYTES, a0 + OP_BYTES, TILE_BYTES, S.bar(BAR_A()));
@@ -270,16 +370,24 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     }
     const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
     const float* gbias = ops.bias + (size_t)b * ops.tiles_c * TC_N;
+    const unsigned char* gbimg = ops.bias_img + (size_t)b * ops.tiles_c * TILE_BYTES;
     for (int lt = 0; lt < nt; ++lt) {
         const int st = lt % TC_S;
         const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
         if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
         if (lane == 0) {
-            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), bbytes + TC_N * 4);
-            bulk_g2s(S.sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, bbytes,
-                     S.bar(BAR_FULL(st)));
-            bulk_g2s(S.sbase + OFF_BIAS + (uint32_t)st * TC_N * 4, gbias + (size_t)(t0 + lt) * TC_N, TC_N * 4,
-                     S.bar(BAR_FULL(st)));
+            const uint32_t sdst = S.sbase + OFF_B + (uint32_t)st * OP_BYTES;
+            const unsigned char* bsrc = bimg + (size_t)(t0 + lt) * OP_BYTES;
+            if (screened) {
+                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), 2 * TILE_BYTES);
+                bulk_g2s(sdst, bsrc, TILE_BYTES, S.bar(BAR_FULL(st)));
+                bulk_g2s(sdst + TILE_BYTES, gbimg + (size_t)(t0 + lt) * TILE_BYTES, TILE_BYTES, S.bar(BAR_FULL(st)));
+            } else {
+                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES + TC_N * 4);
+                bulk_g2s(sdst, bsrc, OP_BYTES, S.bar(BAR_FULL(st)));
+                bulk_g2s(S.sbase + OFF_BIAS + (uint32_t)st * TC_N * 4, gbias + (size_t)(t0 + lt) * TC_N, TC_N * 4,
+                         S.bar(BAR_FULL(st)));
+            }
         }
         issued = lt + 1;
     }
@@ -294,11 +402,13 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     __syncwarp();
 }
 
-// MMA warp (one thread): per column tile and row tile, 12 MMAs of
-// 128 x 128 x 16 -- lo*hi and hi*lo first, then hi*hi -- into the row tile's
-// TMEM buffer (lt & 1); commits signal the epilogue and free the stage.
-// HI_ONLY issues the 4 hi*hi MMAs alone.
-template <bool HI_ONLY>
+// MMA warp (one thread): per column tile and row tile, the MMAs of
+// 128 x 128 x 16 into the row tile's TMEM buffer (lt & 1); commits signal the
+// epilogue and free the stage.  Full half-step: 12 MMAs, lo*hi and hi*lo
+// first, then hi*hi.  Screened half-step: the 4 hi*hi MMAs, then the bias
+// step (row-side constants in the A lo slot times the stage's bias-image tile
+// in its lo slot, K = 0..15).
+template <bool SCREENED>
 __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
@@ -316,7 +426,7 @@ __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
                 const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
                 const uint32_t ahi = S.sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
                 const uint32_t bhi = S.sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
-                if (!HI_ONLY) {
+                if (!SCREENED) {
 #pragma unroll
                     for (int k = 0; k < TC_D / 16; ++k) {
                         const uint32_t ko = 32u * (uint32_t)k;
@@ -327,8 +437,9 @@ __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
 #pragma unroll
                 for (int k = 0; k < TC_D / 16; ++k) {
                     const uint32_t ko = 32u * (uint32_t)k;
-                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, (HI_ONLY && k == 0) ? 0u : 1u);
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, (SCREENED && k == 0) ? 0u : 1u);
                 }
+                if (SCREENED) tc_mma_f16(d, sw128_desc(alo), sw128_desc(blo), idesc, 1u);
                 tc_commit(S.bar(BAR_ACCFULL(r, u)));
             }
             if (!ok) break;
@@ -594,6 +705,7 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
     ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
     ops.bias = plan.bias;
+    ops.bias_img = nullptr;
     {
         const cudaError_t eb = launch_tc_bias(plan, p, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;
@@ -642,27 +754,20 @@ struct TcScreenK {
     int* ovf;
     const unsigned* nrm_r;  // [B][4] with the row side's (hi, residual) pair first
     const unsigned* nrm_c;  // column side's pair at the same stride
+    const unsigned* cmax;   // [B] max |c_j| of this half-step's column biases (float bits)
 };
 
-// Screen one 32-column chunk of a row: scores into v, returns the chunk maximum.
-__device__ __forceinline__ float tc_screen_chunk(const uint32_t (&r)[32], const float* cb, float2 tk2, float (&v)[32]) {
-    float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+// Per-chunk maxima of one row over the 4 x 32 columns of a tile, from the
+// accumulators (raw bits; accumulator units, biases included): one
+// three-input max chain per 32-column chunk.
+__device__ __forceinline__ void tc_chunk_max(const uint32_t (&r)[4][32], float (&mq)[4]) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 8) {
-        const float4 ca = *reinterpret_cast<const float4*>(cb + j);
-        const float4 cc = *reinterpret_cast<const float4*>(cb + j + 4);
-        const float2 e0 = ffma2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), tk2, make_float2(ca.x, ca.y));
-        const float2 e1 = ffma2(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), tk2, make_float2(ca.z, ca.w));
-        const float2 e2 = ffma2(make_float2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])), tk2, make_float2(cc.x, cc.y));
-        const float2 e3 = ffma2(make_float2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])), tk2, make_float2(cc.z, cc.w));
-        v[j] = e0.x; v[j + 1] = e0.y; v[j + 2] = e1.x; v[j + 3] = e1.y;
-        v[j + 4] = e2.x; v[j + 5] = e2.y; v[j + 6] = e3.x; v[j + 7] = e3.y;
-        m0 = fmax3(m0, e0.x, e0.y);
-        m1 = fmax3(m1, e1.x, e1.y);
-        m2 = fmax3(m2, e2.x, e2.y);
-        m3 = fmax3(m3, e3.x, e3.y);
+    for (int q = 0; q < 4; ++q) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) m = fmax3(m, __uint_as_float(r[q][j]), __uint_as_float(r[q][j + 1]));
+        mq[q] = m;
     }
-    return fmax3(m0, m1, fmaxf(m2, m3));
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, TcOps ops, TcScreenK sk) {
@@ -690,7 +795,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
 
     if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
         for (int k = threadIdx.x; k < p.B; k += TC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
-    const uint32_t tmem = tc_setup(S, warp);
+    // Row-side constants of the bias step, (2^E, 2^(E-11), 2^(E-22), 0, ...) in
+    // K = 0..15 of every row, into the lo slots of both row tiles.  A cloud
+    // whose biases need E > 15 is not screened: its rows take the exact LSE.
+    const int E = tc_bias_exp(sk.cmax[b], sc, p.two_kappa);
+    const bool screenable = E <= 15;
+    const int nts = screenable ? nt : 0;  // tiles this CTA screens
+    if (screenable) {
+        const unsigned h0 = __half_as_ushort(__float2half_rn(ldexpf(1.f, E)));
+        const unsigned h1 = __half_as_ushort(__float2half_rn(ldexpf(1.f, E - 11)));
+        const unsigned h2 = __half_as_ushort(__float2half_rn(ldexpf(1.f, E - 22)));
+        const uint4 c0 = make_uint4(h0 | (h1 << 16), h2, 0u, 0u), z = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = threadIdx.x; e < 2 * TC_M * 2; e += TC_THREADS) {
+            const int rt = e / (2 * TC_M), r = (e % (2 * TC_M)) >> 1, c = e & 1;
+            *reinterpret_cast<uint4*>(S.sm + OFF_A + rt * OP_BYTES + TILE_BYTES + sw128_offset(r, 8 * c)) =
+                c ? z : c0;
+        }
+        fence_proxy_async_smem();
+    }
+    const uint32_t tmem = tc_setup(S, warp, 1);  // stages are freed by the MMA commit alone
 
     const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
@@ -699,14 +822,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt, true);
+        tc_producer(S, ops, b, rb, t0, nts, true);
     } else if (warp == 1) {
-        tc_mma<true>(S, tmem, nt);
+        tc_mma<true>(S, tmem, nts);
     } else {
-        // screening margin of this cloud (scaled units -> log2 units)
+        if (!screenable && erow) sk.lost[rbase + row] = 1;
+        // screening margin of this cloud (scaled units -> log2 units); the
+        // last term covers the fp32 rounding of the biases held in the
+        // accumulator and of the products added onto them
         const float hr = __uint_as_float(sk.nrm_r[4 * b]), rr = __uint_as_float(sk.nrm_r[4 * b + 1]);
         const float hc = __uint_as_float(sk.nrm_c[4 * b]), rc = __uint_as_float(sk.nrm_c[4 * b + 1]);
-        const float Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 0.02f;
+        const float cmax = __uint_as_float(sk.cmax[b]);
+        const float Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) +
+                         1.5258789e-5f * cmax + 0.02f;
         const float theta = 26.f + log2f((float)p.nc);
         const float off = theta + Mg + 0.05f + 1.5e-5f * fabsf(old);
         float Lb = -INFINITY;
@@ -717,53 +845,65 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         float runmax = -INFINITY;
         uint2* pool = sk.pool + (cta0 + ch) * (size_t)sk.pool_cap;
         int* pcount = misc + 4;
-        const float2 tk2 = make_float2(tk, tk);
-        const float* bias = S.bias();
-        for (int lt = 0; lt < nt; ++lt) {
-            const int st = lt % TC_S;
-            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter
+        for (int lt = 0; lt < nts; ++lt) {
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
             if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
             tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
-            const float* cb = bias + st * TC_N;
+            const uint32_t tb = tq + (uint32_t)((2 * wg + u) * TC_N);
             const int jt = (t0 + lt) * TC_N;
-            uint32_t ra[32], rbuf[32];
-            tmem_ld32_issue(tb, ra);
-            tmem_wait_ld(ra);
+            uint32_t r[4][32];
 #pragma unroll
-            for (int q = 0; q < TC_N / 32; ++q) {
-                uint32_t (&cur)[32] = (q & 1) ? rbuf : ra;
-                uint32_t (&nxt)[32] = (q & 1) ? ra : rbuf;
-                if (q + 1 < TC_N / 32) tmem_ld32_issue(tb + 32u * (uint32_t)(q + 1), nxt);
-                float v[32];
-                const float cm = tc_screen_chunk(cur, cb + 32 * q, tk2, v);
-                runmax = fmaxf(runmax, cm);
-                const float T = fmaxf(Lb, runmax - Mg) - off;
-                const bool hit = erow && cm >= T;
-                if (__any_sync(0xffffffffu, hit) && hit) {
-                    unsigned mask = 0u;
+            for (int q = 0; q < 4; ++q) tmem_ld32_issue(tb + 32u * (uint32_t)q, r[q]);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) mask |= (v[j] >= T && v[j] > -INFINITY) ? (1u << j) : 0u;
-                    const int k = __popc(mask);
-                    if (k > 0) {
-                        int slot = atomicAdd(pcount, k);
-                        if (slot + k <= sk.pool_cap) {
+            for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
+            // the tile is in registers: hand the buffer back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(wg, u)));
+            float mq[4];
+            tc_chunk_max(r, mq);
+            // thresholds in accumulator units (score = tk * acc, tk > 0)
+            runmax = fmaxf(runmax, tk * fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
+            const float Ta = (fmaxf(Lb, runmax - Mg) - off) / tk;
+            bool hq[4];
+            bool hit = false;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                hq[q] = erow && mq[q] >= Ta;
+                hit = hit || hq[q];
+            }
+            if (__any_sync(0xffffffffu, hit)) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (__any_sync(0xffffffffu, hq[q]) && hq[q]) {
+                        unsigned mask = 0u;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float v = __uint_as_float(r[q][j]);
+                            mask |= (v >= Ta && v > -INFINITY) ? (1u << j) : 0u;
+                        }
+                        const int k = __popc(mask);
+                        if (k > 0) {
+                            // Every reserved slot below the capacity is written, also when
+                            // the reservation runs past it: the finaliser reads slots [0,
+                            // min(count, cap)), and a slot left unwritten would hold a stale
+                            // entry.  The entries of a row that did not fit are ignored (the
+                            // row is lost).
+                            int slot = atomicAdd(pcount, k);
+                            if (slot + k > sk.pool_cap) sk.lost[rbase + row] = 1;
                             while (mask) {
                                 const int j = __ffs(mask) - 1;
                                 mask &= mask - 1u;
-                                pool[slot++] = make_uint2((unsigned)(jt + 32 * q + j), (unsigned)(row - row0));
+                                if (slot < sk.pool_cap)
+                                    pool[slot] = make_uint2((unsigned)(jt + 32 * q + j), (unsigned)(row - row0));
+                                ++slot;
                             }
-                        } else {
-                            sk.lost[rbase + row] = 1;
                         }
                     }
                 }
-                if (q + 1 < TC_N / 32) tmem_wait_ld(nxt);
             }
-            tc_release(S, wg, lt);
         }
     }
 
@@ -909,11 +1049,13 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
     ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
     ops.bias = plan.bias;
+    ops.bias_img = plan.bimg;
     {
-        const cudaError_t eb = launch_tc_bias(plan, p, ops.tiles_c, st);
+        const cudaError_t eb = launch_tc_bias_image(plan, p, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;
     }
     TcScreenK sk;
+    sk.cmax = plan.cmax + 2 * p.B;
     sk.pool = sc.pool;
     sk.pool_cap = sc.pool_cap;
     sk.pool_cnt = sc.pool_cnt;
@@ -1198,6 +1340,7 @@ cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfAr
     ops.tiles_r = plan.tiles_x;
     ops.tiles_c = plan.tiles_y;
     ops.bias = plan.bias;
+    ops.bias_img = nullptr;
     {
         const cudaError_t eb = launch_tc_bias(plan, hp, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;

@@ -17,6 +17,9 @@ struct TcPlan {
     float* scale = nullptr;        // [B] power-of-two coordinate scale used by the images
     float* bias = nullptr;         // [B][max tiles * 128] column biases of the current half-step
     unsigned* nrm = nullptr;       // [B][4] float bits: max |x hi|, max |x - x hi|, max |y hi|, max |y - y hi| (scaled)
+    unsigned* cmax = nullptr;      // [3][B]: running max |c_j| (float bits), block counter, final max of the
+                                   // last screened half-step's column biases; the first two zero between launches
+    unsigned char* bimg = nullptr; // [B][max tiles] 16 KB tiles: fp16 parts of the column biases (screened)
 };
 
 // Screening state of the hi * hi half-step.  Every CTA appends the pairs it

@@ -144,6 +144,12 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core, bulk copy) accesses to them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Three-input maximum (one instruction on sm_100-family parts).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
