@@ -66,10 +66,24 @@ __host__ __device__ constexpr int BAR_A() { return 2 * TC_S + 8; }
 static_assert(BAR_A() + 1 == (int)NBAR, "barrier count");
 static_assert(TC_SMEM <= 227 * 1024, "shared memory budget");
 
+// Layout of the screened half-step: 256-column tiles (one 128 x 256 x 16 MMA
+// per K step and row tile), a single 256-column TMEM accumulator per row tile.
+constexpr int SC_N = 256;                                   // columns per screened tile (MMA N)
+constexpr uint32_t SC_AT = TC_M * 32;                       // row-side constant block: 128 rows x 32 B (sw32)
+constexpr uint32_t SC_BT = SC_N * 32;                       // bias block of a tile: 256 rows x 32 B (sw32)
+constexpr uint32_t SC_STAGE = 2 * TILE_BYTES + SC_BT;       // hi of 256 columns (two 16 KB tiles), bias block
+constexpr uint32_t SC_OFF_A = 0;                            // [2 row tiles] hi, 16 KB each
+constexpr uint32_t SC_OFF_AC = SC_OFF_A + 2 * TILE_BYTES;   // [2 row tiles] constant blocks
+constexpr uint32_t SC_OFF_B = SC_OFF_AC + 2 * SC_AT;        // [TC_S] stages
+constexpr uint32_t SC_OFF_HDR = SC_OFF_B + TC_S * SC_STAGE; // header (as OFF_BAR.. of the full half-step)
+constexpr uint32_t SC_SMEM = SC_OFF_HDR + (OFF_RETRY - OFF_BAR) + TC_ROWS * 4 + 1024;
+static_assert(SC_OFF_B % 1024 == 0 && SC_STAGE % 1024 == 0, "screened stage alignment");
+static_assert(SC_SMEM <= 227 * 1024, "screened shared memory budget");
+
 bool tc_supported(int d) { return d == TC_D; }
 int tc_max_d() { return TC_D; }
 int tc_rows_per_cta() { return TC_ROWS; }
-int tc_cols_per_tile() { return TC_N; }
+int tc_cols_per_tile() { return SC_N; }  // column chunks are whole screened tiles
 bool tc_apply_supported(int d) { return d == TC_D; }
 // Automatic precision at d = 64 uses the tensor-core plan application.
 bool tc_apply_default() { return true; }
@@ -81,7 +95,7 @@ size_t tc_scratch_bytes(int B, int n, int m, int d) {
     (void)d;
     const int tmax = tc_tiles(n) > tc_tiles(m) ? tc_tiles(n) : tc_tiles(m);
     return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 36 + 256 +
-           (size_t)B * tmax * TC_N * sizeof(float) + 256 + (size_t)B * tmax * TILE_BYTES;
+           (size_t)B * tmax * TC_N * sizeof(float) + 256 + (size_t)B * (tmax / 2) * SC_BT;
 }
 
 // ---- operand images -----------------------------------------------------------
@@ -249,10 +263,10 @@ __global__ void tc_cmax_kernel(const float* cw, const float* cst, int nc, unsign
     }
 }
 
-// Column side of the bias step: per column j of tile t, the parts (b1, b2, b3)
-// as fp16 K-elements 0..2 of row j % 128 of a 128B-swizzled K-major tile
-// (elements 3..15 zero; the MMA reads K = 0..15 only).  Columns past nc get
-// b1 = -inf, so their scores are -inf.
+// Column side of the bias step: per column j, the parts (b1, b2, b3) as fp16
+// K-elements 0..2 (3..15 zero) of row j % 256 of the 32-byte-swizzled K-major
+// block of its 256-column tile (8 KB).  Columns past nc get b1 = -inf, so
+// their scores are -inf.
 __global__ void tc_bias_image_kernel(const float* cw, const float* cst, int nc, int nc_pad, const float* scale,
                                      float two_kappa, const unsigned* cmax, unsigned char* img) {
     const int b = blockIdx.y, B = gridDim.y;
@@ -276,12 +290,12 @@ __global__ void tc_bias_image_kernel(const float* cw, const float* cst, int nc, 
         } else {
             h0 = __float2half_rn(-INFINITY);
         }
-        unsigned char* tile = img + ((size_t)b * (nc_pad / TC_N) + j / TC_N) * TILE_BYTES;
-        const int jr = j % TC_N;
-        *reinterpret_cast<uint4*>(tile + sw128_offset(jr, 0)) =
+        unsigned char* tile = img + ((size_t)b * (nc_pad / SC_N) + j / SC_N) * SC_BT;
+        const int jr = j % SC_N;
+        *reinterpret_cast<uint4*>(tile + sw32_offset(jr, 0)) =
             make_uint4((unsigned)__half_as_ushort(h0) | ((unsigned)__half_as_ushort(h1) << 16),
                        (unsigned)__half_as_ushort(h2), 0u, 0u);
-        *reinterpret_cast<uint4*>(tile + sw128_offset(jr, 8)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(tile + sw32_offset(jr, 8)) = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -298,22 +312,27 @@ static cudaError_t launch_tc_bias_image(const TcPlan& plan, const HalfArgs& p, i
     return cudaGetLastError();
 }
 
+// The header (barriers, misc words, reduction scratch, retry list) sits at
+// `hdr`: after the operand buffers, whose layout differs between kernels.
 struct TcSmem {
     uint32_t sbase;       // 1024-aligned shared address of the layout
     unsigned char* sm;    // generic pointer to the same place
-    __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8u * (uint32_t)i; }
+    uint32_t hdr;         // offset of the header
+    __device__ uint32_t bar(int i) const { return sbase + hdr + 8u * (uint32_t)i; }
     __device__ float* bias() const { return reinterpret_cast<float*>(sm + OFF_BIAS); }
-    __device__ int* misc() const { return reinterpret_cast<int*>(sm + OFF_MISC); }  // tmem, abort, nretry, last, pool
+    __device__ uint32_t misc_addr() const { return sbase + hdr + (OFF_MISC - OFF_BAR); }
+    __device__ int* misc() const { return reinterpret_cast<int*>(sm + hdr + (OFF_MISC - OFF_BAR)); }  // tmem, abort, nretry, last, pool
     __device__ volatile int* abort() const { return misc() + 1; }
-    __device__ float* red() const { return reinterpret_cast<float*>(sm + OFF_RED); }
-    __device__ int* retry() const { return reinterpret_cast<int*>(sm + OFF_RETRY); }
+    __device__ float* red() const { return reinterpret_cast<float*>(sm + hdr + (OFF_RED - OFF_BAR)); }
+    __device__ int* retry() const { return reinterpret_cast<int*>(sm + hdr + (OFF_RETRY - OFF_BAR)); }
 };
 
-__device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr) {
+__device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr, uint32_t hdr = OFF_BAR) {
     TcSmem S;
     const uint32_t raw = smem_u32(raw_ptr);
     S.sbase = (raw + 1023u) & ~1023u;
     S.sm = raw_ptr + (S.sbase - raw);
+    S.hdr = hdr;
     return S;
 }
 
@@ -338,7 +357,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(S.sbase + OFF_MISC, 512);
+        tmem_alloc(S.misc_addr(), 512);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -347,52 +366,10 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
     return (uint32_t)S.misc()[0];
 }
 
-// Producer warp (lane 0 issues): the CTA's two row tiles once, then the
-// column tiles of the chunk through the TC_S-stage ring, all by bulk copies
-// completing on the stage's barrier.  Full half-step: hi and lo operand halves
-// plus the 128 fp32 column biases of each tile.  Screened half-step
-// (`screened`): the hi halves only, and in each stage's lo slot the tile of the
-// fp16 bias image (the column side of the tensor-core bias step).
-__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, bool screened = false) {
-    const int lane = threadIdx.x & 31;
-    volatile int* abort = S.abort();
-    int issued = 0;
-    if (lane == 0) {
-        const unsigned char* a0 = ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES;
-        if (screened) {
-            mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * TILE_BYTES);
-            bulk_g2s(S.sbase + OFF_A, a0, TILE_BYTES, S.bar(BAR_A()));
-            bulk_g2s(S.sbase + OFF_A + OP_BYTES, a0 + OP_BYTES, TILE_BYTES, S.bar(BAR_A()));
-        } else {
-            mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * OP_BYTES);
-            bulk_g2s(S.sbase + OFF_A, a0, 2 * OP_BYTES, S.bar(BAR_A()));
-        }
-    }
-    const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
-    const float* gbias = ops.bias + (size_t)b * ops.tiles_c * TC_N;
-    const unsigned char* gbimg = ops.bias_img + (size_t)b * ops.tiles_c * TILE_BYTES;
-    for (int lt = 0; lt < nt; ++lt) {
-        const int st = lt % TC_S;
-        const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
-        if (lane == 0) {
-            const uint32_t sdst = S.sbase + OFF_B + (uint32_t)st * OP_BYTES;
-            const unsigned char* bsrc = bimg + (size_t)(t0 + lt) * OP_BYTES;
-            if (screened) {
-                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), 2 * TILE_BYTES);
-                bulk_g2s(sdst, bsrc, TILE_BYTES, S.bar(BAR_FULL(st)));
-                bulk_g2s(sdst + TILE_BYTES, gbimg + (size_t)(t0 + lt) * TILE_BYTES, TILE_BYTES, S.bar(BAR_FULL(st)));
-            } else {
-                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES + TC_N * 4);
-                bulk_g2s(sdst, bsrc, OP_BYTES, S.bar(BAR_FULL(st)));
-                bulk_g2s(S.sbase + OFF_BIAS + (uint32_t)st * TC_N * 4, gbias + (size_t)(t0 + lt) * TC_N, TC_N * 4,
-                         S.bar(BAR_FULL(st)));
-            }
-        }
-        issued = lt + 1;
-    }
-    // drain: never leave a bulk copy in flight into this CTA's shared memory
-    if (lane == 0) {
+// Never leave a bulk copy in flight into this CTA's shared memory: waits
+// (bounded) for the last TC_S stages issued and for the row tiles.
+__device__ __forceinline__ void tc_producer_drain(const TcSmem& S, int issued) {
+    if ((threadIdx.x & 31) == 0) {
         int dummy = 0;
         for (int lt = (issued > TC_S ? issued - TC_S : 0); lt < issued; ++lt)
             mbar_wait_bounded(S.bar(BAR_FULL(lt % TC_S)), (uint32_t)(lt / TC_S) & 1u, (volatile int*)&dummy,
@@ -402,13 +379,39 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     __syncwarp();
 }
 
-// MMA warp (one thread): per column tile and row tile, the MMAs of
-// 128 x 128 x 16 into the row tile's TMEM buffer (lt & 1); commits signal the
-// epilogue and free the stage.  Full half-step: 12 MMAs, lo*hi and hi*lo
-// first, then hi*hi.  Screened half-step: the 4 hi*hi MMAs, then the bias
-// step (row-side constants in the A lo slot times the stage's bias-image tile
-// in its lo slot, K = 0..15).
-template <bool SCREENED>
+// Producer warp (lane 0 issues): the CTA's two row tiles once, then the
+// column tiles of the chunk through the TC_S-stage ring, each with its 128
+// fp32 column biases, all by bulk copies completing on the stage's barrier.
+__device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt) {
+    const int lane = threadIdx.x & 31;
+    volatile int* abort = S.abort();
+    int issued = 0;
+    if (lane == 0) {
+        const unsigned char* a0 = ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES;
+        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * OP_BYTES);
+        bulk_g2s(S.sbase + OFF_A, a0, 2 * OP_BYTES, S.bar(BAR_A()));
+    }
+    const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
+    const float* gbias = ops.bias + (size_t)b * ops.tiles_c * TC_N;
+    for (int lt = 0; lt < nt; ++lt) {
+        const int st = lt % TC_S;
+        const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES + TC_N * 4);
+            bulk_g2s(S.sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, OP_BYTES,
+                     S.bar(BAR_FULL(st)));
+            bulk_g2s(S.sbase + OFF_BIAS + (uint32_t)st * TC_N * 4, gbias + (size_t)(t0 + lt) * TC_N, TC_N * 4,
+                     S.bar(BAR_FULL(st)));
+        }
+        issued = lt + 1;
+    }
+    tc_producer_drain(S, issued);
+}
+
+// MMA warp (one thread): per column tile and row tile, 12 MMAs of
+// 128 x 128 x 16 -- lo*hi and hi*lo first, then hi*hi -- into the row tile's
+// TMEM buffer (lt & 1); commits signal the epilogue and free the stage.
 __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
@@ -426,20 +429,17 @@ __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
                 const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
                 const uint32_t ahi = S.sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
                 const uint32_t bhi = S.sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
-                if (!SCREENED) {
 #pragma unroll
-                    for (int k = 0; k < TC_D / 16; ++k) {
-                        const uint32_t ko = 32u * (uint32_t)k;
-                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
-                        tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
-                    }
+                for (int k = 0; k < TC_D / 16; ++k) {
+                    const uint32_t ko = 32u * (uint32_t)k;
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, k > 0 ? 1u : 0u);
+                    tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
                 }
 #pragma unroll
                 for (int k = 0; k < TC_D / 16; ++k) {
                     const uint32_t ko = 32u * (uint32_t)k;
-                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, (SCREENED && k == 0) ? 0u : 1u);
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, 1u);
                 }
-                if (SCREENED) tc_mma_f16(d, sw128_desc(alo), sw128_desc(blo), idesc, 1u);
                 tc_commit(S.bar(BAR_ACCFULL(r, u)));
             }
             if (!ok) break;
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     if (warp == 0) {
         tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma<false>(S, tmem, nt);
+        tc_mma(S, tmem, nt);
     } else {
         // ---------------- epilogue: exponentials and row sums ----------------
         m = erow ? stabiliser(p.cold, p.lo_in, b, old) : INFINITY;
@@ -744,7 +744,78 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 constexpr int TC_POOL = 4096;  // kept pairs per CTA
 int tc_screen_pool_cap() { return TC_POOL; }
 constexpr int TC_XS = TC_D + 4;  // row stride of the fp32 row tile in shared memory (bank spread)
-static_assert(TC_ROWS * TC_XS * 4 + TC_ROWS * 16 + 64 * 4 + 64 <= TC_S * OP_BYTES, "finaliser shared memory");
+static_assert(TC_ROWS * TC_XS * 4 + TC_ROWS * 16 + 64 * 4 + 64 <= TC_S * SC_STAGE, "finaliser shared memory");
+
+// Producer of the screened half-step: the hi halves of the CTA's two row
+// tiles once, then per 256-column tile the hi halves of its two 128-point
+// image tiles (back to back: one 256-row K-major operand) and its bias block.
+// t0: first 128-point image tile of the chunk (even); nt: 256-column tiles.
+__device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt) {
+    const int lane = threadIdx.x & 31;
+    volatile int* abort = S.abort();
+    int issued = 0;
+    if (lane == 0) {
+        const unsigned char* a0 = ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES;
+        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * TILE_BYTES);
+        bulk_g2s(S.sbase + SC_OFF_A, a0, TILE_BYTES, S.bar(BAR_A()));
+        bulk_g2s(S.sbase + SC_OFF_A + TILE_BYTES, a0 + OP_BYTES, TILE_BYTES, S.bar(BAR_A()));
+    }
+    const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
+    const unsigned char* gbias = ops.bias_img + (size_t)b * (ops.tiles_c / 2) * SC_BT;
+    for (int lt = 0; lt < nt; ++lt) {
+        const int st = lt % TC_S;
+        const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
+        if (lane == 0) {
+            const uint32_t dst = S.sbase + SC_OFF_B + (uint32_t)st * SC_STAGE;
+            const unsigned char* src = bimg + (size_t)(t0 + 2 * lt) * OP_BYTES;
+            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), SC_STAGE);
+            bulk_g2s(dst, src, TILE_BYTES, S.bar(BAR_FULL(st)));
+            bulk_g2s(dst + TILE_BYTES, src + OP_BYTES, TILE_BYTES, S.bar(BAR_FULL(st)));
+            bulk_g2s(dst + 2 * TILE_BYTES, gbias + (size_t)(t0 / 2 + lt) * SC_BT, SC_BT, S.bar(BAR_FULL(st)));
+        }
+        issued = lt + 1;
+    }
+    tc_producer_drain(S, issued);
+}
+
+// MMA warp of the screened half-step (one thread): per 256-column tile and
+// row tile r, four 128 x 256 x 16 hi*hi MMAs and the bias step (row-side
+// constants times the tile's bias block) into the row tile's accumulator
+// (TMEM columns 256 r ..); the epilogue frees it after loading it.
+__device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt) {
+    if ((threadIdx.x & 31) == 0) {
+        volatile int* abort = S.abort();
+        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, TC_WAIT_NS);
+        const uint32_t idesc = f16_idesc(TC_M, SC_N);
+        for (int lt = 0; ok && lt < nt; ++lt) {
+            const int st = lt % TC_S;
+            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            const uint32_t bst = S.sbase + SC_OFF_B + (uint32_t)st * SC_STAGE;
+            for (int r = 0; r < 2 && ok; ++r) {
+                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, 0)), ((uint32_t)lt & 1u) ^ 1u, abort, TC_WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(r * SC_N);
+                const uint32_t ahi = S.sbase + SC_OFF_A + (uint32_t)r * TILE_BYTES;
+#pragma unroll
+                for (int k = 0; k < TC_D / 16; ++k) {
+                    const uint32_t ko = 32u * (uint32_t)k;
+                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bst + ko), idesc, k > 0 ? 1u : 0u);
+                }
+                tc_mma_f16(d, sw32_desc(S.sbase + SC_OFF_AC + (uint32_t)r * SC_AT), sw32_desc(bst + 2 * TILE_BYTES),
+                           idesc, 1u);
+                tc_commit(S.bar(BAR_ACCFULL(r, 0)));
+            }
+            if (!ok) break;
+            tc_commit(S.bar(BAR_EMPTY(st)));
+        }
+    }
+    __syncwarp();
+}
 
 struct TcScreenK {
     uint2* pool;
@@ -761,19 +832,81 @@ struct TcScreenK {
 // accumulators (raw bits; accumulator units, biases included): one
 // three-input max chain per 32-column chunk.
 __device__ __forceinline__ void tc_chunk_max(const uint32_t (&r)[4][32], float (&mq)[4]) {
+    // two interleaved chains per chunk (8 in flight) keep the max latency hidden
+    float m[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) m[c] = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            m[2 * q] = fmax3(m[2 * q], __uint_as_float(r[q][j]), __uint_as_float(r[q][j + 1]));
+            m[2 * q + 1] = fmax3(m[2 * q + 1], __uint_as_float(r[q][j + 2]), __uint_as_float(r[q][j + 3]));
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mq[q] = fmaxf(m[2 * q], m[2 * q + 1]);
+}
+
+// Screen 128 columns of one row (accumulator bits in r, columns jt ..): the
+// per-chunk maxima raise the running maximum, and every pair of a chunk that
+// reaches the threshold goes to the CTA's pool.
+struct ScRow {
+    float Lb, Mg, off, tk, inv_tk, runmax;
+    uint2* pool;
+    int* pcount;
+    int cap;
+    int* lost;   // this row's "lost" word
+    unsigned rl; // row within the row block
+    bool erow;
+};
+__device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt, ScRow& s) {
+    float mq[4];
+    tc_chunk_max(r, mq);
+    // thresholds in accumulator units (score = tk * acc, tk > 0)
+    s.runmax = fmaxf(s.runmax, s.tk * fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
+    // (a reciprocal, not a division: the margin absorbs its rounding)
+    const float Ta = (fmaxf(s.Lb, s.runmax - s.Mg) - s.off) * s.inv_tk;
+    bool hq[4];
+    bool hit = false;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        float m = -INFINITY;
+        hq[q] = s.erow && mq[q] > Ta;
+        hit = hit || hq[q];
+    }
+    if (!__any_sync(0xffffffffu, hit)) return;
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) m = fmax3(m, __uint_as_float(r[q][j]), __uint_as_float(r[q][j + 1]));
-        mq[q] = m;
+    for (int q = 0; q < 4; ++q) {
+        if (__any_sync(0xffffffffu, hq[q]) && hq[q]) {
+            // bit j = sign of Ta - v_j: set exactly when v_j > Ta (a -inf or NaN
+            // score gives +inf or a positive NaN: never set)
+            unsigned mask = 0u;
+#pragma unroll
+            for (int j = 31; j >= 0; --j)
+                mask = __funnelshift_l(__float_as_uint(__fsub_rn(Ta, __uint_as_float(r[q][j]))), mask, 1);
+            const int k = __popc(mask);
+            if (k > 0) {
+                // Every reserved slot below the capacity is written, also when the
+                // reservation runs past it: the finaliser reads slots [0, min(count,
+                // cap)), and a slot left unwritten would hold a stale entry.  The
+                // entries of a row that did not fit are ignored (the row is lost).
+                int slot = atomicAdd(s.pcount, k);
+                if (slot + k > s.cap) *s.lost = 1;
+                while (mask) {
+                    const int j = __ffs(mask) - 1;
+                    mask &= mask - 1u;
+                    if (slot < s.cap) s.pool[slot] = make_uint2((unsigned)(jt + 32 * q + j), s.rl);
+                    ++slot;
+                }
+            }
+        }
     }
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, TcOps ops, TcScreenK sk) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     extern __shared__ unsigned char smem_raw[];
-    const TcSmem S = tc_smem(smem_raw);
+    const TcSmem S = tc_smem(smem_raw, SC_OFF_HDR);
     int* misc = S.misc();
     volatile int* abort = S.abort();
     int* retry = S.retry();
@@ -782,10 +915,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     const int b = blockIdx.y;
     const int rb = blockIdx.x / p.split, ch = blockIdx.x % p.split;
     const int row0 = rb * TC_ROWS;
-    const int c_begin = ch * p.chunk;
+    const int c_begin = ch * p.chunk;  // a multiple of SC_N
     const int c_end = min(p.nc, c_begin + p.chunk);
     const int t0 = c_begin / TC_N;
-    const int nt = (c_end - c_begin + TC_N - 1) / TC_N;
+    const int nt = (c_end - c_begin + SC_N - 1) / SC_N;  // 256-column tiles
     const float* cw = p.cw2 + (size_t)b * p.nc;
     const float* cst = p.cstate + (size_t)b * p.nc;
     const size_t rbase = (size_t)b * p.nr;
@@ -796,8 +929,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
         for (int k = threadIdx.x; k < p.B; k += TC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
     // Row-side constants of the bias step, (2^E, 2^(E-11), 2^(E-22), 0, ...) in
-    // K = 0..15 of every row, into the lo slots of both row tiles.  A cloud
-    // whose biases need E > 15 is not screened: its rows take the exact LSE.
+    // K = 0..15 of every row of both row tiles.  A cloud whose biases need
+    // E > 15 is not screened: its rows take the exact LSE.
     const int E = tc_bias_exp(sk.cmax[b], sc, p.two_kappa);
     const bool screenable = E <= 15;
     const int nts = screenable ? nt : 0;  // tiles this CTA screens
@@ -808,8 +941,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const uint4 c0 = make_uint4(h0 | (h1 << 16), h2, 0u, 0u), z = make_uint4(0u, 0u, 0u, 0u);
         for (int e = threadIdx.x; e < 2 * TC_M * 2; e += TC_THREADS) {
             const int rt = e / (2 * TC_M), r = (e % (2 * TC_M)) >> 1, c = e & 1;
-            *reinterpret_cast<uint4*>(S.sm + OFF_A + rt * OP_BYTES + TILE_BYTES + sw128_offset(r, 8 * c)) =
-                c ? z : c0;
+            *reinterpret_cast<uint4*>(S.sm + SC_OFF_AC + rt * SC_AT + sw32_offset(r, 8 * c)) = c ? z : c0;
         }
         fence_proxy_async_smem();
     }
@@ -822,9 +954,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nts, true);
+        sc_producer(S, ops, b, rb, t0, nts);
     } else if (warp == 1) {
-        tc_mma<true>(S, tmem, nts);
+        sc_mma(S, tmem, nts);
     } else {
         if (!screenable && erow) sk.lost[rbase + row] = 1;
         // screening margin of this cloud (scaled units -> log2 units); the
@@ -833,77 +965,43 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const float hr = __uint_as_float(sk.nrm_r[4 * b]), rr = __uint_as_float(sk.nrm_r[4 * b + 1]);
         const float hc = __uint_as_float(sk.nrm_c[4 * b]), rc = __uint_as_float(sk.nrm_c[4 * b + 1]);
         const float cmax = __uint_as_float(sk.cmax[b]);
-        const float Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) +
-                         1.5258789e-5f * cmax + 0.02f;
-        const float theta = 26.f + log2f((float)p.nc);
-        const float off = theta + Mg + 0.05f + 1.5e-5f * fabsf(old);
-        float Lb = -INFINITY;
+        ScRow s;
+        s.Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 1.5258789e-5f * cmax + 0.02f;
+        s.off = 26.f + log2f((float)p.nc) + s.Mg + 0.05f + 1.5e-5f * fabsf(old);
+        s.Lb = -INFINITY;
         if (!p.cold && p.lo_in) {
             const float lo = ord_decode(p.lo_in[b]);
-            if (isfinite(lo)) Lb = old + lo;
+            if (isfinite(lo)) s.Lb = old + lo;
         }
-        float runmax = -INFINITY;
-        uint2* pool = sk.pool + (cta0 + ch) * (size_t)sk.pool_cap;
-        int* pcount = misc + 4;
-        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's lane quarter
+        s.tk = tk;
+        s.inv_tk = 1.f / tk;
+        s.runmax = -INFINITY;
+        s.pool = sk.pool + (cta0 + ch) * (size_t)sk.pool_cap;
+        s.pcount = misc + 4;
+        s.cap = sk.pool_cap;
+        s.lost = sk.lost + rbase + (erow ? row : 0);
+        s.rl = (unsigned)(row - row0);
+        s.erow = erow;
+        const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(wg * SC_N);  // this warp's lanes
         for (int lt = 0; lt < nts; ++lt) {
-            const int u = lt & 1;
-            const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, 0)), (uint32_t)lt & 1u, abort, TC_WAIT_NS)) break;
             tc_fence_after();
-            const uint32_t tb = tq + (uint32_t)((2 * wg + u) * TC_N);
-            const int jt = (t0 + lt) * TC_N;
+            const int jt = c_begin + lt * SC_N;
             uint32_t r[4][32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld32_issue(tb + 32u * (uint32_t)q, r[q]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
-            // the tile is in registers: hand the buffer back to the MMA warp
+            sc_screen_128(r, jt, s);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32_issue(tb + 128u + 32u * (uint32_t)q, r[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
+            // the whole accumulator is read: hand it back to the MMA warp
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(wg, u)));
-            float mq[4];
-            tc_chunk_max(r, mq);
-            // thresholds in accumulator units (score = tk * acc, tk > 0)
-            runmax = fmaxf(runmax, tk * fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
-            const float Ta = (fmaxf(Lb, runmax - Mg) - off) / tk;
-            bool hq[4];
-            bool hit = false;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                hq[q] = erow && mq[q] >= Ta;
-                hit = hit || hq[q];
-            }
-            if (__any_sync(0xffffffffu, hit)) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (__any_sync(0xffffffffu, hq[q]) && hq[q]) {
-                        unsigned mask = 0u;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float v = __uint_as_float(r[q][j]);
-                            mask |= (v >= Ta && v > -INFINITY) ? (1u << j) : 0u;
-                        }
-                        const int k = __popc(mask);
-                        if (k > 0) {
-                            // Every reserved slot below the capacity is written, also when
-                            // the reservation runs past it: the finaliser reads slots [0,
-                            // min(count, cap)), and a slot left unwritten would hold a stale
-                            // entry.  The entries of a row that did not fit are ignored (the
-                            // row is lost).
-                            int slot = atomicAdd(pcount, k);
-                            if (slot + k > sk.pool_cap) sk.lost[rbase + row] = 1;
-                            while (mask) {
-                                const int j = __ffs(mask) - 1;
-                                mask &= mask - 1u;
-                                if (slot < sk.pool_cap)
-                                    pool[slot] = make_uint2((unsigned)(jt + 32 * q + j), (unsigned)(row - row0));
-                                ++slot;
-                            }
-                        }
-                    }
-                }
-            }
+            if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(wg, 0)));
+            sc_screen_128(r, jt + 128, s);
         }
     }
 
@@ -932,7 +1030,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     }
 
     // ---------------- finish the row block: exact scores of the kept pairs ----------------
-    float* sx = reinterpret_cast<float*>(S.sm + OFF_B);                     // [TC_ROWS][TC_XS] fp32 rows
+    float* sx = reinterpret_cast<float*>(S.sm + SC_OFF_B);                  // [TC_ROWS][TC_XS] fp32 rows
     float* s_ref = sx + TC_ROWS * TC_XS;                                     // [TC_ROWS] reference L_old
     unsigned* s_max = reinterpret_cast<unsigned*>(s_ref + TC_ROWS);          // [TC_ROWS] ord-encoded max
     unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(s_max + TC_ROWS);  // [TC_ROWS] fixed point
@@ -1063,11 +1161,12 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
     sk.ovf = sc.ovf;
     sk.nrm_r = plan.nrm + (h ? 2 : 0);
     sk.nrm_c = plan.nrm + (h ? 0 : 2);
-    cudaError_t e = cudaFuncSetAttribute(tc_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (p.chunk % SC_N != 0 || ops.tiles_c % 2 != 0) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(tc_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(p.rowtiles * p.split, p.B), block(TC_THREADS);
     count_launches(1);
-    tc_screen_kernel<<<grid, block, TC_SMEM, st>>>(p, ops, sk);
+    tc_screen_kernel<<<grid, block, SC_SMEM, st>>>(p, ops, sk);
     return cudaGetLastError();
 }
 
@@ -1137,7 +1236,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     if (warp == 0) {
         tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma<false>(S, tmem, nt);
+        tc_mma(S, tmem, nt);
     } else {
         const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
         m = erow ? lrow - SOT_STAB_BIAS : INFINITY;

@@ -170,6 +170,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for a K-major operand with K = 16 fp16 (32 bytes per row) stored
+// with the 32-byte swizzle: 8-row x 32-byte atoms, 256 bytes apart.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= (uint64_t)1 << 16;                      // leading byte offset (unused: K fits one atom row)
+    d |= (uint64_t)(256 >> 4) << 32;             // stride byte offset: 8 rows x 32 B
+    d |= (uint64_t)1 << 46;                      // descriptor version for tcgen05
+    d |= (uint64_t)6 << 61;                      // swizzle mode: 32 B
+    return d;
+}
+
 // Instruction descriptor, kind::f16: fp16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
     return (1u << 4)                        // D format: f32
@@ -183,6 +195,13 @@ __host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
 // chunk index (k / 8) is XOR-ed with the row within its 8-row atom.
 __host__ __device__ inline uint32_t sw128_offset(int r, int k) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ (r & 7)) & 7) << 4) + (k & 7) * 2);
+}
+
+// Byte offset of fp16 element (r, k), 0 <= k < 16, in a K-major block of
+// 32-byte rows with the 32-byte swizzle: the 16-byte chunk index (k / 8)
+// is XOR-ed with bit 2 of the row.
+__host__ __device__ inline uint32_t sw32_offset(int r, int k) {
+    return (uint32_t)((r >> 3) * 256 + (r & 7) * 32 + ((((k >> 3) ^ (r >> 2)) & 1) << 4) + (k & 7) * 2);
 }
 
 }  // namespace sot
