@@ -35,6 +35,19 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
     return d;
 }
 
+// Error-free transformations: a + b = s + e exactly (Knuth), a * b = p + e
+// exactly (FMA); explicitly rounded so the compiler neither fuses nor
+// reorders them.
+__device__ __forceinline__ float2 two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float z = __fsub_rn(s, a);
+    return make_float2(s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z)));
+}
+__device__ __forceinline__ float2 two_prod(float a, float b) {
+    const float q = __fmul_rn(a, b);
+    return make_float2(q, __fmaf_rn(a, b, -q));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

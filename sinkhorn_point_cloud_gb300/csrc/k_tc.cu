@@ -1100,10 +1100,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                 es[w] = __fadd_rn(es[w], __fadd_rn(pe, se));
             }
         }
-        const double dot = ((double)hs[0] + (double)hs[1]) + ((double)hs[2] + (double)hs[3]) +
-                           (((double)es[0] + (double)es[1]) + ((double)es[2] + (double)es[3]));
-        const double t = (double)p.two_kappa * dot + ((double)cw[j] - (double)cst[j]);
-        const float trel = (float)(t - (double)s_ref[rl]);
+        // t - ref = 2 kappa (sum hs + sum es) + (cw_j - cst_j) - ref in float-float
+        // arithmetic (error-free sums and products; the fp64 pipe is slow here):
+        // the large parts cancel exactly, the small ones are added last
+        const float2 s01 = two_sum(hs[0], hs[1]), s23 = two_sum(hs[2], hs[3]);
+        const float2 S2 = two_sum(s01.x, s23.x);
+        const float E2 = __fadd_rn(__fadd_rn(__fadd_rn(es[0], es[1]), __fadd_rn(es[2], es[3])),
+                                   __fadd_rn(__fadd_rn(s01.y, s23.y), S2.y));
+        const float2 P2 = two_prod(p.two_kappa, S2.x);
+        const float2 C2 = two_sum(cw[j], -cst[j]);
+        const float2 U2 = two_sum(P2.x, C2.x);
+        const float2 V2 = two_sum(U2.x, -s_ref[rl]);
+        const float trel = __fadd_rn(V2.x, __fadd_rn(__fadd_rn(V2.y, U2.y), __fadd_rn(__fadd_rn(P2.y, C2.y),
+                                                                                       __fmul_rn(p.two_kappa, E2))));
         e->x = __float_as_uint(trel);
         atomicMax(s_max + rl, ord_encode(trel));
     }
@@ -1131,7 +1140,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
             p.rstate_out[rbase + row] = -INFINITY;
         } else {
             p.rstate_out[rbase + row] =
-                (float)((double)s_ref[rl] + (double)ord_decode(s_max[rl]) + log2((double)s_sum[rl]) - 48.0);
+                s_ref[rl] + (ord_decode(s_max[rl]) + (log2f(__ull2float_rn(s_sum[rl])) - 48.f));
         }
     }
     tc_tail(p, S, erow, row, old, b, rb, rbase, cw, cst);
