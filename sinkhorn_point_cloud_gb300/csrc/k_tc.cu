@@ -1037,12 +1037,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     int* s_lost = reinterpret_cast<int*>(s_sum + TC_ROWS);                   // [TC_ROWS]
     int* s_off = s_lost + TC_ROWS;                                           // [split + 1]
     {
+        // the block's fp32 rows: every load issued before the first store
         const float4* src = reinterpret_cast<const float4*>(p.rpack + rbase * TC_D);
-        for (int e = threadIdx.x; e < TC_ROWS * (TC_D / 4); e += TC_THREADS) {
-            const int r = e / (TC_D / 4), q = e % (TC_D / 4);
-            const int rg = row0 + r;
-            *reinterpret_cast<float4*>(sx + r * TC_XS + 4 * q) =
-                (rg < p.nr) ? src[(size_t)rg * (TC_D / 4) + q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        constexpr int NE = TC_ROWS * (TC_D / 4), NL = (NE + TC_THREADS - 1) / TC_THREADS;
+        float4 buf[NL];
+#pragma unroll
+        for (int i = 0; i < NL; ++i) {
+            const int e = threadIdx.x + i * TC_THREADS, rg = row0 + e / (TC_D / 4);
+            buf[i] = (e < NE && rg < p.nr) ? __ldg(src + (size_t)rg * (TC_D / 4) + e % (TC_D / 4))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < NL; ++i) {
+            const int e = threadIdx.x + i * TC_THREADS;
+            if (e < NE) *reinterpret_cast<float4*>(sx + (e / (TC_D / 4)) * TC_XS + 4 * (e % (TC_D / 4))) = buf[i];
         }
         for (int r = threadIdx.x; r < TC_ROWS; r += TC_THREADS) {
             const int rg = row0 + r;
@@ -1071,33 +1079,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     __syncthreads();
     const int total = s_off[p.split];
     const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
-    // pass 1: exact score of every kept pair, relative to the row's reference; row maxima
-    for (int k = threadIdx.x; k < total; k += TC_THREADS) {
+    // pass 1: exact score of every kept pair, relative to the row's reference;
+    // row maxima.  Two pairs per thread and round, all their loads in flight.
+    auto entry = [&](int k) -> uint2* {
         int c = 0;
         while (c + 1 < p.split && s_off[c + 1] <= k) ++c;
-        uint2* e = sk.pool + (cta0 + c) * (size_t)sk.pool_cap + (k - s_off[c]);
-        const uint2 it = __ldcg(e);
-        const int j = (int)it.x, rl = (int)it.y;
-        if (s_lost[rl]) continue;
+        return sk.pool + (cta0 + c) * (size_t)sk.pool_cap + (k - s_off[c]);
+    };
+    auto exact = [&](uint2 it, const float4 (&yv)[TC_D / 4]) -> float {
+        const int rl = (int)it.y, j = (int)it.x;
         const float* xr = sx + rl * TC_XS;
-        const float4* yr = ybase + (size_t)j * (TC_D / 4);
         float hs[4] = {0.f, 0.f, 0.f, 0.f}, es[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < TC_D / 4; ++q) {
-            const float4 y = __ldg(yr + q);
             const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q);
             const float xa[4] = {x.x, x.y, x.z, x.w};
-            const float ya[4] = {y.x, y.y, y.z, y.w};
+            const float ya[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 // error-free product and sum (Dekker / Knuth), errors summed alongside
-                const float pr = __fmul_rn(xa[w], ya[w]);
-                const float pe = __fmaf_rn(xa[w], ya[w], -pr);
-                const float sn = __fadd_rn(hs[w], pr);
-                const float z = __fsub_rn(sn, hs[w]);
-                const float se = __fadd_rn(__fsub_rn(hs[w], __fsub_rn(sn, z)), __fsub_rn(pr, z));
-                hs[w] = sn;
-                es[w] = __fadd_rn(es[w], __fadd_rn(pe, se));
+                const float2 pr = two_prod(xa[w], ya[w]);
+                const float2 sn = two_sum(hs[w], pr.x);
+                hs[w] = sn.x;
+                es[w] = __fadd_rn(es[w], __fadd_rn(pr.y, sn.y));
             }
         }
         // t - ref = 2 kappa (sum hs + sum es) + (cw_j - cst_j) - ref in float-float
@@ -1111,21 +1115,57 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const float2 C2 = two_sum(cw[j], -cst[j]);
         const float2 U2 = two_sum(P2.x, C2.x);
         const float2 V2 = two_sum(U2.x, -s_ref[rl]);
-        const float trel = __fadd_rn(V2.x, __fadd_rn(__fadd_rn(V2.y, U2.y), __fadd_rn(__fadd_rn(P2.y, C2.y),
-                                                                                       __fmul_rn(p.two_kappa, E2))));
-        e->x = __float_as_uint(trel);
-        atomicMax(s_max + rl, ord_encode(trel));
+        return __fadd_rn(V2.x, __fadd_rn(__fadd_rn(V2.y, U2.y),
+                                         __fadd_rn(__fadd_rn(P2.y, C2.y), __fmul_rn(p.two_kappa, E2))));
+    };
+    for (int k0 = threadIdx.x; k0 < total; k0 += 2 * TC_THREADS) {
+        const int k1 = k0 + TC_THREADS;
+        uint2* e0 = entry(k0);
+        uint2* e1 = (k1 < total) ? entry(k1) : e0;
+        const uint2 it0 = __ldcg(e0), it1 = __ldcg(e1);
+        const bool v0 = !s_lost[it0.y] && (int)it0.x < p.nc;
+        const bool v1 = k1 < total && !s_lost[it1.y] && (int)it1.x < p.nc;
+        const float4* y0 = ybase + (size_t)(v0 ? it0.x : 0u) * (TC_D / 4);
+        const float4* y1 = ybase + (size_t)(v1 ? it1.x : 0u) * (TC_D / 4);
+        float4 ya[TC_D / 4], yb[TC_D / 4];
+#pragma unroll
+        for (int q = 0; q < TC_D / 4; ++q) {
+            ya[q] = __ldg(y0 + q);
+            yb[q] = __ldg(y1 + q);
+        }
+        // (an entry past the last column cannot occur; it would add nothing)
+        if (v0) {
+            const float trel = exact(it0, ya);
+            e0->x = __float_as_uint(trel);
+            atomicMax(s_max + it0.y, ord_encode(trel));
+        } else if (!s_lost[it0.y]) {
+            e0->x = __float_as_uint(-INFINITY);
+        }
+        if (v1) {
+            const float trel = exact(it1, yb);
+            e1->x = __float_as_uint(trel);
+            atomicMax(s_max + it1.y, ord_encode(trel));
+        } else if (k1 < total && !s_lost[it1.y]) {
+            e1->x = __float_as_uint(-INFINITY);
+        }
     }
     __syncthreads();
-    // pass 2: row sums in 2^-48 fixed point (each term <= 1)
-    for (int k = threadIdx.x; k < total; k += TC_THREADS) {
-        int c = 0;
-        while (c + 1 < p.split && s_off[c + 1] <= k) ++c;
-        const uint2 it = __ldcg(sk.pool + (cta0 + c) * (size_t)sk.pool_cap + (k - s_off[c]));
-        const int rl = (int)it.y;
-        if (s_lost[rl]) continue;
-        const float w = ex2f(__uint_as_float(it.x) - ord_decode(s_max[rl]));
-        atomicAdd(s_sum + rl, (unsigned long long)__float2ull_rn(w * 281474976710656.f));
+    // pass 2: row sums in 2^-48 fixed point (each term <= 1), four entries per round
+    for (int k0 = threadIdx.x; k0 < total; k0 += 4 * TC_THREADS) {
+        uint2 it[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u * TC_THREADS;
+            it[u] = (k < total) ? __ldcg(entry(k)) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u * TC_THREADS;
+            const int rl = (int)it[u].y;
+            if (k >= total || s_lost[rl]) continue;
+            const float w = ex2f(__uint_as_float(it[u].x) - ord_decode(s_max[rl]));
+            atomicAdd(s_sum + rl, (unsigned long long)__float2ull_rn(w * 281474976710656.f));
+        }
     }
     if (threadIdx.x == 0) misc[2] = 0;
     __syncthreads();
