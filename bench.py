@@ -443,7 +443,7 @@ def main(argv=None):
     ap.add_argument("--n", type=int, default=0, help="override n = m (testing only)")
     ap.add_argument("--iters", type=int, default=0, help="override the iteration count (testing only)")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
-    ap.add_argument("--cpu-baseline-s", type=float, default=12.0,
+    ap.add_argument("--cpu-baseline-s", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample of the GPU arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
