@@ -339,7 +339,9 @@ __device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr, uint32_t hdr =
 // Barriers, TMEM allocation (warp 1, 512 columns); returns the TMEM base address.
 // `empty_count`: arrivals that free a stage (the MMA commit, plus one per
 // epilogue warp when the epilogue reads the stage's biases).
-__device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t empty_count = 1 + 8) {
+// `accempty_count`: epilogue warps that read (and free) one accumulator buffer.
+__device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t empty_count = 1 + 8,
+                                             uint32_t accempty_count = 4) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_S; ++s) {
             mbar_init(S.bar(BAR_FULL(s)), 1);
@@ -348,7 +350,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
         for (int r = 0; r < 2; ++r)
             for (int u = 0; u < 2; ++u) {
                 mbar_init(S.bar(BAR_ACCFULL(r, u)), 1);
-                mbar_init(S.bar(BAR_ACCEMPTY(r, u)), 4);
+                mbar_init(S.bar(BAR_ACCEMPTY(r, u)), accempty_count);
             }
         mbar_init(S.bar(BAR_A()), 1);
         S.misc()[1] = 0;
@@ -742,9 +744,12 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 // on the order).  A row with a pair that did not fit in a pool takes the
 // exact full-row LSE.
 constexpr int TC_POOL = 4096;  // kept pairs per CTA
+constexpr int SC_SEGS = 8;     // pool segments per CTA, one per epilogue warp
+constexpr int SC_SEG = TC_POOL / SC_SEGS;
 int tc_screen_pool_cap() { return TC_POOL; }
+int tc_screen_pool_segments() { return SC_SEGS; }
 constexpr int TC_XS = TC_D + 4;  // row stride of the fp32 row tile in shared memory (bank spread)
-static_assert(TC_ROWS * TC_XS * 4 + TC_ROWS * 16 + 64 * 4 + 64 <= TC_S * SC_STAGE, "finaliser shared memory");
+static_assert(TC_ROWS * TC_XS * 4 + TC_ROWS * 16 + (64 * SC_SEGS + 1) * 4 <= TC_S * SC_STAGE, "finaliser shared memory");
 
 // Producer of the screened half-step: the hi halves of the CTA's two row
 // tiles once, then per 256-column tile the hi halves of its two 128-point
@@ -851,22 +856,24 @@ __device__ __forceinline__ void tc_chunk_max(const uint32_t (&r)[4][32], float (
 // Screen 128 columns of one row (accumulator bits in r, columns jt ..): the
 // per-chunk maxima raise the running maximum, and every pair of a chunk that
 // reaches the threshold goes to the CTA's pool.
-struct ScRow {
-    float Lb, Mg, off, tk, inv_tk, runmax;
-    uint2* pool;
-    int* pcount;
-    int cap;
+struct ScShared {  // the same for every row of the warp
+    float Mg, tk, inv_tk;
+    uint2* seg;   // this warp's pool segment
+    int wcount;   // entries reserved in it (warp-uniform)
+};
+struct ScRow {  // one row's screening state
+    float Lb, off, runmax;
     int* lost;   // this row's "lost" word
     unsigned rl; // row within the row block
     bool erow;
 };
-__device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt, ScRow& s) {
+__device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt, ScShared& c, ScRow& s) {
     float mq[4];
     tc_chunk_max(r, mq);
     // thresholds in accumulator units (score = tk * acc, tk > 0)
-    s.runmax = fmaxf(s.runmax, s.tk * fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
+    s.runmax = fmaxf(s.runmax, c.tk * fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
     // (a reciprocal, not a division: the margin absorbs its rounding)
-    const float Ta = (fmaxf(s.Lb, s.runmax - s.Mg) - s.off) * s.inv_tk;
+    const float Ta = (fmaxf(s.Lb, s.runmax - c.Mg) - s.off) * c.inv_tk;
     bool hq[4];
     bool hit = false;
 #pragma unroll
@@ -875,30 +882,32 @@ __device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt
         hit = hit || hq[q];
     }
     if (!__any_sync(0xffffffffu, hit)) return;
+    const unsigned lt_mask = (1u << (threadIdx.x & 31)) - 1u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        if (__any_sync(0xffffffffu, hq[q]) && hq[q]) {
+        if (!__any_sync(0xffffffffu, hq[q])) continue;
+        unsigned pm = 0u;  // this lane's kept columns of the chunk
+        if (hq[q]) {
             // bit j = sign of Ta - v_j: set exactly when v_j > Ta (a -inf or NaN
             // score gives +inf or a positive NaN: never set)
-            unsigned mask = 0u;
 #pragma unroll
             for (int j = 31; j >= 0; --j)
-                mask = __funnelshift_l(__float_as_uint(__fsub_rn(Ta, __uint_as_float(r[q][j]))), mask, 1);
-            const int k = __popc(mask);
-            if (k > 0) {
-                // Every reserved slot below the capacity is written, also when the
-                // reservation runs past it: the finaliser reads slots [0, min(count,
-                // cap)), and a slot left unwritten would hold a stale entry.  The
-                // entries of a row that did not fit are ignored (the row is lost).
-                int slot = atomicAdd(s.pcount, k);
-                if (slot + k > s.cap) *s.lost = 1;
-                while (mask) {
-                    const int j = __ffs(mask) - 1;
-                    mask &= mask - 1u;
-                    if (slot < s.cap) s.pool[slot] = make_uint2((unsigned)(jt + 32 * q + j), s.rl);
-                    ++slot;
-                }
+                pm = __funnelshift_l(__float_as_uint(__fsub_rn(Ta, __uint_as_float(r[q][j]))), pm, 1);
+        }
+        // Slots of the warp's segment, one pair per lane and round, numbered by
+        // lane order (ballot + popc): dense, so every slot below the capacity that
+        // is counted is written.  A pair past the capacity loses its row.
+        for (;;) {
+            const unsigned act = __ballot_sync(0xffffffffu, pm != 0u);
+            if (act == 0u) break;
+            if (pm) {
+                const int j = __ffs(pm) - 1;
+                pm &= pm - 1u;
+                const int slot = c.wcount + __popc(act & lt_mask);
+                if (slot < SC_SEG) c.seg[slot] = make_uint2((unsigned)(jt + 32 * q + j), s.rl);
+                else *s.lost = 1;
             }
+            c.wcount += __popc(act);
         }
     }
 }
@@ -945,10 +954,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         }
         fence_proxy_async_smem();
     }
-    const uint32_t tmem = tc_setup(S, warp, 1);  // stages are freed by the MMA commit alone
+    // stages are freed by the MMA commit alone; every accumulator is read by all 8 epilogue warps
+    const uint32_t tmem = tc_setup(S, warp, 1, 8);
 
     const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
+    // the row this thread finalises (and whose marginal-error term it forms)
     const int row = row0 + wg * TC_M + q4 * 32 + lane;
     const bool erow = (warp >= 2) && row < p.nr;
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
@@ -958,6 +969,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     } else if (warp == 1) {
         sc_mma(S, tmem, nts);
     } else {
+        // Screening: epilogue warp (wg, q4) reads columns 128 wg .. of both row tiles'
+        // accumulators for TMEM lanes 32 q4 ..: rows row0 + 32 q4 + lane (tile 0) and
+        // row0 + 128 + 32 q4 + lane (tile 1).  An accumulator is freed as soon as all
+        // eight warps have loaded their half, before the screening arithmetic.
         if (!screenable && erow) sk.lost[rbase + row] = 1;
         // screening margin of this cloud (scaled units -> log2 units); the
         // last term covers the fp32 rounding of the biases held in the
@@ -965,44 +980,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const float hr = __uint_as_float(sk.nrm_r[4 * b]), rr = __uint_as_float(sk.nrm_r[4 * b + 1]);
         const float hc = __uint_as_float(sk.nrm_c[4 * b]), rc = __uint_as_float(sk.nrm_c[4 * b + 1]);
         const float cmax = __uint_as_float(sk.cmax[b]);
-        ScRow s;
-        s.Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 1.5258789e-5f * cmax + 0.02f;
-        s.off = 26.f + log2f((float)p.nc) + s.Mg + 0.05f + 1.5e-5f * fabsf(old);
-        s.Lb = -INFINITY;
-        if (!p.cold && p.lo_in) {
-            const float lo = ord_decode(p.lo_in[b]);
-            if (isfinite(lo)) s.Lb = old + lo;
+        ScShared c;
+        c.Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 1.5258789e-5f * cmax + 0.02f;
+        c.tk = tk;
+        c.inv_tk = 1.f / tk;
+        c.seg = sk.pool + ((cta0 + ch) * SC_SEGS + (warp - 2)) * (size_t)SC_SEG;
+        c.wcount = 0;
+        const float theta_off = 26.f + log2f((float)p.nc) + c.Mg + 0.05f;
+        const float lo = (!p.cold && p.lo_in) ? ord_decode(p.lo_in[b]) : -INFINITY;
+        ScRow s[2];
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+            const int rrow = row0 + rt * TC_M + q4 * 32 + lane;
+            const bool ok_row = rrow < p.nr;
+            const float o = (ok_row && p.rstate_in) ? p.rstate_in[rbase + rrow] : 0.f;
+            s[rt].off = theta_off + 1.5e-5f * fabsf(o);
+            s[rt].Lb = isfinite(lo) ? o + lo : -INFINITY;
+            s[rt].runmax = -INFINITY;
+            s[rt].lost = sk.lost + rbase + (ok_row ? rrow : 0);
+            s[rt].rl = (unsigned)(rt * TC_M + q4 * 32 + lane);
+            s[rt].erow = ok_row;
         }
-        s.tk = tk;
-        s.inv_tk = 1.f / tk;
-        s.runmax = -INFINITY;
-        s.pool = sk.pool + (cta0 + ch) * (size_t)sk.pool_cap;
-        s.pcount = misc + 4;
-        s.cap = sk.pool_cap;
-        s.lost = sk.lost + rbase + (erow ? row : 0);
-        s.rl = (unsigned)(row - row0);
-        s.erow = erow;
-        const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(wg * SC_N);  // this warp's lanes
-        for (int lt = 0; lt < nts; ++lt) {
-            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, 0)), (uint32_t)lt & 1u, abort, TC_WAIT_NS)) break;
-            tc_fence_after();
-            const int jt = c_begin + lt * SC_N;
-            uint32_t r[4][32];
+        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(wg * 128);  // lanes, column half
+        bool ok = true;
+        for (int lt = 0; ok && lt < nts; ++lt) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32_issue(tb + 32u * (uint32_t)q, r[q]);
+            for (int rt = 0; rt < 2; ++rt) {
+                if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(rt, 0)), (uint32_t)lt & 1u, abort, TC_WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r[4][32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
-            sc_screen_128(r, jt, s);
+                for (int q = 0; q < 4; ++q) tmem_ld32_issue(tq + (uint32_t)(rt * SC_N) + 32u * (uint32_t)q, r[q]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32_issue(tb + 128u + 32u * (uint32_t)q, r[q]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
-            // the whole accumulator is read: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(wg, 0)));
-            sc_screen_128(r, jt + 128, s);
+                for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
+                // this warp's share of the accumulator is in registers: free it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(rt, 0)));
+                sc_screen_128(r, c_begin + lt * SC_N + 128 * wg, c, s[rt]);
+            }
         }
+        if (lane == 0) sk.pool_cnt[(cta0 + ch) * SC_SEGS + (warp - 2)] = min(c.wcount, SC_SEG);
     }
 
     tc_fence_before();
@@ -1015,7 +1036,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         if (erow) sk.lost[rbase + row] = 2;  // poisoned
         if (threadIdx.x == 0) atomicOr(p.status, SOT_DEV_TIMEOUT);
     }
-    if (threadIdx.x == 0) sk.pool_cnt[cta0 + ch] = min(misc[4], sk.pool_cap);
+    // (pool_cnt: written by each epilogue warp for its segment)
     if (p.split > 1) {
         __threadfence();
         __syncthreads();
@@ -1035,7 +1056,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     unsigned* s_max = reinterpret_cast<unsigned*>(s_ref + TC_ROWS);          // [TC_ROWS] ord-encoded max
     unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(s_max + TC_ROWS);  // [TC_ROWS] fixed point
     int* s_lost = reinterpret_cast<int*>(s_sum + TC_ROWS);                   // [TC_ROWS]
-    int* s_off = s_lost + TC_ROWS;                                           // [split + 1]
+    int* s_off = s_lost + TC_ROWS;                                           // [split * SC_SEGS + 1]
     {
         // the block's fp32 rows: every load issued before the first store
         const float4* src = reinterpret_cast<const float4*>(p.rpack + rbase * TC_D);
@@ -1069,22 +1090,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         }
         if (threadIdx.x == 0) {
             int acc = 0;
-            for (int c = 0; c < p.split; ++c) {
-                s_off[c] = acc;
-                acc += __ldcg(sk.pool_cnt + cta0 + c);
+            for (int g = 0; g < p.split * SC_SEGS; ++g) {
+                s_off[g] = acc;
+                acc += __ldcg(sk.pool_cnt + cta0 * SC_SEGS + g);
             }
-            s_off[p.split] = acc;
+            s_off[p.split * SC_SEGS] = acc;
         }
     }
     __syncthreads();
-    const int total = s_off[p.split];
+    const int nseg = p.split * SC_SEGS;
+    const int total = s_off[nseg];
     const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
     // pass 1: exact score of every kept pair, relative to the row's reference;
     // row maxima.  Two pairs per thread and round, all their loads in flight.
-    auto entry = [&](int k) -> uint2* {
-        int c = 0;
-        while (c + 1 < p.split && s_off[c + 1] <= k) ++c;
-        return sk.pool + (cta0 + c) * (size_t)sk.pool_cap + (k - s_off[c]);
+    auto entry = [&](int k) -> uint2* {  // segment g with s_off[g] <= k < s_off[g + 1] (binary search)
+        int lo = 0, hi = nseg;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_off[mid] <= k) lo = mid; else hi = mid;
+        }
+        return sk.pool + (cta0 * SC_SEGS + lo) * (size_t)SC_SEG + (k - s_off[lo]);
     };
     auto exact = [&](uint2 it, const float4 (&yv)[TC_D / 4]) -> float {
         const int rl = (int)it.y, j = (int)it.x;

@@ -305,7 +305,7 @@ struct Solver {
                 const size_t ctas = (size_t)B * (ctas0 > ctas1 ? ctas0 : ctas1);
                 scr.pool_cap = tc_screen_pool_cap();
                 scr.pool = S.alloc<uint2>(ctas * scr.pool_cap);
-                scr.pool_cnt = S.alloc<int>(ctas);
+                scr.pool_cnt = S.alloc<int>(ctas * tc_screen_pool_segments());
                 scr.lost = S.alloc<int>(rows_max);
                 scr.ovf = S.alloc<int>(1);
                 if (!scr.pool || !scr.pool_cnt || !scr.lost || !scr.ovf)

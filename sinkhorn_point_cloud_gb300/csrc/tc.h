@@ -28,7 +28,7 @@ struct TcPlan {
 struct TcScreen {
     uint2* pool = nullptr;    // [B * rowtiles_max * split_max][pool_cap] (column, local row)
     int pool_cap = 0;
-    int* pool_cnt = nullptr;  // [B * rowtiles_max * split_max] entries used by each CTA
+    int* pool_cnt = nullptr;  // [B * rowtiles_max * split_max][segments] entries used in each pool segment
     int* lost = nullptr;      // [B * max(n, m)] rows with a pair that did not fit; zero between launches
     int* ovf = nullptr;       // running count of lost rows
 };
@@ -46,6 +46,7 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 // are evaluated exactly in fp32.  Same inputs and outputs as launch_tc_half.
 cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const TcScreen& sc, cudaStream_t st);
 int tc_screen_pool_cap();
+int tc_screen_pool_segments();
 bool tc_apply_supported(int d);
 bool tc_apply_default();
 int tc_apply_rows_per_cta();
