@@ -48,6 +48,21 @@ __device__ __forceinline__ float2 two_prod(float a, float b) {
     return make_float2(q, __fmaf_rn(a, b, -q));
 }
 
+// Float-float (unevaluated hi + lo) arithmetic on top of the error-free
+// transformations, renormalised so that |lo| <= ulp(hi) / 2.
+__device__ __forceinline__ float2 ff_renorm(float hi, float lo) {
+    const float s = __fadd_rn(hi, lo);
+    return make_float2(s, __fsub_rn(lo, __fsub_rn(s, hi)));
+}
+__device__ __forceinline__ float2 ff_add(float2 a, float2 b) {
+    const float2 s = two_sum(a.x, b.x);
+    return ff_renorm(s.x, __fadd_rn(s.y, __fadd_rn(a.y, b.y)));
+}
+__device__ __forceinline__ float2 ff_mul(float2 a, float2 b) {
+    const float2 q = two_prod(a.x, b.x);
+    return ff_renorm(q.x, __fmaf_rn(a.x, b.y, __fmaf_rn(a.y, b.x, q.y)));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

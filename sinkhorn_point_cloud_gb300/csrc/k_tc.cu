@@ -1314,7 +1314,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     } else {
         const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
         m = erow ? lrow - SOT_STAB_BIAS : INFINITY;
-        const double fi = erow ? (double)x.f[rbase + row] : 0.0;
+        const float fi = erow ? x.f[rbase + row] : 0.f;
+        const float2 kap = make_float2((float)x.kappa64, (float)(x.kappa64 - (double)(float)x.kappa64));
         const float* yorig = x.Y + (size_t)b * p.nc * TC_D;
         const float* gpot = x.g + (size_t)b * p.nc;
         const float2 tk2 = make_float2(tk, tk);
@@ -1382,8 +1383,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
             r += ts;
             // pass B: cost and barycentre terms of the significant pairs.  The warp
             // takes them one at a time: every lane owns 2 of the 64 coordinates,
-            // C_ij is reduced across the warp in fp64, and the row's v_i update is
-            // one coalesced 256-byte write.
+            // C_ij is reduced across the warp in float-float arithmetic (the fp64
+            // pipe is slow here), and the row's v_i update is one coalesced
+            // 256-byte write.
             const float sig_b = TC_SIG + (lrow - m);
 #pragma unroll 1
             for (int qq = 0; qq < TC_N / 32; ++qq) {
@@ -1398,24 +1400,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                     if (!todo) continue;
                     const int j = (t0 + lt) * TC_N + cl;
                     const float2 yv = *reinterpret_cast<const float2*>(yorig + (size_t)j * TC_D + 2 * lane);
-                    const double gj = (double)gpot[j], lbj = (double)cw[j];
+                    const float gj = gpot[j], lbj = cw[j];
                     while (todo) {
                         const int l = __ffs(todo) - 1;
                         todo &= todo - 1u;
                         const int rl = __shfl_sync(0xffffffffu, row, l);
                         const float2 xv = *reinterpret_cast<const float2*>(x.X + (rbase + rl) * TC_D + 2 * lane);
-                        const double d0 = (double)xv.x - yv.x, d1 = (double)xv.y - yv.y;
-                        double C64 = d0 * d0 + d1 * d1;
+                        // C_lj: exact coordinate differences, their squares to ~2^-48
+                        const float2 d0 = two_sum(xv.x, -yv.x), d1 = two_sum(xv.y, -yv.y);
+                        float2 s0 = two_prod(d0.x, d0.x), s1 = two_prod(d1.x, d1.x);
+                        s0.y = __fmaf_rn(2.f * d0.x, d0.y, s0.y);
+                        s1.y = __fmaf_rn(2.f * d1.x, d1.y, s1.y);
+                        float2 C2 = ff_add(s0, s1);
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) C64 += __shfl_xor_sync(0xffffffffu, C64, o);
-                        const double fl = __shfl_sync(0xffffffffu, fi, l);
+                        for (int o = 16; o > 0; o >>= 1)
+                            C2 = ff_add(C2, make_float2(__shfl_xor_sync(0xffffffffu, C2.x, o),
+                                                        __shfl_xor_sync(0xffffffffu, C2.y, o)));
+                        const float fl = __shfl_sync(0xffffffffu, fi, l);
                         const float off = __shfl_sync(0xffffffffu, lrow - m, l);  // L_l - m_l
-                        // exact term: log2(P/a_l) = log2 b_j + kappa (f_l + g_j - C_lj)
-                        const double ell = lbj + x.kappa64 * (fl + gj - C64);
-                        const float w = (float)exp2(ell + (double)off);
+                        // exact term: log2(P/a_l) = log2 b_j + kappa (f_l + g_j - C_lj); the
+                        // potentials and C_lj cancel to a small number: float-float throughout
+                        const float2 pot = ff_add(two_sum(fl, gj), make_float2(-C2.x, -C2.y));
+                        const float2 ell = ff_add(ff_mul(kap, pot), two_sum(lbj, off));
+                        const float w = exp2f(__fadd_rn(ell.x, ell.y));
+                        const float Cf = __fadd_rn(C2.x, C2.y);
                         if (lane == l) {
                             r += w - ex2f(e);
-                            q = fmaf(w, (float)C64, q);
+                            q = fmaf(w, Cf, q);
                         }
                         float* vr = x.vpart + (((size_t)ch * p.B * p.nr) + rbase + rl) * TC_D + 2 * lane;
                         float2 acc = *reinterpret_cast<float2*>(vr);
