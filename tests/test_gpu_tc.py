@@ -76,6 +76,35 @@ def test_tc_full_size_first_half_step(sot, orc):
     assert err < TOL, err
 
 
+def test_tc_full_size_screened_half_steps(sot, orc):
+    """n = m = 70000, d = 64, as bench.py runs it: every warm half-step is a
+    screened one.  Iteration 11 (both halves) is checked on sampled rows and
+    columns against the oracle's half-steps from the potentials the GPU held
+    after 10 iterations: the solve is bitwise reproducible, so the 11-iteration
+    run passes through exactly those potentials."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4)
+    eps = 0.1
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(True)
+    f10, g10 = sot.sot_potentials(Xd, Yd, ad, bd, eps=eps, iters=10)
+    f11, g11 = sot.sot_potentials(Xd, Yd, ad, bd, eps=eps, iters=11)
+    kinds = sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(False)
+    assert kinds["screened"][0] == 18 + 20, kinds  # 9 + 10 warm iterations, two halves each
+    g10h, f11h, g11h = host(g10)[0].astype(np.float64), host(f11)[0], host(g11)[0]
+    rng = np.random.default_rng(11)
+    rows = rng.choice(X.shape[1], 48, replace=False)
+    cols = rng.choice(Y.shape[1], 48, replace=False)
+    fr = orc.f_half(X[0][rows], Y[0], b[0], g10h, eps)
+    gr = orc.g_half(X[0], Y[0][cols], a[0], f11h.astype(np.float64), eps)
+    ef = np.max(np.abs(f11h[rows] - fr)) / np.max(np.abs(fr))
+    eg = np.max(np.abs(g11h[cols] - gr)) / np.max(np.abs(gr))
+    print(f"screened half-steps at full size: f {ef:.2e} g {eg:.2e}")
+    assert ef < 1e-5 and eg < 1e-5, (ef, eg)
+
+
 def test_tc_full_size_column_marginals(sot):
     """After 100 iterations (ending with a g-half) the column sums of the plan
     equal b exactly; recomputed in float64 for sampled columns."""
