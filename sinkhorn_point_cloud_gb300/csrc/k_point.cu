@@ -38,6 +38,9 @@ constexpr int PT_TC = 2 * PT_T;         // columns per shared-memory tile
 
 int point_rows_per_cta() { return PT_ROWS; }
 int point_cols_per_tile() { return PT_TC; }
+// Resident CTAs of the half-step kernel per SM (from the occupancy calculator,
+// queried once); the column split fills this many slots per SM.
+int point_blocks_per_sm();
 
 // Score relative to a base: acc = base + |u - v|^2 with d = u + (-v), fp32 in
 // this fixed order (the maximum passes and the COO predicate evaluate the same
@@ -570,6 +573,18 @@ cudaError_t launch_point_coo(const CooArgs& p, int write_pass, cudaStream_t st) 
     }
 #undef SOT_CO_CASE
     return cudaGetLastError();
+}
+
+int point_blocks_per_sm() {
+    static int occ = 0;
+    if (occ == 0) {
+        int v = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, point_half_kernel<3, MODE_LSE>, PT_T, 0) != cudaSuccess ||
+            v < 1)
+            v = 4;
+        occ = v;
+    }
+    return occ;
 }
 
 }  // namespace sot

@@ -94,6 +94,7 @@ struct CooArgs {
 // ---- point path (d <= 3), k_point.cu ----
 int point_rows_per_cta();
 int point_cols_per_tile();
+int point_blocks_per_sm();
 cudaError_t launch_point_half(const HalfArgs& p, int mode, cudaStream_t st);
 int point_apply_rows_per_cta();
 cudaError_t launch_point_apply(const ApplyArgs& p, cudaStream_t st);

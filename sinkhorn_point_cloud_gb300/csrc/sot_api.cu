@@ -273,7 +273,8 @@ struct Solver {
         for (int h = 0; h < 2; ++h) {
             const int nr = h ? m : n, nc = h ? n : m;
             if (path == PATH_POINT)
-                choose_split(B, nr, nc, point_rows_per_cta(), point_cols_per_tile(), sms, 4, &split[h], &chunk[h],
+                choose_split(B, nr, nc, point_rows_per_cta(), point_cols_per_tile(), sms, point_blocks_per_sm(),
+                             &split[h], &chunk[h],
                              &rowtiles[h]);
             else if (path == PATH_DENSE)
                 choose_split(B, nr, nc, dense_rows_per_cta(), dense_cols_per_tile(), sms, 2, &split[h], &chunk[h],
@@ -919,7 +920,8 @@ size_t noalloc_required_bytes(int B, int n, int m, int d) {
     int split[2], chunk[2], rowtiles[2];
     const int sms = device_sms();
     for (int h = 0; h < 2; ++h)
-        choose_split(B, h ? m : n, h ? n : m, point_rows_per_cta(), point_cols_per_tile(), sms, 4, &split[h],
+        choose_split(B, h ? m : n, h ? n : m, point_rows_per_cta(), point_cols_per_tile(), sms, point_blocks_per_sm(),
+                     &split[h],
                      &chunk[h], &rowtiles[h]);
     const int smax = split[0] > split[1] ? split[0] : split[1];
     const int rt_max = rowtiles[0] > rowtiles[1] ? rowtiles[0] : rowtiles[1];
