@@ -45,6 +45,7 @@ KERNEL_SOURCES = {
     "tc_screen_kernel": ["k_tc.cu", "tc_ptx.cuh", "common.cuh", "tc.h", "kernels.h"],
     "dense_half_kernel": ["k_dense.cu", "common.cuh", "kernels.h"],
     "point_half_kernel": ["k_point.cu", "common.cuh", "kernels.h"],
+    "point_cluster_kernel": ["k_cluster.cu", "common.cuh", "kernels.h"],
 }
 
 
@@ -267,6 +268,8 @@ def run_gpu(args, ws, rank, local):
     flags = {"auto": sot.SOT_PREC_AUTO, "fp32": sot.SOT_PREC_FP32, "f16x3": sot.SOT_PREC_F16X3}[args.prec]
     if args.no_screen:
         flags |= sot.SOT_TC_NO_SCREEN
+    if args.no_cluster:
+        flags |= sot.SOT_NO_CLUSTER
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -319,8 +322,8 @@ def run_gpu(args, ws, rank, local):
     barrier(ws)
     sot.sot_profile_enable(False)
     kinds = sot.sot_profile_read_kinds()
-    nl = kinds["full"][0] + kinds["screened"][0]
-    half_ms = kinds["full"][1] + kinds["screened"][1]
+    nl = sum(v[0] for v in kinds.values())
+    half_ms = sum(v[1] for v in kinds.values())
     launches = sot.sot_kernel_launches() - launches0
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     t_dev = sum(step_ms) / 1e3
@@ -351,22 +354,23 @@ def run_gpu(args, ws, rank, local):
         return 0
     pk, pk_kind = peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    screened = kinds["screened"][0] > 0
-    # the dominant kernel: the screened half-step when it ran, else the full one
-    nl_dom, ms_dom = kinds["screened"] if screened else kinds["full"]
+    # the dominant kernel: the kind that took the most time (per half-step averages;
+    # a cluster-resident launch counts the half-steps it covers)
+    dom = max(kinds, key=lambda k: kinds[k][1])
+    nl_dom, ms_dom = kinds[dom]
     per_launch_ms = ms_dom / max(nl_dom, 1)
     per_launch_pairs = B * n * m
     mhz = float(pk.get("sm_max_mhz", 2070.0))
     rates = alu_rates()
     secs = per_launch_ms / 1e3
     mufu = None
-    if rates and not screened:  # a screened half-step forms exponentials for the kept pairs only
+    if rates and dom != "screened":  # a screened half-step forms exponentials for the kept pairs only
         mufu_peak = rates["ex2_per_sm_clk"] * sms * mhz * 1e6
         mufu = {"achieved_ex2_per_s": per_launch_pairs / secs, "peak_ex2_per_s": mufu_peak,
                 "frac": per_launch_pairs / secs / mufu_peak}
     path = sot.sot_select_path(d, flags)
     if path == 2:
-        if screened:
+        if dom == "screened":
             flops_pair = 2 * d  # one fp16 product hi*hi per pair, 2 flops per multiply-add
             kname, kern = "tc_screen_kernel", "tc_screen_kernel (tcgen05 kind::f16 hi*hi screen + exact kept pairs)"
         else:
@@ -388,11 +392,16 @@ def run_gpu(args, ws, rank, local):
             src += " x 2"
         else:
             # direct form: one FADD for the bias, d x (FADD + FFMA) for the distance, one FADD into the sum
-            ops_pair, unit, kern = 2 + 2 * d, "Tops/s", \
-                f"point_half_kernel ({2 + 2 * d} FP32 lane-ops + 1 MUFU ex2 per pair)"
+            ops_pair, unit = 2 + 2 * d, "Tops/s"
+            if dom == "cluster":
+                # the cluster-resident kernel evaluates all three coordinates
+                ops_pair = 8
+                kern = "point_cluster_kernel (cluster-resident iterations; 8 FP32 lane-ops + 1 MUFU ex2 per pair)"
+            else:
+                kern = f"point_half_kernel ({2 + 2 * d} FP32 lane-ops + 1 MUFU ex2 per pair)"
             peak = lanes * sms * mhz * 1e6 / 1e12
         achieved = ops_pair * per_launch_pairs / secs / 1e12
-        kname = "dense_half_kernel" if path == 1 else "point_half_kernel"
+        kname = "dense_half_kernel" if path == 1 else ("point_cluster_kernel" if dom == "cluster" else "point_half_kernel")
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": measured_traffic(kname, w["name"]), "peak_source": src, "kernel": kern}
         dtype = "f32"
@@ -414,10 +423,8 @@ def run_gpu(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
         "iters_per_s": ws * sum([info["iters_done"]]) * args.steps / t_max,
-        "half_step": {"launches": nl, "avg_ms": half_ms / max(nl, 1), "pairs_per_launch": per_launch_pairs,
-                      "full": {"launches": kinds["full"][0], "avg_ms": kinds["full"][1] / max(kinds["full"][0], 1)},
-                      "screened": {"launches": kinds["screened"][0],
-                                   "avg_ms": kinds["screened"][1] / max(kinds["screened"][0], 1)}},
+        "half_step": {"count": nl, "avg_ms": half_ms / max(nl, 1), "pairs_per_half_step": per_launch_pairs,
+                      **{k: {"count": v[0], "avg_ms": v[1] / max(v[0], 1)} for k, v in kinds.items()}},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": None if e2e_max is None else {"value": ws * e2e_pairs / e2e_max / 1e9, "unit": UNIT,
@@ -448,6 +455,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--no-screen", action="store_true", help="tensor path: full half-steps only (comparison runs)")
+    ap.add_argument("--no-cluster", action="store_true",
+                    help="point path: streaming half-steps only, no cluster-resident iterations (comparison runs)")
     args = ap.parse_args(argv)
     ws, rank, local = dist_env()
     if args.impl == "reference":

@@ -62,8 +62,11 @@ enum sot_flags {
     SOT_PREC_MASK = 3,
     SOT_WARM_START = 1 << 4,    /* read f, g as the initial potentials instead of f = g = 0 */
     SOT_STAGE_EARLY_EXIT = 1 << 5, /* apply the stop test in every stage, not only at the final eps */
-    SOT_TC_NO_SCREEN = 1 << 6      /* tensor path: evaluate every pair's exponential in every half-step
+    SOT_TC_NO_SCREEN = 1 << 6,     /* tensor path: evaluate every pair's exponential in every half-step
                                       (default: warm half-steps screen pairs with hi*hi products first) */
+    SOT_NO_CLUSTER = 1 << 7        /* point path: stream every half-step (default: when both clouds fit in
+                                      shared memory, the warm iterations of an untested stage run in one
+                                      cluster-resident launch) */
 };
 
 /*
@@ -184,16 +187,19 @@ int sot_check_inputs(const float* X, const float* Y, const float* a, const float
 /*
  * Per-kernel timing with CUDA events recorded on the launching stream around
  * every half-step launch (off by default).  sot_profile_read synchronises the
- * device events, returns the number of half-step launches since the last
- * reset and their summed duration in milliseconds, and resets the counters.
+ * device events, returns the number of half-steps since the last reset (a
+ * cluster-resident launch counts the half-steps it covers) and their summed
+ * duration in milliseconds, and resets the counters.
  */
 int sot_profile_enable(int on);
 int sot_profile_read(long long* launches_host, double* total_ms_host);
 /*
- * The same, split by kind: index 0 counts full half-steps (every pair's
- * exponential formed), index 1 the screened tensor-core half-steps.  Both
- * arrays (host, 2 entries each) may be NULL.  Resets the counters like
- * sot_profile_read.
+ * The same, split by kind: index 0 counts streaming half-steps that form
+ * every pair's exponential, index 1 the screened tensor-core half-steps,
+ * index 2 the half-steps run inside cluster-resident launches (one launch
+ * covers many; its time is counted once).  Counts are half-steps, times are
+ * milliseconds.  Both arrays (host, 3 entries each) may be NULL.  Resets the
+ * counters like sot_profile_read.
  */
 int sot_profile_read_kinds(long long* launches_host, double* ms_host);
 

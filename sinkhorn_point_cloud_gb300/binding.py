@@ -32,6 +32,7 @@ SOT_PREC_F16X3 = 2
 SOT_WARM_START = 1 << 4
 SOT_STAGE_EARLY_EXIT = 1 << 5
 SOT_TC_NO_SCREEN = 1 << 6
+SOT_NO_CLUSTER = 1 << 7
 
 HEADER = os.path.join(_build.ROOT, "include", "sot.h")
 
@@ -302,8 +303,9 @@ def sot_profile_read():
 
 
 def sot_profile_read_kinds():
-    """{"full": (launches, ms), "screened": (launches, ms)} since the last read."""
-    n = (C.c_longlong * 2)()
-    ms = (C.c_double * 2)()
+    """{"full": (half-steps, ms), "screened": (...), "cluster": (...)} since the last read."""
+    n = (C.c_longlong * 3)()
+    ms = (C.c_double * 3)()
     _check(load().sot_profile_read_kinds(n, ms), "sot_profile_read_kinds")
-    return {"full": (int(n[0]), float(ms[0])), "screened": (int(n[1]), float(ms[1]))}
+    return {"full": (int(n[0]), float(ms[0])), "screened": (int(n[1]), float(ms[1])),
+            "cluster": (int(n[2]), float(ms[2]))}

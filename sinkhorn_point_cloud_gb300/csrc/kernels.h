@@ -100,6 +100,14 @@ int point_apply_rows_per_cta();
 cudaError_t launch_point_apply(const ApplyArgs& p, cudaStream_t st);
 cudaError_t launch_point_coo(const CooArgs& p, int write_pass, cudaStream_t st);
 
+// ---- cluster-resident iterations for small point clouds, k_cluster.cu ----
+size_t cluster_smem_bytes(int n, int m);
+bool point_cluster_plan(int B, int n, int m, int sms, int* C, int* T, int* S, size_t* smem);
+// `iters` warm iterations (f-half, then g-half) on the states L, Lam in place;
+// cudaErrorInvalidConfiguration when no cluster of this shape fits the device.
+cudaError_t launch_point_cluster(int B, int n, int m, const float* xpack, const float* ypack, float* L, float* Lam,
+                                 float two_kappa, int iters, int C, int T, int S, size_t smem, cudaStream_t st);
+
 // ---- dense fp32 path (any d <= 256), k_dense.cu ----
 int dense_rows_per_cta();
 int dense_cols_per_tile();

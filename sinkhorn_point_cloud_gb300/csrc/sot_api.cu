@@ -98,7 +98,8 @@ std::mutex g_prof_mu;
 bool g_prof_on = false;
 struct ProfRec {
     cudaEvent_t a, b;
-    int kind;  // 0: full half-step, 1: screened half-step
+    int kind;   // 0: full half-step, 1: screened half-step, 2: cluster-resident iterations
+    int count;  // half-steps the timed launch(es) cover
 };
 std::vector<ProfRec> g_prof_pending;
 std::vector<cudaEvent_t> g_prof_pool;
@@ -118,6 +119,7 @@ struct ProfScope {
     cudaEvent_t a = nullptr, b = nullptr;
     cudaStream_t st;
     int kind = 0;
+    int count = 1;
     ProfScope(cudaStream_t s, bool want) : st(s) {
         if (!want) return;
         std::lock_guard<std::mutex> g(g_prof_mu);
@@ -130,7 +132,7 @@ struct ProfScope {
         if (!a) return;
         cudaEventRecord(b, st);
         std::lock_guard<std::mutex> g(g_prof_mu);
-        g_prof_pending.push_back(ProfRec{a, b, kind});
+        g_prof_pending.push_back(ProfRec{a, b, kind, count});
     }
 };
 
@@ -230,6 +232,11 @@ struct Solver {
     TcScreen scr;
     bool screen_allowed = false;
     bool screen_on = false;
+    // Cluster-resident iterations (point path, clouds that fit in shared memory).
+    bool cluster_allowed = false;
+    bool cluster_ok = false;
+    int cl_C = 0, cl_T = 0, cl_S = 0;
+    size_t cl_smem = 0;
 
     Solver(const float* X_, const float* Y_, const float* a_, const float* b_, int B_, int n_, int m_, int d_, Path p,
            cudaStream_t s)
@@ -283,6 +290,8 @@ struct Solver {
                 choose_split(B, nr, nc, tc_rows_per_cta(), tc_cols_per_tile(), sms, 1, &split[h], &chunk[h],
                              &rowtiles[h]);
         }
+        if (point && cluster_allowed)
+            cluster_ok = point_cluster_plan(B, n, m, sms, &cl_C, &cl_T, &cl_S, &cl_smem);
         const int smax = split[0] > split[1] ? split[0] : split[1];
         const size_t rows_max = (size_t)B * (n > m ? n : m);
         const int rt_max = rowtiles[0] > rowtiles[1] ? rowtiles[0] : rowtiles[1];
@@ -403,6 +412,31 @@ struct Solver {
         return rc;
     }
 
+    // `iters` warm iterations of the current stage in one cluster-resident
+    // launch (after the stage's cold first iteration).  Sets *ran = false, and
+    // changes nothing, when no cluster of the planned shape fits the device.
+    int cluster_iterations(float kappa, long long iters, bool* ran) {
+        *ran = false;
+        if (!cluster_ok || iters < 1 || iters > (1 << 30)) return SOT_OK;
+        cudaError_t e;
+        {
+            ProfScope ps(st, true);
+            ps.kind = 2;
+            ps.count = (int)(2 * iters);
+            e = launch_point_cluster(B, n, m, xpack, ypack, L, Lam, 2.f * kappa, (int)iters, cl_C, cl_T, cl_S,
+                                     cl_smem, st);
+        }
+        if (e == cudaErrorInvalidConfiguration) {
+            (void)cudaGetLastError();
+            cluster_ok = false;
+            return SOT_OK;
+        }
+        if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "cluster launch failed: %s", cudaGetErrorString(e));
+        bound_ok = false;  // the bounds of the streaming half-steps are stale now
+        *ran = true;
+        return SOT_OK;
+    }
+
     // A new eps stage starts: states are rescaled, the last bounds no longer apply.
     void new_stage() {
         bound_ok = false;
@@ -492,7 +526,18 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
         if (!test) {
             long long todo = ips;
             if (total + todo > max_total) todo = max_total - total;
-            for (long long t = 0; t < todo; ++t) {
+            long long t0 = 0;
+            if (sv.cluster_ok && todo >= 3) {
+                // the cold first iteration streams; the rest run cluster-resident
+                rc = sv.iterate(kappa, cold, false);
+                if (rc) return rc;
+                cold = false;
+                bool ran = false;
+                rc = sv.cluster_iterations(kappa, todo - 1, &ran);
+                if (rc) return rc;
+                t0 = ran ? todo : 1;
+            }
+            for (long long t = t0; t < todo; ++t) {
                 rc = sv.iterate(kappa, cold, false);
                 if (rc) return rc;
                 cold = false;
@@ -627,7 +672,7 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     if (!s) return fail(SOT_ERR_INVALID_ARG, "schedule must not be NULL");
     if (!(s->eps > 0.f) || !std::isfinite(s->eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (s->iters_per_stage < 0) return fail(SOT_ERR_INVALID_ARG, "iters_per_stage must be >= 0");
-    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT | SOT_TC_NO_SCREEN))
+    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT | SOT_TC_NO_SCREEN | SOT_NO_CLUSTER))
         return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
     if (B > 0 && (!f || !g)) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
     if (st && st->stage_iters_host && st->stage_iters_cap < 0) return fail(SOT_ERR_INVALID_ARG, "stage_iters_cap < 0");
@@ -640,6 +685,7 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     if (rc) return rc;
     Solver sv(X, Y, a, b, B, n, m, d, path, (cudaStream_t)stream);
     sv.screen_allowed = (path == PATH_TC) && !(s->flags & SOT_TC_NO_SCREEN);
+    sv.cluster_allowed = (path == PATH_POINT) && !(s->flags & SOT_NO_CLUSTER);
     rc = run_schedule(sv, *s, f, g, f, g, st);
     if (rc) return rc;
     cudaError_t e = cudaGetLastError();
@@ -840,14 +886,14 @@ int sot_profile_read_kinds(long long* launches_host, double* ms_host) {
         std::lock_guard<std::mutex> g(g_prof_mu);
         pend.swap(g_prof_pending);
     }
-    long long cnt[2] = {0, 0};
-    double ms[2] = {0.0, 0.0};
+    long long cnt[3] = {0, 0, 0};
+    double ms[3] = {0.0, 0.0, 0.0};
     int rc = SOT_OK;
     for (auto& pr : pend) {
         float t = 0.f;
         if (rc == SOT_OK && cudaEventSynchronize(pr.b) != cudaSuccess) rc = fail(SOT_ERR_CUDA, "event synchronisation failed");
         if (rc == SOT_OK && cudaEventElapsedTime(&t, pr.a, pr.b) != cudaSuccess) rc = fail(SOT_ERR_CUDA, "event timing failed");
-        cnt[pr.kind] += 1;
+        cnt[pr.kind] += pr.count;
         ms[pr.kind] += t;
     }
     {
@@ -858,7 +904,7 @@ int sot_profile_read_kinds(long long* launches_host, double* ms_host) {
         }
     }
     if (rc) return rc;
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 3; ++k) {
         if (launches_host) launches_host[k] = cnt[k];
         if (ms_host) ms_host[k] = ms[k];
     }
@@ -866,12 +912,12 @@ int sot_profile_read_kinds(long long* launches_host, double* ms_host) {
 }
 
 int sot_profile_read(long long* launches_host, double* total_ms_host) {
-    long long c[2];
-    double t[2];
+    long long c[3];
+    double t[3];
     const int rc = sot_profile_read_kinds(c, t);
     if (rc) return rc;
-    if (launches_host) *launches_host = c[0] + c[1];
-    if (total_ms_host) *total_ms_host = t[0] + t[1];
+    if (launches_host) *launches_host = c[0] + c[1] + c[2];
+    if (total_ms_host) *total_ms_host = t[0] + t[1] + t[2];
     return SOT_OK;
 }
 
