@@ -263,12 +263,22 @@ __global__ void coo_validate_kernel(const int* rows, const int* cols, const long
     }
 }
 
-__device__ __forceinline__ long long lower_bound_rows(const int* rows, long long lo, long long hi, int key) {
-    while (lo < hi) {
-        const long long mid = lo + ((hi - lo) >> 1);
-        if (rows[mid] < key) lo = mid + 1; else hi = mid;
+// First e in [lo, hi) with rows[e] >= key (hi if none), rows sorted ascending;
+// the whole warp searches together: 32 probes per round cut the range ~33-fold,
+// so a round trip to memory is paid log_33 of the range times, not log_2.
+__device__ __forceinline__ long long warp_lower_bound_rows(const int* rows, long long lo, long long hi, int key) {
+    const int lane = threadIdx.x & 31;
+    while (hi - lo > 32) {  // invariant: the answer lies in [lo, hi]
+        const long long step = (hi - lo + 32) / 33;
+        const long long pos = lo + step * (lane + 1) - 1;
+        const int c = __popc(__ballot_sync(0xffffffffu, pos < hi && rows[pos] < key));
+        const long long nlo = lo + step * c;
+        const long long nhi = (c == 32) ? hi : lo + step * (c + 1) - 1;
+        lo = nlo;
+        hi = nhi < hi ? nhi : hi;
     }
-    return lo;
+    const long long pos = lo + lane;
+    return lo + __popc(__ballot_sync(0xffffffffu, pos < hi && rows[pos] < key));
 }
 
 __global__ void grad_coo_kernel(const float* X, const float* Y, int n, int m, int d, const int* rows,
@@ -279,8 +289,8 @@ __global__ void grad_coo_kernel(const float* X, const float* Y, int n, int m, in
     const int i = blockIdx.x * (blockDim.x >> 5) + warp;
     if (i >= n) return;
     const long long lo = off[b], hi = off[b + 1];
-    const long long s0 = lower_bound_rows(rows, lo, hi, i);
-    const long long s1 = lower_bound_rows(rows, s0, hi, i + 1);
+    const long long s0 = warp_lower_bound_rows(rows, lo, hi, i);
+    const long long s1 = warp_lower_bound_rows(rows, s0, hi, i + 1);
     const float* xi = X + ((size_t)b * n + i) * d;
     const float* yb = Y + (size_t)b * m * d;
     float* gi = grad + ((size_t)b * n + i) * d;
@@ -318,7 +328,7 @@ __global__ void grad_coo_kernel(const float* X, const float* Y, int n, int m, in
 cudaError_t launch_grad_coo(const float* X, const float* Y, int B, int n, int m, int d, const int* rows,
                             const int* cols, const float* vals, const long long* batch_offsets, float* grad,
                             int* status, cudaStream_t st) {
-    count_launches(1); coo_validate_kernel<<<dim3(64, B), 256, 0, st>>>(rows, cols, batch_offsets, n, m, status);
+    count_launches(1); coo_validate_kernel<<<dim3(4 * 152 / (B > 0 ? B : 1) + 1, B), 256, 0, st>>>(rows, cols, batch_offsets, n, m, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1); grad_coo_kernel<<<dim3((n + 7) / 8, B), 256, 0, st>>>(X, Y, n, m, d, rows, cols, vals, batch_offsets, grad,
