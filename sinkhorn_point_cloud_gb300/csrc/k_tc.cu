@@ -9,7 +9,7 @@
 // an fp16 pair v = hi + lo and summing hi*hi + hi*lo + lo*hi (the lo*lo term
 // is below fp32 rounding), all accumulated in fp32 in TMEM.
 //
-// CTA layout (one CTA per SM; 320 threads):
+// Full half-step (tc_half_kernel), CTA layout (one CTA per SM; 320 threads):
 //   warp 0      producer: bulk copies (TMA engine) of 128-column operand tiles
 //               into a 4-stage shared-memory ring, plus the column biases
 //               c_j = log2 w_j - Lam_j of each tile;
@@ -19,7 +19,8 @@
 // The 256 rows of the CTA stay resident (row-stationary); every column tile
 // is used by both row tiles (12 MMAs of 128 x 128 x 16 each) before its stage
 // is released.  Accumulators are double-buffered per row tile so the MMAs of
-// tile t+1 overlap the exponentials of tile t.
+// tile t+1 overlap the exponentials of tile t.  The screened half-step
+// (tc_screen_kernel, below) keeps the roles with its own tile shapes.
 //
 // Operands live in HBM as images of the exact shared-memory layout (128-byte
 // swizzle, K-major): per 128 points, 16 KB of hi parts then 16 KB of lo parts,
@@ -722,27 +723,31 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 
 // ---- the screened half-step -----------------------------------------------------------
 // At the scales the half-step is used on, a row's log-sum-exp is carried by a
-// handful of columns: every other term lies more than 2^-40 below the row's
-// sum.  The screened half-step finds those columns with the hi * hi products
-// alone (one third of the tensor work of the full half-step) and evaluates
-// only them exactly:
-//   t~_ij = tk acc_ij + c_j  with acc the fp32 accumulation of hi * hi;
+// handful of columns: every other term lies many binary orders below the
+// row's sum.  The screened half-step scores every pair with the hi * hi
+// products alone (one third of the product work of the full half-step) and
+// evaluates exactly only the pairs that can matter:
+//   t~_ij = tk acc_ij  with acc the fp32 accumulation of hi * hi plus the
+//   column bias c_j / tk (added by a fifth MMA step, see the bias image);
 //   |t~_ij - t_ij| <= Mg, from the norms of the hi parts and the residuals
-//   (Cauchy-Schwarz on x.y - hx.hy = rx.hy + hx.ry + rx.ry, plus fp32
-//   accumulation), where t_ij is the exact score.
+//   (Cauchy-Schwarz on x.y - hx.hy = rx.hy + hx.ry + rx.ry) and fp32
+//   accumulation terms, where t_ij is the exact score.
 // A lower bound of the row's new value is Lb = max(L_old + lo, runmax - Mg):
 // lo is the largest drop of any column bias since the row's last half-step
 // (gathered by the other side), runmax the largest screened score seen so far.
-// A pair is kept when t~_ij >= Lb - theta - Mg; every pair dropped has
+// A pair is kept when t~_ij > Lb - theta - Mg; every pair dropped has
 // t_ij < L_new - theta, so the dropped mass is below nc * 2^-theta of the sum,
 // with theta = 26 + log2(nc): 2^-26 relative.
-// Kept pairs go to the CTA's pool (a shared-memory slot counter).  The CTA
-// that finishes the row block evaluates the pools of all its column chunks
-// flattened over its threads (exact scores: compensated fp32 dot products,
-// fp64 combination), takes per-row maxima with shared-memory atomics and the
-// per-row sums in 2^-48 fixed point (integer adds: the result does not depend
-// on the order).  A row with a pair that did not fit in a pool takes the
-// exact full-row LSE.
+// Tiles are 256 columns wide (128 x 256 x 16 MMAs); each of the two row tiles
+// has one 256-column accumulator, read by all eight epilogue warps (half the
+// columns each) and freed as soon as they hold it in registers.  Kept pairs
+// go to the epilogue warp's own segment of the CTA's pool, slots numbered by
+// ballot.  The CTA that finishes the row block evaluates the pools of all its
+// column chunks flattened over its threads (exact scores: compensated fp32
+// dot products, float-float combination), takes per-row maxima with
+// shared-memory atomics and the per-row sums in 2^-48 fixed point (integer
+// adds: the result does not depend on the order).  A row with a pair that did
+// not fit in its segment takes the exact full-row LSE.
 constexpr int TC_POOL = 4096;  // kept pairs per CTA
 constexpr int SC_SEGS = 8;     // pool segments per CTA, one per epilogue warp
 constexpr int SC_SEG = TC_POOL / SC_SEGS;
