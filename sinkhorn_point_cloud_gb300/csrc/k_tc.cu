@@ -894,10 +894,16 @@ __device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt
         unsigned pm = 0u;  // this lane's kept columns of the chunk
         if (hq[q]) {
             // bit j = sign of Ta - v_j: set exactly when v_j > Ta (a -inf or NaN
-            // score gives +inf or a positive NaN: never set)
+            // score gives +inf or a positive NaN: never set); four independent
+            // 8-bit chains
 #pragma unroll
-            for (int j = 31; j >= 0; --j)
-                pm = __funnelshift_l(__float_as_uint(__fsub_rn(Ta, __uint_as_float(r[q][j]))), pm, 1);
+            for (int g = 0; g < 4; ++g) {
+                unsigned mg = 0u;
+#pragma unroll
+                for (int j = 7; j >= 0; --j)
+                    mg = __funnelshift_l(__float_as_uint(__fsub_rn(Ta, __uint_as_float(r[q][8 * g + j]))), mg, 1);
+                pm |= mg << (8 * g);
+            }
         }
         // Slots of the warp's segment, one pair per lane and round, numbered by
         // lane order (ballot + popc): dense, so every slot below the capacity that
@@ -1093,17 +1099,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
             s_sum[r] = 0ull;
             s_lost[r] = lost;
         }
-        if (threadIdx.x == 0) {
-            int acc = 0;
-            for (int g = 0; g < p.split * SC_SEGS; ++g) {
-                s_off[g] = acc;
-                acc += __ldcg(sk.pool_cnt + cta0 * SC_SEGS + g);
-            }
-            s_off[p.split * SC_SEGS] = acc;
-        }
+        // the block's pool segments (every chunk's): sizes ...
+        for (int g = threadIdx.x; g < p.split * SC_SEGS; g += TC_THREADS)
+            s_off[g + 1] = __ldcg(sk.pool_cnt + cta0 * SC_SEGS + g);
     }
     __syncthreads();
     const int nseg = p.split * SC_SEGS;
+    if (warp == 0) {  // ... and their prefix sums (segment g holds entries s_off[g] .. s_off[g + 1])
+        int carry = 0;
+        for (int g0 = 0; g0 < nseg; g0 += 32) {
+            int v = (g0 + lane < nseg) ? s_off[g0 + lane + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            if (g0 + lane < nseg) s_off[g0 + lane + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) s_off[0] = 0;
+    }
+    __syncthreads();
     const int total = s_off[nseg];
     const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
     // pass 1: exact score of every kept pair, relative to the row's reference;
