@@ -32,7 +32,11 @@
  *     eps (or at every stage with early exit);
  *   - marginal error = sum_i | sum_j P_ij - a_i |;
  *   - COO support = { P_ij >= tau * max_j' P_ij' } U { P_ij >= tau * max_i' P_i'j },
- *     row-major order.
+ *     row-major order;
+ *   - cosine cost ("FlashSinkhorn", Conclusies: the structure also holds for
+ *     the cosine distance after normalisation): C_ij = 2 - 2 x_i.y_j / (|x_i| |y_j|)
+ *     for nonzero points.  A zero point has no direction: it normalises to the
+ *     zero vector, so C_ij = [x_i != 0] + [y_j != 0] - 2 xhat_i.yhat_j in general.
  *
  * Parity pins (tests, CPU only): closed forms at n = m = 1 and for 2 x 2
  * problems, the attention-form identity, marginals and duality at
@@ -41,7 +45,7 @@
  * invariances, shift invariance, finite differences of the dual objective.
  *
  * Compile: cc -O2 -fopenmp -fPIC -shared oracle.c -lm  (no fast-math).
- * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..8) that
+ * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..9) that
  * the test suite uses to show that the pins catch plausible mistakes.
  */
 #include <math.h>
@@ -73,8 +77,36 @@ void orc_set_num_threads(int t) {
 #endif
 }
 
-/* Squared Euclidean distance, direct form. */
+/* Cost selected for every call that follows: 0 squared Euclidean, 1 cosine. */
+static int g_cost = 0;
+void orc_set_cost(int kind) { g_cost = (kind == 1) ? 1 : 0; }
+int orc_get_cost(void) { return g_cost; }
+
+static double norm2(const double *v, int d) {
+    double s = 0.0;
+    for (int k = 0; k < d; ++k) s += v[k] * v[k];
+    return sqrt(s);
+}
+
+/* Cosine cost 2 - 2 cos(x, y) (zero points: see the header). */
+static double cosine_ij(const double *x, const double *y, int d) {
+    const double nx = norm2(x, d), ny = norm2(y, d);
+    double dot = 0.0;
+    for (int k = 0; k < d; ++k) dot += x[k] * y[k];
+    double cs = 0.0;
+    if (nx > 0.0 && ny > 0.0) {
+#if ORC_MUTANT == 9
+        cs = dot / nx; /* mutant: y not normalised */
+#else
+        cs = dot / (nx * ny);
+#endif
+    }
+    return (nx > 0.0 ? 1.0 : 0.0) + (ny > 0.0 ? 1.0 : 0.0) - 2.0 * cs;
+}
+
+/* Squared Euclidean distance, direct form (or the cosine cost when selected). */
 static double cost_ij(const double *x, const double *y, int d) {
+    if (g_cost == 1) return cosine_ij(x, y, d);
     double c = 0.0;
 #if ORC_MUTANT == 8
     d = d > 1 ? d - 1 : d; /* mutant: drops the last coordinate */
@@ -325,6 +357,8 @@ int orc_sinkhorn_anneal(int n, int m, int d, const double *X, const double *Y,
  *   P_ij = exp((f_i + g_j - C_ij)/eps + log a_i + log b_j)
  *   cost  = sum_ij P_ij C_ij
  *   grad  = 2 (a_i x_i - sum_j P_ij y_j)        [n x d]
+ *           (cosine cost: sum_j P_ij dC_ij/dx_i with
+ *            dC_ij/dx_i = -2 (yhat_j - (xhat_i.yhat_j) xhat_i) / |x_i|, 0 for a zero x_i)
  *   rowsum[i] = sum_j P_ij, colsum[j] = sum_i P_ij   (optional, may be NULL)
  */
 int orc_plan_apply(int n, int m, int d, const double *X, const double *Y,
@@ -340,6 +374,7 @@ int orc_plan_apply(int n, int m, int d, const double *X, const double *Y,
         double *gi = grad ? grad + (size_t)i * d : NULL;
         if (gi)
             for (int k = 0; k < d; ++k) gi[k] = 0.0;
+        const double nxi = norm2(xi, d);
         for (int j = 0; j < m; ++j) {
             const double *yj = Y + (size_t)j * d;
             double c = cost_ij(xi, yj, d);
@@ -350,10 +385,18 @@ int orc_plan_apply(int n, int m, int d, const double *X, const double *Y,
 #endif
             r += p;
             q += p * c;
-            if (gi)
+            if (gi && g_cost == 1) {
+                const double nyj = norm2(yj, d);
+                if (nxi > 0.0 && nyj > 0.0) {
+                    double cs = 0.0;
+                    for (int k = 0; k < d; ++k) cs += (xi[k] / nxi) * (yj[k] / nyj);
+                    for (int k = 0; k < d; ++k) gi[k] += p * (-2.0) * (yj[k] / nyj - cs * xi[k] / nxi) / nxi;
+                }
+            } else if (gi) {
                 for (int k = 0; k < d; ++k) gi[k] += p * yj[k];
+            }
         }
-        if (gi)
+        if (gi && g_cost != 1)
             for (int k = 0; k < d; ++k)
 #if ORC_MUTANT == 4
                 gi[k] = 2.0 * (xi[k] - gi[k]); /* mutant: drops a_i */
@@ -517,6 +560,7 @@ long long orc_coo(int n, int m, int d, const double *X, const double *Y,
 int orc_grad_support(int n, int m, int d, const double *X, const double *Y,
                      long long nnz, const int *rows, const int *cols,
                      const double *vals, double *grad) {
+    if (g_cost != 0) return -1; /* squared-Euclidean support gradient only */
     for (long long k = 0; k < (long long)n * d; ++k) grad[k] = 0.0;
     for (long long e = 0; e < nnz; ++e) {
         int i = rows[e], j = cols[e];

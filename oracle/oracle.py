@@ -10,6 +10,7 @@ helpers loop over the leading batch axis.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 import subprocess
@@ -79,6 +80,8 @@ class Oracle:
         L.orc_num_threads.restype = C.c_int
         L.orc_set_num_threads.argtypes = [C.c_int]
         L.orc_mutant.restype = C.c_int
+        L.orc_set_cost.argtypes = [C.c_int]
+        L.orc_get_cost.restype = C.c_int
 
     # ---- plumbing -----------------------------------------------------
     @staticmethod
@@ -107,6 +110,25 @@ class Oracle:
     @property
     def mutant(self) -> int:
         return int(self.lib.orc_mutant())
+
+    # ---- cost selection -------------------------------------------------
+    COSTS = {"sqeuclidean": 0, "cosine": 1}
+
+    @property
+    def cost_kind(self) -> str:
+        k = int(self.lib.orc_get_cost())
+        return [name for name, v in self.COSTS.items() if v == k][0]
+
+    @contextlib.contextmanager
+    def cost(self, kind: str):
+        """Select the cost for the calls inside the block ("sqeuclidean" or
+        "cosine"); the previous selection is restored on exit."""
+        prev = int(self.lib.orc_get_cost())
+        self.lib.orc_set_cost(self.COSTS[kind])
+        try:
+            yield self
+        finally:
+            self.lib.orc_set_cost(prev)
 
     # ---- half steps ---------------------------------------------------
     def f_half(self, X, Y, b, g, eps):

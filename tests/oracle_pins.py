@@ -330,6 +330,101 @@ def pin_anneal_schedule(orc):
     assert out["iters_done"] == int(np.sum(out["stage_iters"]))
 
 
+
+# ---- cosine cost ("FlashSinkhorn", Conclusies: the cost structure also holds
+# for the cosine distance after normalisation) ----------------------------------
+
+def pin_cosine_closed_form(orc):
+    """n = m = 1, a = b = 1 under the cosine cost: f = C = 2 - 2 cos(x, y),
+    g = 0, cost = C and grad = -2 (yhat - (xhat.yhat) xhat) / |x|.  The values
+    are worked by hand; the last case is the zero-point convention (a zero
+    point normalises to 0: C = 1 against a nonzero point, gradient 0)."""
+    r2 = np.sqrt(2.0)
+    cases = [
+        ([1.0, 0.0, 0.0], [0.0, 2.0, 0.0], 2.0, [0.0, -2.0, 0.0]),
+        ([1.0, 1.0, 0.0], [3.0, 0.0, 0.0], 2.0 - r2, [-1.0 / r2, 1.0 / r2, 0.0]),
+        ([0.0, 0.0, -2.0], [0.0, 0.0, 5.0], 4.0, [0.0, 0.0, 0.0]),
+        ([0.0, 0.0, 0.0], [1.0, 2.0, 2.0], 1.0, [0.0, 0.0, 0.0]),
+    ]
+    with orc.cost("cosine"):
+        for x, y, c, gr in cases:
+            X, Y = np.array([x]), np.array([y])
+            for eps, it in ((0.05, 1), (0.5, 3)):
+                f, g = orc.sinkhorn(X, Y, [1.0], [1.0], [eps], [it])
+                _close(f, [c], 1e-12, atol=1e-12, what="cosine f at n=1")
+                _close(g, [0.0], 0, atol=1e-12, what="cosine g at n=1")
+                out = orc.plan_apply(X, Y, [1.0], [1.0], f, g, eps)
+                _close(out["cost"], c, 1e-12, atol=1e-12, what="cosine cost at n=1")
+                _close(out["grad"], [gr], 1e-12, atol=1e-12, what="cosine grad at n=1")
+
+
+def _unit(P):
+    return P / np.linalg.norm(P, axis=1, keepdims=True)
+
+
+def pin_cosine_unit_points(orc):
+    """On unit points |x - y|^2 = 2 - 2 x.y: the cosine oracle gives the
+    squared-Euclidean oracle's potentials and cost, and its gradient is the
+    squared-Euclidean gradient projected off x_i, (I - x_i x_i^T) grad_i."""
+    X, Y, a, b = _problem(11, 13, 17, 4)
+    X, Y = _unit(X), _unit(Y)
+    eps, it = 0.2, 40
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [it])
+    ref = orc.plan_apply(X, Y, a, b, f, g, eps)
+    with orc.cost("cosine"):
+        fc, gc = orc.sinkhorn(X, Y, a, b, [eps], [it])
+        out = orc.plan_apply(X, Y, a, b, fc, gc, eps)
+    _close(fc, f, 1e-12, atol=1e-12, what="unit points f")
+    _close(gc, g, 1e-12, atol=1e-12, what="unit points g")
+    _close(out["cost"], ref["cost"], 1e-12, what="unit points cost")
+    proj = ref["grad"] - np.sum(ref["grad"] * X, axis=1, keepdims=True) * X
+    _close(out["grad"], proj, 1e-11, atol=1e-12, what="unit points grad")
+
+
+def pin_cosine_scale_invariance(orc):
+    """The cosine cost sees directions only: positive per-point scales on X and
+    Y leave f, g and the cost unchanged and divide gradient row i by the scale
+    of x_i; every gradient row is orthogonal to its point."""
+    X, Y, a, b = _problem(12, 11, 9, 3)
+    eps, it = 0.1, 30
+    rng = _rng(13)
+    cx = rng.uniform(0.2, 5.0, size=(X.shape[0], 1))
+    cy = rng.uniform(0.2, 5.0, size=(Y.shape[0], 1))
+    with orc.cost("cosine"):
+        f, g = orc.sinkhorn(X, Y, a, b, [eps], [it])
+        out = orc.plan_apply(X, Y, a, b, f, g, eps)
+        f2, g2 = orc.sinkhorn(cx * X, cy * Y, a, b, [eps], [it])
+        out2 = orc.plan_apply(cx * X, cy * Y, a, b, f2, g2, eps)
+    _close(f2, f, 1e-11, atol=1e-12, what="scaled f")
+    _close(g2, g, 1e-11, atol=1e-12, what="scaled g")
+    _close(out2["cost"], out["cost"], 1e-11, what="scaled cost")
+    _close(out2["grad"], out["grad"] / cx, 1e-10, atol=1e-13, what="scaled grad")
+    gmax = np.max(np.abs(out["grad"])) * np.max(np.abs(X))
+    _close(np.sum(out["grad"] * X, axis=1), np.zeros(X.shape[0]), 0, atol=1e-12 * gmax, what="grad . x")
+
+
+def pin_cosine_dual_finite_differences(orc):
+    """Envelope theorem under the cosine cost: at convergence the gradient
+    equals finite differences of <a,f> + <b,g> with respect to X."""
+    X, Y, a, b = _problem(14, 6, 5, 3, scale=0.8)
+    eps = 0.2
+    with orc.cost("cosine"):
+        def obj(Xp):
+            f, g = orc.sinkhorn(Xp, Y, a, b, [eps], [3000])
+            return a @ f + b @ g
+
+        f, g = orc.sinkhorn(X, Y, a, b, [eps], [3000])
+        grad = orc.plan_apply(X, Y, a, b, f, g, eps)["grad"]
+        h = 1e-5
+        fd = np.zeros_like(X)
+        for i in range(X.shape[0]):
+            for k in range(X.shape[1]):
+                Xp, Xm = X.copy(), X.copy()
+                Xp[i, k] += h
+                Xm[i, k] -= h
+                fd[i, k] = (obj(Xp) - obj(Xm)) / (2 * h)
+    _close(grad, fd, 1e-6, atol=1e-9, what="cosine finite differences of the dual")
+
 ALL_PINS = [
     pin_closed_form_single_point,
     pin_two_point_closed_form,
@@ -343,4 +438,8 @@ ALL_PINS = [
     pin_marginal_error_shortcut,
     pin_coo_limits,
     pin_anneal_schedule,
+    pin_cosine_closed_form,
+    pin_cosine_unit_points,
+    pin_cosine_scale_invariance,
+    pin_cosine_dual_finite_differences,
 ]
