@@ -190,12 +190,17 @@ def barrier(ws: int):
 
 
 # ---- reference arm: the fp64 oracle on host cores -------------------------------
-def oracle_rate(target_s: float, X, Y, b, eps):
+def oracle_rate(target_s: float, X, Y, b, eps, cost="sqeuclidean"):
     """Time the oracle's f-half on a sample of rows (all m columns) for about
     target_s seconds; when every row fits in less time, whole f-halves are
     repeated.  Returns (pair-evals/s, sample description, seconds, threads)."""
     from oracle import oracle as O
     orc = O.get()
+    with orc.cost(cost):
+        return _oracle_rate(orc, target_s, X, Y, b, eps)
+
+
+def _oracle_rate(orc, target_s, X, Y, b, eps):
     m = Y.shape[0]
     g = np.zeros(m)
     rows = min(X.shape[0], 2 * orc.num_threads)
@@ -223,17 +228,17 @@ def run_reference(args, ws, rank):
     X, Y, a, b = datagen.make_batch(args.workload, B=1)
     rates = []
     for _ in range(args.warmup):
-        oracle_rate(0.5, X[0], Y[0], b[0], w["eps"])
+        oracle_rate(0.5, X[0], Y[0], b[0], w["eps"], args.cost)
     sample = None
     for _ in range(args.steps):
-        r, sample, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], w["eps"])
+        r, sample, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], w["eps"], args.cost)
         rates.append(r)
     value = float(np.median(rates)) / 1e9
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w["name"], "B": w["B"], "n": w["n"], "m": w["m"], "d": w["d"], "eps": w["eps"],
-                       "iters": w.get("iters")},
+                       "iters": w.get("iters"), **({"cost": "cosine"} if args.cost == "cosine" else {})},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -270,6 +275,8 @@ def run_gpu(args, ws, rank, local):
         flags |= sot.SOT_TC_NO_SCREEN
     if args.no_cluster:
         flags |= sot.SOT_NO_CLUSTER
+    if args.cost == "cosine":
+        flags |= sot.SOT_COST_COSINE
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -288,7 +295,7 @@ def run_gpu(args, ws, rank, local):
             gs = sot.sot_grad_x_coo(Xs, Ys, coo["rows"], coo["cols"], coo["vals"], coo["batch_offsets"])
             info["nnz"] = coo["nnz"]
             return [coo["rows"], coo["cols"], coo["vals"], gs], info
-        cost, grad, _ = sot.sot_plan_apply(Xs, Ys, As, Bs, f, g, eps, flags=flags & 3)
+        cost, grad, _ = sot.sot_plan_apply(Xs, Ys, As, Bs, f, g, eps, flags=flags & (3 | sot.SOT_COST_COSINE))
         return [cost, grad], info
 
     def step_pairs(info):
@@ -410,7 +417,7 @@ def run_gpu(args, ws, rank, local):
     # CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if not args.no_cpu_baseline:
-        r, sample, t, thr = oracle_rate(args.cpu_baseline_s, X[0], Y[0], b[0], eps)
+        r, sample, t, thr = oracle_rate(args.cpu_baseline_s, X[0], Y[0], b[0], eps, args.cost)
         cpu = {"value": r / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample}
     value = ws * pairs_total / t_max / 1e9
     line = {
@@ -420,6 +427,7 @@ def run_gpu(args, ws, rank, local):
         "config": {"workload": w["name"], "B": B, "n": n, "m": m, "d": d, "eps": eps,
                    "iters": info["iters_done"], **({"stages": info["stages_done"]} if wid == 3 else {}),
                    **({"nnz": info.get("nnz")} if wid == 5 else {}),
+                   **({"cost": "cosine"} if args.cost == "cosine" else {}),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
         "iters_per_s": ws * sum([info["iters_done"]]) * args.steps / t_max,
@@ -457,7 +465,11 @@ def main(argv=None):
     ap.add_argument("--no-screen", action="store_true", help="tensor path: full half-steps only (comparison runs)")
     ap.add_argument("--no-cluster", action="store_true",
                     help="point path: streaming half-steps only, no cluster-resident iterations (comparison runs)")
+    ap.add_argument("--cost", choices=["sqeuclidean", "cosine"], default="sqeuclidean",
+                    help="cost function (cosine: 2 - 2 cos, on the normalised points)")
     args = ap.parse_args(argv)
+    if args.cost == "cosine" and args.workload == 5:
+        ap.error("the COO workload runs with the squared-Euclidean cost only")
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)

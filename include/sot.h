@@ -64,9 +64,16 @@ enum sot_flags {
     SOT_STAGE_EARLY_EXIT = 1 << 5, /* apply the stop test in every stage, not only at the final eps */
     SOT_TC_NO_SCREEN = 1 << 6,     /* tensor path: evaluate every pair's exponential in every half-step
                                       (default: warm half-steps screen pairs with hi*hi products first) */
-    SOT_NO_CLUSTER = 1 << 7        /* point path: stream every half-step (default: when both clouds fit in
+    SOT_NO_CLUSTER = 1 << 7,       /* point path: stream every half-step (default: when both clouds fit in
                                       shared memory, the warm iterations of an untested stage run in one
                                       cluster-resident launch) */
+    SOT_COST_COSINE = 1 << 8       /* cosine cost C_ij = 2 - 2 x_i.y_j / (|x_i| |y_j|) ("FlashSinkhorn",
+                                      Conclusies: the cost structure holds for the cosine distance after
+                                      normalisation).  Every step runs on the unit points x/|x|, y/|y|, where
+                                      |xhat - yhat|^2 equals that cost; a zero point stays the zero vector (its
+                                      cost to a unit point is 1, gradient 0).  Plan application carries the
+                                      gradient back through x/|x|.  Accepted by sot_potentials_ex and
+                                      sot_plan_apply; the potentials and plan are those of the cosine cost. */
 };
 
 /*

@@ -33,6 +33,7 @@ SOT_WARM_START = 1 << 4
 SOT_STAGE_EARLY_EXIT = 1 << 5
 SOT_TC_NO_SCREEN = 1 << 6
 SOT_NO_CLUSTER = 1 << 7
+SOT_COST_COSINE = 1 << 8
 
 HEADER = os.path.join(_build.ROOT, "include", "sot.h")
 

@@ -80,6 +80,54 @@ cudaError_t launch_pack(const float* P, const float* w, int B, int n, int d, con
     return cudaGetLastError();
 }
 
+// ---- cosine cost -------------------------------------------------------------
+// Unit directions: out[i] = P[i] / |P[i]| (a zero point stays zero).
+__global__ void normalise_kernel(const float* P, long long count, int d, float* out) {
+    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    const float* s = P + i * d;
+    float* o = out + i * d;
+    float n2 = 0.f;
+    for (int k = 0; k < d; ++k) n2 = fmaf(s[k], s[k], n2);
+    const float nrm = sqrtf(n2);
+    const float inv = nrm > 0.f ? 1.f / nrm : 0.f;
+    for (int k = 0; k < d; ++k) o[k] = s[k] * inv;
+}
+
+cudaError_t launch_normalise(const float* P, long long count, int d, float* out, cudaStream_t st) {
+    if (count <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((count + 255) / 256);
+    count_launches(1); normalise_kernel<<<blocks, 256, 0, st>>>(P, count, d, out);
+    return cudaGetLastError();
+}
+
+// grad_i <- (I - xhat_i xhat_i^T) grad_i / |x_i| (0 for a zero point): the
+// gradient at the unit point xhat_i = x_i / |x_i| carried back to x_i.
+__global__ void cosine_grad_kernel(const float* X, long long count, int d, float* grad) {
+    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    const float* x = X + i * d;
+    float* gr = grad + i * d;
+    float n2 = 0.f, dot = 0.f;
+    for (int k = 0; k < d; ++k) {
+        n2 = fmaf(x[k], x[k], n2);
+        dot = fmaf(x[k], gr[k], dot);
+    }
+    if (!(n2 > 0.f)) {
+        for (int k = 0; k < d; ++k) gr[k] = 0.f;
+        return;
+    }
+    const float inv = 1.f / sqrtf(n2), c = dot / n2;
+    for (int k = 0; k < d; ++k) gr[k] = (gr[k] - c * x[k]) * inv;
+}
+
+cudaError_t launch_cosine_grad(const float* X, long long count, int d, float* grad, cudaStream_t st) {
+    if (count <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((count + 255) / 256);
+    count_launches(1); cosine_grad_kernel<<<blocks, 256, 0, st>>>(X, count, d, grad);
+    return cudaGetLastError();
+}
+
 // ---- state <-> potential ----------------------------------------------------
 // L = kappa (nrm - f);  f = nrm - L / kappa.
 __global__ void state_from_pot_kernel(const float* nrm, const float* pot, float kappa, int count, float* state) {

@@ -357,6 +357,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
         S.misc()[1] = 0;
         S.misc()[2] = 0;
         S.misc()[4] = 0;
+        S.misc()[5] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -539,6 +540,8 @@ __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, 
 // ---- the half-step ------------------------------------------------------------------
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOps ops) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
+    // (after a screened half-step on probation: only the row blocks it left)
+    if (p.redo && !p.redo[(size_t)blockIdx.y * p.rowtiles + blockIdx.x / p.split]) return;
     extern __shared__ unsigned char smem_raw[];
     const TcSmem S = tc_smem(smem_raw);
     int* misc = S.misc();
@@ -748,6 +751,7 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 // shared-memory atomics and the per-row sums in 2^-48 fixed point (integer
 // adds: the result does not depend on the order).  A row with a pair that did
 // not fit in its segment takes the exact full-row LSE.
+constexpr int SC_RETRY_INLINE = 8;  // lost rows a row block retries itself when on probation
 constexpr int TC_POOL = 4096;  // kept pairs per CTA
 constexpr int SC_SEGS = 8;     // pool segments per CTA, one per epilogue warp
 constexpr int SC_SEG = TC_POOL / SC_SEGS;
@@ -1092,7 +1096,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                 const float o = p.rstate_in ? p.rstate_in[rbase + rg] : 0.f;
                 ref = isfinite(o) ? o : 0.f;
                 lost = __ldcg(sk.lost + rbase + rg);
-                if (lost) sk.lost[rbase + rg] = 0;
+                if (lost) {
+                    sk.lost[rbase + rg] = 0;
+                    atomicAdd(&misc[5], 1);
+                }
             }
             s_ref[r] = ref;
             s_max[r] = 0u;  // below the encoding of every float
@@ -1104,6 +1111,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
             s_off[g + 1] = __ldcg(sk.pool_cnt + cta0 * SC_SEGS + g);
     }
     __syncthreads();
+    // On probation (p.redo set): a row block with more lost rows than the
+    // one-row retry handles writes nothing and is left to the full half-step
+    // launched next (its rows keep their old values, which that step reads).
+    if (p.redo && misc[5] > SC_RETRY_INLINE) {
+        if (threadIdx.x == 0) {
+            p.redo[(size_t)b * p.rowtiles + rb] = 1;
+            atomicAdd(sk.ovf, misc[5]);
+        }
+        return;
+    }
     const int nseg = p.split * SC_SEGS;
     if (warp == 0) {  // ... and their prefix sums (segment g holds entries s_off[g] .. s_off[g + 1])
         int carry = 0;

@@ -49,6 +49,9 @@ struct HalfArgs {
     const unsigned* lo_in;  // [B] stabiliser bound from the other side (ord-encoded) or NULL
     unsigned* lo_out;       // [B] receives min over rows of (old - new) (ord-encoded) or NULL
     unsigned* lo_reset;     // [B] slot reset to SOT_ORD_EMPTY by block (0,0) or NULL
+    int* redo;              // NULL, or [B*rowtiles] row-block flags: the screened half-step sets the flag of
+                            // a row block it leaves to the full half-step; the full half-step then runs
+                            // only the flagged row blocks
 };
 
 struct ApplyArgs {
@@ -118,6 +121,10 @@ cudaError_t launch_dense_apply(const ApplyArgs& p, cudaStream_t st);
 cudaError_t launch_dense_coo(const CooArgs& p, int write_pass, cudaStream_t st);
 
 // ---- preprocessing and small kernels, k_prep.cu ----
+// Cosine cost: unit directions of `count` points, and the gradient carried
+// back through x / |x| (in place).
+cudaError_t launch_normalise(const float* P, long long count, int d, float* out, cudaStream_t st);
+cudaError_t launch_cosine_grad(const float* X, long long count, int d, float* grad, cudaStream_t st);
 cudaError_t launch_center(const float* X, const float* Y, int B, int n, int m, int d,
                           float* shift, cudaStream_t st);
 cudaError_t launch_pack(const float* P, const float* w, int B, int n, int d, const float* shift,

@@ -165,6 +165,24 @@ int check_sizes(const float* X, const float* Y, int B, int n, int m, int d) {
     return SOT_OK;
 }
 
+// Cosine cost (SOT_COST_COSINE): unit copies of both clouds in `scr`, which
+// stay alive (stream-ordered) for the rest of the call; *Xu, *Yu point at
+// them.  Without the flag the inputs are used as they are.
+int unit_points(int flags, const float* X, const float* Y, int B, int n, int m, int d, Scratch& scr,
+                const float** Xu, const float** Yu) {
+    *Xu = X;
+    *Yu = Y;
+    if (!(flags & SOT_COST_COSINE) || B == 0) return SOT_OK;
+    float* xn = scr.alloc<float>((size_t)B * n * d);
+    float* yn = scr.alloc<float>((size_t)B * m * d);
+    if (!xn || !yn) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    SOT_CUDA(launch_normalise(X, (long long)B * n, d, xn, scr.st));
+    SOT_CUDA(launch_normalise(Y, (long long)B * m, d, yn, scr.st));
+    *Xu = xn;
+    *Yu = yn;
+    return SOT_OK;
+}
+
 // Column split of one half-step: rows in tiles of rpc, columns in tiles of
 // cpt; choose the number of column chunks that keeps the SMs busy (fewest
 // "rounds" of resident CTAs per unit of work).
@@ -232,6 +250,11 @@ struct Solver {
     TcScreen scr;
     bool screen_allowed = false;
     bool screen_on = false;
+    // The first screened iteration of a stage is on probation: a row block with
+    // more overflowing rows than the kernel retries inline is left, unwritten,
+    // to a full half-step launched right after (on the flagged blocks only).
+    bool screen_probation = false;
+    int* redo = nullptr;
     // Cluster-resident iterations (point path, clouds that fit in shared memory).
     bool cluster_allowed = false;
     bool cluster_ok = false;
@@ -318,7 +341,8 @@ struct Solver {
                 scr.pool_cnt = S.alloc<int>(ctas * tc_screen_pool_segments());
                 scr.lost = S.alloc<int>(rows_max);
                 scr.ovf = S.alloc<int>(1);
-                if (!scr.pool || !scr.pool_cnt || !scr.lost || !scr.ovf)
+                redo = S.alloc<int>((size_t)B * rt_max);
+                if (!scr.pool || !scr.pool_cnt || !scr.lost || !scr.ovf || !redo)
                     return fail(SOT_ERR_NOMEM, "scratch allocation failed");
                 SOT_CUDA(cudaMemsetAsync(scr.lost, 0, sizeof(int) * rows_max, st));
                 SOT_CUDA(cudaMemsetAsync(scr.ovf, 0, sizeof(int), st));
@@ -357,6 +381,7 @@ struct Solver {
         p.errpart = errp;
         p.stop_flag = guarded ? stop_flag() : nullptr;
         p.status = dflags;
+        p.redo = nullptr;
         return p;
     }
 
@@ -381,7 +406,16 @@ struct Solver {
                 e = launch_dense_half(p, mode, st);
             } else if (mode == MODE_LSE && screen_on && !cold && p.lo_in) {
                 ps.kind = 1;
+                if (screen_probation) {
+                    SOT_CUDA(cudaMemsetAsync(redo, 0, sizeof(int) * (size_t)B * rowtiles[h], st));
+                    p.redo = redo;
+                }
                 e = launch_tc_screen(tc, p, h, scr, st);
+                if (e == cudaSuccess && p.redo) {
+                    HalfArgs q = p;  // the flagged row blocks, in full (the bound slot is already reset)
+                    q.lo_reset = nullptr;
+                    e = launch_tc_half(tc, q, h, mode, st);
+                }
             } else {
                 e = launch_tc_half(tc, p, h, mode, st);
             }
@@ -441,6 +475,7 @@ struct Solver {
     void new_stage() {
         bound_ok = false;
         screen_on = screen_allowed;
+        screen_probation = screen_allowed;
     }
 
     // After the first screened iteration of a stage: if more than 1 row in 200
@@ -449,6 +484,7 @@ struct Solver {
     // with full half-steps.
     // Reads one device counter (a stream synchronisation).
     int screen_check() {
+        screen_probation = false;
         if (!screen_on) return SOT_OK;
         int h = 0;
         SOT_CUDA(cudaMemcpyAsync(&h, scr.ovf, sizeof(int), cudaMemcpyDeviceToHost, st));
@@ -672,7 +708,8 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     if (!s) return fail(SOT_ERR_INVALID_ARG, "schedule must not be NULL");
     if (!(s->eps > 0.f) || !std::isfinite(s->eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (s->iters_per_stage < 0) return fail(SOT_ERR_INVALID_ARG, "iters_per_stage must be >= 0");
-    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT | SOT_TC_NO_SCREEN | SOT_NO_CLUSTER))
+    if (s->flags & ~(SOT_PREC_MASK | SOT_WARM_START | SOT_STAGE_EARLY_EXIT | SOT_TC_NO_SCREEN | SOT_NO_CLUSTER |
+                     SOT_COST_COSINE))
         return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
     if (B > 0 && (!f || !g)) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
     if (st && st->stage_iters_host && st->stage_iters_cap < 0) return fail(SOT_ERR_INVALID_ARG, "stage_iters_cap < 0");
@@ -682,6 +719,10 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     }
     Path path;
     rc = choose_path(d, s->flags, &path);
+    if (rc) return rc;
+    // cosine cost: every step runs on the unit points
+    Scratch unit((cudaStream_t)stream);
+    rc = unit_points(s->flags, X, Y, B, n, m, d, unit, &X, &Y);
     if (rc) return rc;
     Solver sv(X, Y, a, b, B, n, m, d, path, (cudaStream_t)stream);
     sv.screen_allowed = (path == PATH_TC) && !(s->flags & SOT_TC_NO_SCREEN);
@@ -715,14 +756,23 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     if (rc) return rc;
     if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (B > 0 && (!f || !g)) return fail(SOT_ERR_INVALID_ARG, "f and g must not be NULL");
-    if (flags & ~SOT_PREC_MASK) return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
+    if (flags & ~(SOT_PREC_MASK | SOT_COST_COSINE)) return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
     if (B == 0 || (!cost && !grad && !rowsum)) return SOT_OK;
+    const float* Xin = X;
+    Scratch unit((cudaStream_t)stream);
+    rc = unit_points(flags, X, Y, B, n, m, d, unit, &X, &Y);
+    if (rc) return rc;
     Path path;
     rc = choose_path(d, flags, &path);
     if (rc) return rc;
     if (path == PATH_TC &&
         (!tc_apply_supported(d) || ((flags & SOT_PREC_MASK) == SOT_PREC_AUTO && !tc_apply_default())))
         path = PATH_DENSE;
+    // Cosine cost: on unit points every score is below 2 kappa in magnitude, so
+    // fp32 scores keep cost and gradient at fp32 accuracy, and the plan is often
+    // dense (the tensor-core apply re-evaluates every significant pair exactly,
+    // which only pays for a few pairs per row).
+    if (path == PATH_TC && (flags & SOT_COST_COSINE) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO) path = PATH_DENSE;
     cudaStream_t cs = (cudaStream_t)stream;
     Solver sv(X, Y, a, b, B, n, m, d, path, cs);
     rc = sv.prepare(0);
@@ -758,6 +808,7 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     }
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "plan-apply launch failed: %s", cudaGetErrorString(e));
     if (cost) SOT_CUDA(launch_reduce_parts(cpart, B, p.rowtiles, cost, cs));
+    if (grad && (flags & SOT_COST_COSINE)) SOT_CUDA(launch_cosine_grad(Xin, (long long)B * n, d, grad, cs));
     return SOT_OK;
 }
 
