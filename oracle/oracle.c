@@ -18,7 +18,9 @@
  *     two-pass LSE is the reference for it.
  *   - same page, Methodologie 3 ("transport matrix application"): the plan
  *     P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps) applied to Y gives the
- *     gradient 2(a_i x_i - sum_j P_ij y_j) and the cost sum_ij P_ij C_ij.
+ *     gradient 2(a_i x_i - sum_j P_ij y_j) and the cost sum_ij P_ij C_ij;
+ *     applied to any matrix V it gives the transport-matrix products
+ *     P V and P^T U that the page's streaming HVP is built from.
  *   - "From Theory to Throughput: CUDA-Optimized APML", Abstract and
  *     Innovation: negligible assignments are thresholded, the plan is kept in
  *     COO form with bidirectional symmetrisation, gradients are kept on the
@@ -45,7 +47,7 @@
  * invariances, shift invariance, finite differences of the dual objective.
  *
  * Compile: cc -O2 -fopenmp -fPIC -shared oracle.c -lm  (no fast-math).
- * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..9) that
+ * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..10) that
  * the test suite uses to show that the pins catch plausible mistakes.
  */
 #include <math.h>
@@ -416,6 +418,38 @@ int orc_plan_apply(int n, int m, int d, const double *X, const double *Y,
                 s += exp((f[i] + g[j] - c) / eps + log(a[i]) + log(b[j]));
             }
             colsum[j] = s;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Transport-matrix products ("FlashSinkhorn", Methodologie 3 and its HVP
+ * paragraph), by the definition of P:
+ *   side 0: out[i][:] = sum_j P_ij V[j][:]   (V is m x c, out is n x c)
+ *   side 1: out[j][:] = sum_i P_ij V[i][:]   (V is n x c, out is m x c)
+ */
+int orc_transport(int n, int m, int d, const double *X, const double *Y,
+                  const double *a, const double *b, const double *f,
+                  const double *g, double eps, const double *V, int c,
+                  int side, double *out) {
+    if (n <= 0 || m <= 0 || d <= 0 || c <= 0 || !(eps > 0) || (side != 0 && side != 1)) return -1;
+    const int nout = side == 0 ? n : m;
+#pragma omp parallel for schedule(static)
+    for (int o = 0; o < nout; ++o) {
+        double *acc = out + (size_t)o * c;
+        for (int k = 0; k < c; ++k) acc[k] = 0.0;
+        const int nin = side == 0 ? m : n;
+        for (int q = 0; q < nin; ++q) {
+            const int i = side == 0 ? o : q, j = side == 0 ? q : o;
+            const double cij = cost_ij(X + (size_t)i * d, Y + (size_t)j * d, d);
+#if ORC_MUTANT == 10
+            const double p = exp((f[i] + g[j] - cij) / eps + log(a[j % n]) + log(b[j])); /* mutant: wrong row weight */
+#else
+            const double p = exp((f[i] + g[j] - cij) / eps + log(a[i]) + log(b[j]));
+#endif
+            const double *v = V + (size_t)q * c;
+            for (int k = 0; k < c; ++k) acc[k] += p * v[k];
         }
     }
     return 0;

@@ -81,6 +81,8 @@ class Oracle:
         L.orc_set_num_threads.argtypes = [C.c_int]
         L.orc_mutant.restype = C.c_int
         L.orc_set_cost.argtypes = [C.c_int]
+        L.orc_transport.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, _dp, _dp, _dp, _dp, C.c_double, _dp,
+                                    C.c_int, C.c_int, _dp]
         L.orc_get_cost.restype = C.c_int
 
     # ---- plumbing -----------------------------------------------------
@@ -215,6 +217,25 @@ class Oracle:
         if rc:
             raise RuntimeError(f"orc_plan_apply failed ({rc})")
         return dict(cost=cost.value, grad=grad, rowsum=r, colsum=c)
+
+    def transport(self, X, Y, a, b, f, g, eps, V, side=0):
+        """Transport-matrix product: side 0 -> P V (V is m x c), side 1 -> P^T V
+        (V is n x c).  A 1-D V gives a 1-D result."""
+        X, Y, a, b, n, m, d = self._prob(X, Y, a, b)
+        V = _d(V)
+        vec = V.ndim == 1
+        if vec:
+            V = V[:, None]
+        if V.shape[0] != (m if side == 0 else n):
+            raise ValueError("V has the wrong number of rows for this side")
+        c = V.shape[1]
+        f, g = _d(f), _d(g)
+        out = np.zeros(((n if side == 0 else m), c))
+        rc = self.lib.orc_transport(n, m, d, _ptr(X), _ptr(Y), _ptr(a), _ptr(b), _ptr(f), _ptr(g),
+                                    float(eps), _ptr(V), c, int(side), _ptr(out))
+        if rc != 0:
+            raise ValueError("orc_transport failed")
+        return out[:, 0] if vec else out
 
     def objectives(self, X, Y, a, b, f, g, eps):
         X, Y, a, b, n, m, d = self._prob(X, Y, a, b)

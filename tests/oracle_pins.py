@@ -425,6 +425,53 @@ def pin_cosine_dual_finite_differences(orc):
                 fd[i, k] = (obj(Xp) - obj(Xm)) / (2 * h)
     _close(grad, fd, 1e-6, atol=1e-9, what="cosine finite differences of the dual")
 
+
+# ---- transport-matrix products ("FlashSinkhorn", Methodologie 3 and its HVP
+# paragraph: P V and P^T U streamed without storing P) -------------------------
+
+def pin_transport_closed_form(orc):
+    """A 1 x 1 plan worked by hand: x = (0.5, -1), y = (1.5, 1), C = 5; with
+    f = 3, g = 1.5, eps = 0.5 the plan is a b exp((3 + 1.5 - 5)/0.5) = a b / e,
+    and both products are that scalar times V."""
+    x, y = np.array([[0.5, -1.0]]), np.array([[1.5, 1.0]])
+    V = np.array([[2.0, -3.0, 0.25]])
+    for a, b in (([1.0], [1.0]), ([0.5], [0.25])):
+        pv = a[0] * b[0] * np.exp(-1.0)
+        for side in (0, 1):
+            out = orc.transport(x, y, a, b, [3.0], [1.5], 0.5, V, side=side)
+            _close(out, pv * V, 1e-14, what=f"1 x 1 transport side {side}")
+
+
+def pin_transport_marginals(orc):
+    """A run ends with a g-half, after which the column marginals are exact:
+    P^T 1 = b.  P 1 approaches a as the run converges, and P Y gives the
+    gradient 2 (a_i x_i - (P Y)_i) of the plan application."""
+    X, Y, a, b = _problem(21, 9, 7, 3)
+    eps = 0.3
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [40])
+    _close(orc.transport(X, Y, a, b, f, g, eps, np.ones(9), side=1), b, 1e-12, what="P^T 1 = b")
+    fc, gc = orc.sinkhorn(X, Y, a, b, [eps], [4000])
+    _close(orc.transport(X, Y, a, b, fc, gc, eps, np.ones(7), side=0), a, 1e-9, what="P 1 -> a")
+    PY = orc.transport(X, Y, a, b, f, g, eps, Y, side=0)
+    ref = orc.plan_apply(X, Y, a, b, f, g, eps)
+    _close(2.0 * (a[:, None] * X - PY), ref["grad"], 1e-12, atol=1e-14, what="gradient from P Y")
+
+
+def pin_transport_adjoint(orc):
+    """The two sides are each other's transpose: <U, P V> = <P^T U, V> for any
+    U (n x c) and V (m x c), and each is linear in its matrix."""
+    X, Y, a, b = _problem(22, 8, 11, 2)
+    eps = 0.2
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [25])
+    rng = _rng(23)
+    U, V, W = rng.normal(size=(8, 3)), rng.normal(size=(11, 3)), rng.normal(size=(11, 3))
+    PV = orc.transport(X, Y, a, b, f, g, eps, V, side=0)
+    PtU = orc.transport(X, Y, a, b, f, g, eps, U, side=1)
+    _close(np.sum(U * PV), np.sum(PtU * V), 1e-12, what="<U, P V> = <P^T U, V>")
+    PW = orc.transport(X, Y, a, b, f, g, eps, W, side=0)
+    PVW = orc.transport(X, Y, a, b, f, g, eps, 2.0 * V - W, side=0)
+    _close(PVW, 2.0 * PV - PW, 1e-12, atol=1e-15, what="linearity")
+
 ALL_PINS = [
     pin_closed_form_single_point,
     pin_two_point_closed_form,
@@ -442,4 +489,7 @@ ALL_PINS = [
     pin_cosine_unit_points,
     pin_cosine_scale_invariance,
     pin_cosine_dual_finite_differences,
+    pin_transport_closed_form,
+    pin_transport_marginals,
+    pin_transport_adjoint,
 ]

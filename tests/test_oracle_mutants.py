@@ -4,7 +4,8 @@ Each mutant is oracle.c compiled with -DORC_MUTANT=k (see the mutant list at
 the top of oracle.c): dropped log-weight term, wrong sign of the cost, weights
 transposed, gradient missing a_i, wrong sign of g in the plan, Jacobi instead
 of Gauss-Seidel order, log-sum-exp without the max added back, a coordinate
-dropped from the cost, a cosine cost that leaves y unnormalised.
+dropped from the cost, a cosine cost that leaves y unnormalised, a transport
+product that weights its pairs with the wrong row weight.
 """
 import pytest
 
@@ -13,7 +14,7 @@ from oracle import oracle as O
 
 MUTANTS = {1: "drops log b", 2: "sign of C", 3: "weights transposed", 4: "grad without a_i",
            5: "sign of g in plan", 6: "Jacobi order", 7: "LSE without max", 8: "cost drops a coordinate",
-           9: "cosine without y normalised"}
+           9: "cosine without y normalised", 10: "transport with the wrong row weight"}
 
 
 @pytest.mark.parametrize("k", sorted(MUTANTS), ids=lambda k: MUTANTS[k])
