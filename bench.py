@@ -446,6 +446,129 @@ def run_gpu(args, ws, rank, local):
     return 0
 
 
+def run_transport(args, ws, rank, local):
+    """Transport-matrix products (sot_transport_apply): one step is P V (V with
+    `args.transport` columns) and P^T U on a workload, from potentials solved
+    once before the timed region.  Same timing rules as the solver line."""
+    import torch
+    import sinkhorn_point_cloud_gb300 as sot
+    from sinkhorn_point_cloud_gb300 import build
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    wid = args.workload
+    w = datagen.WORKLOADS[wid]
+    B, n, m, d, eps = w["B"], w["n"], w["m"], w["d"], w["eps"]
+    if args.n:
+        n = m = args.n
+    c = args.transport
+    flags = sot.SOT_COST_COSINE if args.cost == "cosine" else 0
+    X, Y, a, b = datagen.make_batch(wid, B=B, n=n, m=m, clouds=range(rank * B, rank * B + B))
+    weighted = w["kind"] == "gauss"
+    Xd, Yd = torch.from_numpy(X).to(dev), torch.from_numpy(Y).to(dev)
+    ad, bd = (torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)) if weighted else (None, None)
+    f, g = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=args.iters or 100,
+                                 max_iters=args.iters or 100, flags=flags)
+    rng = np.random.default_rng(20260700 + rank)
+    host_in = [torch.from_numpy(rng.standard_normal((B, m, c)).astype(np.float32)).pin_memory(),
+               torch.from_numpy(rng.standard_normal((B, n, c)).astype(np.float32)).pin_memory()]
+    V, U = [v.to(dev) for v in host_in]
+    outs = [torch.empty(B, n, c, device=dev), torch.empty(B, m, c, device=dev)]
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(v, u):
+        o0 = sot.sot_transport_apply(Xd, Yd, ad, bd, f, g, eps, v, side=0, flags=flags, out=outs[0])
+        o1 = sot.sot_transport_apply(Xd, Yd, ad, bd, f, g, eps, u, side=1, flags=flags, out=outs[1])
+        return [o0, o1]
+
+    for _ in range(args.warmup):
+        step(V, U)
+    torch.cuda.synchronize()
+    launches0 = sot.sot_kernel_launches()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clk_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
+        else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local, clk_path) as cs:
+        for k in range(args.steps):
+            flush_buf.zero_()
+            ev[k][0].record(stream)
+            step(V, U)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = sot.sot_kernel_launches() - launches0
+    t_max = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, ws, dev)
+    clocks = cs.summary()
+    # end to end: V and U from pinned host memory, both products back to the host
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for k in range(0 if args.no_e2e else args.steps):
+        flush_buf.zero_()
+        e0.record(stream)
+        v, u = [h.to(dev, non_blocking=True) for h in host_in]
+        hosts = [o.to("cpu", non_blocking=True) for o in step(v, u)]
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_max = max_over_ranks(e2e_ms / 1e3, ws, dev) if not args.no_e2e else None
+    if rank != 0:
+        return 0
+    pairs_step = 2.0 * B * n * m
+    pk, pk_kind = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rates = alu_rates()
+    lanes = rates["ffma_lanes_per_sm_clk"] if rates else 128.0
+    mhz = float(pk.get("sm_max_mhz", 2070.0))
+    # the fp32 screen of every pair: a subtraction and an FMA per coordinate, one
+    # FMA for the exponent estimate (the exact evaluation of the pairs that
+    # matter and the c FMAs of their terms are extra work, not counted)
+    ops_pair = 2 * d + 1
+    achieved = ops_pair * pairs_step * args.steps / t_max / 1e12
+    peak = lanes * sms * mhz * 1e6 / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import oracle as O
+        orc = O.get()
+        rows = max(1, min(n, int(64 * orc.num_threads)))
+        fh, gh = f[0].double().cpu().numpy(), g[0].double().cpu().numpy()
+        t0 = time.perf_counter()
+        with orc.cost(args.cost):
+            orc.transport(X[0][:rows], Y[0], a[0][:rows] if weighted else None, b[0] if weighted else None,
+                          fh[:rows], gh, eps, host_in[0][0].numpy(), side=0)
+        tc = time.perf_counter() - t0
+        cpu = {"value": rows * m / tc / 1e9, "unit": UNIT, "cores": orc.num_threads, "kind": "oracle",
+               "sample": f"P V on {rows} rows x {m} columns, c={c} (d={d}), {tc:.1f} s"}
+    line = {
+        "metric": f"transport products P V, P^T U pair-evaluations/s ({w['name']}, c={c})",
+        "value": ws * pairs_step * args.steps / t_max / 1e9, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w["name"], "B": B, "n": n, "m": m, "d": d, "eps": eps, "c": c,
+                   **({"cost": "cosine"} if args.cost == "cosine" else {}),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"FP32 lanes/SM/clk from the ALU probe x {sms} SMs x {mhz:.0f} MHz",
+                     "kernel": f"transport_kernel ({ops_pair} FP32 lane-ops per pair in the screen)"},
+        "cpu_baseline": cpu,
+        "e2e": None if e2e_max is None else {"value": ws * pairs_step * args.steps / e2e_max / 1e9, "unit": UNIT,
+                                             "h2d_bytes_per_step": sum(h.numel() * 4 for h in host_in),
+                                             "d2h_bytes_per_step": sum(o.numel() * 4 for o in outs)},
+        "gpu_launches": int(launches),
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,6 +588,8 @@ def main(argv=None):
     ap.add_argument("--no-screen", action="store_true", help="tensor path: full half-steps only (comparison runs)")
     ap.add_argument("--no-cluster", action="store_true",
                     help="point path: streaming half-steps only, no cluster-resident iterations (comparison runs)")
+    ap.add_argument("--transport", type=int, default=0, metavar="C",
+                    help="time the transport products P V and P^T U with C columns instead of the solver")
     ap.add_argument("--cost", choices=["sqeuclidean", "cosine"], default="sqeuclidean",
                     help="cost function (cosine: 2 - 2 cos, on the normalised points)")
     args = ap.parse_args(argv)
@@ -473,6 +598,8 @@ def main(argv=None):
     ws, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
+    if args.transport:
+        return run_transport(args, ws, rank, local)
     return run_gpu(args, ws, rank, local)
 
 

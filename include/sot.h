@@ -142,6 +142,24 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
                    int B, int n, int m, int d, const float* f, const float* g, float eps,
                    float* cost, float* grad, float* rowsum, int flags, void* stream);
 
+/*
+ * Transport-matrix products with the given (f, g) at eps, streamed without
+ * storing P ("FlashSinkhorn", Methodologie 3 and its HVP paragraph: the
+ * Hessian-vector product decomposes into transport-vector and
+ * transport-matrix products), P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps):
+ *   side 0: out[k][i][:] = sum_j P_ij V[k][j][:]    V [B][m][c] -> out [B][n][c]
+ *   side 1: out[k][j][:] = sum_i P_ij V[k][i][:]    V [B][n][c] -> out [B][m][c]
+ * c = 1 is a transport-vector product; 1 <= c <= 64, d <= 256.  Pairs whose
+ * weight is below 2^-30 / (number of summed points) of a_i (side 0) or b_j
+ * (side 1) are skipped, under 2^-30 of it in all; every
+ * other pair's P_ij is evaluated in float-float arithmetic from the caller's
+ * coordinates and potentials.  flags: 0 or SOT_COST_COSINE.  V and out are
+ * device arrays owned by the caller; out is fully written.  Asynchronous.
+ */
+int sot_transport_apply(const float* X, const float* Y, const float* a, const float* b,
+                        int B, int n, int m, int d, const float* f, const float* g, float eps,
+                        const float* V, int c, int side, float* out, int flags, void* stream);
+
 /* Convenience forms of sot_plan_apply (precision auto). */
 int sot_cost(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
              const float* f, const float* g, float eps, float* cost, void* stream);

@@ -10,6 +10,6 @@ from .binding import (SOT_ERR_CAPACITY, SOT_ERR_CUDA, SOT_ERR_INVALID_ARG, SOT_E
                       sot_check_inputs, sot_cost,
                       sot_cost_grad, sot_grad_x, sot_grad_x_coo, sot_kernel_launches, sot_select_path, sot_plan_apply,
                       sot_plan_coo, sot_potentials, sot_potentials_ex, sot_potentials_noalloc, sot_profile_enable,
-                      sot_profile_read, sot_profile_read_kinds, sot_status_string, sot_version)
+                      sot_profile_read, sot_profile_read_kinds, sot_status_string, sot_transport_apply, sot_version)
 
 __all__ = [n for n in dir() if n.startswith(("sot_", "SOT_", "Sot"))]

@@ -96,6 +96,7 @@ def load(path: str | None = None):
         "sot_kernel_launches": [],
         "sot_select_path": [i, i],
         "sot_potentials_noalloc": [P, P, P, P, i, i, i, i, f, i, P, P, P],
+        "sot_transport_apply": [P, P, P, P, i, i, i, i, P, P, f, P, i, i, P, i, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -228,6 +229,25 @@ def sot_plan_apply(X, Y, a, b, f, g, eps, cost=True, grad=True, rowsum=False, fl
                                _ptr(c), _ptr(gr), _ptr(r), int(flags), _stream(stream))
     _check(rc, "sot_plan_apply")
     return c, gr, r
+
+
+def sot_transport_apply(X, Y, a, b, f, g, eps, V, side=0, flags=0, out=None, stream=None):
+    """Transport-matrix product: side 0 -> P V with V [B,m,c] (out [B,n,c]);
+    side 1 -> P^T V with V [B,n,c] (out [B,m,c]).  A [B,rows] V is one column."""
+    X, Y, B, n, m, d = _shapes(X, Y, a, b)
+    vec = V.dim() == 2
+    V3 = V.unsqueeze(-1) if vec else V
+    if V3.dtype != torch.float32 or not V3.is_contiguous() or V3.device != X.device:
+        raise ValueError("V must be a contiguous float32 tensor on the device of X")
+    rows_in, rows_out = (m, n) if side == 0 else (n, m)
+    if V3.shape[0] != B or V3.shape[1] != rows_in:
+        raise ValueError(f"V must have shape [B, {rows_in}, c] for side {side}")
+    c = V3.shape[2]
+    o = torch.empty(B, rows_out, c, device=X.device, dtype=torch.float32) if out is None else out
+    rc = load().sot_transport_apply(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g),
+                                    float(eps), _ptr(V3), int(c), int(side), _ptr(o), int(flags), _stream(stream))
+    _check(rc, "sot_transport_apply")
+    return o[..., 0] if vec else o
 
 
 def sot_cost(X, Y, a, b, f, g, eps, stream=None):

@@ -1,0 +1,154 @@
+// k_transport.cu -- transport-matrix products P V streamed without storing P
+// ("FlashSinkhorn", Methodologie 3: the plan is applied as an attention-like
+// weighted sum; its HVP paragraph builds the Hessian-vector product from
+// such transport-vector and transport-matrix products).
+//
+// One thread per row; column tiles (coordinates transposed, so a row value is
+// reused by four columns) and the tile's V rows sit in shared memory.  Each
+// pair is first scored in fp32 in the direct form: log2(P_ij / w_i) is about
+// log2 w'_j + kappa (f_i + g_j - C_ij).  A pair below -(26 + log2 nc) - 4 is
+// skipped: its weight is under 2^-30 / nc of w_i, so all skipped pairs of a row
+// together carry less than 2^-30 of it (the 4 units cover the fp32 estimate's
+// own error many times over), far below fp32 resolution of the sum.  Every
+// other pair is evaluated exactly: C_ij from error-free coordinate differences
+// and squares in float-float, and the exponent, where the potentials and C_ij
+// cancel to a small number, in float-float throughout (the fp64 pipe is slow
+// on this part).
+#include "common.cuh"
+#include "kernels.h"
+#include "transport.h"
+
+namespace sot {
+
+constexpr int TR_T = 128;        // rows per CTA (one per thread)
+constexpr int TR_CT = 32;        // columns per shared-memory tile
+constexpr int TR_YS = TR_CT + 4; // its row stride (keeps float4 reads aligned; 4-way store conflicts, not 32)
+constexpr int TR_MAXD = 256;
+constexpr int TR_MAXC = 64;
+
+int transport_max_d() { return TR_MAXD; }
+int transport_max_c() { return TR_MAXC; }
+
+// row stride of the row tile in shared memory: odd, so the 32 rows of a warp
+// fall in 32 different banks
+__host__ __device__ inline int tr_ldx(int d) { return (d % 2 == 0) ? d + 1 : d; }
+
+static size_t tr_smem_bytes(int d, int c) {
+    return sizeof(float) * ((size_t)TR_T * tr_ldx(d) + (size_t)d * TR_YS + (size_t)TR_CT * c + 2 * TR_CT);
+}
+
+template <int CV>
+__global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
+    extern __shared__ float smem[];
+    const int d = p.d, c = p.c, ldx = tr_ldx(d);
+    float* xs = smem;                 // [TR_T][ldx] this CTA's rows
+    float* ys = xs + TR_T * ldx;      // [d][TR_YS] column tile, transposed and negated
+    float* vs = ys + d * TR_YS;       // [TR_CT][c] V rows of the tile
+    float* gs = vs + TR_CT * c;       // [TR_CT] column potentials
+    float* ls = gs + TR_CT;           // [TR_CT] log2 column weights (-inf past the end)
+    const int b = blockIdx.y;
+    const int row0 = blockIdx.x * TR_T;
+    const int i = row0 + threadIdx.x;
+    const bool ok = i < p.nr;
+    const float* R = p.R + (size_t)b * p.nr * d;
+    const float* Cl = p.Cl + (size_t)b * p.nc * d;
+    const float* Vb = p.V + (size_t)b * p.nc * c;
+
+    for (int e = threadIdx.x; e < TR_T * d; e += TR_T) {
+        const int r = e / d, k = e % d;
+        xs[r * ldx + k] = (row0 + r < p.nr) ? R[(size_t)(row0 + r) * d + k] : 0.f;
+    }
+    const float fi = ok ? p.fr[(size_t)b * p.nr + i] : 0.f;
+    const float lwi = ok ? (p.wr ? log2f(p.wr[(size_t)b * p.nr + i]) : -log2f((float)p.nr)) : 0.f;
+    const float2 kap = make_float2(p.kap_hi, p.kap_lo);
+    const float sig = -(30.f + log2f((float)p.nc));  // skip threshold on log2(P_ij / w_i)
+    float acc[CV];
+#pragma unroll
+    for (int k = 0; k < CV; ++k) acc[k] = 0.f;
+    const float* xr = xs + threadIdx.x * ldx;
+
+    for (int base = 0; base < p.nc; base += TR_CT) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < TR_CT * d; e += TR_T) {
+            const int jj = e / d, k = e % d, j = base + jj;
+            ys[k * TR_YS + jj] = (j < p.nc) ? -Cl[(size_t)j * d + k] : 0.f;  // negated
+        }
+        for (int e = threadIdx.x; e < TR_CT * c; e += TR_T) {
+            const int jj = e / c, k = e % c, j = base + jj;
+            vs[jj * c + k] = (j < p.nc) ? Vb[(size_t)j * c + k] : 0.f;
+        }
+        if (threadIdx.x < TR_CT) {
+            const int j = base + threadIdx.x;
+            const bool cj = j < p.nc;
+            gs[threadIdx.x] = cj ? p.gc[(size_t)b * p.nc + j] : 0.f;
+            ls[threadIdx.x] = cj ? (p.wc ? log2f(p.wc[(size_t)b * p.nc + j]) : -log2f((float)p.nc)) : -INFINITY;
+        }
+        __syncthreads();
+        if (!ok) continue;
+        for (int j4 = 0; j4 < TR_CT; j4 += 4) {
+            // fp32 direct-form distances of four columns, two per packed instruction
+            float2 c01 = make_float2(0.f, 0.f), c23 = c01;
+            for (int k = 0; k < d; ++k) {
+                const float2 xx = make_float2(xr[k], xr[k]);
+                const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + j4);
+                const float2 t01 = fadd2(xx, make_float2(y4.x, y4.y));
+                const float2 t23 = fadd2(xx, make_float2(y4.z, y4.w));
+                c01 = ffma2(t01, t01, c01);
+                c23 = ffma2(t23, t23, c23);
+            }
+            const float C4[4] = {c01.x, c01.y, c23.x, c23.y};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int jj = j4 + u;
+                // screen: log2(P_ij / w_i) estimated in fp32 (-inf past the last column)
+                const float est = fmaf(p.kap_hi, fi + gs[jj] - C4[u], ls[jj]);
+                if (!(est > sig)) continue;
+                // exact: C_ij from exact differences and squares (float-float)
+                float2 C2 = make_float2(0.f, 0.f);
+                for (int k = 0; k < d; ++k) {
+                    const float2 dd = two_sum(xr[k], ys[k * TR_YS + jj]);
+                    float2 sq = two_prod(dd.x, dd.x);
+                    sq.y = __fmaf_rn(2.f * dd.x, dd.y, sq.y);
+                    C2 = ff_add(C2, sq);
+                }
+                // log2 P_ij = log2 w_i + log2 w'_j + kappa (f_i + g_j - C_ij)
+                const float2 pot = ff_add(two_sum(fi, gs[jj]), make_float2(-C2.x, -C2.y));
+                const float2 ell = ff_add(ff_mul(kap, pot), two_sum(ls[jj], lwi));
+                const float w = exp2f(__fadd_rn(ell.x, ell.y));
+                const float* vj = vs + jj * c;
+#pragma unroll
+                for (int k = 0; k < CV; ++k)
+                    if (k < c) acc[k] = fmaf(w, vj[k], acc[k]);
+            }
+        }
+    }
+    if (ok) {
+        float* o = p.out + ((size_t)b * p.nr + i) * c;
+#pragma unroll
+        for (int k = 0; k < CV; ++k)
+            if (k < c) o[k] = acc[k];
+    }
+}
+
+cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
+    if (p.d < 1 || p.d > TR_MAXD || p.c < 1 || p.c > TR_MAXC || p.B < 1 || p.nr < 1 || p.nc < 1)
+        return cudaErrorInvalidValue;
+    const size_t sm = tr_smem_bytes(p.d, p.c);
+    dim3 grid((p.nr + TR_T - 1) / TR_T, p.B), block(TR_T);
+#define SOT_TR_CASE(CVV)                                                                              \
+    {                                                                                                 \
+        cudaError_t e = cudaFuncSetAttribute(transport_kernel<CVV>,                                   \
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);   \
+        if (e != cudaSuccess) return e;                                                               \
+        count_launches(1);                                                                            \
+        transport_kernel<CVV><<<grid, block, sm, st>>>(p);                                            \
+    }
+    if (p.c <= 1) SOT_TR_CASE(1)
+    else if (p.c <= 4) SOT_TR_CASE(4)
+    else if (p.c <= 16) SOT_TR_CASE(16)
+    else SOT_TR_CASE(64)
+#undef SOT_TR_CASE
+    return cudaGetLastError();
+}
+
+}  // namespace sot

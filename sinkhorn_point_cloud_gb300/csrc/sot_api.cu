@@ -18,6 +18,7 @@
 #include "kernels.h"
 #include "sot.h"
 #include "tc.h"
+#include "transport.h"
 
 using namespace sot;
 
@@ -809,6 +810,40 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "plan-apply launch failed: %s", cudaGetErrorString(e));
     if (cost) SOT_CUDA(launch_reduce_parts(cpart, B, p.rowtiles, cost, cs));
     if (grad && (flags & SOT_COST_COSINE)) SOT_CUDA(launch_cosine_grad(Xin, (long long)B * n, d, grad, cs));
+    return SOT_OK;
+}
+
+int sot_transport_apply(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                        const float* f, const float* g, float eps, const float* V, int c, int side, float* out,
+                        int flags, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (side != 0 && side != 1) return fail(SOT_ERR_INVALID_ARG, "side must be 0 (P V) or 1 (P^T V), got %d", side);
+    if (c < 1 || c > transport_max_c())
+        return fail(SOT_ERR_INVALID_ARG, "c must satisfy 1 <= c <= %d (got %d)", transport_max_c(), c);
+    if (d > transport_max_d())
+        return fail(SOT_ERR_UNSUPPORTED, "transport products support d <= %d (got %d)", transport_max_d(), d);
+    if (flags & ~SOT_COST_COSINE) return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
+    if (B > 0 && (!f || !g || !V || !out)) return fail(SOT_ERR_INVALID_ARG, "f, g, V and out must not be NULL");
+    if (B == 0) return SOT_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    Scratch unit(cs);
+    rc = unit_points(flags, X, Y, B, n, m, d, unit, &X, &Y);
+    if (rc) return rc;
+    const double kap = 1.0 / ((double)eps * SOT_LN2_D);
+    TransportArgs p;
+    p.B = B; p.d = d; p.c = c; p.V = V; p.out = out;
+    p.kap_hi = (float)kap;
+    p.kap_lo = (float)(kap - (double)p.kap_hi);
+    if (side == 0) {
+        p.nr = n; p.nc = m; p.R = X; p.Cl = Y; p.fr = f; p.gc = g; p.wr = a; p.wc = b;
+    } else {
+        p.nr = m; p.nc = n; p.R = Y; p.Cl = X; p.fr = g; p.gc = f; p.wr = b; p.wc = a;
+    }
+    cudaError_t e = launch_transport(p, cs);
+    if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "transport launch failed: %s", cudaGetErrorString(e));
     return SOT_OK;
 }
 

@@ -1,0 +1,31 @@
+// transport.h -- transport-matrix products streamed without storing the plan
+// ("FlashSinkhorn", Methodologie 3 and its HVP paragraph: the Hessian-vector
+// product decomposes into transport-vector and transport-matrix products).
+#pragma once
+#include <cuda_runtime.h>
+
+namespace sot {
+
+// out[b][i][:] = sum_j P_ij V[b][j][:] with
+// P_ij = w_i w'_j exp((fr_i + gc_j - |r_i - c_j|^2) / eps).
+// Rows r (nr points) and columns c (nc points) are any two clouds of a
+// problem: the f-side product uses (X, Y, f, g, a, b), the g-side product the
+// same with the roles swapped.
+struct TransportArgs {
+    int B, nr, nc, d, c;
+    const float* R;   // [B][nr][d] row points
+    const float* Cl;  // [B][nc][d] column points
+    const float* fr;  // [B][nr] row potentials
+    const float* gc;  // [B][nc] column potentials
+    const float* wr;  // [B][nr] row weights, NULL = uniform 1/nr
+    const float* wc;  // [B][nc] column weights, NULL = uniform 1/nc
+    const float* V;   // [B][nc][c]
+    float* out;       // [B][nr][c]
+    float kap_hi, kap_lo;  // 1 / (eps ln 2) as a float-float pair
+};
+
+int transport_max_d();
+int transport_max_c();
+cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st);
+
+}  // namespace sot

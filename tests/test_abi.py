@@ -89,3 +89,18 @@ def test_python_binding_refuses_cpu_tensors():
     X = torch.zeros(1, 4, 3)
     with pytest.raises(ValueError):
         binding.sot_potentials(X, X, eps=0.1, iters=1)
+
+
+def test_transport_arguments_rejected_on_host(lib):
+    p = C.c_void_p(16)
+    tr = lib.sot_transport_apply
+    ok = (p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.1, p)
+    assert tr(*ok, 0, 0, p, 0, NULL) == binding.SOT_ERR_INVALID_ARG      # c = 0
+    assert b"c must satisfy" in lib.sot_last_error()
+    assert tr(*ok, 65, 0, p, 0, NULL) == binding.SOT_ERR_INVALID_ARG     # c above 64
+    assert tr(*ok, 4, 2, p, 0, NULL) == binding.SOT_ERR_INVALID_ARG      # side 2
+    assert tr(*ok, 4, 0, p, 1 << 3, NULL) == binding.SOT_ERR_INVALID_ARG  # unknown flag
+    assert tr(*ok, 4, 0, NULL, 0, NULL) == binding.SOT_ERR_INVALID_ARG   # out NULL
+    assert tr(p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.0, p, 4, 0, p, 0, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert tr(p, p, NULL, NULL, 1, 5, 6, 300, p, p, 0.1, p, 4, 0, p, 0, NULL) == binding.SOT_ERR_UNSUPPORTED
+    assert tr(p, p, NULL, NULL, 0, 5, 6, 3, NULL, NULL, 0.1, NULL, 4, 0, NULL, 0, NULL) == binding.SOT_OK  # B = 0
