@@ -4,7 +4,9 @@
 // such transport-vector and transport-matrix products).
 //
 // One thread per row; column tiles (coordinates transposed, so a row value is
-// reused by four columns) and the tile's V rows sit in shared memory.  Each
+// reused by four columns) and the tile's V rows sit in shared memory.  Columns
+// are split into chunks so that the grid fills the SMs; chunk partial sums are
+// added in chunk order by a second kernel (deterministic).  Each
 // pair is first scored in fp32 in the direct form: log2(P_ij / w_i) is about
 // log2 w'_j + kappa (f_i + g_j - C_ij).  A pair below -(26 + log2 nc) - 4 is
 // skipped: its weight is under 2^-30 / nc of w_i, so all skipped pairs of a row
@@ -47,7 +49,9 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     float* gs = vs + TR_CT * c;       // [TR_CT] column potentials
     float* ls = gs + TR_CT;           // [TR_CT] log2 column weights (-inf past the end)
     const int b = blockIdx.y;
-    const int row0 = blockIdx.x * TR_T;
+    const int rb = blockIdx.x / p.split, ch = blockIdx.x % p.split;
+    const int row0 = rb * TR_T;
+    const int c_begin = ch * p.chunk, c_end = min(p.nc, c_begin + p.chunk);
     const int i = row0 + threadIdx.x;
     const bool ok = i < p.nr;
     const float* R = p.R + (size_t)b * p.nr * d;
@@ -67,19 +71,21 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     for (int k = 0; k < CV; ++k) acc[k] = 0.f;
     const float* xr = xs + threadIdx.x * ldx;
 
-    for (int base = 0; base < p.nc; base += TR_CT) {
+    for (int base = c_begin; base < c_end; base += TR_CT) {
         __syncthreads();
+        // coalesced reads of whole column rows (the transposed stores are 4-way
+        // bank conflicts with the padded stride)
         for (int e = threadIdx.x; e < TR_CT * d; e += TR_T) {
             const int jj = e / d, k = e % d, j = base + jj;
-            ys[k * TR_YS + jj] = (j < p.nc) ? -Cl[(size_t)j * d + k] : 0.f;  // negated
+            ys[k * TR_YS + jj] = (j < c_end) ? -Cl[(size_t)j * d + k] : 0.f;  // negated
         }
         for (int e = threadIdx.x; e < TR_CT * c; e += TR_T) {
             const int jj = e / c, k = e % c, j = base + jj;
-            vs[jj * c + k] = (j < p.nc) ? Vb[(size_t)j * c + k] : 0.f;
+            vs[jj * c + k] = (j < c_end) ? Vb[(size_t)j * c + k] : 0.f;
         }
         if (threadIdx.x < TR_CT) {
             const int j = base + threadIdx.x;
-            const bool cj = j < p.nc;
+            const bool cj = j < c_end;
             gs[threadIdx.x] = cj ? p.gc[(size_t)b * p.nc + j] : 0.f;
             ls[threadIdx.x] = cj ? (p.wc ? log2f(p.wc[(size_t)b * p.nc + j]) : -log2f((float)p.nc)) : -INFINITY;
         }
@@ -123,18 +129,45 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         }
     }
     if (ok) {
-        float* o = p.out + ((size_t)b * p.nr + i) * c;
+        float* o = (p.split > 1 ? p.part + ((size_t)ch * p.B + b) * p.nr * c : p.out + (size_t)b * p.nr * c) +
+                   (size_t)i * c;
 #pragma unroll
         for (int k = 0; k < CV; ++k)
             if (k < c) o[k] = acc[k];
     }
 }
 
+// out = sum over chunks of the partial sums, in chunk order.
+__global__ void transport_merge_kernel(const float* part, long long count, int split, float* out) {
+    const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (e >= count) return;
+    float s = 0.f;
+    for (int ch = 0; ch < split; ++ch) s += part[(size_t)ch * count + e];
+    out[e] = s;
+}
+
+size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk) {
+    // aim for two waves at four resident CTAs per SM; a chunk keeps at least
+    // 8 column tiles so that staging the rows stays a small part of its work
+    const long long blocks = (long long)B * ((nr + TR_T - 1) / TR_T);
+    const long long target = 8LL * (sms > 0 ? sms : 152);
+    const int tiles = (nc + TR_CT - 1) / TR_CT;
+    long long s = (target + blocks - 1) / blocks;
+    const long long smax = (tiles + 7) / 8;
+    if (s > smax) s = smax;
+    if (s < 1) s = 1;
+    const int tpc = (int)((tiles + s - 1) / s);
+    *chunk = tpc * TR_CT;
+    *split = (nc + *chunk - 1) / *chunk;
+    return *split > 1 ? (size_t)*split * B * nr * c : 0;
+}
+
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
-    if (p.d < 1 || p.d > TR_MAXD || p.c < 1 || p.c > TR_MAXC || p.B < 1 || p.nr < 1 || p.nc < 1)
+    if (p.d < 1 || p.d > TR_MAXD || p.c < 1 || p.c > TR_MAXC || p.B < 1 || p.nr < 1 || p.nc < 1 || p.split < 1 ||
+        p.chunk < 1 || (long long)p.split * p.chunk < p.nc || (p.split > 1 && !p.part))
         return cudaErrorInvalidValue;
     const size_t sm = tr_smem_bytes(p.d, p.c);
-    dim3 grid((p.nr + TR_T - 1) / TR_T, p.B), block(TR_T);
+    dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
 #define SOT_TR_CASE(CVV)                                                                              \
     {                                                                                                 \
         cudaError_t e = cudaFuncSetAttribute(transport_kernel<CVV>,                                   \
@@ -148,6 +181,11 @@ cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
     else if (p.c <= 16) SOT_TR_CASE(16)
     else SOT_TR_CASE(64)
 #undef SOT_TR_CASE
+    if (p.split > 1) {
+        const long long count = (long long)p.B * p.nr * p.c;
+        count_launches(1);
+        transport_merge_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(p.part, count, p.split, p.out);
+    }
     return cudaGetLastError();
 }
 

@@ -842,6 +842,9 @@ int sot_transport_apply(const float* X, const float* Y, const float* a, const fl
     } else {
         p.nr = m; p.nc = n; p.R = Y; p.Cl = X; p.fr = g; p.gc = f; p.wr = b; p.wc = a;
     }
+    const size_t nparts = transport_plan(B, p.nr, p.nc, c, device_sms(), &p.split, &p.chunk);
+    p.part = nparts ? unit.alloc<float>(nparts) : nullptr;
+    if (nparts && !p.part) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
     cudaError_t e = launch_transport(p, cs);
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "transport launch failed: %s", cudaGetErrorString(e));
     return SOT_OK;

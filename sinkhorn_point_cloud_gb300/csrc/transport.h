@@ -22,10 +22,15 @@ struct TransportArgs {
     const float* V;   // [B][nc][c]
     float* out;       // [B][nr][c]
     float kap_hi, kap_lo;  // 1 / (eps ln 2) as a float-float pair
+    int split, chunk;      // columns in `split` chunks of `chunk` columns (one CTA each)
+    float* part;           // [split][B][nr][c] partial sums when split > 1
 };
 
 int transport_max_d();
 int transport_max_c();
+// Column split for a problem on `sms` SMs: fills *split and *chunk; returns
+// the floats of partial-sum scratch it needs (0 when split == 1).
+size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk);
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st);
 
 }  // namespace sot
