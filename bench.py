@@ -481,7 +481,11 @@ def run_transport(args, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    gy = torch.empty(B, m, d, device=dev) if args.grad_y else None
+
     def step(v, u):
+        if args.grad_y:  # the gradient with respect to Y: P^T X and a pointwise step
+            return [sot.sot_grad_y(Xd, Yd, ad, bd, f, g, eps, flags=flags, out=gy)]
         o0 = sot.sot_transport_apply(Xd, Yd, ad, bd, f, g, eps, v, side=0, flags=flags, out=outs[0])
         o1 = sot.sot_transport_apply(Xd, Yd, ad, bd, f, g, eps, u, side=1, flags=flags, out=outs[1])
         return [o0, o1]
@@ -520,7 +524,7 @@ def run_transport(args, ws, rank, local):
     e2e_max = max_over_ranks(e2e_ms / 1e3, ws, dev) if not args.no_e2e else None
     if rank != 0:
         return 0
-    pairs_step = 2.0 * B * n * m
+    pairs_step = (1.0 if args.grad_y else 2.0) * B * n * m
     pk, pk_kind = peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     rates = alu_rates()
@@ -546,7 +550,8 @@ def run_transport(args, ws, rank, local):
         cpu = {"value": rows * m / tc / 1e9, "unit": UNIT, "cores": orc.num_threads, "kind": "oracle",
                "sample": f"P V on {rows} rows x {m} columns, c={c} (d={d}), {tc:.1f} s"}
     line = {
-        "metric": f"transport products P V, P^T U pair-evaluations/s ({w['name']}, c={c})",
+        "metric": (f"gradient with respect to Y pair-evaluations/s ({w['name']})" if args.grad_y else
+                   f"transport products P V, P^T U pair-evaluations/s ({w['name']}, c={c})"),
         "value": ws * pairs_step * args.steps / t_max / 1e9, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -560,8 +565,10 @@ def run_transport(args, ws, rank, local):
                      "kernel": f"transport_kernel ({ops_pair} FP32 lane-ops per pair in the screen)"},
         "cpu_baseline": cpu,
         "e2e": None if e2e_max is None else {"value": ws * pairs_step * args.steps / e2e_max / 1e9, "unit": UNIT,
-                                             "h2d_bytes_per_step": sum(h.numel() * 4 for h in host_in),
-                                             "d2h_bytes_per_step": sum(o.numel() * 4 for o in outs)},
+                                             "h2d_bytes_per_step": 0 if args.grad_y else
+                                             sum(h.numel() * 4 for h in host_in),
+                                             "d2h_bytes_per_step": gy.numel() * 4 if args.grad_y else
+                                             sum(o.numel() * 4 for o in outs)},
         "gpu_launches": int(launches),
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
@@ -590,6 +597,7 @@ def main(argv=None):
                     help="point path: streaming half-steps only, no cluster-resident iterations (comparison runs)")
     ap.add_argument("--transport", type=int, default=0, metavar="C",
                     help="time the transport products P V and P^T U with C columns instead of the solver")
+    ap.add_argument("--grad-y", action="store_true", help="with --transport: time sot_grad_y instead")
     ap.add_argument("--cost", choices=["sqeuclidean", "cosine"], default="sqeuclidean",
                     help="cost function (cosine: 2 - 2 cos, on the normalised points)")
     args = ap.parse_args(argv)

@@ -160,6 +160,16 @@ int sot_transport_apply(const float* X, const float* Y, const float* a, const fl
                         int B, int n, int m, int d, const float* f, const float* g, float eps,
                         const float* V, int c, int side, float* out, int flags, void* stream);
 
+/*
+ * Gradient with respect to Y with the given (f, g) at eps, the mirror of the
+ * gradient of sot_plan_apply: grad_y[k][j] = 2 (b_j y_j - sum_i P_ij x_i),
+ * [B][m][d], formed from the transport product P^T X (see
+ * sot_transport_apply; d <= 256).  flags: 0 or SOT_COST_COSINE (then the
+ * gradient is carried back through y/|y|).  Asynchronous.
+ */
+int sot_grad_y(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+               const float* f, const float* g, float eps, float* grad_y, int flags, void* stream);
+
 /* Convenience forms of sot_plan_apply (precision auto). */
 int sot_cost(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
              const float* f, const float* g, float eps, float* cost, void* stream);

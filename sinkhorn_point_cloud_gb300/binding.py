@@ -97,6 +97,7 @@ def load(path: str | None = None):
         "sot_select_path": [i, i],
         "sot_potentials_noalloc": [P, P, P, P, i, i, i, i, f, i, P, P, P],
         "sot_transport_apply": [P, P, P, P, i, i, i, i, P, P, f, P, i, i, P, i, P],
+        "sot_grad_y": [P, P, P, P, i, i, i, i, P, P, f, P, i, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -248,6 +249,16 @@ def sot_transport_apply(X, Y, a, b, f, g, eps, V, side=0, flags=0, out=None, str
                                     float(eps), _ptr(V3), int(c), int(side), _ptr(o), int(flags), _stream(stream))
     _check(rc, "sot_transport_apply")
     return o[..., 0] if vec else o
+
+
+def sot_grad_y(X, Y, a, b, f, g, eps, flags=0, out=None, stream=None):
+    """Gradient with respect to Y: 2 (b_j y_j - sum_i P_ij x_i), [B, m, d]."""
+    X, Y, B, n, m, d = _shapes(X, Y, a, b)
+    o = torch.empty(B, m, d, device=X.device, dtype=torch.float32) if out is None else out
+    rc = load().sot_grad_y(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g), float(eps), _ptr(o),
+                           int(flags), _stream(stream))
+    _check(rc, "sot_grad_y")
+    return o
 
 
 def sot_cost(X, Y, a, b, f, g, eps, stream=None):

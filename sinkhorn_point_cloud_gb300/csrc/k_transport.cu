@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     const bool ok = i < p.nr;
     const float* R = p.R + (size_t)b * p.nr * d;
     const float* Cl = p.Cl + (size_t)b * p.nc * d;
-    const float* Vb = p.V + (size_t)b * p.nc * c;
+    const float* Vb = p.V + (size_t)b * p.nc * p.ldv;
 
     for (int e = threadIdx.x; e < TR_T * d; e += TR_T) {
         const int r = e / d, k = e % d;
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         }
         for (int e = threadIdx.x; e < TR_CT * c; e += TR_T) {
             const int jj = e / c, k = e % c, j = base + jj;
-            vs[jj * c + k] = (j < c_end) ? Vb[(size_t)j * c + k] : 0.f;
+            vs[jj * c + k] = (j < c_end) ? Vb[(size_t)j * p.ldv + k] : 0.f;
         }
         if (threadIdx.x < TR_CT) {
             const int j = base + threadIdx.x;
@@ -129,8 +129,8 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         }
     }
     if (ok) {
-        float* o = (p.split > 1 ? p.part + ((size_t)ch * p.B + b) * p.nr * c : p.out + (size_t)b * p.nr * c) +
-                   (size_t)i * c;
+        float* o = p.split > 1 ? p.part + (((size_t)ch * p.B + b) * p.nr + i) * c
+                               : p.out + ((size_t)b * p.nr + i) * p.ldo;
 #pragma unroll
         for (int k = 0; k < CV; ++k)
             if (k < c) o[k] = acc[k];
@@ -138,12 +138,28 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
 }
 
 // out = sum over chunks of the partial sums, in chunk order.
-__global__ void transport_merge_kernel(const float* part, long long count, int split, float* out) {
+__global__ void transport_merge_kernel(const float* part, long long count, int split, int c, int ldo, float* out) {
     const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     if (e >= count) return;
     float s = 0.f;
     for (int ch = 0; ch < split; ++ch) s += part[(size_t)ch * count + e];
-    out[e] = s;
+    out[(e / c) * ldo + e % c] = s;
+}
+
+__global__ void grad_finish_kernel(const float* P, const float* w, int B, int per_cloud, int d, float* g) {
+    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (i >= (long long)B * per_cloud) return;
+    const float wi = w ? w[i] : 1.f / (float)per_cloud;
+    for (int k = 0; k < d; ++k) g[i * d + k] = 2.f * (wi * P[i * d + k] - g[i * d + k]);
+}
+
+cudaError_t launch_grad_finish(const float* P, const float* w, int B, int per_cloud, int d, float* g,
+                               cudaStream_t st) {
+    const long long count = (long long)B * per_cloud;
+    if (count <= 0) return cudaSuccess;
+    count_launches(1);
+    grad_finish_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(P, w, B, per_cloud, d, g);
+    return cudaGetLastError();
 }
 
 size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk) {
@@ -164,7 +180,8 @@ size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* ch
 
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
     if (p.d < 1 || p.d > TR_MAXD || p.c < 1 || p.c > TR_MAXC || p.B < 1 || p.nr < 1 || p.nc < 1 || p.split < 1 ||
-        p.chunk < 1 || (long long)p.split * p.chunk < p.nc || (p.split > 1 && !p.part))
+        p.chunk < 1 || (long long)p.split * p.chunk < p.nc || (p.split > 1 && !p.part) || p.ldv < p.c ||
+        p.ldo < p.c)
         return cudaErrorInvalidValue;
     const size_t sm = tr_smem_bytes(p.d, p.c);
     dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
@@ -184,7 +201,8 @@ cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
     if (p.split > 1) {
         const long long count = (long long)p.B * p.nr * p.c;
         count_launches(1);
-        transport_merge_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(p.part, count, p.split, p.out);
+        transport_merge_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(p.part, count, p.split, p.c, p.ldo,
+                                                                                 p.out);
     }
     return cudaGetLastError();
 }

@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -834,7 +835,7 @@ int sot_transport_apply(const float* X, const float* Y, const float* a, const fl
     if (rc) return rc;
     const double kap = 1.0 / ((double)eps * SOT_LN2_D);
     TransportArgs p;
-    p.B = B; p.d = d; p.c = c; p.V = V; p.out = out;
+    p.B = B; p.d = d; p.c = c; p.V = V; p.out = out; p.ldv = c; p.ldo = c;
     p.kap_hi = (float)kap;
     p.kap_lo = (float)(kap - (double)p.kap_hi);
     if (side == 0) {
@@ -847,6 +848,43 @@ int sot_transport_apply(const float* X, const float* Y, const float* a, const fl
     if (nparts && !p.part) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
     cudaError_t e = launch_transport(p, cs);
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "transport launch failed: %s", cudaGetErrorString(e));
+    return SOT_OK;
+}
+
+int sot_grad_y(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+               const float* f, const float* g, float eps, float* grad_y, int flags, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (d > transport_max_d())
+        return fail(SOT_ERR_UNSUPPORTED, "sot_grad_y supports d <= %d (got %d)", transport_max_d(), d);
+    if (flags & ~SOT_COST_COSINE) return fail(SOT_ERR_INVALID_ARG, "unknown flag bits");
+    if (B > 0 && (!f || !g || !grad_y)) return fail(SOT_ERR_INVALID_ARG, "f, g and grad_y must not be NULL");
+    if (B == 0) return SOT_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const float* Yin = Y;
+    Scratch unit(cs);
+    rc = unit_points(flags, X, Y, B, n, m, d, unit, &X, &Y);
+    if (rc) return rc;
+    const double kap = 1.0 / ((double)eps * SOT_LN2_D);
+    // P^T X, 64 coordinates of X per product, into grad_y
+    for (int c0 = 0; c0 < d; c0 += transport_max_c()) {
+        TransportArgs p;
+        p.B = B; p.d = d; p.c = std::min(transport_max_c(), d - c0);
+        p.nr = m; p.nc = n; p.R = Y; p.Cl = X; p.fr = g; p.gc = f; p.wr = b; p.wc = a;
+        p.V = X + c0; p.ldv = d;
+        p.out = grad_y + c0; p.ldo = d;
+        p.kap_hi = (float)kap;
+        p.kap_lo = (float)(kap - (double)p.kap_hi);
+        const size_t nparts = transport_plan(B, p.nr, p.nc, p.c, device_sms(), &p.split, &p.chunk);
+        p.part = nparts ? unit.alloc<float>(nparts) : nullptr;
+        if (nparts && !p.part) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        cudaError_t e = launch_transport(p, cs);
+        if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "transport launch failed: %s", cudaGetErrorString(e));
+    }
+    SOT_CUDA(launch_grad_finish(Y, b, B, m, d, grad_y, cs));
+    if (flags & SOT_COST_COSINE) SOT_CUDA(launch_cosine_grad(Yin, (long long)B * m, d, grad_y, cs));
     return SOT_OK;
 }
 

@@ -19,8 +19,9 @@ struct TransportArgs {
     const float* gc;  // [B][nc] column potentials
     const float* wr;  // [B][nr] row weights, NULL = uniform 1/nr
     const float* wc;  // [B][nc] column weights, NULL = uniform 1/nc
-    const float* V;   // [B][nc][c]
-    float* out;       // [B][nr][c]
+    const float* V;   // [B][nc] rows of c values, row stride ldv (>= c)
+    float* out;       // [B][nr] rows of c values, row stride ldo (>= c)
+    int ldv, ldo;
     float kap_hi, kap_lo;  // 1 / (eps ln 2) as a float-float pair
     int split, chunk;      // columns in `split` chunks of `chunk` columns (one CTA each)
     float* part;           // [split][B][nr][c] partial sums when split > 1
@@ -32,5 +33,9 @@ int transport_max_c();
 // the floats of partial-sum scratch it needs (0 when split == 1).
 size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk);
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st);
+// g[k][j][:] <- 2 (w_j p_j - g[k][j][:]) for `count` points of d coordinates
+// (w NULL = uniform 1/per_cloud): the gradient from the transport product.
+cudaError_t launch_grad_finish(const float* P, const float* w, int B, int per_cloud, int d, float* g,
+                               cudaStream_t st);
 
 }  // namespace sot

@@ -104,3 +104,10 @@ def test_transport_arguments_rejected_on_host(lib):
     assert tr(p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.0, p, 4, 0, p, 0, NULL) == binding.SOT_ERR_INVALID_ARG
     assert tr(p, p, NULL, NULL, 1, 5, 6, 300, p, p, 0.1, p, 4, 0, p, 0, NULL) == binding.SOT_ERR_UNSUPPORTED
     assert tr(p, p, NULL, NULL, 0, 5, 6, 3, NULL, NULL, 0.1, NULL, 4, 0, NULL, 0, NULL) == binding.SOT_OK  # B = 0
+
+
+def test_grad_y_arguments_rejected_on_host(lib):
+    p = C.c_void_p(16)
+    assert lib.sot_grad_y(p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.1, NULL, 0, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_grad_y(p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.1, p, 1 << 3, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert lib.sot_grad_y(p, p, NULL, NULL, 1, 5, 6, 300, p, p, 0.1, p, 0, NULL) == binding.SOT_ERR_UNSUPPORTED

@@ -99,3 +99,25 @@ def test_transport_marginals_and_adjoint(sot):
     lhs, rhs = np.sum(U * PV, axis=(1, 2)), np.sum(PtU * V, axis=(1, 2))
     scale = np.sum(np.abs(U) * np.abs(PV), axis=(1, 2))
     assert float(np.max(np.abs(lhs - rhs) / scale)) < 1e-5
+
+
+@pytest.mark.parametrize("w,n,m,d,eps,cosine", [
+    (2, 300, 257, 3, 0.01, False),    # point clouds
+    (4, 200, 190, 8, 0.1, False),     # d = 8
+    (4, 300, 280, 100, 0.5, False),   # d = 100: two products of 64 + 36 coordinates
+    (4, 260, 300, 16, 0.05, True),    # cosine cost
+])
+def test_grad_y(sot, orc, w, n, m, d, eps, cosine):
+    """grad_y = 2 (b_j y_j - sum_i P_ij x_i) vs the oracle's gradient of the
+    swapped problem (Y, X, b, a, g, f), which is the same quantity."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(w, B=2, n=n, m=m, d=d)
+    fl = sot.SOT_COST_COSINE if cosine else 0
+    f, g = potentials(sot, X, Y, a, b, eps, 60, fl)
+    gy = host(sot.sot_grad_y(dev(X), dev(Y), dev(a), dev(b), f, g, eps, flags=fl))
+    fh, gh = host(f), host(g)
+    with orc.cost("cosine" if cosine else "sqeuclidean"):
+        ref = [orc.plan_apply(Y[k], X[k], b[k], a[k], gh[k], fh[k], eps)["grad"] for k in range(2)]
+    err = max(normwise(gy[k], ref[k]) for k in range(2))
+    print(f"grad_y {err:.2e}")
+    assert err < TOL, err
