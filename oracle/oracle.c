@@ -24,7 +24,9 @@
  *   - "From Theory to Throughput: CUDA-Optimized APML", Abstract and
  *     Innovation: negligible assignments are thresholded, the plan is kept in
  *     COO form with bidirectional symmetrisation, gradients are kept on the
- *     stored support.
+ *     stored support; on that support the loss runs an adaptive softmax,
+ *     bidirectional symmetrisation and Sinkhorn normalisation (orc_apml_coo;
+ *     the page does not give the temperature: the caller passes it).
  *
  * Readings where the pages are silent (each one listed in the design notes):
  *   - one iteration = f-half then g-half using the new f (Gauss-Seidel), from
@@ -47,7 +49,7 @@
  * invariances, shift invariance, finite differences of the dual objective.
  *
  * Compile: cc -O2 -fopenmp -fPIC -shared oracle.c -lm  (no fast-math).
- * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..10) that
+ * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..11) that
  * the test suite uses to show that the pins catch plausible mistakes.
  */
 #include <math.h>
@@ -591,6 +593,72 @@ long long orc_coo(int n, int m, int d, const double *X, const double *Y,
 }
 
 /* Gradient on a stored support: grad_i = 2 sum_{(i,j) in S} P_ij (x_i - y_j). */
+/*
+ * Sparse APML on a stored support (row-major COO of one cloud: rows ascending,
+ * columns ascending within a row), temperature T, `iters` normalisations:
+ *   s_ij   = -C_ij / T                                    on the support
+ *   R_ij   = exp(s_ij) / sum_{j' in row i} exp(s_ij')      row softmax
+ *   K_ij   = exp(s_ij) / sum_{i' in column j} exp(s_i'j)   column softmax
+ *   P_ij   = (R_ij + K_ij) / 2                             bidirectional symmetrisation
+ *   repeat iters times: P_ij *= a_i / sum_j P_ij, then P_ij *= b_j / sum_i P_ij
+ *   loss   = sum P_ij C_ij
+ * (empty rows and columns are left alone).  vals receives P; loss is optional.
+ */
+int orc_apml_coo(int n, int m, int d, const double *X, const double *Y,
+                 const double *a, const double *b, long long nnz,
+                 const int *rows, const int *cols, double T, int iters,
+                 double *vals, double *loss) {
+    if (n <= 0 || m <= 0 || d <= 0 || !(T > 0) || iters < 0 || nnz < 0) return -1;
+    for (long long e = 0; e < nnz; ++e)
+        if (rows[e] < 0 || rows[e] >= n || cols[e] < 0 || cols[e] >= m) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(nnz > 0 ? nnz : 1));
+    double *rmax = (double *)malloc(sizeof(double) * (size_t)n);
+    double *rsum = (double *)malloc(sizeof(double) * (size_t)n);
+    double *cmax = (double *)malloc(sizeof(double) * (size_t)m);
+    double *csum = (double *)malloc(sizeof(double) * (size_t)m);
+    if (!s || !rmax || !rsum || !cmax || !csum) {
+        free(s); free(rmax); free(rsum); free(cmax); free(csum);
+        return -2;
+    }
+    for (int i = 0; i < n; ++i) { rmax[i] = -INFINITY; rsum[i] = 0.0; }
+    for (int j = 0; j < m; ++j) { cmax[j] = -INFINITY; csum[j] = 0.0; }
+    for (long long e = 0; e < nnz; ++e) {
+        s[e] = -cost_ij(X + (size_t)rows[e] * d, Y + (size_t)cols[e] * d, d) / T;
+        if (s[e] > rmax[rows[e]]) rmax[rows[e]] = s[e];
+        if (s[e] > cmax[cols[e]]) cmax[cols[e]] = s[e];
+    }
+    for (long long e = 0; e < nnz; ++e) {
+        rsum[rows[e]] += exp(s[e] - rmax[rows[e]]);
+        csum[cols[e]] += exp(s[e] - cmax[cols[e]]);
+    }
+    for (long long e = 0; e < nnz; ++e) {
+        const double r = exp(s[e] - rmax[rows[e]]) / rsum[rows[e]];
+        const double k = exp(s[e] - cmax[cols[e]]) / csum[cols[e]];
+#if ORC_MUTANT == 11
+        vals[e] = r; /* mutant: the column softmax is dropped */
+        (void)k;
+#else
+        vals[e] = 0.5 * (r + k);
+#endif
+    }
+    for (int it = 0; it < iters; ++it) {
+        for (int i = 0; i < n; ++i) rsum[i] = 0.0;
+        for (long long e = 0; e < nnz; ++e) rsum[rows[e]] += vals[e];
+        for (long long e = 0; e < nnz; ++e) vals[e] *= a[rows[e]] / rsum[rows[e]];
+        for (int j = 0; j < m; ++j) csum[j] = 0.0;
+        for (long long e = 0; e < nnz; ++e) csum[cols[e]] += vals[e];
+        for (long long e = 0; e < nnz; ++e) vals[e] *= b[cols[e]] / csum[cols[e]];
+    }
+    if (loss) {
+        double l = 0.0;
+        for (long long e = 0; e < nnz; ++e)
+            l += vals[e] * cost_ij(X + (size_t)rows[e] * d, Y + (size_t)cols[e] * d, d);
+        *loss = l;
+    }
+    free(s); free(rmax); free(rsum); free(cmax); free(csum);
+    return 0;
+}
+
 int orc_grad_support(int n, int m, int d, const double *X, const double *Y,
                      long long nnz, const int *rows, const int *cols,
                      const double *vals, double *grad) {

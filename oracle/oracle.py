@@ -77,6 +77,8 @@ class Oracle:
                               C.c_double, C.c_int, C.c_double, C.c_longlong, _ip, _ip, _dp, _dp]
         L.orc_coo.restype = C.c_longlong
         L.orc_grad_support.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, C.c_longlong, _ip, _ip, _dp, _dp]
+        L.orc_apml_coo.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, _dp, _dp, C.c_longlong, _ip, _ip,
+                                   C.c_double, C.c_int, _dp, _dp]
         L.orc_num_threads.restype = C.c_int
         L.orc_set_num_threads.argtypes = [C.c_int]
         L.orc_mutant.restype = C.c_int
@@ -282,6 +284,20 @@ class Oracle:
         if rc:
             raise ValueError("orc_grad_support: index out of range")
         return grad
+
+    def apml_coo(self, X, Y, a, b, rows, cols, T, iters):
+        """Sparse APML on a row-major support: (P values on the support, loss)."""
+        X, Y, a, b, n, m, d = self._prob(X, Y, a, b)
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        cols = np.ascontiguousarray(cols, dtype=np.int32)
+        vals = np.empty(len(rows))
+        loss = C.c_double(0)
+        rc = self.lib.orc_apml_coo(n, m, d, _ptr(X), _ptr(Y), _ptr(a), _ptr(b), len(rows),
+                                   rows.ctypes.data_as(_ip), cols.ctypes.data_as(_ip), float(T), int(iters),
+                                   _ptr(vals), C.byref(loss))
+        if rc:
+            raise ValueError(f"orc_apml_coo failed ({rc})")
+        return vals, loss.value
 
     # ---- batch helpers -----------------------------------------------
     def sinkhorn_batch(self, X, Y, a, b, eps, iters, clouds=None):

@@ -472,6 +472,68 @@ def pin_transport_adjoint(orc):
     PVW = orc.transport(X, Y, a, b, f, g, eps, 2.0 * V - W, side=0)
     _close(PVW, 2.0 * PV - PW, 1e-12, atol=1e-15, what="linearity")
 
+
+# ---- Sparse APML on a stored support ("From Theory to Throughput:
+# CUDA-Optimized APML", Abstract: adaptive softmax, bidirectional
+# symmetrisation and Sinkhorn normalisation run in COO form) ------------------
+
+def _dense_apml(C, a, b, T, iters):
+    """The same loss with dense numpy / scipy matrices (every pair stored)."""
+    from scipy.special import softmax
+    S = -C / T
+    P = 0.5 * (softmax(S, axis=1) + softmax(S, axis=0))
+    for _ in range(iters):
+        P = P * (a / P.sum(axis=1))[:, None]
+        P = P * (b / P.sum(axis=0))[None, :]
+    return P, float(np.sum(P * C))
+
+
+def pin_apml_dense_reduction(orc):
+    """With every pair stored, sparse APML equals the dense computation
+    (row and column softmax by scipy, symmetrisation, normalisations)."""
+    X, Y, a, b = _problem(31, 7, 9, 3)
+    C = ((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1)
+    rows, cols = np.divmod(np.arange(7 * 9), 9)
+    for T, iters in ((0.3, 0), (0.3, 5), (2.0, 20)):
+        vals, loss = orc.apml_coo(X, Y, a, b, rows, cols, T, iters)
+        P, L = _dense_apml(C, a, b, T, iters)
+        _close(vals, P.ravel(), 1e-12, what=f"dense reduction P (T={T}, iters={iters})")
+        _close(loss, L, 1e-12, what="dense reduction loss")
+
+
+def pin_apml_permutation_support(orc):
+    """One stored entry per row and per column (a permutation): both softmaxes
+    are 1, and after the normalisations every value is b of its column, so the
+    loss is sum_j b_j C_{sigma(j) j}."""
+    X, Y, a, b = _problem(32, 6, 6, 2)
+    sigma = np.array([3, 0, 5, 1, 4, 2])
+    rows = np.arange(6)
+    cols = sigma
+    C = ((X[rows] - Y[cols]) ** 2).sum(-1)
+    vals, loss = orc.apml_coo(X, Y, a, b, rows, cols, 0.1, 3)
+    _close(vals, b[cols], 1e-14, what="permutation values")
+    _close(loss, float(np.sum(b[cols] * C)), 1e-13, what="permutation loss")
+    vals0, _ = orc.apml_coo(X, Y, a, b, rows, cols, 0.1, 0)
+    _close(vals0, np.ones(6), 1e-15, what="softmaxes of single entries")
+
+
+def pin_apml_marginals_and_large_T(orc):
+    """On a thresholded support the last normalisation makes the column sums
+    exactly b; with every pair stored and T -> infinity both softmaxes are
+    uniform, so the plan is a x b and the loss the a x b average of C."""
+    X, Y, a, b = _problem(33, 10, 8, 3)
+    f, g = orc.sinkhorn(X, Y, a, b, [0.05], [200])
+    sup = orc.coo(X, Y, a, b, f, g, 0.05, 1e-6)
+    vals, _ = orc.apml_coo(X, Y, a, b, sup["rows"], sup["cols"], 0.05, 7)
+    col = np.zeros(8)
+    np.add.at(col, sup["cols"], vals)
+    present = np.isin(np.arange(8), sup["cols"])
+    _close(col[present], b[present], 1e-13, what="APML column marginals")
+    rows, cols = np.divmod(np.arange(10 * 8), 8)
+    C = ((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1)
+    _, loss = orc.apml_coo(X, Y, a, b, rows, cols, 1e9, 50)
+    _close(loss, float(a @ C @ b), 1e-7, what="large-T loss")
+
 ALL_PINS = [
     pin_closed_form_single_point,
     pin_two_point_closed_form,
@@ -492,4 +554,7 @@ ALL_PINS = [
     pin_transport_closed_form,
     pin_transport_marginals,
     pin_transport_adjoint,
+    pin_apml_dense_reduction,
+    pin_apml_permutation_support,
+    pin_apml_marginals_and_large_T,
 ]
