@@ -208,6 +208,28 @@ int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b,
  * element is the number of entries.  The call synchronises `stream` once to
  * read the check's result.
  */
+/*
+ * Sparse APML on a stored support ("From Theory to Throughput: CUDA-Optimized
+ * APML", Abstract and Innovation: an adaptive softmax, bidirectional
+ * symmetrisation and Sinkhorn normalisation run directly in COO form, and
+ * gradients are kept on the stored support).  The support is a row-major COO
+ * such as sot_plan_coo returns (rows ascending within a cloud, cloud-local
+ * int32 indices, int64 batch_offsets[B+1] from 0 to nnz; device arrays).
+ * With s_ij = -C_ij / T on the stored pairs:
+ *   P = (row softmax of s + column softmax of s) / 2, then `iters` times the
+ *   rows are scaled to sum to a_i and the columns to sum to b_j;
+ *   vals[nnz]  <- P on the support (fp32);
+ *   loss[B]    <- sum P_ij C_ij (may be NULL);
+ *   grad[B][n][d] <- 2 sum_j P_ij (x_i - y_j) on the support, P held fixed (may be NULL).
+ * T > 0 is the temperature (the page's adaptive temperature is not given; a
+ * caller passes one, e.g. eps).  Synchronises the stream (offsets are checked on
+ * the host; an unsorted or out-of-range support returns SOT_ERR_INVALID_ARG).
+ */
+int sot_apml_coo(const float* X, const float* Y, const float* a, const float* b,
+                 int B, int n, int m, int d, const int* rows, const int* cols,
+                 const long long* batch_offsets, long long nnz, float T, int iters,
+                 float* vals, float* loss, float* grad, void* stream);
+
 int sot_grad_x_coo(const float* X, const float* Y, int B, int n, int m, int d,
                    const int* rows, const int* cols, const float* vals,
                    const long long* batch_offsets, float* grad, void* stream);

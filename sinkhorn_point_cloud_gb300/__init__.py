@@ -4,7 +4,7 @@ The computation lives in libsot (C ABI: include/sot.h, CUDA sources in csrc/);
 ``binding`` marshals torch tensors into it, ``build`` compiles it in-tree and
 ``datagen`` draws the seeded synthetic workloads.
 """
-from .binding import (SOT_ERR_CAPACITY, SOT_ERR_CUDA, SOT_ERR_INVALID_ARG, SOT_ERR_NOMEM, SOT_ERR_NONFINITE,
+from .binding import (sot_apml_coo, SOT_ERR_CAPACITY, SOT_ERR_CUDA, SOT_ERR_INVALID_ARG, SOT_ERR_NOMEM, SOT_ERR_NONFINITE,
                       SOT_ERR_TIMEOUT, SOT_ERR_UNSUPPORTED, SOT_OK, SOT_PREC_AUTO, SOT_PREC_F16X3, SOT_PREC_FP32,
                       SOT_COST_COSINE, SOT_NO_CLUSTER, SOT_STAGE_EARLY_EXIT, SOT_TC_NO_SCREEN, SOT_WARM_START, SotError,
                       sot_check_inputs, sot_cost,

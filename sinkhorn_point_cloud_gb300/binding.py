@@ -98,6 +98,7 @@ def load(path: str | None = None):
         "sot_potentials_noalloc": [P, P, P, P, i, i, i, i, f, i, P, P, P],
         "sot_transport_apply": [P, P, P, P, i, i, i, i, P, P, f, P, i, i, P, i, P],
         "sot_grad_y": [P, P, P, P, i, i, i, i, P, P, f, P, i, P],
+        "sot_apml_coo": [P, P, P, P, i, i, i, i, P, P, P, ll, f, i, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -259,6 +260,21 @@ def sot_grad_y(X, Y, a, b, f, g, eps, flags=0, out=None, stream=None):
                            int(flags), _stream(stream))
     _check(rc, "sot_grad_y")
     return o
+
+
+def sot_apml_coo(X, Y, a, b, coo, T, iters=10, loss=True, grad=True, stream=None):
+    """Sparse APML on a stored support (``coo`` as sot_plan_coo returns it):
+    returns (vals [nnz], loss [B] or None, grad [B,n,d] or None)."""
+    X, Y, B, n, m, d = _shapes(X, Y, a, b)
+    nnz = int(coo["nnz"])
+    vals = torch.empty(max(nnz, 1), device=X.device, dtype=torch.float32)
+    lo = torch.empty(B, device=X.device, dtype=torch.float32) if loss else None
+    gr = torch.empty(B, n, d, device=X.device, dtype=torch.float32) if grad else None
+    rc = load().sot_apml_coo(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(coo["rows"]), _ptr(coo["cols"]),
+                             _ptr(coo["batch_offsets"]), nnz, float(T), int(iters), _ptr(vals), _ptr(lo), _ptr(gr),
+                             _stream(stream))
+    _check(rc, "sot_apml_coo")
+    return vals[:nnz], lo, gr
 
 
 def sot_cost(X, Y, a, b, f, g, eps, stream=None):

@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "sot.h"
+#include "apml.h"
 #include "tc.h"
 #include "transport.h"
 
@@ -976,6 +977,58 @@ int sot_grad_x_coo(const float* X, const float* Y, int B, int n, int m, int d, c
     SOT_CUDA(launch_grad_coo(X, Y, B, n, m, d, rows, cols, vals, batch_offsets, grad, status, cs));
     int h = 0;
     SOT_CUDA(cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, cs));
+    SOT_CUDA(cudaStreamSynchronize(cs));
+    if (h & SOT_DEV_BAD_COO) return fail(SOT_ERR_INVALID_ARG, "COO not row-sorted within a cloud or index out of range");
+    return SOT_OK;
+}
+
+int sot_apml_coo(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                 const int* rows, const int* cols, const long long* batch_offsets, long long nnz, float T, int iters,
+                 float* vals, float* loss, float* grad, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!(T > 0.f) || !std::isfinite(T)) return fail(SOT_ERR_INVALID_ARG, "T must be finite and > 0");
+    if (iters < 0) return fail(SOT_ERR_INVALID_ARG, "iters must be >= 0");
+    if (nnz < 0 || nnz >= (1LL << 31)) return fail(SOT_ERR_INVALID_ARG, "nnz must satisfy 0 <= nnz < 2^31");
+    if (B == 0) return SOT_OK;
+    if (!batch_offsets || (nnz > 0 && (!rows || !cols || !vals)))
+        return fail(SOT_ERR_INVALID_ARG, "batch_offsets, rows, cols and vals must not be NULL");
+    cudaStream_t cs = (cudaStream_t)stream;
+    // the offsets bound every index the kernels take: check them on the host first
+    std::vector<long long> off((size_t)B + 1);
+    SOT_CUDA(cudaMemcpyAsync(off.data(), batch_offsets, sizeof(long long) * off.size(), cudaMemcpyDeviceToHost, cs));
+    SOT_CUDA(cudaStreamSynchronize(cs));
+    if (off[0] != 0 || off[B] != nnz) return fail(SOT_ERR_INVALID_ARG, "batch_offsets must run from 0 to nnz");
+    for (int k = 0; k < B; ++k)
+        if (off[k + 1] < off[k]) return fail(SOT_ERR_INVALID_ARG, "batch_offsets must be non-decreasing");
+    Scratch S(cs);
+    ApmlArgs p;
+    p.B = B; p.n = n; p.m = m; p.d = d;
+    p.X = X; p.Y = Y; p.a = a; p.b = b;
+    p.rows = rows; p.cols = cols; p.off = batch_offsets;
+    p.inv_T = 1.f / T;
+    p.iters = iters;
+    p.vals = vals;
+    p.loss = loss;
+    p.cost = S.alloc<float>((size_t)nnz);
+    p.rstart = S.alloc<int>((size_t)B * n);
+    p.rend = S.alloc<int>((size_t)B * n);
+    p.cmax = S.alloc<unsigned>((size_t)B * m);
+    p.csum = S.alloc<double>((size_t)B * m);
+    p.loss_part = S.alloc<float>((size_t)B * n);
+    p.status = S.alloc<int>(1);
+    if (!p.cost || !p.rstart || !p.rend || !p.cmax || !p.csum || !p.loss_part || !p.status)
+        return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    SOT_CUDA(cudaMemsetAsync(p.rstart, 0, sizeof(int) * (size_t)B * n, cs));
+    SOT_CUDA(cudaMemsetAsync(p.rend, 0, sizeof(int) * (size_t)B * n, cs));
+    SOT_CUDA(cudaMemsetAsync(p.cmax, 0, sizeof(unsigned) * (size_t)B * m, cs));
+    SOT_CUDA(cudaMemsetAsync(p.status, 0, sizeof(int), cs));
+    cudaError_t e = launch_apml(p, cs);
+    if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "APML launch failed: %s", cudaGetErrorString(e));
+    if (grad) SOT_CUDA(launch_grad_coo(X, Y, B, n, m, d, rows, cols, vals, batch_offsets, grad, p.status, cs));
+    int h = 0;
+    SOT_CUDA(cudaMemcpyAsync(&h, p.status, sizeof(int), cudaMemcpyDeviceToHost, cs));
     SOT_CUDA(cudaStreamSynchronize(cs));
     if (h & SOT_DEV_BAD_COO) return fail(SOT_ERR_INVALID_ARG, "COO not row-sorted within a cloud or index out of range");
     return SOT_OK;

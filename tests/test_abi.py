@@ -111,3 +111,14 @@ def test_grad_y_arguments_rejected_on_host(lib):
     assert lib.sot_grad_y(p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.1, NULL, 0, NULL) == binding.SOT_ERR_INVALID_ARG
     assert lib.sot_grad_y(p, p, NULL, NULL, 1, 5, 6, 3, p, p, 0.1, p, 1 << 3, NULL) == binding.SOT_ERR_INVALID_ARG
     assert lib.sot_grad_y(p, p, NULL, NULL, 1, 5, 6, 300, p, p, 0.1, p, 0, NULL) == binding.SOT_ERR_UNSUPPORTED
+
+
+def test_apml_arguments_rejected_on_host(lib):
+    p = C.c_void_p(16)
+    ap = lib.sot_apml_coo
+    assert ap(p, p, NULL, NULL, 1, 5, 6, 3, p, p, p, 10, 0.0, 3, p, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert b"T must be" in lib.sot_last_error()
+    assert ap(p, p, NULL, NULL, 1, 5, 6, 3, p, p, p, 10, 0.1, -1, p, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert ap(p, p, NULL, NULL, 1, 5, 6, 3, p, p, p, -1, 0.1, 3, p, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert ap(p, p, NULL, NULL, 1, 5, 6, 3, p, p, NULL, 10, 0.1, 3, p, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
+    assert ap(p, p, NULL, NULL, 0, 5, 6, 3, NULL, NULL, NULL, 0, 0.1, 3, NULL, NULL, NULL, NULL) == binding.SOT_OK

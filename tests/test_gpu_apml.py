@@ -1,0 +1,98 @@
+"""Sparse APML on a stored support ("From Theory to Throughput: CUDA-Optimized
+APML", Abstract and Innovation) through the C ABI vs the fp64 oracle, entry by
+entry: supports from sot_plan_coo on the sphere + rotation recipe (d = 3) and
+a Gaussian d = 8 problem, every pair stored (tau = 0), 0 and several
+normalisations; invalid supports are rejected.  Tolerance: normwise 1e-4."""
+import numpy as np
+import pytest
+
+from gpu_util import TOL, dev, host, normwise
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sot():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sinkhorn_point_cloud_gb300 as s
+    from sinkhorn_point_cloud_gb300 import build
+    build.build()
+    return s
+
+
+def support(sot, X, Y, a, b, eps, iters, tau, weighted):
+    Xd, Yd = dev(X), dev(Y)
+    ad, bd = (dev(a), dev(b)) if weighted else (None, None)
+    f, g = sot.sot_potentials(Xd, Yd, ad, bd, eps=eps, iters=iters)
+    coo = sot.sot_plan_coo(Xd, Yd, ad, bd, f, g, eps, threshold=tau, dirs=3)
+    torch.cuda.synchronize()
+    return Xd, Yd, ad, bd, coo
+
+
+def check(sot, orc, X, Y, a, b, eps, iters, tau, T, norm_iters, weighted=False):
+    Xd, Yd, ad, bd, coo = support(sot, X, Y, a, b, eps, iters, tau, weighted)
+    vals, loss, grad = sot.sot_apml_coo(Xd, Yd, ad, bd, coo, T, norm_iters)
+    torch.cuda.synchronize()
+    vals, loss, grad = host(vals), host(loss), host(grad)
+    rows, cols, off = host(coo["rows"]).astype(np.int64), host(coo["cols"]).astype(np.int64), \
+        host(coo["batch_offsets"]).astype(np.int64)
+    ev = el = eg = 0.0
+    for k in range(X.shape[0]):
+        s0, s1 = off[k], off[k + 1]
+        aw = a[k] if weighted else None
+        bw = b[k] if weighted else None
+        rv, rl = orc.apml_coo(X[k], Y[k], aw, bw, rows[s0:s1], cols[s0:s1], T, norm_iters)
+        rg = orc.grad_support(X[k], Y[k], rows[s0:s1], cols[s0:s1], rv)
+        ev = max(ev, normwise(vals[s0:s1], rv))
+        el = max(el, abs(loss[k] - rl) / abs(rl))
+        eg = max(eg, normwise(grad[k], rg))
+    print(f"nnz {int(coo['nnz'])}: vals {ev:.2e} loss {el:.2e} grad {eg:.2e}")
+    assert ev < TOL and el < TOL and eg < TOL, (ev, el, eg)
+
+
+@pytest.mark.parametrize("norm_iters", [0, 5])
+def test_apml_point_clouds(sot, orc, norm_iters):
+    """The 8-cloud COO recipe at 2 clouds of 512 points, support at tau = 1e-8."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(5, B=2, n=512)
+    check(sot, orc, X, Y, a, b, 5e-3, 300, 1e-8, 5e-3, norm_iters)
+
+
+def test_apml_d8_weighted(sot, orc):
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=300, m=270, d=8)
+    check(sot, orc, X, Y, a, b, 0.1, 60, 1e-6, 0.1, 8, weighted=True)
+
+
+def test_apml_every_pair_stored(sot, orc):
+    """tau = 0 keeps every pair: the dense special case, ragged sizes."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(2, B=2, n=70, m=53)
+    check(sot, orc, X, Y, a, b, 0.05, 40, 0.0, 0.05, 10)
+
+
+def test_apml_rejects_invalid_support(sot):
+    """An out-of-range column and unsorted rows are reported; every pass skips
+    the bad indices, so nothing outside the arrays is touched first."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(2, B=1, n=64, m=60)
+    Xd, Yd, _, _, coo = support(sot, X, Y, a, b, 0.05, 20, 1e-6, False)
+    nnz = int(coo["nnz"])
+    assert nnz > 4
+    bad = dict(coo)
+    bad["cols"] = coo["cols"].clone()
+    bad["cols"][nnz // 2] = 60  # out of range
+    with pytest.raises(sot.SotError) as ei:
+        sot.sot_apml_coo(Xd, Yd, None, None, bad, 0.05, 3)
+    assert ei.value.status == sot.SOT_ERR_INVALID_ARG
+    bad = dict(coo)
+    bad["rows"] = coo["rows"].flip(0).contiguous()  # rows descending
+    with pytest.raises(sot.SotError) as ei:
+        sot.sot_apml_coo(Xd, Yd, None, None, bad, 0.05, 3)
+    assert ei.value.status == sot.SOT_ERR_INVALID_ARG
+    # the valid support still runs afterwards
+    vals, loss, _ = sot.sot_apml_coo(Xd, Yd, None, None, coo, 0.05, 3, grad=False)
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(host(vals))) and np.isfinite(host(loss)).all()
