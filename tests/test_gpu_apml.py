@@ -96,3 +96,23 @@ def test_apml_rejects_invalid_support(sot):
     vals, loss, _ = sot.sot_apml_coo(Xd, Yd, None, None, coo, 0.05, 3, grad=False)
     torch.cuda.synchronize()
     assert np.all(np.isfinite(host(vals))) and np.isfinite(host(loss)).all()
+
+
+def test_apml_full_workload_sampled_clouds(sot, orc):
+    """The 8-cloud COO workload at full size (8 x 8192 points, the bench's
+    support and 10 normalisations); the oracle follows clouds 0 and 7."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(5)
+    Xd, Yd, _, _, coo = support(sot, X, Y, a, b, 5e-3, 300, 1e-8, False)
+    vals, loss, grad = sot.sot_apml_coo(Xd, Yd, None, None, coo, 5e-3, 10)
+    torch.cuda.synchronize()
+    vals, loss, grad = host(vals), host(loss), host(grad)
+    rows, cols = host(coo["rows"]).astype(np.int64), host(coo["cols"]).astype(np.int64)
+    off = host(coo["batch_offsets"]).astype(np.int64)
+    for k in (0, 7):
+        s0, s1 = off[k], off[k + 1]
+        rv, rl = orc.apml_coo(X[k], Y[k], None, None, rows[s0:s1], cols[s0:s1], 5e-3, 10)
+        rg = orc.grad_support(X[k], Y[k], rows[s0:s1], cols[s0:s1], rv)
+        ev, el, eg = normwise(vals[s0:s1], rv), abs(loss[k] - rl) / abs(rl), normwise(grad[k], rg)
+        print(f"cloud {k}: nnz {s1 - s0} vals {ev:.2e} loss {el:.2e} grad {eg:.2e}")
+        assert ev < TOL and el < TOL and eg < TOL, (k, ev, el, eg)

@@ -121,3 +121,22 @@ def test_grad_y(sot, orc, w, n, m, d, eps, cosine):
     err = max(normwise(gy[k], ref[k]) for k in range(2))
     print(f"grad_y {err:.2e}")
     assert err < TOL, err
+
+
+def test_transport_full_size_sampled_rows(sot, orc):
+    """The n = m = 70000, d = 64 recipe at full size (the bench's launch
+    configuration: 3 column chunks), potentials after 3 iterations; P V with
+    4 columns against the oracle on 12 sampled rows (a row of P V needs only
+    its own point, potential and weight, and every column)."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4)
+    f, g = potentials(sot, X, Y, a, b, 0.1, 3)
+    rng = np.random.default_rng(94)
+    V = rng.normal(size=(1, 70000, 4)).astype(np.float32)
+    out = host(sot.sot_transport_apply(dev(X), dev(Y), dev(a), dev(b), f, g, 0.1, dev(V), side=0))
+    rows = np.sort(rng.choice(70000, size=12, replace=False))
+    fh, gh = host(f), host(g)
+    ref = orc.transport(X[0][rows], Y[0], a[0][rows], b[0], fh[0][rows], gh[0], 0.1, V[0], side=0)
+    err = normwise(out[0][rows], ref)
+    print(f"full size, sampled rows: {err:.2e}")
+    assert err < TOL, err
