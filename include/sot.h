@@ -136,7 +136,9 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
  *   cost[k]     = sum_ij P_ij C_ij                        (may be NULL)
  *   grad[k][i]  = 2 (a_i x_i - sum_j P_ij y_j)  [B][n][d] (may be NULL)
  *   rowsum[k][i]= sum_j P_ij                    [B][n]    (may be NULL)
- * Asynchronous.  flags: SOT_PREC_* (0 = auto).
+ * Asynchronous.  flags: SOT_PREC_* (0 = auto), optionally | SOT_COST_COSINE (the
+ * potentials must then be those of the cosine cost; the gradient is carried back
+ * through x/|x|).
  */
 int sot_plan_apply(const float* X, const float* Y, const float* a, const float* b,
                    int B, int n, int m, int d, const float* f, const float* g, float eps,
