@@ -150,7 +150,9 @@ __global__ void apml_loss_kernel(ApmlArgs p) {
 
 cudaError_t launch_apml(const ApmlArgs& p, cudaStream_t st) {
     if (p.B < 1 || p.n < 1 || p.m < 1 || p.d < 1 || !(p.inv_T > 0.f) || p.iters < 0) return cudaErrorInvalidValue;
-    const dim3 ge(4 * 152 / p.B + 1, p.B), gr((p.n + AM_T / 32 - 1) / (AM_T / 32), p.B);
+    // per-entry passes: ~2048 blocks in all, so that every SM keeps enough loads
+    // in flight (each thread's loop is a chain of dependent loads)
+    const dim3 ge(2048 / p.B + 1, p.B), gr((p.n + AM_T / 32 - 1) / (AM_T / 32), p.B);
     const size_t csum_bytes = sizeof(double) * (size_t)p.B * p.m;
     count_launches(1);
     apml_prep_kernel<<<ge, AM_T, 0, st>>>(p);
