@@ -116,3 +116,25 @@ def test_apml_full_workload_sampled_clouds(sot, orc):
         ev, el, eg = normwise(vals[s0:s1], rv), abs(loss[k] - rl) / abs(rl), normwise(grad[k], rg)
         print(f"cloud {k}: nnz {s1 - s0} vals {ev:.2e} loss {el:.2e} grad {eg:.2e}")
         assert ev < TOL and el < TOL and eg < TOL, (k, ev, el, eg)
+
+
+def test_apml_empty_row_and_column(sot, orc):
+    """A support built by hand with every pair of row 5 and of column 7 left
+    out (and the rest of two rows): empty rows and columns stay empty, the
+    others are normalised as usual."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(2, B=1, n=40, m=36)
+    rows, cols = np.divmod(np.arange(40 * 36), 36)
+    keep = (rows != 5) & (cols != 7) & ~((rows == 9) & (cols > 3)) & ~((rows == 20) & (cols % 2 == 0))
+    rows, cols = rows[keep].astype(np.int32), cols[keep].astype(np.int32)
+    nnz = len(rows)
+    coo = {"rows": dev(rows), "cols": dev(cols), "batch_offsets": dev(np.array([0, nnz], dtype=np.int64)),
+           "nnz": nnz}
+    vals, loss, grad = sot.sot_apml_coo(dev(X), dev(Y), None, None, coo, 0.05, 6)
+    torch.cuda.synchronize()
+    rv, rl = orc.apml_coo(X[0], Y[0], None, None, rows, cols, 0.05, 6)
+    rg = orc.grad_support(X[0], Y[0], rows, cols, rv)
+    ev, el, eg = normwise(host(vals), rv), abs(host(loss)[0] - rl) / abs(rl), normwise(host(grad)[0], rg)
+    print(f"empty row/column: vals {ev:.2e} loss {el:.2e} grad {eg:.2e}")
+    assert ev < TOL and el < TOL and eg < TOL, (ev, el, eg)
+    assert np.all(host(grad)[0][5] == 0.0)

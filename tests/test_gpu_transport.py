@@ -140,3 +140,22 @@ def test_transport_full_size_sampled_rows(sot, orc):
     err = normwise(out[0][rows], ref)
     print(f"full size, sampled rows: {err:.2e}")
     assert err < TOL, err
+
+
+def test_transport_largest_d_and_c(sot, orc):
+    """d = 256 and c = 64, the largest the call takes (175 KB of shared memory per CTA)."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=150, m=140, d=256)
+    check(sot, orc, X, Y, a, b, 2.0, 30, 64, 95)
+
+
+def test_grad_y_largest_d(sot, orc):
+    """d = 256: four transport products of 64 coordinates."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=120, m=110, d=256)
+    f, g = potentials(sot, X, Y, a, b, 2.0, 30)
+    gy = host(sot.sot_grad_y(dev(X), dev(Y), dev(a), dev(b), f, g, 2.0))
+    ref = orc.plan_apply(Y[0], X[0], b[0], a[0], host(g)[0], host(f)[0], 2.0)["grad"]
+    err = normwise(gy[0], ref)
+    print(f"grad_y d=256 {err:.2e}")
+    assert err < TOL, err
