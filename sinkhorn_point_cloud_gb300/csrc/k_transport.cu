@@ -4,7 +4,9 @@
 // such transport-vector and transport-matrix products).
 //
 // One thread per row; column tiles (coordinates transposed, so a row value is
-// reused by four columns) and the tile's V rows sit in shared memory.  Columns
+// reused by a group of W columns: 8 when d > 8, 4 for the low dimensions where
+// the exact evaluation, not the screen, dominates) and the tile's V rows sit
+// in shared memory.  Columns
 // are split into chunks so that the grid fills the SMs; chunk partial sums are
 // added in chunk order by a second kernel (deterministic).  Each
 // pair is first scored in fp32 in the direct form: log2(P_ij / w_i) is about
@@ -39,8 +41,9 @@ static size_t tr_smem_bytes(int d, int c) {
     return sizeof(float) * ((size_t)TR_T * tr_ldx(d) + (size_t)d * TR_YS + (size_t)TR_CT * c + 2 * TR_CT);
 }
 
-template <int CV>
+template <int CV, int W>
 __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
+    static_assert(W == 4 || W == 8, "column group of 4 or 8");
     extern __shared__ float smem[];
     const int d = p.d, c = p.c, ldx = tr_ldx(d);
     float* xs = smem;                 // [TR_T][ldx] this CTA's rows
@@ -91,23 +94,28 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         }
         __syncthreads();
         if (!ok) continue;
-        for (int j4 = 0; j4 < TR_CT; j4 += 4) {
-            // fp32 direct-form distances of four columns, two per packed instruction
-            float2 c01 = make_float2(0.f, 0.f), c23 = c01;
+        for (int jg = 0; jg < TR_CT; jg += W) {
+            // fp32 direct-form distances of W columns, two per packed instruction
+            float2 cp[W / 2];
+#pragma unroll
+            for (int h = 0; h < W / 2; ++h) cp[h] = make_float2(0.f, 0.f);
             for (int k = 0; k < d; ++k) {
                 const float2 xx = make_float2(xr[k], xr[k]);
-                const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + j4);
-                const float2 t01 = fadd2(xx, make_float2(y4.x, y4.y));
-                const float2 t23 = fadd2(xx, make_float2(y4.z, y4.w));
-                c01 = ffma2(t01, t01, c01);
-                c23 = ffma2(t23, t23, c23);
-            }
-            const float C4[4] = {c01.x, c01.y, c23.x, c23.y};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int jj = j4 + u;
+                for (int q = 0; q < W / 4; ++q) {
+                    const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + jg + 4 * q);
+                    const float2 t0 = fadd2(xx, make_float2(y4.x, y4.y));
+                    const float2 t1 = fadd2(xx, make_float2(y4.z, y4.w));
+                    cp[2 * q] = ffma2(t0, t0, cp[2 * q]);
+                    cp[2 * q + 1] = ffma2(t1, t1, cp[2 * q + 1]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < W; ++u) {
+                const int jj = jg + u;
                 // screen: log2(P_ij / w_i) estimated in fp32 (-inf past the last column)
-                const float est = fmaf(p.kap_hi, fi + gs[jj] - C4[u], ls[jj]);
+                const float cu = (u & 1) ? cp[u >> 1].y : cp[u >> 1].x;
+                const float est = fmaf(p.kap_hi, fi + gs[jj] - cu, ls[jj]);
                 if (!(est > sig)) continue;
                 // exact: C_ij from exact differences and squares (float-float)
                 float2 C2 = make_float2(0.f, 0.f);
@@ -187,11 +195,11 @@ cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
     dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
 #define SOT_TR_CASE(CVV)                                                                              \
     {                                                                                                 \
-        cudaError_t e = cudaFuncSetAttribute(transport_kernel<CVV>,                                   \
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);   \
+        auto kern = (p.d > 8) ? transport_kernel<CVV, 8> : transport_kernel<CVV, 4>;                  \
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
         if (e != cudaSuccess) return e;                                                               \
         count_launches(1);                                                                            \
-        transport_kernel<CVV><<<grid, block, sm, st>>>(p);                                            \
+        kern<<<grid, block, sm, st>>>(p);                                                             \
     }
     if (p.c <= 1) SOT_TR_CASE(1)
     else if (p.c <= 4) SOT_TR_CASE(4)
