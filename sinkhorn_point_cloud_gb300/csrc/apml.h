@@ -26,6 +26,7 @@ struct ApmlArgs {
     int* rend;                 // [B][n] one past its last entry (zero on entry)
     unsigned* cmax;            // [B][m] ord-encoded column maxima of s (zero on entry)
     double* csum;              // [B][m] column sums
+    float* cfac;               // [B][m] per-column factor (1 / sum, or b_j / sum)
     float* loss_part;          // [B][n] per-row loss terms
     int* status;               // SOT_DEV_BAD_COO on an invalid support
 };

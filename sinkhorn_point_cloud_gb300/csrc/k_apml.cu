@@ -84,6 +84,21 @@ __global__ void apml_rowsoft_kernel(ApmlArgs p) {
     }
 }
 
+// Per column, once: the fp32 factor the entries are scaled by (the fp64 pipe
+// is slow here, so no entry pass converts or divides in fp64).
+// mode 0: 1 / (column sum of the softmax exponentials); mode 1: b_j / (column sum).
+__global__ void apml_colfactor_kernel(ApmlArgs p, int mode) {
+    const long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (c >= (long long)p.B * p.m) return;
+    const double cs = p.csum[c];
+    if (mode == 0) {
+        p.cfac[c] = cs > 0.0 ? (float)(1.0 / cs) : 0.f;
+    } else {
+        const double bj = p.b ? (double)p.b[c] : 1.0 / (double)p.m;
+        p.cfac[c] = cs > 0.0 ? (float)(bj / cs) : 1.f;
+    }
+}
+
 // P = (R + K) / 2 on every entry.
 __global__ void apml_sym_kernel(ApmlArgs p) {
     const int b = blockIdx.y;
@@ -93,7 +108,7 @@ __global__ void apml_sym_kernel(ApmlArgs p) {
         const int j = p.cols[e];
         if (j < 0 || j >= p.m) continue;
         const size_t cj = (size_t)b * p.m + j;
-        const float k = expf(-p.cost[e] * p.inv_T - ord_decode(p.cmax[cj])) / (float)p.csum[cj];
+        const float k = expf(-p.cost[e] * p.inv_T - ord_decode(p.cmax[cj])) * p.cfac[cj];
         p.vals[e] = 0.5f * (p.vals[e] + k);
     }
 }
@@ -127,10 +142,7 @@ __global__ void apml_colscale_kernel(ApmlArgs p) {
     for (long long e = lo + blockIdx.x * (long long)blockDim.x + threadIdx.x; e < hi; e += stride) {
         const int j = p.cols[e];
         if (j < 0 || j >= p.m) continue;
-        const size_t cj = (size_t)b * p.m + j;
-        const float bj = p.b ? p.b[cj] : 1.f / (float)p.m;
-        const double cs = p.csum[cj];
-        if (cs > 0.0) p.vals[e] = (float)((double)p.vals[e] * ((double)bj / cs));
+        p.vals[e] *= p.cfac[(size_t)b * p.m + j];
     }
 }
 
@@ -160,8 +172,11 @@ cudaError_t launch_apml(const ApmlArgs& p, cudaStream_t st) {
         cudaError_t e = cudaMemsetAsync(p.csum, 0, csum_bytes, st);
         if (e != cudaSuccess) return e;
     }
+    const unsigned gf = (unsigned)(((long long)p.B * p.m + AM_T - 1) / AM_T);
     count_launches(1);
     apml_rowsoft_kernel<<<gr, AM_T, 0, st>>>(p);
+    count_launches(1);
+    apml_colfactor_kernel<<<gf, AM_T, 0, st>>>(p, 0);
     count_launches(1);
     apml_sym_kernel<<<ge, AM_T, 0, st>>>(p);
     for (int it = 0; it < p.iters; ++it) {
@@ -169,6 +184,8 @@ cudaError_t launch_apml(const ApmlArgs& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         count_launches(1);
         apml_rowscale_kernel<<<gr, AM_T, 0, st>>>(p);
+        count_launches(1);
+        apml_colfactor_kernel<<<gf, AM_T, 0, st>>>(p, 1);
         count_launches(1);
         apml_colscale_kernel<<<ge, AM_T, 0, st>>>(p);
     }

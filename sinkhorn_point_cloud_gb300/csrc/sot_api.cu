@@ -1016,9 +1016,10 @@ int sot_apml_coo(const float* X, const float* Y, const float* a, const float* b,
     p.rend = S.alloc<int>((size_t)B * n);
     p.cmax = S.alloc<unsigned>((size_t)B * m);
     p.csum = S.alloc<double>((size_t)B * m);
+    p.cfac = S.alloc<float>((size_t)B * m);
     p.loss_part = S.alloc<float>((size_t)B * n);
     p.status = S.alloc<int>(1);
-    if (!p.cost || !p.rstart || !p.rend || !p.cmax || !p.csum || !p.loss_part || !p.status)
+    if (!p.cost || !p.rstart || !p.rend || !p.cmax || !p.csum || !p.cfac || !p.loss_part || !p.status)
         return fail(SOT_ERR_NOMEM, "scratch allocation failed");
     SOT_CUDA(cudaMemsetAsync(p.rstart, 0, sizeof(int) * (size_t)B * n, cs));
     SOT_CUDA(cudaMemsetAsync(p.rend, 0, sizeof(int) * (size_t)B * n, cs));
