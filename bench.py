@@ -166,6 +166,12 @@ def parse_clocks(text: str):
 
 
 # ---- distributed helpers ------------------------------------------------------
+def clocks_csv_path():
+    """Where to keep the raw nvidia-smi samples of the timed region (the JSON
+    line carries their summary either way): $SOT_CLOCKS_CSV, or nowhere."""
+    return os.environ.get("SOT_CLOCKS_CSV") or None
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -310,8 +316,7 @@ def run_gpu(args, ws, rank, local):
     sot.sot_profile_read()
     sot.sot_profile_enable(True)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
-        else None
+    clk_path = clocks_csv_path()
     barrier(ws)
     torch.cuda.synchronize()
     info = None
@@ -495,8 +500,7 @@ def run_transport(args, ws, rank, local):
     torch.cuda.synchronize()
     launches0 = sot.sot_kernel_launches()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
-        else None
+    clk_path = clocks_csv_path()
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local, clk_path) as cs:
@@ -616,8 +620,7 @@ def run_apml(args, ws, rank, local):
     torch.cuda.synchronize()
     launches0 = sot.sot_kernel_launches()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk_path = os.path.join(ROOT, "gpurun_out", "clocks.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
-        else None
+    clk_path = clocks_csv_path()
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local, clk_path) as cs:
