@@ -3,14 +3,15 @@
 // weighted sum; its HVP paragraph builds the Hessian-vector product from
 // such transport-vector and transport-matrix products).
 //
-// One thread per row; column tiles (coordinates transposed, so a row value is
-// reused by a group of W columns: 8 when d > 8, 4 for the low dimensions where
-// the exact evaluation, not the screen, dominates) and the tile's V rows sit
-// in shared memory.  Columns
-// are split into chunks so that the grid fills the SMs; chunk partial sums are
-// added in chunk order by a second kernel (deterministic).  Each
-// pair is first scored in fp32 in the direct form: log2(P_ij / w_i) is about
-// log2 w'_j + kappa (f_i + g_j - C_ij).  A pair below -(26 + log2 nc) - 4 is
+// One thread per row.  Column tiles (coordinates transposed, so that a row
+// value is reused by a group of W columns: 8 when d > 8, 4 in the low
+// dimensions, where the exact evaluation and not the screen dominates) and the
+// tile's V rows sit in shared memory.  Columns are split into chunks so that
+// the grid fills the SMs; a second kernel adds the chunks' partial sums in
+// chunk order (deterministic).
+//
+// Each pair is first scored in fp32 in the direct form: log2(P_ij / w_i) is
+// about log2 w'_j + kappa (f_i + g_j - C_ij).  A pair below -(26 + log2 nc) - 4 is
 // skipped: its weight is under 2^-30 / nc of w_i, so all skipped pairs of a row
 // together carry less than 2^-30 of it (the 4 units cover the fp32 estimate's
 // own error many times over), far below fp32 resolution of the sum.  Every
