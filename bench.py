@@ -269,10 +269,12 @@ def run_gpu(args, ws, rank, local):
     iters = w.get("iters", 0)
     if args.n:
         n = m = args.n
+    if args.d:
+        d = args.d
     if args.iters:
         iters = args.iters
     # weak scaling: every rank solves its own problem(s), seeded by rank
-    X, Y, a, b = datagen.make_batch(wid, B=B, n=n, m=m, clouds=range(rank * B, rank * B + B))
+    X, Y, a, b = datagen.make_batch(wid, B=B, n=n, m=m, d=d, clouds=range(rank * B, rank * B + B))
     weighted = w["kind"] == "gauss"  # the other recipes use uniform weights (NULL in the ABI)
     host_in = [torch.from_numpy(v).pin_memory() for v in ((X, Y, a, b) if weighted else (X, Y))]
     dev_in = [v.to(dev) for v in host_in]
@@ -674,6 +676,7 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, choices=sorted(datagen.WORKLOADS), default=WORKLOAD_ID,
                     help="1-5; the default (4: n=m=70000, d=64) is the headline configuration")
     ap.add_argument("--n", type=int, default=0, help="override n = m (testing only)")
+    ap.add_argument("--d", type=int, default=0, help="override d (the Gaussian recipe; testing only)")
     ap.add_argument("--iters", type=int, default=0, help="override the iteration count (testing only)")
     ap.add_argument("--ref-step-s", type=float, default=3.0, help="seconds of oracle work per reference step")
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0,

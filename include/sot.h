@@ -56,7 +56,7 @@ enum sot_status {
 
 /* ---- schedule flags ---------------------------------------------------- */
 enum sot_flags {
-    SOT_PREC_AUTO = 0,          /* d <= 3: fp32 FMA; d % 16 == 0, 16 <= d <= 256: tensor cores (fp16 x3); else fp32 */
+    SOT_PREC_AUTO = 0,          /* d <= 3: point path (fp32 FMA); d = 64: tensor cores (fp16 x3); else fp32 FMA (d <= 256) */
     SOT_PREC_FP32 = 1,          /* fp32 FMA contraction for any d */
     SOT_PREC_F16X3 = 2,         /* tcgen05 fp16 products hi*hi + hi*lo + lo*hi (fp32-class accuracy) */
     SOT_PREC_MASK = 3,

@@ -144,7 +144,7 @@ enum Path { PATH_POINT = 0, PATH_DENSE = 1, PATH_TC = 2 };
 int choose_path(int d, int flags, Path* out) {
     const int prec = flags & SOT_PREC_MASK;
     if (prec == SOT_PREC_F16X3) {
-        if (!tc_supported(d)) return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d %% 16 == 0, 16 <= d <= %d", tc_max_d());
+        if (!tc_supported(d)) return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d = %d (got d = %d)", tc_max_d(), d);
         *out = PATH_TC;
         return SOT_OK;
     }

@@ -174,3 +174,11 @@ def test_bitwise_reproducible(sot):
     f1, g1 = sot.sot_potentials(Xd, Yd, eps=0.01, iters=20)
     f2, g2 = sot.sot_potentials(Xd, Yd, eps=0.01, iters=20)
     assert torch.equal(f1, f2) and torch.equal(g1, g2)
+
+
+def test_dense_fp32_path_largest_d(sot, orc):
+    """d = 256, the fp32 path's largest dimension (above the tensor path's d = 64)."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=200, m=170, d=256)
+    assert sot.sot_select_path(256, 0) == 1
+    print(check(sot, orc, X, Y, a, b, 2.0, 60))
