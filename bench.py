@@ -453,20 +453,56 @@ def run_gpu(args, ws, rank, local):
     return 0
 
 
-def run_transport(args, ws, rank, local):
-    """Transport-matrix products (sot_transport_apply): one step is P V (V with
-    `args.transport` columns) and P^T U on a workload, from potentials solved
-    once before the timed region.  Same timing rules as the solver line."""
+def setup_device(ws, local):
+    """One GPU per rank (NCCL process group for N > 1), the library built."""
     import torch
-    import sinkhorn_point_cloud_gb300 as sot
     from sinkhorn_point_cloud_gb300 import build
 
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     build.build()
+    return torch.device("cuda", local)
+
+
+def time_steps(step, args, ws, local, dev):
+    """Warm-up, then args.steps steps bracketed by CUDA events on the current
+    stream, L2 flushed before each and clocks sampled meanwhile.  Returns
+    (max-over-ranks seconds, clock summary, kernel launches)."""
+    import torch
+    import sinkhorn_point_cloud_gb300 as sot
+
+    stream = torch.cuda.current_stream(dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches0 = sot.sot_kernel_launches()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local, clocks_csv_path()) as cs:
+        for k in range(args.steps):
+            flush_buf.zero_()
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = sot.sot_kernel_launches() - launches0
+    t_max = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, ws, dev)
+    return t_max, cs.summary(), launches
+
+
+def run_transport(args, ws, rank, local):
+    """Transport-matrix products (sot_transport_apply): one step is P V (V with
+    `args.transport` columns) and P^T U on a workload, from potentials solved
+    once before the timed region.  Same timing rules as the solver line."""
+    import torch
+    import sinkhorn_point_cloud_gb300 as sot
+
+    dev = setup_device(ws, local)
     wid = args.workload
     w = datagen.WORKLOADS[wid]
     B, n, m, d, eps = w["B"], w["n"], w["m"], w["d"], w["eps"]
@@ -487,7 +523,6 @@ def run_transport(args, ws, rank, local):
     outs = [torch.empty(B, n, c, device=dev), torch.empty(B, m, c, device=dev)]
     stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
     gy = torch.empty(B, m, d, device=dev) if args.grad_y else None
 
     def step(v, u):
@@ -497,25 +532,7 @@ def run_transport(args, ws, rank, local):
         o1 = sot.sot_transport_apply(Xd, Yd, ad, bd, f, g, eps, u, side=1, flags=flags, out=outs[1])
         return [o0, o1]
 
-    for _ in range(args.warmup):
-        step(V, U)
-    torch.cuda.synchronize()
-    launches0 = sot.sot_kernel_launches()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk_path = clocks_csv_path()
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local, clk_path) as cs:
-        for k in range(args.steps):
-            flush_buf.zero_()
-            ev[k][0].record(stream)
-            step(V, U)
-            ev[k][1].record(stream)
-        torch.cuda.synchronize()
-    barrier(ws)
-    launches = sot.sot_kernel_launches() - launches0
-    t_max = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, ws, dev)
-    clocks = cs.summary()
+    t_max, clocks, launches = time_steps(lambda: step(V, U), args, ws, local, dev)
     # end to end: V and U from pinned host memory, both products back to the host
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = 0.0
@@ -589,14 +606,8 @@ def run_apml(args, ws, rank, local):
     gradient).  Same timing rules as the solver line."""
     import torch
     import sinkhorn_point_cloud_gb300 as sot
-    from sinkhorn_point_cloud_gb300 import build
 
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build.build()
+    dev = setup_device(ws, local)
     wid = args.workload
     w = datagen.WORKLOADS[wid]
     B, n, m, d, eps = w["B"], w["n"], w["m"], w["d"], w["eps"]
@@ -611,31 +622,8 @@ def run_apml(args, ws, rank, local):
     coo = sot.sot_plan_coo(Xd, Yd, ad, bd, f, g, eps, threshold=w.get("tau", 1e-8), dirs=3)
     nnz = int(coo["nnz"])
     K = args.apml
-    stream = torch.cuda.current_stream(dev)
-    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        return sot.sot_apml_coo(Xd, Yd, ad, bd, coo, eps, K)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    launches0 = sot.sot_kernel_launches()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk_path = clocks_csv_path()
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local, clk_path) as cs:
-        for k in range(args.steps):
-            flush_buf.zero_()
-            ev[k][0].record(stream)
-            step()
-            ev[k][1].record(stream)
-        torch.cuda.synchronize()
-    barrier(ws)
-    launches = sot.sot_kernel_launches() - launches0
-    t_max = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3, ws, dev)
-    clocks = cs.summary()
+    t_max, clocks, launches = time_steps(lambda: sot.sot_apml_coo(Xd, Yd, ad, bd, coo, eps, K), args, ws, local,
+                                         dev)
     if rank != 0:
         return 0
     pk, pk_kind = peaks()

@@ -14,8 +14,11 @@
  *   Weights must be > 0 and finite, each a[k] and b[k] summing to one.
  * - stream: a cudaStream_t passed as void* (NULL = legacy default stream).
  *   Every call is stream-ordered.  Calls are asynchronous unless documented
- *   otherwise; scratch memory is taken with cudaMallocAsync / cudaFreeAsync on
- *   `stream` and released before the call returns its status.
+ *   otherwise; scratch memory is taken stream-ordered on `stream` and released
+ *   before the call returns its status.  It comes from a pool per device that
+ *   the library creates on first use and keeps for the life of the process;
+ *   the pool holds up to 2 GiB of released scratch for later calls and
+ *   returns the rest to the driver.
  * - Every call returns an int status (SOT_OK = 0 or a negative SOT_ERR_*)
  *   and never throws or aborts.  Arguments are checked on the host before
  *   anything is launched; on error, output contents are unspecified except
@@ -276,7 +279,7 @@ int sot_profile_read_kinds(long long* launches_host, double* ms_host);
  * library until the process exits; a problem whose scratch would not fit is
  * rejected with SOT_ERR_INVALID_ARG (sot_last_error() gives the bytes it would
  * need) before anything runs, and d > 3 gives SOT_ERR_UNSUPPORTED.  The call
- * makes no cudaMalloc / cudaFree / cudaMallocAsync call.
+ * makes no cudaMalloc / cudaFree / cudaMallocAsync / cudaMallocFromPoolAsync call.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call reuses the same array and clears what

@@ -51,6 +51,41 @@ int fail(int code, const char* fmt, ...) {
             return fail(SOT_ERR_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(_e), __FILE__, __LINE__); \
     } while (0)
 
+// Bytes of freed scratch the library's pool keeps for later calls.
+constexpr unsigned long long SCRATCH_KEEP_BYTES = 2ull << 30;
+
+// One stream-ordered pool per device, owned by the library.  A device's
+// default pool keeps no freed memory across a synchronisation, so every call
+// would map its scratch afresh; this one keeps up to SCRATCH_KEEP_BYTES.
+// NULL when the pool cannot be made (the caller then uses the default pool).
+cudaMemPool_t scratch_pool() {
+    static cudaMemPool_t pools[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps pr;
+        std::memset(&pr, 0, sizeof(pr));
+        pr.allocType = cudaMemAllocationTypePinned;
+        pr.handleTypes = cudaMemHandleTypeNone;
+        pr.location.type = cudaMemLocationTypeDevice;
+        pr.location.id = dev;
+        cudaMemPool_t mp = nullptr;
+        if (cudaMemPoolCreate(&mp, &pr) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        unsigned long long keep = SCRATCH_KEEP_BYTES;
+        if (cudaMemPoolSetAttribute(mp, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) cudaGetLastError();
+        pools[dev] = mp;
+    }
+    return pools[dev];
+}
+
 // Stream-ordered scratch: every allocation is released on the same stream
 // when the owning call returns.
 struct Scratch {
@@ -75,7 +110,10 @@ struct Scratch {
             arena_used = off + count * sizeof(T);
             return reinterpret_cast<T*>(arena + off);
         }
-        if (cudaMallocAsync(&p, count * sizeof(T), st) != cudaSuccess) {
+        cudaMemPool_t mp = scratch_pool();
+        const cudaError_t e = mp ? cudaMallocFromPoolAsync(&p, count * sizeof(T), mp, st)
+                                 : cudaMallocAsync(&p, count * sizeof(T), st);
+        if (e != cudaSuccess) {
             cudaGetLastError();
             return nullptr;
         }
