@@ -20,7 +20,10 @@
  *     P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps) applied to Y gives the
  *     gradient 2(a_i x_i - sum_j P_ij y_j) and the cost sum_ij P_ij C_ij;
  *     applied to any matrix V it gives the transport-matrix products
- *     P V and P^T U that the page's streaming HVP is built from.
+ *     P V and P^T U that the page's streaming HVP is built from; the HVP
+ *     itself (orc_hvp) is the Hessian of the converged loss with respect to
+ *     X applied to V, by implicit differentiation of the marginal conditions
+ *     (the page gives no formula: this is the plain reading).
  *   - "From Theory to Throughput: CUDA-Optimized APML", Abstract and
  *     Innovation: negligible assignments are thresholded, the plan is kept in
  *     COO form with bidirectional symmetrisation, gradients are kept on the
@@ -46,10 +49,12 @@
  * problems, the attention-form identity, marginals and duality at
  * convergence, brute-force assignment on tiny clouds, the d = 1 sorted
  * matching, the large-eps closed form, translation / rotation / swap
- * invariances, shift invariance, finite differences of the dual objective.
+ * invariances, shift invariance, finite differences of the dual objective,
+ * and for the HVP finite differences of the gradient, second differences of
+ * the dual, symmetry and the n = 1 and large-eps limits.
  *
  * Compile: cc -O2 -fopenmp -fPIC -shared oracle.c -lm  (no fast-math).
- * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..11) that
+ * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..12) that
  * the test suite uses to show that the pins catch plausible mistakes.
  */
 #include <math.h>
@@ -671,4 +676,139 @@ int orc_grad_support(int n, int m, int d, const double *X, const double *Y,
             grad[(size_t)i * d + k] += 2.0 * vals[e] * (X[(size_t)i * d + k] - Y[(size_t)j * d + k]);
     }
     return 0;
+}
+
+/*
+ * Hessian-vector product of the entropic OT loss with respect to X
+ * ("FlashSinkhorn", Methodologie 3, HVP paragraph: the page streams the
+ * product as transport-vector and transport-matrix products and gives no
+ * formula; this is the plain reading, written out densely).
+ *
+ * At the optimum the loss's gradient is G_i = 2 sum_j P_ij (x_i - y_j).
+ * P depends on X through C and through the optimal potentials.  Moving X
+ * along V (t -> X + t V) changes, to first order,
+ *   C_ij  by  Cd_ij = 2 (x_i - y_j) . v_i
+ *   P_ij  by  P_ij (fd_i + gd_j - Cd_ij) / eps,
+ * where (fd, gd) keep both marginals of P fixed:
+ *   r_i fd_i + sum_j P_ij gd_j = alpha_i := sum_j P_ij Cd_ij
+ *   sum_i P_ij fd_i + c_j gd_j = beta_j  := sum_i P_ij Cd_ij
+ * (r, c: the row and column sums of P).  The system is singular along
+ * (fd + t, gd - t), which leaves the change of P unchanged.  Eliminating fd:
+ *   S gd = beta - P^T (alpha / r),  S = diag(c) - P^T diag(1/r) P,
+ * S has the constant vector as its null space; adding (mean c / m) 1 1^T
+ * makes it positive definite and picks the solution with sum gd = 0
+ * (Cholesky).  Then fd_i = (alpha_i - sum_j P_ij gd_j) / r_i and
+ *   (H V)_i = 2 r_i v_i + (2 / eps) sum_j P_ij (fd_i + gd_j - Cd_ij) (x_i - y_j).
+ * Dense: O(n m + m^2) memory and O(n m^2 + m^3) time, small problems only.
+ * Squared-Euclidean cost only (returns -1 under the cosine cost).
+ * fd [n] and gd [m] may be NULL.
+ */
+int orc_hvp(int n, int m, int d, const double *X, const double *Y,
+            const double *a, const double *b, const double *f,
+            const double *g, double eps, const double *V, double *out,
+            double *fd_out, double *gd_out) {
+    if (n <= 0 || m <= 0 || d <= 0 || !(eps > 0) || g_cost != 0) return -1;
+    const size_t nm = (size_t)n * m;
+    double *P = (double *)malloc(sizeof(double) * nm);
+    double *Cd = (double *)malloc(sizeof(double) * nm);
+    double *S = (double *)malloc(sizeof(double) * (size_t)m * m);
+    double *r = (double *)calloc((size_t)n, sizeof(double));
+    double *al = (double *)calloc((size_t)n, sizeof(double));
+    double *fd = (double *)calloc((size_t)n, sizeof(double));
+    double *c = (double *)calloc((size_t)m, sizeof(double));
+    double *be = (double *)calloc((size_t)m, sizeof(double));
+    double *gd = (double *)calloc((size_t)m, sizeof(double));
+    int rc = 0;
+    if (!P || !Cd || !S || !r || !al || !fd || !c || !be || !gd) {
+        rc = -2;
+        goto done;
+    }
+    /* the plan, the change of the cost, and their row and column sums */
+    for (int i = 0; i < n; ++i) {
+        const double *xi = X + (size_t)i * d, *vi = V + (size_t)i * d;
+        for (int j = 0; j < m; ++j) {
+            const double *yj = Y + (size_t)j * d;
+            const double p = exp((f[i] + g[j] - cost_ij(xi, yj, d)) / eps + log(a[i]) + log(b[j]));
+            double cd = 0.0;
+            for (int k = 0; k < d; ++k) cd += 2.0 * (xi[k] - yj[k]) * vi[k];
+            P[(size_t)i * m + j] = p;
+            Cd[(size_t)i * m + j] = cd;
+            r[i] += p;
+            c[j] += p;
+            al[i] += p * cd;
+            be[j] += p * cd;
+        }
+    }
+    /* Schur complement on gd, the gauge fixed by the rank-one term */
+    {
+        double cmean = 0.0;
+        for (int j = 0; j < m; ++j) cmean += c[j];
+        cmean /= m;
+        const double shift = cmean / m;
+        for (int j = 0; j < m; ++j)
+            for (int l = 0; l <= j; ++l) {
+                double s = (j == l ? c[j] : 0.0) + shift;
+                for (int i = 0; i < n; ++i) s -= P[(size_t)i * m + j] * P[(size_t)i * m + l] / r[i];
+                S[(size_t)j * m + l] = s;
+                S[(size_t)l * m + j] = s;
+            }
+        for (int j = 0; j < m; ++j) {
+#if ORC_MUTANT == 12
+            gd[j] = 0.0; /* mutant: the column potentials are held fixed */
+#else
+            double s = be[j];
+            for (int i = 0; i < n; ++i) s -= P[(size_t)i * m + j] * al[i] / r[i];
+            gd[j] = s;
+#endif
+        }
+#if ORC_MUTANT != 12
+        /* Cholesky S = L L^T in place (lower triangle), then two triangular solves */
+        for (int j = 0; j < m; ++j) {
+            double s = S[(size_t)j * m + j];
+            for (int k = 0; k < j; ++k) s -= S[(size_t)j * m + k] * S[(size_t)j * m + k];
+            if (!(s > 0.0)) {
+                rc = -3;
+                goto done;
+            }
+            const double ljj = sqrt(s);
+            S[(size_t)j * m + j] = ljj;
+            for (int l = j + 1; l < m; ++l) {
+                double t = S[(size_t)l * m + j];
+                for (int k = 0; k < j; ++k) t -= S[(size_t)l * m + k] * S[(size_t)j * m + k];
+                S[(size_t)l * m + j] = t / ljj;
+            }
+        }
+        for (int j = 0; j < m; ++j) {
+            double s = gd[j];
+            for (int k = 0; k < j; ++k) s -= S[(size_t)j * m + k] * gd[k];
+            gd[j] = s / S[(size_t)j * m + j];
+        }
+        for (int j = m - 1; j >= 0; --j) {
+            double s = gd[j];
+            for (int k = j + 1; k < m; ++k) s -= S[(size_t)k * m + j] * gd[k];
+            gd[j] = s / S[(size_t)j * m + j];
+        }
+#endif
+    }
+    for (int i = 0; i < n; ++i) {
+        double s = al[i];
+        for (int j = 0; j < m; ++j) s -= P[(size_t)i * m + j] * gd[j];
+        fd[i] = s / r[i];
+    }
+    /* assembly */
+    for (int i = 0; i < n; ++i) {
+        const double *xi = X + (size_t)i * d, *vi = V + (size_t)i * d;
+        double *oi = out + (size_t)i * d;
+        for (int k = 0; k < d; ++k) oi[k] = 2.0 * r[i] * vi[k];
+        for (int j = 0; j < m; ++j) {
+            const double *yj = Y + (size_t)j * d;
+            const double w = 2.0 / eps * P[(size_t)i * m + j] * (fd[i] + gd[j] - Cd[(size_t)i * m + j]);
+            for (int k = 0; k < d; ++k) oi[k] += w * (xi[k] - yj[k]);
+        }
+    }
+    if (fd_out) memcpy(fd_out, fd, sizeof(double) * (size_t)n);
+    if (gd_out) memcpy(gd_out, gd, sizeof(double) * (size_t)m);
+done:
+    free(P); free(Cd); free(S); free(r); free(al); free(fd); free(c); free(be); free(gd);
+    return rc;
 }

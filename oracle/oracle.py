@@ -86,6 +86,8 @@ class Oracle:
         L.orc_transport.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, _dp, _dp, _dp, _dp, C.c_double, _dp,
                                     C.c_int, C.c_int, _dp]
         L.orc_get_cost.restype = C.c_int
+        L.orc_hvp.argtypes = [C.c_int, C.c_int, C.c_int, _dp, _dp, _dp, _dp, _dp, _dp, C.c_double, _dp, _dp, _dp,
+                              _dp]
 
     # ---- plumbing -----------------------------------------------------
     @staticmethod
@@ -238,6 +240,20 @@ class Oracle:
         if rc != 0:
             raise ValueError("orc_transport failed")
         return out[:, 0] if vec else out
+
+    def hvp(self, X, Y, a, b, f, g, eps, V, derivs=False):
+        """Hessian-vector product of the entropic OT loss with respect to X at
+        the potentials (f, g), applied to V [n, d] (see orc_hvp).  With
+        derivs=True also returns the potentials' first-order changes (fd, gd)."""
+        X, Y, a, b, n, m, d = self._prob(X, Y, a, b)
+        V = _d(V).reshape(n, d)
+        f, g = _d(f), _d(g)
+        out, fd, gd = np.empty((n, d)), np.empty(n), np.empty(m)
+        rc = self.lib.orc_hvp(n, m, d, _ptr(X), _ptr(Y), _ptr(a), _ptr(b), _ptr(f), _ptr(g), float(eps), _ptr(V),
+                              _ptr(out), _ptr(fd), _ptr(gd))
+        if rc != 0:
+            raise ValueError(f"orc_hvp failed ({rc})")
+        return (out, fd, gd) if derivs else out
 
     def objectives(self, X, Y, a, b, f, g, eps):
         X, Y, a, b, n, m, d = self._prob(X, Y, a, b)

@@ -534,6 +534,60 @@ def pin_apml_marginals_and_large_T(orc):
     _, loss = orc.apml_coo(X, Y, a, b, rows, cols, 1e9, 50)
     _close(loss, float(a @ C @ b), 1e-7, what="large-T loss")
 
+def pin_hvp_finite_differences(orc):
+    """The Hessian-vector product is the derivative of the converged gradient
+    along V: central differences of the gradient, of the potentials (up to
+    the constant gauge) and, independently of the gradient formula, second
+    differences of the dual objective <a,f> + <b,g> give V^T H V."""
+    X, Y, a, b = _problem(41, 7, 6, 3, scale=0.6)
+    eps = 0.3
+    V = _rng(42).normal(size=X.shape)
+
+    def solve(Xp):
+        return orc.sinkhorn(Xp, Y, a, b, [eps], [3000])
+
+    f, g = solve(X)
+    hv, fd, gd = orc.hvp(X, Y, a, b, f, g, eps, V, derivs=True)
+    h = 1e-5
+    fp, gp = solve(X + h * V)
+    fm, gm = solve(X - h * V)
+    grad = lambda Xp, fq, gq: orc.plan_apply(Xp, Y, a, b, fq, gq, eps)["grad"]
+    _close(hv, (grad(X + h * V, fp, gp) - grad(X - h * V, fm, gm)) / (2 * h), 1e-6, what="HVP vs gradient differences")
+    dfd, dgd = _gauge((fp - fm) / (2 * h), (gp - gm) / (2 * h), fd, gd)
+    _close(dfd, fd, 1e-6, atol=1e-9, what="potential derivative f")
+    _close(dgd, gd, 1e-6, atol=1e-9, what="potential derivative g")
+    hh = 1e-3
+    dual = lambda Xp: (lambda fg: a @ fg[0] + b @ fg[1])(solve(Xp))
+    second = (dual(X + hh * V) - 2 * dual(X) + dual(X - hh * V)) / hh ** 2
+    _close(np.sum(V * hv), second, 1e-5, what="V^T H V vs second differences of the dual")
+
+
+def pin_hvp_structure(orc):
+    """The Hessian is symmetric (U^T H V = V^T H U); the column marginals stay
+    fixed, so sum_i (H V)_i = 2 sum_i a_i v_i at convergence; rotating both
+    clouds and V rotates H V; n = m = 1 gives H V = 2 v; as eps -> infinity,
+    P -> a x b and H V -> 2 a_i v_i with error O(1 / eps)."""
+    X, Y, a, b = _problem(43, 9, 11, 3)
+    eps = 0.5
+    rng = _rng(44)
+    U, V = rng.normal(size=X.shape), rng.normal(size=X.shape)
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [3000])
+    hv = orc.hvp(X, Y, a, b, f, g, eps, V)
+    hu = orc.hvp(X, Y, a, b, f, g, eps, U)
+    _close(np.sum(U * hv), np.sum(V * hu), 1e-10, what="HVP symmetry")
+    _close(hv.sum(0), 2 * (a[:, None] * V).sum(0), 1e-10, what="HVP column sum")
+    th = 1.1
+    R = np.array([[1.0, 0, 0], [0, np.cos(th), -np.sin(th)], [0, np.sin(th), np.cos(th)]])
+    f3, g3 = orc.sinkhorn(X @ R.T, Y @ R.T, a, b, [eps], [3000])
+    _close(orc.hvp(X @ R.T, Y @ R.T, a, b, f3, g3, eps, V @ R.T), hv @ R.T, 1e-9, what="HVP rotation")
+    x, y, v = rng.normal(size=(1, 4)), rng.normal(size=(1, 4)), rng.normal(size=(1, 4))
+    f1, g1 = orc.sinkhorn(x, y, [1.0], [1.0], [0.2], [2])
+    _close(orc.hvp(x, y, [1.0], [1.0], f1, g1, 0.2, v), 2 * v, 1e-12, what="HVP at n = m = 1")
+    big = 1e6
+    fb, gb = orc.sinkhorn(X, Y, a, b, [big], [3])
+    _close(orc.hvp(X, Y, a, b, fb, gb, big, V), 2 * a[:, None] * V, 1e-4, what="HVP at large eps")
+
+
 ALL_PINS = [
     pin_closed_form_single_point,
     pin_two_point_closed_form,
@@ -557,4 +611,6 @@ ALL_PINS = [
     pin_apml_dense_reduction,
     pin_apml_permutation_support,
     pin_apml_marginals_and_large_T,
+    pin_hvp_finite_differences,
+    pin_hvp_structure,
 ]

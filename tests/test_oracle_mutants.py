@@ -6,7 +6,8 @@ transposed, gradient missing a_i, wrong sign of g in the plan, Jacobi instead
 of Gauss-Seidel order, log-sum-exp without the max added back, a coordinate
 dropped from the cost, a cosine cost that leaves y unnormalised, a transport
 product that weights its pairs with the wrong row weight, a sparse APML that drops
-the column softmax.
+the column softmax, a Hessian-vector product that holds the column potentials
+fixed.
 """
 import pytest
 
@@ -16,7 +17,7 @@ from oracle import oracle as O
 MUTANTS = {1: "drops log b", 2: "sign of C", 3: "weights transposed", 4: "grad without a_i",
            5: "sign of g in plan", 6: "Jacobi order", 7: "LSE without max", 8: "cost drops a coordinate",
            9: "cosine without y normalised", 10: "transport with the wrong row weight",
-           11: "APML without the column softmax"}
+           11: "APML without the column softmax", 12: "HVP with the column potentials fixed"}
 
 
 @pytest.mark.parametrize("k", sorted(MUTANTS), ids=lambda k: MUTANTS[k])
