@@ -135,11 +135,34 @@ def _stream(stream):
     return C.c_void_p(s.cuda_stream)
 
 
+def _want(t, name, count, dev, dtype=torch.float32):
+    """A tensor the caller supplies must be contiguous, of ``dtype``, on ``dev``
+    and hold exactly ``count`` elements (None: any count), since the library
+    reads or writes that many."""
+    if t is None:
+        return t
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if count is not None and t.numel() != count:
+        raise ValueError(f"{name} must hold {count} elements, got shape {tuple(t.shape)}")
+    if t.device != dev:
+        raise ValueError(f"{name} must be on {dev}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
 def _shapes(X, Y, a, b):
+    if not isinstance(X, torch.Tensor) or not isinstance(Y, torch.Tensor):
+        raise TypeError("X and Y must be torch.Tensors")
     if X.dim() == 2:
         X = X.unsqueeze(0)
     if Y.dim() == 2:
         Y = Y.unsqueeze(0)
+    if X.dim() != 3 or Y.dim() != 3:
+        raise ValueError("X must be [B,n,d] or [n,d], Y [B,m,d] or [m,d]")
     B, n, d = X.shape
     B2, m, d2 = Y.shape
     if B != B2 or d != d2:
@@ -148,7 +171,16 @@ def _shapes(X, Y, a, b):
         raise ValueError("a must be [B, n]")
     if b is not None and tuple(b.shape) not in ((B, m), (m,) if B == 1 else (B, m)):
         raise ValueError("b must be [B, m]")
+    dev = X.device
+    _want(X, "X", B * n * d, dev)
+    _want(Y, "Y", B * m * d, dev)
+    _want(a, "a", B * n, dev)
+    _want(b, "b", B * m, dev)
     return X, Y, B, n, m, d
+
+
+def _potentials_args(f, g, B, n, m, dev):
+    return _want(f, "f", B * n, dev), _want(g, "g", B * m, dev)
 
 
 def sot_version() -> int:
@@ -173,6 +205,7 @@ def sot_potentials(X, Y, a=None, b=None, eps=0.1, iters=100, f=None, g=None, str
     X, Y, B, n, m, d = _shapes(X, Y, a, b)
     f = torch.empty(B, n, device=X.device, dtype=torch.float32) if f is None else f
     g = torch.empty(B, m, device=X.device, dtype=torch.float32) if g is None else g
+    _potentials_args(f, g, B, n, m, X.device)
     rc = load().sot_potentials(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, float(eps), int(iters), _ptr(f),
                                _ptr(g), _stream(stream))
     _check(rc, "sot_potentials")
@@ -186,6 +219,7 @@ def sot_potentials_noalloc(X, Y, a=None, b=None, eps=0.1, iters=100, f=None, g=N
     X, Y, B, n, m, d = _shapes(X, Y, a, b)
     f = torch.empty(B, n, device=X.device, dtype=torch.float32) if f is None else f
     g = torch.empty(B, m, device=X.device, dtype=torch.float32) if g is None else g
+    _potentials_args(f, g, B, n, m, X.device)
     rc = load().sot_potentials_noalloc(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, float(eps), int(iters),
                                        _ptr(f), _ptr(g), _stream(stream))
     _check(rc, "sot_potentials_noalloc")
@@ -201,6 +235,7 @@ def sot_potentials_ex(X, Y, a=None, b=None, eps=0.1, eps_init=None, eps_factor=0
         raise ValueError("warm start needs f and g")
     f = torch.empty(B, n, device=X.device, dtype=torch.float32) if f is None else f
     g = torch.empty(B, m, device=X.device, dtype=torch.float32) if g is None else g
+    _potentials_args(f, g, B, n, m, X.device)
     s = sot_schedule(float(eps), float(eps if eps_init is None else eps_init), float(eps_factor),
                      int(iters_per_stage), int(max_iters), float(tol), int(flags))
     st = None
@@ -221,12 +256,18 @@ def sot_potentials_ex(X, Y, a=None, b=None, eps=0.1, eps_init=None, eps_factor=0
 
 
 def sot_plan_apply(X, Y, a, b, f, g, eps, cost=True, grad=True, rowsum=False, flags=0, stream=None):
-    """Returns (cost [B] or None, grad [B,n,d] or None, rowsum [B,n] or None)."""
+    """Returns (cost [B] or None, grad [B,n,d] or None, rowsum [B,n] or None).
+    Each of cost, grad, rowsum is True (allocate), False/None (skip) or a
+    preallocated tensor to write into."""
     X, Y, B, n, m, d = _shapes(X, Y, a, b)
     dev = X.device
-    c = torch.empty(B, device=dev, dtype=torch.float32) if cost is True else (cost or None)
-    gr = torch.empty(B, n, d, device=dev, dtype=torch.float32) if grad is True else (grad or None)
-    r = torch.empty(B, n, device=dev, dtype=torch.float32) if rowsum is True else (rowsum or None)
+    pick = lambda want, shape: torch.empty(*shape, device=dev, dtype=torch.float32) if want is True else \
+        (None if want is None or want is False else want)
+    c, gr, r = pick(cost, (B,)), pick(grad, (B, n, d)), pick(rowsum, (B, n))
+    _potentials_args(f, g, B, n, m, dev)
+    _want(c, "cost", B, dev)
+    _want(gr, "grad", B * n * d, dev)
+    _want(r, "rowsum", B * n, dev)
     rc = load().sot_plan_apply(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g), float(eps),
                                _ptr(c), _ptr(gr), _ptr(r), int(flags), _stream(stream))
     _check(rc, "sot_plan_apply")
@@ -246,6 +287,8 @@ def sot_transport_apply(X, Y, a, b, f, g, eps, V, side=0, flags=0, out=None, str
         raise ValueError(f"V must have shape [B, {rows_in}, c] for side {side}")
     c = V3.shape[2]
     o = torch.empty(B, rows_out, c, device=X.device, dtype=torch.float32) if out is None else out
+    _potentials_args(f, g, B, n, m, X.device)
+    _want(o, "out", B * rows_out * c, X.device)
     rc = load().sot_transport_apply(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g),
                                     float(eps), _ptr(V3), int(c), int(side), _ptr(o), int(flags), _stream(stream))
     _check(rc, "sot_transport_apply")
@@ -256,6 +299,8 @@ def sot_grad_y(X, Y, a, b, f, g, eps, flags=0, out=None, stream=None):
     """Gradient with respect to Y: 2 (b_j y_j - sum_i P_ij x_i), [B, m, d]."""
     X, Y, B, n, m, d = _shapes(X, Y, a, b)
     o = torch.empty(B, m, d, device=X.device, dtype=torch.float32) if out is None else out
+    _potentials_args(f, g, B, n, m, X.device)
+    _want(o, "out", B * m * d, X.device)
     rc = load().sot_grad_y(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g), float(eps), _ptr(o),
                            int(flags), _stream(stream))
     _check(rc, "sot_grad_y")
@@ -267,6 +312,9 @@ def sot_apml_coo(X, Y, a, b, coo, T, iters=10, loss=True, grad=True, stream=None
     returns (vals [nnz], loss [B] or None, grad [B,n,d] or None)."""
     X, Y, B, n, m, d = _shapes(X, Y, a, b)
     nnz = int(coo["nnz"])
+    _want(coo["rows"], "coo rows", nnz, X.device, torch.int32)
+    _want(coo["cols"], "coo cols", nnz, X.device, torch.int32)
+    _want(coo["batch_offsets"], "coo batch_offsets", B + 1, X.device, torch.int64)
     vals = torch.empty(max(nnz, 1), device=X.device, dtype=torch.float32)
     lo = torch.empty(B, device=X.device, dtype=torch.float32) if loss else None
     gr = torch.empty(B, n, d, device=X.device, dtype=torch.float32) if grad else None
@@ -295,6 +343,7 @@ def sot_plan_coo(X, Y, a, b, f, g, eps, threshold=1e-8, dirs=3, capacity=None, s
     With capacity None the call runs twice if needed (count, then write)."""
     X, Y, B, n, m, d = _shapes(X, Y, a, b)
     dev = X.device
+    _potentials_args(f, g, B, n, m, dev)
     L = load()
     off = torch.empty(B + 1, device=dev, dtype=torch.int64)
     nnz = C.c_longlong(0)
@@ -319,13 +368,14 @@ def sot_plan_coo(X, Y, a, b, f, g, eps, threshold=1e-8, dirs=3, capacity=None, s
 
 
 def sot_grad_x_coo(X, Y, rows, cols, vals, batch_offsets, grad=None, stream=None):
-    if X.dim() == 2:
-        X = X.unsqueeze(0)
-    if Y.dim() == 2:
-        Y = Y.unsqueeze(0)
-    B, n, d = X.shape
-    m = Y.shape[1]
+    X, Y, B, n, m, d = _shapes(X, Y, None, None)
+    dev = X.device
+    _want(rows, "rows", None, dev, torch.int32)
+    _want(cols, "cols", rows.numel(), dev, torch.int32)
+    _want(vals, "vals", rows.numel(), dev)
+    _want(batch_offsets, "batch_offsets", B + 1, dev, torch.int64)
     grad = torch.empty(B, n, d, device=X.device, dtype=torch.float32) if grad is None else grad
+    _want(grad, "grad", B * n * d, dev)
     rc = load().sot_grad_x_coo(_ptr(X), _ptr(Y), B, n, m, d, _ptr(rows), _ptr(cols), _ptr(vals),
                                _ptr(batch_offsets), _ptr(grad), _stream(stream))
     _check(rc, "sot_grad_x_coo")

@@ -122,3 +122,41 @@ def test_apml_arguments_rejected_on_host(lib):
     assert ap(p, p, NULL, NULL, 1, 5, 6, 3, p, p, p, -1, 0.1, 3, p, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
     assert ap(p, p, NULL, NULL, 1, 5, 6, 3, p, p, NULL, 10, 0.1, 3, p, p, p, NULL) == binding.SOT_ERR_INVALID_ARG
     assert ap(p, p, NULL, NULL, 0, 5, 6, 3, NULL, NULL, NULL, 0, 0.1, 3, NULL, NULL, NULL, NULL) == binding.SOT_OK
+
+
+def test_python_binding_checks_caller_tensors():
+    """Every tensor a caller supplies is checked for dtype, element count,
+    device and layout before the library is called (CPU tensors of the right
+    layout get as far as the device check)."""
+    import torch
+    B, n, m, d = 2, 5, 4, 3
+    X, Y = torch.zeros(B, n, d), torch.zeros(B, m, d)
+    f, g = torch.zeros(B, n), torch.zeros(B, m)
+    with pytest.raises(TypeError, match="X"):
+        binding.sot_potentials(X.to(torch.int32), Y, eps=0.1, iters=1)
+    with pytest.raises(ValueError, match="f must hold 10"):
+        binding.sot_potentials(X, Y, eps=0.1, iters=1, f=torch.zeros(B, n + 1), g=g)
+    with pytest.raises(ValueError, match="g must hold 8"):
+        binding.sot_plan_apply(X, Y, None, None, f, torch.zeros(m), 0.1)
+    with pytest.raises(ValueError, match="grad must hold 30"):
+        binding.sot_plan_apply(X, Y, None, None, f, g, 0.1, grad=torch.zeros(B, n, d + 1))
+    with pytest.raises(ValueError, match="out must hold 20"):
+        binding.sot_transport_apply(X, Y, None, None, f, g, 0.1, torch.zeros(B, m, 2), side=0,
+                                    out=torch.zeros(B, n + 3, 2))
+    with pytest.raises(ValueError, match="out must hold 24"):
+        binding.sot_grad_y(X, Y, None, None, f, g, 0.1, out=torch.zeros(B, n, d))
+    with pytest.raises(ValueError, match="contiguous"):
+        binding.sot_grad_y(X, Y, None, None, f, g, 0.1, out=torch.zeros(B, d, m).transpose(1, 2))
+    coo = dict(rows=torch.zeros(7, dtype=torch.int64), cols=torch.zeros(7, dtype=torch.int32),
+               batch_offsets=torch.zeros(B + 1, dtype=torch.int64), nnz=7)
+    with pytest.raises(TypeError, match="coo rows"):
+        binding.sot_apml_coo(X, Y, None, None, coo, 0.1)
+    coo["rows"] = torch.zeros(7, dtype=torch.int32)
+    coo["batch_offsets"] = torch.zeros(B, dtype=torch.int64)
+    with pytest.raises(ValueError, match="batch_offsets must hold 3"):
+        binding.sot_apml_coo(X, Y, None, None, coo, 0.1)
+    with pytest.raises(ValueError, match="vals must hold 7"):
+        binding.sot_grad_x_coo(X, Y, coo["rows"], coo["cols"], torch.zeros(6), torch.zeros(B + 1, dtype=torch.int64))
+    # a correct layout passes every check and stops at the device check
+    with pytest.raises(ValueError, match="CUDA device"):
+        binding.sot_plan_apply(X, Y, None, None, f, g, 0.1)
