@@ -588,6 +588,51 @@ def pin_hvp_structure(orc):
     _close(orc.hvp(X, Y, a, b, fb, gb, big, V), 2 * a[:, None] * V, 1e-4, what="HVP at large eps")
 
 
+def pin_hvp_transport_decomposition(orc):
+    """The page's decomposition: H V assembled from transport-vector and
+    transport-matrix products alone (P 1, P^T 1, P Y, P^T V, P^T w, P(g' Y),
+    the packed second moments P (y y^T), and conjugate gradients on the
+    marginal system, each step one P u and one P^T u) equals the dense
+    solve of the same system."""
+    X, Y, a, b = _problem(45, 40, 35, 3)
+    eps = 0.4
+    V = _rng(46).normal(size=X.shape)
+    f, g = orc.sinkhorn(X, Y, a, b, [eps], [2000])
+    T = lambda W, side: orc.transport(X, Y, a, b, f, g, eps, W, side)
+    n, d = X.shape
+    m = Y.shape[0]
+    r, c = T(np.ones(m), 0), T(np.ones(n), 1)
+    PY, PtV = T(Y, 0), T(V, 1)
+    w = np.sum(X * V, 1)
+    alpha = 2 * r * w - 2 * np.sum(PY * V, 1)
+    beta = 2 * T(w, 1) - 2 * np.sum(Y * PtV, 1)
+    res = beta - T(alpha / r, 1)
+    gd = np.zeros(m)
+    z = res / c
+    p, rz, r0 = z.copy(), res @ z, np.linalg.norm(res)
+    for _ in range(500):  # preconditioned CG on diag(c) - P^T diag(1/r) P
+        Sp = c * p - T(T(p, 0) / r, 1)
+        step = rz / (p @ Sp)
+        gd += step * p
+        res -= step * Sp
+        if np.linalg.norm(res) <= 1e-12 * r0:
+            break
+        z = res / c
+        rz, rz_old = res @ z, rz
+        p = z + (rz / rz_old) * p
+    Pg = T(gd, 0)
+    fd = (alpha - Pg) / r
+    iu = np.triu_indices(d)
+    Mp = T((Y[:, :, None] * Y[:, None, :])[:, iu[0], iu[1]], 0)
+    M = np.zeros((n, d, d))
+    M[:, iu[0], iu[1]] = Mp
+    M[:, iu[1], iu[0]] = Mp
+    hv = 2 * r[:, None] * V + (2 / eps) * ((fd - 2 * w)[:, None] * (r[:, None] * X - PY) + Pg[:, None] * X
+                                           - T(gd[:, None] * Y, 0) + 2 * np.sum(PY * V, 1)[:, None] * X
+                                           - 2 * np.einsum("ikl,il->ik", M, V))
+    _close(hv, orc.hvp(X, Y, a, b, f, g, eps, V), 1e-9, what="HVP from transport products vs dense solve")
+
+
 ALL_PINS = [
     pin_closed_form_single_point,
     pin_two_point_closed_form,
@@ -613,4 +658,5 @@ ALL_PINS = [
     pin_apml_marginals_and_large_T,
     pin_hvp_finite_differences,
     pin_hvp_structure,
+    pin_hvp_transport_decomposition,
 ]
