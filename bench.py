@@ -240,8 +240,14 @@ def run_reference(args, ws, rank):
         r, sample, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], w["eps"], args.cost)
         rates.append(r)
     value = float(np.median(rates)) / 1e9
+    # one whole step at this rate (the annealed workload: its 67 stages of 20
+    # iterations, the least it runs)
+    iters = w.get("iters") or 67 * w["iters_per_stage"]
+    ms_step = 2.0 * w["B"] * w["n"] * w["m"] * iters / (value * 1e9) * 1e3 if value > 0 else None
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_basis": "one whole step of the workload at the sampled rate",
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w["name"], "B": w["B"], "n": w["n"], "m": w["m"], "d": w["d"], "eps": w["eps"],
                        "iters": w.get("iters"), **({"cost": "cosine"} if args.cost == "cosine" else {})},

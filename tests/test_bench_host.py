@@ -1,5 +1,6 @@
-"""Host-side logic of bench.py without a GPU: clock-log parsing and the
-max-over-ranks reduction of step times across two gloo ranks on CPU."""
+"""Host-side logic of bench.py without a GPU: clock-log parsing, the
+max-over-ranks reduction of step times across two gloo ranks on CPU, and
+the reference arm's JSON line (it times the oracle on the host cores)."""
 import os
 import socket
 
@@ -55,3 +56,38 @@ def test_max_over_ranks_gloo_two_ranks():
 
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+            "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e")
+
+
+def _bench(args, env_extra=None):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **(env_extra or {}))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], cwd=root, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_line():
+    """The reference arm times the oracle on the host cores (no GPU needed) and
+    prints one line with the contract's keys on rank 0."""
+    (line,) = _bench(["--impl", "reference", "--steps", "2", "--warmup", "0", "--ref-step-s", "0.2"])
+    missing = [k for k in REQUIRED if k not in line]
+    assert not missing, missing
+    assert line["impl"] == "reference" and line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "gauss_n70000_d64"
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    lines = _bench(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2"})
+    assert lines == []
