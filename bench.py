@@ -206,6 +206,21 @@ def oracle_rate(target_s: float, X, Y, b, eps, cost="sqeuclidean"):
         return _oracle_rate(orc, target_s, X, Y, b, eps)
 
 
+def oracle_single_core(target_s: float, X, Y, b, eps, cost="sqeuclidean"):
+    """The same oracle sample with one OpenMP thread: {"value" (G pair-evals/s),
+    "sample"}.  The oracle's thread count is restored afterwards."""
+    from oracle import oracle as O
+    orc = O.get()
+    threads = orc.num_threads
+    orc.set_num_threads(1)
+    try:
+        with orc.cost(cost):
+            r, sample, _, _ = _oracle_rate(orc, target_s, X, Y, b, eps)
+    finally:
+        orc.set_num_threads(threads)
+    return {"value": r / 1e9, "sample": sample}
+
+
 def _oracle_rate(orc, target_s, X, Y, b, eps):
     m = Y.shape[0]
     g = np.zeros(m)
@@ -240,6 +255,7 @@ def run_reference(args, ws, rank):
         r, sample, t, thr = oracle_rate(args.ref_step_s, X[0], Y[0], b[0], w["eps"], args.cost)
         rates.append(r)
     value = float(np.median(rates)) / 1e9
+    one = oracle_single_core(args.ref_step_s / 3, X[0], Y[0], b[0], w["eps"], args.cost)
     # one whole step at this rate (the annealed workload: its 67 stages of 20
     # iterations, the least it runs)
     iters = w.get("iters") or 67 * w["iters_per_stage"]
@@ -251,7 +267,8 @@ def run_reference(args, ws, rank):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w["name"], "B": w["B"], "n": w["n"], "m": w["m"], "d": w["d"], "eps": w["eps"],
                        "iters": w.get("iters"), **({"cost": "cosine"} if args.cost == "cosine" else {})},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample,
+                             "single_core": one},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -431,7 +448,8 @@ def run_gpu(args, ws, rank, local):
     cpu = None
     if not args.no_cpu_baseline:
         r, sample, t, thr = oracle_rate(args.cpu_baseline_s, X[0], Y[0], b[0], eps, args.cost)
-        cpu = {"value": r / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample}
+        cpu = {"value": r / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample,
+               "single_core": oracle_single_core(args.cpu_baseline_s / 5, X[0], Y[0], b[0], eps, args.cost)}
     value = ws * pairs_total / t_max / 1e9
     line = {
         "metric": metric_name(wid), "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,

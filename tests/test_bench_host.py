@@ -83,6 +83,7 @@ def test_reference_arm_line():
     assert not missing, missing
     assert line["impl"] == "reference" and line["value"] > 0 and line["ms_per_step"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["single_core"]["value"] > 0
     assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == "gauss_n70000_d64"
 
