@@ -562,6 +562,26 @@ def pin_hvp_finite_differences(orc):
     _close(np.sum(V * hv), second, 1e-5, what="V^T H V vs second differences of the dual")
 
 
+def pin_hvp_two_point_closed_form(orc):
+    """2 x 2 problems: the gradient 2 sum_j P_ij (x_i - y_j) built from the
+    closed-form plan, differentiated along V by central differences, gives
+    H V with no Sinkhorn iteration involved."""
+    rng = _rng(47)
+    for d, eps in ((1, 0.3), (2, 0.5), (3, 1.2)):
+        X, Y, V = rng.normal(size=(2, d)), rng.normal(size=(2, d)), rng.normal(size=(2, d))
+        a = np.array([0.35, 0.65])
+        b = np.array([0.55, 0.45])
+
+        def grad(Xp):
+            P = two_point_plan(((Xp[:, None, :] - Y[None, :, :]) ** 2).sum(-1), a, b, eps)
+            return 2 * (P[:, :, None] * (Xp[:, None, :] - Y[None, :, :])).sum(1)
+
+        h = 1e-5
+        ref = (grad(X + h * V) - grad(X - h * V)) / (2 * h)
+        f, g = orc.sinkhorn(X, Y, a, b, [eps], [4000])
+        _close(orc.hvp(X, Y, a, b, f, g, eps, V), ref, 1e-7, what=f"2x2 HVP (d = {d})")
+
+
 def pin_hvp_structure(orc):
     """The Hessian is symmetric (U^T H V = V^T H U); the column marginals stay
     fixed, so sum_i (H V)_i = 2 sum_i a_i v_i at convergence; rotating both
@@ -657,6 +677,7 @@ ALL_PINS = [
     pin_apml_permutation_support,
     pin_apml_marginals_and_large_T,
     pin_hvp_finite_differences,
+    pin_hvp_two_point_closed_form,
     pin_hvp_structure,
     pin_hvp_transport_decomposition,
 ]
