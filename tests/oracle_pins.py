@@ -442,6 +442,21 @@ def pin_transport_closed_form(orc):
             _close(out, pv * V, 1e-14, what=f"1 x 1 transport side {side}")
 
 
+def pin_transport_two_point_closed_form(orc):
+    """2 x 2 problems at convergence: both transport products equal the
+    closed-form plan applied to V (and its transpose to U)."""
+    rng = _rng(48)
+    for d, eps in ((2, 0.4), (3, 0.9)):
+        X, Y = rng.normal(size=(2, d)), rng.normal(size=(2, d))
+        a = np.array([0.3, 0.7])
+        b = np.array([0.6, 0.4])
+        P = two_point_plan(((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1), a, b, eps)
+        V, U = rng.normal(size=(2, 3)), rng.normal(size=(2, 5))
+        f, g = orc.sinkhorn(X, Y, a, b, [eps], [4000])
+        _close(orc.transport(X, Y, a, b, f, g, eps, V, side=0), P @ V, 1e-10, what="2x2 P V")
+        _close(orc.transport(X, Y, a, b, f, g, eps, U, side=1), P.T @ U, 1e-10, what="2x2 P^T U")
+
+
 def pin_transport_marginals(orc):
     """A run ends with a g-half, after which the column marginals are exact:
     P^T 1 = b.  P 1 approaches a as the run converges, and P Y gives the
@@ -671,6 +686,7 @@ ALL_PINS = [
     pin_cosine_scale_invariance,
     pin_cosine_dual_finite_differences,
     pin_transport_closed_form,
+    pin_transport_two_point_closed_form,
     pin_transport_marginals,
     pin_transport_adjoint,
     pin_apml_dense_reduction,
