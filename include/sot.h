@@ -127,7 +127,9 @@ int sot_potentials(const float* X, const float* Y, const float* a, const float* 
 /*
  * General schedule (annealing, stop test, warm start, precision), see
  * sot_schedule.  Synchronises `stream` when st != NULL, or when the stop test
- * is active (it reads a device flag every few iterations).
+ * is active (it reads a device flag every few iterations).  The tensor-core
+ * half-steps bound every device-side wait (2 s); one that gives up leaves NaN
+ * potentials, and a call with st != NULL then returns SOT_ERR_TIMEOUT.
  */
 int sot_potentials_ex(const float* X, const float* Y, const float* a, const float* b,
                       int B, int n, int m, int d, const sot_schedule* s,

@@ -690,7 +690,11 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
         SOT_CUDA(cudaMemcpyAsync(counts.data(), sv.dflags + 3, sizeof(int) * K, cudaMemcpyDeviceToHost, sv.st));
         std::vector<float> errs(sv.B > 0 ? sv.B : 1, NAN);
         SOT_CUDA(cudaMemcpyAsync(errs.data(), sv.err, sizeof(float) * sv.B, cudaMemcpyDeviceToHost, sv.st));
+        int dstatus = 0;
+        SOT_CUDA(cudaMemcpyAsync(&dstatus, sv.dflags, sizeof(int), cudaMemcpyDeviceToHost, sv.st));
         SOT_CUDA(cudaStreamSynchronize(sv.st));
+        if (dstatus & SOT_DEV_TIMEOUT)
+            return fail(SOT_ERR_TIMEOUT, "a bounded device-side wait of a half-step gave up; the potentials are NaN");
         for (int k = 0; k < K; ++k)
             if (host_counts[k] >= 0) counts[k] = host_counts[k];
         long long tot = 0;
