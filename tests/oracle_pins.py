@@ -278,6 +278,25 @@ def pin_marginal_error_shortcut(orc):
     _close(orc.marginal_err(X, Y, a, b, f, g, eps), short, 1e-10, what="marginal error shortcut")
 
 
+def pin_maxima_lse_bounds(orc):
+    """A maximum lies between the log-sum-exp and the log-sum-exp minus the log
+    of the count.  After a g-half, -g_j/eps is the column's log-sum-exp of
+    (f_i - C_ij)/eps + log a_i exactly, so -g_j/eps - log n <= Mc_j <= -g_j/eps;
+    at convergence the rows obey the same bounds with f and m.  Both bounds
+    are attained by a dominant pair at small eps."""
+    X, Y, a, b = _problem(49, 13, 11, 2)
+    for eps in (0.5, 0.02):
+        f, g = orc.sinkhorn(X, Y, a, b, [eps], [4000])
+        Mr, Mc = orc.maxima(X, Y, a, b, f, g, eps)
+        n, m = len(f), len(g)
+        slack = 1e-9 * (1 + np.abs(g / eps).max())
+        assert np.all(Mc <= -g / eps + slack) and np.all(Mc >= -g / eps - np.log(n) - slack), "column maxima"
+        slack = 1e-9 * (1 + np.abs(f / eps).max())
+        assert np.all(Mr <= -f / eps + slack) and np.all(Mr >= -f / eps - np.log(m) - slack), "row maxima"
+    # small eps: the maximum carries almost all of the sum
+    _close(Mr, -f / eps, 0, atol=np.log(m) * 0.5 + 1e-9, what="row maxima near the LSE at small eps")
+
+
 def pin_coo_limits(orc):
     """tau = 0 keeps every pair; tau = 1 keeps exactly the row and column
     argmax pairs; tau -> 0 takes the support gradient to the dense gradient,
@@ -679,6 +698,7 @@ ALL_PINS = [
     pin_invariances,
     pin_dual_finite_differences,
     pin_marginal_error_shortcut,
+    pin_maxima_lse_bounds,
     pin_coo_limits,
     pin_anneal_schedule,
     pin_cosine_closed_form,
