@@ -446,7 +446,7 @@ def run_gpu(args, ws, rank, local):
     roof["alu_rates"] = rates
     # CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:  # rank 0 at N = 1 only
         r, sample, t, thr = oracle_rate(args.cpu_baseline_s, X[0], Y[0], b[0], eps, args.cost)
         cpu = {"value": r / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample,
                "single_core": oracle_single_core(args.cpu_baseline_s / 5, X[0], Y[0], b[0], eps, args.cost)}
@@ -584,7 +584,7 @@ def run_transport(args, ws, rank, local):
     achieved = ops_pair * pairs_step * args.steps / t_max / 1e12
     peak = lanes * sms * mhz * 1e6 / 1e12
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:  # rank 0 at N = 1 only
         from oracle import oracle as O
         orc = O.get()
         rows = max(1, min(n, int(64 * orc.num_threads)))
