@@ -267,6 +267,36 @@ def pin_dual_finite_differences(orc):
     _close(grad, fd, 1e-6, atol=1e-9, what="finite differences of the dual")
 
 
+def pin_lse_extremes(orc):
+    """Half-steps on rows of extreme structure, with closed forms:
+    - identical points, a constant g and uniform b: f_i = |x - y|^2 - g exactly;
+    - one column far above the rest (its term exceeds the others by e^40):
+      f_i = C_ij - g_j - eps log b_j for that column, to fp64 rounding;
+    - a spread of 1e4 eps in g: finite, and equal to a log-sum-exp taken
+      independently (scipy) on the same scores."""
+    rng = _rng(50)
+    eps = 0.05
+    x, y = rng.normal(size=(1, 3)), rng.normal(size=(1, 3))
+    X, Y = np.repeat(x, 6, 0), np.repeat(y, 5, 0)
+    c = float(np.sum((x - y) ** 2))
+    _close(orc.f_half(X, Y, None, np.full(5, 0.7), eps), np.full(6, c - 0.7), 1e-13, what="all-equal row")
+    X, Y = rng.normal(size=(4, 3)), rng.normal(size=(9, 3))
+    b = rng.random(9) + 0.1
+    b /= b.sum()
+    C = ((X[:, None, :] - Y[None, :, :]) ** 2).sum(-1)
+    g = np.zeros(9)
+    j0 = 4
+    # column j0's score beats every other by at least 40 (in units of eps)
+    s = -C / eps + np.log(b)[None, :]
+    g[j0] = eps * (40.0 + np.max(s - s[:, [j0]]))
+    _close(orc.f_half(X, Y, b, g, eps), C[:, j0] - g[j0] - eps * np.log(b[j0]), 1e-14, what="dominant column")
+    g = -1e4 * eps * rng.random(9)
+    f = orc.f_half(X, Y, b, g, eps)
+    assert np.all(np.isfinite(f)), "non-finite f on a wide row"
+    ref = -eps * logsumexp((g[None, :] - C) / eps + np.log(b)[None, :], axis=1)
+    _close(f, ref, 1e-13, what="wide row")
+
+
 def pin_marginal_error_shortcut(orc):
     """Row marginal error by definition, sum_i |sum_j P_ij - a_i|, equals the
     shortcut sum_i a_i |exp((f_i - f'_i)/eps) - 1| with f' the next f-half."""
@@ -697,6 +727,7 @@ ALL_PINS = [
     pin_large_eps,
     pin_invariances,
     pin_dual_finite_differences,
+    pin_lse_extremes,
     pin_marginal_error_shortcut,
     pin_maxima_lse_bounds,
     pin_coo_limits,
