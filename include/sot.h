@@ -206,16 +206,6 @@ int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b,
                  long long* nnz_host, void* stream);
 
 /*
- * Gradient on a stored support ("CUDA-Optimized APML", Innovation: gradients
- * preserved on the stored support):
- *   grad[k][i] = 2 sum_{e in cloud k, rows[e] = i} vals[e] (x_i - y_cols[e])
- * The COO must be row-sorted within each cloud (as sot_plan_coo writes it);
- * unsorted or out-of-range entries make the call return SOT_ERR_INVALID_ARG
- * (checked on the device).  batch_offsets is a device array [B+1] whose last
- * element is the number of entries.  The call synchronises `stream` once to
- * read the check's result.
- */
-/*
  * Sparse APML on a stored support ("From Theory to Throughput: CUDA-Optimized
  * APML", Abstract and Innovation: an adaptive softmax, bidirectional
  * symmetrisation and Sinkhorn normalisation run directly in COO form, and
@@ -237,6 +227,16 @@ int sot_apml_coo(const float* X, const float* Y, const float* a, const float* b,
                  const long long* batch_offsets, long long nnz, float T, int iters,
                  float* vals, float* loss, float* grad, void* stream);
 
+/*
+ * Gradient on a stored support ("CUDA-Optimized APML", Innovation: gradients
+ * preserved on the stored support):
+ *   grad[k][i] = 2 sum_{e in cloud k, rows[e] = i} vals[e] (x_i - y_cols[e])
+ * The COO must be row-sorted within each cloud (as sot_plan_coo writes it);
+ * unsorted or out-of-range entries make the call return SOT_ERR_INVALID_ARG
+ * (checked on the device).  batch_offsets is a device array [B+1] whose last
+ * element is the number of entries.  The call synchronises `stream` once to
+ * read the check's result.
+ */
 int sot_grad_x_coo(const float* X, const float* Y, int B, int n, int m, int d,
                    const int* rows, const int* cols, const float* vals,
                    const long long* batch_offsets, float* grad, void* stream);

@@ -54,7 +54,7 @@
  * the dual, symmetry and the n = 1 and large-eps limits.
  *
  * Compile: cc -O2 -fopenmp -fPIC -shared oracle.c -lm  (no fast-math).
- * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..12) that
+ * Optional -DORC_MUTANT=k builds a deliberately wrong variant (k = 1..14) that
  * the test suite uses to show that the pins catch plausible mistakes.
  */
 #include <math.h>
@@ -541,7 +541,11 @@ long long orc_coo(int n, int m, int d, const double *X, const double *Y,
     long long *cnt = (long long *)malloc(sizeof(long long) * (size_t)(n + 1));
     if (!Mr || !Mc || !cnt) { free(Mr); free(Mc); free(cnt); return -2; }
     orc_maxima(n, m, d, X, Y, a, b, f, g, eps, Mr, Mc);
+#if ORC_MUTANT == 13
+    double lt = tau > 0 ? -log(tau) : -INFINITY;
+#else
     double lt = tau > 0 ? log(tau) : -INFINITY;
+#endif
     /* pass 1: counts per row */
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < n; ++i) {
@@ -551,7 +555,11 @@ long long orc_coo(int n, int m, int d, const double *X, const double *Y,
             double mu = -INFINITY;
             if (dirs & 1) {
                 double s = (g[j] - c) / eps + log(b[j]);
+#if ORC_MUTANT == 14
+                double v = (tau > 0) ? s - (Mc[j] + lt) : INFINITY; /* row test against a column maximum */
+#else
                 double v = (tau > 0) ? s - (Mr[i] + lt) : INFINITY;
+#endif
                 if (v > mu) mu = v;
             }
             if (dirs & 2) {
@@ -575,7 +583,11 @@ long long orc_coo(int n, int m, int d, const double *X, const double *Y,
                 double mu = -INFINITY;
                 if (dirs & 1) {
                     double s = (g[j] - c) / eps + log(b[j]);
+#if ORC_MUTANT == 14
+                    double v = (tau > 0) ? s - (Mc[j] + lt) : INFINITY;
+#else
                     double v = (tau > 0) ? s - (Mr[i] + lt) : INFINITY;
+#endif
                     if (v > mu) mu = v;
                 }
                 if (dirs & 2) {

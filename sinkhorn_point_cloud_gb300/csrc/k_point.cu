@@ -26,6 +26,8 @@
 // one 16-byte load yields two 2-lane operands of the packed f32x2 arithmetic:
 //     tile[2p]   = (-v_j.x, -v_j'.x, -v_j.y, -v_j'.y),
 //     tile[2p+1] = (-v_j.z, -v_j'.z, -c_j,   -c_j')      with v = sqrt(kappa) y.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -575,16 +577,19 @@ cudaError_t launch_point_coo(const CooArgs& p, int write_pass, cudaStream_t st) 
     return cudaGetLastError();
 }
 
+// Cached after the first successful query (the kernel's resources do not
+// depend on the device); a failed query returns 4 and is not cached.
 int point_blocks_per_sm() {
-    static int occ = 0;
-    if (occ == 0) {
-        int v = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, point_half_kernel<3, MODE_LSE>, PT_T, 0) != cudaSuccess ||
-            v < 1)
-            v = 4;
-        occ = v;
+    static std::atomic<int> occ{0};
+    int v = occ.load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, point_half_kernel<3, MODE_LSE>, PT_T, 0) != cudaSuccess ||
+        v < 1) {
+        cudaGetLastError();
+        return 4;
     }
-    return occ;
+    occ.store(v, std::memory_order_relaxed);
+    return v;
 }
 
 }  // namespace sot

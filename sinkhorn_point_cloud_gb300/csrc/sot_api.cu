@@ -122,16 +122,23 @@ struct Scratch {
     }
 };
 
+// SM count of the current device, cached per device.  Concurrent first calls
+// may both query; each stores the same value.  A failed query is not cached.
 int device_sms() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = v > 0 ? v : 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 148;
     }
-    return cached[dev];
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    cached[dev].store(v, std::memory_order_relaxed);
+    return v;
 }
 
 // ---- per-launch timing (sot_profile_*) ------------------------------------

@@ -361,6 +361,49 @@ def pin_coo_limits(orc):
         assert np.all(np.linalg.norm(gs - gs_full, axis=1) <= bound + 1e-12), "support gradient bound"
 
 
+def pin_coo_threshold_hand_worked(orc):
+    """The thresholded support for 0 < tau < 1 on a 3 x 3 problem worked by hand
+    ("CUDA-Optimized APML", Abstract / Innovation: negligible assignments are
+    dropped relative to the largest one, in both directions).
+
+    d = 1, eps = 1, x = (0, 1, 3), y = (0, 2, 5), a = (1/2, 1/4, 1/4),
+    b = (1/4, 1/4, 1/2), f = (0, 0, 0), g = (0, 1, 0).  C = [[0, 4, 25],
+    [1, 1, 16], [9, 1, 4]], and P_ij = a_i b_j exp(f_i + g_j - C_ij).
+    Ratios to the row maximum, P_ij / max_j' P_ij':
+        row 0: 1, e^-3, e^-24.3      row 1: e^-1, 1, e^-15.3
+        row 2: e^-9, 1, e^-3.307     (e^-3 = 0.0498, e^-3.307 = 0.0366)
+    Ratios to the column maximum, P_ij / max_i' P_i'j (column j listed down):
+        column 0: 1, e^-1/2, e^-9/2  column 1: e^-2.307, 1, 1
+        column 2: e^-20.3, e^-12, 1  (e^-1/2 = 0.184, e^-2.307 = 0.0996)
+    Each tau below sits between two of these ratios, so every listed pair
+    is decided by a margin of 7 % or more, and the boundary pairs (0, 1),
+    (2, 2), (0, 1) and (1, 0) fall on either side of it in turn."""
+    X = np.array([[0.0], [1.0], [3.0]])
+    Y = np.array([[0.0], [2.0], [5.0]])
+    a = np.array([0.5, 0.25, 0.25])
+    b = np.array([0.25, 0.25, 0.5])
+    f = np.zeros(3)
+    g = np.array([0.0, 1.0, 0.0])
+    P = {(0, 0): 0.125, (0, 1): 0.125 * np.exp(-3.0), (1, 0): 0.0625 * np.exp(-1.0),
+         (1, 1): 0.0625, (2, 1): 0.0625, (2, 2): 0.125 * np.exp(-4.0)}
+    cases = [
+        # (tau, dirs, support)
+        (0.03, 1, [(0, 0), (0, 1), (1, 0), (1, 1), (2, 1), (2, 2)]),  # e^-9 < tau < e^-3.307
+        (0.04, 1, [(0, 0), (0, 1), (1, 0), (1, 1), (2, 1)]),          # e^-3.307 < tau < e^-3
+        (0.06, 1, [(0, 0), (1, 0), (1, 1), (2, 1)]),                  # e^-3 < tau < e^-1
+        (0.06, 2, [(0, 0), (0, 1), (1, 0), (1, 1), (2, 1), (2, 2)]),  # e^-9/2 < tau < e^-2.307
+        (0.15, 2, [(0, 0), (1, 0), (1, 1), (2, 1), (2, 2)]),          # e^-2.307 < tau < e^-1/2
+        (0.20, 2, [(0, 0), (1, 1), (2, 1), (2, 2)]),                  # e^-1/2 < tau < 1
+        (0.15, 3, [(0, 0), (1, 0), (1, 1), (2, 1), (2, 2)]),          # union of the two tests
+        (0.04, 3, [(0, 0), (0, 1), (1, 0), (1, 1), (2, 1), (2, 2)]),
+    ]
+    for tau, dirs, want in cases:
+        got = orc.coo(X, Y, a, b, f, g, 1.0, tau, dirs)
+        pairs = list(zip(got["rows"].tolist(), got["cols"].tolist()))
+        assert pairs == want, f"tau = {tau}, dirs = {dirs}: support {pairs}, expected {want}"
+        _close(got["vals"], [P[k] for k in want], 1e-14, what=f"stored values, tau = {tau}, dirs = {dirs}")
+
+
 def pin_anneal_schedule(orc):
     """eps_k = max(1e-3, 0.9^k): 66 geometric stages from 1.0 down to 0.9^65,
     then one clamped stage at 1e-3 (67 in all).  The annealed solve equals a
@@ -731,6 +774,7 @@ ALL_PINS = [
     pin_marginal_error_shortcut,
     pin_maxima_lse_bounds,
     pin_coo_limits,
+    pin_coo_threshold_hand_worked,
     pin_anneal_schedule,
     pin_cosine_closed_form,
     pin_cosine_unit_points,

@@ -7,7 +7,8 @@ of Gauss-Seidel order, log-sum-exp without the max added back, a coordinate
 dropped from the cost, a cosine cost that leaves y unnormalised, a transport
 product that weights its pairs with the wrong row weight, a sparse APML that drops
 the column softmax, a Hessian-vector product that holds the column potentials
-fixed.
+fixed, a COO threshold with the sign of log tau flipped, a COO row test made
+against a column maximum.
 """
 import pytest
 
@@ -17,7 +18,8 @@ from oracle import oracle as O
 MUTANTS = {1: "drops log b", 2: "sign of C", 3: "weights transposed", 4: "grad without a_i",
            5: "sign of g in plan", 6: "Jacobi order", 7: "LSE without max", 8: "cost drops a coordinate",
            9: "cosine without y normalised", 10: "transport with the wrong row weight",
-           11: "APML without the column softmax", 12: "HVP with the column potentials fixed"}
+           11: "APML without the column softmax", 12: "HVP with the column potentials fixed",
+           13: "COO threshold with the sign of log tau flipped", 14: "COO row test against the column maximum"}
 
 
 @pytest.mark.parametrize("k", sorted(MUTANTS), ids=lambda k: MUTANTS[k])
