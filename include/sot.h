@@ -129,7 +129,8 @@ int sot_potentials(const float* X, const float* Y, const float* a, const float* 
  * sot_schedule.  Synchronises `stream` when st != NULL, or when the stop test
  * is active (it reads a device flag every few iterations).  The tensor-core
  * half-steps bound every device-side wait (2 s); one that gives up leaves NaN
- * potentials, and a call with st != NULL then returns SOT_ERR_TIMEOUT.
+ * potentials, and a call with st != NULL then returns SOT_ERR_TIMEOUT (a call
+ * without st reports it through sot_async_status).
  */
 int sot_potentials_ex(const float* X, const float* Y, const float* a, const float* b,
                       int B, int n, int m, int d, const sot_schedule* s,
@@ -204,6 +205,34 @@ int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b,
                  float threshold, int dirs, long long capacity,
                  int* rows, int* cols, float* vals, long long* batch_offsets,
                  long long* nnz_host, void* stream);
+
+/*
+ * The fp32 operands that sot_plan_coo's predicate reads, for auditing its
+ * decisions ("CUDA-Optimized APML", Abstract / Innovation: the thresholded
+ * support).  Given the same inputs as sot_plan_coo, it writes (device arrays
+ * owned by the caller):
+ *   xc[B][n][d], yc[B][m][d]  coordinates less the common per-cloud shift
+ *                             t = (mean x + mean y) / 2 (the cost is unchanged);
+ *   lwx[B][n], lwy[B][m]      log2 of the weights (log2(1/n) when a is NULL);
+ *   Lx[B][n], Ly[B][m]        the base-2 states of f and g, kappa = 1 / (eps ln 2):
+ *                             Lx = kappa (|xc|^2 - f) for d > 3 and kappa (0 - f) for d <= 3;
+ *   Mr[B][n], Mc[B][m]        the row and column maxima of the two scores;
+ * and scalars_host[2] = { kappa, log2(threshold) } (host).  Every kept or
+ * dropped pair of sot_plan_coo is decided from these values alone, with
+ * single rounding (round to nearest even) at every step, by:
+ *   d <= 3 (k ascending, u = fl(sqrt(kappa) xc), v = fl(sqrt(kappa) yc)):
+ *     row score  t_ij = -fma chain over k of (fl(u_ik - v_jk))^2 started at -fl(lwy_j - Ly_j);
+ *     col score  t'_ij = -fma chain over k of (fl(v_jk - u_ik))^2 started at -fl(lwx_i - Lx_i);
+ *   d > 3: p_ij = fma chain over k of xc_ik yc_jk from 0;
+ *     t_ij = fma(2 kappa, p_ij, fl(lwy_j - Ly_j)), t'_ij = fma(2 kappa, p_ij, fl(lwx_i - Lx_i));
+ *   Mr_i = max_j t_ij, Mc_j = max_i t'_ij, and pair (i, j) is kept when
+ *   (dirs & 1) and t_ij >= fl(Mr_i + log2 tau), or (dirs & 2) and t'_ij >= fl(Mc_j + log2 tau).
+ * Asynchronous on `stream`; same argument errors as sot_plan_coo.
+ */
+int sot_plan_coo_operands(const float* X, const float* Y, const float* a, const float* b,
+                          int B, int n, int m, int d, const float* f, const float* g, float eps,
+                          float threshold, float* xc, float* lwx, float* Lx, float* yc, float* lwy,
+                          float* Ly, float* Mr, float* Mc, float* scalars_host, void* stream);
 
 /*
  * Sparse APML on a stored support ("From Theory to Throughput: CUDA-Optimized
@@ -292,6 +321,30 @@ int sot_profile_read_kinds(long long* launches_host, double* ms_host);
 int sot_potentials_noalloc(const float* X, const float* Y, const float* a, const float* b,
                            int B, int n, int m, int d, float eps, int iters,
                            float* f, float* g, void* stream);
+
+/*
+ * Device-side status of the asynchronous calls (sot_potentials,
+ * sot_potentials_ex without stats, sot_plan_apply and its convenience forms)
+ * made on the current device since the last sot_async_status.  Synchronises
+ * `stream` (give the stream of those calls, or NULL after synchronising them),
+ * returns SOT_ERR_TIMEOUT when a bounded device-side wait of a tensor-core
+ * kernel gave up in one of them (the rows that kernel held are NaN) and
+ * SOT_OK otherwise, and clears the status.
+ */
+int sot_async_status(void* stream);
+
+/*
+ * Testing hook for the timeout path of the tensor-core kernels.  With
+ * tile >= 0, the tensor-core kernels launched after the next
+ * `after_launches` ones issue no bulk copy from column tile `tile` of their
+ * column chunk onward, so their waits on that tile run out after wait_ns
+ * nanoseconds (wait_ns <= 0: the default 2 s): such a kernel waits for the
+ * copies and MMAs it did issue, frees TMEM, leaves NaN rows and reports
+ * SOT_ERR_TIMEOUT as above.  tile < 0 turns the hook off and restores the
+ * default limit.  Process-wide and not synchronised with work in flight: set
+ * it between calls.  Not for production use.
+ */
+int sot_test_hold_tile(int tile, int after_launches, long long wait_ns);
 
 /*
  * Which kernel family a solve of dimension d with these flags would use:

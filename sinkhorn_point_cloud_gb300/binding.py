@@ -99,6 +99,10 @@ def load(path: str | None = None):
         "sot_transport_apply": [P, P, P, P, i, i, i, i, P, P, f, P, i, i, P, i, P],
         "sot_grad_y": [P, P, P, P, i, i, i, i, P, P, f, P, i, P],
         "sot_apml_coo": [P, P, P, P, i, i, i, i, P, P, P, ll, f, i, P, P, P, P],
+        "sot_async_status": [P],
+        "sot_test_hold_tile": [i, i, ll],
+        "sot_plan_coo_operands": [P, P, P, P, i, i, i, i, P, P, f, f, P, P, P, P, P, P, P, P,
+                                  C.POINTER(C.c_float), P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -367,6 +371,27 @@ def sot_plan_coo(X, Y, a, b, f, g, eps, threshold=1e-8, dirs=3, capacity=None, s
     return dict(rows=rows[:k], cols=cols[:k], vals=vals[:k], batch_offsets=off, nnz=k)
 
 
+def sot_plan_coo_operands(X, Y, a, b, f, g, eps, threshold=1e-8, stream=None):
+    """The fp32 operands sot_plan_coo decides its support from; returns
+    dict(xc, lwx, Lx, yc, lwy, Ly, Mr, Mc, kappa, log2tau)."""
+    X, Y, B, n, m, d = _shapes(X, Y, a, b)
+    dev = X.device
+    _potentials_args(f, g, B, n, m, dev)
+    L = load()
+    out = dict(xc=torch.empty(B, n, d, device=dev), lwx=torch.empty(B, n, device=dev),
+               Lx=torch.empty(B, n, device=dev), yc=torch.empty(B, m, d, device=dev),
+               lwy=torch.empty(B, m, device=dev), Ly=torch.empty(B, m, device=dev),
+               Mr=torch.empty(B, n, device=dev), Mc=torch.empty(B, m, device=dev))
+    sc = (C.c_float * 2)()
+    rc = L.sot_plan_coo_operands(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g), float(eps),
+                                 float(threshold), *(_ptr(out[k]) for k in ("xc", "lwx", "Lx", "yc", "lwy", "Ly",
+                                                                            "Mr", "Mc")),
+                                 sc, _stream(stream))
+    _check(rc, "sot_plan_coo_operands")
+    out["kappa"], out["log2tau"] = float(sc[0]), float(sc[1])
+    return out
+
+
 def sot_grad_x_coo(X, Y, rows, cols, vals, batch_offsets, grad=None, stream=None):
     X, Y, B, n, m, d = _shapes(X, Y, None, None)
     dev = X.device
@@ -380,6 +405,19 @@ def sot_grad_x_coo(X, Y, rows, cols, vals, batch_offsets, grad=None, stream=None
                                _ptr(batch_offsets), _ptr(grad), _stream(stream))
     _check(rc, "sot_grad_x_coo")
     return grad
+
+
+def sot_async_status(stream=None):
+    """Raises SotError(SOT_ERR_TIMEOUT) when a bounded device-side wait gave up
+    in an asynchronous call since the last check on this device; clears it."""
+    _check(load().sot_async_status(_stream(stream)), "sot_async_status")
+
+
+def sot_test_hold_tile(tile: int, after_launches: int = 0, wait_ns: int = 0):
+    """Testing hook: after `after_launches` more tensor-core launches, those
+    kernels withhold column tile `tile` of their chunk onward (tile < 0: off),
+    so their waits run out after wait_ns nanoseconds."""
+    _check(load().sot_test_hold_tile(int(tile), int(after_launches), int(wait_ns)), "sot_test_hold_tile")
 
 
 def sot_check_inputs(X, Y, a=None, b=None, stream=None) -> int:

@@ -63,6 +63,25 @@ __device__ __forceinline__ float2 ff_mul(float2 a, float2 b) {
     return ff_renorm(q.x, __fmaf_rn(a.x, b.y, __fmaf_rn(a.y, b.x, q.y)));
 }
 
+// log2 P_ij = log2 w_i + log2 w'_j + kappa (f_i + g_j - C_ij) in float-float:
+// C_ij from error-free coordinate differences and squares of the caller's
+// points, the potentials and C_ij cancelling exactly before the product with
+// kappa = kap.x + kap.y.  Accurate to a few fp32 ulps of the (small) result,
+// where fp32 would round at the size of kappa |f_i|.
+__device__ __forceinline__ float exact_log2_plan(const float* x, const float* y, int d, float fi, float gj,
+                                                 float lwi, float lwj, float2 kap) {
+    float2 C2 = make_float2(0.f, 0.f);
+    for (int k = 0; k < d; ++k) {
+        const float2 dd = two_sum(x[k], -y[k]);
+        float2 sq = two_prod(dd.x, dd.x);
+        sq.y = __fmaf_rn(2.f * dd.x, dd.y, sq.y);
+        C2 = ff_add(C2, sq);
+    }
+    const float2 pot = ff_add(two_sum(fi, gj), make_float2(-C2.x, -C2.y));
+    const float2 ell = ff_add(ff_mul(kap, pot), two_sum(lwi, lwj));
+    return __fadd_rn(ell.x, ell.y);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -456,7 +456,8 @@ cudaError_t launch_dense_apply(const ApplyArgs& p, cudaStream_t st) {
 // u_ji = fma(2 kappa, x_i.y_j, log2 a_i - L_i) with the dot product
 // accumulated k-ascending from zero, exactly as in the maximum pass, so the
 // predicate and the maxima agree bit for bit.  One warp per row; lanes take
-// 32 consecutive columns; ballot / popc order the writes.
+// 32 consecutive columns; ballot / popc order the writes.  Stored values are
+// P_ij with the exponent in float-float (exact_log2_plan).
 constexpr int DC_T = 256;
 template <bool WRITE>
 __global__ void __launch_bounds__(DC_T) dense_coo_kernel(CooArgs p) {
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(DC_T) dense_coo_kernel(CooArgs p) {
     if (!ok) return;  // whole warp leaves together
     const float thr = p.Mr[xb + i] + p.log2tau;
     const float e_i = p.lw2x[xb + i] - p.L[xb + i];
-    const float ai = p.a ? p.a[xb + i] : 1.f / (float)p.n;
+    const float2 kap = make_float2(p.kap_hi, p.kap_lo);
     long long pos = WRITE ? p.rowptr[xb + i] : 0;
     int cnt = 0;
     for (int base = 0; base < p.m; base += 32) {
@@ -493,7 +494,8 @@ __global__ void __launch_bounds__(DC_T) dense_coo_kernel(CooArgs p) {
                 const long long o = pos + __popc(mask & ((1u << lane) - 1u));
                 p.rows[o] = i;
                 p.cols[o] = j;
-                p.vals[o] = ai * ex2f(fmaf(p.two_kappa, acc, c) - p.L[xb + i]);
+                p.vals[o] = exp2f(exact_log2_plan(p.X + (xb + i) * d, p.Y + (yb + j) * d, d, p.f[xb + i],
+                                                  p.g[yb + j], p.lw2x[xb + i], p.lw2y[yb + j], kap));
             }
             pos += __popc(mask);
         } else {

@@ -462,7 +462,11 @@ cudaError_t launch_point_apply(const ApplyArgs& p, cudaStream_t st) {
 // u_ji = e_i - kappa|x_i - y_j|^2 (e_i = log2 a_i - L_i), each evaluated by the
 // same fp32 chain as the maximum pass of its half (the scaled difference
 // u - v is exactly the negation of v - u, so both directions see the same
-// squares); the maxima and the predicate therefore agree bit for bit.  One
+// squares); the maxima and the predicate therefore agree bit for bit.  A kept
+// pair stores P_ij = 2^(log2 a_i + log2 b_j + kappa (f_i + g_j - C_ij)) with
+// the exponent in float-float from the caller's points and potentials
+// (exact_log2_plan), so the value does not carry the fp32 rounding of the
+// large, cancelling terms kappa f_i and kappa g_j.  One
 // warp owns CO_RW rows; its lanes take 32 consecutive columns, and a ballot /
 // popc over the predicate gives each kept pair its slot, so a row's entries
 // come out in ascending column order with coalesced stores.
@@ -473,7 +477,7 @@ constexpr int CO_TC = 256;                    // columns per tile
 
 template <int D, bool WRITE>
 __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
-    __shared__ float4 cy[CO_TC];   // (y, -c_j)  with c_j = log2 b_j - Lam_j
+    __shared__ float cy[CO_TC];    // -c_j  with c_j = log2 b_j - Lam_j
     __shared__ float4 cv[CO_TC];   // (-sqrt(kappa) y, Mc_j + log2 tau)
     const int b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -482,9 +486,10 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
     const float4* yp = reinterpret_cast<const float4*>(p.ypack) + (size_t)b * p.m;
     const size_t xb = (size_t)b * p.n, yb = (size_t)b * p.m;
     const float sk = sqrtf(p.kappa);
+    const float2 kap = make_float2(p.kap_hi, p.kap_lo);
 
     float4 x[CO_RW];
-    float u0[CO_RW], u1[CO_RW], u2[CO_RW], thr_r[CO_RW], ne_r[CO_RW], arow[CO_RW];
+    float u0[CO_RW], u1[CO_RW], u2[CO_RW], thr_r[CO_RW], ne_r[CO_RW];
     long long pos[CO_RW];
     int cnt[CO_RW];
 #pragma unroll
@@ -497,7 +502,6 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
         u2[r] = scaled(sk, x[r].z);
         thr_r[r] = ok ? __fadd_rn(p.Mr[xb + i], p.log2tau) : INFINITY;
         ne_r[r] = ok ? neg_bias(x[r].w, p.L[xb + i]) : 0.f;  // -(log2 a_i - L_i)
-        arow[r] = ok ? p.kappa * p.nx[xb + i] - p.L[xb + i] : 0.f;
         pos[r] = (WRITE && ok) ? p.rowptr[xb + i] : 0;
         cnt[r] = 0;
     }
@@ -505,11 +509,11 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
         __syncthreads();
         for (int t = threadIdx.x; t < CO_TC; t += CO_T) {
             const int j = base + t;
-            float4 c = make_float4(0.f, 0.f, 0.f, INFINITY);
+            float c = INFINITY;
             float4 c2 = make_float4(0.f, 0.f, 0.f, INFINITY);
             if (j < p.m) {
                 const float4 y = yp[j];
-                c = make_float4(y.x, y.y, y.z, neg_bias(y.w, p.Lam[yb + j]));
+                c = neg_bias(y.w, p.Lam[yb + j]);
                 c2 = make_float4(-scaled(sk, y.x), -scaled(sk, y.y), -scaled(sk, y.z),
                                  __fadd_rn(p.Mc[yb + j], p.log2tau));
             }
@@ -520,11 +524,12 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
         for (int cc = 0; cc < CO_TC; cc += 32) {
             const int t = cc + lane;
             const int j = base + t;
-            const float4 c = cy[t], c2 = cv[t];
+            const float c = cy[t];
+            const float4 c2 = cv[t];
 #pragma unroll
             for (int r = 0; r < CO_RW; ++r) {
                 bool keep = false;
-                const float trow = -scalar_chain<D>(c.w, u0[r], u1[r], u2[r], c2.x, c2.y, c2.z);
+                const float trow = -scalar_chain<D>(c, u0[r], u1[r], u2[r], c2.x, c2.y, c2.z);
                 if (p.dirs & 1) keep = trow >= thr_r[r];
                 if (p.dirs & 2) {
                     // column direction: rows Y, columns X; d = v + (-u) = -(u - v) exactly
@@ -536,15 +541,12 @@ __global__ void __launch_bounds__(CO_T) point_coo_kernel(CooArgs p) {
                 if (WRITE) {
                     const long long o = pos[r] + __popc(mask & ((1u << lane) - 1u));
                     if (keep && o < p.capacity) {
-                        const float d0 = x[r].x - c.x, d1 = x[r].y - c.y, d2 = x[r].z - c.z;
-                        float C = d0 * d0;
-                        if (D >= 2) C = fmaf(d1, d1, C);
-                        if (D >= 3) C = fmaf(d2, d2, C);
-                        const float ai = p.a ? p.a[xb + rowb + r] : 1.f / (float)p.n;
-                        // P_ij = a_i 2^(c_j - kappa C_ij - L_i)
-                        p.rows[o] = rowb + r;
+                        const int i = rowb + r;
+                        const float l2 = exact_log2_plan(p.X + (xb + i) * D, p.Y + (yb + j) * D, D, p.f[xb + i],
+                                                         p.g[yb + j], x[r].w, yp[j].w, kap);
+                        p.rows[o] = i;
                         p.cols[o] = j;
-                        p.vals[o] = ai * ex2f(fmaf(-p.kappa, C, arow[r] - c.w));
+                        p.vals[o] = exp2f(l2);
                     }
                     pos[r] += __popc(mask);
                 } else {

@@ -239,6 +239,27 @@ cudaError_t launch_count_iter(const int* stop_flag, int* counter, cudaStream_t s
     return cudaGetLastError();
 }
 
+// ---- device status of asynchronous calls -------------------------------------
+// Bits of the per-call status words of asynchronous calls, gathered per device
+// until the host reads and clears them (sot_async_status).
+__device__ unsigned g_async_status;
+
+__global__ void status_merge_kernel(const int* status) { atomicOr(&g_async_status, (unsigned)*status); }
+cudaError_t launch_status_merge(const int* status, cudaStream_t st) {
+    count_launches(1); status_merge_kernel<<<1, 1, 0, st>>>(status);
+    return cudaGetLastError();
+}
+cudaError_t read_clear_async_status(cudaStream_t st, unsigned* out) {
+    unsigned v = 0;
+    const unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_async_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbolAsync(g_async_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    *out = v;
+    return e;
+}
+
 // ---- input validation ---------------------------------------------------------
 __global__ void check_kernel(const float* X, long long npts, const float* w, long long nw, int* bad) {
     const long long stride = (long long)gridDim.x * blockDim.x;

@@ -33,6 +33,8 @@
 // timeout bit, drains its own bulk copies, frees TMEM and returns.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "tc.h"
 #include "tc_ptx.cuh"
@@ -51,7 +53,7 @@ constexpr uint32_t OFF_A = 0;                           // [2 row tiles][hi, lo]
 constexpr uint32_t OFF_B = OFF_A + 2 * OP_BYTES;        // [TC_S][hi, lo]
 constexpr uint32_t OFF_BIAS = OFF_B + TC_S * OP_BYTES;  // [TC_S][TC_N] float
 constexpr uint32_t OFF_BAR = OFF_BIAS + TC_S * TC_N * 4;
-constexpr uint32_t NBAR = 17;
+constexpr uint32_t NBAR = 18;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last, pool count
 constexpr uint32_t OFF_RED = OFF_MISC + 32;             // 16 floats
 constexpr uint32_t OFF_RETRY = OFF_RED + 64;            // TC_ROWS ints
@@ -64,7 +66,9 @@ __host__ __device__ constexpr int BAR_EMPTY(int s) { return TC_S + s; }
 __host__ __device__ constexpr int BAR_ACCFULL(int r, int u) { return 2 * TC_S + 2 * r + u; }
 __host__ __device__ constexpr int BAR_ACCEMPTY(int r, int u) { return 2 * TC_S + 4 + 2 * r + u; }
 __host__ __device__ constexpr int BAR_A() { return 2 * TC_S + 8; }
-static_assert(BAR_A() + 1 == (int)NBAR, "barrier count");
+__host__ __device__ constexpr int BAR_DRAIN() { return 2 * TC_S + 9; }  // every MMA of the CTA has completed
+static_assert(BAR_DRAIN() + 1 == (int)NBAR, "barrier count");
+static_assert(NBAR * 8 <= 256, "barriers fit the header");
 static_assert(TC_SMEM <= 227 * 1024, "shared memory budget");
 
 // Layout of the screened half-step: 256-column tiles (one 128 x 256 x 16 MMA
@@ -204,7 +208,27 @@ struct TcOps {
     const float* bias;          // [B][tiles_c * TC_N] column biases c_j, -inf past the last column
     const unsigned char* bias_img;  // [B][tiles_c] 16 KB tiles: fp16 bias parts (screened half-step)
     int tiles_r, tiles_c;
+    int hold_tile;                  // testing hook: the producer issues no copy from this column tile of its
+                                    // chunk on (-1: off), so the waits on it run out
+    unsigned long long wait_ns;     // limit of every bounded wait
 };
+
+// Host-side settings every tensor-core launch copies into TcOps.
+static std::atomic<int> g_hold_tile{-1};
+static std::atomic<int> g_hold_after{0};  // launches left alone before the hook applies
+static std::atomic<unsigned long long> g_wait_ns{TC_WAIT_NS};
+
+void tc_set_test_hold(int tile, int after, unsigned long long wait_ns) {
+    g_hold_after.store(after > 0 ? after : 0);
+    g_hold_tile.store(tile < 0 ? -1 : tile);
+    g_wait_ns.store(wait_ns > 0 ? wait_ns : TC_WAIT_NS);
+}
+
+static void tc_fill_waits(TcOps& ops) {
+    ops.hold_tile = g_hold_tile.load();
+    ops.wait_ns = g_wait_ns.load();
+    if (ops.hold_tile >= 0 && g_hold_after.load() > 0 && g_hold_after.fetch_sub(1) > 0) ops.hold_tile = -1;
+}
 
 // Column biases of one half-step, c_j = log2 w_j - state_j, padded with -inf
 // to whole tiles: the producer moves a tile's biases with one bulk copy.
@@ -354,6 +378,7 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
                 mbar_init(S.bar(BAR_ACCEMPTY(r, u)), accempty_count);
             }
         mbar_init(S.bar(BAR_A()), 1);
+        mbar_init(S.bar(BAR_DRAIN()), 1);
         S.misc()[1] = 0;
         S.misc()[2] = 0;
         S.misc()[4] = 0;
@@ -371,16 +396,28 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
 }
 
 // Never leave a bulk copy in flight into this CTA's shared memory: waits
-// (bounded) for the last TC_S stages issued and for the row tiles.
-__device__ __forceinline__ void tc_producer_drain(const TcSmem& S, int issued) {
+// (bounded, and not cut short by the abort flag) for the last TC_S stages
+// issued and for the row tiles.
+__device__ __forceinline__ void tc_producer_drain(const TcSmem& S, int issued, uint64_t wait_ns) {
     if ((threadIdx.x & 31) == 0) {
         int dummy = 0;
         for (int lt = (issued > TC_S ? issued - TC_S : 0); lt < issued; ++lt)
             mbar_wait_bounded(S.bar(BAR_FULL(lt % TC_S)), (uint32_t)(lt / TC_S) & 1u, (volatile int*)&dummy,
-                              TC_WAIT_NS);
-        mbar_wait_bounded(S.bar(BAR_A()), 0u, (volatile int*)&dummy, TC_WAIT_NS);
+                              wait_ns);
+        mbar_wait_bounded(S.bar(BAR_A()), 0u, (volatile int*)&dummy, wait_ns);
     }
     __syncwarp();
+}
+
+// Never leave an MMA in flight when the CTA frees TMEM and exits: the MMA
+// thread commits everything it issued to the drain barrier and waits for it
+// (bounded, and not cut short by the abort flag).  On the normal path the
+// MMAs have completed by then or are about to.
+__device__ __forceinline__ void tc_mma_drain(const TcSmem& S, bool issued_any, uint64_t wait_ns) {
+    if (!issued_any) return;
+    int dummy = 0;
+    tc_commit(S.bar(BAR_DRAIN()));
+    mbar_wait_bounded(S.bar(BAR_DRAIN()), 0u, (volatile int*)&dummy, wait_ns);
 }
 
 // Producer warp (lane 0 issues): the CTA's two row tiles once, then the
@@ -398,9 +435,10 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
     const float* gbias = ops.bias + (size_t)b * ops.tiles_c * TC_N;
     for (int lt = 0; lt < nt; ++lt) {
+        if (lt == ops.hold_tile) break;
         const int st = lt % TC_S;
         const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
+        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, ops.wait_ns)) break;
         if (lane == 0) {
             mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), OP_BYTES + TC_N * 4);
             bulk_g2s(S.sbase + OFF_B + (uint32_t)st * OP_BYTES, bimg + (size_t)(t0 + lt) * OP_BYTES, OP_BYTES,
@@ -410,26 +448,28 @@ __device__ void tc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
         }
         issued = lt + 1;
     }
-    tc_producer_drain(S, issued);
+    tc_producer_drain(S, issued, ops.wait_ns);
 }
 
 // MMA warp (one thread): per column tile and row tile, 12 MMAs of
 // 128 x 128 x 16 -- lo*hi and hi*lo first, then hi*hi -- into the row tile's
 // TMEM buffer (lt & 1); commits signal the epilogue and free the stage.
-__device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
+__device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns) {
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
-        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, TC_WAIT_NS);
+        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, wait_ns);
+        bool issued_any = false;
         const uint32_t idesc = f16_idesc(TC_M, TC_N);
         for (int lt = 0; ok && lt < nt; ++lt) {
             const int st = lt % TC_S;
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, wait_ns)) break;
             for (int r = 0; r < 2 && ok; ++r) {
-                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, u)), pu ^ 1u, abort, TC_WAIT_NS)) { ok = false; break; }
+                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, u)), pu ^ 1u, abort, wait_ns)) { ok = false; break; }
                 tc_fence_after();
+                issued_any = true;
                 const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
                 const uint32_t ahi = S.sbase + OFF_A + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
                 const uint32_t bhi = S.sbase + OFF_B + (uint32_t)st * OP_BYTES, blo = bhi + TILE_BYTES;
@@ -449,6 +489,7 @@ __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt) {
             if (!ok) break;
             tc_commit(S.bar(BAR_EMPTY(st)));
         }
+        tc_mma_drain(S, issued_any, wait_ns);
     }
     __syncwarp();
 }
@@ -577,7 +618,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     if (warp == 0) {
         tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma(S, tmem, nt);
+        tc_mma(S, tmem, nt, ops.wait_ns);
     } else {
         // ---------------- epilogue: exponentials and row sums ----------------
         m = erow ? stabiliser(p.cold, p.lo_in, b, old) : INFINITY;
@@ -589,8 +630,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
-            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, ops.wait_ns)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, ops.wait_ns)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
             const float* cb = bias + st * TC_N;
@@ -712,6 +753,7 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
     ops.bias = plan.bias;
     ops.bias_img = nullptr;
+    tc_fill_waits(ops);
     {
         const cudaError_t eb = launch_tc_bias(plan, p, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;
@@ -777,9 +819,10 @@ __device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
     const unsigned char* gbias = ops.bias_img + (size_t)b * (ops.tiles_c / 2) * SC_BT;
     for (int lt = 0; lt < nt; ++lt) {
+        if (lt == ops.hold_tile) break;
         const int st = lt % TC_S;
         const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, TC_WAIT_NS)) break;
+        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, ops.wait_ns)) break;
         if (lane == 0) {
             const uint32_t dst = S.sbase + SC_OFF_B + (uint32_t)st * SC_STAGE;
             const unsigned char* src = bimg + (size_t)(t0 + 2 * lt) * OP_BYTES;
@@ -790,29 +833,31 @@ __device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
         }
         issued = lt + 1;
     }
-    tc_producer_drain(S, issued);
+    tc_producer_drain(S, issued, ops.wait_ns);
 }
 
 // MMA warp of the screened half-step (one thread): per 256-column tile and
 // row tile r, four 128 x 256 x 16 hi*hi MMAs and the bias step (row-side
 // constants times the tile's bias block) into the row tile's accumulator
 // (TMEM columns 256 r ..); the epilogue frees it after loading it.
-__device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt) {
+__device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns) {
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
-        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, TC_WAIT_NS);
+        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, wait_ns);
+        bool issued_any = false;
         const uint32_t idesc = f16_idesc(TC_M, SC_N);
         for (int lt = 0; ok && lt < nt; ++lt) {
             const int st = lt % TC_S;
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, wait_ns)) break;
             const uint32_t bst = S.sbase + SC_OFF_B + (uint32_t)st * SC_STAGE;
             for (int r = 0; r < 2 && ok; ++r) {
-                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, 0)), ((uint32_t)lt & 1u) ^ 1u, abort, TC_WAIT_NS)) {
+                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, 0)), ((uint32_t)lt & 1u) ^ 1u, abort, wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                issued_any = true;
                 const uint32_t d = tmem + (uint32_t)(r * SC_N);
                 const uint32_t ahi = S.sbase + SC_OFF_A + (uint32_t)r * TILE_BYTES;
 #pragma unroll
@@ -827,6 +872,7 @@ __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt) {
             if (!ok) break;
             tc_commit(S.bar(BAR_EMPTY(st)));
         }
+        tc_mma_drain(S, issued_any, wait_ns);
     }
     __syncwarp();
 }
@@ -982,7 +1028,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     if (warp == 0) {
         sc_producer(S, ops, b, rb, t0, nts);
     } else if (warp == 1) {
-        sc_mma(S, tmem, nts);
+        sc_mma(S, tmem, nts, ops.wait_ns);
     } else {
         // Screening: epilogue warp (wg, q4) reads columns 128 wg .. of both row tiles'
         // accumulators for TMEM lanes 32 q4 ..: rows row0 + 32 q4 + lane (tile 0) and
@@ -1021,7 +1067,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         for (int lt = 0; ok && lt < nts; ++lt) {
 #pragma unroll
             for (int rt = 0; rt < 2; ++rt) {
-                if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(rt, 0)), (uint32_t)lt & 1u, abort, TC_WAIT_NS)) {
+                if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(rt, 0)), (uint32_t)lt & 1u, abort, ops.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -1260,6 +1306,7 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
     ops.bias = plan.bias;
     ops.bias_img = plan.bimg;
+    tc_fill_waits(ops);
     {
         const cudaError_t eb = launch_tc_bias_image(plan, p, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;
@@ -1348,7 +1395,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     if (warp == 0) {
         tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma(S, tmem, nt);
+        tc_mma(S, tmem, nt, ops.wait_ns);
     } else {
         const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
         m = erow ? lrow - SOT_STAB_BIAS : INFINITY;
@@ -1362,8 +1409,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, TC_WAIT_NS)) break;
-            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, TC_WAIT_NS)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, ops.wait_ns)) break;
+            if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, ops.wait_ns)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
             const float* cb = S.bias() + st * TC_N;
@@ -1563,6 +1610,7 @@ cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfAr
     ops.tiles_c = plan.tiles_y;
     ops.bias = plan.bias;
     ops.bias_img = nullptr;
+    tc_fill_waits(ops);
     {
         const cudaError_t eb = launch_tc_bias(plan, hp, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;

@@ -84,7 +84,10 @@ struct CooArgs {
     const float* Mr;      // [B][n] row maxima of the f-side score (log2)
     const float* Mc;      // [B][m] column maxima of the g-side score (log2)
     const float* a;       // linear weights or NULL
+    const float *X, *Y;   // the caller's points [B][n][d], [B][m][d] (stored values)
+    const float *f, *g;   // the caller's potentials (stored values)
     float two_kappa, kappa, log2tau;
+    float kap_hi, kap_lo; // 1 / (eps ln 2) as a float-float pair (stored values)
     int dirs;
     int* counts;               // [B*n] count pass output
     const long long* rowptr;   // [B*n+1] write pass input (global offsets)
@@ -143,6 +146,10 @@ cudaError_t launch_decide(const float* errpart, int B, int parts, float tol, int
                           float* err_out, int* stop_flag, int* conv_flag, const float* L_next,
                           float* L_cur, int count, cudaStream_t st);
 cudaError_t launch_count_iter(const int* stop_flag, int* counter, cudaStream_t st);
+// OR a call's status word into the device's word for asynchronous calls.
+cudaError_t launch_status_merge(const int* status, cudaStream_t st);
+// Read and clear that word (synchronises `st`).
+cudaError_t read_clear_async_status(cudaStream_t st, unsigned* out);
 cudaError_t launch_check_inputs(const float* X, const float* w, long long count_pts, int d,
                                 long long count_w, int* bad, cudaStream_t st);
 cudaError_t launch_scan_counts(const int* counts, int B, int n, long long* rowptr,

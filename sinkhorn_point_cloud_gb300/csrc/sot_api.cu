@@ -781,8 +781,24 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     sv.cluster_allowed = (path == PATH_POINT) && !(s->flags & SOT_NO_CLUSTER);
     rc = run_schedule(sv, *s, f, g, f, g, st);
     if (rc) return rc;
+    if (!st) SOT_CUDA(launch_status_merge(sv.dflags, sv.st));  // asynchronous: reported by sot_async_status
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "%s", cudaGetErrorString(e));
+    return SOT_OK;
+}
+
+int sot_async_status(void* stream) {
+    g_err[0] = 0;
+    unsigned v = 0;
+    SOT_CUDA(read_clear_async_status((cudaStream_t)stream, &v));
+    if (v & SOT_DEV_TIMEOUT)
+        return fail(SOT_ERR_TIMEOUT, "a bounded device-side wait gave up in an asynchronous call; its rows are NaN");
+    return SOT_OK;
+}
+
+int sot_test_hold_tile(int tile, int after_launches, long long wait_ns) {
+    g_err[0] = 0;
+    tc_set_test_hold(tile, after_launches, wait_ns > 0 ? (unsigned long long)wait_ns : 0ull);
     return SOT_OK;
 }
 
@@ -861,6 +877,7 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "plan-apply launch failed: %s", cudaGetErrorString(e));
     if (cost) SOT_CUDA(launch_reduce_parts(cpart, B, p.rowtiles, cost, cs));
     if (grad && (flags & SOT_COST_COSINE)) SOT_CUDA(launch_cosine_grad(Xin, (long long)B * n, d, grad, cs));
+    SOT_CUDA(launch_status_merge(sv.dflags, cs));  // asynchronous: reported by sot_async_status
     return SOT_OK;
 }
 
@@ -954,6 +971,57 @@ int sot_cost_grad(const float* X, const float* Y, const float* a, const float* b
     return sot_plan_apply(X, Y, a, b, B, n, m, d, f, g, eps, cost, grad, nullptr, 0, stream);
 }
 
+namespace {
+// Everything the COO passes read, prepared once: the solver's packed clouds and
+// states for (f, g), and the row and column maxima of the two scores (computed
+// by the maximum passes with the predicate's own fp32 chain).
+struct CooPrep {
+    Solver sv;
+    CooArgs p;
+    CooPrep(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+            cudaStream_t cs)
+        : sv(X, Y, a, b, B, n, m, d, d <= 3 ? PATH_POINT : PATH_DENSE, cs) {}
+    int run(const float* f, const float* g, float eps, float threshold, int dirs) {
+        const int B = sv.B, n = sv.n, m = sv.m, d = sv.d;
+        if (d > dense_max_d()) return fail(SOT_ERR_UNSUPPORTED, "COO extraction supports d <= %d", dense_max_d());
+        int rc = sv.prepare(0);
+        if (rc) return rc;
+        const float kappa = 1.f / (eps * SOT_LN2_D);
+        rc = sv.init_states(f, g, kappa);
+        if (rc) return rc;
+        float* Mr = sv.S.alloc<float>((size_t)B * n);
+        float* Mc = sv.S.alloc<float>((size_t)B * m);
+        int* counts = sv.S.alloc<int>((size_t)B * n);
+        long long* rowptr = sv.S.alloc<long long>((size_t)B * n + 1);
+        if (!Mr || !Mc || !counts || !rowptr) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+        rc = sv.half(0, MODE_MAX, kappa, true, nullptr, Mr, nullptr, false);
+        if (rc) return rc;
+        rc = sv.half(1, MODE_MAX, kappa, true, nullptr, Mc, nullptr, false);
+        if (rc) return rc;
+        p.B = B; p.n = n; p.m = m; p.d = d;
+        p.xpack = sv.xpack; p.ypack = sv.ypack; p.lw2x = sv.lw2x; p.lw2y = sv.lw2y;
+        p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam; p.Mr = Mr; p.Mc = Mc; p.a = sv.a;
+        p.X = sv.X; p.Y = sv.Y; p.f = f; p.g = g;
+        p.two_kappa = 2.f * kappa; p.kappa = kappa;
+        const double kap = 1.0 / ((double)eps * SOT_LN2_D);
+        p.kap_hi = (float)kap;
+        p.kap_lo = (float)(kap - (double)p.kap_hi);
+        p.log2tau = threshold > 0.f ? log2f(threshold) : -INFINITY;
+        p.dirs = dirs;
+        p.counts = counts; p.rowptr = rowptr; p.rows = nullptr; p.cols = nullptr; p.vals = nullptr;
+        p.capacity = 0;
+        return SOT_OK;
+    }
+};
+
+int check_coo_args(float eps, float threshold, int dirs) {
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (!(threshold >= 0.f && threshold <= 1.f)) return fail(SOT_ERR_INVALID_ARG, "threshold must lie in [0, 1]");
+    if (dirs < 1 || dirs > 3) return fail(SOT_ERR_INVALID_ARG, "dirs must be 1, 2 or 3");
+    return SOT_OK;
+}
+}  // namespace
+
 int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
                  const float* f, const float* g, float eps, float threshold, int dirs, long long capacity, int* rows,
                  int* cols, float* vals, long long* batch_offsets, long long* nnz_host, void* stream) {
@@ -962,43 +1030,23 @@ int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b,
     if (rc) return rc;
     if (!nnz_host) return fail(SOT_ERR_INVALID_ARG, "nnz_host must not be NULL");
     *nnz_host = 0;
-    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
-    if (!(threshold >= 0.f && threshold <= 1.f)) return fail(SOT_ERR_INVALID_ARG, "threshold must lie in [0, 1]");
-    if (dirs < 1 || dirs > 3) return fail(SOT_ERR_INVALID_ARG, "dirs must be 1, 2 or 3");
+    rc = check_coo_args(eps, threshold, dirs);
+    if (rc) return rc;
     if (capacity < 0) return fail(SOT_ERR_INVALID_ARG, "capacity must be >= 0");
     if (B > 0 && (!f || !g || !batch_offsets)) return fail(SOT_ERR_INVALID_ARG, "f, g, batch_offsets must not be NULL");
     if (B == 0) return SOT_OK;
     if (capacity > 0 && (!rows || !cols || !vals)) return fail(SOT_ERR_INVALID_ARG, "rows, cols, vals must not be NULL");
     cudaStream_t cs = (cudaStream_t)stream;
-    Solver sv(X, Y, a, b, B, n, m, d, d <= 3 ? PATH_POINT : PATH_DENSE, cs);
-    if (d > dense_max_d()) return fail(SOT_ERR_UNSUPPORTED, "COO extraction supports d <= %d", dense_max_d());
-    rc = sv.prepare(0);
+    CooPrep cp(X, Y, a, b, B, n, m, d, cs);
+    rc = cp.run(f, g, eps, threshold, dirs);
     if (rc) return rc;
-    const float kappa = 1.f / (eps * SOT_LN2_D);
-    rc = sv.init_states(f, g, kappa);
-    if (rc) return rc;
-    float* Mr = sv.S.alloc<float>((size_t)B * n);
-    float* Mc = sv.S.alloc<float>((size_t)B * m);
-    int* counts = sv.S.alloc<int>((size_t)B * n);
-    long long* rowptr = sv.S.alloc<long long>((size_t)B * n + 1);
-    long long* dnnz = sv.S.alloc<long long>(1);
-    if (!Mr || !Mc || !counts || !rowptr || !dnnz) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
-    rc = sv.half(0, MODE_MAX, kappa, true, nullptr, Mr, nullptr, false);
-    if (rc) return rc;
-    rc = sv.half(1, MODE_MAX, kappa, true, nullptr, Mc, nullptr, false);
-    if (rc) return rc;
-    CooArgs p;
-    p.B = B; p.n = n; p.m = m; p.d = d;
-    p.xpack = sv.xpack; p.ypack = sv.ypack; p.lw2x = sv.lw2x; p.lw2y = sv.lw2y;
-    p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam; p.Mr = Mr; p.Mc = Mc; p.a = a;
-    p.two_kappa = 2.f * kappa; p.kappa = kappa;
-    p.log2tau = threshold > 0.f ? log2f(threshold) : -INFINITY;
-    p.dirs = dirs;
-    p.counts = counts; p.rowptr = rowptr; p.rows = rows; p.cols = cols; p.vals = vals;
+    CooArgs& p = cp.p;
+    p.rows = rows; p.cols = cols; p.vals = vals;
     p.capacity = capacity;
     cudaError_t e = (d <= 3) ? launch_point_coo(p, 0, cs) : launch_dense_coo(p, 0, cs);
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "COO count launch failed: %s", cudaGetErrorString(e));
-    SOT_CUDA(launch_scan_counts(counts, B, n, rowptr, batch_offsets, cs));
+    long long* rowptr = const_cast<long long*>(p.rowptr);
+    SOT_CUDA(launch_scan_counts(p.counts, B, n, rowptr, batch_offsets, cs));
     long long nnz = 0;
     SOT_CUDA(cudaMemcpyAsync(&nnz, rowptr + (size_t)B * n, sizeof(long long), cudaMemcpyDeviceToHost, cs));
     SOT_CUDA(cudaStreamSynchronize(cs));
@@ -1008,6 +1056,44 @@ int sot_plan_coo(const float* X, const float* Y, const float* a, const float* b,
         e = (d <= 3) ? launch_point_coo(p, 1, cs) : launch_dense_coo(p, 1, cs);
         if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "COO write launch failed: %s", cudaGetErrorString(e));
     }
+    return SOT_OK;
+}
+
+int sot_plan_coo_operands(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                          const float* f, const float* g, float eps, float threshold, float* xc, float* lwx, float* Lx,
+                          float* yc, float* lwy, float* Ly, float* Mr, float* Mc, float* scalars_host, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    rc = check_coo_args(eps, threshold, 3);
+    if (rc) return rc;
+    if (!scalars_host) return fail(SOT_ERR_INVALID_ARG, "scalars_host must not be NULL");
+    if (B == 0) return SOT_OK;
+    if (!f || !g || !xc || !lwx || !Lx || !yc || !lwy || !Ly || !Mr || !Mc)
+        return fail(SOT_ERR_INVALID_ARG, "f, g and every output must not be NULL");
+    cudaStream_t cs = (cudaStream_t)stream;
+    CooPrep cp(X, Y, a, b, B, n, m, d, cs);
+    rc = cp.run(f, g, eps, threshold, 3);
+    if (rc) return rc;
+    const CooArgs& p = cp.p;
+    const size_t fs = sizeof(float);
+    for (int side = 0; side < 2; ++side) {
+        const size_t cnt = (size_t)B * (side ? m : n);
+        const float* pack = side ? p.ypack : p.xpack;
+        float* oc = side ? yc : xc;
+        float* ow = side ? lwy : lwx;
+        if (d <= 3) {  // float4 (coordinates, log2 w) per point
+            SOT_CUDA(cudaMemcpy2DAsync(oc, d * fs, pack, 4 * fs, d * fs, cnt, cudaMemcpyDeviceToDevice, cs));
+            SOT_CUDA(cudaMemcpy2DAsync(ow, fs, pack + 3, 4 * fs, fs, cnt, cudaMemcpyDeviceToDevice, cs));
+        } else {
+            SOT_CUDA(cudaMemcpyAsync(oc, pack, cnt * d * fs, cudaMemcpyDeviceToDevice, cs));
+            SOT_CUDA(cudaMemcpyAsync(ow, side ? p.lw2y : p.lw2x, cnt * fs, cudaMemcpyDeviceToDevice, cs));
+        }
+        SOT_CUDA(cudaMemcpyAsync(side ? Ly : Lx, side ? p.Lam : p.L, cnt * fs, cudaMemcpyDeviceToDevice, cs));
+        SOT_CUDA(cudaMemcpyAsync(side ? Mc : Mr, side ? p.Mc : p.Mr, cnt * fs, cudaMemcpyDeviceToDevice, cs));
+    }
+    scalars_host[0] = p.kappa;
+    scalars_host[1] = p.log2tau;
     return SOT_OK;
 }
 

@@ -33,6 +33,11 @@ struct TcScreen {
     int* ovf = nullptr;       // running count of lost rows
 };
 
+// Testing hook for the timeout path: after `after` more tensor-core launches,
+// every tensor-core producer issues no copy from column tile `tile` of its
+// chunk on (tile < 0: off), and every bounded wait gives up after wait_ns
+// (0: 2 s).
+void tc_set_test_hold(int tile, int after, unsigned long long wait_ns);
 bool tc_supported(int d);
 int tc_max_d();
 int tc_rows_per_cta();

@@ -121,6 +121,31 @@ def test_tc_full_size_column_marginals(sot):
         assert abs(col - b64[j]) / b64[j] < 5e-3, (j, col / b64[j])
 
 
+def test_tc_full_size_cost_gradient_and_error(sot, orc):
+    """n = m = 70000, d = 64, as bench.py runs it: 100 iterations, then the
+    cost and the gradient from the tensor-core plan application.  The oracle
+    applies the plan of the GPU's own fp32 potentials over every pair
+    ("FlashSinkhorn", Methodologie 3): cost and gradient (all rows) within
+    1e-4, and the marginal error the solve reports equals the oracle's
+    sum_i |sum_j P_ij - a_i| of the same potentials."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4)
+    eps = 0.1
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    f, g, info = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=100, max_iters=100, stats=True)
+    c, gr, r = sot.sot_plan_apply(Xd, Yd, ad, bd, f, g, eps, rowsum=True)
+    sot.sot_async_status()
+    out = orc.plan_apply(X[0], Y[0], a[0], b[0], host(f)[0], host(g)[0], eps)
+    ec = abs(host(c)[0] - out["cost"]) / abs(out["cost"])
+    egr = normwise(host(gr)[0], out["grad"])
+    er = normwise(host(r)[0], out["rowsum"])
+    err_ref = float(np.sum(np.abs(out["rowsum"] - a[0].astype(np.float64))))
+    print(f"70000 points: cost {ec:.2e} grad {egr:.2e} rowsum {er:.2e}; marginal error GPU {info['err'][0]:.4e} "
+          f"oracle {err_ref:.4e}")
+    assert ec < TOL and egr < TOL and er < TOL, (ec, egr, er)
+    assert abs(info["err"][0] - err_ref) <= 1e-2 * err_ref + 1e-7, (info["err"][0], err_ref)
+
+
 @pytest.mark.parametrize("n,m,B", [(1000, 1100, 1), (300, 257, 2)])
 def test_tc_plan_apply_matches_oracle(sot, orc, n, m, B):
     """Cost, gradient and row sums from the tensor-core plan application, with
