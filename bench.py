@@ -678,6 +678,67 @@ def run_apml(args, ws, rank, local):
     return 0
 
 
+def run_hvp(args, ws, rank, local):
+    """Hessian-vector products (sot_hvp) on a d <= 9 workload, from potentials
+    solved once before the timed region: one step is one H V with exactly
+    `args.hvp` conjugate-gradient steps (cg_tol = 0), i.e. 3 + 2 K transport
+    products of n x m pairs per cloud.  Same timing rules as the solver line."""
+    import torch
+    import sinkhorn_point_cloud_gb300 as sot
+
+    dev = setup_device(ws, local)
+    wid = args.workload
+    w = datagen.WORKLOADS[wid]
+    B, n, m, d, eps = w["B"], w["n"], w["m"], w["d"], w["eps"]
+    if args.n:
+        n = m = args.n
+    X, Y, a, b = datagen.make_batch(wid, B=B, n=n, m=m, clouds=range(rank * B, rank * B + B))
+    weighted = w["kind"] == "gauss"
+    Xd, Yd = torch.from_numpy(X).to(dev), torch.from_numpy(Y).to(dev)
+    ad, bd = (torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)) if weighted else (None, None)
+    iters = args.iters or w.get("iters") or 100
+    f, g = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=iters, max_iters=iters)
+    rng = np.random.default_rng(20260800 + rank)
+    host_v = torch.from_numpy(rng.standard_normal((B, n, d)).astype(np.float32)).pin_memory()
+    Vd = host_v.to(dev)
+    out = torch.empty(B, n, d, device=dev)
+    K = args.hvp
+    t_max, clocks, launches = time_steps(
+        lambda: sot.sot_hvp(Xd, Yd, ad, bd, f, g, eps, Vd, cg_iters=K, cg_tol=0.0, out=out), args, ws, local, dev)
+    if rank != 0:
+        return 0
+    pairs_step = (3 + 2 * K) * B * n * m
+    pk, pk_kind = peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rates = alu_rates()
+    lanes = rates["ffma_lanes_per_sm_clk"] if rates else 128.0
+    mhz = float(pk.get("sm_max_mhz", 2070.0))
+    ops_pair = 2 * d + 1  # the transport kernel's fp32 screen of every pair
+    achieved = ops_pair * pairs_step * args.steps / t_max / 1e12
+    peak = lanes * sms * mhz * 1e6 / 1e12
+    line = {
+        "metric": f"Hessian-vector products/s ({w['name']}, {K} CG steps)",
+        "value": ws * B * args.steps / t_max, "unit": "HVP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w["name"], "B": B, "n": n, "m": m, "d": d, "eps": eps, "cg_iters": K,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "pair_evals_per_s": ws * pairs_step * args.steps / t_max / 1e9, "pair_evals_unit": UNIT,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"FP32 lanes/SM/clk from the ALU probe x {sms} SMs x {mhz:.0f} MHz",
+                     "kernel": f"transport_kernel ({ops_pair} FP32 lane-ops per pair in the screen, "
+                               f"{3 + 2 * K} products per step)"},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": int(launches),
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -703,6 +764,8 @@ def main(argv=None):
     ap.add_argument("--grad-y", action="store_true", help="with --transport: time sot_grad_y instead")
     ap.add_argument("--apml", type=int, default=0, metavar="K",
                     help="time sparse APML with K normalisations on the workload's COO support instead")
+    ap.add_argument("--hvp", type=int, default=0, metavar="K",
+                    help="time Hessian-vector products with K CG steps on a d <= 9 workload instead")
     ap.add_argument("--cost", choices=["sqeuclidean", "cosine"], default="sqeuclidean",
                     help="cost function (cosine: 2 - 2 cos, on the normalised points)")
     args = ap.parse_args(argv)
@@ -715,6 +778,8 @@ def main(argv=None):
         return run_transport(args, ws, rank, local)
     if args.apml:
         return run_apml(args, ws, rank, local)
+    if args.hvp:
+        return run_hvp(args, ws, rank, local)
     return run_gpu(args, ws, rank, local)
 
 

@@ -178,6 +178,29 @@ int sot_transport_apply(const float* X, const float* Y, const float* a, const fl
 int sot_grad_y(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
                const float* f, const float* g, float eps, float* grad_y, int flags, void* stream);
 
+/*
+ * Hessian-vector product of the entropic OT loss with respect to X
+ * ("FlashSinkhorn", Methodologie 3, HVP paragraph: streamed as transport-vector
+ * and transport-matrix products, P never stored).  Reading: the Hessian of the
+ * converged loss, whose gradient is 2 sum_j P_ij (x_i - y_j), with the
+ * potentials' first-order change keeping both marginals fixed:
+ *   out = H V,  V and out [B][n][d] fp32 device arrays (row-major, caller-owned).
+ * The marginal system is solved by conjugate gradients preconditioned with the
+ * column sums of P: at most cg_iters steps, all clouds at once, stopping when
+ * every cloud's preconditioned residual has fallen to cg_tol of its start
+ * (checked every 8 steps; a cloud that is done keeps its solution).  Each step
+ * is one P u and one P^T u.  The assembly forms its sums pair by pair around
+ * each row's barycentre.  The clouds are first moved by their common centre
+ * (H does not change).  Squared-Euclidean cost, d <= 9, flags must be 0.  f, g
+ * are the potentials the plan is built from (converged ones for the Hessian of
+ * the loss).  Synchronises `stream` every 8 CG steps; scratch O((n + m) d).
+ * Errors: SOT_ERR_INVALID_ARG (sizes, eps, cg arguments, NULL pointers, flags),
+ * SOT_ERR_UNSUPPORTED (d > 9), SOT_ERR_NOMEM, SOT_ERR_CUDA.
+ */
+int sot_hvp(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+            const float* f, const float* g, float eps, const float* V, int cg_iters, float cg_tol, float* out,
+            int flags, void* stream);
+
 /* Convenience forms of sot_plan_apply (precision auto). */
 int sot_cost(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
              const float* f, const float* g, float eps, float* cost, void* stream);

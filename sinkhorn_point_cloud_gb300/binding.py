@@ -100,6 +100,7 @@ def load(path: str | None = None):
         "sot_grad_y": [P, P, P, P, i, i, i, i, P, P, f, P, i, P],
         "sot_apml_coo": [P, P, P, P, i, i, i, i, P, P, P, ll, f, i, P, P, P, P],
         "sot_async_status": [P],
+        "sot_hvp": [P, P, P, P, i, i, i, i, P, P, f, P, i, f, P, i, P],
         "sot_test_hold_tile": [i, i, ll],
         "sot_plan_coo_operands": [P, P, P, P, i, i, i, i, P, P, f, f, P, P, P, P, P, P, P, P,
                                   C.POINTER(C.c_float), P],
@@ -308,6 +309,20 @@ def sot_grad_y(X, Y, a, b, f, g, eps, flags=0, out=None, stream=None):
     rc = load().sot_grad_y(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g), float(eps), _ptr(o),
                            int(flags), _stream(stream))
     _check(rc, "sot_grad_y")
+    return o
+
+
+def sot_hvp(X, Y, a, b, f, g, eps, V, cg_iters=300, cg_tol=1e-5, out=None, stream=None):
+    """Hessian-vector product of the entropic OT loss with respect to X at the
+    potentials (f, g), applied to V [B, n, d]; returns H V [B, n, d]."""
+    X, Y, B, n, m, d = _shapes(X, Y, a, b)
+    _potentials_args(f, g, B, n, m, X.device)
+    _want(V, "V", B * n * d, X.device)
+    o = torch.empty(B, n, d, device=X.device, dtype=torch.float32) if out is None else out
+    _want(o, "out", B * n * d, X.device)
+    rc = load().sot_hvp(_ptr(X), _ptr(Y), _ptr(a), _ptr(b), B, n, m, d, _ptr(f), _ptr(g), float(eps), _ptr(V),
+                        int(cg_iters), float(cg_tol), _ptr(o), 0, _stream(stream))
+    _check(rc, "sot_hvp")
     return o
 
 

@@ -42,7 +42,14 @@ static size_t tr_smem_bytes(int d, int c) {
     return sizeof(float) * ((size_t)TR_T * tr_ldx(d) + (size_t)d * TR_YS + (size_t)TR_CT * c + 2 * TR_CT);
 }
 
-template <int CV, int W>
+// CENTRED (row-centred products for the Hessian-vector product, d <= TR_CD):
+// per row i, with yhat_i = p.rc[i] and v_i = p.rv[i] (both [d]) and the
+// column values g_j = V[j][0] (c = 1), out[i] = [ sum_j w_ij ((y_j - yhat_i).v_i)(y_j - yhat_i),
+// sum_j w_ij g_j (y_j - yhat_i) ] (2d values): the differences are formed per
+// pair, so no two large sums cancel.
+constexpr int TR_CD = 9;
+
+template <int CV, int W, bool CENTRED = false>
 __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     static_assert(W == 4 || W == 8, "column group of 4 or 8");
     extern __shared__ float smem[];
@@ -74,6 +81,18 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
 #pragma unroll
     for (int k = 0; k < CV; ++k) acc[k] = 0.f;
     const float* xr = xs + threadIdx.x * ldx;
+    // centred mode: the row's barycentre and direction, and the two sums
+    float yh[CENTRED ? TR_CD : 1], vr[CENTRED ? TR_CD : 1], aco[CENTRED ? TR_CD : 1], agy[CENTRED ? TR_CD : 1];
+    if (CENTRED) {
+#pragma unroll
+        for (int k = 0; k < TR_CD; ++k) {
+            const bool kk = ok && k < d;
+            yh[k] = kk ? p.rc[((size_t)b * p.nr + i) * d + k] : 0.f;
+            vr[k] = kk ? p.rv[((size_t)b * p.nr + i) * d + k] : 0.f;
+            aco[k] = 0.f;
+            agy[k] = 0.f;
+        }
+    }
 
     for (int base = c_begin; base < c_end; base += TR_CT) {
         __syncthreads();
@@ -131,13 +150,39 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
                 const float2 ell = ff_add(ff_mul(kap, pot), two_sum(ls[jj], lwi));
                 const float w = exp2f(__fadd_rn(ell.x, ell.y));
                 const float* vj = vs + jj * c;
+                if (CENTRED) {
+                    // y_j - yhat_i (the tile holds -y_j), its projection on v_i
+                    float dk[TR_CD], dv = 0.f;
 #pragma unroll
-                for (int k = 0; k < CV; ++k)
-                    if (k < c) acc[k] = fmaf(w, vj[k], acc[k]);
+                    for (int k = 0; k < TR_CD; ++k) {
+                        dk[k] = (k < d) ? -ys[k * TR_YS + jj] - yh[k] : 0.f;
+                        dv = fmaf(dk[k], vr[k], dv);
+                    }
+                    const float wdv = w * dv, wg = w * vj[0];
+#pragma unroll
+                    for (int k = 0; k < TR_CD; ++k) {
+                        aco[k] = fmaf(wdv, dk[k], aco[k]);
+                        agy[k] = fmaf(wg, dk[k], agy[k]);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < CV; ++k)
+                        if (k < c) acc[k] = fmaf(w, vj[k], acc[k]);
+                }
             }
         }
     }
-    if (ok) {
+    if (ok && CENTRED) {
+        // 2d outputs per row: the partial layout uses a row width of 2d
+        float* o = p.split > 1 ? p.part + (((size_t)ch * p.B + b) * p.nr + i) * (2 * d)
+                               : p.out + ((size_t)b * p.nr + i) * p.ldo;
+#pragma unroll
+        for (int k = 0; k < TR_CD; ++k)
+            if (k < d) {
+                o[k] = aco[k];
+                o[d + k] = agy[k];
+            }
+    } else if (ok) {
         float* o = p.split > 1 ? p.part + (((size_t)ch * p.B + b) * p.nr + i) * c
                                : p.out + ((size_t)b * p.nr + i) * p.ldo;
 #pragma unroll
@@ -185,6 +230,29 @@ size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* ch
     *chunk = tpc * TR_CT;
     *split = (nc + *chunk - 1) / *chunk;
     return *split > 1 ? (size_t)*split * B * nr * c : 0;
+}
+
+// Row-centred products (see CENTRED above): V holds g (c = 1, ldv = 1), out has
+// ldo >= 2d; p.rc, p.rv are [B][nr][d].  The partial sums need split * B * nr * 2d floats.
+cudaError_t launch_transport_centred(const TransportArgs& p, cudaStream_t st) {
+    if (p.d < 1 || p.d > TR_CD || p.c != 1 || p.ldv != 1 || p.ldo < 2 * p.d || !p.rc || !p.rv || p.B < 1 ||
+        p.nr < 1 || p.nc < 1 || p.split < 1 || p.chunk < 1 || (long long)p.split * p.chunk < p.nc ||
+        (p.split > 1 && !p.part))
+        return cudaErrorInvalidValue;
+    const size_t sm = tr_smem_bytes(p.d, 1);
+    dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
+    auto kern = (p.d > 8) ? transport_kernel<1, 8, true> : transport_kernel<1, 4, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    kern<<<grid, block, sm, st>>>(p);
+    if (p.split > 1) {
+        const long long count = (long long)p.B * p.nr * 2 * p.d;
+        count_launches(1);
+        transport_merge_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(p.part, count, p.split, 2 * p.d,
+                                                                                 p.ldo, p.out);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {

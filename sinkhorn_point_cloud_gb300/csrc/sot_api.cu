@@ -19,6 +19,7 @@
 #include "kernels.h"
 #include "sot.h"
 #include "apml.h"
+#include "hvp.h"
 #include "tc.h"
 #include "transport.h"
 
@@ -952,6 +953,130 @@ int sot_grad_y(const float* X, const float* Y, const float* a, const float* b, i
     }
     SOT_CUDA(launch_grad_finish(Y, b, B, m, d, grad_y, cs));
     if (flags & SOT_COST_COSINE) SOT_CUDA(launch_cosine_grad(Yin, (long long)B * m, d, grad_y, cs));
+    return SOT_OK;
+}
+
+int sot_hvp(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+            const float* f, const float* g, float eps, const float* V, int cg_iters, float cg_tol, float* out,
+            int flags, void* stream) {
+    g_err[0] = 0;
+    int rc = check_sizes(X, Y, B, n, m, d);
+    if (rc) return rc;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return fail(SOT_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (d > HVP_MAX_D) return fail(SOT_ERR_UNSUPPORTED, "sot_hvp supports d <= %d (got %d)", HVP_MAX_D, d);
+    if (flags) return fail(SOT_ERR_INVALID_ARG, "sot_hvp takes no flags (squared-Euclidean cost only)");
+    if (cg_iters < 1 || !(cg_tol >= 0.f) || !std::isfinite(cg_tol))
+        return fail(SOT_ERR_INVALID_ARG, "cg_iters must be >= 1 and cg_tol finite and >= 0");
+    if (B > 0 && (!f || !g || !V || !out)) return fail(SOT_ERR_INVALID_ARG, "f, g, V and out must not be NULL");
+    if (B == 0) return SOT_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    const int c1 = 1 + d, c2 = 3 + d;
+    const long long rn = (long long)B * n, rm = (long long)B * m;
+    const double kap = 1.0 / ((double)eps * SOT_LN2_D);
+    const int sms = device_sms();
+    size_t nparts = 0;  // partial-sum scratch: the largest any of the products needs
+    {
+        int s, ch;
+        nparts = std::max(nparts, transport_plan(B, n, m, std::max(c1, 2 * d), sms, &s, &ch));
+        nparts = std::max(nparts, transport_plan(B, m, n, c2, sms, &s, &ch));
+    }
+    Scratch S(cs);
+    const size_t rmax = (size_t)B * std::max(n, m);
+    float* shift = S.alloc<float>((size_t)B * d);
+    float* Xc = S.alloc<float>((size_t)rn * d);
+    float* Yc = S.alloc<float>((size_t)rm * d);
+    float* lw = S.alloc<float>(rmax);
+    float* nrm = S.alloc<float>(rmax);
+    float* A1 = S.alloc<float>((size_t)rm * c1);
+    float* PY1 = S.alloc<float>((size_t)rn * c1);
+    float* W = S.alloc<float>((size_t)rn * c2);
+    float* PT = S.alloc<float>((size_t)rm * c2);
+    float* rhs = S.alloc<float>((size_t)rm);
+    float* cvec = S.alloc<float>((size_t)rm);
+    float* res = S.alloc<float>((size_t)rm);
+    float* z = S.alloc<float>((size_t)rm);
+    float* p = S.alloc<float>((size_t)rm);
+    float* Sp = S.alloc<float>((size_t)rm);
+    float* Ptq = S.alloc<float>((size_t)rm);
+    float* gd = S.alloc<float>((size_t)rm);
+    float* Pp = S.alloc<float>((size_t)rn);
+    float* q = S.alloc<float>((size_t)rn);
+    float* YH = S.alloc<float>((size_t)rn * d);
+    float* CP = S.alloc<float>((size_t)rn * 2 * d);
+    double* dd = S.alloc<double>((size_t)4 * B);
+    float* part = nparts ? S.alloc<float>(nparts) : nullptr;
+    if (!shift || !Xc || !Yc || !lw || !nrm || !A1 || !PY1 || !W || !PT || !rhs || !cvec || !res || !z || !p ||
+        !Sp || !Ptq || !gd || !Pp || !q || !YH || !CP || !dd || (nparts && !part))
+        return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    HvpDots dots{dd, dd + B, dd + 3 * B};
+#define SOT_HVP_STEP(call)                                                                          \
+    do {                                                                                            \
+        cudaError_t _e = (call);                                                                    \
+        if (_e != cudaSuccess) return fail(SOT_ERR_CUDA, "sot_hvp: %s", cudaGetErrorString(_e));    \
+    } while (0)
+    // Both clouds less their common centre t = (mean x + mean y) / 2: H does not
+    // change under a common translation, and the right-hand side's terms
+    // (r_i x_i - (P Y)_i, x_i . v_i - y_j . v_i) cancel at the size of |x|.
+    SOT_HVP_STEP(launch_center(X, Y, B, n, m, d, shift, cs));
+    SOT_HVP_STEP(launch_pack(X, a, B, n, d, shift, 0, Xc, lw, nrm, cs));
+    SOT_HVP_STEP(launch_pack(Y, b, B, m, d, shift, 0, Yc, lw, nrm, cs));
+    // side 0: o[B][n][c] = P Vin (Vin [B][m][c]); side 1: o[B][m][c] = P^T Vin (Vin [B][n][c])
+    auto product = [&](int side, const float* Vin, int c, float* o) -> cudaError_t {
+        TransportArgs t;
+        t.B = B; t.d = d; t.c = c; t.V = Vin; t.out = o; t.ldv = c; t.ldo = c;
+        t.kap_hi = (float)kap;
+        t.kap_lo = (float)(kap - (double)t.kap_hi);
+        if (side == 0) {
+            t.nr = n; t.nc = m; t.R = Xc; t.Cl = Yc; t.fr = f; t.gc = g; t.wr = a; t.wc = b;
+        } else {
+            t.nr = m; t.nc = n; t.R = Yc; t.Cl = Xc; t.fr = g; t.gc = f; t.wr = b; t.wc = a;
+        }
+        transport_plan(B, t.nr, t.nc, c, sms, &t.split, &t.chunk);
+        t.part = part;
+        return launch_transport(t, cs);
+    };
+    // r and P Y, then the right-hand side of the marginal system and c
+    SOT_HVP_STEP(launch_hvp_pack_ones(rm, d, Yc, A1, cs));
+    SOT_HVP_STEP(product(0, A1, c1, PY1));
+    SOT_HVP_STEP(launch_hvp_pack_side1(rn, d, Xc, V, PY1, W, cs));
+    SOT_HVP_STEP(product(1, W, c2, PT));
+    SOT_HVP_STEP(launch_hvp_rhs(rm, d, Yc, PT, rhs, cvec, cs));
+    // conjugate gradients on S gdot = rhs, every cloud at once; every 8 steps
+    // the host reads the clouds' residuals and stops when all are done
+    SOT_HVP_STEP(launch_hvp_cg_init(B, m, rhs, cvec, res, z, p, gd, dots, cs));
+    std::vector<double> hrz(2 * (size_t)B);
+    for (int it = 0; it < cg_iters; ++it) {
+        SOT_HVP_STEP(product(0, p, 1, Pp));
+        SOT_HVP_STEP(launch_hvp_div_r(rn, d, Pp, PY1, q, cs));
+        SOT_HVP_STEP(product(1, q, 1, Ptq));
+        SOT_HVP_STEP(launch_hvp_cg_step(B, m, it, cg_tol, cvec, Ptq, p, Sp, res, z, gd, dots, cs));
+        if ((it & 7) == 7 && it + 1 < cg_iters) {
+            SOT_HVP_STEP(cudaMemcpyAsync(hrz.data(), dots.rz0, sizeof(double) * B, cudaMemcpyDeviceToHost, cs));
+            SOT_HVP_STEP(cudaMemcpyAsync(hrz.data() + B, dots.rz + (size_t)((it + 1) & 1) * B, sizeof(double) * B,
+                                         cudaMemcpyDeviceToHost, cs));
+            SOT_HVP_STEP(cudaStreamSynchronize(cs));
+            bool done = true;
+            for (int k = 0; k < B; ++k)
+                if (hrz[B + k] > (double)cg_tol * (double)cg_tol * hrz[k]) done = false;
+            if (done) break;
+        }
+    }
+    // assembly from the row-centred product of gdot: [sum_j P_ij ((y_j - yhat_i).v_i)(y_j - yhat_i),
+    // sum_j P_ij gdot_j (y_j - yhat_i)]
+    SOT_HVP_STEP(launch_hvp_barycentre(rn, d, PY1, YH, cs));
+    {
+        TransportArgs t;
+        t.B = B; t.d = d; t.c = 1; t.V = gd; t.ldv = 1; t.out = CP; t.ldo = 2 * d;
+        t.kap_hi = (float)kap;
+        t.kap_lo = (float)(kap - (double)t.kap_hi);
+        t.nr = n; t.nc = m; t.R = Xc; t.Cl = Yc; t.fr = f; t.gc = g; t.wr = a; t.wc = b;
+        t.rc = YH; t.rv = V;
+        transport_plan(B, n, m, 2 * d, sms, &t.split, &t.chunk);
+        t.part = part;
+        SOT_HVP_STEP(launch_transport_centred(t, cs));
+    }
+    SOT_HVP_STEP(launch_hvp_assemble_centred(rn, d, eps, V, PY1, CP, out, cs));
+#undef SOT_HVP_STEP
     return SOT_OK;
 }
 

@@ -25,6 +25,8 @@ struct TransportArgs {
     float kap_hi, kap_lo;  // 1 / (eps ln 2) as a float-float pair
     int split, chunk;      // columns in `split` chunks of `chunk` columns (one CTA each)
     float* part;           // [split][B][nr][c] partial sums when split > 1
+    const float* rc = nullptr;  // centred products: [B][nr][d] row barycentres
+    const float* rv = nullptr;  // centred products: [B][nr][d] row directions
 };
 
 int transport_max_d();
@@ -33,6 +35,7 @@ int transport_max_c();
 // the floats of partial-sum scratch it needs (0 when split == 1).
 size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk);
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st);
+cudaError_t launch_transport_centred(const TransportArgs& p, cudaStream_t st);
 // g[k][j][:] <- 2 (w_j p_j - g[k][j][:]) for `count` points of d coordinates
 // (w NULL = uniform 1/per_cloud): the gradient from the transport product.
 cudaError_t launch_grad_finish(const float* P, const float* w, int B, int per_cloud, int d, float* g,

@@ -179,3 +179,15 @@ def test_path_selection(lib):
     for d in (8, 128):
         assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED
     assert lib.sot_select_path(257, binding.SOT_PREC_AUTO) == binding.SOT_ERR_UNSUPPORTED
+
+
+def test_hvp_arguments_rejected_on_host(lib):
+    p = C.c_void_p(16)
+    args = lambda d, it, tol, flags: (p, p, NULL, NULL, 1, 5, 5, d, p, p, 0.1, p, it, tol, p, flags, NULL)
+    assert lib.sot_hvp(*args(10, 50, 1e-5, 0)) == binding.SOT_ERR_UNSUPPORTED  # d <= 9
+    assert lib.sot_hvp(*args(3, 0, 1e-5, 0)) == binding.SOT_ERR_INVALID_ARG  # cg_iters >= 1
+    assert lib.sot_hvp(*args(3, 50, -1.0, 0)) == binding.SOT_ERR_INVALID_ARG  # cg_tol >= 0
+    assert lib.sot_hvp(*args(3, 50, 1e-5, 1)) == binding.SOT_ERR_INVALID_ARG  # no flags
+    assert lib.sot_hvp(p, p, NULL, NULL, 1, 5, 5, 3, p, p, 0.1, NULL, 50, 1e-5, p, 0, NULL) == \
+        binding.SOT_ERR_INVALID_ARG  # V must not be NULL
+    assert lib.sot_hvp(p, p, NULL, NULL, 0, 5, 5, 3, NULL, NULL, 0.1, NULL, 50, 1e-5, NULL, 0, NULL) == binding.SOT_OK
