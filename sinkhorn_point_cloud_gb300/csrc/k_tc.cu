@@ -55,8 +55,8 @@ constexpr uint32_t OFF_BIAS = OFF_B + TC_S * OP_BYTES;  // [TC_S][TC_N] float
 constexpr uint32_t OFF_BAR = OFF_BIAS + TC_S * TC_N * 4;
 constexpr uint32_t NBAR = 18;
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;            // tmem slot, abort, nretry, last, pool count
-constexpr uint32_t OFF_RED = OFF_MISC + 32;             // 16 floats
-constexpr uint32_t OFF_RETRY = OFF_RED + 64;            // TC_ROWS ints
+constexpr uint32_t OFF_RED = OFF_MISC + 32;             // 32 floats (one per warp of a block reduction)
+constexpr uint32_t OFF_RETRY = OFF_RED + 128;           // TC_ROWS ints
 constexpr uint32_t TC_SMEM = OFF_RETRY + TC_ROWS * 4 + 1024;  // + alignment slack
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 
@@ -507,6 +507,7 @@ __device__ __forceinline__ void tc_release(const TcSmem& S, int wg, int lt) {
 // Exact two-pass LSE of one row over all columns, by the whole CTA (the
 // fallback for rows whose fast path could not give the value): fp32 dot
 // products of the centred coordinates, x held in registers, y read as float4.
+template <int NT>
 __device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc,
                              int row, float tk, float* red) {
     const float4* xr = reinterpret_cast<const float4*>(rows + (size_t)row * TC_D);
@@ -527,12 +528,12 @@ __device__ float tc_row_full(const float* rows, const float* cols, const float* 
         return fmaf(tk, a0 + a1, cw[j] - cst[j]);
     };
     float mx = -INFINITY;
-    for (int j = threadIdx.x; j < nc; j += TC_THREADS) mx = fmaxf(mx, score(j));
-    mx = block_max<TC_THREADS>(mx, red);
+    for (int j = threadIdx.x; j < nc; j += NT) mx = fmaxf(mx, score(j));
+    mx = block_max<NT>(mx, red);
     if (mx == -INFINITY) return -INFINITY;
     float sm = 0.f;
-    for (int j = threadIdx.x; j < nc; j += TC_THREADS) sm += ex2f(score(j) - mx);
-    sm = block_sum<TC_THREADS>(sm, red);
+    for (int j = threadIdx.x; j < nc; j += NT) sm += ex2f(score(j) - mx);
+    sm = block_sum<NT>(sm, red);
     return mx + log2f(sm);
 }
 
@@ -540,6 +541,7 @@ __device__ float tc_row_full(const float* rows, const float* cols, const float* 
 // row values: rows queued in the retry list get the exact two-pass row LSE
 // (whole CTA), then the marginal-error partial and the bound for the next
 // half-step are formed from the new row values.
+template <int NT>
 __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, float old, int b, int rb,
                         size_t rbase, const float* cw, const float* cst) {
     int* misc = S.misc();
@@ -552,7 +554,7 @@ __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, 
     const float* cols_fp32 = p.cpack + (size_t)b * p.nc * TC_D;
     for (int k = 0; k < nretry; ++k) {
         const int r = retry[k];
-        const float v = tc_row_full(rows_fp32, cols_fp32, cw, cst, p.nc, r, p.two_kappa, red);
+        const float v = tc_row_full<NT>(rows_fp32, cols_fp32, cw, cst, p.nc, r, p.two_kappa, red);
         if (threadIdx.x == 0) {
             p.rstate_out[rbase + r] = v;
             atomicOr(p.status, SOT_DEV_RETRY_ROWS);
@@ -568,7 +570,7 @@ __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, 
             lo = old - nv;
         }
         if (p.errpart) {
-            e = block_sum<TC_THREADS>(e, red);
+            e = block_sum<NT>(e, red);
             if (threadIdx.x == 0) p.errpart[b * p.rowtiles + rb] = e;
         }
         if (p.lo_out) {
@@ -740,7 +742,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             retry[atomicAdd(&misc[2], 1)] = row;
         }
     }
-    tc_tail(p, S, erow, row, old, b, rb, rbase, cw, cst);
+    tc_tail<TC_THREADS>(p, S, erow, row, old, b, rb, rbase, cw, cst);
 }
 
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st) {
@@ -794,9 +796,14 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 // adds: the result does not depend on the order).  A row with a pair that did
 // not fit in its segment takes the exact full-row LSE.
 constexpr int SC_RETRY_INLINE = 8;  // lost rows a row block retries itself when on probation
+constexpr int SC_EPI = 16;                     // epilogue warps
+constexpr int SC_THREADS = 32 * (2 + SC_EPI);  // producer, MMA, epilogue
+constexpr int SC_COLS = 4 * SC_N / SC_EPI;     // columns of a tile each epilogue warp screens (64)
+constexpr int SC_NQ = SC_COLS / 32;            // 32-column chunks per warp and row tile
 constexpr int TC_POOL = 4096;  // kept pairs per CTA
-constexpr int SC_SEGS = 8;     // pool segments per CTA, one per epilogue warp
+constexpr int SC_SEGS = SC_EPI;  // pool segments per CTA, one per epilogue warp
 constexpr int SC_SEG = TC_POOL / SC_SEGS;
+static_assert(SC_COLS % 32 == 0 && 4 * SC_N == SC_EPI * SC_COLS, "epilogue column split");
 int tc_screen_pool_cap() { return TC_POOL; }
 int tc_screen_pool_segments() { return SC_SEGS; }
 constexpr int TC_XS = TC_D + 4;  // row stride of the fp32 row tile in shared memory (bank spread)
@@ -888,29 +895,30 @@ struct TcScreenK {
     const unsigned* cmax;   // [B] max |c_j| of this half-step's column biases (float bits)
 };
 
-// Per-chunk maxima of one row over the 4 x 32 columns of a tile, from the
+// Per-chunk maxima of one row over NQ x 32 columns of a tile, from the
 // accumulators (raw bits; accumulator units, biases included): one
 // three-input max chain per 32-column chunk.
-__device__ __forceinline__ void tc_chunk_max(const uint32_t (&r)[4][32], float (&mq)[4]) {
-    // two interleaved chains per chunk (8 in flight) keep the max latency hidden
-    float m[8];
+template <int NQ>
+__device__ __forceinline__ void tc_chunk_max(const uint32_t (&r)[NQ][32], float (&mq)[NQ]) {
+    // two interleaved chains per chunk keep the max latency hidden
+    float m[2 * NQ];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) m[c] = -INFINITY;
+    for (int c = 0; c < 2 * NQ; ++c) m[c] = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < NQ; ++q) {
             m[2 * q] = fmax3(m[2 * q], __uint_as_float(r[q][j]), __uint_as_float(r[q][j + 1]));
             m[2 * q + 1] = fmax3(m[2 * q + 1], __uint_as_float(r[q][j + 2]), __uint_as_float(r[q][j + 3]));
         }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) mq[q] = fmaxf(m[2 * q], m[2 * q + 1]);
+    for (int q = 0; q < NQ; ++q) mq[q] = fmaxf(m[2 * q], m[2 * q + 1]);
 }
 
-// Screen 128 columns of one row (accumulator bits in r, columns jt ..): the
-// per-chunk maxima raise the running maximum, and every pair of a chunk that
-// reaches the threshold goes to the CTA's pool.
+// Screen NQ x 32 columns of one row (accumulator bits in r, columns jt ..):
+// the per-chunk maxima raise the running maximum, and every pair of a chunk
+// that reaches the threshold goes to the CTA's pool.
 struct ScShared {  // the same for every row of the warp
     float Mg, tk, inv_tk;
     uint2* seg;   // this warp's pool segment
@@ -922,24 +930,28 @@ struct ScRow {  // one row's screening state
     unsigned rl; // row within the row block
     bool erow;
 };
-__device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt, ScShared& c, ScRow& s) {
-    float mq[4];
-    tc_chunk_max(r, mq);
+template <int NQ>
+__device__ __forceinline__ void sc_screen(const uint32_t (&r)[NQ][32], int jt, ScShared& c, ScRow& s) {
+    float mq[NQ];
+    tc_chunk_max<NQ>(r, mq);
     // thresholds in accumulator units (score = tk * acc, tk > 0)
-    s.runmax = fmaxf(s.runmax, c.tk * fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3])));
+    float mall = mq[0];
+#pragma unroll
+    for (int q = 1; q < NQ; ++q) mall = fmaxf(mall, mq[q]);
+    s.runmax = fmaxf(s.runmax, c.tk * mall);
     // (a reciprocal, not a division: the margin absorbs its rounding)
     const float Ta = (fmaxf(s.Lb, s.runmax - c.Mg) - s.off) * c.inv_tk;
-    bool hq[4];
+    bool hq[NQ];
     bool hit = false;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
         hq[q] = s.erow && mq[q] > Ta;
         hit = hit || hq[q];
     }
     if (!__any_sync(0xffffffffu, hit)) return;
     const unsigned lt_mask = (1u << (threadIdx.x & 31)) - 1u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
         if (!__any_sync(0xffffffffu, hq[q])) continue;
         unsigned pm = 0u;  // this lane's kept columns of the chunk
         if (hq[q]) {
@@ -973,7 +985,9 @@ __device__ __forceinline__ void sc_screen_128(const uint32_t (&r)[4][32], int jt
     }
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, TcOps ops, TcScreenK sk) {
+// 18 warps put five on one SM sub-partition, whose 16384 registers then allow
+// 96 per thread.
+__global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, TcOps ops, TcScreenK sk) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     extern __shared__ unsigned char smem_raw[];
     const TcSmem S = tc_smem(smem_raw, SC_OFF_HDR);
@@ -997,7 +1011,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     const size_t cta0 = ((size_t)b * p.rowtiles + rb) * p.split;  // first pool of this row block
 
     if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
-        for (int k = threadIdx.x; k < p.B; k += TC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
+        for (int k = threadIdx.x; k < p.B; k += SC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
     // Row-side constants of the bias step, (2^E, 2^(E-11), 2^(E-22), 0, ...) in
     // K = 0..15 of every row of both row tiles.  A cloud whose biases need
     // E > 15 is not screened: its rows take the exact LSE.
@@ -1009,20 +1023,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const unsigned h1 = __half_as_ushort(__float2half_rn(ldexpf(1.f, E - 11)));
         const unsigned h2 = __half_as_ushort(__float2half_rn(ldexpf(1.f, E - 22)));
         const uint4 c0 = make_uint4(h0 | (h1 << 16), h2, 0u, 0u), z = make_uint4(0u, 0u, 0u, 0u);
-        for (int e = threadIdx.x; e < 2 * TC_M * 2; e += TC_THREADS) {
+        for (int e = threadIdx.x; e < 2 * TC_M * 2; e += SC_THREADS) {
             const int rt = e / (2 * TC_M), r = (e % (2 * TC_M)) >> 1, c = e & 1;
             *reinterpret_cast<uint4*>(S.sm + SC_OFF_AC + rt * SC_AT + sw32_offset(r, 8 * c)) = c ? z : c0;
         }
         fence_proxy_async_smem();
     }
     // stages are freed by the MMA commit alone; every accumulator is read by all 8 epilogue warps
-    const uint32_t tmem = tc_setup(S, warp, 1, 8);
+    const uint32_t tmem = tc_setup(S, warp, 1, SC_EPI);
 
-    const int wg = (warp - 2) >> 2;
-    const int q4 = warp & 3;
-    // the row this thread finalises (and whose marginal-error term it forms)
-    const int row = row0 + wg * TC_M + q4 * 32 + lane;
-    const bool erow = (warp >= 2) && row < p.nr;
+    const int q4 = warp & 3;  // the TMEM lane quarter this warp may access
+    // the row this thread finalises (and whose marginal-error term it forms):
+    // warps 2..9, row tile (warp - 2) / 4
+    const int row = row0 + ((warp - 2) >> 2) * TC_M + q4 * 32 + lane;
+    const bool erow = (warp >= 2) && (warp < 10) && row < p.nr;
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
@@ -1030,10 +1044,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     } else if (warp == 1) {
         sc_mma(S, tmem, nts, ops.wait_ns);
     } else {
-        // Screening: epilogue warp (wg, q4) reads columns 128 wg .. of both row tiles'
-        // accumulators for TMEM lanes 32 q4 ..: rows row0 + 32 q4 + lane (tile 0) and
-        // row0 + 128 + 32 q4 + lane (tile 1).  An accumulator is freed as soon as all
-        // eight warps have loaded their half, before the screening arithmetic.
+        // Screening: epilogue warp ew = warp - 2 (column group cg = ew / 4, lane
+        // quarter q4) reads columns SC_COLS cg .. of both row tiles' accumulators for
+        // TMEM lanes 32 q4 ..: rows row0 + 32 q4 + lane (tile 0) and row0 + 128 +
+        // 32 q4 + lane (tile 1).  An accumulator is freed as soon as all SC_EPI warps
+        // have loaded their share, before the screening arithmetic.
+        const int ew = warp - 2, cg = ew >> 2;
         if (!screenable && erow) sk.lost[rbase + row] = 1;
         // screening margin of this cloud (scaled units -> log2 units); the
         // last term covers the fp32 rounding of the biases held in the
@@ -1045,7 +1061,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         c.Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 1.5258789e-5f * cmax + 0.02f;
         c.tk = tk;
         c.inv_tk = 1.f / tk;
-        c.seg = sk.pool + ((cta0 + ch) * SC_SEGS + (warp - 2)) * (size_t)SC_SEG;
+        c.seg = sk.pool + ((cta0 + ch) * SC_SEGS + ew) * (size_t)SC_SEG;
         c.wcount = 0;
         const float theta_off = 26.f + log2f((float)p.nc) + c.Mg + 0.05f;
         const float lo = (!p.cold && p.lo_in) ? ord_decode(p.lo_in[b]) : -INFINITY;
@@ -1062,7 +1078,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
             s[rt].rl = (unsigned)(rt * TC_M + q4 * 32 + lane);
             s[rt].erow = ok_row;
         }
-        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(wg * 128);  // lanes, column half
+        const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(cg * SC_COLS);  // lanes, columns
         bool ok = true;
         for (int lt = 0; ok && lt < nts; ++lt) {
 #pragma unroll
@@ -1072,19 +1088,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                     break;
                 }
                 tc_fence_after();
-                uint32_t r[4][32];
+                uint32_t r[SC_NQ][32];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_ld32_issue(tq + (uint32_t)(rt * SC_N) + 32u * (uint32_t)q, r[q]);
+                for (int q = 0; q < SC_NQ; ++q)
+                    tmem_ld32_issue(tq + (uint32_t)(rt * SC_N) + 32u * (uint32_t)q, r[q]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_wait_ld(r[q]);
+                for (int q = 0; q < SC_NQ; ++q) tmem_wait_ld(r[q]);
                 // this warp's share of the accumulator is in registers: free it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(rt, 0)));
-                sc_screen_128(r, c_begin + lt * SC_N + 128 * wg, c, s[rt]);
+                sc_screen<SC_NQ>(r, c_begin + lt * SC_N + SC_COLS * cg, c, s[rt]);
             }
         }
-        if (lane == 0) sk.pool_cnt[(cta0 + ch) * SC_SEGS + (warp - 2)] = min(c.wcount, SC_SEG);
+        if (lane == 0) sk.pool_cnt[(cta0 + ch) * SC_SEGS + ew] = min(c.wcount, SC_SEG);
     }
 
     tc_fence_before();
@@ -1121,20 +1138,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     {
         // the block's fp32 rows: every load issued before the first store
         const float4* src = reinterpret_cast<const float4*>(p.rpack + rbase * TC_D);
-        constexpr int NE = TC_ROWS * (TC_D / 4), NL = (NE + TC_THREADS - 1) / TC_THREADS;
+        constexpr int NE = TC_ROWS * (TC_D / 4), NL = (NE + SC_THREADS - 1) / SC_THREADS;
         float4 buf[NL];
 #pragma unroll
         for (int i = 0; i < NL; ++i) {
-            const int e = threadIdx.x + i * TC_THREADS, rg = row0 + e / (TC_D / 4);
+            const int e = threadIdx.x + i * SC_THREADS, rg = row0 + e / (TC_D / 4);
             buf[i] = (e < NE && rg < p.nr) ? __ldg(src + (size_t)rg * (TC_D / 4) + e % (TC_D / 4))
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int i = 0; i < NL; ++i) {
-            const int e = threadIdx.x + i * TC_THREADS;
+            const int e = threadIdx.x + i * SC_THREADS;
             if (e < NE) *reinterpret_cast<float4*>(sx + (e / (TC_D / 4)) * TC_XS + 4 * (e % (TC_D / 4))) = buf[i];
         }
-        for (int r = threadIdx.x; r < TC_ROWS; r += TC_THREADS) {
+        for (int r = threadIdx.x; r < TC_ROWS; r += SC_THREADS) {
             const int rg = row0 + r;
             float ref = 0.f;
             int lost = 0;
@@ -1153,7 +1170,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
             s_lost[r] = lost;
         }
         // the block's pool segments (every chunk's): sizes ...
-        for (int g = threadIdx.x; g < p.split * SC_SEGS; g += TC_THREADS)
+        for (int g = threadIdx.x; g < p.split * SC_SEGS; g += SC_THREADS)
             s_off[g + 1] = __ldcg(sk.pool_cnt + cta0 * SC_SEGS + g);
     }
     __syncthreads();
@@ -1186,7 +1203,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     const int total = s_off[nseg];
     const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
     // pass 1: exact score of every kept pair, relative to the row's reference;
-    // row maxima.  Two pairs per thread and round, all their loads in flight.
+    // row maxima.  One pair per thread and round.
     auto entry = [&](int k) -> uint2* {  // segment g with s_off[g] <= k < s_off[g + 1] (binary search)
         int lo = 0, hi = nseg;
         while (hi - lo > 1) {
@@ -1195,22 +1212,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         }
         return sk.pool + (cta0 * SC_SEGS + lo) * (size_t)SC_SEG + (k - s_off[lo]);
     };
-    auto exact = [&](uint2 it, const float4 (&yv)[TC_D / 4]) -> float {
+    // y: the column's fp32 coordinates, read in two halves (every load of a half
+    // in flight before its products)
+    auto exact = [&](uint2 it, const float4* y) -> float {
         const int rl = (int)it.y, j = (int)it.x;
         const float* xr = sx + rl * TC_XS;
         float hs[4] = {0.f, 0.f, 0.f, 0.f}, es[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < TC_D / 4; ++q) {
-            const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q);
-            const float xa[4] = {x.x, x.y, x.z, x.w};
-            const float ya[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+        for (int h = 0; h < 2; ++h) {
+            float4 yv[TC_D / 8];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                // error-free product and sum (Dekker / Knuth), errors summed alongside
-                const float2 pr = two_prod(xa[w], ya[w]);
-                const float2 sn = two_sum(hs[w], pr.x);
-                hs[w] = sn.x;
-                es[w] = __fadd_rn(es[w], __fadd_rn(pr.y, sn.y));
+            for (int q = 0; q < TC_D / 8; ++q) yv[q] = __ldg(y + h * (TC_D / 8) + q);
+#pragma unroll
+            for (int q = 0; q < TC_D / 8; ++q) {
+                const float4 x = *reinterpret_cast<const float4*>(xr + 4 * (h * (TC_D / 8) + q));
+                const float xa[4] = {x.x, x.y, x.z, x.w};
+                const float ya[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    // error-free product and sum (Dekker / Knuth), errors summed alongside
+                    const float2 pr = two_prod(xa[w], ya[w]);
+                    const float2 sn = two_sum(hs[w], pr.x);
+                    hs[w] = sn.x;
+                    es[w] = __fadd_rn(es[w], __fadd_rn(pr.y, sn.y));
+                }
             }
         }
         // t - ref = 2 kappa (sum hs + sum es) + (cw_j - cst_j) - ref in float-float
@@ -1227,49 +1252,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         return __fadd_rn(V2.x, __fadd_rn(__fadd_rn(V2.y, U2.y),
                                          __fadd_rn(__fadd_rn(P2.y, C2.y), __fmul_rn(p.two_kappa, E2))));
     };
-    for (int k0 = threadIdx.x; k0 < total; k0 += 2 * TC_THREADS) {
-        const int k1 = k0 + TC_THREADS;
-        uint2* e0 = entry(k0);
-        uint2* e1 = (k1 < total) ? entry(k1) : e0;
-        const uint2 it0 = __ldcg(e0), it1 = __ldcg(e1);
+    for (int k = threadIdx.x; k < total; k += SC_THREADS) {
+        uint2* e0 = entry(k);
+        const uint2 it0 = __ldcg(e0);
         const bool v0 = !s_lost[it0.y] && (int)it0.x < p.nc;
-        const bool v1 = k1 < total && !s_lost[it1.y] && (int)it1.x < p.nc;
-        const float4* y0 = ybase + (size_t)(v0 ? it0.x : 0u) * (TC_D / 4);
-        const float4* y1 = ybase + (size_t)(v1 ? it1.x : 0u) * (TC_D / 4);
-        float4 ya[TC_D / 4], yb[TC_D / 4];
-#pragma unroll
-        for (int q = 0; q < TC_D / 4; ++q) {
-            ya[q] = __ldg(y0 + q);
-            yb[q] = __ldg(y1 + q);
-        }
         // (an entry past the last column cannot occur; it would add nothing)
         if (v0) {
-            const float trel = exact(it0, ya);
+            const float trel = exact(it0, ybase + (size_t)it0.x * (TC_D / 4));
             e0->x = __float_as_uint(trel);
             atomicMax(s_max + it0.y, ord_encode(trel));
         } else if (!s_lost[it0.y]) {
             e0->x = __float_as_uint(-INFINITY);
         }
-        if (v1) {
-            const float trel = exact(it1, yb);
-            e1->x = __float_as_uint(trel);
-            atomicMax(s_max + it1.y, ord_encode(trel));
-        } else if (k1 < total && !s_lost[it1.y]) {
-            e1->x = __float_as_uint(-INFINITY);
-        }
     }
     __syncthreads();
     // pass 2: row sums in 2^-48 fixed point (each term <= 1), four entries per round
-    for (int k0 = threadIdx.x; k0 < total; k0 += 4 * TC_THREADS) {
+    for (int k0 = threadIdx.x; k0 < total; k0 += 4 * SC_THREADS) {
         uint2 it[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int k = k0 + u * TC_THREADS;
+            const int k = k0 + u * SC_THREADS;
             it[u] = (k < total) ? __ldcg(entry(k)) : make_uint2(0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int k = k0 + u * TC_THREADS;
+            const int k = k0 + u * SC_THREADS;
             const int rl = (int)it[u].y;
             if (k >= total || s_lost[rl]) continue;
             const float w = ex2f(__uint_as_float(it[u].x) - ord_decode(s_max[rl]));
@@ -1292,7 +1299,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                 s_ref[rl] + (ord_decode(s_max[rl]) + (log2f(__ull2float_rn(s_sum[rl])) - 48.f));
         }
     }
-    tc_tail(p, S, erow, row, old, b, rb, rbase, cw, cst);
+    tc_tail<SC_THREADS>(p, S, erow, row, old, b, rb, rbase, cw, cst);
 }
 
 cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const TcScreen& sc, cudaStream_t st) {
@@ -1323,7 +1330,7 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
     if (p.chunk % SC_N != 0 || ops.tiles_c % 2 != 0) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(tc_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.rowtiles * p.split, p.B), block(TC_THREADS);
+    dim3 grid(p.rowtiles * p.split, p.B), block(SC_THREADS);
     count_launches(1);
     tc_screen_kernel<<<grid, block, SC_SMEM, st>>>(p, ops, sk);
     return cudaGetLastError();
