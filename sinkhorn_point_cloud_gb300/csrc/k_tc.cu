@@ -847,17 +847,27 @@ __device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
 // row tile r, four 128 x 256 x 16 hi*hi MMAs and the bias step (row-side
 // constants times the tile's bias block) into the row tile's accumulator
 // (TMEM columns 256 r ..); the epilogue frees it after loading it.
+// The thread shares its SM sub-partition with four busy epilogue warps, so
+// the work between two groups is kept short: every descriptor is formed
+// before the loop, and the commit that frees a tile's stage is issued after
+// the next tile's first group, off the path from one group to the next.
 __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns) {
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
         bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, wait_ns);
         bool issued_any = false;
         const uint32_t idesc = f16_idesc(TC_M, SC_N);
+        // Descriptors: the start address field (bits 0-13, address / 16) is the
+        // only part that differs, and every address here is below 256 KB, so a
+        // byte offset o is added to a descriptor as o / 16 with no carry out of
+        // the field; it advances by 2 per K = 16 step (32 bytes).
+        const uint64_t adesc0 = sw128_desc(S.sbase + SC_OFF_A), acdesc0 = sw32_desc(S.sbase + SC_OFF_AC);
+        const uint64_t bdesc0 = sw128_desc(S.sbase + SC_OFF_B), bbdesc0 = sw32_desc(S.sbase + SC_OFF_B + 2 * TILE_BYTES);
+        int prev_st = -1;
         for (int lt = 0; ok && lt < nt; ++lt) {
             const int st = lt % TC_S;
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, wait_ns)) break;
-            const uint32_t bst = S.sbase + SC_OFF_B + (uint32_t)st * SC_STAGE;
             for (int r = 0; r < 2 && ok; ++r) {
                 if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, 0)), ((uint32_t)lt & 1u) ^ 1u, abort, wait_ns)) {
                     ok = false;
@@ -866,19 +876,24 @@ __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns)
                 tc_fence_after();
                 issued_any = true;
                 const uint32_t d = tmem + (uint32_t)(r * SC_N);
-                const uint32_t ahi = S.sbase + SC_OFF_A + (uint32_t)r * TILE_BYTES;
+                const uint64_t ad = adesc0 + (uint64_t)(r * (TILE_BYTES >> 4));
+                const uint64_t bd = bdesc0 + (uint64_t)(st * (SC_STAGE >> 4));
 #pragma unroll
-                for (int k = 0; k < TC_D / 16; ++k) {
-                    const uint32_t ko = 32u * (uint32_t)k;
-                    tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bst + ko), idesc, k > 0 ? 1u : 0u);
-                }
-                tc_mma_f16(d, sw32_desc(S.sbase + SC_OFF_AC + (uint32_t)r * SC_AT), sw32_desc(bst + 2 * TILE_BYTES),
-                           idesc, 1u);
+                for (int k = 0; k < TC_D / 16; ++k)
+                    tc_mma_f16(d, ad + 2u * (uint64_t)k, bd + 2u * (uint64_t)k, idesc, k > 0 ? 1u : 0u);
+                tc_mma_f16(d, acdesc0 + (uint64_t)(r * (SC_AT >> 4)), bbdesc0 + (uint64_t)(st * (SC_STAGE >> 4)), idesc,
+                           1u);
                 tc_commit(S.bar(BAR_ACCFULL(r, 0)));
+                if (r == 0 && prev_st >= 0) {
+                    // the previous tile's stage: its last readers were issued before this group
+                    tc_commit(S.bar(BAR_EMPTY(prev_st)));
+                    prev_st = -1;
+                }
             }
             if (!ok) break;
-            tc_commit(S.bar(BAR_EMPTY(st)));
+            prev_st = st;
         }
+        if (prev_st >= 0) tc_commit(S.bar(BAR_EMPTY(prev_st)));
         tc_mma_drain(S, issued_any, wait_ns);
     }
     __syncwarp();
