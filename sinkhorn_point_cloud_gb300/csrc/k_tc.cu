@@ -807,7 +807,11 @@ static_assert(SC_COLS % 32 == 0 && 4 * SC_N == SC_EPI * SC_COLS, "epilogue colum
 int tc_screen_pool_cap() { return TC_POOL; }
 int tc_screen_pool_segments() { return SC_SEGS; }
 constexpr int TC_XS = TC_D + 4;  // row stride of the fp32 row tile in shared memory (bank spread)
-static_assert(TC_ROWS * TC_XS * 4 + TC_ROWS * 16 + (64 * SC_SEGS + 1) * 4 <= TC_S * SC_STAGE, "finaliser shared memory");
+// Finaliser shared memory (the ring's space): fp32 rows, per-row words, the
+// segment offsets, then a dense copy of the kept pairs when they fit.
+constexpr int SC_LIST_CAP = 8192;
+constexpr uint32_t SC_FIN_LIST = (TC_ROWS * TC_XS * 4 + TC_ROWS * 20 + (64 * SC_SEGS + 1) * 4 + 15) & ~15u;
+static_assert(SC_FIN_LIST + SC_LIST_CAP * 8 <= TC_S * SC_STAGE, "finaliser shared memory");
 
 // Producer of the screened half-step: the hi halves of the CTA's two row
 // tiles once, then per 256-column tile the hi halves of its two 128-point
@@ -938,6 +942,8 @@ struct ScShared {  // the same for every row of the warp
     float Mg, tk, inv_tk;
     uint2* seg;   // this warp's pool segment
     int wcount;   // entries reserved in it (warp-uniform)
+    const float* ycol;  // the columns' fp32 coordinates (the finaliser reads a kept pair's row)
+    int nc;
 };
 struct ScRow {  // one row's screening state
     float Lb, off, runmax;
@@ -992,8 +998,17 @@ __device__ __forceinline__ void sc_screen(const uint32_t (&r)[NQ][32], int jt, S
                 const int j = __ffs(pm) - 1;
                 pm &= pm - 1u;
                 const int slot = c.wcount + __popc(act & lt_mask);
-                if (slot < SC_SEG) c.seg[slot] = make_uint2((unsigned)(jt + 32 * q + j), s.rl);
-                else *s.lost = 1;
+                const int jc = jt + 32 * q + j;
+                if (slot < SC_SEG) {
+                    c.seg[slot] = make_uint2((unsigned)jc, s.rl);
+                    if (jc < c.nc) {  // the finaliser reads this column's row: bring it into L2 now
+                        const float* yr = c.ycol + (size_t)jc * TC_D;
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(yr));
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(yr + 32));
+                    }
+                } else {
+                    *s.lost = 1;
+                }
             }
             c.wcount += __popc(act);
         }
@@ -1078,6 +1093,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         c.inv_tk = 1.f / tk;
         c.seg = sk.pool + ((cta0 + ch) * SC_SEGS + ew) * (size_t)SC_SEG;
         c.wcount = 0;
+        c.ycol = p.cpack + (size_t)b * p.nc * TC_D;
+        c.nc = p.nc;
         const float theta_off = 26.f + log2f((float)p.nc) + c.Mg + 0.05f;
         const float lo = (!p.cold && p.lo_in) ? ord_decode(p.lo_in[b]) : -INFINITY;
         ScRow s[2];
@@ -1217,9 +1234,22 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     __syncthreads();
     const int total = s_off[nseg];
     const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
+    // the kept pairs, segment after segment, into one dense list in shared
+    // memory when they fit (every later lookup is one shared load)
+    uint2* s_list = reinterpret_cast<uint2*>(S.sm + SC_OFF_B + SC_FIN_LIST);
+    const bool dense = total <= SC_LIST_CAP;
+    if (dense) {
+        for (int g = warp; g < nseg; g += SC_THREADS / 32) {
+            const uint2* src = sk.pool + (cta0 * SC_SEGS + g) * (size_t)SC_SEG;
+            const int o = s_off[g], cnt = s_off[g + 1] - o;
+            for (int i = lane; i < cnt; i += 32) s_list[o + i] = __ldcg(src + i);
+        }
+        __syncthreads();
+    }
     // pass 1: exact score of every kept pair, relative to the row's reference;
-    // row maxima.  One pair per thread and round.
-    auto entry = [&](int k) -> uint2* {  // segment g with s_off[g] <= k < s_off[g + 1] (binary search)
+    // row maxima.
+    auto entry = [&](int k) -> uint2* {  // the dense list, or segment g with s_off[g] <= k < s_off[g + 1]
+        if (dense) return s_list + k;
         int lo = 0, hi = nseg;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
@@ -1227,25 +1257,36 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         }
         return sk.pool + (cta0 * SC_SEGS + lo) * (size_t)SC_SEG + (k - s_off[lo]);
     };
-    // y: the column's fp32 coordinates, read in two halves (every load of a half
-    // in flight before its products)
-    auto exact = [&](uint2 it, const float4* y) -> float {
-        const int rl = (int)it.y, j = (int)it.x;
-        const float* xr = sx + rl * TC_XS;
+    // Four lanes per kept pair (a quad), each taking TC_D / 4 coordinates:
+    // short dependency chains and few live registers.  The quad's partial
+    // dot products are error-free float-float values (Dekker / Knuth
+    // transformations, errors summed alongside), combined across the quad
+    // by shuffles; lane 0 of the quad forms
+    //   t - ref = 2 kappa (sum hs + sum es) + (cw_j - cst_j) - ref
+    // in float-float arithmetic (the fp64 pipe is slow here): the large parts
+    // cancel exactly, the small ones are added last.
+    constexpr int QD = TC_D / 4;  // coordinates per lane of a quad
+    const int sub = lane & 3;
+    for (int k0 = 0; k0 < total; k0 += SC_THREADS / 4) {
+        const int k = k0 + (threadIdx.x >> 2);
+        const bool in = k < total;
+        uint2* e0 = in ? entry(k) : nullptr;
+        const uint2 it0 = in ? (dense ? *e0 : __ldcg(e0)) : make_uint2(0u, 0u);
+        const bool v0 = in && !s_lost[it0.y] && (int)it0.x < p.nc;
         float hs[4] = {0.f, 0.f, 0.f, 0.f}, es[4] = {0.f, 0.f, 0.f, 0.f};
+        if (v0) {
+            const float4* y = ybase + (size_t)it0.x * (TC_D / 4) + sub * (QD / 4);
+            const float* xr = sx + it0.y * TC_XS + sub * QD;
+            float4 yv[QD / 4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float4 yv[TC_D / 8];
+            for (int q = 0; q < QD / 4; ++q) yv[q] = __ldg(y + q);
 #pragma unroll
-            for (int q = 0; q < TC_D / 8; ++q) yv[q] = __ldg(y + h * (TC_D / 8) + q);
-#pragma unroll
-            for (int q = 0; q < TC_D / 8; ++q) {
-                const float4 x = *reinterpret_cast<const float4*>(xr + 4 * (h * (TC_D / 8) + q));
+            for (int q = 0; q < QD / 4; ++q) {
+                const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q);
                 const float xa[4] = {x.x, x.y, x.z, x.w};
                 const float ya[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    // error-free product and sum (Dekker / Knuth), errors summed alongside
                     const float2 pr = two_prod(xa[w], ya[w]);
                     const float2 sn = two_sum(hs[w], pr.x);
                     hs[w] = sn.x;
@@ -1253,31 +1294,35 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                 }
             }
         }
-        // t - ref = 2 kappa (sum hs + sum es) + (cw_j - cst_j) - ref in float-float
-        // arithmetic (error-free sums and products; the fp64 pipe is slow here):
-        // the large parts cancel exactly, the small ones are added last
+        // this lane's partial as one float-float value (S, E) ...
         const float2 s01 = two_sum(hs[0], hs[1]), s23 = two_sum(hs[2], hs[3]);
-        const float2 S2 = two_sum(s01.x, s23.x);
-        const float E2 = __fadd_rn(__fadd_rn(__fadd_rn(es[0], es[1]), __fadd_rn(es[2], es[3])),
-                                   __fadd_rn(__fadd_rn(s01.y, s23.y), S2.y));
-        const float2 P2 = two_prod(p.two_kappa, S2.x);
-        const float2 C2 = two_sum(cw[j], -cst[j]);
-        const float2 U2 = two_sum(P2.x, C2.x);
-        const float2 V2 = two_sum(U2.x, -s_ref[rl]);
-        return __fadd_rn(V2.x, __fadd_rn(__fadd_rn(V2.y, U2.y),
-                                         __fadd_rn(__fadd_rn(P2.y, C2.y), __fmul_rn(p.two_kappa, E2))));
-    };
-    for (int k = threadIdx.x; k < total; k += SC_THREADS) {
-        uint2* e0 = entry(k);
-        const uint2 it0 = __ldcg(e0);
-        const bool v0 = !s_lost[it0.y] && (int)it0.x < p.nc;
-        // (an entry past the last column cannot occur; it would add nothing)
-        if (v0) {
-            const float trel = exact(it0, ybase + (size_t)it0.x * (TC_D / 4));
-            e0->x = __float_as_uint(trel);
-            atomicMax(s_max + it0.y, ord_encode(trel));
-        } else if (!s_lost[it0.y]) {
-            e0->x = __float_as_uint(-INFINITY);
+        float2 S2 = two_sum(s01.x, s23.x);
+        float E2 = __fadd_rn(__fadd_rn(__fadd_rn(es[0], es[1]), __fadd_rn(es[2], es[3])),
+                             __fadd_rn(__fadd_rn(s01.y, s23.y), S2.y));
+        float Sv = S2.x;
+        // ... then the quad's (every lane of the warp takes part in the shuffles)
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+            const float So = __shfl_xor_sync(0xffffffffu, Sv, o);
+            const float Eo = __shfl_xor_sync(0xffffffffu, E2, o);
+            const float2 t = two_sum(Sv, So);
+            Sv = t.x;
+            E2 = __fadd_rn(__fadd_rn(E2, Eo), t.y);
+        }
+        if (in && sub == 0) {
+            if (v0) {
+                const int rl = (int)it0.y, j = (int)it0.x;
+                const float2 P2 = two_prod(p.two_kappa, Sv);
+                const float2 C2 = two_sum(cw[j], -cst[j]);
+                const float2 U2 = two_sum(P2.x, C2.x);
+                const float2 V2 = two_sum(U2.x, -s_ref[rl]);
+                const float trel = __fadd_rn(
+                    V2.x, __fadd_rn(__fadd_rn(V2.y, U2.y), __fadd_rn(__fadd_rn(P2.y, C2.y), __fmul_rn(p.two_kappa, E2))));
+                e0->x = __float_as_uint(trel);
+                atomicMax(s_max + rl, ord_encode(trel));
+            } else if (!s_lost[it0.y]) {
+                e0->x = __float_as_uint(-INFINITY);
+            }
         }
     }
     __syncthreads();
@@ -1287,7 +1332,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int k = k0 + u * SC_THREADS;
-            it[u] = (k < total) ? __ldcg(entry(k)) : make_uint2(0u, 0u);
+            it[u] = (k < total) ? (dense ? s_list[k] : __ldcg(entry(k))) : make_uint2(0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
