@@ -77,19 +77,35 @@ constexpr int SC_N = 256;                                   // columns per scree
 constexpr uint32_t SC_AT = TC_M * 32;                       // row-side constant block: 128 rows x 32 B (sw32)
 constexpr uint32_t SC_BT = SC_N * 32;                       // bias block of a tile: 256 rows x 32 B (sw32)
 constexpr uint32_t SC_STAGE = 2 * TILE_BYTES + SC_BT;       // hi of 256 columns (two 16 KB tiles), bias block
-constexpr uint32_t SC_OFF_A = 0;                            // [2 row tiles] hi, 16 KB each
-constexpr uint32_t SC_OFF_AC = SC_OFF_A + 2 * TILE_BYTES;   // [2 row tiles] constant blocks
-constexpr uint32_t SC_OFF_B = SC_OFF_AC + 2 * SC_AT;        // [TC_S] stages
-constexpr uint32_t SC_OFF_HDR = SC_OFF_B + TC_S * SC_STAGE; // header (as OFF_BAR.. of the full half-step)
-constexpr uint32_t SC_SMEM = SC_OFF_HDR + (OFF_RETRY - OFF_BAR) + TC_ROWS * 4 + 1024;
-static_assert(SC_OFF_B % 1024 == 0 && SC_STAGE % 1024 == 0, "screened stage alignment");
-static_assert(SC_SMEM <= 227 * 1024, "screened shared memory budget");
+constexpr int TC_MAXD = 256;  // the screened half-step streams d in slices of 64 (K = 64 per image tile)
 
-bool tc_supported(int d) { return d == TC_D; }
-int tc_max_d() { return TC_D; }
+// Shared-memory layout of the screened half-step for NS slices of K = 64:
+// the hi parts of both row tiles for every slice (resident), the row-side
+// constant blocks, a ring of NST stages (one slice of one 256-column tile
+// each, plus its bias block), then the header.  Wider d leaves room for
+// fewer stages.
+template <int NS>
+struct ScLayout {
+    static constexpr int NST = NS == 1 ? 4 : (NS == 4 ? 2 : 3);
+    static constexpr uint32_t OFF_A = 0;                              // [2 row tiles][NS] hi, 16 KB each
+    static constexpr uint32_t OFF_AC = OFF_A + 2u * NS * TILE_BYTES;  // [2 row tiles] constant blocks
+    static constexpr uint32_t OFF_B = OFF_AC + 2 * SC_AT;             // [NST] stages
+    static constexpr uint32_t OFF_HDR = OFF_B + NST * SC_STAGE;       // header (as OFF_BAR.. of the full half-step)
+    static constexpr uint32_t SMEM = OFF_HDR + (OFF_RETRY - OFF_BAR) + TC_ROWS * 4 + 1024;
+};
+static_assert(ScLayout<1>::OFF_B % 1024 == 0 && SC_STAGE % 1024 == 0, "screened stage alignment");
+static_assert(ScLayout<1>::SMEM <= 227 * 1024 && ScLayout<2>::SMEM <= 227 * 1024 &&
+                  ScLayout<3>::SMEM <= 227 * 1024 && ScLayout<4>::SMEM <= 227 * 1024,
+              "screened shared memory budget");
+static_assert(ScLayout<4>::NST <= TC_S && ScLayout<1>::NST == TC_S, "stage barriers");
+
+bool tc_supported(int d) { return d >= TC_D && d <= TC_MAXD && d % TC_D == 0; }
+bool tc_half_supported(int d) { return d == TC_D; }
+int tc_max_d() { return TC_MAXD; }
 int tc_rows_per_cta() { return TC_ROWS; }
 int tc_cols_per_tile() { return SC_N; }  // column chunks are whole screened tiles
 bool tc_apply_supported(int d) { return d == TC_D; }
+static inline int tc_slices(int d) { return d > TC_D ? d / TC_D : 1; }
 // Automatic precision at d = 64 uses the tensor-core plan application.
 bool tc_apply_default() { return true; }
 int tc_apply_rows_per_cta() { return TC_ROWS; }
@@ -97,9 +113,8 @@ int tc_apply_rows_per_cta() { return TC_ROWS; }
 static inline int tc_tiles(int n) { return 2 * ((n + TC_ROWS - 1) / TC_ROWS); }
 
 size_t tc_scratch_bytes(int B, int n, int m, int d) {
-    (void)d;
     const int tmax = tc_tiles(n) > tc_tiles(m) ? tc_tiles(n) : tc_tiles(m);
-    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * OP_BYTES + 256 + (size_t)B * 36 + 256 +
+    return (size_t)B * (tc_tiles(n) + tc_tiles(m)) * tc_slices(d) * OP_BYTES + 256 + (size_t)B * 36 + 256 +
            (size_t)B * tmax * TC_N * sizeof(float) + 256 + (size_t)B * (tmax / 2) * SC_BT;
 }
 
@@ -126,28 +141,31 @@ __device__ __forceinline__ float tc_scale_of(unsigned bits) {
     return ldexpf(1.f, 9 - e);
 }
 
-// One thread per point (row of a 128-row tile): 8 chunks of 8 fp16 for hi and lo.
+// One thread per point (row of a 128-row tile): per slice of K = 64, 8 chunks
+// of 8 fp16 for hi and lo (coordinates past d are zero).  Slice k of tile t
+// of cloud b sits at ((b tiles + t) ns + k) OP_BYTES.
 // nrm[b][0] / nrm[b][1] receive (as float bits, atomicMax) the largest norm of a
 // point's hi part and of its exact residual v - hi, in scaled units: the
 // screening margin of the hi * hi product is built from them.
-__global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigned* maxbits, float* scale,
-                                unsigned char* img, unsigned* nrm, int nrm_stride) {
+__global__ void tc_image_kernel(const float* pc, int n, int d, int ns, int tiles, const unsigned* maxbits,
+                                float* scale, unsigned char* img, unsigned* nrm, int nrm_stride) {
     const int b = blockIdx.y;
     const int tile = blockIdx.x;
     const int r = threadIdx.x;
     const int p = tile * TC_M + r;
     const float s = tc_scale_of(maxbits[b]);
     if (tile == 0 && r == 0) scale[b] = s;
-    unsigned char* hi = img + ((size_t)b * tiles + tile) * OP_BYTES;
-    unsigned char* lo = hi + TILE_BYTES;
-    const float* src = pc + ((size_t)b * n + p) * TC_D;
+    const float* src = pc + ((size_t)b * n + p) * d;
     float hh = 0.f, rr = 0.f;
-#pragma unroll
-    for (int c = 0; c < TC_D / 8; ++c) {
+    for (int c = 0; c < ns * (TC_D / 8); ++c) {
+        const int sl = c / (TC_D / 8), cc = c % (TC_D / 8);
+        unsigned char* hi = img + (((size_t)b * tiles + tile) * ns + sl) * OP_BYTES;
+        unsigned char* lo = hi + TILE_BYTES;
         __align__(16) __half h[8], l[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float v = (p < n) ? src[8 * c + k] * s : 0.f;
+            const int kk = 8 * c + k;
+            const float v = (p < n && kk < d) ? src[kk] * s : 0.f;
             const __half hv = __float2half_rn(v);
             const float res = v - __half2float(hv);  // exact in fp32
             h[k] = hv;
@@ -155,7 +173,7 @@ __global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigne
             hh = fmaf(__half2float(hv), __half2float(hv), hh);
             rr = fmaf(res, res, rr);
         }
-        const uint32_t off = sw128_offset(r, 8 * c);
+        const uint32_t off = sw128_offset(r, 8 * cc);
         *reinterpret_cast<uint4*>(hi + off) = *reinterpret_cast<const uint4*>(h);
         *reinterpret_cast<uint4*>(lo + off) = *reinterpret_cast<const uint4*>(l);
     }
@@ -170,14 +188,15 @@ __global__ void tc_image_kernel(const float* pc, int n, int tiles, const unsigne
 
 cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m, int d, const float* xc,
                        const float* yc, cudaStream_t st) {
-    if (d != TC_D) return cudaErrorInvalidValue;
+    if (!tc_supported(d)) return cudaErrorInvalidValue;
     plan.B = B; plan.n = n; plan.m = m; plan.d = d;
+    plan.S = tc_slices(d);
     plan.tiles_x = tc_tiles(n);
     plan.tiles_y = tc_tiles(m);
     uintptr_t base = ((uintptr_t)scratch + 255) & ~(uintptr_t)255;
     plan.xop = reinterpret_cast<unsigned char*>(base);
-    plan.yop = plan.xop + (size_t)B * plan.tiles_x * OP_BYTES;
-    unsigned* maxbits = reinterpret_cast<unsigned*>(plan.yop + (size_t)B * plan.tiles_y * OP_BYTES);
+    plan.yop = plan.xop + (size_t)B * plan.tiles_x * plan.S * OP_BYTES;
+    unsigned* maxbits = reinterpret_cast<unsigned*>(plan.yop + (size_t)B * plan.tiles_y * plan.S * OP_BYTES);
     plan.scale = reinterpret_cast<float*>(maxbits + B);
     plan.nrm = reinterpret_cast<unsigned*>(plan.scale + B);
     plan.cmax = plan.nrm + 4 * B;
@@ -192,11 +211,11 @@ cudaError_t tc_prepare(TcPlan& plan, unsigned char* scratch, int B, int n, int m
     count_launches(1);
     tc_maxabs_kernel<<<dim3(64, B), 256, 0, st>>>(xc, (long long)n * d, yc, (long long)m * d, maxbits);
     count_launches(1);
-    tc_image_kernel<<<dim3(plan.tiles_x, B), TC_M, 0, st>>>(xc, n, plan.tiles_x, maxbits, plan.scale, plan.xop,
-                                                            plan.nrm, 4);
+    tc_image_kernel<<<dim3(plan.tiles_x, B), TC_M, 0, st>>>(xc, n, d, plan.S, plan.tiles_x, maxbits, plan.scale,
+                                                            plan.xop, plan.nrm, 4);
     count_launches(1);
-    tc_image_kernel<<<dim3(plan.tiles_y, B), TC_M, 0, st>>>(yc, m, plan.tiles_y, maxbits, plan.scale, plan.yop,
-                                                            plan.nrm + 2, 4);
+    tc_image_kernel<<<dim3(plan.tiles_y, B), TC_M, 0, st>>>(yc, m, d, plan.S, plan.tiles_y, maxbits, plan.scale,
+                                                            plan.yop, plan.nrm + 2, 4);
     return cudaGetLastError();
 }
 
@@ -208,6 +227,7 @@ struct TcOps {
     const float* bias;          // [B][tiles_c * TC_N] column biases c_j, -inf past the last column
     const unsigned char* bias_img;  // [B][tiles_c] 16 KB tiles: fp16 bias parts (screened half-step)
     int tiles_r, tiles_c;
+    int S;                          // slices of K = 64 per image tile
     int hold_tile;                  // testing hook: the producer issues no copy from this column tile of its
                                     // chunk on (-1: off), so the waits on it run out
     unsigned long long wait_ns;     // limit of every bounded wait
@@ -396,13 +416,13 @@ __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t
 }
 
 // Never leave a bulk copy in flight into this CTA's shared memory: waits
-// (bounded, and not cut short by the abort flag) for the last TC_S stages
-// issued and for the row tiles.
-__device__ __forceinline__ void tc_producer_drain(const TcSmem& S, int issued, uint64_t wait_ns) {
+// (bounded, and not cut short by the abort flag) for the last nst stages
+// issued (a ring of nst stages) and for the row tiles.
+__device__ __forceinline__ void tc_producer_drain(const TcSmem& S, int issued, uint64_t wait_ns, int nst = TC_S) {
     if ((threadIdx.x & 31) == 0) {
         int dummy = 0;
-        for (int lt = (issued > TC_S ? issued - TC_S : 0); lt < issued; ++lt)
-            mbar_wait_bounded(S.bar(BAR_FULL(lt % TC_S)), (uint32_t)(lt / TC_S) & 1u, (volatile int*)&dummy,
+        for (int lt = (issued > nst ? issued - nst : 0); lt < issued; ++lt)
+            mbar_wait_bounded(S.bar(BAR_FULL(lt % nst)), (uint32_t)(lt / nst) & 1u, (volatile int*)&dummy,
                               wait_ns);
         mbar_wait_bounded(S.bar(BAR_A()), 0u, (volatile int*)&dummy, wait_ns);
     }
@@ -508,22 +528,19 @@ __device__ __forceinline__ void tc_release(const TcSmem& S, int wg, int lt) {
 // fallback for rows whose fast path could not give the value): fp32 dot
 // products of the centred coordinates, x held in registers, y read as float4.
 template <int NT>
-__device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc,
+__device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc, int d,
                              int row, float tk, float* red) {
-    const float4* xr = reinterpret_cast<const float4*>(rows + (size_t)row * TC_D);
-    float4 xv[TC_D / 4];
-#pragma unroll
-    for (int q = 0; q < TC_D / 4; ++q) xv[q] = xr[q];
+    const float4* xr = reinterpret_cast<const float4*>(rows + (size_t)row * d);  // read per column (L1)
     auto score = [&](int j) {
-        const float4* y = reinterpret_cast<const float4*>(cols + (size_t)j * TC_D);
+        const float4* y = reinterpret_cast<const float4*>(cols + (size_t)j * d);
         float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int q = 0; q < TC_D / 4; ++q) {
-            const float4 v = __ldg(y + q);
-            a0 = fmaf(xv[q].x, v.x, a0);
-            a1 = fmaf(xv[q].y, v.y, a1);
-            a0 = fmaf(xv[q].z, v.z, a0);
-            a1 = fmaf(xv[q].w, v.w, a1);
+#pragma unroll 4
+        for (int q = 0; q < d / 4; ++q) {
+            const float4 xv = __ldg(xr + q), v = __ldg(y + q);
+            a0 = fmaf(xv.x, v.x, a0);
+            a1 = fmaf(xv.y, v.y, a1);
+            a0 = fmaf(xv.z, v.z, a0);
+            a1 = fmaf(xv.w, v.w, a1);
         }
         return fmaf(tk, a0 + a1, cw[j] - cst[j]);
     };
@@ -550,11 +567,11 @@ __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, 
     const int lane = threadIdx.x & 31;
     __syncthreads();
     const int nretry = misc[2];
-    const float* rows_fp32 = p.rpack + (size_t)b * p.nr * TC_D;
-    const float* cols_fp32 = p.cpack + (size_t)b * p.nc * TC_D;
+    const float* rows_fp32 = p.rpack + (size_t)b * p.nr * p.d;
+    const float* cols_fp32 = p.cpack + (size_t)b * p.nc * p.d;
     for (int k = 0; k < nretry; ++k) {
         const int r = retry[k];
-        const float v = tc_row_full<NT>(rows_fp32, cols_fp32, cw, cst, p.nc, r, p.two_kappa, red);
+        const float v = tc_row_full<NT>(rows_fp32, cols_fp32, cw, cst, p.nc, p.d, r, p.two_kappa, red);
         if (threadIdx.x == 0) {
             p.rstate_out[rbase + r] = v;
             atomicOr(p.status, SOT_DEV_RETRY_ROWS);
@@ -746,13 +763,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
 }
 
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st) {
-    if (mode != MODE_LSE || p.d != TC_D) return cudaErrorInvalidValue;
+    if (mode != MODE_LSE || p.d != TC_D || plan.S != 1) return cudaErrorInvalidValue;
     TcOps ops;
     ops.aimg = h ? plan.yop : plan.xop;
     ops.bimg = h ? plan.xop : plan.yop;
     ops.scale = plan.scale;
     ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
+    ops.S = plan.S;
     ops.bias = plan.bias;
     ops.bias_img = nullptr;
     tc_fill_waits(ops);
@@ -807,55 +825,80 @@ static_assert(SC_COLS % 32 == 0 && 4 * SC_N == SC_EPI * SC_COLS, "epilogue colum
 int tc_screen_pool_cap() { return TC_POOL; }
 int tc_screen_pool_segments() { return SC_SEGS; }
 constexpr int TC_XS = TC_D + 4;  // row stride of the fp32 row tile in shared memory (bank spread)
-// Finaliser shared memory (the ring's space): fp32 rows, per-row words, the
-// segment offsets, then a dense copy of the kept pairs when they fit.
-constexpr int SC_LIST_CAP = 8192;
-constexpr uint32_t SC_FIN_LIST = (TC_ROWS * TC_XS * 4 + TC_ROWS * 20 + (64 * SC_SEGS + 1) * 4 + 15) & ~15u;
-static_assert(SC_FIN_LIST + SC_LIST_CAP * 8 <= TC_S * SC_STAGE, "finaliser shared memory");
+// Finaliser shared memory (the ring's space): the block's fp32 rows (NS = 1
+// only; wider rows are read from global memory), per-row words, the segment
+// offsets, then a dense copy of the kept pairs when they fit.
+template <int NS>
+struct ScFin {
+    static constexpr uint32_t SX = NS == 1 ? TC_ROWS * TC_XS * 4 : 0;
+    static constexpr uint32_t LIST = (SX + TC_ROWS * 20 + (64 * SC_SEGS + 1) * 4 + 15) & ~15u;
+    static constexpr int CAP = 8192;
+};
+static_assert(ScFin<1>::LIST + ScFin<1>::CAP * 8 <= ScLayout<1>::NST * SC_STAGE &&
+                  ScFin<2>::LIST + ScFin<2>::CAP * 8 <= ScLayout<2>::NST * SC_STAGE &&
+                  ScFin<3>::LIST + ScFin<3>::CAP * 8 <= ScLayout<3>::NST * SC_STAGE &&
+                  ScFin<4>::LIST + ScFin<4>::CAP * 8 <= ScLayout<4>::NST * SC_STAGE,
+              "finaliser shared memory");
 
 // Producer of the screened half-step: the hi halves of the CTA's two row
-// tiles once, then per 256-column tile the hi halves of its two 128-point
-// image tiles (back to back: one 256-row K-major operand) and its bias block.
+// tiles (every slice) once, then per 256-column tile and slice of K = 64 the
+// hi halves of its two 128-point image tiles (back to back: one 256-row
+// K-major operand), with the tile's bias block on its last slice.
 // t0: first 128-point image tile of the chunk (even); nt: 256-column tiles.
+template <int NS>
 __device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt) {
+    using L = ScLayout<NS>;
     const int lane = threadIdx.x & 31;
     volatile int* abort = S.abort();
     int issued = 0;
     if (lane == 0) {
-        const unsigned char* a0 = ops.aimg + ((size_t)b * ops.tiles_r + 2 * rb) * OP_BYTES;
-        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * TILE_BYTES);
-        bulk_g2s(S.sbase + SC_OFF_A, a0, TILE_BYTES, S.bar(BAR_A()));
-        bulk_g2s(S.sbase + SC_OFF_A + TILE_BYTES, a0 + OP_BYTES, TILE_BYTES, S.bar(BAR_A()));
+        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * NS * TILE_BYTES);
+        for (int r = 0; r < 2; ++r)
+            for (int k = 0; k < NS; ++k) {
+                const unsigned char* src = ops.aimg + (((size_t)b * ops.tiles_r + 2 * rb + r) * NS + k) * OP_BYTES;
+                bulk_g2s(S.sbase + L::OFF_A + (uint32_t)(r * NS + k) * TILE_BYTES, src, TILE_BYTES, S.bar(BAR_A()));
+            }
     }
-    const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * OP_BYTES;
+    const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * NS * OP_BYTES;
     const unsigned char* gbias = ops.bias_img + (size_t)b * (ops.tiles_c / 2) * SC_BT;
-    for (int lt = 0; lt < nt; ++lt) {
+    bool ok = true;
+    for (int lt = 0; ok && lt < nt; ++lt) {
         if (lt == ops.hold_tile) break;
-        const int st = lt % TC_S;
-        const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-        if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, ops.wait_ns)) break;
-        if (lane == 0) {
-            const uint32_t dst = S.sbase + SC_OFF_B + (uint32_t)st * SC_STAGE;
-            const unsigned char* src = bimg + (size_t)(t0 + 2 * lt) * OP_BYTES;
-            mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), SC_STAGE);
-            bulk_g2s(dst, src, TILE_BYTES, S.bar(BAR_FULL(st)));
-            bulk_g2s(dst + TILE_BYTES, src + OP_BYTES, TILE_BYTES, S.bar(BAR_FULL(st)));
-            bulk_g2s(dst + 2 * TILE_BYTES, gbias + (size_t)(t0 / 2 + lt) * SC_BT, SC_BT, S.bar(BAR_FULL(st)));
+        for (int k = 0; k < NS; ++k) {
+            const int it = lt * NS + k;
+            const int st = it % L::NST;
+            const uint32_t ph = (uint32_t)(it / L::NST) & 1u;
+            if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, ops.wait_ns)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                const uint32_t dst = S.sbase + L::OFF_B + (uint32_t)st * SC_STAGE;
+                const bool last = (k == NS - 1);
+                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), 2 * TILE_BYTES + (last ? SC_BT : 0u));
+                bulk_g2s(dst, bimg + ((size_t)(t0 + 2 * lt) * NS + k) * OP_BYTES, TILE_BYTES, S.bar(BAR_FULL(st)));
+                bulk_g2s(dst + TILE_BYTES, bimg + ((size_t)(t0 + 2 * lt + 1) * NS + k) * OP_BYTES, TILE_BYTES,
+                         S.bar(BAR_FULL(st)));
+                if (last)
+                    bulk_g2s(dst + 2 * TILE_BYTES, gbias + (size_t)(t0 / 2 + lt) * SC_BT, SC_BT, S.bar(BAR_FULL(st)));
+            }
+            issued = it + 1;
         }
-        issued = lt + 1;
     }
-    tc_producer_drain(S, issued, ops.wait_ns);
+    tc_producer_drain(S, issued, ops.wait_ns, L::NST);
 }
 
 // MMA warp of the screened half-step (one thread): per 256-column tile and
-// row tile r, four 128 x 256 x 16 hi*hi MMAs and the bias step (row-side
-// constants times the tile's bias block) into the row tile's accumulator
-// (TMEM columns 256 r ..); the epilogue frees it after loading it.
-// The thread shares its SM sub-partition with four busy epilogue warps, so
-// the work between two groups is kept short: every descriptor is formed
-// before the loop, and the commit that frees a tile's stage is issued after
-// the next tile's first group, off the path from one group to the next.
+// row tile r, four 128 x 256 x 16 hi*hi MMAs per slice of K = 64, then the
+// bias step (row-side constants times the tile's bias block), into the row
+// tile's accumulator (TMEM columns 256 r ..); the epilogue frees it after
+// loading it.  The thread shares its SM sub-partition with busy epilogue
+// warps, so the work between two groups is kept short: descriptors are
+// formed by adding offsets, and the commit that frees a stage is issued
+// after the next stage's first group, off the path from one group to the next.
+template <int NS>
 __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns) {
+    using L = ScLayout<NS>;
     if ((threadIdx.x & 31) == 0) {
         volatile int* abort = S.abort();
         bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, wait_ns);
@@ -865,37 +908,47 @@ __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns)
         // only part that differs, and every address here is below 256 KB, so a
         // byte offset o is added to a descriptor as o / 16 with no carry out of
         // the field; it advances by 2 per K = 16 step (32 bytes).
-        const uint64_t adesc0 = sw128_desc(S.sbase + SC_OFF_A), acdesc0 = sw32_desc(S.sbase + SC_OFF_AC);
-        const uint64_t bdesc0 = sw128_desc(S.sbase + SC_OFF_B), bbdesc0 = sw32_desc(S.sbase + SC_OFF_B + 2 * TILE_BYTES);
+        const uint64_t adesc0 = sw128_desc(S.sbase + L::OFF_A), acdesc0 = sw32_desc(S.sbase + L::OFF_AC);
+        const uint64_t bdesc0 = sw128_desc(S.sbase + L::OFF_B), bbdesc0 = sw32_desc(S.sbase + L::OFF_B + 2 * TILE_BYTES);
         int prev_st = -1;
         for (int lt = 0; ok && lt < nt; ++lt) {
-            const int st = lt % TC_S;
-            const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, wait_ns)) break;
-            for (int r = 0; r < 2 && ok; ++r) {
-                if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, 0)), ((uint32_t)lt & 1u) ^ 1u, abort, wait_ns)) {
+            for (int k = 0; ok && k < NS; ++k) {
+                const int it = lt * NS + k;
+                const int st = it % L::NST;
+                const uint32_t ph = (uint32_t)(it / L::NST) & 1u;
+                if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, wait_ns)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                issued_any = true;
-                const uint32_t d = tmem + (uint32_t)(r * SC_N);
-                const uint64_t ad = adesc0 + (uint64_t)(r * (TILE_BYTES >> 4));
-                const uint64_t bd = bdesc0 + (uint64_t)(st * (SC_STAGE >> 4));
+                for (int r = 0; r < 2; ++r) {
+                    if (k == 0) {
+                        if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, 0)), ((uint32_t)lt & 1u) ^ 1u, abort, wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    issued_any = true;
+                    const uint32_t d = tmem + (uint32_t)(r * SC_N);
+                    const uint64_t ad = adesc0 + (uint64_t)((r * NS + k) * (TILE_BYTES >> 4));
+                    const uint64_t bd = bdesc0 + (uint64_t)(st * (SC_STAGE >> 4));
 #pragma unroll
-                for (int k = 0; k < TC_D / 16; ++k)
-                    tc_mma_f16(d, ad + 2u * (uint64_t)k, bd + 2u * (uint64_t)k, idesc, k > 0 ? 1u : 0u);
-                tc_mma_f16(d, acdesc0 + (uint64_t)(r * (SC_AT >> 4)), bbdesc0 + (uint64_t)(st * (SC_STAGE >> 4)), idesc,
-                           1u);
-                tc_commit(S.bar(BAR_ACCFULL(r, 0)));
-                if (r == 0 && prev_st >= 0) {
-                    // the previous tile's stage: its last readers were issued before this group
-                    tc_commit(S.bar(BAR_EMPTY(prev_st)));
-                    prev_st = -1;
+                    for (int kk = 0; kk < TC_D / 16; ++kk)
+                        tc_mma_f16(d, ad + 2u * (uint64_t)kk, bd + 2u * (uint64_t)kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+                    if (k == NS - 1) {
+                        tc_mma_f16(d, acdesc0 + (uint64_t)(r * (SC_AT >> 4)),
+                                   bbdesc0 + (uint64_t)(st * (SC_STAGE >> 4)), idesc, 1u);
+                        tc_commit(S.bar(BAR_ACCFULL(r, 0)));
+                    }
+                    if (r == 0 && prev_st >= 0) {
+                        // the previous stage: its last readers were issued before this group
+                        tc_commit(S.bar(BAR_EMPTY(prev_st)));
+                        prev_st = -1;
+                    }
                 }
+                if (!ok) break;
+                prev_st = st;
             }
-            if (!ok) break;
-            prev_st = st;
         }
         if (prev_st >= 0) tc_commit(S.bar(BAR_EMPTY(prev_st)));
         tc_mma_drain(S, issued_any, wait_ns);
@@ -943,7 +996,7 @@ struct ScShared {  // the same for every row of the warp
     uint2* seg;   // this warp's pool segment
     int wcount;   // entries reserved in it (warp-uniform)
     const float* ycol;  // the columns' fp32 coordinates (the finaliser reads a kept pair's row)
-    int nc;
+    int nc, d;
 };
 struct ScRow {  // one row's screening state
     float Lb, off, runmax;
@@ -1002,9 +1055,8 @@ __device__ __forceinline__ void sc_screen(const uint32_t (&r)[NQ][32], int jt, S
                 if (slot < SC_SEG) {
                     c.seg[slot] = make_uint2((unsigned)jc, s.rl);
                     if (jc < c.nc) {  // the finaliser reads this column's row: bring it into L2 now
-                        const float* yr = c.ycol + (size_t)jc * TC_D;
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(yr));
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(yr + 32));
+                        const float* yr = c.ycol + (size_t)jc * c.d;
+                        for (int o = 0; o < c.d; o += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(yr + o));
                     }
                 } else {
                     *s.lost = 1;
@@ -1017,10 +1069,14 @@ __device__ __forceinline__ void sc_screen(const uint32_t (&r)[NQ][32], int jt, S
 
 // 18 warps put five on one SM sub-partition, whose 16384 registers then allow
 // 96 per thread.
+template <int NS>
 __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, TcOps ops, TcScreenK sk) {
+    using L = ScLayout<NS>;
+    using F = ScFin<NS>;
+    constexpr int D = NS * TC_D;  // coordinates (the images' K)
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     extern __shared__ unsigned char smem_raw[];
-    const TcSmem S = tc_smem(smem_raw, SC_OFF_HDR);
+    const TcSmem S = tc_smem(smem_raw, L::OFF_HDR);
     int* misc = S.misc();
     volatile int* abort = S.abort();
     int* retry = S.retry();
@@ -1055,7 +1111,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const uint4 c0 = make_uint4(h0 | (h1 << 16), h2, 0u, 0u), z = make_uint4(0u, 0u, 0u, 0u);
         for (int e = threadIdx.x; e < 2 * TC_M * 2; e += SC_THREADS) {
             const int rt = e / (2 * TC_M), r = (e % (2 * TC_M)) >> 1, c = e & 1;
-            *reinterpret_cast<uint4*>(S.sm + SC_OFF_AC + rt * SC_AT + sw32_offset(r, 8 * c)) = c ? z : c0;
+            *reinterpret_cast<uint4*>(S.sm + L::OFF_AC + rt * SC_AT + sw32_offset(r, 8 * c)) = c ? z : c0;
         }
         fence_proxy_async_smem();
     }
@@ -1070,9 +1126,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
-        sc_producer(S, ops, b, rb, t0, nts);
+        sc_producer<NS>(S, ops, b, rb, t0, nts);
     } else if (warp == 1) {
-        sc_mma(S, tmem, nts, ops.wait_ns);
+        sc_mma<NS>(S, tmem, nts, ops.wait_ns);
     } else {
         // Screening: epilogue warp ew = warp - 2 (column group cg = ew / 4, lane
         // quarter q4) reads columns SC_COLS cg .. of both row tiles' accumulators for
@@ -1088,13 +1144,15 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const float hc = __uint_as_float(sk.nrm_c[4 * b]), rc = __uint_as_float(sk.nrm_c[4 * b + 1]);
         const float cmax = __uint_as_float(sk.cmax[b]);
         ScShared c;
-        c.Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + 1.5258789e-5f * hr * hc) + 1.5258789e-5f * cmax + 0.02f;
+        c.Mg = 1.01f * tk * (rr * hc + hr * rc + rr * rc + (float)NS * 1.5258789e-5f * hr * hc) + 1.5258789e-5f * cmax +
+               0.02f;
         c.tk = tk;
         c.inv_tk = 1.f / tk;
         c.seg = sk.pool + ((cta0 + ch) * SC_SEGS + ew) * (size_t)SC_SEG;
         c.wcount = 0;
-        c.ycol = p.cpack + (size_t)b * p.nc * TC_D;
+        c.ycol = p.cpack + (size_t)b * p.nc * D;
         c.nc = p.nc;
+        c.d = D;
         const float theta_off = 26.f + log2f((float)p.nc) + c.Mg + 0.05f;
         const float lo = (!p.cold && p.lo_in) ? ord_decode(p.lo_in[b]) : -INFINITY;
         ScRow s[2];
@@ -1161,27 +1219,29 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     }
 
     // ---------------- finish the row block: exact scores of the kept pairs ----------------
-    float* sx = reinterpret_cast<float*>(S.sm + SC_OFF_B);                  // [TC_ROWS][TC_XS] fp32 rows
-    float* s_ref = sx + TC_ROWS * TC_XS;                                     // [TC_ROWS] reference L_old
+    float* sx = reinterpret_cast<float*>(S.sm + L::OFF_B);                  // [TC_ROWS][TC_XS] fp32 rows (NS = 1)
+    float* s_ref = reinterpret_cast<float*>(S.sm + L::OFF_B + F::SX);       // [TC_ROWS] reference L_old
     unsigned* s_max = reinterpret_cast<unsigned*>(s_ref + TC_ROWS);          // [TC_ROWS] ord-encoded max
     unsigned long long* s_sum = reinterpret_cast<unsigned long long*>(s_max + TC_ROWS);  // [TC_ROWS] fixed point
     int* s_lost = reinterpret_cast<int*>(s_sum + TC_ROWS);                   // [TC_ROWS]
     int* s_off = s_lost + TC_ROWS;                                           // [split * SC_SEGS + 1]
     {
-        // the block's fp32 rows: every load issued before the first store
-        const float4* src = reinterpret_cast<const float4*>(p.rpack + rbase * TC_D);
-        constexpr int NE = TC_ROWS * (TC_D / 4), NL = (NE + SC_THREADS - 1) / SC_THREADS;
-        float4 buf[NL];
+        if (NS == 1) {
+            // the block's fp32 rows: every load issued before the first store
+            const float4* src = reinterpret_cast<const float4*>(p.rpack + rbase * TC_D);
+            constexpr int NE = TC_ROWS * (TC_D / 4), NL = (NE + SC_THREADS - 1) / SC_THREADS;
+            float4 buf[NL];
 #pragma unroll
-        for (int i = 0; i < NL; ++i) {
-            const int e = threadIdx.x + i * SC_THREADS, rg = row0 + e / (TC_D / 4);
-            buf[i] = (e < NE && rg < p.nr) ? __ldg(src + (size_t)rg * (TC_D / 4) + e % (TC_D / 4))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+            for (int i = 0; i < NL; ++i) {
+                const int e = threadIdx.x + i * SC_THREADS, rg = row0 + e / (TC_D / 4);
+                buf[i] = (e < NE && rg < p.nr) ? __ldg(src + (size_t)rg * (TC_D / 4) + e % (TC_D / 4))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-        for (int i = 0; i < NL; ++i) {
-            const int e = threadIdx.x + i * SC_THREADS;
-            if (e < NE) *reinterpret_cast<float4*>(sx + (e / (TC_D / 4)) * TC_XS + 4 * (e % (TC_D / 4))) = buf[i];
+            for (int i = 0; i < NL; ++i) {
+                const int e = threadIdx.x + i * SC_THREADS;
+                if (e < NE) *reinterpret_cast<float4*>(sx + (e / (TC_D / 4)) * TC_XS + 4 * (e % (TC_D / 4))) = buf[i];
+            }
         }
         for (int r = threadIdx.x; r < TC_ROWS; r += SC_THREADS) {
             const int rg = row0 + r;
@@ -1233,11 +1293,11 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
     }
     __syncthreads();
     const int total = s_off[nseg];
-    const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * TC_D);
+    const float4* ybase = reinterpret_cast<const float4*>(p.cpack + (size_t)b * p.nc * D);
     // the kept pairs, segment after segment, into one dense list in shared
     // memory when they fit (every later lookup is one shared load)
-    uint2* s_list = reinterpret_cast<uint2*>(S.sm + SC_OFF_B + SC_FIN_LIST);
-    const bool dense = total <= SC_LIST_CAP;
+    uint2* s_list = reinterpret_cast<uint2*>(S.sm + L::OFF_B + F::LIST);
+    const bool dense = total <= F::CAP;
     if (dense) {
         for (int g = warp; g < nseg; g += SC_THREADS / 32) {
             const uint2* src = sk.pool + (cta0 * SC_SEGS + g) * (size_t)SC_SEG;
@@ -1257,7 +1317,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         }
         return sk.pool + (cta0 * SC_SEGS + lo) * (size_t)SC_SEG + (k - s_off[lo]);
     };
-    // Four lanes per kept pair (a quad), each taking TC_D / 4 coordinates:
+    // Four lanes per kept pair (a quad), each taking a quarter of every slice of 64:
     // short dependency chains and few live registers.  The quad's partial
     // dot products are error-free float-float values (Dekker / Knuth
     // transformations, errors summed alongside), combined across the quad
@@ -1275,22 +1335,27 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         const bool v0 = in && !s_lost[it0.y] && (int)it0.x < p.nc;
         float hs[4] = {0.f, 0.f, 0.f, 0.f}, es[4] = {0.f, 0.f, 0.f, 0.f};
         if (v0) {
-            const float4* y = ybase + (size_t)it0.x * (TC_D / 4) + sub * (QD / 4);
-            const float* xr = sx + it0.y * TC_XS + sub * QD;
-            float4 yv[QD / 4];
+            // x: the staged row (NS = 1) or the row in global memory
+            const float* xrow = (NS == 1) ? sx + it0.y * TC_XS : p.rpack + (rbase + row0 + it0.y) * (size_t)D;
+#pragma unroll 1
+            for (int sl = 0; sl < NS; ++sl) {
+                const float4* y = ybase + (size_t)it0.x * (D / 4) + sl * (TC_D / 4) + sub * (QD / 4);
+                const float* xr = xrow + sl * TC_D + sub * QD;
+                float4 yv[QD / 4];
 #pragma unroll
-            for (int q = 0; q < QD / 4; ++q) yv[q] = __ldg(y + q);
+                for (int q = 0; q < QD / 4; ++q) yv[q] = __ldg(y + q);
 #pragma unroll
-            for (int q = 0; q < QD / 4; ++q) {
-                const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q);
-                const float xa[4] = {x.x, x.y, x.z, x.w};
-                const float ya[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
+                for (int q = 0; q < QD / 4; ++q) {
+                    const float4 x = *reinterpret_cast<const float4*>(xr + 4 * q);
+                    const float xa[4] = {x.x, x.y, x.z, x.w};
+                    const float ya[4] = {yv[q].x, yv[q].y, yv[q].z, yv[q].w};
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float2 pr = two_prod(xa[w], ya[w]);
-                    const float2 sn = two_sum(hs[w], pr.x);
-                    hs[w] = sn.x;
-                    es[w] = __fadd_rn(es[w], __fadd_rn(pr.y, sn.y));
+                    for (int w = 0; w < 4; ++w) {
+                        const float2 pr = two_prod(xa[w], ya[w]);
+                        const float2 sn = two_sum(hs[w], pr.x);
+                        hs[w] = sn.x;
+                        es[w] = __fadd_rn(es[w], __fadd_rn(pr.y, sn.y));
+                    }
                 }
             }
         }
@@ -1363,7 +1428,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
 }
 
 cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const TcScreen& sc, cudaStream_t st) {
-    if (p.d != TC_D || !p.lo_in || !sc.pool || !sc.pool_cnt || !sc.lost || sc.pool_cap != TC_POOL)
+    if (!tc_supported(p.d) || p.d != plan.d || !p.lo_in || !sc.pool || !sc.pool_cnt || !sc.lost ||
+        sc.pool_cap != TC_POOL)
         return cudaErrorInvalidValue;
     TcOps ops;
     ops.aimg = h ? plan.yop : plan.xop;
@@ -1371,6 +1437,7 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
     ops.scale = plan.scale;
     ops.tiles_r = h ? plan.tiles_y : plan.tiles_x;
     ops.tiles_c = h ? plan.tiles_x : plan.tiles_y;
+    ops.S = plan.S;
     ops.bias = plan.bias;
     ops.bias_img = plan.bimg;
     tc_fill_waits(ops);
@@ -1388,11 +1455,24 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
     sk.nrm_r = plan.nrm + (h ? 2 : 0);
     sk.nrm_c = plan.nrm + (h ? 0 : 2);
     if (p.chunk % SC_N != 0 || ops.tiles_c % 2 != 0) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc_screen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM);
-    if (e != cudaSuccess) return e;
     dim3 grid(p.rowtiles * p.split, p.B), block(SC_THREADS);
-    count_launches(1);
-    tc_screen_kernel<<<grid, block, SC_SMEM, st>>>(p, ops, sk);
+#define SOT_SC_CASE(NSV)                                                                                   \
+    case NSV: {                                                                                            \
+        cudaError_t e = cudaFuncSetAttribute(tc_screen_kernel<NSV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                             (int)ScLayout<NSV>::SMEM);                                    \
+        if (e != cudaSuccess) return e;                                                                    \
+        count_launches(1);                                                                                 \
+        tc_screen_kernel<NSV><<<grid, block, ScLayout<NSV>::SMEM, st>>>(p, ops, sk);                       \
+        break;                                                                                             \
+    }
+    switch (plan.S) {
+        SOT_SC_CASE(1)
+        SOT_SC_CASE(2)
+        SOT_SC_CASE(3)
+        SOT_SC_CASE(4)
+        default: return cudaErrorInvalidValue;
+    }
+#undef SOT_SC_CASE
     return cudaGetLastError();
 }
 
@@ -1675,6 +1755,7 @@ cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfAr
     ops.scale = plan.scale;
     ops.tiles_r = plan.tiles_x;
     ops.tiles_c = plan.tiles_y;
+    ops.S = plan.S;
     ops.bias = plan.bias;
     ops.bias_img = nullptr;
     tc_fill_waits(ops);

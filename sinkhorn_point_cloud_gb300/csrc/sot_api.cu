@@ -190,7 +190,8 @@ enum Path { PATH_POINT = 0, PATH_DENSE = 1, PATH_TC = 2 };
 int choose_path(int d, int flags, Path* out) {
     const int prec = flags & SOT_PREC_MASK;
     if (prec == SOT_PREC_F16X3) {
-        if (!tc_supported(d)) return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d = %d (got d = %d)", tc_max_d(), d);
+        if (!tc_supported(d))
+            return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d = 64, 128, 192 or 256 (got d = %d)", d);
         *out = PATH_TC;
         return SOT_OK;
     }
@@ -293,6 +294,11 @@ struct Solver {
     int nstage_slots = 0;
     int sms;
     int split[2], chunk[2], rowtiles[2];  // [0] f-half (rows X), [1] g-half (rows Y)
+    // Tensor path with d > 64: the screened half-step takes the warm half-steps,
+    // the fp32 dense half-step (with its own split plan) every other one.
+    bool tc_dense_full = false;
+    int dsplit[2], dchunk[2], drowtiles[2];
+    int last_rowtiles[2] = {0, 0};  // row tiles of the last half-step of each side (its error partials)
     TcPlan tc;
     // Screened tensor-core half-steps: allowed by the caller, and on for the
     // current stage until too many rows overflow their candidate lists.
@@ -362,11 +368,20 @@ struct Solver {
                 choose_split(B, nr, nc, tc_rows_per_cta(), tc_cols_per_tile(), sms, 1, &split[h], &chunk[h],
                              &rowtiles[h]);
         }
+        tc_dense_full = (path == PATH_TC) && !tc_half_supported(d);
+        for (int h = 0; h < 2; ++h) {
+            dsplit[h] = split[h];
+            dchunk[h] = chunk[h];
+            drowtiles[h] = rowtiles[h];
+            if (tc_dense_full)
+                choose_split(B, h ? m : n, h ? n : m, dense_rows_per_cta(), dense_cols_per_tile(), sms, 2, &dsplit[h],
+                             &dchunk[h], &drowtiles[h]);
+        }
         if (point && cluster_allowed)
             cluster_ok = point_cluster_plan(B, n, m, sms, &cl_C, &cl_T, &cl_S, &cl_smem);
-        const int smax = split[0] > split[1] ? split[0] : split[1];
+        const int smax = std::max(std::max(split[0], split[1]), std::max(dsplit[0], dsplit[1]));
         const size_t rows_max = (size_t)B * (n > m ? n : m);
-        const int rt_max = rowtiles[0] > rowtiles[1] ? rowtiles[0] : rowtiles[1];
+        const int rt_max = std::max(std::max(rowtiles[0], rowtiles[1]), std::max(drowtiles[0], drowtiles[1]));
         if (smax > 1) {
             part_m = S.alloc<float>(rows_max * smax);
             part_s = S.alloc<float>(rows_max * smax);
@@ -434,6 +449,13 @@ struct Solver {
         return p;
     }
 
+    // The same with the dense kernels' split plan (tensor path, d > 64).
+    void use_dense_plan(HalfArgs& p, int h) const {
+        p.split = dsplit[h];
+        p.chunk = dchunk[h];
+        p.rowtiles = drowtiles[h];
+    }
+
     int half(int h, int mode, float kappa, bool cold, const float* rin, float* rout, float* errp, bool guarded) {
         HalfArgs p = half_args(h, kappa, cold, rin, rout, errp, guarded);
         p.lo_in = nullptr;
@@ -455,7 +477,11 @@ struct Solver {
                 e = launch_dense_half(p, mode, st);
             } else if (mode == MODE_LSE && screen_on && !cold && p.lo_in) {
                 ps.kind = 1;
-                if (screen_probation) {
+                // On probation, row blocks with many overflowing rows are left to a full
+                // tensor-core half-step.  At d > 64 there is none: every overflowing row
+                // takes the exact full-row LSE inline, and screen_check() then ends
+                // screening for the stage if there were many.
+                if (screen_probation && !tc_dense_full) {
                     SOT_CUDA(cudaMemsetAsync(redo, 0, sizeof(int) * (size_t)B * rowtiles[h], st));
                     p.redo = redo;
                 }
@@ -465,10 +491,14 @@ struct Solver {
                     q.lo_reset = nullptr;
                     e = launch_tc_half(tc, q, h, mode, st);
                 }
+            } else if (tc_dense_full) {
+                use_dense_plan(p, h);
+                e = launch_dense_half(p, mode, st);
             } else {
                 e = launch_tc_half(tc, p, h, mode, st);
             }
         }
+        last_rowtiles[h] = p.rowtiles;
         if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "half-step launch failed: %s", cudaGetErrorString(e));
         return SOT_OK;
     }
@@ -554,7 +584,8 @@ struct Solver {
         }
         int rc = half(0, MODE_LSE, kappa, !bound_ok, L, Lnext, errpart, true);
         if (rc) return rc;
-        SOT_CUDA(launch_decide(errpart, B, rowtiles[0], tol, force, err, stop_flag(), conv_flag(), Lnext, L, B * n, st));
+        SOT_CUDA(launch_decide(errpart, B, last_rowtiles[0], tol, force, err, stop_flag(), conv_flag(), Lnext, L, B * n,
+                               st));
         return SOT_OK;
     }
 };
@@ -722,6 +753,51 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
 
 }  // namespace
 
+// Plan application from transport products (the tensor path at d > 64, where
+// no tensor-core plan application exists): r and sum_j P_ij C_ij from the
+// cost mode, P Y in blocks of 64 coordinates, every weight and distance in
+// float-float, then grad = 2 (a x - P Y) and cost = sum_i q_i.
+int plan_apply_transport(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
+                         const float* f, const float* g, float eps, float* cost, float* grad, float* rowsum,
+                         cudaStream_t cs) {
+    const double kap = 1.0 / ((double)eps * SOT_LN2_D);
+    const int sms = device_sms();
+    Scratch S(cs);
+    float* rq = S.alloc<float>((size_t)B * n * 2);
+    float* q = S.alloc<float>((size_t)B * n);
+    size_t nparts = 0;
+    {
+        int sp, chn;
+        nparts = std::max(nparts, transport_plan(B, n, m, 2, sms, &sp, &chn));
+        nparts = std::max(nparts, transport_plan(B, n, m, std::min(d, transport_max_c()), sms, &sp, &chn));
+    }
+    float* part = nparts ? S.alloc<float>(nparts) : nullptr;
+    if (!rq || !q || (nparts && !part)) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    TransportArgs t;
+    t.B = B; t.nr = n; t.nc = m; t.d = d; t.R = X; t.Cl = Y; t.fr = f; t.gc = g; t.wr = a; t.wc = b;
+    t.kap_hi = (float)kap;
+    t.kap_lo = (float)(kap - (double)t.kap_hi);
+    t.part = part;
+    // r_i and q_i = sum_j P_ij C_ij (V is not read)
+    t.c = 2; t.V = Y; t.ldv = 2; t.out = rq; t.ldo = 2;
+    transport_plan(B, n, m, 2, sms, &t.split, &t.chunk);
+    SOT_CUDA(launch_transport_cost(t, cs));
+    SOT_CUDA(launch_cost_rows(rq, (long long)B * n, rowsum, q, cs));
+    if (cost) SOT_CUDA(launch_reduce_parts(q, B, n, cost, cs));
+    if (grad) {
+        // (P Y)_i into grad, 64 coordinates per product, then grad = 2 (a x - P Y)
+        for (int k0 = 0; k0 < d; k0 += transport_max_c()) {
+            t.c = std::min(transport_max_c(), d - k0);
+            t.V = Y + k0; t.ldv = d;
+            t.out = grad + k0; t.ldo = d;
+            transport_plan(B, n, m, t.c, sms, &t.split, &t.chunk);
+            SOT_CUDA(launch_transport(t, cs));
+        }
+        SOT_CUDA(launch_grad_finish(X, a, B, n, d, grad, cs));
+    }
+    return SOT_OK;
+}
+
 // ===========================================================================
 extern "C" {
 
@@ -834,8 +910,7 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     Path path;
     rc = choose_path(d, flags, &path);
     if (rc) return rc;
-    if (path == PATH_TC &&
-        (!tc_apply_supported(d) || ((flags & SOT_PREC_MASK) == SOT_PREC_AUTO && !tc_apply_default())))
+    if (path == PATH_TC && tc_apply_supported(d) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO && !tc_apply_default())
         path = PATH_DENSE;
     // Cosine cost: on unit points every score is below 2 kappa in magnitude, so
     // fp32 scores keep cost and gradient at fp32 accuracy, and the plan is often
@@ -843,6 +918,12 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     // which only pays for a few pairs per row).
     if (path == PATH_TC && (flags & SOT_COST_COSINE) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO) path = PATH_DENSE;
     cudaStream_t cs = (cudaStream_t)stream;
+    if (path == PATH_TC && !tc_apply_supported(d)) {
+        rc = plan_apply_transport(X, Y, a, b, B, n, m, d, f, g, eps, cost, grad, rowsum, cs);
+        if (rc) return rc;
+        if (grad && (flags & SOT_COST_COSINE)) SOT_CUDA(launch_cosine_grad(Xin, (long long)B * n, d, grad, cs));
+        return SOT_OK;
+    }
     Solver sv(X, Y, a, b, B, n, m, d, path, cs);
     rc = sv.prepare(0);
     if (rc) return rc;

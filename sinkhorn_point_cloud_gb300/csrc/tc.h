@@ -11,8 +11,9 @@ namespace sot {
 // the centred coordinates.
 struct TcPlan {
     int B = 0, n = 0, m = 0, d = 0;
+    int S = 1;                     // slices of K = 64 per image tile (d / 64)
     int tiles_x = 0, tiles_y = 0;  // 128-point tiles per cloud in each image (even count)
-    unsigned char* xop = nullptr;  // operand image of X: per tile 16 KB fp16 hi + 16 KB fp16 lo, swizzled
+    unsigned char* xop = nullptr;  // operand image of X: per tile and slice 16 KB fp16 hi + 16 KB fp16 lo, swizzled
     unsigned char* yop = nullptr;  // operand image of Y
     float* scale = nullptr;        // [B] power-of-two coordinate scale used by the images
     float* bias = nullptr;         // [B][max tiles * 128] column biases of the current half-step
@@ -38,7 +39,10 @@ struct TcScreen {
 // chunk on (tile < 0: off), and every bounded wait gives up after wait_ns
 // (0: 2 s).
 void tc_set_test_hold(int tile, int after, unsigned long long wait_ns);
+// The screened half-step takes d = 64, 128, 192, 256; the full half-step and
+// the plan application d = 64 only.
 bool tc_supported(int d);
+bool tc_half_supported(int d);
 int tc_max_d();
 int tc_rows_per_cta();
 int tc_cols_per_tile();

@@ -164,21 +164,22 @@ def test_python_binding_checks_caller_tensors():
 
 def test_path_selection(lib):
     """The kernel family each dimension and precision flag takes (host logic,
-    no GPU needed): d <= 3 the point kernels, d = 64 the tensor cores under
-    automatic precision, other d up to 256 the fp32 kernels; the fp16 split is
-    d = 64 only and nothing goes past d = 256."""
+    no GPU needed): d <= 3 the point kernels; d = 64, 128, 192, 256 the tensor
+    cores under automatic precision; other d up to 256 the fp32 kernels; the
+    fp16 split takes those four d only and nothing goes past d = 256."""
     point, dense, tensor = 0, 1, 2
     for d in (1, 2, 3):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == point
         assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == point
-    for d in (4, 8, 17, 63, 65, 128, 256):
+    for d in (4, 8, 17, 63, 65, 100, 200, 255):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == dense, d
-    assert lib.sot_select_path(64, binding.SOT_PREC_AUTO) == tensor
-    assert lib.sot_select_path(64, binding.SOT_PREC_F16X3) == tensor
-    assert lib.sot_select_path(64, binding.SOT_PREC_FP32) == dense
-    for d in (8, 128):
-        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED
+        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED, d
+    for d in (64, 128, 192, 256):
+        assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == tensor, d
+        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == tensor, d
+        assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
     assert lib.sot_select_path(257, binding.SOT_PREC_AUTO) == binding.SOT_ERR_UNSUPPORTED
+    assert lib.sot_select_path(320, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED
 
 
 def test_hvp_arguments_rejected_on_host(lib):

@@ -177,8 +177,8 @@ def test_bitwise_reproducible(sot):
 
 
 def test_dense_fp32_path_largest_d(sot, orc):
-    """d = 256, the fp32 path's largest dimension (above the tensor path's d = 64)."""
+    """d = 256, the fp32 path's largest dimension."""
     from sinkhorn_point_cloud_gb300 import datagen as dg
     X, Y, a, b = dg.make_batch(4, B=1, n=200, m=170, d=256)
-    assert sot.sot_select_path(256, 0) == 1
-    print(check(sot, orc, X, Y, a, b, 2.0, 60))
+    assert sot.sot_select_path(256, sot.SOT_PREC_FP32) == 1
+    print(check(sot, orc, X, Y, a, b, 2.0, 60, flags=sot.SOT_PREC_FP32))

@@ -222,3 +222,47 @@ def test_tc_screened_annealed_schedule(sot, orc):
     fr, gref = orc.sinkhorn(X[0], Y[0], a[0], b[0], stages, [10] * len(stages))
     ef, eg = potentials_error(host(f), host(g), fr[None], gref[None])
     assert ef < TOL and eg < TOL, (ef, eg)
+
+
+@pytest.mark.parametrize("d,n,m,eps", [(128, 1100, 1000, 0.2), (192, 600, 520, 0.3), (256, 700, 650, 0.4)])
+def test_tc_wide_matches_oracle(sot, orc, d, n, m, eps):
+    """d = 128, 192, 256 on the tensor path ("FlashSinkhorn", Experimentele
+    Resultaten: the streaming kernels run up to d = 1024): warm half-steps on
+    the screened kernel with a K loop over slices of 64, cold half-steps and
+    the plan application on the fp32 kernels.  Gaussian recipe with softmax
+    weights; potentials, cost and gradient against the oracle."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=n, m=m, d=d)
+    iters = 60
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    assert sot.sot_select_path(d, 0) == 2
+    sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(True)
+    f, g = sot.sot_potentials(Xd, Yd, ad, bd, eps=eps, iters=iters)
+    kinds = sot.sot_profile_read_kinds()
+    sot.sot_profile_enable(False)
+    assert kinds["screened"][0] == 2 * iters - 2, kinds  # the cold first iteration is dense
+    c, gr, _ = sot.sot_plan_apply(Xd, Yd, ad, bd, f, g, eps)
+    fr, gref = orc.sinkhorn(X[0], Y[0], a[0], b[0], [eps], [iters])
+    ef, eg = potentials_error(host(f), host(g), fr[None], gref[None])
+    out = orc.plan_apply(X[0], Y[0], a[0], b[0], host(f)[0], host(g)[0], eps)
+    ec = abs(host(c)[0] - out["cost"]) / abs(out["cost"])
+    egr = normwise(host(gr)[0], out["grad"])
+    msg = f"d = {d}: f {ef:.2e} g {eg:.2e} cost {ec:.2e} grad {egr:.2e}"
+    print(msg)
+    assert max(ef, eg, ec, egr) < TOL, msg
+
+
+def test_tc_wide_screened_agrees_with_fp32(sot):
+    """d = 128 and 256 with two clouds: the tensor path and the fp32 path give
+    the same potentials to well below the parity tolerance."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    for d, eps in ((128, 0.2), (256, 0.4)):
+        X, Y, a, b = dg.make_batch(4, B=2, n=1500, m=1300, d=d)
+        Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+        ft, gt = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=40, max_iters=40,
+                                       flags=sot.SOT_PREC_F16X3)
+        ff, gf = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=40, max_iters=40,
+                                       flags=sot.SOT_PREC_FP32)
+        ef, eg = potentials_error(host(ft), host(gt), host(ff), host(gf))
+        assert ef < 2e-5 and eg < 2e-5, (d, ef, eg)
