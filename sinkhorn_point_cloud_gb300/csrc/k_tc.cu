@@ -526,21 +526,38 @@ __device__ __forceinline__ void tc_release(const TcSmem& S, int wg, int lt) {
 
 // Exact two-pass LSE of one row over all columns, by the whole CTA (the
 // fallback for rows whose fast path could not give the value): fp32 dot
-// products of the centred coordinates, x held in registers, y read as float4.
-template <int NT>
+// products of the centred coordinates, y read as float4.  DC = TC_D keeps
+// the row in registers; DC = 0 takes any d (a multiple of 4) and reads the
+// row per column (L1).  The d = 64 form is kept as it is: the register
+// allocation of the kernels that inline it depends on it.
+template <int NT, int DC>
 __device__ float tc_row_full(const float* rows, const float* cols, const float* cw, const float* cst, int nc, int d,
                              int row, float tk, float* red) {
-    const float4* xr = reinterpret_cast<const float4*>(rows + (size_t)row * d);  // read per column (L1)
+    const float4* xr = reinterpret_cast<const float4*>(rows + (size_t)row * d);
+    float4 xv[DC > 0 ? DC / 4 : 1];
+#pragma unroll
+    for (int q = 0; q < (DC > 0 ? DC / 4 : 0); ++q) xv[q] = xr[q];
     auto score = [&](int j) {
         const float4* y = reinterpret_cast<const float4*>(cols + (size_t)j * d);
         float a0 = 0.f, a1 = 0.f;
+        if (DC > 0) {
+#pragma unroll
+            for (int q = 0; q < (DC > 0 ? DC / 4 : 0); ++q) {
+                const float4 v = __ldg(y + q);
+                a0 = fmaf(xv[q].x, v.x, a0);
+                a1 = fmaf(xv[q].y, v.y, a1);
+                a0 = fmaf(xv[q].z, v.z, a0);
+                a1 = fmaf(xv[q].w, v.w, a1);
+            }
+        } else {
 #pragma unroll 4
-        for (int q = 0; q < d / 4; ++q) {
-            const float4 xv = __ldg(xr + q), v = __ldg(y + q);
-            a0 = fmaf(xv.x, v.x, a0);
-            a1 = fmaf(xv.y, v.y, a1);
-            a0 = fmaf(xv.z, v.z, a0);
-            a1 = fmaf(xv.w, v.w, a1);
+            for (int q = 0; q < d / 4; ++q) {
+                const float4 x4 = __ldg(xr + q), v = __ldg(y + q);
+                a0 = fmaf(x4.x, v.x, a0);
+                a1 = fmaf(x4.y, v.y, a1);
+                a0 = fmaf(x4.z, v.z, a0);
+                a1 = fmaf(x4.w, v.w, a1);
+            }
         }
         return fmaf(tk, a0 + a1, cw[j] - cst[j]);
     };
@@ -558,7 +575,7 @@ __device__ float tc_row_full(const float* rows, const float* cols, const float* 
 // row values: rows queued in the retry list get the exact two-pass row LSE
 // (whole CTA), then the marginal-error partial and the bound for the next
 // half-step are formed from the new row values.
-template <int NT>
+template <int NT, int DC>
 __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, float old, int b, int rb,
                         size_t rbase, const float* cw, const float* cst) {
     int* misc = S.misc();
@@ -571,7 +588,7 @@ __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, 
     const float* cols_fp32 = p.cpack + (size_t)b * p.nc * p.d;
     for (int k = 0; k < nretry; ++k) {
         const int r = retry[k];
-        const float v = tc_row_full<NT>(rows_fp32, cols_fp32, cw, cst, p.nc, p.d, r, p.two_kappa, red);
+        const float v = tc_row_full<NT, DC>(rows_fp32, cols_fp32, cw, cst, p.nc, p.d, r, p.two_kappa, red);
         if (threadIdx.x == 0) {
             p.rstate_out[rbase + r] = v;
             atomicOr(p.status, SOT_DEV_RETRY_ROWS);
@@ -759,7 +776,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             retry[atomicAdd(&misc[2], 1)] = row;
         }
     }
-    tc_tail<TC_THREADS>(p, S, erow, row, old, b, rb, rbase, cw, cst);
+    tc_tail<TC_THREADS, TC_D>(p, S, erow, row, old, b, rb, rbase, cw, cst);
 }
 
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st) {
@@ -1424,7 +1441,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                 s_ref[rl] + (ord_decode(s_max[rl]) + (log2f(__ull2float_rn(s_sum[rl])) - 48.f));
         }
     }
-    tc_tail<SC_THREADS>(p, S, erow, row, old, b, rb, rbase, cw, cst);
+    tc_tail<SC_THREADS, NS == 1 ? TC_D : 0>(p, S, erow, row, old, b, rb, rbase, cw, cst);
 }
 
 cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const TcScreen& sc, cudaStream_t st) {
