@@ -653,11 +653,14 @@ def run_apml(args, ws, rank, local):
     if rank != 0:
         return 0
     pk, pk_kind = peaks()
-    # algorithmic bytes per stored entry: the first passes read the indices and
-    # write C, P (8 + 8 B) and re-read them (16 B); each normalisation reads P and
-    # the column index twice and writes P twice (24 B); the loss and the support
-    # gradient read P, C and the indices once more (16 B)
-    bytes_entry = 32 + 24 * K + 16
+    # algorithmic bytes per stored entry of the factored passes: validation and
+    # cost read both indices and write C (12 B); the row softmax statistics read
+    # C and the column (8 B); the symmetrisation reads them again and writes S
+    # (12 B); each further normalisation reads S and the column (8 B); the last
+    # pass reads S, the column and C and writes P (16 B; 12 B without
+    # normalisations, P being S).  The support gradient is fused into the last
+    # pass for d <= 3; otherwise its own pass reads both indices and P (12 B).
+    bytes_entry = 12 + 8 + 12 + (8 * (K - 1) + 16 if K > 0 else 12) + (0 if d <= 3 else 12)
     achieved = bytes_entry * nnz * args.steps / t_max / 1e9
     peak = float(pk.get("hbm_gbs", 6800.0))
     line = {

@@ -271,8 +271,11 @@ int sot_plan_coo_operands(const float* X, const float* Y, const float* a, const 
  *   loss[B]    <- sum P_ij C_ij (may be NULL);
  *   grad[B][n][d] <- 2 sum_j P_ij (x_i - y_j) on the support, P held fixed (may be NULL).
  * T > 0 is the temperature (the page's adaptive temperature is not given; a
- * caller passes one, e.g. eps).  Synchronises the stream (offsets are checked on
- * the host; an unsorted or out-of-range support returns SOT_ERR_INVALID_ARG).
+ * caller passes one, e.g. eps).  The offsets and the support are checked on the
+ * device before any entry is read through them: offsets that do not run
+ * non-decreasing from 0 to nnz, unsorted rows or an out-of-range index return
+ * SOT_ERR_INVALID_ARG.  Synchronises the stream once, at the end, to read that
+ * check (twice with a gradient at d > 3).  nnz < 2^31.
  */
 int sot_apml_coo(const float* X, const float* Y, const float* a, const float* b,
                  int B, int n, int m, int d, const int* rows, const int* cols,

@@ -1336,43 +1336,66 @@ int sot_apml_coo(const float* X, const float* Y, const float* a, const float* b,
     if (!batch_offsets || (nnz > 0 && (!rows || !cols || !vals)))
         return fail(SOT_ERR_INVALID_ARG, "batch_offsets, rows, cols and vals must not be NULL");
     cudaStream_t cs = (cudaStream_t)stream;
-    // the offsets bound every index the kernels take: check them on the host first
-    std::vector<long long> off((size_t)B + 1);
-    SOT_CUDA(cudaMemcpyAsync(off.data(), batch_offsets, sizeof(long long) * off.size(), cudaMemcpyDeviceToHost, cs));
-    SOT_CUDA(cudaStreamSynchronize(cs));
-    if (off[0] != 0 || off[B] != nnz) return fail(SOT_ERR_INVALID_ARG, "batch_offsets must run from 0 to nnz");
-    for (int k = 0; k < B; ++k)
-        if (off[k + 1] < off[k]) return fail(SOT_ERR_INVALID_ARG, "batch_offsets must be non-decreasing");
-    Scratch S(cs);
     ApmlArgs p;
     p.B = B; p.n = n; p.m = m; p.d = d;
     p.X = X; p.Y = Y; p.a = a; p.b = b;
-    p.rows = rows; p.cols = cols; p.off = batch_offsets;
+    p.rows = rows; p.cols = cols; p.off = batch_offsets; p.nnz = nnz;
     p.inv_T = 1.f / T;
     p.iters = iters;
     p.vals = vals;
     p.loss = loss;
-    p.cost = S.alloc<float>((size_t)nnz);
-    p.rstart = S.alloc<int>((size_t)B * n);
-    p.rend = S.alloc<int>((size_t)B * n);
-    p.cmax = S.alloc<unsigned>((size_t)B * m);
-    p.csum = S.alloc<double>((size_t)B * m);
-    p.cfac = S.alloc<float>((size_t)B * m);
-    p.loss_part = S.alloc<float>((size_t)B * n);
-    p.status = S.alloc<int>(1);
-    if (!p.cost || !p.rstart || !p.rend || !p.cmax || !p.csum || !p.cfac || !p.loss_part || !p.status)
-        return fail(SOT_ERR_NOMEM, "scratch allocation failed");
-    SOT_CUDA(cudaMemsetAsync(p.rstart, 0, sizeof(int) * (size_t)B * n, cs));
-    SOT_CUDA(cudaMemsetAsync(p.rend, 0, sizeof(int) * (size_t)B * n, cs));
-    SOT_CUDA(cudaMemsetAsync(p.cmax, 0, sizeof(unsigned) * (size_t)B * m, cs));
+    p.grad = d <= 3 ? grad : nullptr;  // fused into the last pass
+    const size_t nparts = apml_plan(B, n, m, device_sms(), &p.cpc, &p.rpc);
+    const size_t bn = (size_t)B * n, bm = (size_t)B * m;
+    // one scratch block, carved in 256-byte aligned pieces
+    size_t total = 0;
+    auto piece = [&](size_t bytes) {
+        const size_t o = total;
+        total += (std::max<size_t>(bytes, 1) + 255) & ~(size_t)255;
+        return o;
+    };
+    const size_t o_cost = piece(sizeof(float) * (size_t)nnz), o_rs = piece(sizeof(int) * bn),
+                 o_re = piece(sizeof(int) * bn), o_rstat = piece(sizeof(float2) * bn), o_uf = piece(sizeof(float) * bn),
+                 o_cm = piece(sizeof(float) * bm), o_cf = piece(sizeof(float) * bm), o_vf = piece(sizeof(float) * bm),
+                 o_part = piece(sizeof(float) * nparts), o_cmax = piece(nparts ? 0 : sizeof(unsigned) * bm),
+                 o_csum = piece(nparts ? 0 : sizeof(double) * bm), o_lp = piece(sizeof(float) * bn),
+                 o_st = piece(sizeof(int));
+    Scratch S(cs);
+    unsigned char* blk = S.alloc<unsigned char>(total);
+    if (!blk) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    p.cost = reinterpret_cast<float*>(blk + o_cost);
+    p.rstart = reinterpret_cast<int*>(blk + o_rs);
+    p.rend = reinterpret_cast<int*>(blk + o_re);
+    p.rstat = reinterpret_cast<float2*>(blk + o_rstat);
+    p.ufac = reinterpret_cast<float*>(blk + o_uf);
+    p.cm = reinterpret_cast<float*>(blk + o_cm);
+    p.cfac = reinterpret_cast<float*>(blk + o_cf);
+    p.vfac = reinterpret_cast<float*>(blk + o_vf);
+    p.part = nparts ? reinterpret_cast<float*>(blk + o_part) : nullptr;
+    p.cmax = nparts ? nullptr : reinterpret_cast<unsigned*>(blk + o_cmax);
+    p.csum = nparts ? nullptr : reinterpret_cast<double*>(blk + o_csum);
+    p.loss_part = reinterpret_cast<float*>(blk + o_lp);
+    p.status = reinterpret_cast<int*>(blk + o_st);
+    // rstart and rend are adjacent pieces: one clear covers both
+    SOT_CUDA(cudaMemsetAsync(p.rstart, 0, o_rstat - o_rs, cs));
+    if (!nparts) SOT_CUDA(cudaMemsetAsync(blk + o_cmax, 0, o_lp - o_cmax, cs));
     SOT_CUDA(cudaMemsetAsync(p.status, 0, sizeof(int), cs));
+    // the offsets are checked on the device by the first pass, which bounds every
+    // index the later passes take
     cudaError_t e = launch_apml(p, cs);
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "APML launch failed: %s", cudaGetErrorString(e));
-    if (grad) SOT_CUDA(launch_grad_coo(X, Y, B, n, m, d, rows, cols, vals, batch_offsets, grad, p.status, cs));
+    const char* bad = "batch_offsets not non-decreasing from 0 to nnz, COO not row-sorted within a cloud, or index "
+                      "out of range";
     int h = 0;
     SOT_CUDA(cudaMemcpyAsync(&h, p.status, sizeof(int), cudaMemcpyDeviceToHost, cs));
     SOT_CUDA(cudaStreamSynchronize(cs));
-    if (h & SOT_DEV_BAD_COO) return fail(SOT_ERR_INVALID_ARG, "COO not row-sorted within a cloud or index out of range");
+    if (h & SOT_DEV_BAD_COO) return fail(SOT_ERR_INVALID_ARG, "%s", bad);
+    if (grad && !p.grad) {  // d > 3: the gradient's own pass, on offsets now known to be valid
+        SOT_CUDA(launch_grad_coo(X, Y, B, n, m, d, rows, cols, vals, batch_offsets, grad, p.status, cs));
+        SOT_CUDA(cudaMemcpyAsync(&h, p.status, sizeof(int), cudaMemcpyDeviceToHost, cs));
+        SOT_CUDA(cudaStreamSynchronize(cs));
+        if (h & SOT_DEV_BAD_COO) return fail(SOT_ERR_INVALID_ARG, "%s", bad);
+    }
     return SOT_OK;
 }
 

@@ -73,6 +73,22 @@ def test_apml_every_pair_stored(sot, orc):
     check(sot, orc, X, Y, a, b, 0.05, 40, 0.0, 0.05, 10)
 
 
+def test_apml_many_columns(sot, orc):
+    """More columns (m = 17000) than the row passes stage in shared memory
+    (16384): the column maxima and sums go through global atomics instead;
+    weighted, d = 3 (the support gradient fused into the last pass)."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=193, m=17000, d=3)
+    check(sot, orc, X, Y, a, b, 0.1, 40, 1e-4, 0.1, 4, weighted=True)
+
+
+def test_apml_gradient_unfused_d5(sot, orc):
+    """d = 5: the support gradient runs as its own pass after the last one."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=2, n=150, m=161, d=5)
+    check(sot, orc, X, Y, a, b, 0.2, 40, 1e-5, 0.2, 3, weighted=True)
+
+
 def test_apml_rejects_invalid_support(sot):
     """An out-of-range column and unsorted rows are reported; every pass skips
     the bad indices, so nothing outside the arrays is touched first."""
@@ -91,6 +107,19 @@ def test_apml_rejects_invalid_support(sot):
     bad["rows"] = coo["rows"].flip(0).contiguous()  # rows descending
     with pytest.raises(sot.SotError) as ei:
         sot.sot_apml_coo(Xd, Yd, None, None, bad, 0.05, 3)
+    assert ei.value.status == sot.SOT_ERR_INVALID_ARG
+    # offsets that do not run from 0 to nnz, or decrease, are found on the device
+    for off in ([0, nnz - 1], [0, nnz + 7]):
+        bad = dict(coo)
+        bad["batch_offsets"] = dev(np.array(off, dtype=np.int64))
+        with pytest.raises(sot.SotError) as ei:
+            sot.sot_apml_coo(Xd, Yd, None, None, bad, 0.05, 3)
+        assert ei.value.status == sot.SOT_ERR_INVALID_ARG
+    X3, Y3 = np.concatenate([X, X, X]), np.concatenate([Y, Y, Y])
+    bad = {"rows": torch.cat([coo["rows"], coo["rows"]]), "cols": torch.cat([coo["cols"], coo["cols"]]),
+           "batch_offsets": dev(np.array([0, nnz, nnz - 5, 2 * nnz], dtype=np.int64)), "nnz": 2 * nnz}
+    with pytest.raises(sot.SotError) as ei:
+        sot.sot_apml_coo(dev(X3), dev(Y3), None, None, bad, 0.05, 3)
     assert ei.value.status == sot.SOT_ERR_INVALID_ARG
     # the valid support still runs afterwards
     vals, loss, _ = sot.sot_apml_coo(Xd, Yd, None, None, coo, 0.05, 3, grad=False)
