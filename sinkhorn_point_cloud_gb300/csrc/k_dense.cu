@@ -1,4 +1,4 @@
-// k_dense.cu -- fp32 FMA Sinkhorn kernels for any dimension d <= 256.
+// k_dense.cu -- fp32 FMA Sinkhorn kernels for any dimension d <= 1024.
 //
 // This is the full-precision path for d > 3 (SOT_PREC_FP32, and dimensions
 // the tensor-core path does not take).  Same fused half-step as the point
@@ -6,39 +6,41 @@
 // shared memory while 64-column tiles stream past; each thread forms a 4 x 4
 // micro-tile of dot products in registers, turns it into scores, and the row
 // log-sum-exp is reduced across the 16 threads that share a row with
-// shuffles.  Nothing of size n x m is written.
+// shuffles.  Nothing of size n x m is written.  Above d = 256 ("FlashSinkhorn",
+// Experimentele Resultaten: d up to 1024) the coordinates stream in slices of
+// 256: the row block's slice is staged again with each column tile's, and the
+// dot products carry on across the slices in the same k-ascending order.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace sot {
 
 constexpr int DN_T = 256;
-constexpr int DN_RT = 64;   // rows per CTA
-constexpr int DN_CT = 64;   // columns per tile
-constexpr int DN_MAXD = 256;
+constexpr int DN_RT = 64;    // rows per CTA
+constexpr int DN_CT = 64;    // columns per tile
+constexpr int DN_DK = 256;   // coordinates per shared-memory slice
+constexpr int DN_MAXD = 1024;
 
 int dense_rows_per_cta() { return DN_RT; }
 int dense_cols_per_tile() { return DN_CT; }
 int dense_max_d() { return DN_MAXD; }
 
-// Shared-memory layout: Xs[DN_RT][d+1], Ys[DN_CT][d+1] (padded rows keep the
-// strided accesses conflict-free), cs[DN_CT] column bias.
+__host__ __device__ inline int dense_dk(int d) { return d < DN_DK ? d : DN_DK; }
+
+// Shared-memory layout: Xs[DN_RT][dk+1], Ys[DN_CT][dk+1] with dk = min(d, 256)
+// (padded rows keep the strided accesses conflict-free), cs[DN_CT] column bias.
 __host__ __device__ inline size_t dense_smem_bytes(int d) {
-    return sizeof(float) * ((size_t)(DN_RT + DN_CT) * (d + 1) + DN_CT + DN_T / 32 + 8);
+    return sizeof(float) * ((size_t)(DN_RT + DN_CT) * (dense_dk(d) + 1) + DN_CT + DN_T / 32 + 8);
 }
 
-// acc[rr][cc] = sum_k x[4tr+rr][k] * y[tc+16cc][k], k ascending, fp32 FMA.
-__device__ __forceinline__ void dense_dot_tile(const float* Xs, const float* Ys, int d, int tr, int tc,
+// acc[rr][cc] += sum_k x[4tr+rr][k] * y[tc+16cc][k] over the kw coordinates of
+// a staged slice (row stride ld), k ascending, fp32 FMA.
+__device__ __forceinline__ void dense_dot_tile(const float* Xs, const float* Ys, int kw, int ld, int tr, int tc,
                                                float acc[4][4]) {
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) acc[rr][cc] = 0.f;
-    const int ld = d + 1;
     const float* xr = Xs + (4 * tr) * ld;
     const float* yc = Ys + tc * ld;
 #pragma unroll 4
-    for (int k = 0; k < d; ++k) {
+    for (int k = 0; k < kw; ++k) {
         float xv[4], yv[4];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) xv[rr] = xr[rr * ld + k];
@@ -49,6 +51,13 @@ __device__ __forceinline__ void dense_dot_tile(const float* Xs, const float* Ys,
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) acc[rr][cc] = fmaf(xv[rr], yv[cc], acc[rr][cc]);
     }
+}
+
+__device__ __forceinline__ void zero_tile(float acc[4][4]) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) acc[rr][cc] = 0.f;
 }
 
 __device__ __forceinline__ float sum16(float v) {
@@ -62,14 +71,37 @@ __device__ __forceinline__ float max16(float v) {
     return v;
 }
 
-// Copy `cnt` rows (row-major [*][d]) starting at `row0` into S[DN][d+1],
-// zero-filling rows past `lim`.
-__device__ __forceinline__ void dense_stage(float* S, const float* src, int row0, int cnt, int lim, int d) {
-    const int ld = d + 1;
-    for (int e = threadIdx.x; e < cnt * d; e += DN_T) {
-        const int r = e / d, k = e - r * d;
+// Copy coordinates [k0, k0 + kw) of `cnt` rows (row-major [*][d]) starting at
+// `row0` into S[DN][kw+1], zero-filling rows past `lim`.
+__device__ __forceinline__ void dense_stage(float* S, const float* src, int row0, int cnt, int lim, int d, int k0,
+                                            int kw) {
+    const int ld = kw + 1;
+    for (int e = threadIdx.x; e < cnt * kw; e += DN_T) {
+        const int r = e / kw, k = e - r * kw;
         const int gr = row0 + r;
-        S[r * ld + k] = (gr < lim) ? src[(size_t)gr * d + k] : 0.f;
+        S[r * ld + k] = (gr < lim) ? src[(size_t)gr * d + k0 + k] : 0.f;
+    }
+}
+
+// acc = the row block's dot products with column tile [base, base + DN_CT):
+// for d <= 256 the row block is staged once by the caller (Xs) and only the
+// column tile is staged here; above, both are staged slice by slice.
+// `cols_bias` runs with the first slice's staging, before its barrier.  On
+// return the last slice is still staged.
+template <class Bias>
+__device__ __forceinline__ void dense_tile_dots(float* Xs, float* Ys, const float* rows, const float* cols, int row0,
+                                                int nr, int base, int c_end, int d, int tr, int tc, float acc[4][4],
+                                                Bias&& cols_bias) {
+    const int dk = dense_dk(d);
+    zero_tile(acc);
+    for (int k0 = 0; k0 < d; k0 += dk) {
+        const int kw = min(dk, d - k0);
+        __syncthreads();  // the previous slice (or tile) is no longer read
+        if (d > dk) dense_stage(Xs, rows, row0, DN_RT, nr, d, k0, kw);
+        dense_stage(Ys, cols, base, DN_CT, c_end, d, k0, kw);
+        if (k0 == 0) cols_bias();
+        __syncthreads();
+        dense_dot_tile(Xs, Ys, kw, kw + 1, tr, tc, acc);
     }
 }
 
@@ -84,7 +116,7 @@ template <int MODE>
 __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     extern __shared__ float smem[];
-    const int d = p.d, ld = d + 1;
+    const int d = p.d, ld = dense_dk(d) + 1;
     float* Xs = smem;
     float* Ys = Xs + DN_RT * ld;
     float* cs = Ys + DN_CT * ld;
@@ -104,7 +136,7 @@ __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
 
     if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
         for (int k = threadIdx.x; k < p.B; k += DN_T) p.lo_reset[k] = SOT_ORD_EMPTY;
-    dense_stage(Xs, rows, row0, DN_RT, p.nr, d);
+    if (d <= DN_DK) dense_stage(Xs, rows, row0, DN_RT, p.nr, d, 0, d);
     float m[4], s[4], old[4];
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -118,15 +150,13 @@ __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
     const float tk = p.two_kappa;
 
     for (int base = c_begin; base < c_end; base += DN_CT) {
-        __syncthreads();
-        dense_stage(Ys, cols, base, DN_CT, c_end, d);
-        for (int c = threadIdx.x; c < DN_CT; c += DN_T) {
-            const int j = base + c;
-            cs[c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
-        }
-        __syncthreads();
         float acc[4][4];
-        dense_dot_tile(Xs, Ys, d, tr, tc, acc);
+        dense_tile_dots(Xs, Ys, rows, cols, row0, p.nr, base, c_end, d, tr, tc, acc, [&] {
+            for (int c = threadIdx.x; c < DN_CT; c += DN_T) {
+                const int j = base + c;
+                cs[c] = (j < c_end) ? cw[j] - cst[j] : -INFINITY;
+            }
+        });
         float cb[4];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) cb[cc] = cs[tc + 16 * cc];
@@ -301,7 +331,7 @@ cudaError_t launch_dense_half(const HalfArgs& p, int mode, cudaStream_t st) {
 template <int KV>
 __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
     extern __shared__ float smem[];
-    const int d = p.d, ld = d + 1;
+    const int d = p.d, dk = dense_dk(d), ld = dk + 1;
     float* Xs = smem;
     float* Ys = Xs + DN_RT * ld;
     float* cs = Ys + DN_CT * ld;
@@ -310,13 +340,15 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
     float* nys = Ps + DN_RT * (DN_CT + 1);
     const int b = blockIdx.y;
     const int row0 = blockIdx.x * DN_RT;
+    // coordinates [kb0, kb0 + kwz) of the gradient (blockIdx.z: one slice of 256 each above d = 256)
+    const int kb0 = blockIdx.z * dk, kwz = min(dk, d - kb0);
     const float* rows = p.xpack + (size_t)b * p.n * d;
     const float* cols = p.ypack + (size_t)b * p.m * d;
     const size_t xb = (size_t)b * p.n, yb = (size_t)b * p.m;
     const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
     const float tk = 2.f * p.kappa;
 
-    dense_stage(Xs, rows, row0, DN_RT, p.n, d);
+    if (d <= DN_DK) dense_stage(Xs, rows, row0, DN_RT, p.n, d, 0, d);
     float Lr[4], nxr[4], m[4], r_[4], q_[4], v[4][KV];
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
@@ -330,16 +362,14 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
         for (int kk = 0; kk < KV; ++kk) v[rr][kk] = 0.f;
     }
     for (int base = 0; base < p.m; base += DN_CT) {
-        __syncthreads();
-        dense_stage(Ys, cols, base, DN_CT, p.m, d);
-        for (int c = threadIdx.x; c < DN_CT; c += DN_T) {
-            const int j = base + c;
-            cs[c] = (j < p.m) ? p.lw2y[yb + j] - p.Lam[yb + j] : -INFINITY;
-            nys[c] = (j < p.m) ? p.ny[yb + j] : 0.f;
-        }
-        __syncthreads();
         float acc[4][4];
-        dense_dot_tile(Xs, Ys, d, tr, tc, acc);
+        dense_tile_dots(Xs, Ys, rows, cols, row0, p.n, base, p.m, d, tr, tc, acc, [&] {
+            for (int c = threadIdx.x; c < DN_CT; c += DN_T) {
+                const int j = base + c;
+                cs[c] = (j < p.m) ? p.lw2y[yb + j] - p.Lam[yb + j] : -INFINITY;
+                nys[c] = (j < p.m) ? p.ny[yb + j] : 0.f;
+            }
+        });
         float cb[4], nyc[4];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) { cb[cc] = cs[tc + 16 * cc]; nyc[cc] = nys[tc + 16 * cc]; }
@@ -381,7 +411,13 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
             q_[rr] = q_[rr] * sc[rr] + sum16(tq);
         }
         __syncthreads();
-        // v[rows][k] += sum_c P[rows][c] * Y[c][k], thread owns k = tc + 16 kk
+        // the tile's coordinates of this block's slice, if another slice is staged
+        if (kb0 + dk < d) {
+            dense_stage(Ys, cols, base, DN_CT, p.m, d, kb0, kwz);
+            __syncthreads();
+        }
+        const int ldv = (d <= dk) ? ld : kwz + 1;
+        // v[rows][k] += sum_c P[rows][c] * Y[c][kb0 + k], thread owns k = tc + 16 kk
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
@@ -393,7 +429,7 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
 #pragma unroll
             for (int kk = 0; kk < KV; ++kk) {
                 const int k = tc + 16 * kk;
-                const float yv = (k < d) ? Ys[c * ld + k] : 0.f;
+                const float yv = (k < kwz) ? Ys[c * ldv + k] : 0.f;
 #pragma unroll
                 for (int rr = 0; rr < 4; ++rr) v[rr][kk] = fmaf(pv[rr], yv, v[rr][kk]);
             }
@@ -407,22 +443,22 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
         const float ai = p.a ? p.a[xb + row] : 1.f / (float)p.n;
         const float fac = ai * ex2f(m[rr]);
         const float ri = r_[rr] * fac;
-        if (tc == 0) {
+        if (tc == 0 && blockIdx.z == 0) {
             qsum += q_[rr] * fac;
             if (p.rowsum) p.rowsum[xb + row] = ri;
         }
         if (p.grad) {
-            const float* sh = p.shift + (size_t)b * d;
-            const float* xo = p.X + (xb + row) * d;
-            float* gr = p.grad + (xb + row) * d;
+            const float* sh = p.shift + (size_t)b * d + kb0;
+            const float* xo = p.X + (xb + row) * d + kb0;
+            float* gr = p.grad + (xb + row) * d + kb0;
 #pragma unroll
             for (int kk = 0; kk < KV; ++kk) {
                 const int k = tc + 16 * kk;
-                if (k < d) gr[k] = 2.f * (ai * xo[k] - fmaf(ri, sh[k], v[rr][kk] * fac));
+                if (k < kwz) gr[k] = 2.f * (ai * xo[k] - fmaf(ri, sh[k], v[rr][kk] * fac));
             }
         }
     }
-    if (p.cost_part) {
+    if (p.cost_part && blockIdx.z == 0) {
         qsum = block_sum<DN_T>(qsum, red);
         if (threadIdx.x == 0) p.cost_part[b * p.rowtiles + blockIdx.x] = qsum;
     }
@@ -433,8 +469,9 @@ int dense_apply_rows_per_cta() { return DN_RT; }
 cudaError_t launch_dense_apply(const ApplyArgs& p, cudaStream_t st) {
     if (p.d < 1 || p.d > DN_MAXD) return cudaErrorInvalidValue;
     const size_t sm = dense_smem_bytes(p.d) + sizeof(float) * ((size_t)DN_RT * (DN_CT + 1) + DN_CT + 8);
-    dim3 grid(p.rowtiles, p.B), block(DN_T);
-    const int kv = (p.d + 15) / 16;
+    // above d = 256, one CTA per row block and 256-coordinate slice of the gradient
+    dim3 grid(p.rowtiles, p.B, (p.d + DN_DK - 1) / DN_DK), block(DN_T);
+    const int kv = (dense_dk(p.d) + 15) / 16;
 #define SOT_AP_CASE(KVV)                                                                                   \
     {                                                                                                      \
         cudaError_t e = cudaFuncSetAttribute(dense_apply_kernel<KVV>,                                      \

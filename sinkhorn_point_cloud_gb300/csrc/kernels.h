@@ -114,7 +114,7 @@ bool point_cluster_plan(int B, int n, int m, int sms, int* C, int* T, int* S, si
 cudaError_t launch_point_cluster(int B, int n, int m, const float* xpack, const float* ypack, float* L, float* Lam,
                                  float two_kappa, int iters, int C, int T, int S, size_t smem, cudaStream_t st);
 
-// ---- dense fp32 path (any d <= 256), k_dense.cu ----
+// ---- dense fp32 path (any d <= 1024), k_dense.cu ----
 int dense_rows_per_cta();
 int dense_cols_per_tile();
 int dense_max_d();

@@ -58,8 +58,10 @@ def test_unsupported_precision_rejected(lib):
     s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, binding.SOT_PREC_F16X3)
     # d = 3 has no tensor-core path
     assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 3, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
-    s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, 0)
+    # d = 300 has no tensor-core path either; d = 1025 has no path at all
     assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 300, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
+    s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, 0)
+    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 1025, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
 
 
 def test_coo_argument_checks(lib):
@@ -165,8 +167,8 @@ def test_python_binding_checks_caller_tensors():
 def test_path_selection(lib):
     """The kernel family each dimension and precision flag takes (host logic,
     no GPU needed): d <= 3 the point kernels; d = 64, 128, 192, 256 the tensor
-    cores under automatic precision; other d up to 256 the fp32 kernels; the
-    fp16 split takes those four d only and nothing goes past d = 256."""
+    cores under automatic precision; other d up to 1024 the fp32 kernels; the
+    fp16 split takes those four d only and nothing goes past d = 1024."""
     point, dense, tensor = 0, 1, 2
     for d in (1, 2, 3):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == point
@@ -178,8 +180,11 @@ def test_path_selection(lib):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == tensor, d
         assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == tensor, d
         assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
-    assert lib.sot_select_path(257, binding.SOT_PREC_AUTO) == binding.SOT_ERR_UNSUPPORTED
-    assert lib.sot_select_path(320, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED
+    for d in (257, 320, 512, 1000, 1024):
+        assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == dense, d
+        assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
+        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED, d
+    assert lib.sot_select_path(1025, binding.SOT_PREC_AUTO) == binding.SOT_ERR_UNSUPPORTED
 
 
 def test_hvp_arguments_rejected_on_host(lib):

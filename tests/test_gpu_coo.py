@@ -108,10 +108,11 @@ def test_coo_gate_a_bit_exact(sot, prob, dirs):
     gate_a(sot, Xd, Yd, None, None, f, g, eps, 1e-8, dirs)
 
 
-@pytest.mark.parametrize("d,tau", [(2, 1e-8), (8, 1e-8), (8, 1e-3), (64, 1e-8)])
+@pytest.mark.parametrize("d,tau", [(2, 1e-8), (8, 1e-8), (8, 1e-3), (64, 1e-8), (512, 1e-8)])
 def test_coo_gate_a_other_layouts(sot, d, tau):
-    """Weighted clouds in d = 2 (point layout) and d = 8, 64 (the dense
-    layout's expanded-form scores); potentials from a GPU solve."""
+    """Weighted clouds in d = 2 (point layout) and d = 8, 64, 512 (the dense
+    layout's expanded-form scores; at 512 the maxima pass streams the
+    coordinates in slices); potentials from a GPU solve."""
     rng = np.random.default_rng(100 + d)
     B, n, m = 2, 700, 650
     X = rng.normal(size=(B, n, d)).astype(np.float32)
