@@ -27,25 +27,26 @@ int dense_max_d() { return DN_MAXD; }
 
 __host__ __device__ inline int dense_dk(int d) { return d < DN_DK ? d : DN_DK; }
 
-// Shared-memory layout: Xs[DN_RT][dk+1], Ys[DN_CT][dk+1] with dk = min(d, 256)
-// (padded rows keep the strided accesses conflict-free), cs[DN_CT] column bias.
+// Shared memory holds the staged slices k-major: coordinate k of row r at
+// k * DN_LDT + r, so that a thread's four rows (and four columns) at one k are
+// one 16-byte read.  Xs[dk][DN_LDT], Ys[dk][DN_LDT] with dk = min(d, 256), then
+// cs[DN_CT] column bias.
+constexpr int DN_LDT = DN_RT + 4;
+static_assert(DN_RT == DN_CT && DN_LDT % 4 == 0, "k-major tiles");
 __host__ __device__ inline size_t dense_smem_bytes(int d) {
-    return sizeof(float) * ((size_t)(DN_RT + DN_CT) * (dense_dk(d) + 1) + DN_CT + DN_T / 32 + 8);
+    return sizeof(float) * ((size_t)2 * dense_dk(d) * DN_LDT + DN_CT + DN_T / 32 + 8);
 }
 
-// acc[rr][cc] += sum_k x[4tr+rr][k] * y[tc+16cc][k] over the kw coordinates of
-// a staged slice (row stride ld), k ascending, fp32 FMA.
-__device__ __forceinline__ void dense_dot_tile(const float* Xs, const float* Ys, int kw, int ld, int tr, int tc,
+// acc[rr][cc] += sum_k x[4tr+rr][k] * y[4tc+cc][k] over the kw coordinates of
+// a staged slice, k ascending, fp32 FMA.
+__device__ __forceinline__ void dense_dot_tile(const float* Xs, const float* Ys, int kw, int tr, int tc,
                                                float acc[4][4]) {
-    const float* xr = Xs + (4 * tr) * ld;
-    const float* yc = Ys + tc * ld;
+    const float4* xp = reinterpret_cast<const float4*>(Xs) + tr;
+    const float4* yp = reinterpret_cast<const float4*>(Ys) + tc;
 #pragma unroll 4
     for (int k = 0; k < kw; ++k) {
-        float xv[4], yv[4];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) xv[rr] = xr[rr * ld + k];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) yv[cc] = yc[(16 * cc) * ld + k];
+        const float4 x4 = xp[k * (DN_LDT / 4)], y4 = yp[k * (DN_LDT / 4)];
+        const float xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
@@ -72,14 +73,13 @@ __device__ __forceinline__ float max16(float v) {
 }
 
 // Copy coordinates [k0, k0 + kw) of `cnt` rows (row-major [*][d]) starting at
-// `row0` into S[DN][kw+1], zero-filling rows past `lim`.
+// `row0` into the k-major S[kw][DN_LDT], zero-filling rows past `lim`.
 __device__ __forceinline__ void dense_stage(float* S, const float* src, int row0, int cnt, int lim, int d, int k0,
                                             int kw) {
-    const int ld = kw + 1;
     for (int e = threadIdx.x; e < cnt * kw; e += DN_T) {
         const int r = e / kw, k = e - r * kw;
         const int gr = row0 + r;
-        S[r * ld + k] = (gr < lim) ? src[(size_t)gr * d + k0 + k] : 0.f;
+        S[k * DN_LDT + r] = (gr < lim) ? src[(size_t)gr * d + k0 + k] : 0.f;
     }
 }
 
@@ -101,7 +101,7 @@ __device__ __forceinline__ void dense_tile_dots(float* Xs, float* Ys, const floa
         dense_stage(Ys, cols, base, DN_CT, c_end, d, k0, kw);
         if (k0 == 0) cols_bias();
         __syncthreads();
-        dense_dot_tile(Xs, Ys, kw, kw + 1, tr, tc, acc);
+        dense_dot_tile(Xs, Ys, kw, tr, tc, acc);
     }
 }
 
@@ -116,10 +116,10 @@ template <int MODE>
 __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     extern __shared__ float smem[];
-    const int d = p.d, ld = dense_dk(d) + 1;
+    const int d = p.d, dk = dense_dk(d);
     float* Xs = smem;
-    float* Ys = Xs + DN_RT * ld;
-    float* cs = Ys + DN_CT * ld;
+    float* Ys = Xs + dk * DN_LDT;
+    float* cs = Ys + dk * DN_LDT;
     float* red = cs + DN_CT;
     int* flags = reinterpret_cast<int*>(red + DN_T / 32);  // [0] last, [1] nretry
 
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(DN_T) dense_half_kernel(HalfArgs p) {
         });
         float cb[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) cb[cc] = cs[tc + 16 * cc];
+        for (int cc = 0; cc < 4; ++cc) cb[cc] = cs[4 * tc + cc];
         if (MODE == MODE_MAX) {
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
@@ -331,10 +331,10 @@ cudaError_t launch_dense_half(const HalfArgs& p, int mode, cudaStream_t st) {
 template <int KV>
 __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
     extern __shared__ float smem[];
-    const int d = p.d, dk = dense_dk(d), ld = dk + 1;
+    const int d = p.d, dk = dense_dk(d);
     float* Xs = smem;
-    float* Ys = Xs + DN_RT * ld;
-    float* cs = Ys + DN_CT * ld;
+    float* Ys = Xs + dk * DN_LDT;
+    float* cs = Ys + dk * DN_LDT;
     float* red = cs + DN_CT;
     float* Ps = red + DN_T / 32 + 8;  // [DN_RT][DN_CT + 1]
     float* nys = Ps + DN_RT * (DN_CT + 1);
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
         });
         float cb[4], nyc[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) { cb[cc] = cs[tc + 16 * cc]; nyc[cc] = nys[tc + 16 * cc]; }
+        for (int cc = 0; cc < 4; ++cc) { cb[cc] = cs[4 * tc + cc]; nyc[cc] = nys[4 * tc + cc]; }
         float sc[4];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
                 const float C = nxr[rr] + nyc[cc] - 2.f * acc[rr][cc];
                 tq = fmaf(w[cc], C, tq);
                 trs += w[cc];
-                Ps[(4 * tr + rr) * (DN_CT + 1) + tc + 16 * cc] = w[cc];
+                Ps[(4 * tr + rr) * (DN_CT + 1) + 4 * tc + cc] = w[cc];
             }
             r_[rr] = r_[rr] * sc[rr] + sum16(trs);
             q_[rr] = q_[rr] * sc[rr] + sum16(tq);
@@ -416,7 +416,6 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
             dense_stage(Ys, cols, base, DN_CT, p.m, d, kb0, kwz);
             __syncthreads();
         }
-        const int ldv = (d <= dk) ? ld : kwz + 1;
         // v[rows][k] += sum_c P[rows][c] * Y[c][kb0 + k], thread owns k = tc + 16 kk
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
@@ -429,7 +428,7 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
 #pragma unroll
             for (int kk = 0; kk < KV; ++kk) {
                 const int k = tc + 16 * kk;
-                const float yv = (k < kwz) ? Ys[c * ldv + k] : 0.f;
+                const float yv = (k < kwz) ? Ys[k * DN_LDT + c] : 0.f;
 #pragma unroll
                 for (int rr = 0; rr < 4; ++rr) v[rr][kk] = fmaf(pv[rr], yv, v[rr][kk]);
             }
