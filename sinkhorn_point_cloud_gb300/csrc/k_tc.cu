@@ -987,24 +987,6 @@ struct TcScreenK {
 // Per-chunk maxima of one row over NQ x 32 columns of a tile, from the
 // accumulators (raw bits; accumulator units, biases included): one
 // three-input max chain per 32-column chunk.
-template <int NQ>
-__device__ __forceinline__ void tc_chunk_max(const uint32_t (&r)[NQ][32], float (&mq)[NQ]) {
-    // two interleaved chains per chunk keep the max latency hidden
-    float m[2 * NQ];
-#pragma unroll
-    for (int c = 0; c < 2 * NQ; ++c) m[c] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            m[2 * q] = fmax3(m[2 * q], __uint_as_float(r[q][j]), __uint_as_float(r[q][j + 1]));
-            m[2 * q + 1] = fmax3(m[2 * q + 1], __uint_as_float(r[q][j + 2]), __uint_as_float(r[q][j + 3]));
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) mq[q] = fmaxf(m[2 * q], m[2 * q + 1]);
-}
-
 // Screen NQ x 32 columns of one row (accumulator bits in r, columns jt ..):
 // the per-chunk maxima raise the running maximum, and every pair of a chunk
 // that reaches the threshold goes to the CTA's pool.
@@ -1021,10 +1003,13 @@ struct ScRow {  // one row's screening state
     unsigned rl; // row within the row block
     bool erow;
 };
+// mq[q]: the maximum of chunk q, formed by the TMEM load itself.
 template <int NQ>
-__device__ __forceinline__ void sc_screen(const uint32_t (&r)[NQ][32], int jt, ScShared& c, ScRow& s) {
+__device__ __forceinline__ void sc_screen(const uint32_t (&r)[NQ][32], const uint32_t (&mqb)[NQ], int jt,
+                                          ScShared& c, ScRow& s) {
     float mq[NQ];
-    tc_chunk_max<NQ>(r, mq);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) mq[q] = __uint_as_float(mqb[q]);
     // thresholds in accumulator units (score = tk * acc, tk > 0)
     float mall = mq[0];
 #pragma unroll
@@ -1195,17 +1180,18 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
                     break;
                 }
                 tc_fence_after();
-                uint32_t r[SC_NQ][32];
+                // the loads reduce each lane's 32 columns to their maximum on the way
+                uint32_t r[SC_NQ][32], mq[SC_NQ];
 #pragma unroll
                 for (int q = 0; q < SC_NQ; ++q)
-                    tmem_ld32_issue(tq + (uint32_t)(rt * SC_N) + 32u * (uint32_t)q, r[q]);
+                    tmem_ld32_max_issue(tq + (uint32_t)(rt * SC_N) + 32u * (uint32_t)q, r[q], mq[q]);
 #pragma unroll
-                for (int q = 0; q < SC_NQ; ++q) tmem_wait_ld(r[q]);
+                for (int q = 0; q < SC_NQ; ++q) tmem_wait_ld_max(r[q], mq[q]);
                 // this warp's share of the accumulator is in registers: free it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(S.bar(BAR_ACCEMPTY(rt, 0)));
-                sc_screen<SC_NQ>(r, c_begin + lt * SC_N + SC_COLS * cg, c, s[rt]);
+                sc_screen<SC_NQ>(r, mq, c_begin + lt * SC_N + SC_COLS * cg, c, s[rt]);
             }
         }
         if (lane == 0) sk.pool_cnt[(cta0 + ch) * SC_SEGS + ew] = min(c.wcount, SC_SEG);
