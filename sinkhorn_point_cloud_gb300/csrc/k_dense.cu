@@ -347,6 +347,9 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
     const size_t xb = (size_t)b * p.n, yb = (size_t)b * p.m;
     const int tr = threadIdx.x >> 4, tc = threadIdx.x & 15;
     const float tk = 2.f * p.kappa;
+    const float kh = (float)p.kappa64;
+    const float2 kap = make_float2(kh, (float)(p.kappa64 - (double)kh));
+    const float sig_thr = -(30.f + log2f((float)p.m));
 
     if (d <= DN_DK) dense_stage(Xs, rows, row0, DN_RT, p.n, d, 0, d);
     float Lr[4], nxr[4], m[4], r_[4], q_[4], v[4][KV];
@@ -397,6 +400,22 @@ __global__ void __launch_bounds__(DN_T) dense_apply_kernel(ApplyArgs p) {
                     m[rr] = mn;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) w[cc] = ex2f(fmaf(tk, acc[rr][cc], cb[cc] - Lr[rr] - mn));
+                }
+            }
+            if (p.exact_sig) {
+                // A pair whose fp32 weight is within 2^-30 / m of a_i is re-evaluated
+                // exactly: its exponent, log2 b_j + kappa (f_i + g_j - C_ij), rounds in
+                // fp32 at the size of kappa |x||y|, which moves the gradient by ~1e-4 at
+                // wide d; the rest carry less than 2^-30 of the row between them.
+                const int row = row0 + 4 * tr + rr;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int j = base + 4 * tc + cc;
+                    if (row < p.n && j < p.m && fmaf(tk, acc[rr][cc], cb[cc] - Lr[rr]) > sig_thr) {
+                        const float e = exact_log2_plan(p.X + (xb + row) * d, p.Yorig + (yb + j) * d, d,
+                                                        p.fpot[xb + row], p.gpot[yb + j], 0.f, p.lw2y[yb + j], kap);
+                        w[cc] = ex2f(e - m[rr]);
+                    }
                 }
             }
             float tq = 0.f, trs = 0.f;

@@ -76,30 +76,38 @@ static_assert(TC_SMEM <= 227 * 1024, "shared memory budget");
 constexpr int SC_N = 256;                                   // columns per screened tile (MMA N)
 constexpr uint32_t SC_AT = TC_M * 32;                       // row-side constant block: 128 rows x 32 B (sw32)
 constexpr uint32_t SC_BT = SC_N * 32;                       // bias block of a tile: 256 rows x 32 B (sw32)
-constexpr uint32_t SC_STAGE = 2 * TILE_BYTES + SC_BT;       // hi of 256 columns (two 16 KB tiles), bias block
-constexpr int TC_MAXD = 256;  // the screened half-step streams d in slices of 64 (K = 64 per image tile)
+constexpr int TC_MAXD = 1024;  // the screened half-step streams d in slices of 64 (K = 64 per image tile)
 
-// Shared-memory layout of the screened half-step for NS slices of K = 64:
-// the hi parts of both row tiles for every slice (resident), the row-side
-// constant blocks, a ring of NST stages (one slice of one 256-column tile
-// each, plus its bias block), then the header.  Wider d leaves room for
-// fewer stages.
+// Shared-memory layout of the screened half-step for NS slices of K = 64.
+// Up to d = 256: the hi parts of both row tiles for every slice (resident),
+// the row-side constant blocks, a ring of NST stages (one slice of one
+// 256-column tile each, plus its bias block), then the header; wider d leaves
+// room for fewer stages.  At d = 512 and 1024 (NS = 8, 16) the row tiles no
+// longer fit: each stage also carries the slice of both row tiles, which are
+// streamed again with every column tile.
 template <int NS>
 struct ScLayout {
-    static constexpr int NST = NS == 1 ? 4 : (NS == 4 ? 2 : 3);
-    static constexpr uint32_t OFF_A = 0;                              // [2 row tiles][NS] hi, 16 KB each
-    static constexpr uint32_t OFF_AC = OFF_A + 2u * NS * TILE_BYTES;  // [2 row tiles] constant blocks
-    static constexpr uint32_t OFF_B = OFF_AC + 2 * SC_AT;             // [NST] stages
-    static constexpr uint32_t OFF_HDR = OFF_B + NST * SC_STAGE;       // header (as OFF_BAR.. of the full half-step)
+    static constexpr bool STREAM = NS > 4;
+    static constexpr uint32_t ST_B = STREAM ? 2 * TILE_BYTES : 0;  // a stage: [row tiles' slice], column tile's hi,
+    static constexpr uint32_t ST_BIAS = ST_B + 2 * TILE_BYTES;     // then its bias block
+    static constexpr uint32_t STAGE = ST_BIAS + SC_BT;
+    static constexpr int NST = STREAM ? 2 : (NS == 1 ? 4 : (NS == 4 ? 2 : 3));
+    static constexpr uint32_t OFF_A = 0;                                               // [2 row tiles][NS] hi
+    static constexpr uint32_t OFF_AC = OFF_A + (STREAM ? 0u : 2u * NS * TILE_BYTES);  // [2 row tiles] constants
+    static constexpr uint32_t OFF_B = OFF_AC + 2 * SC_AT;                              // [NST] stages
+    static constexpr uint32_t OFF_HDR = OFF_B + NST * STAGE;  // header (as OFF_BAR.. of the full half-step)
     static constexpr uint32_t SMEM = OFF_HDR + (OFF_RETRY - OFF_BAR) + TC_ROWS * 4 + 1024;
 };
-static_assert(ScLayout<1>::OFF_B % 1024 == 0 && SC_STAGE % 1024 == 0, "screened stage alignment");
+static_assert(ScLayout<1>::OFF_B % 1024 == 0 && ScLayout<8>::OFF_B % 1024 == 0 && ScLayout<1>::STAGE % 1024 == 0 &&
+                  ScLayout<8>::STAGE % 1024 == 0,
+              "screened stage alignment");
 static_assert(ScLayout<1>::SMEM <= 227 * 1024 && ScLayout<2>::SMEM <= 227 * 1024 &&
-                  ScLayout<3>::SMEM <= 227 * 1024 && ScLayout<4>::SMEM <= 227 * 1024,
+                  ScLayout<3>::SMEM <= 227 * 1024 && ScLayout<4>::SMEM <= 227 * 1024 &&
+                  ScLayout<8>::SMEM <= 227 * 1024 && ScLayout<16>::SMEM <= 227 * 1024,
               "screened shared memory budget");
-static_assert(ScLayout<4>::NST <= TC_S && ScLayout<1>::NST == TC_S, "stage barriers");
+static_assert(ScLayout<4>::NST <= TC_S && ScLayout<1>::NST == TC_S && ScLayout<16>::NST <= TC_S, "stage barriers");
 
-bool tc_supported(int d) { return d >= TC_D && d <= TC_MAXD && d % TC_D == 0; }
+bool tc_supported(int d) { return d >= TC_D && d % TC_D == 0 && (d <= 256 || d == 512 || d == 1024); }
 bool tc_half_supported(int d) { return d == TC_D; }
 int tc_max_d() { return TC_MAXD; }
 int tc_rows_per_cta() { return TC_ROWS; }
@@ -851,10 +859,12 @@ struct ScFin {
     static constexpr uint32_t LIST = (SX + TC_ROWS * 20 + (64 * SC_SEGS + 1) * 4 + 15) & ~15u;
     static constexpr int CAP = 8192;
 };
-static_assert(ScFin<1>::LIST + ScFin<1>::CAP * 8 <= ScLayout<1>::NST * SC_STAGE &&
-                  ScFin<2>::LIST + ScFin<2>::CAP * 8 <= ScLayout<2>::NST * SC_STAGE &&
-                  ScFin<3>::LIST + ScFin<3>::CAP * 8 <= ScLayout<3>::NST * SC_STAGE &&
-                  ScFin<4>::LIST + ScFin<4>::CAP * 8 <= ScLayout<4>::NST * SC_STAGE,
+static_assert(ScFin<1>::LIST + ScFin<1>::CAP * 8 <= ScLayout<1>::NST * ScLayout<1>::STAGE &&
+                  ScFin<2>::LIST + ScFin<2>::CAP * 8 <= ScLayout<2>::NST * ScLayout<2>::STAGE &&
+                  ScFin<3>::LIST + ScFin<3>::CAP * 8 <= ScLayout<3>::NST * ScLayout<3>::STAGE &&
+                  ScFin<4>::LIST + ScFin<4>::CAP * 8 <= ScLayout<4>::NST * ScLayout<4>::STAGE &&
+                  ScFin<8>::LIST + ScFin<8>::CAP * 8 <= ScLayout<8>::NST * ScLayout<8>::STAGE &&
+                  ScFin<16>::LIST + ScFin<16>::CAP * 8 <= ScLayout<16>::NST * ScLayout<16>::STAGE,
               "finaliser shared memory");
 
 // Producer of the screened half-step: the hi halves of the CTA's two row
@@ -869,12 +879,17 @@ __device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
     volatile int* abort = S.abort();
     int issued = 0;
     if (lane == 0) {
-        mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * NS * TILE_BYTES);
-        for (int r = 0; r < 2; ++r)
-            for (int k = 0; k < NS; ++k) {
-                const unsigned char* src = ops.aimg + (((size_t)b * ops.tiles_r + 2 * rb + r) * NS + k) * OP_BYTES;
-                bulk_g2s(S.sbase + L::OFF_A + (uint32_t)(r * NS + k) * TILE_BYTES, src, TILE_BYTES, S.bar(BAR_A()));
-            }
+        if (L::STREAM) {
+            mbar_arrive(S.bar(BAR_A()));  // nothing resident: the wait on the row tiles passes at once
+        } else {
+            mbar_arrive_expect_tx(S.bar(BAR_A()), 2 * NS * TILE_BYTES);
+            for (int r = 0; r < 2; ++r)
+                for (int k = 0; k < NS; ++k) {
+                    const unsigned char* src = ops.aimg + (((size_t)b * ops.tiles_r + 2 * rb + r) * NS + k) * OP_BYTES;
+                    bulk_g2s(S.sbase + L::OFF_A + (uint32_t)(r * NS + k) * TILE_BYTES, src, TILE_BYTES,
+                             S.bar(BAR_A()));
+                }
+        }
     }
     const unsigned char* bimg = ops.bimg + (size_t)b * ops.tiles_c * NS * OP_BYTES;
     const unsigned char* gbias = ops.bias_img + (size_t)b * (ops.tiles_c / 2) * SC_BT;
@@ -890,14 +905,21 @@ __device__ void sc_producer(const TcSmem& S, const TcOps& ops, int b, int rb, in
                 break;
             }
             if (lane == 0) {
-                const uint32_t dst = S.sbase + L::OFF_B + (uint32_t)st * SC_STAGE;
+                const uint32_t dst = S.sbase + L::OFF_B + (uint32_t)st * L::STAGE;
                 const bool last = (k == NS - 1);
-                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), 2 * TILE_BYTES + (last ? SC_BT : 0u));
-                bulk_g2s(dst, bimg + ((size_t)(t0 + 2 * lt) * NS + k) * OP_BYTES, TILE_BYTES, S.bar(BAR_FULL(st)));
-                bulk_g2s(dst + TILE_BYTES, bimg + ((size_t)(t0 + 2 * lt + 1) * NS + k) * OP_BYTES, TILE_BYTES,
+                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)),
+                                      (L::STREAM ? 4 : 2) * TILE_BYTES + (last ? SC_BT : 0u));
+                if (L::STREAM)  // slice k of both row tiles
+                    for (int r = 0; r < 2; ++r)
+                        bulk_g2s(dst + (uint32_t)r * TILE_BYTES,
+                                 ops.aimg + (((size_t)b * ops.tiles_r + 2 * rb + r) * NS + k) * OP_BYTES, TILE_BYTES,
+                                 S.bar(BAR_FULL(st)));
+                bulk_g2s(dst + L::ST_B, bimg + ((size_t)(t0 + 2 * lt) * NS + k) * OP_BYTES, TILE_BYTES,
                          S.bar(BAR_FULL(st)));
+                bulk_g2s(dst + L::ST_B + TILE_BYTES, bimg + ((size_t)(t0 + 2 * lt + 1) * NS + k) * OP_BYTES,
+                         TILE_BYTES, S.bar(BAR_FULL(st)));
                 if (last)
-                    bulk_g2s(dst + 2 * TILE_BYTES, gbias + (size_t)(t0 / 2 + lt) * SC_BT, SC_BT, S.bar(BAR_FULL(st)));
+                    bulk_g2s(dst + L::ST_BIAS, gbias + (size_t)(t0 / 2 + lt) * SC_BT, SC_BT, S.bar(BAR_FULL(st)));
             }
             issued = it + 1;
         }
@@ -925,8 +947,10 @@ __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns)
         // only part that differs, and every address here is below 256 KB, so a
         // byte offset o is added to a descriptor as o / 16 with no carry out of
         // the field; it advances by 2 per K = 16 step (32 bytes).
-        const uint64_t adesc0 = sw128_desc(S.sbase + L::OFF_A), acdesc0 = sw32_desc(S.sbase + L::OFF_AC);
-        const uint64_t bdesc0 = sw128_desc(S.sbase + L::OFF_B), bbdesc0 = sw32_desc(S.sbase + L::OFF_B + 2 * TILE_BYTES);
+        const uint64_t adesc0 = sw128_desc(S.sbase + (L::STREAM ? L::OFF_B : L::OFF_A)),
+                       acdesc0 = sw32_desc(S.sbase + L::OFF_AC);
+        const uint64_t bdesc0 = sw128_desc(S.sbase + L::OFF_B + L::ST_B),
+                       bbdesc0 = sw32_desc(S.sbase + L::OFF_B + L::ST_BIAS);
         int prev_st = -1;
         for (int lt = 0; ok && lt < nt; ++lt) {
             for (int k = 0; ok && k < NS; ++k) {
@@ -947,14 +971,15 @@ __device__ void sc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns)
                     }
                     issued_any = true;
                     const uint32_t d = tmem + (uint32_t)(r * SC_N);
-                    const uint64_t ad = adesc0 + (uint64_t)((r * NS + k) * (TILE_BYTES >> 4));
-                    const uint64_t bd = bdesc0 + (uint64_t)(st * (SC_STAGE >> 4));
+                    const uint64_t ad = adesc0 + (uint64_t)(L::STREAM ? st * (L::STAGE >> 4) + r * (TILE_BYTES >> 4)
+                                                                      : (r * NS + k) * (TILE_BYTES >> 4));
+                    const uint64_t bd = bdesc0 + (uint64_t)(st * (L::STAGE >> 4));
 #pragma unroll
                     for (int kk = 0; kk < TC_D / 16; ++kk)
                         tc_mma_f16(d, ad + 2u * (uint64_t)kk, bd + 2u * (uint64_t)kk, idesc, (k > 0 || kk > 0) ? 1u : 0u);
                     if (k == NS - 1) {
                         tc_mma_f16(d, acdesc0 + (uint64_t)(r * (SC_AT >> 4)),
-                                   bbdesc0 + (uint64_t)(st * (SC_STAGE >> 4)), idesc, 1u);
+                                   bbdesc0 + (uint64_t)(st * (L::STAGE >> 4)), idesc, 1u);
                         tc_commit(S.bar(BAR_ACCFULL(r, 0)));
                     }
                     if (r == 0 && prev_st >= 0) {
@@ -1473,6 +1498,8 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
         SOT_SC_CASE(2)
         SOT_SC_CASE(3)
         SOT_SC_CASE(4)
+        SOT_SC_CASE(8)
+        SOT_SC_CASE(16)
         default: return cudaErrorInvalidValue;
     }
 #undef SOT_SC_CASE

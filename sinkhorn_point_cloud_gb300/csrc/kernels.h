@@ -76,6 +76,7 @@ struct ApplyArgs {
     const float* fpot;    // caller's potentials (exact pair terms)
     const float* gpot;
     double kappa64;       // 1 / (eps ln 2) in double
+    int exact_sig = 0;    // dense path: re-evaluate each significant pair's weight exactly (float-float)
 };
 
 struct CooArgs {

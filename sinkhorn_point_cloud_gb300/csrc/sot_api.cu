@@ -191,7 +191,7 @@ int choose_path(int d, int flags, Path* out) {
     const int prec = flags & SOT_PREC_MASK;
     if (prec == SOT_PREC_F16X3) {
         if (!tc_supported(d))
-            return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d = 64, 128, 192 or 256 (got d = %d)", d);
+            return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d = 64, 128, 192, 256, 512 or 1024 (got d = %d)", d);
         *out = PATH_TC;
         return SOT_OK;
     }
@@ -918,6 +918,8 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     // which only pays for a few pairs per row).
     if (path == PATH_TC && (flags & SOT_COST_COSINE) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO) path = PATH_DENSE;
     cudaStream_t cs = (cudaStream_t)stream;
+    // above the transport products' dimension limit the fp32 plan application runs (d <= 1024)
+    if (path == PATH_TC && !tc_apply_supported(d) && d > transport_max_d()) path = PATH_DENSE;
     if (path == PATH_TC && !tc_apply_supported(d)) {
         rc = plan_apply_transport(X, Y, a, b, B, n, m, d, f, g, eps, cost, grad, rowsum, cs);
         if (rc) return rc;
@@ -936,6 +938,9 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam;
     p.X = X; p.a = a; p.shift = sv.shift; p.kappa = kappa;
     p.Yorig = Y; p.fpot = f; p.gpot = g; p.kappa64 = 1.0 / ((double)eps * SOT_LN2_D);
+    // above the transport products' dimension limit the dense plan application takes
+    // the significant pairs' weights exactly, as those products do below it
+    p.exact_sig = (sv.path == PATH_DENSE && d > transport_max_d()) ? 1 : 0;
     const int rpc = (sv.path == PATH_POINT) ? point_apply_rows_per_cta()
                     : (sv.path == PATH_TC) ? tc_apply_rows_per_cta() : dense_apply_rows_per_cta();
     p.rowtiles = (sv.path == PATH_TC) ? sv.rowtiles[0] : (n + rpc - 1) / rpc;

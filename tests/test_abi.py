@@ -167,8 +167,9 @@ def test_python_binding_checks_caller_tensors():
 def test_path_selection(lib):
     """The kernel family each dimension and precision flag takes (host logic,
     no GPU needed): d <= 3 the point kernels; d = 64, 128, 192, 256 the tensor
-    cores under automatic precision; other d up to 1024 the fp32 kernels; the
-    fp16 split takes those four d only and nothing goes past d = 1024."""
+    cores under automatic precision, and so do d = 512 and 1024; other d up to
+    1024 the fp32 kernels; the fp16 split takes those six d only and nothing
+    goes past d = 1024."""
     point, dense, tensor = 0, 1, 2
     for d in (1, 2, 3):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == point
@@ -176,11 +177,11 @@ def test_path_selection(lib):
     for d in (4, 8, 17, 63, 65, 100, 200, 255):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == dense, d
         assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED, d
-    for d in (64, 128, 192, 256):
+    for d in (64, 128, 192, 256, 512, 1024):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == tensor, d
         assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == tensor, d
         assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
-    for d in (257, 320, 512, 1000, 1024):
+    for d in (257, 320, 448, 576, 1000):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == dense, d
         assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
         assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED, d

@@ -187,11 +187,11 @@ def test_dense_fp32_path_d256(sot, orc):
 @pytest.mark.parametrize("d,n,m,B", [(512, 200, 170, 1), (1000, 130, 111, 2), (1024, 97, 140, 1)])
 def test_dense_fp32_path_wide_d(sot, orc, d, n, m, B):
     """d = 512, a ragged 1000 and the largest, 1024 ("FlashSinkhorn",
-    Experimentele Resultaten: d up to 1024): the coordinates stream in slices
-    of 256 and the plan application takes the gradient in 256-coordinate
-    slices.  Automatic precision takes the fp32 path above d = 256; eps grows
-    with d, as the costs do."""
+    Experimentele Resultaten: d up to 1024) on the fp32 path: the coordinates
+    stream in slices of 256 and the plan application takes the gradient in
+    256-coordinate slices, with the significant pairs' weights exact.  eps
+    grows with d, as the costs do."""
     from sinkhorn_point_cloud_gb300 import datagen as dg
     X, Y, a, b = dg.make_batch(4, B=B, n=n, m=m, d=d)
-    assert sot.sot_select_path(d, 0) == 1
-    print(check(sot, orc, X, Y, a, b, d / 128.0, 60))
+    assert sot.sot_select_path(d, sot.SOT_PREC_FP32) == 1
+    print(check(sot, orc, X, Y, a, b, d / 128.0, 60, flags=sot.SOT_PREC_FP32))

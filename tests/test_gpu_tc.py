@@ -224,12 +224,14 @@ def test_tc_screened_annealed_schedule(sot, orc):
     assert ef < TOL and eg < TOL, (ef, eg)
 
 
-@pytest.mark.parametrize("d,n,m,eps", [(128, 1100, 1000, 0.2), (192, 600, 520, 0.3), (256, 700, 650, 0.4)])
+@pytest.mark.parametrize("d,n,m,eps", [(128, 1100, 1000, 0.2), (192, 600, 520, 0.3), (256, 700, 650, 0.4),
+                                       (512, 600, 520, 0.8), (1024, 400, 300, 1.6)])
 def test_tc_wide_matches_oracle(sot, orc, d, n, m, eps):
-    """d = 128, 192, 256 on the tensor path ("FlashSinkhorn", Experimentele
-    Resultaten: the streaming kernels run up to d = 1024): warm half-steps on
-    the screened kernel with a K loop over slices of 64, cold half-steps and
-    the plan application on the fp32 kernels.  Gaussian recipe with softmax
+    """d = 128, 192, 256, 512 and 1024 on the tensor path ("FlashSinkhorn",
+    Experimentele Resultaten: the streaming kernels run up to d = 1024): warm
+    half-steps on the screened kernel with a K loop over slices of 64 (at 512
+    and 1024 the row tiles' slices stream with the column tiles'), cold
+    half-steps and the plan application on the fp32 kernels.  Gaussian recipe with softmax
     weights; potentials, cost and gradient against the oracle."""
     from sinkhorn_point_cloud_gb300 import datagen as dg
     X, Y, a, b = dg.make_batch(4, B=1, n=n, m=m, d=d)
@@ -254,10 +256,10 @@ def test_tc_wide_matches_oracle(sot, orc, d, n, m, eps):
 
 
 def test_tc_wide_screened_agrees_with_fp32(sot):
-    """d = 128 and 256 with two clouds: the tensor path and the fp32 path give
-    the same potentials to well below the parity tolerance."""
+    """d = 128, 256 and 512 with two clouds: the tensor path and the fp32 path
+    give the same potentials to well below the parity tolerance."""
     from sinkhorn_point_cloud_gb300 import datagen as dg
-    for d, eps in ((128, 0.2), (256, 0.4)):
+    for d, eps in ((128, 0.2), (256, 0.4), (512, 0.8)):
         X, Y, a, b = dg.make_batch(4, B=2, n=1500, m=1300, d=d)
         Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
         ft, gt = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=40, max_iters=40,
