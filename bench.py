@@ -406,8 +406,6 @@ def run_gpu(args, ws, rank, local):
         mufu = {"achieved_ex2_per_s": per_launch_pairs / secs, "peak_ex2_per_s": mufu_peak,
                 "frac": per_launch_pairs / secs / mufu_peak}
     path = sot.sot_select_path(d, flags)
-    if path == 2 and dom != "screened" and d != 64:
-        path = 1  # at d > 64 the tensor path's full half-steps run on the fp32 kernels
     if path == 2:
         if dom == "screened":
             flops_pair = 2 * d  # one fp16 product hi*hi per pair, 2 flops per multiply-add

@@ -108,7 +108,7 @@ static_assert(ScLayout<1>::SMEM <= 227 * 1024 && ScLayout<2>::SMEM <= 227 * 1024
 static_assert(ScLayout<4>::NST <= TC_S && ScLayout<1>::NST == TC_S && ScLayout<16>::NST <= TC_S, "stage barriers");
 
 bool tc_supported(int d) { return d >= TC_D && d % TC_D == 0 && (d <= 256 || d == 512 || d == 1024); }
-bool tc_half_supported(int d) { return d == TC_D; }
+bool tc_half_supported(int d) { return tc_supported(d); }
 int tc_max_d() { return TC_MAXD; }
 int tc_rows_per_cta() { return TC_ROWS; }
 int tc_cols_per_tile() { return SC_N; }  // column chunks are whole screened tiles
@@ -393,12 +393,14 @@ __device__ __forceinline__ TcSmem tc_smem(unsigned char* raw_ptr, uint32_t hdr =
 // `empty_count`: arrivals that free a stage (the MMA commit, plus one per
 // epilogue warp when the epilogue reads the stage's biases).
 // `accempty_count`: epilogue warps that read (and free) one accumulator buffer.
+// `empty_count_hi`: when nonzero, the arrivals that free stages TC_S / 2 ..
+// (the bias slots of the sliced full half-step).
 __device__ __forceinline__ uint32_t tc_setup(const TcSmem& S, int warp, uint32_t empty_count = 1 + 8,
-                                             uint32_t accempty_count = 4) {
+                                             uint32_t accempty_count = 4, uint32_t empty_count_hi = 0) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_S; ++s) {
             mbar_init(S.bar(BAR_FULL(s)), 1);
-            mbar_init(S.bar(BAR_EMPTY(s)), empty_count);
+            mbar_init(S.bar(BAR_EMPTY(s)), (empty_count_hi && s >= TC_S / 2) ? empty_count_hi : empty_count);
         }
         for (int r = 0; r < 2; ++r)
             for (int u = 0; u < 2; ++u) {
@@ -522,6 +524,124 @@ __device__ void tc_mma(const TcSmem& S, uint32_t tmem, int nt, uint64_t wait_ns)
     __syncwarp();
 }
 
+// ---- the full half-step at d = 128 ... 1024 (ns slices of K = 64) ----------
+// The row tiles' hi and lo parts (64 KB a slice) no longer stay resident:
+// each of two operand stages (96 KB) carries one slice of both row tiles and
+// of the column tile, hi and lo, and the accumulator gathers the slices.  The
+// column biases go to two slots of their own (one per accumulator buffer),
+// loaded with the tile's first slice and freed by the epilogue.
+constexpr int TCS_ST = 2;                      // operand stages
+constexpr uint32_t TCS_STAGE = 3 * OP_BYTES;   // [row tile 0][row tile 1][column tile], hi + lo each
+static_assert(TCS_ST * TCS_STAGE <= OFF_BIAS && TCS_STAGE % 1024 == 0, "sliced operand stages");
+static_assert(TCS_ST == TC_S / 2, "bias slots use the upper stage barriers");
+__host__ __device__ constexpr int BAR_BFULL(int u) { return BAR_FULL(TCS_ST + u); }
+__host__ __device__ constexpr int BAR_BEMPTY(int u) { return BAR_EMPTY(TCS_ST + u); }
+
+__device__ void tc_producer_sl(const TcSmem& S, const TcOps& ops, int b, int rb, int t0, int nt, int ns) {
+    const int lane = threadIdx.x & 31;
+    volatile int* abort = S.abort();
+    int issued = 0, bissued = 0;
+    if (lane == 0) mbar_arrive(S.bar(BAR_A()));  // nothing resident: the wait on the row tiles passes at once
+    const float* gbias = ops.bias + (size_t)b * ops.tiles_c * TC_N;
+    bool ok = true;
+    for (int lt = 0; ok && lt < nt; ++lt) {
+        if (lt == ops.hold_tile) break;
+        const int u = lt & 1;
+        if (!mbar_wait_bounded(S.bar(BAR_BEMPTY(u)), ((uint32_t)(lt >> 1) & 1u) ^ 1u, abort, ops.wait_ns)) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(S.bar(BAR_BFULL(u)), TC_N * 4);
+            bulk_g2s(S.sbase + OFF_BIAS + (uint32_t)u * TC_N * 4, gbias + (size_t)(t0 + lt) * TC_N, TC_N * 4,
+                     S.bar(BAR_BFULL(u)));
+        }
+        bissued = lt + 1;
+        for (int k = 0; k < ns; ++k) {
+            const int it = lt * ns + k, st = it % TCS_ST;
+            const uint32_t ph = (uint32_t)(it / TCS_ST) & 1u;
+            if (!mbar_wait_bounded(S.bar(BAR_EMPTY(st)), ph ^ 1u, abort, ops.wait_ns)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                const uint32_t dst = S.sbase + (uint32_t)st * TCS_STAGE;
+                mbar_arrive_expect_tx(S.bar(BAR_FULL(st)), TCS_STAGE);
+                for (int r = 0; r < 2; ++r)
+                    bulk_g2s(dst + (uint32_t)r * OP_BYTES,
+                             ops.aimg + (((size_t)b * ops.tiles_r + 2 * rb + r) * ns + k) * OP_BYTES, OP_BYTES,
+                             S.bar(BAR_FULL(st)));
+                bulk_g2s(dst + 2 * OP_BYTES, ops.bimg + (((size_t)b * ops.tiles_c + t0 + lt) * ns + k) * OP_BYTES,
+                         OP_BYTES, S.bar(BAR_FULL(st)));
+            }
+            issued = it + 1;
+        }
+    }
+    // never leave a copy in flight: the last stages and bias slots issued
+    if (lane == 0) {
+        int dummy = 0;
+        for (int it = (issued > TCS_ST ? issued - TCS_ST : 0); it < issued; ++it)
+            mbar_wait_bounded(S.bar(BAR_FULL(it % TCS_ST)), (uint32_t)(it / TCS_ST) & 1u, (volatile int*)&dummy,
+                              ops.wait_ns);
+        for (int lt = (bissued > 2 ? bissued - 2 : 0); lt < bissued; ++lt)
+            mbar_wait_bounded(S.bar(BAR_BFULL(lt & 1)), (uint32_t)(lt >> 1) & 1u, (volatile int*)&dummy,
+                              ops.wait_ns);
+        mbar_wait_bounded(S.bar(BAR_A()), 0u, (volatile int*)&dummy, ops.wait_ns);
+    }
+    __syncwarp();
+}
+
+// Per column tile, row tile and slice: 4 lo*hi + 4 hi*lo, then 4 hi*hi
+// 128 x 128 x 16 MMAs into the row tile's buffer (lt & 1), committed after
+// the last slice; each slice's stage is freed by its own commit.
+__device__ void tc_mma_sl(const TcSmem& S, uint32_t tmem, int nt, int ns, uint64_t wait_ns) {
+    if ((threadIdx.x & 31) == 0) {
+        volatile int* abort = S.abort();
+        bool ok = mbar_wait_bounded(S.bar(BAR_A()), 0u, abort, wait_ns);
+        bool issued_any = false;
+        const uint32_t idesc = f16_idesc(TC_M, TC_N);
+        for (int lt = 0; ok && lt < nt; ++lt) {
+            const int u = lt & 1;
+            const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
+            for (int k = 0; ok && k < ns; ++k) {
+                const int it = lt * ns + k, st = it % TCS_ST;
+                const uint32_t ph = (uint32_t)(it / TCS_ST) & 1u;
+                if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t base = S.sbase + (uint32_t)st * TCS_STAGE;
+                for (int r = 0; r < 2 && ok; ++r) {
+                    if (k == 0) {
+                        if (!mbar_wait_bounded(S.bar(BAR_ACCEMPTY(r, u)), pu ^ 1u, abort, wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    issued_any = true;
+                    const uint32_t d = tmem + (uint32_t)((2 * r + u) * TC_N);
+                    const uint32_t ahi = base + (uint32_t)r * OP_BYTES, alo = ahi + TILE_BYTES;
+                    const uint32_t bhi = base + 2 * OP_BYTES, blo = bhi + TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < TC_D / 16; ++kk) {
+                        const uint32_t ko = 32u * (uint32_t)kk;
+                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(blo + ko), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_f16(d, sw128_desc(alo + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < TC_D / 16; ++kk) {
+                        const uint32_t ko = 32u * (uint32_t)kk;
+                        tc_mma_f16(d, sw128_desc(ahi + ko), sw128_desc(bhi + ko), idesc, 1u);
+                    }
+                    if (k == ns - 1) tc_commit(S.bar(BAR_ACCFULL(r, u)));
+                }
+                if (!ok) break;
+                tc_commit(S.bar(BAR_EMPTY(st)));
+            }
+        }
+        tc_mma_drain(S, issued_any, wait_ns);
+    }
+    __syncwarp();
+}
+
 // After an epilogue warp has consumed tile lt: release its TMEM buffer and its stage.
 __device__ __forceinline__ void tc_release(const TcSmem& S, int wg, int lt) {
     tc_fence_before();
@@ -623,6 +743,8 @@ __device__ void tc_tail(const HalfArgs& p, const TcSmem& S, bool erow, int row, 
 }
 
 // ---- the half-step ------------------------------------------------------------------
+// SL: d > 64, the operands stream in slices (tc_producer_sl / tc_mma_sl).
+template <bool SL>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOps ops) {
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     // (after a screened half-step on probation: only the row blocks it left)
@@ -650,7 +772,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
 
     if (p.lo_reset && blockIdx.x == 0 && blockIdx.y == 0)
         for (int k = threadIdx.x; k < p.B; k += TC_THREADS) p.lo_reset[k] = SOT_ORD_EMPTY;
-    const uint32_t tmem = tc_setup(S, warp);
+    // sliced: operand stages freed by the MMA commit alone, bias slots by the 8 epilogue warps
+    const uint32_t tmem = SL ? tc_setup(S, warp, 1, 4, 8) : tc_setup(S, warp);
 
     float m = 0.f, s = 0.f;  // epilogue row state
     const int wg = (warp - 2) >> 2;  // row tile of this epilogue warp
@@ -660,9 +783,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
     const float old = (erow && p.rstate_in) ? p.rstate_in[rbase + row] : 0.f;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt);
+        if (SL) tc_producer_sl(S, ops, b, rb, t0, nt, ops.S);
+        else tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma(S, tmem, nt, ops.wait_ns);
+        if (SL) tc_mma_sl(S, tmem, nt, ops.S, ops.wait_ns);
+        else tc_mma(S, tmem, nt, ops.wait_ns);
     } else {
         // ---------------- epilogue: exponentials and row sums ----------------
         m = erow ? stabiliser(p.cold, p.lo_in, b, old) : INFINITY;
@@ -674,11 +799,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, ops.wait_ns)) break;
+            // the tile's biases: in its stage, or (sliced) in bias slot u
+            if (!mbar_wait_bounded(S.bar(SL ? BAR_BFULL(u) : BAR_FULL(st)), SL ? pu : ph, abort, ops.wait_ns)) break;
             if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, ops.wait_ns)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
-            const float* cb = bias + st * TC_N;
+            const float* cb = bias + (SL ? u : st) * TC_N;
             const float2 nm2 = make_float2(-m, -m);
             float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll 1
@@ -728,7 +854,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
                 if (ovf && mn > -INFINITY) ts = ts2;
             }
             s += ts;
-            tc_release(S, wg, lt);
+            if (SL) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(S.bar(BAR_ACCEMPTY(wg, u)));
+                    mbar_arrive(S.bar(BAR_BEMPTY(u)));
+                }
+            } else {
+                tc_release(S, wg, lt);
+            }
         }
     }
 
@@ -784,11 +919,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_half_kernel(HalfArgs p, TcOp
             retry[atomicAdd(&misc[2], 1)] = row;
         }
     }
-    tc_tail<TC_THREADS, TC_D>(p, S, erow, row, old, b, rb, rbase, cw, cst);
+    tc_tail<TC_THREADS, SL ? 0 : TC_D>(p, S, erow, row, old, b, rb, rbase, cw, cst);
 }
 
 cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mode, cudaStream_t st) {
-    if (mode != MODE_LSE || p.d != TC_D || plan.S != 1) return cudaErrorInvalidValue;
+    if (mode != MODE_LSE || !tc_supported(p.d) || p.d != plan.d || plan.S != tc_slices(p.d))
+        return cudaErrorInvalidValue;
     TcOps ops;
     ops.aimg = h ? plan.yop : plan.xop;
     ops.bimg = h ? plan.xop : plan.yop;
@@ -803,11 +939,19 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
         const cudaError_t eb = launch_tc_bias(plan, p, ops.tiles_c, st);
         if (eb != cudaSuccess) return eb;
     }
-    cudaError_t e = cudaFuncSetAttribute(tc_half_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
-    if (e != cudaSuccess) return e;
     dim3 grid(p.rowtiles * p.split, p.B), block(TC_THREADS);
-    count_launches(1);
-    tc_half_kernel<<<grid, block, TC_SMEM, st>>>(p, ops);
+    cudaError_t e;
+    if (plan.S == 1) {
+        e = cudaFuncSetAttribute(tc_half_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        tc_half_kernel<false><<<grid, block, TC_SMEM, st>>>(p, ops);
+    } else {
+        e = cudaFuncSetAttribute(tc_half_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        tc_half_kernel<true><<<grid, block, TC_SMEM, st>>>(p, ops);
+    }
     return cudaGetLastError();
 }
 

@@ -478,9 +478,7 @@ struct Solver {
             } else if (mode == MODE_LSE && screen_on && !cold && p.lo_in) {
                 ps.kind = 1;
                 // On probation, row blocks with many overflowing rows are left to a full
-                // tensor-core half-step.  At d > 64 there is none: every overflowing row
-                // takes the exact full-row LSE inline, and screen_check() then ends
-                // screening for the stage if there were many.
+                // tensor-core half-step launched right after.
                 if (screen_probation && !tc_dense_full) {
                     SOT_CUDA(cudaMemsetAsync(redo, 0, sizeof(int) * (size_t)B * rowtiles[h], st));
                     p.redo = redo;
