@@ -112,7 +112,7 @@ bool tc_half_supported(int d) { return tc_supported(d); }
 int tc_max_d() { return TC_MAXD; }
 int tc_rows_per_cta() { return TC_ROWS; }
 int tc_cols_per_tile() { return SC_N; }  // column chunks are whole screened tiles
-bool tc_apply_supported(int d) { return d == TC_D; }
+bool tc_apply_supported(int d) { return tc_supported(d); }
 static inline int tc_slices(int d) { return d > TC_D ? d / TC_D : 1; }
 // Automatic precision at d = 64 uses the tensor-core plan application.
 bool tc_apply_default() { return true; }
@@ -1667,23 +1667,26 @@ cudaError_t launch_tc_screen(const TcPlan& plan, const HalfArgs& p, int h, const
 struct TcApplyExtra {
     const float* nx;      // [B][n]
     const float* ny;      // [B][m]
-    const float* X;       // [B][n][64] caller coordinates
-    const float* Y;       // [B][m][64] caller coordinates
+    const float* X;       // [B][n][d] caller coordinates
+    const float* Y;       // [B][m][d] caller coordinates
     const float* f;       // [B][n] caller potentials
     const float* g;       // [B][m]
     double kappa64;
     const float* a;       // [B][n] or NULL (uniform)
-    const float* shift;   // [B][64]
-    float* vpart;         // [split][B*n][64], zero on entry
+    const float* shift;   // [B][d]
+    float* vpart;         // [split][B*n][d], zero on entry
     float* part_r;        // [split][B*n]
     float* part_q;        // [split][B*n]
     float* cost_part;     // [B][rowtiles] or NULL
-    float* grad;          // [B][n][64] or NULL
+    float* grad;          // [B][n][d] or NULL
     float* rowsum;        // [B][n] or NULL
 };
 
 constexpr float TC_SIG = -40.f;  // a pair is significant when log2(P_ij / a_i) > TC_SIG
 
+// SL: d > 64, the operands stream in slices as in the sliced full half-step;
+// a lane of pass B then owns 2 coordinates of every slice of 64.
+template <bool SL>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcOps ops, TcApplyExtra x) {
     extern __shared__ unsigned char smem_raw[];
     const TcSmem S = tc_smem(smem_raw);
@@ -1703,26 +1706,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     const size_t rbase = (size_t)b * p.nr;
     const float sc = ops.scale[b];
     const float tk = p.two_kappa / (sc * sc);
+    const int D = SL ? p.d : TC_D;  // coordinates (a multiple of 64)
+    const int ns = D / TC_D;
 
-    const uint32_t tmem = tc_setup(S, warp);
+    const uint32_t tmem = SL ? tc_setup(S, warp, 1, 4, 8) : tc_setup(S, warp);
 
     float m = 0.f, r = 0.f, q = 0.f;
     const int wg = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int row = row0 + wg * TC_M + q4 * 32 + lane;
     const bool erow = (warp >= 2) && row < p.nr;
-    float* vrow = erow ? x.vpart + (((size_t)ch * p.B * p.nr) + rbase + row) * TC_D : nullptr;
+    float* vrow = erow ? x.vpart + (((size_t)ch * p.B * p.nr) + rbase + row) * D : nullptr;
 
     if (warp == 0) {
-        tc_producer(S, ops, b, rb, t0, nt);
+        if (SL) tc_producer_sl(S, ops, b, rb, t0, nt, ns);
+        else tc_producer(S, ops, b, rb, t0, nt);
     } else if (warp == 1) {
-        tc_mma(S, tmem, nt, ops.wait_ns);
+        if (SL) tc_mma_sl(S, tmem, nt, ns, ops.wait_ns);
+        else tc_mma(S, tmem, nt, ops.wait_ns);
     } else {
         const float lrow = erow ? p.rstate_in[rbase + row] : 0.f;
         m = erow ? lrow - SOT_STAB_BIAS : INFINITY;
         const float fi = erow ? x.f[rbase + row] : 0.f;
         const float2 kap = make_float2((float)x.kappa64, (float)(x.kappa64 - (double)(float)x.kappa64));
-        const float* yorig = x.Y + (size_t)b * p.nc * TC_D;
+        const float* yorig = x.Y + (size_t)b * p.nc * D;
         const float* gpot = x.g + (size_t)b * p.nc;
         const float2 tk2 = make_float2(tk, tk);
         for (int lt = 0; lt < nt; ++lt) {
@@ -1730,11 +1737,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
             const uint32_t ph = (uint32_t)(lt / TC_S) & 1u;
             const int u = lt & 1;
             const uint32_t pu = (uint32_t)(lt >> 1) & 1u;
-            if (!mbar_wait_bounded(S.bar(BAR_FULL(st)), ph, abort, ops.wait_ns)) break;
+            // the tile's biases: in its stage, or (sliced) in bias slot u
+            if (!mbar_wait_bounded(S.bar(SL ? BAR_BFULL(u) : BAR_FULL(st)), SL ? pu : ph, abort, ops.wait_ns)) break;
             if (!mbar_wait_bounded(S.bar(BAR_ACCFULL(wg, u)), pu, abort, ops.wait_ns)) break;
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)((2 * wg + u) * TC_N);
-            const float* cb = S.bias() + st * TC_N;
+            const float* cb = S.bias() + (SL ? u : st) * TC_N;
             // pass A: row sum, significance marks per 4-column group.  A pair is
             // significant when t - L_i > TC_SIG, i.e. e = t - m > TC_SIG + (L_i - m).
             const float2 nm2 = make_float2(-m, -m);
@@ -1773,7 +1781,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                     const float f = ex2f(m - mn);
                     r *= f;
                     q *= f;
-                    for (int k = 0; k < TC_D; ++k) vrow[k] *= f;
+                    for (int k = 0; k < D; ++k) vrow[k] *= f;
                     m = mn;
                 }
                 float ts2 = 0.f;
@@ -1805,19 +1813,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                     unsigned todo = __ballot_sync(0xffffffffu, erow && e > sig_b);
                     if (!todo) continue;
                     const int j = (t0 + lt) * TC_N + cl;
-                    const float2 yv = *reinterpret_cast<const float2*>(yorig + (size_t)j * TC_D + 2 * lane);
+                    const float* yj = yorig + (size_t)j * D + 2 * lane;
                     const float gj = gpot[j], lbj = cw[j];
                     while (todo) {
                         const int l = __ffs(todo) - 1;
                         todo &= todo - 1u;
                         const int rl = __shfl_sync(0xffffffffu, row, l);
-                        const float2 xv = *reinterpret_cast<const float2*>(x.X + (rbase + rl) * TC_D + 2 * lane);
+                        const float* xl = x.X + (rbase + rl) * D + 2 * lane;
                         // C_lj: exact coordinate differences, their squares to ~2^-48
-                        const float2 d0 = two_sum(xv.x, -yv.x), d1 = two_sum(xv.y, -yv.y);
-                        float2 s0 = two_prod(d0.x, d0.x), s1 = two_prod(d1.x, d1.x);
-                        s0.y = __fmaf_rn(2.f * d0.x, d0.y, s0.y);
-                        s1.y = __fmaf_rn(2.f * d1.x, d1.y, s1.y);
-                        float2 C2 = ff_add(s0, s1);
+                        float2 C2 = make_float2(0.f, 0.f);
+                        for (int sl = 0; sl < ns; ++sl) {
+                            const float2 xv = *reinterpret_cast<const float2*>(xl + sl * TC_D);
+                            const float2 yv = *reinterpret_cast<const float2*>(yj + sl * TC_D);
+                            const float2 d0 = two_sum(xv.x, -yv.x), d1 = two_sum(xv.y, -yv.y);
+                            float2 s0 = two_prod(d0.x, d0.x), s1 = two_prod(d1.x, d1.x);
+                            s0.y = __fmaf_rn(2.f * d0.x, d0.y, s0.y);
+                            s1.y = __fmaf_rn(2.f * d1.x, d1.y, s1.y);
+                            C2 = ff_add(C2, ff_add(s0, s1));
+                        }
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
                             C2 = ff_add(C2, make_float2(__shfl_xor_sync(0xffffffffu, C2.x, o),
@@ -1834,15 +1847,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
                             r += w - ex2f(e);
                             q = fmaf(w, Cf, q);
                         }
-                        float* vr = x.vpart + (((size_t)ch * p.B * p.nr) + rbase + rl) * TC_D + 2 * lane;
-                        float2 acc = *reinterpret_cast<float2*>(vr);
-                        acc.x = fmaf(w, yv.x, acc.x);
-                        acc.y = fmaf(w, yv.y, acc.y);
-                        *reinterpret_cast<float2*>(vr) = acc;
+                        float* vr = x.vpart + (((size_t)ch * p.B * p.nr) + rbase + rl) * D + 2 * lane;
+                        for (int sl = 0; sl < ns; ++sl) {
+                            const float2 yv = *reinterpret_cast<const float2*>(yj + sl * TC_D);
+                            float2 acc = *reinterpret_cast<float2*>(vr + sl * TC_D);
+                            acc.x = fmaf(w, yv.x, acc.x);
+                            acc.y = fmaf(w, yv.y, acc.y);
+                            *reinterpret_cast<float2*>(vr + sl * TC_D) = acc;
+                        }
                     }
                 }
             }
-            tc_release(S, wg, lt);
+            if (SL) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(S.bar(BAR_ACCEMPTY(wg, u)));
+                    mbar_arrive(S.bar(BAR_BEMPTY(u)));
+                }
+            } else {
+                tc_release(S, wg, lt);
+            }
         }
     }
 
@@ -1885,17 +1910,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
             M = fmaxf(M, mc);
         }
         float R = 0.f, Q = 0.f;
-        float V[TC_D];
-#pragma unroll
-        for (int k = 0; k < TC_D; ++k) V[k] = 0.f;
         for (int c = 0; c < p.split; ++c) {
             const float mc = (p.split > 1) ? __ldcg(p.part_m + c * stride + rbase + row) : m;
             const float f = (mc == -INFINITY || M == -INFINITY) ? 0.f : ex2f(mc - M);
             R += f * ((p.split > 1) ? __ldcg(x.part_r + c * stride + rbase + row) : r);
             Q += f * ((p.split > 1) ? __ldcg(x.part_q + c * stride + rbase + row) : q);
-            const float* vc = x.vpart + ((size_t)c * stride + rbase + row) * TC_D;
-#pragma unroll
-            for (int k = 0; k < TC_D; ++k) V[k] = fmaf(f, __ldcg(vc + k), V[k]);
         }
         // the exponents were taken against m (= L_i - bias), so P_ij / a_i = 2^(e + m - L_i)
         const float ai = x.a ? x.a[rbase + row] : 1.f / (float)p.nr;
@@ -1904,10 +1923,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
         qi = fac * Q;
         if (x.rowsum) x.rowsum[rbase + row] = ri;
         if (x.grad) {
-            const float* xo = x.X + (rbase + row) * TC_D;
-            float* gr = x.grad + (rbase + row) * TC_D;
+            // v in caller coordinates, merged over the chunks 64 coordinates at a time
+            for (int k0 = 0; k0 < D; k0 += TC_D) {
+                float V[TC_D];
 #pragma unroll
-            for (int k = 0; k < TC_D; ++k) gr[k] = 2.f * (ai * xo[k] - fac * V[k]);  // v in caller coordinates
+                for (int k = 0; k < TC_D; ++k) V[k] = 0.f;
+                for (int c = 0; c < p.split; ++c) {
+                    const float mc = (p.split > 1) ? __ldcg(p.part_m + c * stride + rbase + row) : m;
+                    const float f = (mc == -INFINITY || M == -INFINITY) ? 0.f : ex2f(mc - M);
+                    const float* vc = x.vpart + ((size_t)c * stride + rbase + row) * D + k0;
+#pragma unroll
+                    for (int k = 0; k < TC_D; ++k) V[k] = fmaf(f, __ldcg(vc + k), V[k]);
+                }
+                const float* xo = x.X + (rbase + row) * D + k0;
+                float* gr = x.grad + (rbase + row) * D + k0;
+#pragma unroll
+                for (int k = 0; k < TC_D; ++k) gr[k] = 2.f * (ai * xo[k] - fac * V[k]);
+            }
         }
     }
     if (x.cost_part) {
@@ -1916,13 +1948,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_apply_kernel(HalfArgs p, TcO
     }
 }
 
-size_t tc_apply_scratch_floats(int B, int n, int split) {
-    return (size_t)split * B * n * (TC_D + 2);
+size_t tc_apply_scratch_floats(int B, int n, int d, int split) {
+    return (size_t)split * B * n * (d + 2);
 }
 
 cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfArgs& hp, float* scratch,
                             cudaStream_t st) {
-    if (a.d != TC_D) return cudaErrorInvalidValue;
+    if (!tc_supported(a.d) || a.d != plan.d || plan.S != tc_slices(a.d)) return cudaErrorInvalidValue;
     TcOps ops;
     ops.aimg = plan.xop;
     ops.bimg = plan.yop;
@@ -1949,18 +1981,25 @@ cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfAr
     x.a = a.a;
     x.shift = a.shift;
     x.vpart = scratch;
-    x.part_r = scratch + (size_t)hp.split * rows * TC_D;
+    x.part_r = scratch + (size_t)hp.split * rows * a.d;
     x.part_q = x.part_r + (size_t)hp.split * rows;
     x.cost_part = a.cost_part;
     x.grad = a.grad;
     x.rowsum = a.rowsum;
-    cudaError_t e = cudaMemsetAsync(x.vpart, 0, sizeof(float) * (size_t)hp.split * rows * TC_D, st);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    cudaError_t e = cudaMemsetAsync(x.vpart, 0, sizeof(float) * (size_t)hp.split * rows * a.d, st);
     if (e != cudaSuccess) return e;
     dim3 grid(hp.rowtiles * hp.split, hp.B), block(TC_THREADS);
-    count_launches(1);
-    tc_apply_kernel<<<grid, block, TC_SMEM, st>>>(hp, ops, x);
+    if (plan.S == 1) {
+        e = cudaFuncSetAttribute(tc_apply_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        tc_apply_kernel<false><<<grid, block, TC_SMEM, st>>>(hp, ops, x);
+    } else {
+        e = cudaFuncSetAttribute(tc_apply_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        tc_apply_kernel<true><<<grid, block, TC_SMEM, st>>>(hp, ops, x);
+    }
     return cudaGetLastError();
 }
 

@@ -952,7 +952,7 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     if (sv.path == PATH_POINT) {
         e = launch_point_apply(p, cs);
     } else if (sv.path == PATH_TC) {
-        float* scr = sv.S.alloc<float>(tc_apply_scratch_floats(B, n, sv.split[0]));
+        float* scr = sv.S.alloc<float>(tc_apply_scratch_floats(B, n, d, sv.split[0]));
         if (!scr) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
         const HalfArgs hp = sv.half_args(0, kappa, false, sv.L, nullptr, nullptr, false);
         e = launch_tc_apply(sv.tc, p, hp, scr, cs);

@@ -62,7 +62,7 @@ int tc_apply_rows_per_cta();
 // Plan application on the tensor cores.  `hp` carries the split plan and the
 // f-half operands (rows X, columns Y, column state Lam, row state L); scratch
 // holds tc_apply_scratch_floats() floats.
-size_t tc_apply_scratch_floats(int B, int n, int split);
+size_t tc_apply_scratch_floats(int B, int n, int d, int split);
 cudaError_t launch_tc_apply(const TcPlan& plan, const ApplyArgs& a, const HalfArgs& hp, float* scratch,
                             cudaStream_t st);
 
