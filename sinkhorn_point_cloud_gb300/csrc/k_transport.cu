@@ -49,10 +49,7 @@ static size_t tr_smem_bytes(int d, int c) {
 // pair, so no two large sums cancel.
 constexpr int TR_CD = 9;
 
-// COSTM (plan application): c = 2 outputs per row, out[i] = [ sum_j P_ij,
-// sum_j P_ij C_ij ] with C_ij the float-float distance of the exact branch; V
-// is not read.
-template <int CV, int W, bool CENTRED = false, bool COSTM = false>
+template <int CV, int W, bool CENTRED = false>
 __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     static_assert(W == 4 || W == 8, "column group of 4 or 8");
     extern __shared__ float smem[];
@@ -105,11 +102,10 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
             const int jj = e / d, k = e % d, j = base + jj;
             ys[k * TR_YS + jj] = (j < c_end) ? -Cl[(size_t)j * d + k] : 0.f;  // negated
         }
-        if (!COSTM)
-            for (int e = threadIdx.x; e < TR_CT * c; e += TR_T) {
-                const int jj = e / c, k = e % c, j = base + jj;
-                vs[jj * c + k] = (j < c_end) ? Vb[(size_t)j * p.ldv + k] : 0.f;
-            }
+        for (int e = threadIdx.x; e < TR_CT * c; e += TR_T) {
+            const int jj = e / c, k = e % c, j = base + jj;
+            vs[jj * c + k] = (j < c_end) ? Vb[(size_t)j * p.ldv + k] : 0.f;
+        }
         if (threadIdx.x < TR_CT) {
             const int j = base + threadIdx.x;
             const bool cj = j < c_end;
@@ -168,9 +164,6 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
                         aco[k] = fmaf(wdv, dk[k], aco[k]);
                         agy[k] = fmaf(wg, dk[k], agy[k]);
                     }
-                } else if (COSTM) {
-                    acc[0] = __fadd_rn(acc[0], w);
-                    acc[1] = fmaf(w, __fadd_rn(C2.x, C2.y), acc[1]);
                 } else {
 #pragma unroll
                     for (int k = 0; k < CV; ++k)
@@ -237,42 +230,6 @@ size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* ch
     *chunk = tpc * TR_CT;
     *split = (nc + *chunk - 1) / *chunk;
     return *split > 1 ? (size_t)*split * B * nr * c : 0;
-}
-
-// Row sums and cost terms of the plan (see COSTM above): out [B][nr][2]
-// (ldo >= 2), c = 2; V is not read.  The partial sums need split * B * nr * 2 floats.
-cudaError_t launch_transport_cost(const TransportArgs& p, cudaStream_t st) {
-    if (p.d < 1 || p.d > TR_MAXD || p.c != 2 || p.ldo < 2 || p.B < 1 || p.nr < 1 || p.nc < 1 || p.split < 1 ||
-        p.chunk < 1 || (long long)p.split * p.chunk < p.nc || (p.split > 1 && !p.part))
-        return cudaErrorInvalidValue;
-    const size_t sm = tr_smem_bytes(p.d, 2);
-    dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
-    auto kern = (p.d > 8) ? transport_kernel<4, 8, false, true> : transport_kernel<4, 4, false, true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    count_launches(1);
-    kern<<<grid, block, sm, st>>>(p);
-    if (p.split > 1) {
-        const long long count = (long long)p.B * p.nr * 2;
-        count_launches(1);
-        transport_merge_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(p.part, count, p.split, 2, p.ldo,
-                                                                                 p.out);
-    }
-    return cudaGetLastError();
-}
-
-// [count][2] pairs (r, q) -> r[count] (may be NULL) and q[count].
-__global__ void cost_rows_kernel(const float* rq, long long count, float* r, float* q) {
-    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (i >= count) return;
-    if (r) r[i] = rq[2 * i];
-    q[i] = rq[2 * i + 1];
-}
-cudaError_t launch_cost_rows(const float* rq, long long count, float* r, float* q, cudaStream_t st) {
-    if (count <= 0) return cudaSuccess;
-    count_launches(1);
-    cost_rows_kernel<<<(unsigned)((count + 255) / 256), 256, 0, st>>>(rq, count, r, q);
-    return cudaGetLastError();
 }
 
 // Row-centred products (see CENTRED above): V holds g (c = 1, ldv = 1), out has

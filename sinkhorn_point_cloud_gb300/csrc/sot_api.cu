@@ -751,51 +751,6 @@ int run_schedule(Solver& sv, const sot_schedule& s, const float* f0, const float
 
 }  // namespace
 
-// Plan application from transport products (the tensor path at d > 64, where
-// no tensor-core plan application exists): r and sum_j P_ij C_ij from the
-// cost mode, P Y in blocks of 64 coordinates, every weight and distance in
-// float-float, then grad = 2 (a x - P Y) and cost = sum_i q_i.
-int plan_apply_transport(const float* X, const float* Y, const float* a, const float* b, int B, int n, int m, int d,
-                         const float* f, const float* g, float eps, float* cost, float* grad, float* rowsum,
-                         cudaStream_t cs) {
-    const double kap = 1.0 / ((double)eps * SOT_LN2_D);
-    const int sms = device_sms();
-    Scratch S(cs);
-    float* rq = S.alloc<float>((size_t)B * n * 2);
-    float* q = S.alloc<float>((size_t)B * n);
-    size_t nparts = 0;
-    {
-        int sp, chn;
-        nparts = std::max(nparts, transport_plan(B, n, m, 2, sms, &sp, &chn));
-        nparts = std::max(nparts, transport_plan(B, n, m, std::min(d, transport_max_c()), sms, &sp, &chn));
-    }
-    float* part = nparts ? S.alloc<float>(nparts) : nullptr;
-    if (!rq || !q || (nparts && !part)) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
-    TransportArgs t;
-    t.B = B; t.nr = n; t.nc = m; t.d = d; t.R = X; t.Cl = Y; t.fr = f; t.gc = g; t.wr = a; t.wc = b;
-    t.kap_hi = (float)kap;
-    t.kap_lo = (float)(kap - (double)t.kap_hi);
-    t.part = part;
-    // r_i and q_i = sum_j P_ij C_ij (V is not read)
-    t.c = 2; t.V = Y; t.ldv = 2; t.out = rq; t.ldo = 2;
-    transport_plan(B, n, m, 2, sms, &t.split, &t.chunk);
-    SOT_CUDA(launch_transport_cost(t, cs));
-    SOT_CUDA(launch_cost_rows(rq, (long long)B * n, rowsum, q, cs));
-    if (cost) SOT_CUDA(launch_reduce_parts(q, B, n, cost, cs));
-    if (grad) {
-        // (P Y)_i into grad, 64 coordinates per product, then grad = 2 (a x - P Y)
-        for (int k0 = 0; k0 < d; k0 += transport_max_c()) {
-            t.c = std::min(transport_max_c(), d - k0);
-            t.V = Y + k0; t.ldv = d;
-            t.out = grad + k0; t.ldo = d;
-            transport_plan(B, n, m, t.c, sms, &t.split, &t.chunk);
-            SOT_CUDA(launch_transport(t, cs));
-        }
-        SOT_CUDA(launch_grad_finish(X, a, B, n, d, grad, cs));
-    }
-    return SOT_OK;
-}
-
 // ===========================================================================
 extern "C" {
 
@@ -916,14 +871,6 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     // which only pays for a few pairs per row).
     if (path == PATH_TC && (flags & SOT_COST_COSINE) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO) path = PATH_DENSE;
     cudaStream_t cs = (cudaStream_t)stream;
-    // above the transport products' dimension limit the fp32 plan application runs (d <= 1024)
-    if (path == PATH_TC && !tc_apply_supported(d) && d > transport_max_d()) path = PATH_DENSE;
-    if (path == PATH_TC && !tc_apply_supported(d)) {
-        rc = plan_apply_transport(X, Y, a, b, B, n, m, d, f, g, eps, cost, grad, rowsum, cs);
-        if (rc) return rc;
-        if (grad && (flags & SOT_COST_COSINE)) SOT_CUDA(launch_cosine_grad(Xin, (long long)B * n, d, grad, cs));
-        return SOT_OK;
-    }
     Solver sv(X, Y, a, b, B, n, m, d, path, cs);
     rc = sv.prepare(0);
     if (rc) return rc;
@@ -936,9 +883,9 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam;
     p.X = X; p.a = a; p.shift = sv.shift; p.kappa = kappa;
     p.Yorig = Y; p.fpot = f; p.gpot = g; p.kappa64 = 1.0 / ((double)eps * SOT_LN2_D);
-    // above the transport products' dimension limit the dense plan application takes
-    // the significant pairs' weights exactly, as those products do below it
-    p.exact_sig = (sv.path == PATH_DENSE && d > transport_max_d()) ? 1 : 0;
+    // above d = 256 the fp32 plan application takes the significant pairs' weights
+    // exactly: the fp32 exponent's rounding, at the size of kappa |x||y|, grows with d
+    p.exact_sig = (sv.path == PATH_DENSE && d > 256) ? 1 : 0;
     const int rpc = (sv.path == PATH_POINT) ? point_apply_rows_per_cta()
                     : (sv.path == PATH_TC) ? tc_apply_rows_per_cta() : dense_apply_rows_per_cta();
     p.rowtiles = (sv.path == PATH_TC) ? sv.rowtiles[0] : (n + rpc - 1) / rpc;

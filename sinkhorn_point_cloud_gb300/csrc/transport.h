@@ -36,10 +36,6 @@ int transport_max_c();
 size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk);
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st);
 cudaError_t launch_transport_centred(const TransportArgs& p, cudaStream_t st);
-// out[b][i] = [ sum_j P_ij, sum_j P_ij C_ij ] (c = 2, V unused), float-float weights and distances.
-cudaError_t launch_transport_cost(const TransportArgs& p, cudaStream_t st);
-// [count][2] (r, q) -> r (may be NULL), q.
-cudaError_t launch_cost_rows(const float* rq, long long count, float* r, float* q, cudaStream_t st);
 // g[k][j][:] <- 2 (w_j p_j - g[k][j][:]) for `count` points of d coordinates
 // (w NULL = uniform 1/per_cloud): the gradient from the transport product.
 cudaError_t launch_grad_finish(const float* P, const float* w, int B, int per_cloud, int d, float* g,
