@@ -973,8 +973,9 @@ cudaError_t launch_tc_half(const TcPlan& plan, const HalfArgs& p, int h, int mod
 // t_ij < L_new - theta, so the dropped mass is below nc * 2^-theta of the sum,
 // with theta = 26 + log2(nc): 2^-26 relative.
 // Tiles are 256 columns wide (128 x 256 x 16 MMAs); each of the two row tiles
-// has one 256-column accumulator, read by all eight epilogue warps (half the
-// columns each) and freed as soon as they hold it in registers.  Kept pairs
+// has one 256-column accumulator, read by all sixteen epilogue warps (64
+// columns of 32 rows each, with reducing loads that also give each 32-column
+// chunk's maximum) and freed as soon as they hold it in registers.  Kept pairs
 // go to the epilogue warp's own segment of the CTA's pool, slots numbered by
 // ballot.  The CTA that finishes the row block evaluates the pools of all its
 // column chunks flattened over its threads (exact scores: compensated fp32
@@ -1286,7 +1287,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) tc_screen_kernel(HalfArgs p, Tc
         }
         fence_proxy_async_smem();
     }
-    // stages are freed by the MMA commit alone; every accumulator is read by all 8 epilogue warps
+    // stages are freed by the MMA commit alone; every accumulator is read by all 16 epilogue warps
     const uint32_t tmem = tc_setup(S, warp, 1, SC_EPI);
 
     const int q4 = warp & 3;  // the TMEM lane quarter this warp may access
