@@ -59,11 +59,13 @@ enum sot_status {
 
 /* ---- schedule flags ---------------------------------------------------- */
 enum sot_flags {
-    SOT_PREC_AUTO = 0,          /* d <= 3: point path (fp32 FMA); d = 64, 128, 192, 256, 512, 1024: tensor cores
-                                   (fp16 x3); else fp32 FMA (d <= 1024; above 256 the coordinates stream in slices
-                                   of 256) */
-    SOT_PREC_FP32 = 1,          /* fp32 FMA contraction for any d <= 1024 */
-    SOT_PREC_F16X3 = 2,         /* tcgen05 fp16 products hi*hi + hi*lo + lo*hi (fp32-class accuracy) */
+    SOT_PREC_AUTO = 0,          /* d <= 3: point path (fp32 FMA); 4 <= d <= 16: fp32 FMA; 17 <= d <= 1024: tensor
+                                   cores (fp16 x3) at d = 64, 128, 192, 256, 512 or 1024, other d zero-padded to
+                                   the next of these */
+    SOT_PREC_FP32 = 1,          /* fp32 FMA contraction for any d <= 1024 (above 256 the coordinates stream in
+                                   slices of 256) */
+    SOT_PREC_F16X3 = 2,         /* tcgen05 fp16 products hi*hi + hi*lo + lo*hi (fp32-class accuracy), any
+                                   4 <= d <= 1024 (zero-padded as above) */
     SOT_PREC_MASK = 3,
     SOT_WARM_START = 1 << 4,    /* read f, g as the initial potentials instead of f = g = 0 */
     SOT_STAGE_EARLY_EXIT = 1 << 5, /* apply the stop test in every stage, not only at the final eps */

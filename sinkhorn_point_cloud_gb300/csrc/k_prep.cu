@@ -101,6 +101,24 @@ cudaError_t launch_normalise(const float* P, long long count, int d, float* out,
     return cudaGetLastError();
 }
 
+// dst[i][k] = src[i][k] for k < d, 0 for d <= k < D (count points): a cloud
+// at the tensor-core dimension D, whose extra coordinates add nothing.
+__global__ void pad_kernel(const float* src, long long count, int d, int D, float* dst) {
+    const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (e >= count * D) return;
+    const long long i = e / D;
+    const int k = (int)(e - i * D);
+    dst[e] = k < d ? src[i * d + k] : 0.f;
+}
+
+cudaError_t launch_pad(const float* src, long long count, int d, int D, float* dst, cudaStream_t st) {
+    if (count <= 0) return cudaSuccess;
+    const long long total = count * D;
+    count_launches(1);
+    pad_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(src, count, d, D, dst);
+    return cudaGetLastError();
+}
+
 // grad_i <- (I - xhat_i xhat_i^T) grad_i / |x_i| (0 for a zero point): the
 // gradient at the unit point xhat_i = x_i / |x_i| carried back to x_i.
 __global__ void cosine_grad_kernel(const float* X, long long count, int d, float* grad) {

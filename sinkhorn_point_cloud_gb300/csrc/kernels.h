@@ -128,6 +128,7 @@ cudaError_t launch_dense_coo(const CooArgs& p, int write_pass, cudaStream_t st);
 // Cosine cost: unit directions of `count` points, and the gradient carried
 // back through x / |x| (in place).
 cudaError_t launch_normalise(const float* P, long long count, int d, float* out, cudaStream_t st);
+cudaError_t launch_pad(const float* src, long long count, int d, int D, float* dst, cudaStream_t st);
 cudaError_t launch_cosine_grad(const float* X, long long count, int d, float* grad, cudaStream_t st);
 cudaError_t launch_center(const float* X, const float* Y, int B, int n, int m, int d,
                           float* shift, cudaStream_t st);

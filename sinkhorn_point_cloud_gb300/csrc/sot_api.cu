@@ -187,17 +187,28 @@ struct ProfScope {
 
 enum Path { PATH_POINT = 0, PATH_DENSE = 1, PATH_TC = 2 };
 
+// The tensor cores' dimension for d: the smallest of 64, 128, 192, 256, 512 and
+// 1024 not below d (0 past 1024).  A cloud of another d runs there with its
+// coordinates zero-padded.
+int tc_dim(int d) {
+    static const int dims[] = {64, 128, 192, 256, 512, 1024};
+    for (int D : dims)
+        if (d <= D) return D;
+    return 0;
+}
+constexpr int TC_AUTO_MIN_D = 17;  // automatic precision takes the tensor cores above d = 16
+
 int choose_path(int d, int flags, Path* out) {
     const int prec = flags & SOT_PREC_MASK;
     if (prec == SOT_PREC_F16X3) {
-        if (!tc_supported(d))
-            return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs d = 64, 128, 192, 256, 512 or 1024 (got d = %d)", d);
+        if (d < 4 || !tc_dim(d))
+            return fail(SOT_ERR_UNSUPPORTED, "SOT_PREC_F16X3 needs 4 <= d <= 1024 (got d = %d)", d);
         *out = PATH_TC;
         return SOT_OK;
     }
     if (prec != SOT_PREC_AUTO && prec != SOT_PREC_FP32) return fail(SOT_ERR_INVALID_ARG, "unknown precision flag");
     if (d <= 3) { *out = PATH_POINT; return SOT_OK; }
-    if (prec == SOT_PREC_AUTO && tc_supported(d)) { *out = PATH_TC; return SOT_OK; }
+    if (prec == SOT_PREC_AUTO && d >= TC_AUTO_MIN_D && tc_dim(d)) { *out = PATH_TC; return SOT_OK; }
     if (d > dense_max_d()) return fail(SOT_ERR_UNSUPPORTED, "d = %d exceeds the fp32 path limit %d", d, dense_max_d());
     *out = PATH_DENSE;
     return SOT_OK;
@@ -230,6 +241,23 @@ int unit_points(int flags, const float* X, const float* Y, int B, int n, int m, 
     SOT_CUDA(launch_normalise(Y, (long long)B * m, d, yn, scr.st));
     *Xu = xn;
     *Yu = yn;
+    return SOT_OK;
+}
+
+// The tensor path at a d it does not take natively: zero-padded copies of both
+// clouds at D = tc_dim(d) in `scr` (alive for the rest of the call).
+int pad_points(const float* X, const float* Y, int B, int n, int m, int d, int D, Scratch& scr, const float** Xp,
+               const float** Yp) {
+    *Xp = X;
+    *Yp = Y;
+    if (D == d || B == 0) return SOT_OK;
+    float* xp = scr.alloc<float>((size_t)B * n * D);
+    float* yp = scr.alloc<float>((size_t)B * m * D);
+    if (!xp || !yp) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    SOT_CUDA(launch_pad(X, (long long)B * n, d, D, xp, scr.st));
+    SOT_CUDA(launch_pad(Y, (long long)B * m, d, D, yp, scr.st));
+    *Xp = xp;
+    *Yp = yp;
     return SOT_OK;
 }
 
@@ -806,7 +834,10 @@ int sot_potentials_ex(const float* X, const float* Y, const float* a, const floa
     Scratch unit((cudaStream_t)stream);
     rc = unit_points(s->flags, X, Y, B, n, m, d, unit, &X, &Y);
     if (rc) return rc;
-    Solver sv(X, Y, a, b, B, n, m, d, path, (cudaStream_t)stream);
+    const int dr = (path == PATH_TC) ? tc_dim(d) : d;  // the dimension the kernels run at
+    rc = pad_points(X, Y, B, n, m, d, dr, unit, &X, &Y);
+    if (rc) return rc;
+    Solver sv(X, Y, a, b, B, n, m, dr, path, (cudaStream_t)stream);
     sv.screen_allowed = (path == PATH_TC) && !(s->flags & SOT_TC_NO_SCREEN);
     sv.cluster_allowed = (path == PATH_POINT) && !(s->flags & SOT_NO_CLUSTER);
     rc = run_schedule(sv, *s, f, g, f, g, st);
@@ -863,29 +894,36 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     Path path;
     rc = choose_path(d, flags, &path);
     if (rc) return rc;
-    if (path == PATH_TC && tc_apply_supported(d) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO && !tc_apply_default())
-        path = PATH_DENSE;
+    if (path == PATH_TC && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO && !tc_apply_default()) path = PATH_DENSE;
     // Cosine cost: on unit points every score is below 2 kappa in magnitude, so
     // fp32 scores keep cost and gradient at fp32 accuracy, and the plan is often
     // dense (the tensor-core apply re-evaluates every significant pair exactly,
     // which only pays for a few pairs per row).
     if (path == PATH_TC && (flags & SOT_COST_COSINE) && (flags & SOT_PREC_MASK) == SOT_PREC_AUTO) path = PATH_DENSE;
     cudaStream_t cs = (cudaStream_t)stream;
-    Solver sv(X, Y, a, b, B, n, m, d, path, cs);
+    const int dr = (path == PATH_TC) ? tc_dim(d) : d;  // the dimension the kernels run at
+    rc = pad_points(X, Y, B, n, m, d, dr, unit, &X, &Y);
+    if (rc) return rc;
+    float* gpad = nullptr;  // the gradient at dr, when that differs from d
+    if (grad && dr != d) {
+        gpad = unit.alloc<float>((size_t)B * n * dr);
+        if (!gpad) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
+    }
+    Solver sv(X, Y, a, b, B, n, m, dr, path, cs);
     rc = sv.prepare(0);
     if (rc) return rc;
     const float kappa = 1.f / (eps * SOT_LN2_D);
     rc = sv.init_states(f, g, kappa);
     if (rc) return rc;
     ApplyArgs p;
-    p.B = B; p.n = n; p.m = m; p.d = d;
+    p.B = B; p.n = n; p.m = m; p.d = dr;
     p.xpack = sv.xpack; p.ypack = sv.ypack; p.lw2x = sv.lw2x; p.lw2y = sv.lw2y;
     p.nx = sv.nx; p.ny = sv.ny; p.L = sv.L; p.Lam = sv.Lam;
     p.X = X; p.a = a; p.shift = sv.shift; p.kappa = kappa;
     p.Yorig = Y; p.fpot = f; p.gpot = g; p.kappa64 = 1.0 / ((double)eps * SOT_LN2_D);
     // above d = 256 the fp32 plan application takes the significant pairs' weights
     // exactly: the fp32 exponent's rounding, at the size of kappa |x||y|, grows with d
-    p.exact_sig = (sv.path == PATH_DENSE && d > 256) ? 1 : 0;
+    p.exact_sig = (sv.path == PATH_DENSE && dr > 256) ? 1 : 0;
     const int rpc = (sv.path == PATH_POINT) ? point_apply_rows_per_cta()
                     : (sv.path == PATH_TC) ? tc_apply_rows_per_cta() : dense_apply_rows_per_cta();
     p.rowtiles = (sv.path == PATH_TC) ? sv.rowtiles[0] : (n + rpc - 1) / rpc;
@@ -894,12 +932,12 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
         cpart = sv.S.alloc<float>((size_t)B * p.rowtiles);
         if (!cpart) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
     }
-    p.cost_part = cpart; p.grad = grad; p.rowsum = rowsum;
+    p.cost_part = cpart; p.grad = gpad ? gpad : grad; p.rowsum = rowsum;
     cudaError_t e;
     if (sv.path == PATH_POINT) {
         e = launch_point_apply(p, cs);
     } else if (sv.path == PATH_TC) {
-        float* scr = sv.S.alloc<float>(tc_apply_scratch_floats(B, n, d, sv.split[0]));
+        float* scr = sv.S.alloc<float>(tc_apply_scratch_floats(B, n, dr, sv.split[0]));
         if (!scr) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
         const HalfArgs hp = sv.half_args(0, kappa, false, sv.L, nullptr, nullptr, false);
         e = launch_tc_apply(sv.tc, p, hp, scr, cs);
@@ -908,6 +946,9 @@ int sot_plan_apply(const float* X, const float* Y, const float* a, const float* 
     }
     if (e != cudaSuccess) return fail(SOT_ERR_CUDA, "plan-apply launch failed: %s", cudaGetErrorString(e));
     if (cost) SOT_CUDA(launch_reduce_parts(cpart, B, p.rowtiles, cost, cs));
+    if (gpad)  // the first d coordinates of each row (the padded ones are zero)
+        SOT_CUDA(cudaMemcpy2DAsync(grad, sizeof(float) * d, gpad, sizeof(float) * dr, sizeof(float) * d,
+                                   (size_t)B * n, cudaMemcpyDeviceToDevice, cs));
     if (grad && (flags & SOT_COST_COSINE)) SOT_CUDA(launch_cosine_grad(Xin, (long long)B * n, d, grad, cs));
     SOT_CUDA(launch_status_merge(sv.dflags, cs));  // asynchronous: reported by sot_async_status
     return SOT_OK;

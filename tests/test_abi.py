@@ -58,8 +58,8 @@ def test_unsupported_precision_rejected(lib):
     s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, binding.SOT_PREC_F16X3)
     # d = 3 has no tensor-core path
     assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 3, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
-    # d = 300 has no tensor-core path either; d = 1025 has no path at all
-    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 300, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
+    # d = 1025 has no path at all
+    assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 1025, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
     s = binding.sot_schedule(0.1, 0.1, 0.5, 10, 10, 0.0, 0)
     assert lib.sot_potentials_ex(p, p, NULL, NULL, 1, 5, 5, 1025, C.byref(s), p, p, NULL, NULL) == binding.SOT_ERR_UNSUPPORTED
 
@@ -166,26 +166,25 @@ def test_python_binding_checks_caller_tensors():
 
 def test_path_selection(lib):
     """The kernel family each dimension and precision flag takes (host logic,
-    no GPU needed): d <= 3 the point kernels; d = 64, 128, 192, 256 the tensor
-    cores under automatic precision, and so do d = 512 and 1024; other d up to
-    1024 the fp32 kernels; the fp16 split takes those six d only and nothing
-    goes past d = 1024."""
+    no GPU needed): d <= 3 the point kernels; under automatic precision the
+    fp32 kernels for 4 <= d <= 16 and the tensor cores for 17 <= d <= 1024
+    (zero-padded to 64, 128, 192, 256, 512 or 1024); the fp16 split takes any
+    4 <= d <= 1024; fp32 any d up to 1024; nothing goes past d = 1024."""
     point, dense, tensor = 0, 1, 2
     for d in (1, 2, 3):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == point
         assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == point
-    for d in (4, 8, 17, 63, 65, 100, 200, 255):
+        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED
+    for d in (4, 8, 13, 16):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == dense, d
-        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED, d
-    for d in (64, 128, 192, 256, 512, 1024):
+        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == tensor, d
+        assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
+    for d in (17, 63, 64, 65, 100, 128, 192, 200, 255, 256, 257, 320, 512, 1000, 1024):
         assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == tensor, d
         assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == tensor, d
         assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
-    for d in (257, 320, 448, 576, 1000):
-        assert lib.sot_select_path(d, binding.SOT_PREC_AUTO) == dense, d
-        assert lib.sot_select_path(d, binding.SOT_PREC_FP32) == dense, d
-        assert lib.sot_select_path(d, binding.SOT_PREC_F16X3) == binding.SOT_ERR_UNSUPPORTED, d
-    assert lib.sot_select_path(1025, binding.SOT_PREC_AUTO) == binding.SOT_ERR_UNSUPPORTED
+    for flags in (binding.SOT_PREC_AUTO, binding.SOT_PREC_F16X3, binding.SOT_PREC_FP32):
+        assert lib.sot_select_path(1025, flags) == binding.SOT_ERR_UNSUPPORTED
 
 
 def test_hvp_arguments_rejected_on_host(lib):

@@ -268,3 +268,30 @@ def test_tc_wide_screened_agrees_with_fp32(sot):
                                        flags=sot.SOT_PREC_FP32)
         ef, eg = potentials_error(host(ft), host(gt), host(ff), host(gf))
         assert ef < 2e-5 and eg < 2e-5, (d, ef, eg)
+
+
+@pytest.mark.parametrize("d,n,m,eps,forced", [(17, 700, 650, 0.03, False), (100, 600, 520, 0.16, False),
+                                              (300, 500, 450, 0.47, False), (700, 400, 300, 1.1, False),
+                                              (8, 700, 650, 0.0125, True)])
+def test_tc_padded_dims_match_oracle(sot, orc, d, n, m, eps, forced):
+    """Dimensions the tensor cores do not take natively run there with the
+    coordinates zero-padded (17 -> 64, 100 -> 128, 300 -> 512, 700 -> 1024;
+    d = 8 with the fp16 split forced): potentials, cost and gradient (at the
+    caller's d) against the oracle."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=n, m=m, d=d)
+    flags = sot.SOT_PREC_F16X3 if forced else 0
+    assert sot.sot_select_path(d, flags) == 2
+    Xd, Yd, ad, bd = dev(X), dev(Y), dev(a), dev(b)
+    iters = 60
+    f, g = sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=eps, iters_per_stage=iters, max_iters=iters, flags=flags)
+    c, gr, _ = sot.sot_plan_apply(Xd, Yd, ad, bd, f, g, eps, flags=flags)
+    assert tuple(gr.shape) == (1, n, d)
+    fr, gref = orc.sinkhorn(X[0], Y[0], a[0], b[0], [eps], [iters])
+    ef, eg = potentials_error(host(f), host(g), fr[None], gref[None])
+    out = orc.plan_apply(X[0], Y[0], a[0], b[0], host(f)[0], host(g)[0], eps)
+    ec = abs(host(c)[0] - out["cost"]) / abs(out["cost"])
+    egr = normwise(host(gr)[0], out["grad"])
+    msg = f"d = {d}: f {ef:.2e} g {eg:.2e} cost {ec:.2e} grad {egr:.2e}"
+    print(msg)
+    assert max(ef, eg, ec, egr) < TOL, msg
