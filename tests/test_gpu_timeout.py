@@ -102,3 +102,41 @@ def test_device_usable_after_timeouts(sot, orc, prob):
     out = orc.plan_apply(X[0], Y[0], a[0], b[0], host(f)[0], host(g)[0], eps)
     egr = normwise(host(gr)[0], out["grad"])
     assert max(ef, eg, egr) < TOL, (ef, eg, egr)
+
+
+@pytest.fixture(scope="module")
+def prob_wide():
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=4096, m=4096, d=128)
+    return dev(X), dev(Y), dev(a), dev(b)
+
+
+@pytest.mark.parametrize("tile,after", [(1, 0), (1, 2)],
+                         ids=["sliced full half-step", "sliced screened half-step"])
+def test_timeout_sliced_kernels(sot, orc, prob_wide, tile, after):
+    """d = 128: the kernels that stream K slices (the full and the screened
+    half-step) give up the same way; a plan application with a withheld tile
+    reports it asynchronously; a normal solve on the same device afterwards
+    matches the oracle."""
+    Xd, Yd, ad, bd = prob_wide
+    sot.sot_test_hold_tile(tile, after, LIMIT_NS)
+    with pytest.raises(sot.SotError) as ei:
+        sot.sot_potentials_ex(Xd, Yd, ad, bd, eps=0.2, iters_per_stage=3, stats=True)
+    assert ei.value.status == sot.SOT_ERR_TIMEOUT
+    sot.sot_test_hold_tile(-1)
+    f, g = sot.sot_potentials(Xd, Yd, ad, bd, eps=0.2, iters=3)
+    sot.sot_async_status()
+    sot.sot_test_hold_tile(1, 0, LIMIT_NS)
+    c, gr, _ = sot.sot_plan_apply(Xd, Yd, ad, bd, f, g, 0.2)
+    with pytest.raises(sot.SotError) as ei:
+        sot.sot_async_status()
+    assert ei.value.status == sot.SOT_ERR_TIMEOUT
+    assert torch.isnan(gr).any()
+    sot.sot_test_hold_tile(-1)
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(4, B=1, n=400, m=360, d=128)
+    f, g = sot.sot_potentials(dev(X), dev(Y), dev(a), dev(b), eps=0.2, iters=30)
+    sot.sot_async_status()
+    fr, gref = orc.sinkhorn(X[0], Y[0], a[0], b[0], [0.2], [30])
+    ef, eg = potentials_error(host(f), host(g), fr[None], gref[None])
+    assert max(ef, eg) < TOL, (ef, eg)
