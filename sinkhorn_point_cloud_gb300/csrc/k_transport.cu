@@ -14,11 +14,23 @@
 // about log2 w'_j + kappa (f_i + g_j - C_ij).  A pair below -(26 + log2 nc) - 4 is
 // skipped: its weight is under 2^-30 / nc of w_i, so all skipped pairs of a row
 // together carry less than 2^-30 of it (the 4 units cover the fp32 estimate's
-// own error many times over), far below fp32 resolution of the sum.  Every
+// own error many times over), far below fp32 resolution of the sum.  The test
+// is taken as C_ij < f_i + h_j with the column's limit
+// h_j = g_j + (log2 w'_j + 30 + log2 nc) / kappa staged with the tile.  Every
 // other pair is evaluated exactly: C_ij from error-free coordinate differences
 // and squares in float-float, and the exponent, where the potentials and C_ij
 // cancel to a small number, in float-float throughout (the fp64 pipe is slow
 // on this part).
+//
+// The exact evaluations are shared out over the warp: per block of columns
+// (the whole tile when d <= 8, where they dominate; 8 columns above, where the
+// screen does and shared memory is scarcer), the pairs its 32 rows' screens
+// passed are queued in shared memory (row by row, each row's in column order)
+// and evaluated one per lane, so a column that matters to one row of a warp
+// costs one lane, not the warp.  Each row then adds its pairs' terms in
+// column order, as a serial loop over the columns would.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "transport.h"
@@ -28,6 +40,7 @@ namespace sot {
 constexpr int TR_T = 128;        // rows per CTA (one per thread)
 constexpr int TR_CT = 32;        // columns per shared-memory tile
 constexpr int TR_YS = TR_CT + 4; // its row stride (keeps float4 reads aligned; 4-way store conflicts, not 32)
+constexpr int TR_VS = TR_CT + 1; // row stride of the tile's V values, transposed (rows read at 32 columns at once)
 constexpr int TR_MAXD = 256;
 constexpr int TR_MAXC = 64;
 
@@ -38,8 +51,14 @@ int transport_max_c() { return TR_MAXC; }
 // fall in 32 different banks
 __host__ __device__ inline int tr_ldx(int d) { return (d % 2 == 0) ? d + 1 : d; }
 
+// column group of the screen (one row value reused by W columns) and columns
+// per exact-evaluation queue
+__host__ __device__ constexpr int tr_w(int d) { return d > 8 ? 8 : 4; }
+__host__ __device__ constexpr int tr_qg(int w) { return w == 8 ? 8 : TR_CT; }
+
 static size_t tr_smem_bytes(int d, int c) {
-    return sizeof(float) * ((size_t)TR_T * tr_ldx(d) + (size_t)d * TR_YS + (size_t)TR_CT * c + 2 * TR_CT);
+    return sizeof(float) * ((size_t)TR_T * tr_ldx(d) + (size_t)d * TR_YS + 3 * TR_CT + 2 * TR_T + (size_t)TR_VS * c +
+                            (size_t)TR_T * tr_qg(tr_w(d)));
 }
 
 // CENTRED (row-centred products for the Hessian-vector product, d <= TR_CD):
@@ -56,9 +75,17 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     const int d = p.d, c = p.c, ldx = tr_ldx(d);
     float* xs = smem;                 // [TR_T][ldx] this CTA's rows
     float* ys = xs + TR_T * ldx;      // [d][TR_YS] column tile, transposed and negated
-    float* vs = ys + d * TR_YS;       // [TR_CT][c] V rows of the tile
-    float* gs = vs + TR_CT * c;       // [TR_CT] column potentials
+    float* hs = ys + d * TR_YS;       // [TR_CT] screen limits h_j (-inf past the end; float4 reads)
+    float* gs = hs + TR_CT;           // [TR_CT] column potentials
     float* ls = gs + TR_CT;           // [TR_CT] log2 column weights (-inf past the end)
+    float* frs = ls + TR_CT;          // [TR_T] row potentials
+    float* lws = frs + TR_T;          // [TR_T] log2 row weights
+    float* vs = lws + TR_T;           // [c][TR_VS] V values of the tile, transposed
+    constexpr int QG = tr_qg(W);
+    unsigned* qs = reinterpret_cast<unsigned*>(vs + TR_VS * c);  // [TR_T / 32][32 QG] per-warp pair queues
+    const int lane = threadIdx.x & 31, wrp = threadIdx.x >> 5;
+    unsigned* q = qs + wrp * (32 * QG);  // entries (row lane << 5 | column), then their weights
+    float* qw = reinterpret_cast<float*>(q);
     const int b = blockIdx.y;
     const int rb = blockIdx.x / p.split, ch = blockIdx.x % p.split;
     const int row0 = rb * TR_T;
@@ -75,6 +102,8 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     }
     const float fi = ok ? p.fr[(size_t)b * p.nr + i] : 0.f;
     const float lwi = ok ? (p.wr ? log2f(p.wr[(size_t)b * p.nr + i]) : -log2f((float)p.nr)) : 0.f;
+    frs[threadIdx.x] = fi;
+    lws[threadIdx.x] = lwi;
     const float2 kap = make_float2(p.kap_hi, p.kap_lo);
     const float sig = -(30.f + log2f((float)p.nc));  // skip threshold on log2(P_ij / w_i)
     float acc[CV];
@@ -104,72 +133,113 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         }
         for (int e = threadIdx.x; e < TR_CT * c; e += TR_T) {
             const int jj = e / c, k = e % c, j = base + jj;
-            vs[jj * c + k] = (j < c_end) ? Vb[(size_t)j * p.ldv + k] : 0.f;
+            vs[k * TR_VS + jj] = (j < c_end) ? Vb[(size_t)j * p.ldv + k] : 0.f;
         }
         if (threadIdx.x < TR_CT) {
             const int j = base + threadIdx.x;
             const bool cj = j < c_end;
             gs[threadIdx.x] = cj ? p.gc[(size_t)b * p.nc + j] : 0.f;
-            ls[threadIdx.x] = cj ? (p.wc ? log2f(p.wc[(size_t)b * p.nc + j]) : -log2f((float)p.nc)) : -INFINITY;
+            const float lj = cj ? (p.wc ? log2f(p.wc[(size_t)b * p.nc + j]) : -log2f((float)p.nc)) : -INFINITY;
+            ls[threadIdx.x] = lj;
+            hs[threadIdx.x] = cj ? gs[threadIdx.x] + (lj - sig) / p.kap_hi : -INFINITY;
         }
         __syncthreads();
-        if (!ok) continue;
-        for (int jg = 0; jg < TR_CT; jg += W) {
-            // fp32 direct-form distances of W columns, two per packed instruction
-            float2 cp[W / 2];
+        for (int qb = 0; qb < TR_CT; qb += QG) {
+            // screen: bit jj of `sm` is set when pair (i, base + jj) needs its exact weight
+            unsigned sm = 0;
+            if (ok) {
+                for (int jg = qb; jg < qb + QG; jg += W) {
+                    // fp32 direct-form distances of W columns, two per packed instruction
+                    float2 cp[W / 2];
 #pragma unroll
-            for (int h = 0; h < W / 2; ++h) cp[h] = make_float2(0.f, 0.f);
-            for (int k = 0; k < d; ++k) {
-                const float2 xx = make_float2(xr[k], xr[k]);
+                    for (int h = 0; h < W / 2; ++h) cp[h] = make_float2(0.f, 0.f);
+                    for (int k = 0; k < d; ++k) {
+                        const float2 xx = make_float2(xr[k], xr[k]);
 #pragma unroll
-                for (int q = 0; q < W / 4; ++q) {
-                    const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + jg + 4 * q);
-                    const float2 t0 = fadd2(xx, make_float2(y4.x, y4.y));
-                    const float2 t1 = fadd2(xx, make_float2(y4.z, y4.w));
-                    cp[2 * q] = ffma2(t0, t0, cp[2 * q]);
-                    cp[2 * q + 1] = ffma2(t1, t1, cp[2 * q + 1]);
+                        for (int qq = 0; qq < W / 4; ++qq) {
+                            const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + jg + 4 * qq);
+                            const float2 t0 = fadd2(xx, make_float2(y4.x, y4.y));
+                            const float2 t1 = fadd2(xx, make_float2(y4.z, y4.w));
+                            cp[2 * qq] = ffma2(t0, t0, cp[2 * qq]);
+                            cp[2 * qq + 1] = ffma2(t1, t1, cp[2 * qq + 1]);
+                        }
+                    }
+#pragma unroll
+                    for (int qq = 0; qq < W / 4; ++qq) {
+                        // the screen in fp32: C_ij < f_i + h_j
+                        const float4 h4 = *reinterpret_cast<const float4*>(hs + jg + 4 * qq);
+                        const int u = jg + 4 * qq;
+                        if (cp[2 * qq].x < fi + h4.x) sm |= 1u << u;
+                        if (cp[2 * qq].y < fi + h4.y) sm |= 2u << u;
+                        if (cp[2 * qq + 1].x < fi + h4.z) sm |= 4u << u;
+                        if (cp[2 * qq + 1].y < fi + h4.w) sm |= 8u << u;
+                    }
                 }
             }
+            // queue the warp's pairs of this block: this lane's run starts at `o`
+            const int cnt = __popc(sm);
+            int o = cnt;
 #pragma unroll
-            for (int u = 0; u < W; ++u) {
-                const int jj = jg + u;
-                // screen: log2(P_ij / w_i) estimated in fp32 (-inf past the last column)
-                const float cu = (u & 1) ? cp[u >> 1].y : cp[u >> 1].x;
-                const float est = fmaf(p.kap_hi, fi + gs[jj] - cu, ls[jj]);
-                if (!(est > sig)) continue;
-                // exact: C_ij from exact differences and squares (float-float)
+            for (int s = 1; s < 32; s <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, o, s);
+                if (lane >= s) o += t;
+            }
+            const int total = __shfl_sync(0xffffffffu, o, 31);
+            o -= cnt;
+            if (total == 0) continue;  // warp-uniform
+            {
+                int k = o;
+                for (unsigned mm = sm; mm; mm &= mm - 1) q[k++] = ((unsigned)lane << 5) | (unsigned)(__ffs(mm) - 1);
+            }
+            __syncwarp();
+            // exact weights, one queued pair per lane: C_ij from exact differences
+            // and squares, log2 P_ij = log2 w_i + log2 w'_j + kappa (f_i + g_j - C_ij),
+            // all in float-float
+            for (int t = lane; t < total; t += 32) {
+                const unsigned e = q[t];
+                const int jj = (int)(e & 31u), r = (wrp << 5) | (int)(e >> 5);
+                const float* xq = xs + r * ldx;
                 float2 C2 = make_float2(0.f, 0.f);
                 for (int k = 0; k < d; ++k) {
-                    const float2 dd = two_sum(xr[k], ys[k * TR_YS + jj]);
+                    const float2 dd = two_sum(xq[k], ys[k * TR_YS + jj]);
                     float2 sq = two_prod(dd.x, dd.x);
                     sq.y = __fmaf_rn(2.f * dd.x, dd.y, sq.y);
                     C2 = ff_add(C2, sq);
                 }
-                // log2 P_ij = log2 w_i + log2 w'_j + kappa (f_i + g_j - C_ij)
-                const float2 pot = ff_add(two_sum(fi, gs[jj]), make_float2(-C2.x, -C2.y));
-                const float2 ell = ff_add(ff_mul(kap, pot), two_sum(ls[jj], lwi));
-                const float w = exp2f(__fadd_rn(ell.x, ell.y));
-                const float* vj = vs + jj * c;
-                if (CENTRED) {
-                    // y_j - yhat_i (the tile holds -y_j), its projection on v_i
-                    float dk[TR_CD], dv = 0.f;
+                const float2 pot = ff_add(two_sum(frs[r], gs[jj]), make_float2(-C2.x, -C2.y));
+                const float2 ell = ff_add(ff_mul(kap, pot), two_sum(ls[jj], lws[r]));
+                qw[t] = exp2f(__fadd_rn(ell.x, ell.y));
+            }
+            __syncwarp();
+            // this row's terms, in column order
+            {
+                int k = o;
+                for (unsigned mm = sm; mm; mm &= mm - 1, ++k) {
+                    const int jj = __ffs(mm) - 1;
+                    const float w = qw[k];
+                    const float* vj = vs + jj;  // V_j[k] at vj[k TR_VS]
+                    if (CENTRED) {
+                        // y_j - yhat_i (the tile holds -y_j), its projection on v_i
+                        float dk[TR_CD], dv = 0.f;
 #pragma unroll
-                    for (int k = 0; k < TR_CD; ++k) {
-                        dk[k] = (k < d) ? -ys[k * TR_YS + jj] - yh[k] : 0.f;
-                        dv = fmaf(dk[k], vr[k], dv);
+                        for (int kk = 0; kk < TR_CD; ++kk) {
+                            dk[kk] = (kk < d) ? -ys[kk * TR_YS + jj] - yh[kk] : 0.f;
+                            dv = fmaf(dk[kk], vr[kk], dv);
+                        }
+                        const float wdv = w * dv, wg = w * vj[0];
+#pragma unroll
+                        for (int kk = 0; kk < TR_CD; ++kk) {
+                            aco[kk] = fmaf(wdv, dk[kk], aco[kk]);
+                            agy[kk] = fmaf(wg, dk[kk], agy[kk]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < CV; ++kk)
+                            if (kk < c) acc[kk] = fmaf(w, vj[kk * TR_VS], acc[kk]);
                     }
-                    const float wdv = w * dv, wg = w * vj[0];
-#pragma unroll
-                    for (int k = 0; k < TR_CD; ++k) {
-                        aco[k] = fmaf(wdv, dk[k], aco[k]);
-                        agy[k] = fmaf(wg, dk[k], agy[k]);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < CV; ++k)
-                        if (k < c) acc[k] = fmaf(w, vj[k], acc[k]);
                 }
             }
+            __syncwarp();  // the queue is refilled by the next block
         }
     }
     if (ok && CENTRED) {
@@ -216,20 +286,58 @@ cudaError_t launch_grad_finish(const float* P, const float* w, int B, int per_cl
     return cudaGetLastError();
 }
 
-size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk) {
-    // aim for two waves at four resident CTAs per SM; a chunk keeps at least
-    // 8 column tiles so that staging the rows stays a small part of its work
+using TrKernel = void (*)(TransportArgs);
+
+// The kernel for d coordinates and c values per column (centred: the
+// row-centred products, c = 1).
+static TrKernel tr_kernel(int d, int c, bool centred) {
+    const bool w8 = tr_w(d) == 8;
+    if (centred) return w8 ? transport_kernel<1, 8, true> : transport_kernel<1, 4, true>;
+    if (c <= 1) return w8 ? transport_kernel<1, 8> : transport_kernel<1, 4>;
+    if (c <= 4) return w8 ? transport_kernel<4, 8> : transport_kernel<4, 4>;
+    if (c <= 16) return w8 ? transport_kernel<16, 8> : transport_kernel<16, 4>;
+    return w8 ? transport_kernel<64, 8> : transport_kernel<64, 4>;
+}
+
+// CTAs of that kernel resident on one SM (4 when the device cannot say).
+static int tr_resident(int d, int c, bool centred) {
+    const TrKernel k = tr_kernel(d, c, centred);
+    const size_t sm = tr_smem_bytes(d, centred ? 1 : c);
+    int nb = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k, TR_T, sm) != cudaSuccess || nb < 1) {
+        (void)cudaGetLastError();
+        return 4;
+    }
+    return nb;
+}
+
+size_t transport_plan(int B, int nr, int nc, int d, int c, bool centred, int sms, int* split, int* chunk) {
+    // CTAs all do the same work, so the split is chosen for whole waves: the
+    // fewest chunks, from one full wave of CTAs on, whose last wave is within
+    // 2 % of the fullest any split gives.  A chunk keeps at least 8 column
+    // tiles so that staging the rows stays a small part of its work.
     const long long blocks = (long long)B * ((nr + TR_T - 1) / TR_T);
-    const long long target = 8LL * (sms > 0 ? sms : 152);
+    const long long cap = (long long)(sms > 0 ? sms : 152) * tr_resident(d, c, centred);
     const int tiles = (nc + TR_CT - 1) / TR_CT;
-    long long s = (target + blocks - 1) / blocks;
-    const long long smax = (tiles + 7) / 8;
-    if (s > smax) s = smax;
-    if (s < 1) s = 1;
-    const int tpc = (int)((tiles + s - 1) / s);
-    *chunk = tpc * TR_CT;
+    const int smax = std::max(1, (tiles + 7) / 8);
+    const int smin = (int)std::min<long long>(smax, std::max<long long>(1, (cap + blocks - 1) / blocks));
+    int best_tpc = (tiles + smin - 1) / smin;
+    double best = -1.0;
+    for (int s = smin; s <= smax; ++s) {
+        const int tpc = (tiles + s - 1) / s;
+        if ((tiles + tpc - 1) / tpc != s) continue;  // the same chunks as a smaller s
+        const long long g = blocks * s;
+        const double fill = (double)g / (double)(((g + cap - 1) / cap) * cap);
+        if (fill > best + 0.02) {
+            best = fill;
+            best_tpc = tpc;
+        }
+    }
+    *chunk = best_tpc * TR_CT;
     *split = (nc + *chunk - 1) / *chunk;
-    return *split > 1 ? (size_t)*split * B * nr * c : 0;
+    const size_t width = centred ? 2 * (size_t)d : (size_t)c;
+    return *split > 1 ? (size_t)*split * B * nr * width : 0;
 }
 
 // Row-centred products (see CENTRED above): V holds g (c = 1, ldv = 1), out has
@@ -241,7 +349,7 @@ cudaError_t launch_transport_centred(const TransportArgs& p, cudaStream_t st) {
         return cudaErrorInvalidValue;
     const size_t sm = tr_smem_bytes(p.d, 1);
     dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
-    auto kern = (p.d > 8) ? transport_kernel<1, 8, true> : transport_kernel<1, 4, true>;
+    const TrKernel kern = tr_kernel(p.d, 1, true);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     count_launches(1);
@@ -262,19 +370,11 @@ cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st) {
         return cudaErrorInvalidValue;
     const size_t sm = tr_smem_bytes(p.d, p.c);
     dim3 grid(((p.nr + TR_T - 1) / TR_T) * p.split, p.B), block(TR_T);
-#define SOT_TR_CASE(CVV)                                                                              \
-    {                                                                                                 \
-        auto kern = (p.d > 8) ? transport_kernel<CVV, 8> : transport_kernel<CVV, 4>;                  \
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
-        if (e != cudaSuccess) return e;                                                               \
-        count_launches(1);                                                                            \
-        kern<<<grid, block, sm, st>>>(p);                                                             \
-    }
-    if (p.c <= 1) SOT_TR_CASE(1)
-    else if (p.c <= 4) SOT_TR_CASE(4)
-    else if (p.c <= 16) SOT_TR_CASE(16)
-    else SOT_TR_CASE(64)
-#undef SOT_TR_CASE
+    const TrKernel kern = tr_kernel(p.d, p.c, false);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    kern<<<grid, block, sm, st>>>(p);
     if (p.split > 1) {
         const long long count = (long long)p.B * p.nr * p.c;
         count_launches(1);

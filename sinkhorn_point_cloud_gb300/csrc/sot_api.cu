@@ -983,7 +983,7 @@ int sot_transport_apply(const float* X, const float* Y, const float* a, const fl
     } else {
         p.nr = m; p.nc = n; p.R = Y; p.Cl = X; p.fr = g; p.gc = f; p.wr = b; p.wc = a;
     }
-    const size_t nparts = transport_plan(B, p.nr, p.nc, c, device_sms(), &p.split, &p.chunk);
+    const size_t nparts = transport_plan(B, p.nr, p.nc, d, c, false, device_sms(), &p.split, &p.chunk);
     p.part = nparts ? unit.alloc<float>(nparts) : nullptr;
     if (nparts && !p.part) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
     cudaError_t e = launch_transport(p, cs);
@@ -1017,7 +1017,7 @@ int sot_grad_y(const float* X, const float* Y, const float* a, const float* b, i
         p.out = grad_y + c0; p.ldo = d;
         p.kap_hi = (float)kap;
         p.kap_lo = (float)(kap - (double)p.kap_hi);
-        const size_t nparts = transport_plan(B, p.nr, p.nc, p.c, device_sms(), &p.split, &p.chunk);
+        const size_t nparts = transport_plan(B, p.nr, p.nc, d, p.c, false, device_sms(), &p.split, &p.chunk);
         p.part = nparts ? unit.alloc<float>(nparts) : nullptr;
         if (nparts && !p.part) return fail(SOT_ERR_NOMEM, "scratch allocation failed");
         cudaError_t e = launch_transport(p, cs);
@@ -1049,8 +1049,11 @@ int sot_hvp(const float* X, const float* Y, const float* a, const float* b, int 
     size_t nparts = 0;  // partial-sum scratch: the largest any of the products needs
     {
         int s, ch;
-        nparts = std::max(nparts, transport_plan(B, n, m, std::max(c1, 2 * d), sms, &s, &ch));
-        nparts = std::max(nparts, transport_plan(B, m, n, c2, sms, &s, &ch));
+        nparts = std::max(nparts, transport_plan(B, n, m, d, c1, false, sms, &s, &ch));
+        nparts = std::max(nparts, transport_plan(B, m, n, d, c2, false, sms, &s, &ch));
+        nparts = std::max(nparts, transport_plan(B, n, m, d, 1, false, sms, &s, &ch));
+        nparts = std::max(nparts, transport_plan(B, m, n, d, 1, false, sms, &s, &ch));
+        nparts = std::max(nparts, transport_plan(B, n, m, d, 1, true, sms, &s, &ch));
     }
     Scratch S(cs);
     const size_t rmax = (size_t)B * std::max(n, m);
@@ -1103,7 +1106,7 @@ int sot_hvp(const float* X, const float* Y, const float* a, const float* b, int 
         } else {
             t.nr = m; t.nc = n; t.R = Yc; t.Cl = Xc; t.fr = g; t.gc = f; t.wr = b; t.wc = a;
         }
-        transport_plan(B, t.nr, t.nc, c, sms, &t.split, &t.chunk);
+        transport_plan(B, t.nr, t.nc, d, c, false, sms, &t.split, &t.chunk);
         t.part = part;
         return launch_transport(t, cs);
     };
@@ -1143,7 +1146,7 @@ int sot_hvp(const float* X, const float* Y, const float* a, const float* b, int 
         t.kap_lo = (float)(kap - (double)t.kap_hi);
         t.nr = n; t.nc = m; t.R = Xc; t.Cl = Yc; t.fr = f; t.gc = g; t.wr = a; t.wc = b;
         t.rc = YH; t.rv = V;
-        transport_plan(B, n, m, 2 * d, sms, &t.split, &t.chunk);
+        transport_plan(B, n, m, d, 1, true, sms, &t.split, &t.chunk);
         t.part = part;
         SOT_HVP_STEP(launch_transport_centred(t, cs));
     }

@@ -31,9 +31,11 @@ struct TransportArgs {
 
 int transport_max_d();
 int transport_max_c();
-// Column split for a problem on `sms` SMs: fills *split and *chunk; returns
-// the floats of partial-sum scratch it needs (0 when split == 1).
-size_t transport_plan(int B, int nr, int nc, int c, int sms, int* split, int* chunk);
+// Column split for a problem of d coordinates and c values per column on `sms`
+// SMs (centred: the row-centred products, c = 1 with 2d values out per row):
+// fills *split and *chunk; returns the floats of partial-sum scratch it needs
+// (0 when split == 1).
+size_t transport_plan(int B, int nr, int nc, int d, int c, bool centred, int sms, int* split, int* chunk);
 cudaError_t launch_transport(const TransportArgs& p, cudaStream_t st);
 cudaError_t launch_transport_centred(const TransportArgs& p, cudaStream_t st);
 // g[k][j][:] <- 2 (w_j p_j - g[k][j][:]) for `count` points of d coordinates
