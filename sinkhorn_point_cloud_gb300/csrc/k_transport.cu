@@ -68,19 +68,19 @@ static size_t tr_smem_bytes(int d, int c) {
 // pair, so no two large sums cancel.
 constexpr int TR_CD = 9;
 
-template <int CV, int W, bool CENTRED = false>
+// DF: the number of coordinates fixed at compile time (0: p.d at run time).
+template <int CV, int W, bool CENTRED = false, int DF = 0>
 __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
     static_assert(W == 4 || W == 8, "column group of 4 or 8");
+    static_assert(DF >= 0 && DF <= 8, "fixed dimension of at most 8");
     extern __shared__ float smem[];
-    const int d = p.d, c = p.c, ldx = tr_ldx(d);
+    const int d = DF ? DF : p.d, c = p.c, ldx = tr_ldx(d);
     float* xs = smem;                 // [TR_T][ldx] this CTA's rows
     float* ys = xs + TR_T * ldx;      // [d][TR_YS] column tile, transposed and negated
     float* hs = ys + d * TR_YS;       // [TR_CT] screen limits h_j (-inf past the end; float4 reads)
-    float* gs = hs + TR_CT;           // [TR_CT] column potentials
-    float* ls = gs + TR_CT;           // [TR_CT] log2 column weights (-inf past the end)
-    float* frs = ls + TR_CT;          // [TR_T] row potentials
-    float* lws = frs + TR_T;          // [TR_T] log2 row weights
-    float* vs = lws + TR_T;           // [c][TR_VS] V values of the tile, transposed
+    float2* bs = reinterpret_cast<float2*>(hs + TR_CT);  // [TR_CT] kappa g_j + log2 w'_j (float-float)
+    float2* as = bs + TR_CT;          // [TR_T] kappa f_i + log2 w_i (float-float)
+    float* vs = reinterpret_cast<float*>(as + TR_T);  // [c][TR_VS] V values of the tile, transposed
     constexpr int QG = tr_qg(W);
     unsigned* qs = reinterpret_cast<unsigned*>(vs + TR_VS * c);  // [TR_T / 32][32 QG] per-warp pair queues
     const int lane = threadIdx.x & 31, wrp = threadIdx.x >> 5;
@@ -100,12 +100,22 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         const int r = e / d, k = e % d;
         xs[r * ldx + k] = (row0 + r < p.nr) ? R[(size_t)(row0 + r) * d + k] : 0.f;
     }
-    const float fi = ok ? p.fr[(size_t)b * p.nr + i] : 0.f;
-    const float lwi = ok ? (p.wr ? log2f(p.wr[(size_t)b * p.nr + i]) : -log2f((float)p.nr)) : 0.f;
-    frs[threadIdx.x] = fi;
-    lws[threadIdx.x] = lwi;
     const float2 kap = make_float2(p.kap_hi, p.kap_lo);
+    const float fi = ok ? p.fr[(size_t)b * p.nr + i] : 0.f;
+    {
+        const float lwi = ok ? (p.wr ? log2f(p.wr[(size_t)b * p.nr + i]) : -log2f((float)p.nr)) : 0.f;
+        as[threadIdx.x] = ff_add(ff_mul(kap, make_float2(fi, 0.f)), make_float2(lwi, 0.f));
+    }
     const float sig = -(30.f + log2f((float)p.nc));  // skip threshold on log2(P_ij / w_i)
+    // a fixed small dimension keeps the row in registers, each value paired for the packed screen
+    float2 xp[DF ? DF : 1];
+    if (DF) {
+#pragma unroll
+        for (int k = 0; k < (DF ? DF : 1); ++k) {
+            const float x = ok ? R[(size_t)i * d + k] : 0.f;
+            xp[k] = make_float2(x, x);
+        }
+    }
     float acc[CV];
 #pragma unroll
     for (int k = 0; k < CV; ++k) acc[k] = 0.f;
@@ -138,10 +148,10 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
         if (threadIdx.x < TR_CT) {
             const int j = base + threadIdx.x;
             const bool cj = j < c_end;
-            gs[threadIdx.x] = cj ? p.gc[(size_t)b * p.nc + j] : 0.f;
-            const float lj = cj ? (p.wc ? log2f(p.wc[(size_t)b * p.nc + j]) : -log2f((float)p.nc)) : -INFINITY;
-            ls[threadIdx.x] = lj;
-            hs[threadIdx.x] = cj ? gs[threadIdx.x] + (lj - sig) / p.kap_hi : -INFINITY;
+            const float gj = cj ? p.gc[(size_t)b * p.nc + j] : 0.f;
+            const float lj = cj ? (p.wc ? log2f(p.wc[(size_t)b * p.nc + j]) : -log2f((float)p.nc)) : 0.f;
+            hs[threadIdx.x] = cj ? gj + (lj - sig) / p.kap_hi : -INFINITY;
+            bs[threadIdx.x] = ff_add(ff_mul(kap, make_float2(gj, 0.f)), make_float2(lj, 0.f));
         }
         __syncthreads();
         for (int qb = 0; qb < TR_CT; qb += QG) {
@@ -149,30 +159,59 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
             unsigned sm = 0;
             if (ok) {
                 for (int jg = qb; jg < qb + QG; jg += W) {
-                    // fp32 direct-form distances of W columns, two per packed instruction
+                    // fp32 direct-form distances of W columns less f_i, two per packed instruction
                     float2 cp[W / 2];
 #pragma unroll
-                    for (int h = 0; h < W / 2; ++h) cp[h] = make_float2(0.f, 0.f);
-                    for (int k = 0; k < d; ++k) {
-                        const float2 xx = make_float2(xr[k], xr[k]);
+                    for (int h = 0; h < W / 2; ++h) cp[h] = make_float2(-fi, -fi);
+                    if (DF) {
 #pragma unroll
-                        for (int qq = 0; qq < W / 4; ++qq) {
-                            const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + jg + 4 * qq);
-                            const float2 t0 = fadd2(xx, make_float2(y4.x, y4.y));
-                            const float2 t1 = fadd2(xx, make_float2(y4.z, y4.w));
-                            cp[2 * qq] = ffma2(t0, t0, cp[2 * qq]);
-                            cp[2 * qq + 1] = ffma2(t1, t1, cp[2 * qq + 1]);
+                        for (int k = 0; k < (DF ? DF : 1); ++k) {
+#pragma unroll
+                            for (int qq = 0; qq < W / 4; ++qq) {
+                                const float4 y4 = *reinterpret_cast<const float4*>(ys + k * TR_YS + jg + 4 * qq);
+                                const float2 t0 = fadd2(xp[k], make_float2(y4.x, y4.y));
+                                const float2 t1 = fadd2(xp[k], make_float2(y4.z, y4.w));
+                                cp[2 * qq] = ffma2(t0, t0, cp[2 * qq]);
+                                cp[2 * qq + 1] = ffma2(t1, t1, cp[2 * qq + 1]);
+                            }
+                        }
+                    } else {
+                        // the next coordinate's values are loaded while this one's are
+                        // used (the loads one past the last coordinate stay inside the
+                        // shared arrays and are not used)
+                        float xn = xr[0];
+                        float4 yn[W / 4];
+#pragma unroll
+                        for (int qq = 0; qq < W / 4; ++qq)
+                            yn[qq] = *reinterpret_cast<const float4*>(ys + jg + 4 * qq);
+#pragma unroll 4
+                        for (int k = 0; k < d; ++k) {
+                            const float2 xx = make_float2(xn, xn);
+                            float4 yc[W / 4];
+#pragma unroll
+                            for (int qq = 0; qq < W / 4; ++qq) {
+                                yc[qq] = yn[qq];
+                                yn[qq] = *reinterpret_cast<const float4*>(ys + (k + 1) * TR_YS + jg + 4 * qq);
+                            }
+                            xn = xr[k + 1];
+#pragma unroll
+                            for (int qq = 0; qq < W / 4; ++qq) {
+                                const float2 t0 = fadd2(xx, make_float2(yc[qq].x, yc[qq].y));
+                                const float2 t1 = fadd2(xx, make_float2(yc[qq].z, yc[qq].w));
+                                cp[2 * qq] = ffma2(t0, t0, cp[2 * qq]);
+                                cp[2 * qq + 1] = ffma2(t1, t1, cp[2 * qq + 1]);
+                            }
                         }
                     }
 #pragma unroll
                     for (int qq = 0; qq < W / 4; ++qq) {
-                        // the screen in fp32: C_ij < f_i + h_j
+                        // the screen in fp32: C_ij - f_i < h_j
                         const float4 h4 = *reinterpret_cast<const float4*>(hs + jg + 4 * qq);
-                        const int u = jg + 4 * qq;
-                        if (cp[2 * qq].x < fi + h4.x) sm |= 1u << u;
-                        if (cp[2 * qq].y < fi + h4.y) sm |= 2u << u;
-                        if (cp[2 * qq + 1].x < fi + h4.z) sm |= 4u << u;
-                        if (cp[2 * qq + 1].y < fi + h4.w) sm |= 8u << u;
+                        const int u = jg + 4 * qq - qb;
+                        sm |= (cp[2 * qq].x < h4.x ? 1u : 0u) << u;
+                        sm |= (cp[2 * qq].y < h4.y ? 2u : 0u) << u;
+                        sm |= (cp[2 * qq + 1].x < h4.z ? 4u : 0u) << u;
+                        sm |= (cp[2 * qq + 1].y < h4.w ? 8u : 0u) << u;
                     }
                 }
             }
@@ -189,25 +228,44 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
             if (total == 0) continue;  // warp-uniform
             {
                 int k = o;
-                for (unsigned mm = sm; mm; mm &= mm - 1) q[k++] = ((unsigned)lane << 5) | (unsigned)(__ffs(mm) - 1);
+                for (unsigned mm = sm; mm; mm &= mm - 1)
+                    q[k++] = ((unsigned)lane << 5) | (unsigned)(qb + __ffs(mm) - 1);
             }
             __syncwarp();
             // exact weights, one queued pair per lane: C_ij from exact differences
-            // and squares, log2 P_ij = log2 w_i + log2 w'_j + kappa (f_i + g_j - C_ij),
+            // and squares (positive terms: their high parts added error-free, the
+            // low parts in fp32), then
+            // log2 P_ij = (kappa f_i + log2 w_i) + (kappa g_j + log2 w'_j) - kappa C_ij,
             // all in float-float
             for (int t = lane; t < total; t += 32) {
                 const unsigned e = q[t];
                 const int jj = (int)(e & 31u), r = (wrp << 5) | (int)(e >> 5);
                 const float* xq = xs + r * ldx;
-                float2 C2 = make_float2(0.f, 0.f);
-                for (int k = 0; k < d; ++k) {
-                    const float2 dd = two_sum(xq[k], ys[k * TR_YS + jj]);
-                    float2 sq = two_prod(dd.x, dd.x);
-                    sq.y = __fmaf_rn(2.f * dd.x, dd.y, sq.y);
-                    C2 = ff_add(C2, sq);
+                // NC independent sums (coordinates k = u mod NC) when d is only known
+                // at run time, so that a long row is not one chain of dependent adds
+                // (one with 64 accumulators per row, which leave no registers for more)
+                constexpr int NC = (DF || CV > 16) ? 1 : 4;
+                float chi[NC], clo[NC];
+#pragma unroll
+                for (int u = 0; u < NC; ++u) chi[u] = clo[u] = 0.f;
+                for (int k0 = 0; k0 < d; k0 += NC) {
+#pragma unroll
+                    for (int u = 0; u < NC; ++u) {
+                        const int k = k0 + u;
+                        if (NC == 1 || k < d) {
+                            const float2 dd = two_sum(xq[k], ys[k * TR_YS + jj]);
+                            const float2 sq = two_prod(dd.x, dd.x);
+                            const float2 sh = two_sum(chi[u], sq.x);
+                            chi[u] = sh.x;
+                            clo[u] = __fadd_rn(clo[u], __fadd_rn(sh.y, __fmaf_rn(__fadd_rn(dd.x, dd.x), dd.y, sq.y)));
+                        }
+                    }
                 }
-                const float2 pot = ff_add(two_sum(frs[r], gs[jj]), make_float2(-C2.x, -C2.y));
-                const float2 ell = ff_add(ff_mul(kap, pot), two_sum(ls[jj], lws[r]));
+                float2 C2 = ff_renorm(chi[0], clo[0]);
+#pragma unroll
+                for (int u = 1; u < NC; ++u) C2 = ff_add(C2, ff_renorm(chi[u], clo[u]));
+                const float2 kc = ff_mul(kap, C2);
+                const float2 ell = ff_add(ff_add(as[r], bs[jj]), make_float2(-kc.x, -kc.y));
                 qw[t] = exp2f(__fadd_rn(ell.x, ell.y));
             }
             __syncwarp();
@@ -215,7 +273,7 @@ __global__ void __launch_bounds__(TR_T) transport_kernel(TransportArgs p) {
             {
                 int k = o;
                 for (unsigned mm = sm; mm; mm &= mm - 1, ++k) {
-                    const int jj = __ffs(mm) - 1;
+                    const int jj = qb + __ffs(mm) - 1;
                     const float w = qw[k];
                     const float* vj = vs + jj;  // V_j[k] at vj[k TR_VS]
                     if (CENTRED) {
@@ -290,13 +348,18 @@ using TrKernel = void (*)(TransportArgs);
 
 // The kernel for d coordinates and c values per column (centred: the
 // row-centred products, c = 1).
+template <int CV, bool CENTRED = false>
+static TrKernel tr_pick(int d) {
+    if (d == 3) return transport_kernel<CV, 4, CENTRED, 3>;
+    return tr_w(d) == 8 ? transport_kernel<CV, 8, CENTRED> : transport_kernel<CV, 4, CENTRED>;
+}
+
 static TrKernel tr_kernel(int d, int c, bool centred) {
-    const bool w8 = tr_w(d) == 8;
-    if (centred) return w8 ? transport_kernel<1, 8, true> : transport_kernel<1, 4, true>;
-    if (c <= 1) return w8 ? transport_kernel<1, 8> : transport_kernel<1, 4>;
-    if (c <= 4) return w8 ? transport_kernel<4, 8> : transport_kernel<4, 4>;
-    if (c <= 16) return w8 ? transport_kernel<16, 8> : transport_kernel<16, 4>;
-    return w8 ? transport_kernel<64, 8> : transport_kernel<64, 4>;
+    if (centred) return tr_pick<1, true>(d);
+    if (c <= 1) return tr_pick<1>(d);
+    if (c <= 4) return tr_pick<4>(d);
+    if (c <= 16) return tr_pick<16>(d);
+    return tr_pick<64>(d);
 }
 
 // CTAs of that kernel resident on one SM (4 when the device cannot say).
