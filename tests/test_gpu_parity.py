@@ -108,6 +108,15 @@ def test_workload5_reduced_potentials(sot, orc):
     print(check(sot, orc, X, Y, a, b, 5e-3, 300, uniform=True))
 
 
+def test_workload5_full_size_sampled_cloud(sot, orc):
+    """The full batch B=8, n=m=8192, eps=5e-3, 300 iterations as timed; the
+    oracle follows cloud 0 through all 300 iterations (about 4e10 pair
+    evaluations: half a minute on 16 cores) and its plan application."""
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(5)
+    print(check(sot, orc, X, Y, a, b, 5e-3, 300, uniform=True, clouds=[0]))
+
+
 def test_single_point_closed_form(sot):
     """n = m = 1: f = |x - y|^2, g = 0, cost = |x - y|^2, grad = 2 (x - y)."""
     X = np.array([[[0.3, -0.2, 0.9]]], dtype=np.float32)
