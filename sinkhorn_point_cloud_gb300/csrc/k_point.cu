@@ -34,15 +34,13 @@
 namespace sot {
 
 constexpr int PT_T = 128;               // threads per CTA
-constexpr int PT_RPT = 4;               // rows per thread
-constexpr int PT_ROWS = PT_T * PT_RPT;  // rows per CTA
 constexpr int PT_TC = 2 * PT_T;         // columns per shared-memory tile
+// Rows per thread (RPT) is 4, 2 or 1: a CTA holds PT_T * RPT rows.  More rows
+// per thread reuse each staged column for more rows; fewer give more row
+// blocks, so that a workload of few, short rows still fills the GPU with CTAs
+// that each cover several column tiles (see point_plan).
 
-int point_rows_per_cta() { return PT_ROWS; }
 int point_cols_per_tile() { return PT_TC; }
-// Resident CTAs of the half-step kernel per SM (from the occupancy calculator,
-// queried once); the column split fills this many slots per SM.
-int point_blocks_per_sm();
 
 // Score relative to a base: acc = base + |u - v|^2 with d = u + (-v), fp32 in
 // this fixed order (the maximum passes and the COO predicate evaluate the same
@@ -111,8 +109,9 @@ __device__ float point_row_full(const float4* cp, const float* cst, int nc, floa
     return mx + log2f(sm);
 }
 
-template <int D, int MODE>
+template <int D, int MODE, int PT_RPT>
 __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
+    constexpr int PT_ROWS = PT_T * PT_RPT;  // rows per CTA
     if (p.stop_flag && *(volatile const int*)p.stop_flag) return;
     __shared__ float4 tile[PT_TC];
     __shared__ float red[PT_T / 32];
@@ -316,20 +315,29 @@ __global__ void __launch_bounds__(PT_T) point_half_kernel(HalfArgs p) {
     }
 }
 
-cudaError_t launch_point_half(const HalfArgs& p, int mode, cudaStream_t st) {
-    dim3 grid(p.rowtiles * p.split, p.B), block(PT_T);
-#define SOT_PT_CASE(DD)                                                               \
-    case DD:                                                                          \
-        if (mode == MODE_MAX) { count_launches(1); point_half_kernel<DD, MODE_MAX><<<grid, block, 0, st>>>(p); } \
-        else { count_launches(1); point_half_kernel<DD, MODE_LSE><<<grid, block, 0, st>>>(p); } \
-        break;
-    switch (p.d) {
-        SOT_PT_CASE(1)
-        SOT_PT_CASE(2)
-        SOT_PT_CASE(3)
-        default: return cudaErrorInvalidValue;
+using PointKernel = void (*)(HalfArgs);
+
+template <int RPT>
+static PointKernel point_kernel_rpt(int d, int mode) {
+    const bool mx = mode == MODE_MAX;
+    switch (d) {
+        case 1: return mx ? point_half_kernel<1, MODE_MAX, RPT> : point_half_kernel<1, MODE_LSE, RPT>;
+        case 2: return mx ? point_half_kernel<2, MODE_MAX, RPT> : point_half_kernel<2, MODE_LSE, RPT>;
+        case 3: return mx ? point_half_kernel<3, MODE_MAX, RPT> : point_half_kernel<3, MODE_LSE, RPT>;
+        default: return nullptr;
     }
-#undef SOT_PT_CASE
+}
+
+static PointKernel point_kernel(int d, int mode, int rpt) {
+    return rpt == 1 ? point_kernel_rpt<1>(d, mode) : rpt == 2 ? point_kernel_rpt<2>(d, mode) : rpt == 4 ? point_kernel_rpt<4>(d, mode) : nullptr;
+}
+
+cudaError_t launch_point_half(const HalfArgs& p, int mode, cudaStream_t st) {
+    const PointKernel k = point_kernel(p.d, mode, p.rpt);
+    if (!k || p.rowtiles != (p.nr + PT_T * p.rpt - 1) / (PT_T * p.rpt)) return cudaErrorInvalidValue;
+    dim3 grid(p.rowtiles * p.split, p.B), block(PT_T);
+    count_launches(1);
+    k<<<grid, block, 0, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -579,19 +587,77 @@ cudaError_t launch_point_coo(const CooArgs& p, int write_pass, cudaStream_t st) 
     return cudaGetLastError();
 }
 
+// Resident CTAs per SM of the half-step kernel with `rpt` rows per thread.
 // Cached after the first successful query (the kernel's resources do not
 // depend on the device); a failed query returns 4 and is not cached.
-int point_blocks_per_sm() {
-    static std::atomic<int> occ{0};
-    int v = occ.load(std::memory_order_relaxed);
+static int point_blocks_per_sm(int rpt) {
+    static std::atomic<int> occ[3] = {};
+    const int slot = rpt == 1 ? 0 : rpt == 2 ? 1 : 2;
+    int v = occ[slot].load(std::memory_order_relaxed);
     if (v > 0) return v;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, point_half_kernel<3, MODE_LSE>, PT_T, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, point_kernel(3, MODE_LSE, rpt), PT_T, 0) != cudaSuccess ||
         v < 1) {
         cudaGetLastError();
         return 4;
     }
-    occ.store(v, std::memory_order_relaxed);
+    occ[slot].store(v, std::memory_order_relaxed);
     return v;
+}
+
+// Rows per thread and column split of a half-step over B clouds of nr rows
+// and nc columns.  For each choice of rows per thread r the split is the one
+// of fewest rounds of CTAs per unit of work (a 1 % charge per extra chunk for
+// the combining step); the choices are then compared by the work each SM
+// carries: its CTAs times r * (column tiles * PT_PAIR[r] + PT_FIXED), where
+// PT_PAIR is the cost of a pair relative to 4 rows per thread (each staged
+// column feeds fewer rows) and PT_FIXED the per-row work that does not depend
+// on the chunk's length (loading and stabilising the rows, combining the
+// chunks, finishing the rows), in tiles.  Both were fitted to the half-step
+// times of the three d = 3 workloads of 65536 rows (2048, 8192 and 16384
+// columns) with 4, 2 and 1 rows per thread.  An SM holding fewer than 16 warps
+// is charged for the lanes they leave idle.
+constexpr double PT_FIXED = 0.2;
+
+static double pt_pair_cost(int r) { return r == 4 ? 1.0 : r == 2 ? 1.06 : 1.12; }
+
+void point_plan(int B, int nr, int nc, int sms, int* rpt, int* split, int* chunk, int* rowtiles) {
+    const int ntiles = (nc + PT_TC - 1) / PT_TC;
+    const int smax = ntiles < 64 ? ntiles : 64;
+    const long long nsm = sms > 0 ? sms : 1;
+    double best_cost = 1e300;
+    int br = 4, bs = 1;
+    for (int r = 4; r >= 1; r /= 2) {
+        const long long base = (long long)B * ((nr + PT_T * r - 1) / (PT_T * r));
+        const long long occ = point_blocks_per_sm(r);
+        const long long slots = nsm * occ;
+        double best = 1e300;
+        int s_r = 1;
+        for (int s = 1; s <= smax; ++s) {
+            const long long units = base * s;
+            const double rounds = (double)((units + slots - 1) / slots);
+            const double t = rounds / s * (1.0 + 0.01 * (s - 1));
+            if (t < best * 0.999) {
+                best = t;
+                s_r = s;
+            }
+        }
+        const int tpc = (ntiles + s_r - 1) / s_r;
+        const long long units = base * ((ntiles + tpc - 1) / tpc);
+        const long long per_sm = (units + nsm - 1) / nsm;
+        const long long resident = per_sm < occ ? per_sm : occ;
+        const double starve = resident * 4 < 16 ? 16.0 / (double)(resident * 4) : 1.0;
+        const double cost = (double)per_sm * r * (tpc * pt_pair_cost(r) + PT_FIXED) * starve;
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            br = r;
+            bs = s_r;
+        }
+    }
+    *rpt = br;
+    *rowtiles = (nr + PT_T * br - 1) / (PT_T * br);
+    const int tiles_per_chunk = (ntiles + bs - 1) / bs;
+    *chunk = tiles_per_chunk * PT_TC;
+    *split = (nc + *chunk - 1) / *chunk;
 }
 
 }  // namespace sot

@@ -52,6 +52,7 @@ struct HalfArgs {
     int* redo;              // NULL, or [B*rowtiles] row-block flags: the screened half-step sets the flag of
                             // a row block it leaves to the full half-step; the full half-step then runs
                             // only the flagged row blocks
+    int rpt = 4;            // point path: rows per thread (point_plan); rowtiles = ceil(nr / (128 rpt))
 };
 
 struct ApplyArgs {
@@ -99,9 +100,10 @@ struct CooArgs {
 };
 
 // ---- point path (d <= 3), k_point.cu ----
-int point_rows_per_cta();
 int point_cols_per_tile();
-int point_blocks_per_sm();
+// Rows per thread (1, 2 or 4), column split and row tiles of a half-step over
+// B clouds of nr rows and nc columns (the plan of least estimated time).
+void point_plan(int B, int nr, int nc, int sms, int* rpt, int* split, int* chunk, int* rowtiles);
 cudaError_t launch_point_half(const HalfArgs& p, int mode, cudaStream_t st);
 int point_apply_rows_per_cta();
 cudaError_t launch_point_apply(const ApplyArgs& p, cudaStream_t st);

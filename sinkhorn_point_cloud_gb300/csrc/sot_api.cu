@@ -322,6 +322,7 @@ struct Solver {
     int nstage_slots = 0;
     int sms;
     int split[2], chunk[2], rowtiles[2];  // [0] f-half (rows X), [1] g-half (rows Y)
+    int rpt[2] = {4, 4};                  // point path: rows per thread
     // Tensor path with d > 64: the screened half-step takes the warm half-steps,
     // the fp32 dense half-step (with its own split plan) every other one.
     bool tc_dense_full = false;
@@ -386,9 +387,7 @@ struct Solver {
         for (int h = 0; h < 2; ++h) {
             const int nr = h ? m : n, nc = h ? n : m;
             if (path == PATH_POINT)
-                choose_split(B, nr, nc, point_rows_per_cta(), point_cols_per_tile(), sms, point_blocks_per_sm(),
-                             &split[h], &chunk[h],
-                             &rowtiles[h]);
+                point_plan(B, nr, nc, sms, &rpt[h], &split[h], &chunk[h], &rowtiles[h]);
             else if (path == PATH_DENSE)
                 choose_split(B, nr, nc, dense_rows_per_cta(), dense_cols_per_tile(), sms, 2, &split[h], &chunk[h],
                              &rowtiles[h]);
@@ -467,6 +466,7 @@ struct Solver {
         p.split = split[h];
         p.chunk = chunk[h];
         p.rowtiles = rowtiles[h];
+        p.rpt = rpt[h];
         p.part_m = part_m;
         p.part_s = part_s;
         p.counters = counters;
@@ -1502,12 +1502,9 @@ size_t noalloc_required_bytes(int B, int n, int m, int d) {
     const size_t Bn = (size_t)B * n, Bm = (size_t)B * m;
     size_t total = piece(sizeof(float) * B * d) + piece(4 * Bn) + piece(4 * Bm) + piece(4 * Bn) + piece(4 * Bm) +
                    piece(sizeof(int) * 3) + piece(sizeof(unsigned) * 4 * B) + piece(16 * Bn) + piece(16 * Bm);
-    int split[2], chunk[2], rowtiles[2];
+    int split[2], chunk[2], rowtiles[2], rpt[2];
     const int sms = device_sms();
-    for (int h = 0; h < 2; ++h)
-        choose_split(B, h ? m : n, h ? n : m, point_rows_per_cta(), point_cols_per_tile(), sms, point_blocks_per_sm(),
-                     &split[h],
-                     &chunk[h], &rowtiles[h]);
+    for (int h = 0; h < 2; ++h) point_plan(B, h ? m : n, h ? n : m, sms, &rpt[h], &split[h], &chunk[h], &rowtiles[h]);
     const int smax = split[0] > split[1] ? split[0] : split[1];
     const int rt_max = rowtiles[0] > rowtiles[1] ? rowtiles[0] : rowtiles[1];
     const size_t rows_max = (size_t)B * (n > m ? n : m);
