@@ -211,15 +211,21 @@ int orc_g_half(int n, int m, int d, const double *X, const double *Y,
 static int row_sums(int n, int m, int d, const double *X, const double *Y,
                     const double *a, const double *b, const double *f,
                     const double *g, double eps, double *r) {
+    /* log b_j once per column (the same values the sum would compute per pair) */
+    double *lb = (double *)malloc(sizeof(double) * (size_t)m);
+    if (!lb) return -2;
+    for (int j = 0; j < m; ++j) lb[j] = log(b[j]);
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < n; ++i) {
+        const double la = log(a[i]);
         double acc = 0.0;
         for (int j = 0; j < m; ++j) {
             double c = cost_ij(X + (size_t)i * d, Y + (size_t)j * d, d);
-            acc += exp((f[i] + g[j] - c) / eps + log(a[i]) + log(b[j]));
+            acc += exp((f[i] + g[j] - c) / eps + la + lb[j]);
         }
         r[i] = acc;
     }
+    free(lb);
     return 0;
 }
 
@@ -229,7 +235,10 @@ double orc_marginal_err(int n, int m, int d, const double *X, const double *Y,
                         const double *g, double eps) {
     double *r = (double *)malloc(sizeof(double) * (size_t)n);
     if (!r) return NAN;
-    row_sums(n, m, d, X, Y, a, b, f, g, eps, r);
+    if (row_sums(n, m, d, X, Y, a, b, f, g, eps, r)) {
+        free(r);
+        return NAN;
+    }
     double e = 0.0;
     for (int i = 0; i < n; ++i) e += fabs(r[i] - a[i]);
     free(r);
