@@ -8,7 +8,9 @@ test passed, the final marginal error) and the final potentials on 256 seeded
 sampled rows and columns, for tests/test_gpu_anneal.py.  It calls only the
 oracle and the seeded input generator.
 
-The solve takes hours on a few cores, so it runs in pieces, each a call of the
+The solve takes about four hours on 8 x86 cores (about one on 16 Arm cores:
+the last stage's marginal-error test after every iteration costs more than the
+iteration), so it runs in pieces, each a call of the
 oracle that continues from the previous piece's potentials: the stages of
 fixed length one at a time (the oracle's fixed-schedule solve, one stage), then
 the last stage in chunks of iterations (the oracle's annealed solve on that one

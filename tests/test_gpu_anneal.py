@@ -10,6 +10,9 @@ usual 1e-4.  Separately, the realised counts are compared with the oracle's
 own stop with a small allowance, and the oracle's marginal error after the
 replay must be below the tolerance.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -131,3 +134,42 @@ def test_max_iters_cap_without_convergence(sot):
                                        stats=True)
     assert info["iters_done"] == 12 and not info["converged"]
     assert np.isfinite(info["err"][0])
+
+
+RECORD = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "anneal_gmm8_n16384_cloud0.json")
+
+
+def test_workload3_full_size_against_oracle_record(sot):
+    """Cloud 0 of the 4-cloud Gaussian-mixture workload at full size (n = m =
+    16384) on its annealed schedule (eps 1 -> 1e-3 by x0.9 per stage, 20
+    iterations per stage, stop at a marginal error below 1e-4, at most 5000
+    iterations) against the oracle's own run of the same schedule, stored in
+    tests/golden by make_anneal_record.py (which calls only the oracle): the
+    realised schedule (stages, iterations of the fixed stages, the iteration
+    count of the last stage within the stop-rule allowance of the reduced
+    test) and the final potentials on the record's 256 sampled rows and
+    columns after the gauge fix (f + c, g - c with c from the full means)."""
+    with open(RECORD) as fh:
+        rec = json.load(fh)
+    from sinkhorn_point_cloud_gb300 import datagen as dg
+    X, Y, a, b = dg.make_batch(3, B=1)
+    s = rec["schedule"]
+    f, g, info = sot.sot_potentials_ex(dev(X), dev(Y), eps=s["eps_min"], eps_init=s["eps0"], eps_factor=s["factor"],
+                                       iters_per_stage=s["iters_per_stage"], tol=s["tol"],
+                                       max_iters=s["max_iters"], stats=True)
+    gi = [int(v) for v in info["stage_iters"]][: info["stages_done"]]
+    print(f"GPU: {info['stages_done']} stages, {info['iters_done']} iterations, converged {info['converged']}, "
+          f"err {info['err'][0]:.4e}; oracle: {rec['stages_done']} stages, {rec['iters_done']} iterations, "
+          f"converged {rec['converged']}, err {rec['err']:.4e}")
+    assert info["stages_done"] == rec["stages_done"]
+    assert gi[:-1] == rec["stage_iters"][:-1]  # the stages of fixed length
+    ref = rec["iters_done"]
+    assert abs(info["iters_done"] - ref) <= max(3, 0.02 * ref), (info["iters_done"], ref)
+    fN, gN = host(f)[0], host(g)[0]
+    c = rec["f_mean"] - float(np.mean(fN))
+    rows, cols = np.array(rec["rows"]), np.array(rec["cols"])
+    scale = max(rec["f_absmax"], rec["g_absmax"])
+    ef = float(np.max(np.abs(fN[rows] + c - np.array(rec["f"])))) / scale
+    eg = float(np.max(np.abs(gN[cols] - c - np.array(rec["g"])))) / scale
+    print(f"sampled potentials (gauge-fixed): f {ef:.2e} g {eg:.2e}")
+    assert ef < TOL and eg < TOL, (ef, eg)
